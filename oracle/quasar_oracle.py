@@ -1,0 +1,237 @@
+"""CPU oracle for the Quasar W8A8 verification path.
+
+TEST INFRASTRUCTURE.  Only the tests, the smoke check and the CPU-baseline
+leg of the benchmark may import this module.  The product library never
+calls it, and it shares no code with the CUDA kernels.
+
+Source: "Quasar: Quantized Self-Speculative Acceleration for Rapid Inference
+via Memory-Efficient Verification" (arXiv 2603.01399), as summarised on four
+gist.science pages (pt, nl, zh, ko).  Citations below name the page language
+and its technical-summary section:
+
+  * zh §2 "方法论" / pt §2 "Metodologia": W8A8 verifier; SmoothQuant smoothing
+    Y = (W·diag(s)^-1)·(diag(s)·X) with s calibrated offline; offline smooth +
+    INT8 weight quantization; online smooth + quantize of the BF16
+    activations; INT8 matmul; dequantize to BF16 before the nonlinear layers
+    and softmax; rejection sampling on the high-precision logits.
+  * pt §2: symmetric uniform quantization of weights and activations.
+  * pt §4 / zh §4: greedy (T=0) and sampled (T>0) verification, acceptance
+    length.
+
+The pages leave the numeric details open.  The readings taken here are:
+
+  R1  smooth[k] multiplies activations and divides weights (the pages'
+      identity), with smooth[k] = max|W[:,k]|^(1-a) / max|X[:,k]|^a, which is
+      SmoothQuant's migration factor inverted, so outlier channels shrink.
+      a = 0.5.  A channel whose maximum is 0 gets smooth = 1.
+  R2  weights: per output channel; activations: per token; symmetric,
+      codes in [-127, 127], scale = absmax/127, code = rne(v * (127/absmax)),
+      all in fp32 with correctly rounded division and multiplication; a
+      zero row gets scale 0 and all-zero codes.
+  R3  the INT8 products are accumulated exactly (INT32 on the device).
+  R4  dequantization: y = bf16_rne((fp32(acc) * sa[m]) * sw[n]), two fp32
+      multiplies in that order, no bias.
+  R5  greedy acceptance: draft j is accepted iff it equals the first-index
+      argmax of logits row j; the accepted length is the first rejected j
+      (or D); the next token is the argmax of row n_acc.
+  R6  T > 0: the drafter is deterministic, so draft j is accepted iff
+      u[j] < p_j, p_j = softmax(logits_j / T)[draft_j], evaluated in fp64.
+
+Every function below is pinned by tests under ``tests/`` against hand-derived
+values, closed forms, invariants or brute force (see each docstring).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F32 = np.float32
+F64 = np.float64
+QMAX = 127
+
+
+# ---------------------------------------------------------------------------
+# BF16 helpers (independent of the data generator's copy on purpose).
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns -> fp32 values (exact widening)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(F32)
+
+
+def f32_to_bf16(x: np.ndarray) -> np.ndarray:
+    """fp32 -> BF16 bits, round to nearest, ties to even (finite inputs).
+
+    Pinned by the BF16 rounding fixtures (257 -> 256, 259 -> 260, ...)."""
+    u = np.asarray(x, dtype=F32).view(np.uint32).astype(np.uint64)
+    keep = u >> 16
+    rem = u & 0xFFFF
+    up = (rem > 0x8000) | ((rem == 0x8000) & ((keep & 1) == 1))
+    return (keep + up.astype(np.uint64)).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# Offline calibration of the smoothing vector (reading R1).
+
+def calibrate_smooth(x_cal_bits: np.ndarray, w_bits: np.ndarray, alpha: float = 0.5) -> np.ndarray:
+    """smooth[k] = max_n|W[n,k]|^(1-alpha) / max_m|X[m,k]|^alpha  (fp64, then fp32).
+
+    zh §2: the smoothing factor s is calibrated offline from activation and
+    weight statistics; with the pages' identity s multiplies X, so the factor
+    that shrinks an outlier channel is the inverse of SmoothQuant's.
+    Pinned: hand fixture (max|X|=4, max|W|=9 -> 1.5), degenerate columns -> 1.
+    """
+    x = bf16_to_f32(x_cal_bits).astype(F64)
+    w = bf16_to_f32(w_bits).astype(F64)
+    xmax = np.abs(x).max(axis=0)          # per input channel k, over tokens
+    wmax = np.abs(w).max(axis=0)          # per input channel k, over output rows
+    smooth = np.ones(x.shape[1], dtype=F64)
+    ok = (xmax > 0) & (wmax > 0)
+    if alpha == 0.5:
+        smooth[ok] = np.sqrt(wmax[ok]) / np.sqrt(xmax[ok])
+    else:
+        smooth[ok] = wmax[ok] ** (1.0 - alpha) / xmax[ok] ** alpha
+    return smooth.astype(F32)
+
+
+# ---------------------------------------------------------------------------
+# Symmetric per-row quantizer (reading R2).
+
+def quantize_rows(v: np.ndarray):
+    """Quantize each row of an fp32 matrix to INT8 codes with one fp32 scale.
+
+    pt §2: symmetric uniform quantization to 8 bits.  For a row with
+    absmax a > 0: scale = a/127, code = clamp(rne(v * (127/a)), -127, 127).
+    Pinned: tie-rounding fixture, |code*scale - v| <= scale/2 bound, a code
+    of magnitude 127 in every nonzero row, zero rows.
+    """
+    v = np.asarray(v, dtype=F32)
+    amax = np.abs(v).max(axis=1) if v.shape[1] else np.zeros(v.shape[0], F32)
+    scale = np.zeros(v.shape[0], dtype=F32)
+    codes = np.zeros(v.shape, dtype=np.int8)
+    nz = amax > 0
+    if nz.any():
+        a = amax[nz]
+        inv = F32(QMAX) / a                     # one correctly rounded fp32 division
+        scale[nz] = a / F32(QMAX)
+        q = np.rint(v[nz] * inv[:, None])       # fp32 product, round half to even
+        codes[nz] = np.clip(q, -QMAX, QMAX).astype(np.int8)
+    return codes, scale
+
+
+def pack_weights(w_bits: np.ndarray, smooth: np.ndarray):
+    """Offline weight preparation: fold diag(smooth)^-1 into W, quantize each
+    output channel.  w'[n,k] = fp32(W[n,k]) / smooth[k].
+
+    pt §2 step 1 / zh §2 "离线准备": weights are smoothed and quantized to INT8.
+    Returns (Wq int8 [N][K], sw fp32 [N]).
+    """
+    w = bf16_to_f32(w_bits)
+    wp = w / np.asarray(smooth, dtype=F32)[None, :]     # correctly rounded fp32 division
+    return quantize_rows(wp)
+
+
+def smooth_quant_act(x_bits: np.ndarray, smooth: np.ndarray):
+    """Online activation step: x'[m,k] = fp32(X[m,k]) * smooth[k], then quantize
+    each token.  pt §2 step 2 / zh §2 "在线验证".
+    Returns (Xq int8 [M][K], sa fp32 [M])."""
+    x = bf16_to_f32(x_bits)
+    xp = x * np.asarray(smooth, dtype=F32)[None, :]
+    return quantize_rows(xp)
+
+
+# ---------------------------------------------------------------------------
+# INT8 GEMM and dequantization (readings R3, R4).
+
+def int_gemm(xq: np.ndarray, wq: np.ndarray) -> np.ndarray:
+    """acc[m,n] = sum_k Xq[m,k] * Wq[n,k], exact, as int64.
+
+    pt §2 step 3: the matmul runs on INT8 operands.  The sum is formed with an
+    fp64 matmul: every product and every partial sum is an integer of
+    magnitude <= 127*127*K < 2^53, so fp64 represents each one exactly in any
+    summation order.  Pinned against brute-force integer loops."""
+    acc = np.asarray(xq, dtype=F64) @ np.asarray(wq, dtype=F64).T
+    return np.rint(acc).astype(np.int64)
+
+
+def dequant(acc: np.ndarray, sa: np.ndarray, sw: np.ndarray) -> np.ndarray:
+    """Y[m,n] = bf16_rne((fp32(acc[m,n]) * sa[m]) * sw[n]) -> BF16 bits.
+
+    pt §2 step 4: results return to BF16 before the nonlinear layers.
+    int -> fp32 is one round-to-nearest-even step (exact through fp64 for
+    |acc| < 2^53).  Pinned by the dequant fixtures."""
+    return f32_to_bf16(dequant_f32(acc, sa, sw))
+
+
+def dequant_f32(acc, sa, sw) -> np.ndarray:
+    """The fp32 value that dequant() rounds to BF16: (fp32(acc) * sa) * sw."""
+    a = np.asarray(acc, dtype=np.int64).astype(F64).astype(F32)
+    t = a * np.asarray(sa, dtype=F32)[:, None]
+    return t * np.asarray(sw, dtype=F32)[None, :]
+
+
+def w8a8_linear(xq, sa, wq, sw) -> np.ndarray:
+    """The whole verify linear on quantized operands -> BF16 bits."""
+    return dequant(int_gemm(xq, wq), sa, sw)
+
+
+def reference_linear_f64(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """Unquantized Y = X·W^T in fp64 from the BF16 inputs (the accuracy yardstick)."""
+    return bf16_to_f32(x_bits).astype(F64) @ bf16_to_f32(w_bits).astype(F64).T
+
+
+def smoothed_linear_f64(x_bits, w_bits, smooth) -> np.ndarray:
+    """(W·diag(s)^-1)(diag(s)·X) in fp64: the pages' identity, zh §2."""
+    s = np.asarray(smooth, dtype=F64)
+    x = bf16_to_f32(x_bits).astype(F64) * s[None, :]
+    w = bf16_to_f32(w_bits).astype(F64) / s[None, :]
+    return x @ w.T
+
+
+# ---------------------------------------------------------------------------
+# Verification (readings R5, R6).
+
+def acceptance_probabilities(logits_bits: np.ndarray, draft: np.ndarray, temperature: float) -> np.ndarray:
+    """p[b,j] = softmax(logits[b,j,:] / T)[draft[b,j]] in fp64, for j < D.
+
+    zh §2 "无损拒绝采样": rejection sampling on the high-precision logits.
+    Pinned by the two-level closed form p = c / (c + V - 1)."""
+    lg = bf16_to_f32(logits_bits).astype(F64)
+    B, R, V = lg.shape
+    D = R - 1
+    p = np.zeros((B, D), dtype=F64)
+    for b in range(B):
+        for j in range(D):
+            z = lg[b, j] / temperature
+            e = np.exp(z - z.max())
+            p[b, j] = e[draft[b, j]] / e.sum()
+    return p
+
+
+def verify_accept(logits_bits: np.ndarray, draft: np.ndarray, temperature: float = 0.0,
+                  u: np.ndarray | None = None):
+    """Accepted prefix length per sequence (and the greedy next token).
+
+    logits [B][D+1][V] (BF16 bits): row j scores the position drafted as
+    draft[b,j]; row D is the bonus position.  T == 0: draft j is accepted iff
+    it equals the lowest-index argmax of row j.  T > 0: accepted iff
+    u[b,j] < p[b,j].  n_acc[b] = first rejected j, or D.  For T == 0,
+    next[b] = argmax of row n_acc[b]; for T > 0 next is -1 (not produced).
+    Pinned by hand-built acceptance cases.
+    """
+    lg = bf16_to_f32(logits_bits)
+    B, R, V = lg.shape
+    D = R - 1
+    n_acc = np.full(B, D, dtype=np.int32)
+    nxt = np.full(B, -1, dtype=np.int32)
+    p = acceptance_probabilities(logits_bits, draft, temperature) if temperature > 0 else None
+    for b in range(B):
+        for j in range(D):
+            if temperature > 0:
+                ok = bool(u[b, j] < p[b, j])
+            else:
+                ok = int(draft[b, j]) == int(np.argmax(lg[b, j]))
+            if not ok:
+                n_acc[b] = j
+                break
+        if temperature == 0:
+            nxt[b] = int(np.argmax(lg[b, n_acc[b]]))
+    return n_acc, nxt

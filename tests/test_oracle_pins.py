@@ -1,0 +1,353 @@
+"""Pins for the CPU oracle: every oracle function is checked here against
+something other than itself -- hand-derived fixtures under tests/golden/,
+closed forms, exact rational arithmetic, invariants that follow from the
+definitions, or brute force on tiny inputs.  CPU only.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as orc
+from tests.exact import round_to_f32, ulp_f32
+from w8a8_quantized_speculative_gb300 import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def bf16(values):
+    """Exact BF16 bits of values that are representable in BF16."""
+    a = np.asarray(values, dtype=np.float32)
+    bits = a.view(np.uint32)
+    assert np.all((bits & 0xFFFF) == 0), "fixture value not representable in BF16"
+    return (bits >> 16).astype(np.uint16)
+
+
+# ---------------------------------------------------------------- BF16 rounding
+
+def test_bf16_rne_fixture():
+    for c in load("bf16_rne.json")["cases"]:
+        got = int(orc.f32_to_bf16(np.array([c["x"]], np.float32))[0])
+        assert got == int(c["bf16"], 16), c
+
+
+def test_bf16_roundtrip_exact():
+    rng = np.random.default_rng(0)
+    bits = rng.integers(0, 0x7F80, size=5000).astype(np.uint16)   # finite positives
+    bits = np.concatenate([bits, bits | 0x8000])
+    assert np.array_equal(orc.f32_to_bf16(orc.bf16_to_f32(bits)), bits)
+
+
+def test_bf16_rounding_is_nearest():
+    # Against exact rationals: the chosen BF16 is at most half a BF16 ulp away.
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal(2000) * 100).astype(np.float32)
+    y = orc.bf16_to_f32(orc.f32_to_bf16(x))
+    for xi, yi in zip(x[:400], y[:400]):
+        q = Fraction(float(xi))
+        half_ulp = ulp_f32(q) * 2 ** 16 / 2
+        assert abs(Fraction(float(yi)) - q) <= half_ulp
+
+
+# ---------------------------------------------------------------- quantizer
+
+@pytest.mark.parametrize("kind", ["activation_cases", "weight_cases"])
+def test_quantizer_fixture(kind):
+    for c in load("quantizer_rows.json")[kind]:
+        smooth = np.asarray(c["smooth"], np.float32)
+        if kind == "activation_cases":
+            codes, scale = orc.smooth_quant_act(bf16([c["x"]]), smooth)
+        else:
+            codes, scale = orc.pack_weights(bf16([c["w"]]), smooth)
+        assert codes.tolist() == [c["codes"]], c["why"]
+        num, den = c["scale_exact"]
+        exact = Fraction(num, den)
+        # the scale is the correctly rounded fp32 value of absmax/127
+        assert Fraction(float(scale[0])) == round_to_f32(exact), c["why"]
+
+
+def test_quantizer_invariants_random():
+    rng = np.random.default_rng(2)
+    v = (rng.standard_normal((64, 300)) * np.exp(rng.uniform(-6, 6, size=(64, 1)))).astype(np.float32)
+    v[5] = 0.0
+    codes, scale = orc.quantize_rows(v)
+    assert codes.dtype == np.int8
+    assert codes.min() >= -127 and codes.max() <= 127
+    assert scale[5] == 0 and not codes[5].any()
+    nz = np.abs(v).max(axis=1) > 0
+    # every nonzero row uses the full range once (its absmax maps to +-127)
+    assert np.all(np.abs(codes[nz]).max(axis=1) == 127)
+    # reconstruction error at most half a step (plus fp32 rounding of the scales)
+    amax = np.abs(v).max(axis=1).astype(np.float64)
+    err = np.abs(codes.astype(np.float64) * scale[:, None].astype(np.float64) - v.astype(np.float64))
+    bound = scale[:, None].astype(np.float64) * 0.5 + amax[:, None] * 2.0 ** -20
+    assert np.all(err <= bound)
+
+
+def test_quantizer_is_nearest_code():
+    # brute force: for each element, no other code is strictly closer to v/scale
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal((8, 40)) * 3).astype(np.float32)
+    codes, scale = orc.quantize_rows(v)
+    for i in range(v.shape[0]):
+        t = v[i].astype(np.float64) * 127.0 / np.abs(v[i]).max()
+        for j in range(v.shape[1]):
+            best = np.abs(np.arange(-127, 128) - t[j]).min()
+            assert abs(int(codes[i, j]) - t[j]) <= best + 1e-5
+
+
+def test_smoothing_direction():
+    """Activations are multiplied by smooth and weights divided (the pages'
+    identity): the dequantized operands must approximate X*s and W/s."""
+    rng = np.random.default_rng(4)
+    K = 96
+    s = np.exp(rng.uniform(-2.5, 2.5, K)).astype(np.float32)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((6, K)).astype(np.float32))
+    w = synth.f32_to_bf16_bits((rng.standard_normal((10, K)) * 0.02).astype(np.float32))
+    xq, sa = orc.smooth_quant_act(x, s)
+    wq, sw = orc.pack_weights(w, s)
+    xs = synth.bf16_bits_to_f32(x).astype(np.float64) * s
+    ws = synth.bf16_bits_to_f32(w).astype(np.float64) / s
+    assert np.all(np.abs(xq * sa[:, None].astype(np.float64) - xs) <= sa[:, None] * 0.5000001)
+    assert np.all(np.abs(wq * sw[:, None].astype(np.float64) - ws) <= sw[:, None] * 0.5000001)
+
+
+# ---------------------------------------------------------------- calibration
+
+def test_calibrate_fixture():
+    g = load("calibrate.json")
+    x = bf16(g["x_cal"])
+    w = bf16(g["w"])
+    s = orc.calibrate_smooth(x, w, 0.5)
+    assert s.dtype == np.float32
+    assert s.tolist() == g["alpha_0.5"]
+    s2 = orc.calibrate_smooth(x, w, 0.25)
+    for got, want in zip(s2.tolist(), g["alpha_0.25"]):
+        if want is not None:
+            assert got == want
+
+
+def test_calibrate_shrinks_outliers():
+    case = synth.small_case()
+    s = orc.calibrate_smooth(case.x_cal(), case.w())
+    out = case.outliers()
+    rest = np.setdiff1d(np.arange(case.K), out)
+    # outlier channels get a much smaller factor than the others
+    assert s[out].max() < 0.5 * np.median(s[rest])
+
+
+# ---------------------------------------------------------------- integer GEMM
+
+def brute_gemm(xq, wq):
+    M, K = xq.shape
+    N = wq.shape[0]
+    out = [[0] * N for _ in range(M)]
+    for m in range(M):
+        for n in range(N):
+            t = 0
+            for k in range(K):
+                t += int(xq[m, k]) * int(wq[n, k])
+            out[m][n] = t
+    return np.array(out, dtype=np.int64)
+
+
+def test_int_gemm_brute_force():
+    rng = np.random.default_rng(5)
+    for (M, N, K) in [(1, 1, 1), (3, 5, 7), (4, 8, 32), (2, 3, 64)]:
+        xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+        wq = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+        xq[0, 0] = -127
+        wq[0, 0] = -127
+        assert np.array_equal(orc.int_gemm(xq, wq), brute_gemm(xq, wq))
+
+
+def test_int_gemm_closed_forms():
+    K = 1024
+    ones = np.full((1, K), 127, np.int8)
+    assert orc.int_gemm(ones, ones)[0, 0] == 127 * 127 * K == 16516096
+    alt = np.tile(np.array([127, -127], np.int8), K // 2)[None, :]
+    assert orc.int_gemm(alt, ones)[0, 0] == 0
+    assert orc.int_gemm(alt, alt)[0, 0] == 16516096
+    neg = np.full((1, K), -127, np.int8)
+    assert orc.int_gemm(neg, ones)[0, 0] == -16516096
+    # beyond 2^24 the integer result is still exact
+    K2 = 131072
+    big = np.full((1, K2), 127, np.int8)
+    assert orc.int_gemm(big, big)[0, 0] == 127 * 127 * K2
+
+
+def test_int_gemm_matches_int64_matmul():
+    rng = np.random.default_rng(6)
+    xq = rng.integers(-127, 128, size=(9, 700)).astype(np.int8)
+    wq = rng.integers(-127, 128, size=(13, 700)).astype(np.int8)
+    assert np.array_equal(orc.int_gemm(xq, wq), xq.astype(np.int64) @ wq.astype(np.int64).T)
+
+
+# ---------------------------------------------------------------- dequant
+
+def test_dequant_fixture():
+    g = load("dequant.json")
+    y = orc.dequant(np.array(g["acc"], np.int64), np.array(g["sa"], np.float32), np.array(g["sw"], np.float32))
+    want = np.array([[int(h, 16) for h in row] for row in g["bf16"]], np.uint16)
+    assert np.array_equal(y, want)
+
+
+def test_dequant_int_to_f32_rounding():
+    # 2^24 + 1 is a tie between 2^24 and 2^24 + 2 -> even -> 2^24; then x1 x1 -> bf16(2^24)
+    acc = np.array([[16777217, 16777219, -16777217]], np.int64)
+    one = np.array([1.0], np.float32)
+    f = orc.dequant_f32(acc, one, np.ones(3, np.float32))
+    assert f.tolist() == [[16777216.0, 16777220.0, -16777216.0]]
+
+
+def test_dequant_is_correctly_rounded_steps():
+    # each fp32 multiply is a single correct rounding (exact rational model)
+    rng = np.random.default_rng(7)
+    M, N = 16, 40
+    acc = rng.integers(-2 ** 26, 2 ** 26, size=(M, N)).astype(np.int64)
+    sa = (rng.uniform(0.001, 0.2, M)).astype(np.float32)
+    sw = (rng.uniform(1e-5, 1e-3, N)).astype(np.float32)
+    f = orc.dequant_f32(acc, sa, sw)
+    for m in range(M):
+        for n in range(N):
+            a = round_to_f32(Fraction(int(acc[m, n])))
+            t = round_to_f32(a * Fraction(float(sa[m])))
+            y = round_to_f32(t * Fraction(float(sw[n])))
+            assert Fraction(float(f[m, n])) == y
+
+
+# ---------------------------------------------------------------- whole linear
+
+def test_fp64_identity():
+    """(W diag(s)^-1)(diag(s) X) == W X (zh §2) for arbitrary positive s."""
+    rng = np.random.default_rng(8)
+    x = synth.activations(11, 7, 64)
+    w = synth.weights(12, 9, 64)
+    s = np.exp(rng.uniform(-3, 3, 64)).astype(np.float32)
+    a = orc.smoothed_linear_f64(x, w, s)
+    b = orc.reference_linear_f64(x, w)
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+def test_scaled_identity_weight_closed_form():
+    """W = c*I, smooth = 1: each weight row quantizes to a single 127 with
+    sw = c/127, so acc = 127 * Xq exactly."""
+    K = 48
+    c = 0.5
+    w = bf16(np.eye(K) * c)
+    x = synth.activations(13, 5, K)
+    wq, sw = orc.pack_weights(w, np.ones(K, np.float32))
+    assert np.array_equal(wq, (np.eye(K) * 127).astype(np.int8))
+    assert np.all(Fraction(float(sw[0])) == round_to_f32(Fraction(1, 2) / 127))
+    xq, sa = orc.smooth_quant_act(x, np.ones(K, np.float32))
+    acc = orc.int_gemm(xq, wq)
+    assert np.array_equal(acc, 127 * xq.astype(np.int64))
+    y = synth.bf16_bits_to_f32(orc.dequant(acc, sa, sw)).astype(np.float64)
+    xv = synth.bf16_bits_to_f32(x).astype(np.float64)
+    assert np.all(np.abs(y - c * xv) <= c * sa[:, None] * 0.5 + np.abs(c * xv) * 2 ** -7 + 1e-6)
+
+
+def rel_fro(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def test_small_case_accuracy_and_reading():
+    """Calibrated smoothing keeps the W8A8 output within 2e-2 relative
+    Frobenius error of the unquantized product; the literal inverse reading
+    of s (outlier channels multiplied up) is clearly worse."""
+    case = synth.small_case()
+    x, w, xc = case.x(), case.w(), case.x_cal()
+    s = orc.calibrate_smooth(xc, w)
+    ref = orc.reference_linear_f64(x, w)
+
+    def run(smooth):
+        xq, sa = orc.smooth_quant_act(x, smooth)
+        wq, sw = orc.pack_weights(w, smooth)
+        return synth.bf16_bits_to_f32(orc.w8a8_linear(xq, sa, wq, sw)).astype(np.float64)
+
+    e_good = rel_fro(run(s), ref)
+    e_lit = rel_fro(run((1.0 / s.astype(np.float64)).astype(np.float32)), ref)
+    e_none = rel_fro(run(np.ones(case.K, np.float32)), ref)
+    assert e_good <= 2e-2, e_good
+    assert e_lit > 2 * e_good
+    assert e_none > e_good
+
+
+def test_smooth_one_reduces_to_plain_w8a8():
+    case = synth.small_case()
+    x, w = case.x(), case.w()
+    one = np.ones(case.K, np.float32)
+    xq, sa = orc.smooth_quant_act(x, one)
+    xq2, sa2 = orc.quantize_rows(synth.bf16_bits_to_f32(x))
+    assert np.array_equal(xq, xq2) and np.array_equal(sa, sa2)
+    wq, sw = orc.pack_weights(w, one)
+    wq2, sw2 = orc.quantize_rows(synth.bf16_bits_to_f32(w))
+    assert np.array_equal(wq, wq2) and np.array_equal(sw, sw2)
+
+
+# ---------------------------------------------------------------- verification
+
+def test_verify_greedy_fixture():
+    g = load("verify_cases.json")
+    lg = bf16(g["logits"])
+    for row, am in zip(g["logits"], g["argmax_by_row"]):
+        assert int(np.argmax(row)) == am
+    for c in g["cases"]:
+        n_acc, nxt = orc.verify_accept(lg[None], np.array([c["draft"]], np.int32), 0.0)
+        assert int(n_acc[0]) == c["n_acc"], c["why"]
+        assert int(nxt[0]) == c["next"], c["why"]
+
+
+def test_verify_no_drafts():
+    g = load("verify_cases.json")
+    lg = bf16(g["logits"])[:1][None]
+    n_acc, nxt = orc.verify_accept(lg, np.zeros((1, 0), np.int32), 0.0)
+    assert n_acc.tolist() == [0] and nxt.tolist() == [2]
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5, 2.0])
+def test_verify_two_level_closed_form(T):
+    """Logits: one entry L, the rest 0 -> p = e^(L/T) / (e^(L/T) + V - 1)."""
+    V, L, hot = 1000, 2.0, 17
+    row = np.zeros(V, np.float32)
+    row[hot] = L
+    lg = np.stack([row, row, row])[None]          # D = 2
+    bits = bf16(lg)
+    c = math.exp(L / T)
+    p_hot = c / (c + V - 1)
+    p_cold = 1.0 / (c + V - 1)
+    p = orc.acceptance_probabilities(bits, np.array([[hot, 3]], np.int32), T)
+    assert abs(p[0, 0] - p_hot) < 1e-12 and abs(p[0, 1] - p_cold) < 1e-12
+    cases = [
+        ([hot, hot], [p_hot / 2, p_hot / 2], 2),
+        ([hot, hot], [(1 + p_hot) / 2, 0.0], 0),
+        ([hot, 5], [p_hot / 2, p_cold / 2], 2),
+        ([hot, 5], [p_hot / 2, (p_cold + 1) / 2], 1),
+    ]
+    for draft, u, want in cases:
+        n_acc, nxt = orc.verify_accept(bits, np.array([draft], np.int32), T, np.array([u], np.float32))
+        assert int(n_acc[0]) == want
+        assert int(nxt[0]) == -1
+
+
+def test_verify_forced_mask_invariant():
+    """Drafts forced to the argmax on a seeded mask: n_acc is the first
+    unforced position unless a random draft happens to match."""
+    B, D, V = 6, 5, 257
+    lg, draft, mask, _ = synth.verify_inputs(B, D, V, 11, 12, 13, 14)
+    am = np.argmax(orc.bf16_to_f32(lg), axis=2)
+    d = np.where(mask, am[:, :D], draft).astype(np.int32)
+    n_acc, nxt = orc.verify_accept(lg, d, 0.0)
+    for b in range(B):
+        ok = d[b] == am[b, :D]
+        want = D if ok.all() else int(np.argmin(ok))
+        assert n_acc[b] == want
+        assert nxt[b] == am[b, want]
