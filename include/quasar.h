@@ -1,0 +1,208 @@
+/*
+ * quasar.h -- C ABI of libquasar.so, the GB300 (sm_103a) W8A8 verification
+ * path of Quasar quantized self-speculative decoding.
+ *
+ * Source of the method: "Quasar: Quantized Self-Speculative Acceleration for
+ * Rapid Inference via Memory-Efficient Verification" (arXiv 2603.01399), in
+ * its gist.science summaries.  Sections cited below are the summaries'
+ * technical sections: pt §2 "Metodologia", zh §2 "方法论", ko §2 "방법론".
+ *
+ * Common conventions
+ *  - Every pointer argument is DEVICE memory owned by the caller unless the
+ *    comment says otherwise.  The library never allocates device memory and
+ *    keeps no per-call state; the only library-owned device object is a
+ *    32-bit error word read by quasar_get_device_error().
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Host-side argument checks happen first; a call that
+ *    fails them returns an error code and launches nothing.
+ *  - Matrices are row-major.  "ld" arguments are row strides in elements.
+ *  - Base pointers of BF16 / INT8 matrices must be 16-byte aligned and their
+ *    row strides multiples of 16 bytes (TMA and 128-bit loads); fp32 / int32
+ *    vectors must be 4-byte aligned.  Violations return
+ *    QUASAR_ERR_UNSUPPORTED.
+ *  - Inputs are finite by contract; NaN/Inf behaviour is unspecified.
+ *  - Results are deterministic: integer work is exact and every floating
+ *    point reduction has a fixed order.
+ */
+#ifndef QUASAR_H
+#define QUASAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Binary-compatible with cudaStream_t. */
+typedef struct CUstream_st* quasar_stream_t;
+
+typedef enum {
+  QUASAR_OK = 0,
+  QUASAR_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad value   */
+  QUASAR_ERR_UNSUPPORTED = 2,   /* alignment / shape outside the contract   */
+  QUASAR_ERR_WORKSPACE = 3,     /* workspace missing or too small           */
+  QUASAR_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed         */
+  QUASAR_ERR_TIMEOUT = 5        /* a device-side bounded wait ran out        */
+} quasar_status_t;
+
+/* Static, NUL-terminated description of a status code (host only). */
+const char* quasar_status_string(int status);
+
+/* Library ABI version, (major << 16) | minor. */
+int quasar_version(void);
+
+/* Device-side error word.  Kernels never trap: a bounded wait that runs out
+ * (an mbarrier that is never completed, see the kernels) records its site in
+ * a device word and the kernel returns early.  This call synchronises
+ * `stream`, reads and clears the word, and returns QUASAR_OK or
+ * QUASAR_ERR_TIMEOUT (also QUASAR_ERR_CUDA if the synchronisation fails).
+ * If `site` is non-NULL (HOST pointer) it receives the recorded site code.
+ * After a timeout, any workspace in use must be zero-filled again. */
+quasar_status_t quasar_get_device_error(quasar_stream_t stream, uint32_t* site);
+
+/* Bound for the device-side waits, in nanoseconds (default 2e9 = 2 s).
+ * Host-side setting applied to the next launches; 0 restores the default. */
+quasar_status_t quasar_set_wait_limit_ns(uint64_t ns);
+
+/* ------------------------------------------------------------------------
+ * A0  Offline calibration of the smoothing vector.
+ *
+ * zh §2: the smoothing factor s is calibrated offline so that
+ * Y = (W·diag(s)^-1)·(diag(s)·X); s multiplies the activations and divides
+ * the weights.  Computed here as
+ *   smooth[k] = max_n|W[n][k]|^(1-alpha) / max_m|Xcal[m][k]|^alpha
+ * (SmoothQuant's migration factor inverted, so outlier activation channels
+ * shrink), in fp64 and rounded once to fp32; smooth[k] = 1 when either
+ * maximum is 0.  alpha == 0.5 uses IEEE sqrt and division (correctly
+ * rounded, bit-reproducible); other alpha in (0,1) use pow().
+ *
+ *   Xcal    [Mcal][ldx] BF16 calibration activations, Mcal >= 1
+ *   W       [N][ldw]    BF16 weights (all output rows that share this input,
+ *                       e.g. fused q/k/v), N >= 1, K >= 1
+ *   smooth  [K] fp32 output
+ *   workspace: >= quasar_calibrate_workspace_size(K) bytes, any contents;
+ *              the call clears what it uses.
+ * ------------------------------------------------------------------------ */
+size_t quasar_calibrate_workspace_size(int K);
+quasar_status_t quasar_calibrate_smooth(const void* Xcal_bf16, int Mcal, int ldx,
+                                        const void* W_bf16, int N, int ldw, int K,
+                                        float alpha, float* smooth,
+                                        void* workspace, size_t ws_bytes,
+                                        quasar_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * A1  Offline weight packing (fold diag(smooth)^-1, per-channel INT8).
+ *
+ * pt §2 step 1 / zh §2 / ko §2: weights are smoothed and quantized to INT8
+ * offline.  Per output channel n, in fp32 with IEEE rounding:
+ *   w'[k]  = float(W[n][k]) / smooth[k]
+ *   a      = max_k |w'[k]|
+ *   sw[n]  = a / 127                 (0 if a == 0)
+ *   Wq[n][k] = clamp(rne(w'[k] * (127 / a)), -127, 127)   (0 if a == 0)
+ *
+ *   W      [N][ldw] BF16, ldw >= K, ldw % 8 == 0
+ *   smooth [K] fp32, nonzero
+ *   Wq     [N][K] INT8 output (K-contiguous; K % 16 == 0)
+ *   sw     [N] fp32 output
+ * ------------------------------------------------------------------------ */
+quasar_status_t quasar_pack_weights(const void* W_bf16, int ldw, const float* smooth,
+                                    int N, int K, int8_t* Wq, float* sw,
+                                    quasar_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * A2  Online activation smoothing + per-token INT8 quantization.
+ *
+ * pt §2 step 2 / zh §2: during verification the BF16 input activations are
+ * smoothed and quantized on the fly.  Per token m, in fp32:
+ *   x'[k] = float(X[m][k]) * smooth[k]
+ *   a     = max_k |x'[k]|
+ *   sa[m] = a / 127                  (0 if a == 0)
+ *   Xq[m][k] = clamp(rne(x'[k] * (127 / a)), -127, 127)   (0 if a == 0)
+ *
+ *   X      [M][ldx] BF16, ldx >= K, ldx % 8 == 0; M >= 0 (M == 0: no-op)
+ *   smooth [K] fp32
+ *   Xq     [M][K] INT8 output (K % 16 == 0)
+ *   sa     [M] fp32 output
+ * ------------------------------------------------------------------------ */
+quasar_status_t quasar_smooth_quant_act(const void* X_bf16, int ldx, const float* smooth,
+                                        int M, int K, int8_t* Xq, float* sa,
+                                        quasar_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * A3 + A4  W8A8 linear: exact INT8 GEMM with fused BF16 dequant epilogue.
+ *
+ * pt §2 steps 3-4 / ko §2: the matmul runs on INT8 operands and the result
+ * is dequantized back to BF16 before the nonlinear layers:
+ *   acc[m][n] = sum_k Xq[m][k] * Wq[n][k]          (exact, int32)
+ *   Y[m][n]   = bf16_rne((float(acc[m][n]) * sa[m]) * sw[n])
+ *
+ *   Xq [M][K] INT8, sa [M] fp32 (from quasar_smooth_quant_act)
+ *   Wq [N][K] INT8, sw [N] fp32 (from quasar_pack_weights)
+ *   Y  [M][ldy] BF16 output, ldy >= N, ldy % 8 == 0
+ *   Sizes: M >= 0 (0 = no-op), 16 <= K <= 131072 with K % 16 == 0 (the int32
+ *   accumulator cannot overflow: 127*127*131072 < 2^31), N >= 8 with
+ *   N % 8 == 0.  Tuned for M <= 256 (verification passes); larger M works.
+ *   workspace: >= quasar_w8a8_linear_workspace_size(M, N, K) bytes of device
+ *   memory that is ZERO-FILLED before its first use.  The call leaves it
+ *   zero-filled again when it completes without a device error, so one
+ *   workspace can serve every linear on a stream.  Calls that share a
+ *   workspace must not run concurrently.  After QUASAR_ERR_TIMEOUT from
+ *   quasar_get_device_error the workspace must be zero-filled again.
+ * ------------------------------------------------------------------------ */
+size_t quasar_w8a8_linear_workspace_size(int M, int N, int K);
+quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
+                                   const int8_t* Wq, const float* sw,
+                                   int M, int N, int K,
+                                   void* Y_bf16, int ldy,
+                                   void* workspace, size_t ws_bytes,
+                                   quasar_stream_t stream);
+
+/* A3 alone: the exact int32 accumulator acc[M][N] (row stride N) instead of
+ * Y, same kernel and workspace contract.  For checking and for callers
+ * with their own epilogue. */
+quasar_status_t quasar_int8_gemm_s32(const int8_t* Xq, const int8_t* Wq,
+                                     int M, int N, int K, int32_t* acc,
+                                     void* workspace, size_t ws_bytes,
+                                     quasar_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * A5  Verification: accepted prefix length per sequence.
+ *
+ * zh §2 / ko §2: drafted tokens are checked against the dequantized,
+ * high-precision logits with rejection sampling; pt §4: greedy (T = 0)
+ * acceptance length.  Row j of sequence b scores the position that draft
+ * j fills; row D is the bonus position after the last draft.
+ *   T == 0:  ok_j = (draft[b][j] == argmax_v logits[b][j][v]), the lowest
+ *            index wins ties (values compared as BF16 numbers).
+ *   T  > 0:  p_j = softmax(float(logits[b][j][:]) / T)[draft[b][j]] in fp32;
+ *            ok_j = (u[b][j] < p_j).  The drafter is treated as
+ *            deterministic (its proposal probability is 1).
+ *   n_acc[b] = first j with !ok_j, or D.
+ *   next_token[b] (optional, T == 0 only) = argmax of row n_acc[b]: the
+ *   correction token on a rejection or the bonus token after D accepts.
+ *
+ *   logits [B][D+1][V] BF16, rows `ldl` elements apart (ldl >= V,
+ *          ldl % 8 == 0), row (b, j) at logits + (b*(D+1) + j)*ldl
+ *   draft  [B][D] int32, values in [0, V)
+ *   u      [B][D] fp32 in [0,1); required iff T > 0, else may be NULL
+ *   n_acc  [B] int32 output
+ *   next_token [B] int32 output or NULL; must be NULL when T > 0
+ *   Sizes: B >= 0 (0 = no-op), D >= 0, V >= 1.
+ *   workspace: >= quasar_verify_accept_workspace_size(B, D, V) bytes,
+ *   ZERO-FILLED before first use and left zero-filled by the call (same
+ *   contract as quasar_w8a8_linear).
+ * ------------------------------------------------------------------------ */
+size_t quasar_verify_accept_workspace_size(int B, int D, int V);
+quasar_status_t quasar_verify_accept(const void* logits_bf16, int ldl,
+                                     const int32_t* draft, int B, int D, int V,
+                                     float temperature, const float* u,
+                                     int32_t* n_acc, int32_t* next_token,
+                                     void* workspace, size_t ws_bytes,
+                                     quasar_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QUASAR_H */

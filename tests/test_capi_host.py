@@ -1,0 +1,112 @@
+"""Host-only checks of the C ABI: the library builds and loads without a GPU,
+exports every function include/quasar.h declares, and rejects bad arguments
+on the host before touching CUDA.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from w8a8_quantized_speculative_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build.build_library()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(quasar_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for want in ("quasar_pack_weights", "quasar_smooth_quant_act", "quasar_w8a8_linear", "quasar_verify_accept",
+                 "quasar_calibrate_smooth", "quasar_int8_gemm_s32", "quasar_get_device_error"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    lib.quasar_status_string.restype = ctypes.c_char_p
+    assert lib.quasar_status_string(0) == b"ok"
+    assert b"timed out" in lib.quasar_status_string(5)
+    assert lib.quasar_status_string(99) == b"unknown status"
+    assert lib.quasar_version() >> 16 == 1
+
+
+def test_workspace_sizes(lib):
+    lib.quasar_w8a8_linear_workspace_size.restype = ctypes.c_size_t
+    lib.quasar_verify_accept_workspace_size.restype = ctypes.c_size_t
+    lib.quasar_calibrate_workspace_size.restype = ctypes.c_size_t
+    ws = lib.quasar_w8a8_linear_workspace_size
+    # counters for 48 tiles x 8 warps (1536 B) + int32 accumulator 20 x 6144
+    assert ws(20, 6144, 4096) == 1536 + 20 * 6144 * 4
+    assert ws(0, 6144, 4096) == 0
+    assert ws(256, 4096, 4096) >= 256 * 4096 * 4
+    assert lib.quasar_calibrate_workspace_size(4096) == 8 * 4096
+    assert lib.quasar_verify_accept_workspace_size(32, 8, 151936) > 0
+    assert lib.quasar_verify_accept_workspace_size(0, 8, 151936) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)   # aligned, never dereferenced: validation fails first
+FAKE_ODD = ctypes.c_void_p(0x10004)
+
+
+def test_linear_rejects_bad_arguments(lib):
+    f = lib.quasar_w8a8_linear
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                                               ctypes.c_size_t, ctypes.c_void_p]
+    ok_args = [FAKE, FAKE, FAKE, FAKE, 8, 128, 128, FAKE, 128, FAKE, 1 << 20, None]
+
+    def call(**kw):
+        a = list(ok_args)
+        names = ["xq", "sa", "wq", "sw", "M", "N", "K", "y", "ldy", "ws", "wsb", "stream"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+
+    assert call(xq=None) == 1
+    assert call(M=-1) == 1
+    assert call(K=0) == 1
+    assert call(K=100) == 2          # K % 16
+    assert call(N=12) == 2           # N % 8
+    assert call(K=131072 + 16) == 2  # int32 overflow bound
+    assert call(ldy=64) == 2         # ldy < N
+    assert call(xq=FAKE_ODD) == 2    # 16-byte alignment
+    assert call(ws=None) == 3
+    assert call(wsb=16) == 3
+    assert call(M=0) == 0            # empty batch is a no-op
+
+
+def test_quant_and_verify_reject_bad_arguments(lib):
+    q = lib.quasar_smooth_quant_act
+    q.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    assert q(FAKE, 128, FAKE, 4, 120, FAKE, FAKE, None) == 2     # K % 16
+    assert q(FAKE, 64, FAKE, 4, 128, FAKE, FAKE, None) == 2      # ldx < K
+    assert q(None, 128, FAKE, 4, 128, FAKE, FAKE, None) == 1
+    assert q(FAKE, 128, FAKE, 0, 128, FAKE, FAKE, None) == 0     # M == 0
+    v = lib.quasar_verify_accept
+    v.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_size_t, ctypes.c_void_p]
+    assert v(FAKE, 1000, FAKE, 2, 3, 1000, 1.0, None, FAKE, None, FAKE, 1 << 20, None) == 1   # T>0 needs u
+    assert v(FAKE, 1000, FAKE, 2, 3, 1000, 1.0, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == 1   # next only for T=0
+    assert v(FAKE, 1000, FAKE, 2, 3, 1000, -1.0, None, FAKE, None, FAKE, 1 << 20, None) == 1  # T<0
+    assert v(FAKE, 1001, FAKE, 2, 3, 1000, 0.0, None, FAKE, None, FAKE, 1 << 20, None) == 2   # ldl % 8
+    assert v(FAKE, 1000, FAKE, 2, 3, 1000, 0.0, None, FAKE, None, FAKE, 16, None) == 3        # workspace
+    assert v(FAKE, 1000, FAKE, 0, 3, 1000, 0.0, None, FAKE, None, FAKE, 0, None) == 0         # B == 0

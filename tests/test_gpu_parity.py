@@ -1,0 +1,277 @@
+"""GPU parity: every C-ABI entry point against the CPU oracle on the same
+seeded inputs.  Integer outputs (codes, int32 accumulators, accepted
+lengths) and fp32 scales must match bit for bit; BF16 outputs within 1 BF16
+ulp of the oracle's identically ordered fp32 dequant (the kernels are built
+to match exactly, and the tests report the worst distance).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import oracle as orc  # noqa: E402
+from tests.gpu_util import bf16_ulp_distance, dev, dev_bf16, host_bf16_bits  # noqa: E402
+from w8a8_quantized_speculative_gb300 import synth  # noqa: E402
+from w8a8_quantized_speculative_gb300 import quasar as q  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+BF16_ULP_TOL = 1
+
+
+def check_ws_zero(ws):
+    torch.cuda.synchronize()
+    assert int(ws.buf.count_nonzero()) == 0, "workspace not left zero-filled"
+
+
+def gpu_linear_case(case):
+    x, w, xc = case.x(), case.w(), case.x_cal()
+    smooth = q.calibrate_smooth(dev_bf16(xc), dev_bf16(w))
+    s_ref = orc.calibrate_smooth(xc, w)
+    assert np.array_equal(smooth.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    wq, sw = q.pack_weights(dev_bf16(w), smooth)
+    xq, sa = q.smooth_quant_act(dev_bf16(x), smooth)
+    return x, w, s_ref, (xq, sa, wq, sw)
+
+
+# ---------------------------------------------------------------- A0 / A1 / A2
+
+def test_calibrate_alpha_quarter_within_one_ulp():
+    case = synth.small_case()
+    xc, w = case.x_cal(), case.w()
+    g = q.calibrate_smooth(dev_bf16(xc), dev_bf16(w), alpha=0.25).cpu().numpy()
+    r = orc.calibrate_smooth(xc, w, 0.25)
+    assert np.all(np.abs(g.view(np.int32) - r.view(np.int32)) <= 1)
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (3, 48), (8, 256), (20, 4096), (40, 12288), (256, 4096), (7, 4112)])
+def test_smooth_quant_act_bit_exact(M, K):
+    rng = np.random.default_rng(M * 1000 + K)
+    x = synth.activations(1000 + M, M, K, synth.outlier_channels(7, K, max(1, K // 100)), 30.0)
+    s = np.exp(rng.uniform(-2, 2, K)).astype(np.float32)
+    if M > 2:
+        x[2] = 0  # an all-zero token
+    xq, sa = q.smooth_quant_act(dev_bf16(x), dev(s))
+    xq_r, sa_r = orc.smooth_quant_act(x, s)
+    assert np.array_equal(xq.cpu().numpy(), xq_r)
+    assert np.array_equal(sa.cpu().numpy().view(np.uint32), sa_r.view(np.uint32))
+
+
+def test_smooth_quant_act_strided_rows():
+    M, K, ld = 5, 256, 384
+    full = synth.activations(77, M, ld)
+    s = np.linspace(0.5, 2.0, K).astype(np.float32)
+    xd = dev_bf16(full)[:, :K]
+    xq, sa = q.smooth_quant_act(xd, dev(s))
+    xq_r, sa_r = orc.smooth_quant_act(np.ascontiguousarray(full[:, :K]), s)
+    assert np.array_equal(xq.cpu().numpy(), xq_r) and np.array_equal(sa.cpu().numpy(), sa_r)
+
+
+@pytest.mark.parametrize("name", ["qkv", "down"])
+def test_pack_weights_full_size_bit_exact(name):
+    K, N = synth.LINEARS[name]
+    case = synth.sweep_case(name, 16)
+    w = case.w()
+    s = orc.calibrate_smooth(case.x_cal(), w)
+    wq, sw = q.pack_weights(dev_bf16(w), dev(s))
+    wq_r, sw_r = orc.pack_weights(w, s)
+    assert np.array_equal(wq.cpu().numpy(), wq_r)
+    assert np.array_equal(sw.cpu().numpy().view(np.uint32), sw_r.view(np.uint32))
+
+
+# ---------------------------------------------------------------- A3 exact integer GEMM
+
+SHAPES = [
+    (1, 8, 16), (5, 136, 144), (8, 512, 256), (16, 128, 1024), (17, 264, 1040), (20, 384, 4096),
+    (33, 256, 2048), (64, 640, 1152), (65, 128, 384), (128, 256, 512), (130, 136, 272), (256, 512, 1024),
+]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_int8_gemm_bit_exact(M, N, K):
+    rng = np.random.default_rng(M * 7919 + N * 31 + K)
+    xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    wq = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    ws = q.Workspace()
+    acc = q.int8_gemm_s32(dev(xq), dev(wq), workspace=ws).cpu().numpy()
+    assert np.array_equal(acc.astype(np.int64), orc.int_gemm(xq, wq))
+    check_ws_zero(ws)
+
+
+@pytest.mark.parametrize("K", [1024, 4096, 12288])
+def test_int8_gemm_adversarial_extremes(K):
+    """All products at +-127^2: every fp32 accumulation run sits at its exactness limit."""
+    M, N = 24, 256
+    xq = np.full((M, K), 127, np.int8)
+    xq[1::2] = -127
+    xq[2, ::2] = -127
+    wq = np.full((N, K), 127, np.int8)
+    wq[3::4] = -127
+    wq[5, 1::3] = -127
+    acc = q.int8_gemm_s32(dev(xq), dev(wq)).cpu().numpy()
+    assert np.array_equal(acc.astype(np.int64), orc.int_gemm(xq, wq))
+    assert acc[0, 0] == 127 * 127 * K
+
+
+def test_int8_gemm_deterministic_and_reusable_workspace():
+    rng = np.random.default_rng(3)
+    xq = dev(rng.integers(-127, 128, size=(20, 4096)).astype(np.int8))
+    wq = dev(rng.integers(-127, 128, size=(4096, 4096)).astype(np.int8))
+    ws = q.Workspace()
+    a = q.int8_gemm_s32(xq, wq, workspace=ws)
+    b = q.int8_gemm_s32(xq, wq, workspace=ws)
+    assert torch.equal(a, b)
+    check_ws_zero(ws)
+
+
+def test_gemm_empty_batch_is_noop():
+    y = torch.full((0, 128), 1.0, dtype=torch.bfloat16, device="cuda")
+    out = q.w8a8_linear(torch.empty((0, 128), dtype=torch.int8, device="cuda"),
+                        torch.empty(0, device="cuda"), torch.zeros((128, 128), dtype=torch.int8, device="cuda"),
+                        torch.ones(128, device="cuda"), y=y)
+    assert out.shape == (0, 128)
+
+
+# ---------------------------------------------------------------- A3 + A4 fused linear
+
+def test_small_case_end_to_end():
+    case = synth.small_case()
+    x, w, s, (xq, sa, wq, sw) = gpu_linear_case(case)
+    y = q.w8a8_linear(xq, sa, wq, sw)
+    xq_r, sa_r = orc.smooth_quant_act(x, s)
+    wq_r, sw_r = orc.pack_weights(w, s)
+    assert np.array_equal(xq.cpu().numpy(), xq_r) and np.array_equal(wq.cpu().numpy(), wq_r)
+    y_r = orc.w8a8_linear(xq_r, sa_r, wq_r, sw_r)
+    d = bf16_ulp_distance(host_bf16_bits(y), y_r)
+    assert d.max() <= BF16_ULP_TOL
+    assert d.max() == 0, "fused epilogue is expected to reproduce the oracle's order exactly"
+    yv = synth.bf16_bits_to_f32(host_bf16_bits(y)).astype(np.float64)
+    ref = orc.reference_linear_f64(x, w)
+    assert np.linalg.norm(yv - ref) / np.linalg.norm(ref) <= 2e-2
+
+
+@pytest.mark.parametrize("maker", ["attention", "mlp"])
+def test_qwen3_shaped_linears(maker):
+    cases = synth.attention_cases() if maker == "attention" else synth.mlp_cases()
+    ws = q.Workspace()
+    for case in cases:
+        x, w, s, (xq, sa, wq, sw) = gpu_linear_case(case)
+        y = q.w8a8_linear(xq, sa, wq, sw, workspace=ws)
+        xq_r, sa_r = orc.smooth_quant_act(x, s)
+        wq_r, sw_r = orc.pack_weights(w, s)
+        assert np.array_equal(xq.cpu().numpy(), xq_r)
+        assert np.array_equal(sa.cpu().numpy(), sa_r)
+        y_r = orc.w8a8_linear(xq_r, sa_r, wq_r, sw_r)
+        d = bf16_ulp_distance(host_bf16_bits(y), y_r)
+        assert d.max() <= BF16_ULP_TOL, (case.name, int(d.max()))
+        yv = synth.bf16_bits_to_f32(host_bf16_bits(y)).astype(np.float64)
+        ref = orc.reference_linear_f64(x, w)
+        assert np.linalg.norm(yv - ref) / np.linalg.norm(ref) <= 2e-2, case.name
+    check_ws_zero(ws)
+
+
+@pytest.mark.parametrize("M", [1, 64, 256])
+def test_sweep_linear_sampled(M):
+    """Full-size qkv / gate_up at sweep sizes, the launch configuration the
+    benchmark times; every output compared (the oracle is a BLAS matmul)."""
+    ws = q.Workspace()
+    for name in ("qkv", "gate_up"):
+        case = synth.sweep_case(name, M)
+        x, w, s, (xq, sa, wq, sw) = gpu_linear_case(case)
+        y = q.w8a8_linear(xq, sa, wq, sw, workspace=ws)
+        xq_r, sa_r = orc.smooth_quant_act(x, s)
+        wq_r, sw_r = orc.pack_weights(w, s)
+        y_r = orc.w8a8_linear(xq_r, sa_r, wq_r, sw_r)
+        d = bf16_ulp_distance(host_bf16_bits(y), y_r)
+        assert d.max() <= BF16_ULP_TOL, (name, M, int(d.max()))
+    check_ws_zero(ws)
+
+
+def test_linear_output_row_stride():
+    rng = np.random.default_rng(9)
+    M, N, K = 12, 136, 160
+    xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    wq = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    sa = rng.uniform(0.01, 0.1, M).astype(np.float32)
+    sw = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
+    ybig = torch.zeros((M, 200), dtype=torch.bfloat16, device="cuda")
+    q.w8a8_linear(dev(xq), dev(sa), dev(wq), dev(sw), y=ybig[:, :N])
+    y = host_bf16_bits(ybig)
+    assert np.array_equal(y[:, :N], orc.w8a8_linear(xq, sa, wq, sw))
+    assert not y[:, N:].any()
+
+
+# ---------------------------------------------------------------- A5 verification
+
+def test_verify_greedy_fixture():
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "verify_cases.json")))
+    lg = synth.f32_to_bf16_bits(np.array(g["logits"], np.float32))
+    # pad V to a multiple of 8 with very negative logits
+    V = 8
+    pad = np.full((lg.shape[0], V), synth.f32_to_bf16_bits(np.array([-100.0], np.float32))[0], np.uint16)
+    pad[:, :lg.shape[1]] = lg
+    for c in g["cases"]:
+        n_acc, nxt = q.verify_accept(dev_bf16(pad[None]), dev(np.array([c["draft"]], np.int32)))
+        assert int(n_acc[0]) == c["n_acc"] and int(nxt[0]) == c["next"], c["why"]
+
+
+@pytest.mark.parametrize("B,D,V", [(32, 8, 151936), (3, 0, 1000), (5, 4, 257), (2, 40, 4096), (64, 4, 32000)])
+def test_verify_greedy_random(B, D, V):
+    lg, draft, mask, _ = synth.verify_inputs(B, D, V, 501, 502, 503, 504)
+    am = np.argmax(orc.bf16_to_f32(lg), axis=2)
+    d = np.where(mask, am[:, :D], draft).astype(np.int32)
+    # plant ties: copy the max to a later and to an earlier index in some rows
+    for b in range(0, B, 3):
+        j = 0
+        k = int(am[b, j])
+        lg[b, j, (k + 7) % V] = lg[b, j, k]
+    am = np.argmax(orc.bf16_to_f32(lg), axis=2)
+    d = np.where(mask, am[:, :D], d).astype(np.int32)
+    ws = q.Workspace()
+    Vp = (V + 7) // 8 * 8            # row stride must be a multiple of 8 elements
+    padded = np.zeros((B, D + 1, Vp), np.uint16)
+    padded[:, :, :V] = lg
+    n_acc, nxt = q.verify_accept(dev_bf16(padded)[:, :, :V], dev(d), workspace=ws)
+    n_r, nxt_r = orc.verify_accept(lg, d, 0.0)
+    assert np.array_equal(n_acc.cpu().numpy(), n_r)
+    assert np.array_equal(nxt.cpu().numpy(), nxt_r)
+    check_ws_zero(ws)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_verify_sampled(T):
+    """Rejection test u < p: decisions must agree wherever |u - p| is larger
+    than the fp32 softmax error bound; drafts are made likely by sharpening
+    the logits so that acceptance actually happens."""
+    B, D, V = 16, 6, 4096
+    lg, draft, mask, u = synth.verify_inputs(B, D, V, 601, 602, 603, 604, std=3.0)
+    am = np.argmax(orc.bf16_to_f32(lg), axis=2)
+    d = np.where(mask, am[:, :D], draft).astype(np.int32)
+    p = orc.acceptance_probabilities(lg, d, T)
+    # keep decisions well away from the boundary: u at 0.5p (accept) or p + 0.5(1-p) (reject)
+    acc_mask = np.random.default_rng(605).random((B, D)) < 0.7
+    u = np.where(acc_mask, 0.5 * p, p + 0.5 * (1 - p)).astype(np.float32)
+    n_acc, nxt = q.verify_accept(dev_bf16(lg), dev(d), temperature=T, u=dev(u))
+    assert nxt is None
+    n_r, _ = orc.verify_accept(lg, d, T, u)
+    assert np.array_equal(n_acc.cpu().numpy(), n_r)
+
+
+def test_verify_sampled_two_level_closed_form():
+    import math
+    V, L, hot = 1024, 2.0, 17
+    row = np.zeros(V, np.float32)
+    row[hot] = L
+    lg = synth.f32_to_bf16_bits(np.stack([row, row, row])[None].astype(np.float32))
+    c = math.exp(L)
+    p_hot = c / (c + V - 1)
+    cases = [([hot, hot], [p_hot * 0.99, p_hot * 0.99], 2), ([hot, hot], [p_hot * 1.01, 0.0], 0),
+             ([hot, 5], [p_hot / 2, 0.9], 1)]
+    for draft, u, want in cases:
+        n_acc, _ = q.verify_accept(dev_bf16(lg), dev(np.array([draft], np.int32)), temperature=1.0,
+                                   u=dev(np.array([u], np.float32)))
+        assert int(n_acc[0]) == want

@@ -1,0 +1,89 @@
+// Library-wide C-ABI pieces: status strings, version, the device error word
+// and the wait limit used by every bounded device-side wait.
+#include <atomic>
+#include <mutex>
+
+#include "quasar_common.cuh"
+
+namespace quasar {
+
+// Site code of the first device-side wait that ran out since the last
+// quasar_get_device_error() (0 = none).  One word per device image.
+__device__ unsigned int g_error_word = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+int g_sms[kMaxDevices] = {0};
+std::mutex g_mu;
+}  // namespace
+
+unsigned int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = reinterpret_cast<unsigned int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(); }
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+quasar_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? QUASAR_OK : QUASAR_ERR_CUDA; }
+
+}  // namespace quasar
+
+extern "C" {
+
+const char* quasar_status_string(int status) {
+  switch (status) {
+    case QUASAR_OK: return "ok";
+    case QUASAR_ERR_INVALID_ARG: return "invalid argument";
+    case QUASAR_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+    case QUASAR_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case QUASAR_ERR_CUDA: return "CUDA runtime/driver error";
+    case QUASAR_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int quasar_version(void) { return (1 << 16) | 0; }
+
+quasar_status_t quasar_set_wait_limit_ns(uint64_t ns) {
+  quasar::g_wait_ns.store(ns ? ns : quasar::kDefaultWaitNs);
+  return QUASAR_OK;
+}
+
+quasar_status_t quasar_get_device_error(quasar_stream_t stream, uint32_t* site) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return QUASAR_ERR_CUDA;
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, quasar::g_error_word, sizeof(v));
+  if (e != cudaSuccess) return QUASAR_ERR_CUDA;
+  if (site) *site = v;
+  if (v) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(quasar::g_error_word, &zero, sizeof(zero)) != cudaSuccess) return QUASAR_ERR_CUDA;
+    return QUASAR_ERR_TIMEOUT;
+  }
+  return QUASAR_OK;
+}
+
+}  // extern "C"

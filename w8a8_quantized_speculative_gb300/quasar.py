@@ -1,0 +1,230 @@
+"""Thin ctypes binding of libquasar.so (argument marshalling only).
+
+Every function here checks tensor dtypes/devices, allocates outputs with
+torch when the caller does not pass them, and forwards raw device pointers
+and the current CUDA stream to the C ABI declared in ``include/quasar.h``.
+All arithmetic happens in the library's CUDA kernels.  Importing this module
+raises ImportError when the library has not been built: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libquasar.so is not built ({LIB_PATH}); run "
+                      "`python -m w8a8_quantized_speculative_gb300.build`")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_SIGS = {
+    "quasar_status_string": (ctypes.c_char_p, [_i]),
+    "quasar_version": (_i, []),
+    "quasar_get_device_error": (_i, [_p, ctypes.POINTER(ctypes.c_uint32)]),
+    "quasar_set_wait_limit_ns": (_i, [ctypes.c_uint64]),
+    "quasar_calibrate_workspace_size": (_sz, [_i]),
+    "quasar_calibrate_smooth": (_i, [_p, _i, _i, _p, _i, _i, _i, _f, _p, _p, _sz, _p]),
+    "quasar_pack_weights": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
+    "quasar_smooth_quant_act": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
+    "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
+    "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
+    "quasar_int8_gemm_s32": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
+    "quasar_verify_accept_workspace_size": (_sz, [_i, _i, _i]),
+    "quasar_verify_accept": (_i, [_p, _i, _p, _i, _i, _i, _f, _p, _p, _p, _p, _sz, _p]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+OK = 0
+STATUS = {0: "QUASAR_OK", 1: "QUASAR_ERR_INVALID_ARG", 2: "QUASAR_ERR_UNSUPPORTED", 3: "QUASAR_ERR_WORKSPACE",
+          4: "QUASAR_ERR_CUDA", 5: "QUASAR_ERR_TIMEOUT"}
+
+
+class QuasarError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib.quasar_status_string(status).decode()
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({msg})")
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise QuasarError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _rowmajor(t: torch.Tensor, name: str):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit inner stride")
+    return t.stride(0)
+
+
+class Workspace:
+    """Zero-filled device scratch that grows on demand.  The library leaves a
+    workspace zero-filled after each successful call, so one instance can be
+    shared by consecutive calls on the same stream."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda")
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        nbytes = max(int(nbytes), 256)
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+    def reset(self):
+        if self.buf is not None:
+            self.buf.zero_()
+
+
+_default_ws = {}
+
+
+def _ws(ws, device):
+    if ws is not None:
+        return ws
+    key = torch.device(device).index
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(device)
+    return _default_ws[key]
+
+
+# ---------------------------------------------------------------- entry points
+
+def calibrate_smooth(x_cal: torch.Tensor, w: torch.Tensor, alpha: float = 0.5, out=None, stream=None):
+    """smooth[k] = max|W[:,k]|^(1-alpha) / max|Xcal[:,k]|^alpha (fp32 [K])."""
+    _need(x_cal, torch.bfloat16, "x_cal")
+    _need(w, torch.bfloat16, "w")
+    ldx = _rowmajor(x_cal, "x_cal")
+    ldw = _rowmajor(w, "w")
+    K = x_cal.shape[1]
+    if w.shape[1] != K:
+        raise ValueError("x_cal and w disagree on K")
+    out = torch.empty(K, dtype=torch.float32, device=x_cal.device) if out is None else out
+    ws = torch.empty(max(int(lib.quasar_calibrate_workspace_size(K)), 16), dtype=torch.uint8, device=x_cal.device)
+    _check(lib.quasar_calibrate_smooth(_ptr(x_cal), x_cal.shape[0], ldx, _ptr(w), w.shape[0], ldw, K, alpha,
+                                       _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "calibrate_smooth")
+    return out
+
+
+def pack_weights(w: torch.Tensor, smooth: torch.Tensor, wq=None, sw=None, stream=None):
+    """(Wq int8 [N][K], sw fp32 [N]) from BF16 W [N][K] and smooth [K]."""
+    _need(w, torch.bfloat16, "w")
+    _need(smooth, torch.float32, "smooth")
+    ldw = _rowmajor(w, "w")
+    N, K = w.shape
+    wq = torch.empty((N, K), dtype=torch.int8, device=w.device) if wq is None else wq
+    sw = torch.empty(N, dtype=torch.float32, device=w.device) if sw is None else sw
+    _check(lib.quasar_pack_weights(_ptr(w), ldw, _ptr(smooth), N, K, _ptr(wq), _ptr(sw), _stream(stream)),
+           "pack_weights")
+    return wq, sw
+
+
+def smooth_quant_act(x: torch.Tensor, smooth: torch.Tensor, xq=None, sa=None, stream=None):
+    """(Xq int8 [M][K], sa fp32 [M]) from BF16 X [M][K] and smooth [K]."""
+    _need(x, torch.bfloat16, "x")
+    _need(smooth, torch.float32, "smooth")
+    ldx = _rowmajor(x, "x")
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.int8, device=x.device) if xq is None else xq
+    sa = torch.empty(M, dtype=torch.float32, device=x.device) if sa is None else sa
+    _check(lib.quasar_smooth_quant_act(_ptr(x), ldx, _ptr(smooth), M, K, _ptr(xq), _ptr(sa), _stream(stream)),
+           "smooth_quant_act")
+    return xq, sa
+
+
+def w8a8_linear(xq, sa, wq, sw, y=None, workspace: Workspace | None = None, stream=None):
+    """Y bf16 [M][N] = dequant(Xq · Wq^T) with the per-token / per-channel scales."""
+    _need(xq, torch.int8, "xq")
+    _need(wq, torch.int8, "wq")
+    M, K = xq.shape
+    N = wq.shape[0]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if y is None else y
+    ldy = _rowmajor(y, "y")
+    ws = _ws(workspace, xq.device)
+    need = int(lib.quasar_w8a8_linear_workspace_size(M, N, K))
+    buf = ws.get(need)
+    _check(lib.quasar_w8a8_linear(_ptr(xq), _ptr(sa), _ptr(wq), _ptr(sw), M, N, K, _ptr(y), ldy, _ptr(buf),
+                                  buf.numel(), _stream(stream)), "w8a8_linear")
+    return y
+
+
+def int8_gemm_s32(xq, wq, acc=None, workspace: Workspace | None = None, stream=None):
+    """acc int32 [M][N] = Xq · Wq^T, exact."""
+    _need(xq, torch.int8, "xq")
+    _need(wq, torch.int8, "wq")
+    M, K = xq.shape
+    N = wq.shape[0]
+    acc = torch.empty((M, N), dtype=torch.int32, device=xq.device) if acc is None else acc
+    ws = _ws(workspace, xq.device)
+    buf = ws.get(int(lib.quasar_w8a8_linear_workspace_size(M, N, K)))
+    _check(lib.quasar_int8_gemm_s32(_ptr(xq), _ptr(wq), M, N, K, _ptr(acc), _ptr(buf), buf.numel(),
+                                    _stream(stream)), "int8_gemm_s32")
+    return acc
+
+
+def verify_accept(logits: torch.Tensor, draft: torch.Tensor, temperature: float = 0.0, u=None,
+                  want_next: bool = True, n_acc=None, next_token=None, workspace: Workspace | None = None,
+                  stream=None):
+    """Accepted prefix length per sequence (int32 [B]) and, for T == 0, the
+    next token (argmax of row n_acc) or None.  logits: bf16 [B][D+1][V]."""
+    _need(logits, torch.bfloat16, "logits")
+    _need(draft, torch.int32, "draft")
+    if logits.dim() != 3 or logits.stride(2) != 1 or logits.stride(0) != logits.shape[1] * logits.stride(1):
+        raise ValueError("logits must be [B][D+1][V] with unit inner stride and packed rows")
+    B, R, V = logits.shape
+    D = R - 1
+    ldl = logits.stride(1)
+    n_acc = torch.empty(B, dtype=torch.int32, device=logits.device) if n_acc is None else n_acc
+    sampled = temperature > 0
+    if sampled:
+        _need(u, torch.float32, "u")
+        next_token = None
+    elif want_next and next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=logits.device)
+    ws = _ws(workspace, logits.device)
+    buf = ws.get(int(lib.quasar_verify_accept_workspace_size(B, D, V)))
+    _check(lib.quasar_verify_accept(_ptr(logits), ldl, _ptr(draft), B, D, V, float(temperature), _ptr(u),
+                                    _ptr(n_acc), _ptr(next_token), _ptr(buf), buf.numel(), _stream(stream)),
+           "verify_accept")
+    return n_acc, next_token
+
+
+def get_device_error(stream=None):
+    """Synchronise and return (status, site) of the library's device error word."""
+    site = ctypes.c_uint32(0)
+    st = lib.quasar_get_device_error(_stream(stream), ctypes.byref(site))
+    return st, site.value
+
+
+def set_wait_limit_ns(ns: int):
+    _check(lib.quasar_set_wait_limit_ns(ns), "set_wait_limit_ns")
