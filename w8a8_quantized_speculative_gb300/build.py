@@ -22,7 +22,7 @@ OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(LIB_DIR, "libquasar.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
+NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "-I", INCLUDE] + ARCH
 
 

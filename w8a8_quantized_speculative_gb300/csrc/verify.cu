@@ -13,7 +13,7 @@
 // loads; a CTA reduces its chunk to (max, first argmax, running max, sum of
 // exp) and stores that record.  The last CTA of a sequence (an atomic count;
 // nobody waits) merges the records of its D+1 rows in chunk order, which
-// makes every result deterministic, and resets the counter.
+// makes every result deterministic, then zeroes those records and the counter.
 #include <climits>
 
 #include "quasar_common.cuh"
@@ -188,8 +188,14 @@ verify_kernel(const uint16_t* __restrict__ logits, int ldl, const int32_t* __res
       for (int cc = 0; cc < S; ++cc) arg_merge(rb, ri, __ldcg(&pr[cc].best), __ldcg(&pr[cc].idx));
       next_token[b] = ri;
     }
-    atomicExch(&cnt[b], 0u);
   }
+  // Leave the workspace zero-filled for the next call (its records and counter).
+  __syncwarp();
+  for (int j = lane; j <= D; j += 32) {
+    Partial* pr = part + ((size_t)b * (D + 1) + j) * S;
+    for (int cc = 0; cc < S; ++cc) __stcg(reinterpret_cast<float4*>(&pr[cc]), make_float4(0.f, 0.f, 0.f, 0.f));
+  }
+  if (lane == 0) atomicExch(&cnt[b], 0u);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

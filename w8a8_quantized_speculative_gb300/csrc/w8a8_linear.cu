@@ -201,7 +201,7 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
       bool ok = true;
       for (long long i = b0; i < b1 && ok; ++i, ++li) {
         const int t = (int)(i / KB), kb = (int)(i % KB);
-        const long long seg_start = std::max(b0, (long long)t * KB);
+        const long long seg_start = b0 > (long long)t * KB ? b0 : (long long)t * KB;
         const int pos = (int)(i - seg_start);
         const bool seg_last = (i == b1 - 1) || (kb == KB - 1);
         const bool run_first = (pos % RUN_MAX) == 0;
@@ -252,7 +252,7 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     int R = -1;
     for (long long i = b0; i < b1; ++i, ++li) {
       const int t = (int)(i / KB), kb = (int)(i % KB);
-      const long long seg_start = std::max(b0, (long long)t * KB);
+      const long long seg_start = b0 > (long long)t * KB ? b0 : (long long)t * KB;
       const int pos = (int)(i - seg_start);
       const bool seg_last = (i == b1 - 1) || (kb == KB - 1);
       const bool run_first = (pos % RUN_MAX) == 0;

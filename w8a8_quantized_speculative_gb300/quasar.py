@@ -199,8 +199,9 @@ def verify_accept(logits: torch.Tensor, draft: torch.Tensor, temperature: float 
     next token (argmax of row n_acc) or None.  logits: bf16 [B][D+1][V]."""
     _need(logits, torch.bfloat16, "logits")
     _need(draft, torch.int32, "draft")
-    if logits.dim() != 3 or logits.stride(2) != 1 or logits.stride(0) != logits.shape[1] * logits.stride(1):
-        raise ValueError("logits must be [B][D+1][V] with unit inner stride and packed rows")
+    if logits.dim() != 3 or logits.stride(2) != 1 or (
+            logits.shape[0] > 1 and logits.stride(0) != logits.shape[1] * logits.stride(1)):
+        raise ValueError("logits must be [B][D+1][V] with unit inner stride and evenly spaced rows")
     B, R, V = logits.shape
     D = R - 1
     ldl = logits.stride(1)
