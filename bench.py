@@ -449,7 +449,8 @@ def run_sweep(q, dev, stream, ws, hbm):
     for name in ("qkv", "o", "gate_up", "down"):
         K, N = synth.LINEARS[name]
         ncopy = copies_for_cold_l2(N * K)
-        wqs = [torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev, generator=gen) for _ in range(ncopy)]
+        # random codes in the packed layout (N and K are multiples of 128 here)
+        wqs = [torch.randint(-127, 128, (N * K,), dtype=torch.int8, device=dev, generator=gen) for _ in range(ncopy)]
         sws = [torch.rand(N, device=dev, generator=gen) * 1e-3 for _ in range(ncopy)]
         nb = max(2, -(-4 * L2_BYTES // (2 * N * K)))
         wbf = [torch.randn((N, K), device=dev, generator=gen).to(torch.bfloat16) for _ in range(min(nb, 6))]

@@ -101,13 +101,29 @@ quasar_status_t quasar_calibrate_smooth(const void* Xcal_bf16, int Mcal, int ldx
  *   sw[n]  = a / 127                 (0 if a == 0)
  *   Wq[n][k] = clamp(rne(w'[k] * (127 / a)), -127, 127)   (0 if a == 0)
  *
+ * Packed layout (what quasar_w8a8_linear streams): the codes are stored in
+ * blocks of 128 rows x 128 K, block (tn, kb) at byte offset
+ * (tn * KB + kb) * 16384 with KB = ceil(K/128), so each block is 16 KB of
+ * contiguous memory.  Inside a block, row r (n = 128*tn + r) takes bytes
+ * [128r, 128r + 128); its 16-byte chunk c (k = 128*kb + 16c .. +15) sits at
+ * chunk position c ^ (r % 8).  Each byte holds the code plus 128 (the code
+ * with its sign bit flipped), so widening it needs no sign fix-up.  Rows
+ * n >= N and columns k >= K of the last tiles hold code 0 (byte 0x80).
+ * Size: quasar_packed_weight_bytes(N, K).
+ *
  *   W      [N][ldw] BF16, ldw >= K, ldw % 8 == 0
  *   smooth [K] fp32, nonzero
- *   Wq     [N][K] INT8 output (K-contiguous; K % 16 == 0)
+ *   Wp     packed INT8 output (K % 16 == 0)
  *   sw     [N] fp32 output
  * ------------------------------------------------------------------------ */
+size_t quasar_packed_weight_bytes(int N, int K);
 quasar_status_t quasar_pack_weights(const void* W_bf16, int ldw, const float* smooth,
-                                    int N, int K, int8_t* Wq, float* sw,
+                                    int N, int K, int8_t* Wp, float* sw,
+                                    quasar_stream_t stream);
+
+/* Relayout row-major INT8 codes Wq [N][K] (K % 16 == 0) into the packed
+ * layout above, for callers that quantized their weights themselves. */
+quasar_status_t quasar_tile_weights(const int8_t* Wq, int N, int K, int8_t* Wp,
                                     quasar_stream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -137,12 +153,17 @@ quasar_status_t quasar_smooth_quant_act(const void* X_bf16, int ldx, const float
  *   acc[m][n] = sum_k Xq[m][k] * Wq[n][k]          (exact, int32)
  *   Y[m][n]   = bf16_rne((float(acc[m][n]) * sa[m]) * sw[n])
  *
- *   Xq [M][K] INT8, sa [M] fp32 (from quasar_smooth_quant_act)
- *   Wq [N][K] INT8, sw [N] fp32 (from quasar_pack_weights)
+ *   Xq [M][K] INT8 row-major, sa [M] fp32 (from quasar_smooth_quant_act)
+ *   Wp packed INT8 weights, sw [N] fp32 (from quasar_pack_weights or
+ *      quasar_tile_weights)
  *   Y  [M][ldy] BF16 output, ldy >= N, ldy % 8 == 0
  *   Sizes: M >= 0 (0 = no-op), 16 <= K <= 131072 with K % 16 == 0 (the int32
  *   accumulator cannot overflow: 127*127*131072 < 2^31), N >= 8 with
  *   N % 8 == 0.  Tuned for M <= 256 (verification passes); larger M works.
+ *   The kernel is launched with programmatic dependent launch: it may start
+ *   streaming Wp before the previous kernel on `stream` has finished, and it
+ *   reads Xq / sa and writes Y and the workspace only after that kernel's
+ *   writes are visible.
  *   workspace: >= quasar_w8a8_linear_workspace_size(M, N, K) bytes of device
  *   memory that is ZERO-FILLED before its first use.  The call leaves it
  *   zero-filled again when it completes without a device error, so one
@@ -152,7 +173,7 @@ quasar_status_t quasar_smooth_quant_act(const void* X_bf16, int ldx, const float
  * ------------------------------------------------------------------------ */
 size_t quasar_w8a8_linear_workspace_size(int M, int N, int K);
 quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
-                                   const int8_t* Wq, const float* sw,
+                                   const int8_t* Wp, const float* sw,
                                    int M, int N, int K,
                                    void* Y_bf16, int ldy,
                                    void* workspace, size_t ws_bytes,
@@ -161,7 +182,7 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
 /* A3 alone: the exact int32 accumulator acc[M][N] (row stride N) instead of
  * Y, same kernel and workspace contract.  For checking and for callers
  * with their own epilogue. */
-quasar_status_t quasar_int8_gemm_s32(const int8_t* Xq, const int8_t* Wq,
+quasar_status_t quasar_int8_gemm_s32(const int8_t* Xq, const int8_t* Wp,
                                      int M, int N, int K, int32_t* acc,
                                      void* workspace, size_t ws_bytes,
                                      quasar_stream_t stream);

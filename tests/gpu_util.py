@@ -22,3 +22,16 @@ def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
         u = u.astype(np.int32)
         return np.where(u & 0x8000, -(u & 0x7FFF), u & 0x7FFF)
     return np.abs(key(a_bits) - key(b_bits))
+
+
+def unpack_weights(packed: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Row-major [N][K] INT8 codes from the packed layout documented in
+    include/quasar.h (128 x 128 blocks, tile-major, 16-byte chunks of row r
+    stored at chunk position c ^ (r % 8), bytes holding code + 128)."""
+    KB = (K + 127) // 128
+    TN = (N + 127) // 128
+    a = (np.asarray(packed).view(np.uint8)[: TN * KB * 16384] ^ 0x80).view(np.int8).reshape(TN, KB, 128, 8, 16)
+    r = np.arange(128)[:, None]
+    phys = np.arange(8)[None, :] ^ (r & 7)              # logical chunk c lives at phys[r, c]
+    logical = a[:, :, r, phys, :]                        # [TN][KB][128][8][16]
+    return logical.transpose(0, 2, 1, 3, 4).reshape(TN * 128, KB * 128)[:N, :K]

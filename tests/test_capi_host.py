@@ -53,8 +53,11 @@ def test_workspace_sizes(lib):
     lib.quasar_verify_accept_workspace_size.restype = ctypes.c_size_t
     lib.quasar_calibrate_workspace_size.restype = ctypes.c_size_t
     ws = lib.quasar_w8a8_linear_workspace_size
-    # counters for 48 tiles x 8 warps (1536 B) + int32 accumulator 20 x 6144
-    assert ws(20, 6144, 4096) == 1536 + 20 * 6144 * 4
+    # counters for 48 tiles x 16 converter warps (3072 B) + int32 accumulator 20 x 6144
+    assert ws(20, 6144, 4096) == 3072 + 20 * 6144 * 4
+    lib.quasar_packed_weight_bytes.restype = ctypes.c_size_t
+    assert lib.quasar_packed_weight_bytes(6144, 4096) == 6144 * 4096
+    assert lib.quasar_packed_weight_bytes(136, 144) == 2 * 2 * 16384
     assert ws(0, 6144, 4096) == 0
     assert ws(256, 4096, 4096) >= 256 * 4096 * 4
     assert lib.quasar_calibrate_workspace_size(4096) == 8 * 4096

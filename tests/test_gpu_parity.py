@@ -12,7 +12,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import oracle as orc  # noqa: E402
-from tests.gpu_util import bf16_ulp_distance, dev, dev_bf16, host_bf16_bits  # noqa: E402
+from tests.gpu_util import bf16_ulp_distance, dev, dev_bf16, host_bf16_bits, unpack_weights  # noqa: E402
 from w8a8_quantized_speculative_gb300 import synth  # noqa: E402
 from w8a8_quantized_speculative_gb300 import quasar as q  # noqa: E402
 
@@ -75,10 +75,28 @@ def test_pack_weights_full_size_bit_exact(name):
     case = synth.sweep_case(name, 16)
     w = case.w()
     s = orc.calibrate_smooth(case.x_cal(), w)
-    wq, sw = q.pack_weights(dev_bf16(w), dev(s))
+    wp, sw = q.pack_weights(dev_bf16(w), dev(s))
     wq_r, sw_r = orc.pack_weights(w, s)
-    assert np.array_equal(wq.cpu().numpy(), wq_r)
+    assert np.array_equal(unpack_weights(wp.cpu().numpy(), N, K), wq_r)
     assert np.array_equal(sw.cpu().numpy().view(np.uint32), sw_r.view(np.uint32))
+
+
+@pytest.mark.parametrize("N,K", [(136, 144), (8, 16), (300, 1040)])
+def test_pack_and_tile_ragged(N, K):
+    """Ragged N and K: packed codes match the oracle, padding is zero, and
+    tiling row-major codes gives the same buffer."""
+    rng = np.random.default_rng(N + K)
+    w = synth.weights(55, N, K)
+    s = np.exp(rng.uniform(-1, 1, K)).astype(np.float32)
+    wp, sw = q.pack_weights(dev_bf16(w), dev(s))
+    wq_r, sw_r = orc.pack_weights(w, s)
+    host = wp.cpu().numpy()
+    assert host.size == q.packed_weight_bytes(N, K)
+    assert np.array_equal(unpack_weights(host, N, K), wq_r)
+    assert np.array_equal(sw.cpu().numpy(), sw_r)
+    full = unpack_weights(host, ((N + 127) // 128) * 128, ((K + 127) // 128) * 128)
+    assert not full[N:].any() and not full[:, K:].any()
+    assert torch.equal(q.tile_weights(dev(wq_r)), wp)
 
 
 # ---------------------------------------------------------------- A3 exact integer GEMM
@@ -95,7 +113,7 @@ def test_int8_gemm_bit_exact(M, N, K):
     xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
     wq = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
     ws = q.Workspace()
-    acc = q.int8_gemm_s32(dev(xq), dev(wq), workspace=ws).cpu().numpy()
+    acc = q.int8_gemm_s32(dev(xq), q.tile_weights(dev(wq)), N, workspace=ws).cpu().numpy()
     assert np.array_equal(acc.astype(np.int64), orc.int_gemm(xq, wq))
     check_ws_zero(ws)
 
@@ -110,7 +128,7 @@ def test_int8_gemm_adversarial_extremes(K):
     wq = np.full((N, K), 127, np.int8)
     wq[3::4] = -127
     wq[5, 1::3] = -127
-    acc = q.int8_gemm_s32(dev(xq), dev(wq)).cpu().numpy()
+    acc = q.int8_gemm_s32(dev(xq), q.tile_weights(dev(wq)), N).cpu().numpy()
     assert np.array_equal(acc.astype(np.int64), orc.int_gemm(xq, wq))
     assert acc[0, 0] == 127 * 127 * K
 
@@ -118,10 +136,10 @@ def test_int8_gemm_adversarial_extremes(K):
 def test_int8_gemm_deterministic_and_reusable_workspace():
     rng = np.random.default_rng(3)
     xq = dev(rng.integers(-127, 128, size=(20, 4096)).astype(np.int8))
-    wq = dev(rng.integers(-127, 128, size=(4096, 4096)).astype(np.int8))
+    wp = q.tile_weights(dev(rng.integers(-127, 128, size=(4096, 4096)).astype(np.int8)))
     ws = q.Workspace()
-    a = q.int8_gemm_s32(xq, wq, workspace=ws)
-    b = q.int8_gemm_s32(xq, wq, workspace=ws)
+    a = q.int8_gemm_s32(xq, wp, 4096, workspace=ws)
+    b = q.int8_gemm_s32(xq, wp, 4096, workspace=ws)
     assert torch.equal(a, b)
     check_ws_zero(ws)
 
@@ -129,7 +147,7 @@ def test_int8_gemm_deterministic_and_reusable_workspace():
 def test_gemm_empty_batch_is_noop():
     y = torch.full((0, 128), 1.0, dtype=torch.bfloat16, device="cuda")
     out = q.w8a8_linear(torch.empty((0, 128), dtype=torch.int8, device="cuda"),
-                        torch.empty(0, device="cuda"), torch.zeros((128, 128), dtype=torch.int8, device="cuda"),
+                        torch.empty(0, device="cuda"), torch.zeros(128 * 128, dtype=torch.int8, device="cuda"),
                         torch.ones(128, device="cuda"), y=y)
     assert out.shape == (0, 128)
 
@@ -142,7 +160,8 @@ def test_small_case_end_to_end():
     y = q.w8a8_linear(xq, sa, wq, sw)
     xq_r, sa_r = orc.smooth_quant_act(x, s)
     wq_r, sw_r = orc.pack_weights(w, s)
-    assert np.array_equal(xq.cpu().numpy(), xq_r) and np.array_equal(wq.cpu().numpy(), wq_r)
+    assert np.array_equal(xq.cpu().numpy(), xq_r)
+    assert np.array_equal(unpack_weights(wq.cpu().numpy(), case.N, case.K), wq_r)
     y_r = orc.w8a8_linear(xq_r, sa_r, wq_r, sw_r)
     d = bf16_ulp_distance(host_bf16_bits(y), y_r)
     assert d.max() <= BF16_ULP_TOL
@@ -197,7 +216,7 @@ def test_linear_output_row_stride():
     sa = rng.uniform(0.01, 0.1, M).astype(np.float32)
     sw = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
     ybig = torch.zeros((M, 200), dtype=torch.bfloat16, device="cuda")
-    q.w8a8_linear(dev(xq), dev(sa), dev(wq), dev(sw), y=ybig[:, :N])
+    q.w8a8_linear(dev(xq), dev(sa), q.tile_weights(dev(wq)), dev(sw), y=ybig[:, :N])
     y = host_bf16_bits(ybig)
     assert np.array_equal(y[:, :N], orc.w8a8_linear(xq, sa, wq, sw))
     assert not y[:, N:].any()

@@ -13,6 +13,12 @@
 // absmax, then a second pass that re-derives v (bit-identical) and stores
 // 8 codes per 64-bit store.  Rows are short (<= 24 KB) and the second pass
 // is served from L1/L2.
+//
+// Activation codes are written row-major [M][K].  Weight codes are written in
+// the packed layout the W8A8 linear streams: 128 x 128 blocks, tile-major,
+// each block 16 KB contiguous with the 16-byte chunks of row r stored in
+// 128B-swizzled order (chunk c at position c ^ (r % 8)), each byte holding
+// code + 128; see quasar.h.
 #include <algorithm>
 
 #include "quasar_common.cuh"
@@ -36,10 +42,21 @@ QUASAR_DEVICE_INLINE void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
-template <bool DIVIDE>
+// Byte offset of code (n, k) in the packed weight layout (k a multiple of 8).
+QUASAR_DEVICE_INLINE size_t packed_offset(int n, int k, int KB) {
+  const int r = n & 127, kk = k & 127, c = kk >> 4;
+  return (((size_t)(n >> 7) * KB + (k >> 7)) * 128 + r) * 128 + ((c ^ (r & 7)) << 4) + (kk & 15);
+}
+
+template <bool DIVIDE, bool PACKED>
 __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const uint16_t* __restrict__ in, int ld,
                                                              const float* __restrict__ smooth, int K,
                                                              int8_t* __restrict__ q, float* __restrict__ scale) {
+  // Launched with programmatic dependent launch: let the next kernel start
+  // its independent prologue (e.g. a GEMM's weight stream) at once, then
+  // wait until the previous kernel's writes (our input) are visible.
+  pdl_launch_dependents();
+  pdl_wait();
   const int row = blockIdx.x;
   const uint16_t* src = in + (size_t)row * ld;
   const int nvec = K / 8;
@@ -75,6 +92,7 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const uint16_t* __r
 
   // Pass 2: codes.
   int8_t* dst = q + (size_t)row * K;
+  const int KB = (K + 127) >> 7;
   for (int v = threadIdx.x; v < nvec; v += THREADS) {
     uint32_t packed[2] = {0u, 0u};
     if (amax > 0.f) {
@@ -91,11 +109,31 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const uint16_t* __r
         packed[i >> 2] |= (uint32_t)(c & 0xFF) << (8 * (i & 3));
       }
     }
-    reinterpret_cast<uint2*>(dst)[v] = make_uint2(packed[0], packed[1]);
+    if (PACKED)  // packed weight bytes hold code + 128
+      *reinterpret_cast<uint2*>(q + packed_offset(row, 8 * v, KB)) =
+          make_uint2(packed[0] ^ 0x80808080u, packed[1] ^ 0x80808080u);
+    else
+      reinterpret_cast<uint2*>(dst)[v] = make_uint2(packed[0], packed[1]);
   }
 }
 
-template <bool DIVIDE>
+// Row-major INT8 codes [N][K] -> packed layout, 16 bytes per thread.
+__global__ void tile_weights_kernel(const int8_t* __restrict__ src, int N, int K, int8_t* __restrict__ dst) {
+  const int chunks = K / 16;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)N * chunks) return;
+  const int n = (int)(i / chunks), k = (int)(i % chunks) * 16;
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (size_t)n * K + k));
+  const uint32_t b = 0x80808080u;  // packed bytes hold code + 128
+  *reinterpret_cast<uint4*>(dst + packed_offset(n, k, (K + 127) >> 7)) = make_uint4(v.x ^ b, v.y ^ b, v.z ^ b, v.w ^ b);
+}
+
+size_t packed_bytes(int N, int K) {
+  if (N <= 0 || K <= 0) return 0;
+  return (size_t)((N + 127) / 128) * ((K + 127) / 128) * 128 * 128;
+}
+
+template <bool DIVIDE, bool PACKED>
 static quasar_status_t run(const void* in, int ld, const float* smooth, int rows, int K, int8_t* q, float* scale,
                            cudaStream_t stream) {
   if (rows < 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
@@ -104,9 +142,26 @@ static quasar_status_t run(const void* in, int ld, const float* smooth, int rows
   if (!in || !smooth || !q || !scale) return QUASAR_ERR_INVALID_ARG;
   if (!aligned(in, 16) || !aligned(smooth, 16) || !aligned(q, 16) || !aligned(scale, 4))
     return QUASAR_ERR_UNSUPPORTED;
-  quant_rows_kernel<DIVIDE><<<rows, THREADS, 0, stream>>>(reinterpret_cast<const uint16_t*>(in), ld, smooth, K,
-                                                          q, scale);
-  return cuda_status(cudaGetLastError());
+  if (PACKED) {
+    // The padding of the last row tile and K block must read as zero codes
+    // (byte 0x80 in the biased packed format).
+    cudaError_t e = cudaMemsetAsync(q, 0x80, packed_bytes(rows, K), stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    quant_rows_kernel<DIVIDE, PACKED><<<rows, THREADS, 0, stream>>>(reinterpret_cast<const uint16_t*>(in), ld,
+                                                                    smooth, K, q, scale);
+    return cuda_status(cudaGetLastError());
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(THREADS);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, quant_rows_kernel<DIVIDE, PACKED>,
+                                        reinterpret_cast<const uint16_t*>(in), ld, smooth, K, q, scale));
 }
 
 }  // namespace quant
@@ -114,15 +169,31 @@ static quasar_status_t run(const void* in, int ld, const float* smooth, int rows
 
 extern "C" {
 
-quasar_status_t quasar_pack_weights(const void* W_bf16, int ldw, const float* smooth, int N, int K, int8_t* Wq,
+size_t quasar_packed_weight_bytes(int N, int K) { return quasar::quant::packed_bytes(N, K); }
+
+quasar_status_t quasar_pack_weights(const void* W_bf16, int ldw, const float* smooth, int N, int K, int8_t* Wp,
                                     float* sw, quasar_stream_t stream) {
   if (N <= 0) return QUASAR_ERR_INVALID_ARG;
-  return quasar::quant::run<true>(W_bf16, ldw, smooth, N, K, Wq, sw, reinterpret_cast<cudaStream_t>(stream));
+  return quasar::quant::run<true, true>(W_bf16, ldw, smooth, N, K, Wp, sw, reinterpret_cast<cudaStream_t>(stream));
+}
+
+quasar_status_t quasar_tile_weights(const int8_t* Wq, int N, int K, int8_t* Wp, quasar_stream_t stream_) {
+  using namespace quasar;
+  if (N <= 0 || K <= 0 || !Wq || !Wp) return QUASAR_ERR_INVALID_ARG;
+  if (K % 16 != 0) return QUASAR_ERR_UNSUPPORTED;
+  if (!aligned(Wq, 16) || !aligned(Wp, 16)) return QUASAR_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  cudaError_t e = cudaMemsetAsync(Wp, 0x80, quant::packed_bytes(N, K), stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  const long long items = (long long)N * (K / 16);
+  quant::tile_weights_kernel<<<(unsigned)((items + 255) / 256), 256, 0, stream>>>(Wq, N, K, Wp);
+  return cuda_status(cudaGetLastError());
 }
 
 quasar_status_t quasar_smooth_quant_act(const void* X_bf16, int ldx, const float* smooth, int M, int K,
                                         int8_t* Xq, float* sa, quasar_stream_t stream) {
-  return quasar::quant::run<false>(X_bf16, ldx, smooth, M, K, Xq, sa, reinterpret_cast<cudaStream_t>(stream));
+  return quasar::quant::run<false, false>(X_bf16, ldx, smooth, M, K, Xq, sa,
+                                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -111,6 +111,37 @@ QUASAR_DEVICE_INLINE void tma_load_2d(void* dst, const void* tmap, int x, int y,
       : "memory");
 }
 
+// 1-D bulk copy global -> shared memory, completing on `bar` (tx bytes).
+// Both addresses 16-byte aligned, size a multiple of 16.
+QUASAR_DEVICE_INLINE void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// independent prologue now / wait until the previous kernel's writes are
+// visible.  Both are no-ops for a launch without the PDL attribute.
+QUASAR_DEVICE_INLINE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+QUASAR_DEVICE_INLINE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Named-barrier synchronisation of `count` threads (whole warps) that also
+// returns the OR of every participant's `pred`; involves no memory access.
+QUASAR_DEVICE_INLINE bool named_barrier_or(int id, int count, uint32_t pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pin, pout;\n\t"
+      "setp.ne.b32 pin, %1, 0;\n\t"
+      "barrier.red.or.pred pout, %2, %3, pin;\n\t"
+      "selp.u32 %0, 1, 0, pout;\n\t}"
+      : "=r"(out)
+      : "r"(pred), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+
 QUASAR_DEVICE_INLINE uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -186,8 +217,26 @@ QUASAR_DEVICE_INLINE void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 
+// Store 16 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+QUASAR_DEVICE_INLINE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Load 4 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+QUASAR_DEVICE_INLINE void tmem_ld4(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+}
+
 // Load 8 consecutive 32-bit columns of this warp's 32 TMEM lanes.
-QUASAR_DEVICE_INLINE void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+QUASAR_DEVICE_INLINE void tmem_ld8(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                : "r"(taddr)
@@ -201,8 +250,15 @@ QUASAR_DEVICE_INLINE void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
 // number 1024 + (b + 128) (exponent field 0x64: ulp 1 on [1024, 2048));
 // subtracting 1152 = 1024 + 128 leaves b.  Integer-valued fp16 arithmetic
 // in this range is exact.
+QUASAR_DEVICE_INLINE void u8x4_to_f16x4(uint32_t u, uint32_t& lo, uint32_t& hi);
 QUASAR_DEVICE_INLINE void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
+  u8x4_to_f16x4(w ^ 0x80808080u, lo, hi);
+}
+
+// Four bytes holding code + 128 (code in [-128, 127]) -> two fp16x2 words
+// holding the codes, exactly (same construction as above without the bias
+// flip).
+QUASAR_DEVICE_INLINE void u8x4_to_f16x4(uint32_t u, uint32_t& lo, uint32_t& hi) {
   uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);  // bytes: u0, 0x64, u1, 0x64
   uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);  // bytes: u2, 0x64, u3, 0x64
   const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));

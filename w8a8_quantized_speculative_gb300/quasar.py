@@ -34,7 +34,9 @@ _SIGS = {
     "quasar_set_wait_limit_ns": (_i, [ctypes.c_uint64]),
     "quasar_calibrate_workspace_size": (_sz, [_i]),
     "quasar_calibrate_smooth": (_i, [_p, _i, _i, _p, _i, _i, _i, _f, _p, _p, _sz, _p]),
+    "quasar_packed_weight_bytes": (_sz, [_i, _i]),
     "quasar_pack_weights": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
+    "quasar_tile_weights": (_i, [_p, _i, _i, _p, _p]),
     "quasar_smooth_quant_act": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
     "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
@@ -136,17 +138,33 @@ def calibrate_smooth(x_cal: torch.Tensor, w: torch.Tensor, alpha: float = 0.5, o
     return out
 
 
-def pack_weights(w: torch.Tensor, smooth: torch.Tensor, wq=None, sw=None, stream=None):
-    """(Wq int8 [N][K], sw fp32 [N]) from BF16 W [N][K] and smooth [K]."""
+def packed_weight_bytes(N: int, K: int) -> int:
+    return int(lib.quasar_packed_weight_bytes(N, K))
+
+
+def pack_weights(w: torch.Tensor, smooth: torch.Tensor, wp=None, sw=None, stream=None):
+    """(Wp packed int8 [packed_weight_bytes], sw fp32 [N]) from BF16 W [N][K]
+    and smooth [K].  The packed layout is described in include/quasar.h."""
     _need(w, torch.bfloat16, "w")
     _need(smooth, torch.float32, "smooth")
     ldw = _rowmajor(w, "w")
     N, K = w.shape
-    wq = torch.empty((N, K), dtype=torch.int8, device=w.device) if wq is None else wq
+    wp = torch.empty(packed_weight_bytes(N, K), dtype=torch.int8, device=w.device) if wp is None else wp
     sw = torch.empty(N, dtype=torch.float32, device=w.device) if sw is None else sw
-    _check(lib.quasar_pack_weights(_ptr(w), ldw, _ptr(smooth), N, K, _ptr(wq), _ptr(sw), _stream(stream)),
+    _check(lib.quasar_pack_weights(_ptr(w), ldw, _ptr(smooth), N, K, _ptr(wp), _ptr(sw), _stream(stream)),
            "pack_weights")
-    return wq, sw
+    return wp, sw
+
+
+def tile_weights(wq: torch.Tensor, wp=None, stream=None):
+    """Packed int8 weights from row-major int8 codes [N][K]."""
+    _need(wq, torch.int8, "wq")
+    if not wq.is_contiguous():
+        raise ValueError("wq must be contiguous")
+    N, K = wq.shape
+    wp = torch.empty(packed_weight_bytes(N, K), dtype=torch.int8, device=wq.device) if wp is None else wp
+    _check(lib.quasar_tile_weights(_ptr(wq), N, K, _ptr(wp), _stream(stream)), "tile_weights")
+    return wp
 
 
 def smooth_quant_act(x: torch.Tensor, smooth: torch.Tensor, xq=None, sa=None, stream=None):
@@ -162,32 +180,38 @@ def smooth_quant_act(x: torch.Tensor, smooth: torch.Tensor, xq=None, sa=None, st
     return xq, sa
 
 
-def w8a8_linear(xq, sa, wq, sw, y=None, workspace: Workspace | None = None, stream=None):
-    """Y bf16 [M][N] = dequant(Xq · Wq^T) with the per-token / per-channel scales."""
+def _check_packed(wp, N, K):
+    _need(wp, torch.int8, "wp")
+    if wp.numel() < packed_weight_bytes(N, K) or not wp.is_contiguous():
+        raise ValueError("wp must be a contiguous packed weight buffer of packed_weight_bytes(N, K)")
+
+
+def w8a8_linear(xq, sa, wp, sw, y=None, workspace: Workspace | None = None, stream=None):
+    """Y bf16 [M][N] = dequant(Xq · Wq^T) with the per-token / per-channel
+    scales; wp is the packed weight buffer, N = len(sw)."""
     _need(xq, torch.int8, "xq")
-    _need(wq, torch.int8, "wq")
     M, K = xq.shape
-    N = wq.shape[0]
+    N = sw.numel()
+    _check_packed(wp, N, K)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if y is None else y
     ldy = _rowmajor(y, "y")
     ws = _ws(workspace, xq.device)
     need = int(lib.quasar_w8a8_linear_workspace_size(M, N, K))
     buf = ws.get(need)
-    _check(lib.quasar_w8a8_linear(_ptr(xq), _ptr(sa), _ptr(wq), _ptr(sw), M, N, K, _ptr(y), ldy, _ptr(buf),
+    _check(lib.quasar_w8a8_linear(_ptr(xq), _ptr(sa), _ptr(wp), _ptr(sw), M, N, K, _ptr(y), ldy, _ptr(buf),
                                   buf.numel(), _stream(stream)), "w8a8_linear")
     return y
 
 
-def int8_gemm_s32(xq, wq, acc=None, workspace: Workspace | None = None, stream=None):
-    """acc int32 [M][N] = Xq · Wq^T, exact."""
+def int8_gemm_s32(xq, wp, N: int, acc=None, workspace: Workspace | None = None, stream=None):
+    """acc int32 [M][N] = Xq · Wq^T, exact; wp is the packed weight buffer."""
     _need(xq, torch.int8, "xq")
-    _need(wq, torch.int8, "wq")
     M, K = xq.shape
-    N = wq.shape[0]
+    _check_packed(wp, N, K)
     acc = torch.empty((M, N), dtype=torch.int32, device=xq.device) if acc is None else acc
     ws = _ws(workspace, xq.device)
     buf = ws.get(int(lib.quasar_w8a8_linear_workspace_size(M, N, K)))
-    _check(lib.quasar_int8_gemm_s32(_ptr(xq), _ptr(wq), M, N, K, _ptr(acc), _ptr(buf), buf.numel(),
+    _check(lib.quasar_int8_gemm_s32(_ptr(xq), _ptr(wp), M, N, K, _ptr(acc), _ptr(buf), buf.numel(),
                                     _stream(stream)), "int8_gemm_s32")
     return acc
 
