@@ -187,6 +187,32 @@ quasar_status_t quasar_int8_gemm_s32(const int8_t* Xq, const int8_t* Wp,
                                      void* workspace, size_t ws_bytes,
                                      quasar_stream_t stream);
 
+/* The same W8A8 linear for callers that cannot hand the library a
+ * workspace: code hosted inside another runtime or plugin interface that
+ * owns every device buffer and offers no scratch, or serving loops that
+ * forbid device allocation once they are running.  (This entry point is a
+ * library convenience; the paper has no counterpart.)  It allocates nothing:
+ * its split-K scratch is one fixed array of QUASAR_NOALLOC_SCRATCH_BYTES in
+ * the library's device image, which every GPU that loads the library keeps
+ * until the process exits.
+ *   - Arguments, outputs and results are those of quasar_w8a8_linear.
+ *   - Returns QUASAR_ERR_WORKSPACE when quasar_w8a8_linear_workspace_size(M,
+ *     N, K) exceeds QUASAR_NOALLOC_SCRATCH_BYTES (4 MiB: e.g. M x N up to
+ *     about one million output elements).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Each call clears the part of the array it uses on `stream` before the
+ *     kernel runs, so it does not depend on what a previous call left.
+ *   - All calls in the process share the one array: calls that may overlap
+ *     on the GPU (different streams, or different host threads) race and
+ *     must be serialized by the caller. */
+#define QUASAR_NOALLOC_SCRATCH_BYTES (4u << 20)
+quasar_status_t quasar_w8a8_linear_noalloc(const int8_t* Xq, const float* sa,
+                                           const int8_t* Wp, const float* sw,
+                                           int M, int N, int K,
+                                           void* Y_bf16, int ldy,
+                                           quasar_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * A5  Verification: accepted prefix length per sequence.
  *

@@ -1,0 +1,86 @@
+"""GPU test of quasar_w8a8_linear_noalloc, the W8A8 linear for callers that
+cannot give the library a workspace (for example code hosted in another
+runtime's plugin interface that owns all device memory, or serving loops that
+may not allocate once running).  Its split-K scratch is a fixed array inside
+the library, so the test checks, through the C ABI, that two calls in a row
+give the same BF16 output as the workspace-taking quasar_w8a8_linear (within
+the 1-ulp BF16 tolerance the other parity tests use), and that sizes beyond
+the fixed array are refused.
+
+Kept in a file of its own that pytest collects last; it needs no state from
+the other tests and also runs alone in a fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from tests.gpu_util import bf16_ulp_distance, dev_bf16, host_bf16_bits  # noqa: E402
+from w8a8_quantized_speculative_gb300 import quasar as q  # noqa: E402
+from w8a8_quantized_speculative_gb300 import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+BF16_ULP_TOL = 1
+QUASAR_ERR_WORKSPACE = 3
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _prepared(case):
+    x, w, xc = case.x(), case.w(), case.x_cal()
+    smooth = q.calibrate_smooth(dev_bf16(xc), dev_bf16(w))
+    wp, sw = q.pack_weights(dev_bf16(w), smooth)
+    xq, sa = q.smooth_quant_act(dev_bf16(x), smooth)
+    return xq, sa, wp, sw
+
+
+def _noalloc(xq, sa, wp, sw, y):
+    M, K = xq.shape
+    N = sw.numel()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return q.lib.quasar_w8a8_linear_noalloc(_p(xq), _p(sa), _p(wp), _p(sw), M, N, K, _p(y), y.stride(0), stream)
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    # two calls in a row on different layers (qkv then o_proj, M = 20)
+    for case in synth.attention_cases():
+        xq, sa, wp, sw = _prepared(case)
+        want = q.w8a8_linear(xq, sa, wp, sw, workspace=q.Workspace())
+        got = torch.full_like(want, float("nan"))
+        assert _noalloc(xq, sa, wp, sw, got) == 0
+        torch.cuda.synchronize()
+        d = bf16_ulp_distance(host_bf16_bits(got), host_bf16_bits(want))
+        assert d.max() <= BF16_ULP_TOL, (case.name, int(d.max()))
+    st, site = q.get_device_error()
+    assert st == 0, site
+
+
+def test_noalloc_repeated_call_same_layer():
+    case = synth.small_case()
+    xq, sa, wp, sw = _prepared(case)
+    want = host_bf16_bits(q.w8a8_linear(xq, sa, wp, sw, workspace=q.Workspace()))
+    for _ in range(2):
+        got = torch.zeros((case.M, case.N), dtype=torch.bfloat16, device="cuda")
+        assert _noalloc(xq, sa, wp, sw, got) == 0
+        torch.cuda.synchronize()
+        assert bf16_ulp_distance(host_bf16_bits(got), want).max() <= BF16_ULP_TOL
+
+
+def test_noalloc_rejects_sizes_beyond_the_fixed_scratch():
+    M, N, K = 256, 24576, 4096          # needs ~25 MB of split-K scratch
+    assert q.lib.quasar_w8a8_linear_workspace_size(M, N, K) > (4 << 20)
+    xq = torch.zeros((M, K), dtype=torch.int8, device="cuda")
+    sa = torch.zeros(M, device="cuda")
+    wp = torch.zeros(16, dtype=torch.int8, device="cuda")   # never read: the call is refused first
+    sw = torch.zeros(N, device="cuda")
+    y = torch.zeros((1, N), dtype=torch.bfloat16, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = q.lib.quasar_w8a8_linear_noalloc(_p(xq), _p(sa), _p(wp), _p(sw), M, N, K, _p(y), N, stream)
+    assert rc == QUASAR_ERR_WORKSPACE

@@ -656,10 +656,52 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   return cuda_status(e);
 }
 
+// ---------------------------------------------------------- no-allocation path
+//
+// For callers that cannot pass a workspace.  The split-K scratch lives in a
+// fixed array of this file's device image; host code only ever handles its
+// device address, looked up once per device (the symbol itself is a host-side
+// stand-in and must never be passed to a kernel).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[QUASAR_NOALLOC_SCRATCH_BYTES];
+
+static void* noalloc_scratch_address() {
+  static void* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+quasar_status_t run_noalloc(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N,
+                            int K, void* Y, int ldy, cudaStream_t stream) {
+  if (M < 0 || N <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
+  if (M == 0) return QUASAR_OK;
+  const size_t need = workspace_size(M, N, K);
+  if (need > QUASAR_NOALLOC_SCRATCH_BYTES) return QUASAR_ERR_WORKSPACE;
+  if (!Y) return QUASAR_ERR_INVALID_ARG;
+  void* scratch = noalloc_scratch_address();
+  if (!scratch) return QUASAR_ERR_CUDA;
+  // Start from zeroed counters and sums whatever an earlier call left.
+  const cudaError_t e = cudaMemsetAsync(scratch, 0, need, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  return run(Xq, sa, Wp, sw, M, N, K, Y, ldy, nullptr, scratch, QUASAR_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 }  // namespace gemm
 }  // namespace quasar
 
 extern "C" {
+
+quasar_status_t quasar_w8a8_linear_noalloc(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw,
+                                           int M, int N, int K, void* Y_bf16, int ldy, quasar_stream_t stream) {
+  return quasar::gemm::run_noalloc(Xq, sa, Wp, sw, M, N, K, Y_bf16, ldy, reinterpret_cast<cudaStream_t>(stream));
+}
 
 size_t quasar_w8a8_linear_workspace_size(int M, int N, int K) { return quasar::gemm::workspace_size(M, N, K); }
 

@@ -41,6 +41,7 @@ _SIGS = {
     "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_int8_gemm_s32": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
+    "quasar_w8a8_linear_noalloc": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p]),
     "quasar_verify_accept_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_verify_accept": (_i, [_p, _i, _p, _i, _i, _i, _f, _p, _p, _p, _p, _sz, _p]),
 }
