@@ -211,19 +211,22 @@ struct PendingRun {
   int R = -1;
   bool flush = false;
   int t = 0, kb_first = 0, kb_last = 0;
+  int s2 = 0;        // converted stage holding the run's last blocks
+  uint32_t ph2 = 0;  // parity of that stage's MMA-completion phase
 };
 
 // Drain run `pr.R` from TMEM into the int32 registers; if it closes a
 // segment, publish / finish the segment (see the file comment) and clear the
 // registers.  Returns false if a bounded wait ran out.
 template <int NT>
-QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4], uint64_t* accfull,
+QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4], uint64_t* empty2,
                                      uint64_t* accempty, uint32_t tmem_lane, int h, volatile int* abort_flag,
                                      const Params& p, int warp, int lane, int row, int KB, int m_tiles) {
   constexpr int TOK = NT / 4;
   const int a = pr.R & 1;
-  const bool okf =
-      mbar_wait(&accfull[a], (uint32_t)(pr.R >> 1) & 1, abort_flag, p.err, SITE_GEMM_ACCFULL, p.limit_ns);
+  // The commit that frees the run's last stage tracks every MMA issued
+  // before it, i.e. the whole run: its completion means the sums are final.
+  const bool okf = mbar_wait(&empty2[pr.s2], pr.ph2, abort_flag, p.err, SITE_GEMM_ACCFULL, p.limit_ns);
   if (!__all_sync(0xffffffffu, okf)) return false;
   tc_fence_after();
   drain_acc<NT>(tmem_lane + (uint32_t)(a * NT + h * TOK), acc);
@@ -299,8 +302,7 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   uint64_t* empty1 = full1 + C::S1;           // [S1] converters -> producer
   uint64_t* full2 = empty1 + C::S1;           // [S2] converters -> MMA
   uint64_t* empty2 = full2 + C::S2;           // [S2] MMA -> converters
-  uint64_t* accfull = empty2 + C::S2;         // [2]  MMA -> drain
-  uint64_t* accempty = accfull + 2;           // [2]  drain -> MMA
+  uint64_t* accempty = empty2 + C::S2;        // [2]  drain -> MMA
   uint64_t* mma_done = accempty + 2;          // [1]  final MMA drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -314,7 +316,7 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::S1; ++s) { mbar_init(&full1[s], 1); mbar_init(&empty1[s], CONV_WARPS); }
     for (int s = 0; s < C::S2; ++s) { mbar_init(&full2[s], CONV_WARPS); mbar_init(&empty2[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], 1); mbar_init(&accempty[a], CONV_WARPS); }
+    for (int a = 0; a < 2; ++a) mbar_init(&accempty[a], CONV_WARPS);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -415,7 +417,6 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
             mma_burst4<NT, 4>(d_tmem, a1, b1, 1u);
           }
           tc_commit(&empty2[rg.s]);
-          if (w.run_last(KB)) tc_commit(&accfull[R & 1]);
         }
         __syncwarp();
       }
@@ -504,7 +505,7 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       // Drain the run finished one stage ago (its MMAs have had a whole
       // stage to complete), then remember this stage's run if it ends here.
       if (pend.R >= 0) {
-        if (!finish_run<NT>(pend, acc, accfull, accempty, tmem + lane_off, h, abort_flag, p, warp, lane, row, KB,
+        if (!finish_run<NT>(pend, acc, empty2, accempty, tmem + lane_off, h, abort_flag, p, warp, lane, row, KB,
                             m_tiles))
           break;
         pend.R = -1;
@@ -515,10 +516,12 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         pend.t = w.t;
         pend.kb_first = w.kb_first;
         pend.kb_last = w.kb + w.g - 1;
+        pend.s2 = r2.s;
+        pend.ph2 = r2.ph;
       }
     }
     if (pend.R >= 0)
-      finish_run<NT>(pend, acc, accfull, accempty, tmem + lane_off, h, abort_flag, p, warp, lane, row, KB, m_tiles);
+      finish_run<NT>(pend, acc, empty2, accempty, tmem + lane_off, h, abort_flag, p, warp, lane, row, KB, m_tiles);
   }
 
   tc_fence_before();
