@@ -133,6 +133,43 @@ def test_int8_gemm_adversarial_extremes(K):
     assert acc[0, 0] == 127 * 127 * K
 
 
+# M <= 32 runs on the register-path kernel: every token-tile width (8, 16,
+# 24, 32 columns), ragged M / N / K, and a CTA range that covers several
+# tiles and both ends of the stage ring.
+SKINNY_SHAPES = [(1, 8, 16), (2, 1000, 4112), (7, 136, 1040), (9, 512, 256), (16, 4096, 4096),
+                 (23, 264, 2064), (24, 6144, 4096), (31, 8, 12288), (32, 1152, 2048)]
+
+
+@pytest.mark.parametrize("M,N,K", SKINNY_SHAPES)
+def test_int8_gemm_skinny_bit_exact(M, N, K):
+    rng = np.random.default_rng(M * 104729 + N * 17 + K)
+    xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    wq = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    ws = q.Workspace()
+    acc = q.int8_gemm_s32(dev(xq), q.tile_weights(dev(wq)), N, workspace=ws).cpu().numpy()
+    assert np.array_equal(acc.astype(np.int64), orc.int_gemm(xq, wq))
+    check_ws_zero(ws)
+
+
+@pytest.mark.parametrize("M", [1, 32])
+def test_int8_gemm_long_segments_at_exactness_limit(M):
+    """N = 8192, K = 16384: each CTA streams ~54 blocks of one tile, so its
+    fp32 runs end at the 32-block limit inside a segment.  All products are
+    +-127^2, so every run's partial sums sit at the largest value they can
+    take."""
+    N, K = 8192, 16384
+    xq = np.full((M, K), 127, np.int8)
+    xq[1::2] = -127
+    if M > 2:
+        xq[2, ::2] = -127
+    wq = np.full((N, K), 127, np.int8)
+    wq[3::4] = -127
+    wq[5, 1::3] = -127
+    acc = q.int8_gemm_s32(dev(xq), q.tile_weights(dev(wq)), N).cpu().numpy()
+    assert np.array_equal(acc.astype(np.int64), orc.int_gemm(xq, wq))
+    assert acc[0, 0] == 127 * 127 * K
+
+
 def test_int8_gemm_deterministic_and_reusable_workspace():
     rng = np.random.default_rng(3)
     xq = dev(rng.integers(-127, 128, size=(20, 4096)).astype(np.int8))

@@ -7,6 +7,7 @@
 // unwinds without trapping.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -26,6 +27,11 @@ unsigned long long wait_limit_ns();
 int sm_count();                             // SMs of the current device (cached)
 quasar_status_t cuda_status(cudaError_t e); // maps a CUDA error to a status
 
+// 2-D tensor map over a row-major uint8 matrix [outer][inner] (row stride =
+// inner bytes, a multiple of 16), 128B-swizzled boxes of box_outer rows x
+// box_inner bytes; out-of-range elements read as zero.
+bool encode_2d_u8(CUtensorMap* map, const void* base, int inner, int outer, int box_inner, int box_outer);
+
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Error site codes recorded in the device error word (low 16 bits = site,
@@ -38,6 +44,9 @@ enum : unsigned int {
   SITE_GEMM_ACCFULL = 5,
   SITE_GEMM_ACCEMPTY = 6,
   SITE_GEMM_DRAIN = 7,
+  SITE_SKINNY_FULL = 8,
+  SITE_SKINNY_EMPTY = 9,
+  SITE_SKINNY_DRAIN = 10,
 };
 
 // ---------------------------------------------------------------- device side

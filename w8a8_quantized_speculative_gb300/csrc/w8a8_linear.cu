@@ -44,15 +44,19 @@
 //    loads and every global write wait for it (griddepcontrol.wait).
 //  * Warp roles: warps 0-15 convert (and drain / run the epilogue), warp 16
 //    issues the copies, warp 17 allocates TMEM and issues MMAs.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 #include <mutex>
 
 #include "quasar_common.cuh"
 
 namespace quasar {
+namespace skinny {  // w8a8_skinny.cu: the register-path kernel for M <= 32
+bool handles(int M);
+size_t slots_bytes(int M, int N, int K);
+quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
+                    void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream);
+}  // namespace skinny
+
 namespace gemm {
 
 constexpr int BM = 128;        // weight rows per tile (MMA M)
@@ -534,33 +538,6 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
 // ------------------------------------------------------------------ host side
 
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-static bool encode_2d_u8(CUtensorMap* map, const void* base, int inner, int outer, int box_inner, int box_outer) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  cuuint64_t strides[1] = {(cuuint64_t)inner};
-  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 static int pick_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
 
 struct Shape {
@@ -582,7 +559,10 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 size_t workspace_size(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   Shape s = shape_of(M, N, K);
-  return align256((size_t)s.tiles * CONV_WARPS * 4) + align256((size_t)M * N * 4);
+  // counters, then the int32 split-K sums of this kernel or the partial-sum
+  // slots of the register-path kernel
+  return align256((size_t)s.tiles * CONV_WARPS * 4) +
+         align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K)));
 }
 
 template <int NT>
@@ -623,6 +603,13 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   if (!ws || ws_bytes < need || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
 
   Shape s = shape_of(M, N, K);
+  uint32_t* ws_cnt = reinterpret_cast<uint32_t*>(ws);
+  int32_t* ws_acc = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + align256((size_t)s.tiles * CONV_WARPS * 4));
+  // A few tokens: the register-path kernel (same packed weights, same
+  // workspace layout, fewer counters per tile).
+  if (skinny::handles(M)) return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream);
+
+
   CUtensorMap tx;
   if (!encode_2d_u8(&tx, Xq, K, M, BK, s.NT)) return QUASAR_ERR_CUDA;
 
@@ -640,8 +627,8 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   p.Y = reinterpret_cast<__nv_bfloat16*>(Y);
   p.ldy = ldy;
   p.acc_out = acc_out;
-  p.ws_cnt = reinterpret_cast<uint32_t*>(ws);
-  p.ws_acc = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + align256((size_t)s.tiles * CONV_WARPS * 4));
+  p.ws_cnt = ws_cnt;
+  p.ws_acc = ws_acc;
   p.err = device_error_word();
   p.limit_ns = wait_limit_ns();
   if (!p.err) return QUASAR_ERR_CUDA;
