@@ -1,6 +1,5 @@
-// A3 + A4 for a few tokens (the library routes M <= 16 here; the kernel is
-// instantiated for up to 32): the W8A8 verify linear on the register tensor
-// path.
+// A3 + A4 for a few tokens (M <= 16): the W8A8 verify linear on the
+// register tensor path.
 //
 //   acc[m][n] = sum_k Xq[m][k] * Wq[n][k]        exact integer
 //   Y[m][n]   = bf16_rne((float(acc) * sa[m]) * sw[n])
@@ -31,12 +30,19 @@
 // eight times; the four K owners of a row tile are summed through shared
 // memory once per accumulation run.
 //
-// Split tiles.  A tile whose K blocks are spread over several CTAs is summed
-// without atomics on the data: each contributor stores its integer partial
-// sums into a slot of its own in the workspace, then counts its K blocks on a
-// per-(tile, warp) counter; the warp that completes the count adds up the
-// slots of every contributor and runs the epilogue.  A CTA publishes its
-// first (head) segment together with its last one, so no CTA stalls twice.
+// Schedules.  A split tile's sums must cross CTAs, and doing that at the end
+// of a launch puts a chain of dependent memory round trips after the last
+// weight byte, so the exchange is kept off the launch's tail:
+//  * few tiles (2 x tiles <= SMs): a thread-block cluster of C CTAs takes one
+//    tile, each CTA a 1/C slice of its K blocks; the slices are summed
+//    through distributed shared memory between two cluster barriers.
+//  * otherwise: the tiles that do not divide evenly over the CTAs are split
+//    stream-K over all CTAs and done first; each CTA then streams whole
+//    tiles.  A split tile is summed without atomics on the data: each
+//    contributor stores its integer partial sums into a slot of its own in
+//    the workspace and counts its K blocks on a per-(tile, warp) counter; the
+//    warp that completes the count adds up the slots of every contributor and
+//    runs the epilogue, while the whole tiles still stream.
 //
 // K order inside an MMA.  ldmatrix hands thread (g, c) of a warp the four
 // consecutive bytes 4c..4c+3 of row g of an 8 x 16-byte matrix.  The MMA's
@@ -90,7 +96,11 @@ struct Params {
   const float* sw;
   int M, N, K;
   int KB;           // K blocks per tile
-  int total;        // n_tiles * KB
+  int mode;         // 0: split tiles stream-K, then whole tiles; 1: cluster per tile
+  int csize;        // mode 1: CTAs per cluster (K slices per tile)
+  int split_tiles;  // mode 0: tiles [0, split_tiles) are split stream-K ...
+  int total1;       //   ... over their split_tiles * KB blocks
+  int whole_per;    // mode 0: whole tiles per CTA, after the split tiles
   __nv_bfloat16* Y;
   int ldy;
   int32_t* acc_out;   // int32 mode when non-null
@@ -100,12 +110,52 @@ struct Params {
   unsigned long long limit_ns;
 };
 
-// One CTA's contiguous range of (tile, K block) items, one block per step.
-// Segments (the CTA's blocks of one tile) and accumulation runs (<=
-// RUN_BLOCKS blocks of a segment) are contiguous.
+// One CTA's work: split items [s0, s1) (item i = K block i % KB of tile
+// i / KB), then whole tiles [w0, w1).
+struct Sched {
+  int s0, s1, w0, w1;
+};
+
+QUASAR_DEVICE_INLINE int range_begin(int c, int total, int grid);
+
+QUASAR_DEVICE_INLINE Sched schedule_of(int c, int grid, int KB, int mode, int csize, int split_tiles, int total1,
+                                       int whole_per) {
+  Sched sc;
+  if (mode == 1) {
+    const int t = c / csize, q = c % csize;
+    sc.s0 = t * KB + (q * KB) / csize;
+    sc.s1 = t * KB + ((q + 1) * KB) / csize;
+    sc.w0 = sc.w1 = 0;
+  } else {
+    sc.s0 = range_begin(c, total1, grid);
+    sc.s1 = range_begin(c + 1, total1, grid);
+    sc.w0 = split_tiles + c * whole_per;
+    sc.w1 = sc.w0 + whole_per;
+  }
+  return sc;
+}
+
+// Walks a schedule one K block per step.  Segments (the CTA's blocks of one
+// tile within a phase) and accumulation runs (<= RUN_BLOCKS blocks of a
+// segment) are contiguous.
 struct Walk {
-  int t, kb, kb_first, left;
-  __device__ Walk(int b0, int b1, int KB) : t(b0 / KB), kb(b0 % KB), kb_first(b0 % KB), left(b1 - b0) {}
+  int t, kb, kb_first, left, left2, w_next, phase;
+  __device__ Walk(const Sched& sc, int KB) {
+    if (sc.s1 > sc.s0) {
+      phase = 1;
+      t = sc.s0 / KB;
+      kb = kb_first = sc.s0 % KB;
+      left = sc.s1 - sc.s0;
+      left2 = (sc.w1 - sc.w0) * KB;
+    } else {
+      phase = 2;
+      t = sc.w0;
+      kb = kb_first = 0;
+      left = (sc.w1 - sc.w0) * KB;
+      left2 = 0;
+    }
+    w_next = sc.w0;
+  }
   __device__ bool more() const { return left > 0; }
   __device__ bool seg_last(int KB) const { return left == 1 || kb + 1 == KB; }
   __device__ bool run_last(int KB) const { return seg_last(KB) || ((kb - kb_first + 1) % RUN_BLOCKS) == 0; }
@@ -115,6 +165,13 @@ struct Walk {
       kb = 0;
       kb_first = 0;
       ++t;
+    }
+    if (left == 0 && left2 > 0) {   // enter the whole tiles
+      phase = 2;
+      t = w_next;
+      kb = kb_first = 0;
+      left = left2;
+      left2 = 0;
     }
   }
 };
@@ -141,6 +198,24 @@ QUASAR_DEVICE_INLINE void ldsm_x4(uint32_t addr, uint32_t& d0, uint32_t& d1, uin
 QUASAR_DEVICE_INLINE uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Cluster-wide barrier of every thread of every CTA in the cluster (release
+// on arrive, acquire on wait); warp-converged callers only.
+QUASAR_DEVICE_INLINE void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// int4 at the same shared-memory offset in cluster CTA `rank`.
+QUASAR_DEVICE_INLINE int4 ld_dsmem_int4(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  int4 v;
+  asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(remote)
+               : "memory");
   return v;
 }
 
@@ -201,7 +276,7 @@ QUASAR_DEVICE_INLINE void epilogue(const Params& p, const int4 (&v4)[NT8], int t
 // 1); every one is partial.
 template <int NT8>
 QUASAR_DEVICE_INLINE int4* slot_ptr(const Params& p, int cc, int t, int mt, int lane, int grid) {
-  const int first_t = range_begin(cc, p.total, grid) / p.KB;
+  const int first_t = range_begin(cc, p.total1, grid) / p.KB;
   return p.slots + ((size_t)cc * 2 + (first_t == t ? 0 : 1)) * Cfg<NT8>::SLOT + (size_t)mt * NT8 * 32 + lane;
 }
 
@@ -209,8 +284,8 @@ QUASAR_DEVICE_INLINE int4* slot_ptr(const Params& p, int cc, int t, int mt, int 
 // (loads only: four contributors in flight at a time).
 template <int NT8>
 QUASAR_DEVICE_INLINE void load_slots(const Params& p, int t, int mt, int lane, int grid, int4 (&s)[NT8]) {
-  const int c_lo = cta_of_block(t * p.KB, p.total, grid);
-  const int c_hi = cta_of_block((t + 1) * p.KB - 1, p.total, grid);
+  const int c_lo = cta_of_block(t * p.KB, p.total1, grid);
+  const int c_hi = cta_of_block((t + 1) * p.KB - 1, p.total1, grid);
 #pragma unroll
   for (int ni = 0; ni < NT8; ++ni) s[ni] = make_int4(0, 0, 0, 0);
   for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
@@ -237,8 +312,8 @@ QUASAR_DEVICE_INLINE void load_slots(const Params& p, int t, int mt, int lane, i
 // and zeroed after the read, so the workspace is left as it was found.
 template <int NT8>
 QUASAR_DEVICE_INLINE void zero_slots(const Params& p, int t, int mt, int lane, int grid) {
-  const int c_lo = cta_of_block(t * p.KB, p.total, grid);
-  const int c_hi = cta_of_block((t + 1) * p.KB - 1, p.total, grid);
+  const int c_lo = cta_of_block(t * p.KB, p.total1, grid);
+  const int c_hi = cta_of_block((t + 1) * p.KB - 1, p.total1, grid);
   for (int cc = c_lo; cc <= c_hi; ++cc) {
     int4* slot = slot_ptr<NT8>(p, cc, t, mt, lane, grid);
 #pragma unroll
@@ -313,9 +388,8 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   __syncthreads();
 
   const int grid = (int)gridDim.x;
-  const int b0 = range_begin((int)blockIdx.x, p.total, grid);
-  const int b1 = range_begin((int)blockIdx.x + 1, p.total, grid);
   const int KB = p.KB;
+  const Sched sc = schedule_of((int)blockIdx.x, grid, KB, p.mode, p.csize, p.split_tiles, p.total1, p.whole_per);
 
   if (warp == PRODUCER_WARP) {
     if (lane == 0) {
@@ -324,7 +398,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       // Weights do not depend on the previous kernel: fill every stage first.
       int pre = 0;
       {
-        Walk w(b0, b1, KB);
+        Walk w(sc, KB);
         for (; pre < C::S && w.more(); ++pre, w.next(KB)) {
           mbar_arrive_expect_tx(&full[pre], (uint32_t)C::STAGE);
           bulk_load(stages + pre * C::STAGE, p.wp + ((size_t)w.t * KB + w.kb) * BLOCK_BYTES, BLOCK_BYTES,
@@ -332,7 +406,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         }
       }
       pdl_wait();  // token codes come from the previous kernel
-      Walk w(b0, b1, KB);
+      Walk w(sc, KB);
       Ring<C::S> rg;
       int issued = 0;
       for (; w.more(); w.next(KB), rg.next(), ++issued) {
@@ -351,6 +425,11 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         mbar_wait(&full[s], (uint32_t)(last / C::S) & 1u, &dummy, p.err, SITE_SKINNY_DRAIN, p.limit_ns);
       }
     }
+    __syncwarp();
+    if (p.mode == 1) {   // the consumers' two cluster barriers
+      cluster_sync_all();
+      cluster_sync_all();
+    }
     return;
   }
 
@@ -360,10 +439,12 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   const int g = lane >> 2, c = lane & 3;
   const int mt_f = warp;            // the row tile this warp finalizes
   pdl_wait();                       // scales and workspace belong to the previous kernel until here
-  const int t_first = b0 / KB, t_last = (b1 - 1) / KB;
+  const int t_first = (sc.s1 > sc.s0) ? sc.s0 / KB : sc.w0;
+  const int t_last = (sc.w1 > sc.w0) ? sc.w1 - 1 : (sc.s1 - 1) / KB;
+  const int t_first1 = sc.s0 / KB;  // first tile of the split range (its slot 0)
   // Stage the dequantization scales the epilogues will need: every token's
-  // sa, and sw of the first and last tile of this CTA's range (read after
-  // the first run-end barrier, which orders these stores).
+  // sa, and sw of the first and last tile of this CTA (read after the first
+  // run-end barrier, which orders these stores).
   if (!p.acc_out) {
     for (int i = threadIdx.x; i < 32 + 2 * BM; i += CWARPS * 32) {
       if (i < 32) {
@@ -398,14 +479,14 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   const uint32_t stages_u32 = smem_u32(stages);
 
   bool bad = false;
-  // Partial segments (at most two: the range's first and last) wait to be
-  // counted until the end, so that one fence covers both.
+  // Partial segments of the split range (at most two: its first and last)
+  // are counted together when the range ends, so that one fence covers both.
   int seg_ta = -1, seg_na = 0, seg_tb = -1, seg_nb = 0;
-  // sw of tile t: staged for the range's first and last tile.
+  // sw of tile t: staged for the CTA's first and last tile.
   auto sw_of = [&](int t) -> const float* {
     return t == t_first ? sw_s : t == t_last ? sw_s + BM : p.sw + (size_t)t * BM;
   };
-  Walk w(b0, b1, KB);
+  Walk w(sc, KB);
   Ring<C::S> r;
   for (; w.more(); w.next(KB), r.next()) {
     if (!bad) {
@@ -473,16 +554,17 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     // ---- end of this CTA's segment of tile t.
     const int t = w.t;
     const int nb = w.kb - w.kb_first + 1;
+    if (p.mode == 1) break;   // the only segment: summed across the cluster below
     if (nb == KB) {
       int4 v[NT8];
 #pragma unroll
       for (int ni = 0; ni < NT8; ++ni) v[ni] = share[ni * 32];
       epilogue<NT8>(p, v, t, mt_f, lane, sa_s, sw_of(t));   // the whole tile
     } else {
-      // Partial tile: store the share into this CTA's slot for the segment
-      // (0 = its first segment, 1 = its last).
-      int4* slot = p.slots + ((size_t)blockIdx.x * 2 + (t == t_first ? 0 : 1)) * C::SLOT + (size_t)mt_f * NT8 * 32 +
-                   lane;
+      // Partial segment of the split range: store the share into this CTA's
+      // slot for it (0 = the range's first segment, 1 = its last).
+      int4* slot = p.slots + ((size_t)blockIdx.x * 2 + (t == t_first1 ? 0 : 1)) * C::SLOT +
+                   (size_t)mt_f * NT8 * 32 + lane;
 #pragma unroll
       for (int ni = 0; ni < NT8; ++ni) slot[ni * 32] = share[ni * 32];
       if (seg_ta < 0) {
@@ -493,44 +575,142 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         seg_nb = nb;
       }
     }
+    if (w.phase == 1 && w.left == 1 && seg_ta >= 0) {
+      // The split range ends here: publish its partial segments now, while
+      // the whole tiles (if any) still stream.
+      count_segments<NT8>(p, seg_ta, seg_na, seg_tb, seg_nb, mt_f, lane, grid, sa_s, sw_of(seg_ta),
+                          seg_tb >= 0 ? sw_of(seg_tb) : sw_s);
+      seg_ta = -1;
+    }
 #pragma unroll
     for (int ni = 0; ni < NT8; ++ni) share[ni * 32] = make_int4(0, 0, 0, 0);
   }
-  if (seg_ta >= 0 && !bad)
-    count_segments<NT8>(p, seg_ta, seg_na, seg_tb, seg_nb, mt_f, lane, grid, sa_s, sw_of(seg_ta),
-                        seg_tb >= 0 ? sw_of(seg_tb) : sw_s);
+
+  if (p.mode == 1) {
+    // Cluster split: every CTA of the cluster holds the sums of one K slice of
+    // tile t in `fin`.  After the barrier each row tile is finished by one
+    // CTA (row tile mt in the CTA of rank mt % C), reading the other slices
+    // through distributed shared memory; the second barrier keeps every CTA's
+    // shared memory alive until those reads are done.
+    __syncwarp();
+    cluster_sync_all();
+    const int csz = p.csize;
+    const int rank = (int)blockIdx.x % csz;
+    if (!bad && (mt_f % csz) == rank) {
+      int4 v[NT8];
+#pragma unroll
+      for (int ni = 0; ni < NT8; ++ni) v[ni] = share[ni * 32];
+      for (int q = 0; q < csz; ++q) {
+        if (q == rank) continue;
+#pragma unroll
+        for (int ni = 0; ni < NT8; ++ni) {
+          const int4 u = ld_dsmem_int4(share + ni * 32, (uint32_t)q);
+          v[ni].x += u.x;
+          v[ni].y += u.y;
+          v[ni].z += u.z;
+          v[ni].w += u.w;
+        }
+      }
+      epilogue<NT8>(p, v, t_first, mt_f, lane, sa_s, sw_s);
+    }
+    __syncwarp();
+    cluster_sync_all();
+  }
 }
 
 // ------------------------------------------------------------------ host side
 
 template <int NT8>
-static cudaError_t launch(const CUtensorMap& tx, const Params& p, int grid, cudaStream_t stream) {
+static cudaError_t configure(int dev) {
   static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(w8a8_skinny_kernel<NT8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<NT8>::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
+  return cudaSuccess;
+}
+
+template <int NT8>
+static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = Cfg<NT8>::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)csize;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = csize > 1 ? 2 : 1;
+  return cfg;
+}
+
+// Clusters of `csize` CTAs of this kernel that the device keeps resident at
+// once (0 if unknown); cached per device and cluster size.
+template <int NT8>
+static int resident_clusters(int dev, int csize) {
+  static int cache[64][9];
+  static bool init[64][9] = {};
+  if (dev < 0 || dev >= 64 || csize < 2 || csize > 8) return 0;
+  if (!init[dev][csize]) {
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = config_of<NT8>(csize * 16, csize, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, w8a8_skinny_kernel<NT8>, &cfg) != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();
+    }
+    cache[dev][csize] = n;
+    init[dev][csize] = true;
+  }
+  return cache[dev][csize];
+}
+
+template <int NT8>
+static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t e = configure<NT8>(dev);
+  if (e != cudaSuccess) return e;
+  const int n_tiles = (p.N + BM - 1) / BM;
+  // Few tiles: one cluster per tile, as many K slices as fit in one wave.
+  int csize = std::min(std::min(8, sms / n_tiles), p.KB);
+  while (csize >= 2 && resident_clusters<NT8>(dev, csize) < n_tiles) --csize;
+  int grid;
+  if (csize >= 2) {
+    p.mode = 1;
+    p.csize = csize;
+    p.split_tiles = 0;
+    p.total1 = 0;
+    p.whole_per = 0;
+    grid = n_tiles * csize;
+  } else {
+    p.mode = 0;
+    p.csize = 1;
+    grid = std::min(sms, MAX_CTAS);
+    p.whole_per = n_tiles / grid;
+    p.split_tiles = n_tiles - p.whole_per * grid;
+    p.total1 = p.split_tiles * p.KB;
+    if (p.whole_per == 0) grid = std::min(grid, p.total1);
+    if ((unsigned long long)(p.total1 + 1) * (unsigned long long)(grid + 1) >= (1ull << 32))
+      return cudaErrorInvalidValue;
+  }
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = config_of<NT8>(grid, p.csize, stream, attr);
   return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8>, tx, p);
 }
 
 bool handles(int M) { return M >= 1 && M <= 16; }
 
-// Partial-sum slots this kernel needs after the counters: two per CTA.  Like
-// the counters they are zero between calls (each is zeroed by its reader).
+// Partial-sum slots this kernel may need after the counters: two per CTA.
+// Like the counters they are zero between calls (each is zeroed by its
+// reader).
 size_t slots_bytes(int M, int N, int K) {
   if (!handles(M) || N <= 0 || K <= 0) return 0;
   const long long total = (long long)((N + BM - 1) / BM) * ((K + BK - 1) / BK);
@@ -553,7 +733,6 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   p.N = N;
   p.K = K;
   p.KB = (K + BK - 1) / BK;
-  p.total = ((N + BM - 1) / BM) * p.KB;
   p.Y = reinterpret_cast<__nv_bfloat16*>(Y);
   p.ldy = ldy;
   p.acc_out = acc_out;
@@ -564,15 +743,12 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   if (!p.err) return QUASAR_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return QUASAR_ERR_CUDA;
-  const int grid = std::min(std::min(p.total, sms), MAX_CTAS);
-  if ((unsigned long long)(p.total + 1) * (unsigned long long)(grid + 1) >= (1ull << 32)) return QUASAR_ERR_UNSUPPORTED;
   cudaError_t e;
   switch (nt8) {
-    case 1: e = launch<1>(tx, p, grid, stream); break;
-    case 2: e = launch<2>(tx, p, grid, stream); break;
-    case 3: e = launch<3>(tx, p, grid, stream); break;
-    default: e = launch<4>(tx, p, grid, stream); break;
+    case 1: e = launch<1>(tx, p, sms, stream); break;
+    default: e = launch<2>(tx, p, sms, stream); break;   // handles() keeps M <= 16
   }
+  if (e == cudaErrorInvalidValue) return QUASAR_ERR_UNSUPPORTED;
   return cuda_status(e);
 }
 
