@@ -41,8 +41,12 @@ from w8a8_quantized_speculative_gb300 import synth  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-GEMM_SRC = os.path.join(ROOT, "w8a8_quantized_speculative_gb300", "csrc", "w8a8_linear.cu")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "w8a8_linear_qkv_m20.json")
+# The library runs M <= 24 on the register-path kernel (w8a8_skinny.cu) and
+# larger M on the tcgen05 kernel (w8a8_linear.cu, which also dispatches).
+GEMM_SRCS = [os.path.join(ROOT, "w8a8_quantized_speculative_gb300", "csrc", f)
+             for f in ("w8a8_linear.cu", "w8a8_skinny.cu")]
+SKINNY_MAX_M = 24
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "w8a8_skinny_qkv_m20.json")
 WORKLOAD = ("Qwen3-8B attention projections, W8A8: fused qkv 4096->6144 and o_proj 4096->4096, "
             "M=20 tokens (4 sequences x (4 drafts + 1)), each linear preceded by smooth+quantize")
 
@@ -87,8 +91,11 @@ def load_peaks():
 
 
 def gemm_source_hash() -> str:
-    with open(GEMM_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in GEMM_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic():
@@ -350,7 +357,9 @@ def main_gpu(args):
     achieved = alg / (gemm_us * 1e-6) / 1e9
     traffic = profiled_traffic()
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": traffic, "kernel": f"w8a8_linear_kernel<32> qkv M={c.M} N={c.N} K={c.K}",
+                "traffic": traffic,
+                "kernel": (f"{'w8a8_skinny_kernel' if c.M <= SKINNY_MAX_M else 'w8a8_linear_kernel'} "
+                           f"qkv M={c.M} N={c.N} K={c.K}"),
                 "launch_us": gemm_us, "algorithmic_bytes_per_launch": alg,
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s"}
 

@@ -53,13 +53,12 @@ def test_workspace_sizes(lib):
     lib.quasar_verify_accept_workspace_size.restype = ctypes.c_size_t
     lib.quasar_calibrate_workspace_size.restype = ctypes.c_size_t
     ws = lib.quasar_w8a8_linear_workspace_size
-    # M <= 16 (register-path kernel): counters for 48 tiles x 16 warps (3072 B)
-    # + two partial-sum slots (128 rows x 16 token columns of int32) for each
-    # of at most 160 CTAs
-    assert ws(16, 6144, 4096) == 3072 + 2 * 160 * 128 * 16 * 4
-    assert ws(8, 512, 256) == 256 + 2 * 8 * 128 * 8 * 4          # 8 work items -> 8 CTAs
-    # M > 16 (tcgen05 kernel): counters for the tiles x 16 warps + int32 sums M x N
-    assert ws(20, 6144, 4096) == 3072 + 20 * 6144 * 4
+    # M <= 24 (register-path kernel): counters for 48 tiles x 16 (3072 B) + two
+    # partial-sum slots (64 rows x 24 token columns of int32) for each of at
+    # most 320 CTAs (two per SM)
+    assert ws(20, 6144, 4096) == 3072 + 2 * 320 * 64 * 24 * 4
+    assert ws(8, 512, 256) == 256 + 2 * 16 * 64 * 8 * 4          # 16 work items -> 16 CTAs
+    # M > 24 (tcgen05 kernel): counters for the tiles x 16 warps + int32 sums M x N
     assert ws(64, 4096, 4096) == 2048 + 64 * 4096 * 4
     lib.quasar_packed_weight_bytes.restype = ctypes.c_size_t
     assert lib.quasar_packed_weight_bytes(6144, 4096) == 6144 * 4096

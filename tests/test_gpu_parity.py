@@ -133,12 +133,13 @@ def test_int8_gemm_adversarial_extremes(K):
     assert acc[0, 0] == 127 * 127 * K
 
 
-# M <= 16 runs on the register-path kernel, both token-tile widths, ragged M /
-# N / K and each schedule: one cluster per tile (few tiles, cluster sizes 2-8),
-# split tiles stream-K only (96 tiles), whole tiles only (152 tiles), and
-# split-then-whole (192 tiles).  M > 16 shapes check the tcgen05 kernel.
+# M <= 24 runs on the register-path kernel (64-row units, two CTAs per SM):
+# every token-tile width, ragged M / N / K and each schedule: one cluster per
+# unit (few units, cluster sizes 2-8), split units stream-K only (<= 303
+# units), whole units only (304 units), and split-then-whole (384 units).
+# Larger M checks the tcgen05 kernel.
 SKINNY_SHAPES = [(1, 8, 16), (2, 1000, 4112), (7, 136, 1040), (9, 512, 256), (16, 4096, 4096),
-                 (3, 12288, 256), (5, 19456, 512), (12, 24576, 1024),
+                 (3, 12288, 256), (5, 19456, 512), (12, 24576, 1024), (20, 6144, 4096),
                  (23, 264, 2064), (24, 6144, 4096), (31, 8, 12288), (32, 1152, 2048)]
 
 

@@ -1,4 +1,4 @@
-// A3 + A4 for a few tokens (M <= 16): the W8A8 verify linear on the
+// A3 + A4 for a few tokens (M <= 24): the W8A8 verify linear on the
 // register tensor path.
 //
 //   acc[m][n] = sum_k Xq[m][k] * Wq[n][k]        exact integer
@@ -16,33 +16,33 @@
 // runs at ~2048 flop/clk/SM on sm_103a and takes its weight operand straight
 // from registers: at M <= 8 it covers 128 weight bytes per cycle, at M = 32
 // still 32, against the ~22 bytes per cycle an SM must stream for HBM-rate.
-// So for M <= 32 the weights go HBM -> shared memory (1-D bulk copies, the
+// So for M <= 32 the weights go HBM -> shared memory (1-D bulk copies of the
 // same packed blocks the tcgen05 kernel reads) -> registers (ldmatrix) ->
 // fp16 (exact) -> mma.sync, with fp32 accumulators that stay exact integers
 // (see RUN_BLOCKS), and the tcgen05 kernel keeps the larger M.
 //
-// Work split.  Persistent grid, one CTA per SM, each CTA streaming an equal
-// contiguous range of (weight tile, 128-K block) items (stream-K).  Inside a
-// block, consumer warp (kq, rg) owns K bytes [32 kq, 32 kq + 32) of weight
-// rows [64 rg, 64 rg + 64): 4 row tiles x 2 K steps x NT/8 token tiles of
-// MMAs.  Owning K rather than rows means each warp widens only its own token
-// columns, so the token operand is converted twice per block instead of
-// eight times; the four K owners of a row tile are summed through shared
-// memory once per accumulation run.
+// Work units.  A unit is 64 weight rows (half of a packed 128-row tile: its
+// blocks are contiguous 8 KB halves of the 16 KB packed blocks) over all of
+// K.  Two CTAs share each SM (~112 KB of shared memory each), so sixteen
+// consumer warps per SM hide each other's latencies.  Inside a CTA,
+// consumer warp (kq, rg) owns K bytes [32 kq, 32 kq + 32) of rows
+// [32 rg, 32 rg + 32) of the unit: 2 row tiles x 2 K steps x NT/8 token
+// tiles of MMAs per block.  The four K owners of a row tile are summed
+// through shared memory once per accumulation run.
 //
-// Schedules.  A split tile's sums must cross CTAs, and doing that at the end
+// Schedules.  A split unit's sums must cross CTAs, and doing that at the end
 // of a launch puts a chain of dependent memory round trips after the last
 // weight byte, so the exchange is kept off the launch's tail:
-//  * few tiles (2 x tiles <= SMs): a thread-block cluster of C CTAs takes one
-//    tile, each CTA a 1/C slice of its K blocks; the slices are summed
-//    through distributed shared memory between two cluster barriers.
-//  * otherwise: the tiles that do not divide evenly over the CTAs are split
+//  * few units: a thread-block cluster of C CTAs takes one unit, each CTA a
+//    1/C slice of its K blocks; the slices are summed through distributed
+//    shared memory between two cluster barriers.
+//  * otherwise: the units that do not divide evenly over the CTAs are split
 //    stream-K over all CTAs and done first; each CTA then streams whole
-//    tiles.  A split tile is summed without atomics on the data: each
+//    units.  A split unit is summed without atomics on the data: each
 //    contributor stores its integer partial sums into a slot of its own in
-//    the workspace and counts its K blocks on a per-(tile, warp) counter; the
+//    the workspace and counts its K blocks on a per-(unit, warp) counter; the
 //    warp that completes the count adds up the slots of every contributor and
-//    runs the epilogue, while the whole tiles still stream.
+//    runs the epilogue, while the whole units still stream.
 //
 // K order inside an MMA.  ldmatrix hands thread (g, c) of a warp the four
 // consecutive bytes 4c..4c+3 of row g of an 8 x 16-byte matrix.  The MMA's
@@ -57,17 +57,21 @@
 namespace quasar {
 namespace skinny {
 
-constexpr int BM = 128;           // weight rows per tile
+constexpr int TILE_ROWS = 128;    // rows of a packed weight tile
+constexpr int UM = 64;            // rows of a work unit (half a tile)
 constexpr int BK = 128;           // K bytes per block
-constexpr int BLOCK_BYTES = BM * BK;
+constexpr int PACKED_BLOCK = TILE_ROWS * BK;   // 16 KB packed block
+constexpr int HALF_BYTES = UM * BK;            // 8 KB: one unit's part of a block
 constexpr int KQ = 4;             // K quarters (32 K = 2 MMA K steps each)
-constexpr int RG = 2;             // row groups (64 rows = 4 row tiles each)
-constexpr int CWARPS = KQ * RG;   // consumer warps; warp w finalizes row tile w
-constexpr int CNT_STRIDE = 16;    // counters per tile in the shared workspace layout
+constexpr int RG = 2;             // row groups (32 rows = 2 row tiles each)
+constexpr int UT = UM / 16;       // row tiles per unit
+constexpr int CWARPS = KQ * RG;   // consumer warps; warp w finalizes (row tile w >> 1, token-tile parity w & 1)
 constexpr int PRODUCER_WARP = CWARPS;
 constexpr int THREADS = 32 * (CWARPS + 1);
 constexpr int RED_BAR = 1;        // named barrier of the consumer warps
-constexpr int MAX_CTAS = 160;     // grid cap; sizes the partial-sum slots
+constexpr int MAX_CTAS = 320;     // grid cap (two CTAs per SM); sizes the partial-sum slots
+constexpr int CNT_PER_UNIT = 8;   // workspace counters per unit (16 per 128-row tile)
+constexpr int SMEM_CAP = 112 * 1024;
 // A warp adds 32 products per block into each fp32 accumulator, each product
 // at most 127^2 = 16129 in magnitude: 32 blocks x 32 x 16129 < 2^24, so over
 // a run of <= 32 blocks every partial sum is an exact integer in fp32.
@@ -76,18 +80,20 @@ constexpr int RUN_BLOCKS = 32;
 template <int NT8>
 struct Cfg {
   static constexpr int NT = 8 * NT8;                        // token columns (padded to 8)
+  static constexpr int NH = (NT8 + 1) / 2;                  // token tiles of one finalizer share
   static constexpr int XB = NT * BK;                        // INT8 token tile of a block
-  static constexpr int STAGE = BLOCK_BYTES + XB;            // multiple of 1024 (swizzle atoms)
-  static constexpr int RED = 8 * KQ * NT8 * 32 * 16;        // fp32 partials: [row tile][kq][token tile][lane]
-  static constexpr int FIN = 8 * NT8 * 32 * 16;             // int32 run sums: [row tile][token tile][lane]
-  static constexpr int SLOT = 8 * NT8 * 32;                 // int4 per partial-sum slot (128 rows x NT)
-  static constexpr int SCL = (32 + 2 * BM) * 4;             // staged scales: sa[32], sw of 2 tiles
-  static constexpr int S_FIT = (225 * 1024 - RED - FIN - SCL - 1024 - 256) / STAGE;
+  static constexpr int STAGE = HALF_BYTES + XB;             // multiple of 1024 (swizzle atoms)
+  static constexpr int RED = UT * KQ * NT8 * 32 * 16;       // fp32 partials: [row tile][kq][token tile][lane]
+  static constexpr int FIN = UT * NT8 * 32 * 16;            // int32 run sums: [row tile][token tile][lane]
+  static constexpr int SLOT = UT * NT8 * 32;                // int4 per partial-sum slot (64 rows x NT)
+  static constexpr int SCL = 1024;                          // staged scales: sa[32], sw of 2 units
+  static constexpr int FIXED = 1024 + RED + FIN + SCL + 256;
+  static constexpr int S_FIT = (SMEM_CAP - FIXED) / STAGE;
   static constexpr int S = S_FIT < 12 ? S_FIT : 12;         // stages in flight
-  static constexpr int SMEM = 1024 + S * STAGE + RED + FIN + SCL + 256;
+  static constexpr int SMEM = FIXED + S * STAGE;
   static_assert(STAGE % 1024 == 0, "stage alignment");
   static_assert(S >= 4, "pipeline depth");
-  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(SMEM <= SMEM_CAP, "two CTAs per SM");
 };
 
 struct Params {
@@ -95,61 +101,69 @@ struct Params {
   const float* sa;
   const float* sw;
   int M, N, K;
-  int KB;           // K blocks per tile
-  int mode;         // 0: split tiles stream-K, then whole tiles; 1: cluster per tile
-  int csize;        // mode 1: CTAs per cluster (K slices per tile)
-  int split_tiles;  // mode 0: tiles [0, split_tiles) are split stream-K ...
-  int total1;       //   ... over their split_tiles * KB blocks
-  int whole_per;    // mode 0: whole tiles per CTA, after the split tiles
+  int KB;           // K blocks per unit
+  int mode;         // 0: split units stream-K, then whole units; 1: cluster per unit
+  int csize;        // mode 1: CTAs per cluster (K slices per unit)
+  int split_units;  // mode 0: units [0, split_units) are split stream-K ...
+  int total1;       //   ... over their split_units * KB blocks
+  int whole_per;    // mode 0: whole units per CTA, after the split units
   __nv_bfloat16* Y;
   int ldy;
   int32_t* acc_out;   // int32 mode when non-null
   int4* slots;        // [grid][2] partial sums, each [row tile][token tile][lane] int4
-  uint32_t* ws_cnt;   // [n_tiles][16] K-block counters per finalizer warp (8 used), zero between calls
+  uint32_t* ws_cnt;   // [units][8] K-block counters per finalizer warp, zero between calls
   unsigned int* err;
   unsigned long long limit_ns;
 };
 
-// One CTA's work: split items [s0, s1) (item i = K block i % KB of tile
-// i / KB), then whole tiles [w0, w1).
+// First block of CTA c, and the CTA whose range holds block b, for the even
+// split of `total` items over `grid` CTAs.  The host guarantees
+// (total + 1) * (grid + 1) < 2^32, so 32-bit unsigned arithmetic is exact
+// (64-bit division is emulated and far slower).
+QUASAR_DEVICE_INLINE int range_begin(int c, int total, int grid) {
+  return (int)(((unsigned)c * (unsigned)total) / (unsigned)grid);
+}
+QUASAR_DEVICE_INLINE int cta_of_block(int b, int total, int grid) {
+  return (int)(((unsigned)(b + 1) * (unsigned)grid + (unsigned)total - 1u) / (unsigned)total) - 1;
+}
+
+// One CTA's work: split items [s0, s1) (item i = K block i % KB of unit
+// i / KB), then whole units [w0, w1).
 struct Sched {
   int s0, s1, w0, w1;
 };
 
-QUASAR_DEVICE_INLINE int range_begin(int c, int total, int grid);
-
-QUASAR_DEVICE_INLINE Sched schedule_of(int c, int grid, int KB, int mode, int csize, int split_tiles, int total1,
-                                       int whole_per) {
+QUASAR_DEVICE_INLINE Sched schedule_of(int c, int grid, const Params& p) {
   Sched sc;
-  if (mode == 1) {
-    const int t = c / csize, q = c % csize;
-    sc.s0 = t * KB + (q * KB) / csize;
-    sc.s1 = t * KB + ((q + 1) * KB) / csize;
+  if (p.mode == 1) {
+    const int u = c / p.csize, q = c % p.csize;
+    sc.s0 = u * p.KB + (q * p.KB) / p.csize;
+    sc.s1 = u * p.KB + ((q + 1) * p.KB) / p.csize;
     sc.w0 = sc.w1 = 0;
   } else {
-    sc.s0 = range_begin(c, total1, grid);
-    sc.s1 = range_begin(c + 1, total1, grid);
-    sc.w0 = split_tiles + c * whole_per;
-    sc.w1 = sc.w0 + whole_per;
+    sc.s0 = range_begin(c, p.total1, grid);
+    sc.s1 = range_begin(c + 1, p.total1, grid);
+    sc.w0 = p.split_units + c * p.whole_per;
+    sc.w1 = sc.w0 + p.whole_per;
   }
   return sc;
 }
 
 // Walks a schedule one K block per step.  Segments (the CTA's blocks of one
-// tile within a phase) and accumulation runs (<= RUN_BLOCKS blocks of a
+// unit within a phase) and accumulation runs (<= RUN_BLOCKS blocks of a
 // segment) are contiguous.
 struct Walk {
-  int t, kb, kb_first, left, left2, w_next, phase;
+  int u, kb, kb_first, left, left2, w_next, phase;
   __device__ Walk(const Sched& sc, int KB) {
     if (sc.s1 > sc.s0) {
       phase = 1;
-      t = sc.s0 / KB;
+      u = sc.s0 / KB;
       kb = kb_first = sc.s0 % KB;
       left = sc.s1 - sc.s0;
       left2 = (sc.w1 - sc.w0) * KB;
     } else {
       phase = 2;
-      t = sc.w0;
+      u = sc.w0;
       kb = kb_first = 0;
       left = (sc.w1 - sc.w0) * KB;
       left2 = 0;
@@ -164,11 +178,11 @@ struct Walk {
     if (++kb == KB) {
       kb = 0;
       kb_first = 0;
-      ++t;
+      ++u;
     }
-    if (left == 0 && left2 > 0) {   // enter the whole tiles
+    if (left == 0 && left2 > 0) {   // enter the whole units
       phase = 2;
-      t = w_next;
+      u = w_next;
       kb = kb_first = 0;
       left = left2;
       left2 = 0;
@@ -187,6 +201,11 @@ struct Ring {
     }
   }
 };
+
+// Global address of unit u's half of packed block (tile u / 2, K block kb).
+QUASAR_DEVICE_INLINE const uint8_t* unit_block(const Params& p, int u, int kb) {
+  return p.wp + ((size_t)(u >> 1) * p.KB + kb) * PACKED_BLOCK + (size_t)(u & 1) * HALF_BYTES;
+}
 
 QUASAR_DEVICE_INLINE void ldsm_x4(uint32_t addr, uint32_t& d0, uint32_t& d1, uint32_t& d2, uint32_t& d3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -228,35 +247,26 @@ QUASAR_DEVICE_INLINE void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// First block of CTA c, and the CTA whose range holds block b, for the even
-// split of `total` items over `grid` CTAs.  The host guarantees
-// (total + 1) * (grid + 1) < 2^32, so 32-bit unsigned arithmetic is exact
-// (64-bit division is emulated and far slower).
-QUASAR_DEVICE_INLINE int range_begin(int c, int total, int grid) {
-  return (int)(((unsigned)c * (unsigned)total) / (unsigned)grid);
-}
-QUASAR_DEVICE_INLINE int cta_of_block(int b, int total, int grid) {
-  return (int)(((unsigned)(b + 1) * (unsigned)grid + (unsigned)total - 1u) / (unsigned)total) - 1;
-}
-
-// A finalizer warp's share of a tile is row tile mt, all token tiles: lane
-// holds int4 v[ni] per token tile ni, whose element j is row 8 (j >> 1) + g
-// of the row tile, token 8 ni + 2c + (j & 1).  `sa_s` holds sa of every
-// token (shared memory), `swt` sw of the tile's 128 rows (shared memory for
-// the CTA's first and last tile, else global).
+// A finalizer warp's share of a unit is row tile mt and token tiles nh,
+// nh + 2, ...: lane holds int4 v[h] for token tile ni = nh + 2h, whose
+// element j is row 8 (j >> 1) + g of the row tile, token 8 ni + 2c + (j & 1).
+// `sa_s` holds sa of every token (shared memory), `swu` sw of the unit's 64
+// rows (shared memory for the CTA's first and last unit, else global).
 template <int NT8>
-QUASAR_DEVICE_INLINE void epilogue(const Params& p, const int4 (&v4)[NT8], int t, int mt, int lane,
-                                   const float* sa_s, const float* swt) {
+QUASAR_DEVICE_INLINE void epilogue(const Params& p, const int4 (&v4)[Cfg<NT8>::NH], int u, int mt, int nh, int lane,
+                                   const float* sa_s, const float* swu) {
   const int g = lane >> 2, c = lane & 3;
-  const int nrow0 = t * BM + mt * 16 + g;
+  const int nrow0 = u * UM + mt * 16 + g;
   float swr[2] = {0.f, 0.f};
   if (!p.acc_out) {
-    swr[0] = swt[mt * 16 + g];
-    swr[1] = swt[mt * 16 + g + 8];
+    swr[0] = swu[mt * 16 + g];
+    swr[1] = swu[mt * 16 + g + 8];
   }
 #pragma unroll
-  for (int ni = 0; ni < NT8; ++ni) {
-    const int32_t v[4] = {v4[ni].x, v4[ni].y, v4[ni].z, v4[ni].w};
+  for (int h = 0; h < Cfg<NT8>::NH; ++h) {
+    const int ni = nh + 2 * h;
+    if (ni >= NT8) break;
+    const int32_t v[4] = {v4[h].x, v4[h].y, v4[h].z, v4[h].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int m = ni * 8 + 2 * c + (j & 1), n = nrow0 + 8 * (j >> 1);
@@ -271,102 +281,109 @@ QUASAR_DEVICE_INLINE void epilogue(const Params& p, const int4 (&v4)[NT8], int t
   }
 }
 
-// Contributors of split tile t and the slot each used: a contributor's
-// segment of a split tile is its first segment (slot 0) or its last (slot
-// 1); every one is partial.
+// Slot of contributor cc for split unit u: a contributor's segment of a split
+// unit is the first segment of its split range (slot 0) or the last (slot 1);
+// every one is partial.  Points at lane's int4 of the share's token tile nh.
 template <int NT8>
-QUASAR_DEVICE_INLINE int4* slot_ptr(const Params& p, int cc, int t, int mt, int lane, int grid) {
-  const int first_t = range_begin(cc, p.total1, grid) / p.KB;
-  return p.slots + ((size_t)cc * 2 + (first_t == t ? 0 : 1)) * Cfg<NT8>::SLOT + (size_t)mt * NT8 * 32 + lane;
+QUASAR_DEVICE_INLINE int4* slot_ptr(const Params& p, int cc, int u, int mt, int nh, int lane, int grid) {
+  const int first_u = range_begin(cc, p.total1, grid) / p.KB;
+  return p.slots + ((size_t)cc * 2 + (first_u == u ? 0 : 1)) * Cfg<NT8>::SLOT + ((size_t)mt * NT8 + nh) * 32 + lane;
 }
 
-// Sum of every contributor's slot for this warp's share of split tile t
+// Sum of every contributor's slot for this warp's share of split unit u
 // (loads only: four contributors in flight at a time).
 template <int NT8>
-QUASAR_DEVICE_INLINE void load_slots(const Params& p, int t, int mt, int lane, int grid, int4 (&s)[NT8]) {
-  const int c_lo = cta_of_block(t * p.KB, p.total1, grid);
-  const int c_hi = cta_of_block((t + 1) * p.KB - 1, p.total1, grid);
+QUASAR_DEVICE_INLINE void load_slots(const Params& p, int u, int mt, int nh, int lane, int grid,
+                                     int4 (&s)[Cfg<NT8>::NH]) {
+  constexpr int NH = Cfg<NT8>::NH;
+  const int c_lo = cta_of_block(u * p.KB, p.total1, grid);
+  const int c_hi = cta_of_block((u + 1) * p.KB - 1, p.total1, grid);
 #pragma unroll
-  for (int ni = 0; ni < NT8; ++ni) s[ni] = make_int4(0, 0, 0, 0);
+  for (int h = 0; h < NH; ++h) s[h] = make_int4(0, 0, 0, 0);
   for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
-    int4 v[4][NT8];
+    int4 v[4][NH];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int q = 0; q < 4; ++q) {
+      const int4* slot = slot_ptr<NT8>(p, c0 + q <= c_hi ? c0 + q : c_hi, u, mt, nh, lane, grid);
 #pragma unroll
-      for (int ni = 0; ni < NT8; ++ni)
-        v[u][ni] = (c0 + u <= c_hi) ? __ldcg(slot_ptr<NT8>(p, c0 + u, t, mt, lane, grid) + ni * 32)
-                                    : make_int4(0, 0, 0, 0);
+      for (int h = 0; h < NH; ++h)
+        v[q][h] = (c0 + q <= c_hi && nh + 2 * h < NT8) ? __ldcg(slot + 2 * h * 32) : make_int4(0, 0, 0, 0);
+    }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int q = 0; q < 4; ++q)
 #pragma unroll
-      for (int ni = 0; ni < NT8; ++ni) {
-        s[ni].x += v[u][ni].x;
-        s[ni].y += v[u][ni].y;
-        s[ni].z += v[u][ni].z;
-        s[ni].w += v[u][ni].w;
+      for (int h = 0; h < NH; ++h) {
+        s[h].x += v[q][h].x;
+        s[h].y += v[q][h].y;
+        s[h].z += v[q][h].z;
+        s[h].w += v[q][h].w;
       }
   }
 }
 
-// Each slot share is read exactly once (by the warp that completes the tile)
+// Each slot share is read exactly once (by the warp that completes the unit)
 // and zeroed after the read, so the workspace is left as it was found.
 template <int NT8>
-QUASAR_DEVICE_INLINE void zero_slots(const Params& p, int t, int mt, int lane, int grid) {
-  const int c_lo = cta_of_block(t * p.KB, p.total1, grid);
-  const int c_hi = cta_of_block((t + 1) * p.KB - 1, p.total1, grid);
+QUASAR_DEVICE_INLINE void zero_slots(const Params& p, int u, int mt, int nh, int lane, int grid) {
+  const int c_lo = cta_of_block(u * p.KB, p.total1, grid);
+  const int c_hi = cta_of_block((u + 1) * p.KB - 1, p.total1, grid);
   for (int cc = c_lo; cc <= c_hi; ++cc) {
-    int4* slot = slot_ptr<NT8>(p, cc, t, mt, lane, grid);
+    int4* slot = slot_ptr<NT8>(p, cc, u, mt, nh, lane, grid);
 #pragma unroll
-    for (int ni = 0; ni < NT8; ++ni) __stcg(slot + ni * 32, make_int4(0, 0, 0, 0));
+    for (int h = 0; h < Cfg<NT8>::NH; ++h)
+      if (nh + 2 * h < NT8) __stcg(slot + 2 * h * 32, make_int4(0, 0, 0, 0));
   }
 }
 
 // Publish partial segments: one fence for this warp's slot stores, then the
-// K-block count of each segment (tile ta with na blocks, and tile tb with nb
-// blocks when tb >= 0); a warp whose count completes a tile sums the tile's
-// slots and runs its epilogue.  Both tiles' slots are loaded before either
+// K-block count of each segment (unit ua with na blocks, and unit ub with nb
+// blocks when ub >= 0); a warp whose count completes a unit sums the unit's
+// slots and runs its epilogue.  Both units' slots are loaded before either
 // epilogue so that their latencies overlap.
 template <int NT8>
-QUASAR_DEVICE_INLINE void count_segments(const Params& p, int ta, int na, int tb, int nb, int mt, int lane,
-                                         int grid, const float* sa_s, const float* swa, const float* swb) {
+QUASAR_DEVICE_INLINE void count_segments(const Params& p, int ua, int na, int ub, int nb, int warp, int mt, int nh,
+                                         int lane, int grid, const float* sa_s, const float* swa,
+                                         const float* swb) {
+  constexpr int NH = Cfg<NT8>::NH;
   __threadfence();
   __syncwarp();
   uint32_t last_mask = 0;
   if (lane == 0) {
-    const uint32_t old_a = atomicAdd(&p.ws_cnt[(size_t)ta * CNT_STRIDE + mt], (uint32_t)na);
-    const uint32_t old_b = (tb >= 0) ? atomicAdd(&p.ws_cnt[(size_t)tb * CNT_STRIDE + mt], (uint32_t)nb) : 0u;
+    const uint32_t old_a = atomicAdd(&p.ws_cnt[(size_t)ua * CNT_PER_UNIT + warp], (uint32_t)na);
+    const uint32_t old_b = (ub >= 0) ? atomicAdd(&p.ws_cnt[(size_t)ub * CNT_PER_UNIT + warp], (uint32_t)nb) : 0u;
     if (old_a + (uint32_t)na == (uint32_t)p.KB) last_mask |= 1u;
-    if (tb >= 0 && old_b + (uint32_t)nb == (uint32_t)p.KB) last_mask |= 2u;
+    if (ub >= 0 && old_b + (uint32_t)nb == (uint32_t)p.KB) last_mask |= 2u;
   }
   last_mask = __shfl_sync(0xffffffffu, last_mask, 0);
   if (!last_mask) return;
   __threadfence();
-  int4 va[NT8], vb[NT8];
-  if (last_mask & 1u) load_slots<NT8>(p, ta, mt, lane, grid, va);
-  if (last_mask & 2u) load_slots<NT8>(p, tb, mt, lane, grid, vb);
+  int4 va[NH], vb[NH];
+  if (last_mask & 1u) load_slots<NT8>(p, ua, mt, nh, lane, grid, va);
+  if (last_mask & 2u) load_slots<NT8>(p, ub, mt, nh, lane, grid, vb);
   if (last_mask & 1u) {
-    zero_slots<NT8>(p, ta, mt, lane, grid);
-    epilogue<NT8>(p, va, ta, mt, lane, sa_s, swa);
-    if (lane == 0) p.ws_cnt[(size_t)ta * CNT_STRIDE + mt] = 0u;   // ready for the next call
+    zero_slots<NT8>(p, ua, mt, nh, lane, grid);
+    epilogue<NT8>(p, va, ua, mt, nh, lane, sa_s, swa);
+    if (lane == 0) p.ws_cnt[(size_t)ua * CNT_PER_UNIT + warp] = 0u;   // ready for the next call
   }
   if (last_mask & 2u) {
-    zero_slots<NT8>(p, tb, mt, lane, grid);
-    epilogue<NT8>(p, vb, tb, mt, lane, sa_s, swb);
-    if (lane == 0) p.ws_cnt[(size_t)tb * CNT_STRIDE + mt] = 0u;
+    zero_slots<NT8>(p, ub, mt, nh, lane, grid);
+    epilogue<NT8>(p, vb, ub, mt, nh, lane, sa_s, swb);
+    if (lane == 0) p.ws_cnt[(size_t)ub * CNT_PER_UNIT + warp] = 0u;
   }
 }
 
 template <int NT8>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
 w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   using C = Cfg<NT8>;
+  constexpr int NH = C::NH;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stages = smem;                                     // S x [W 16 KB | X NT x 128 B]
+  uint8_t* stages = smem;                                     // S x [W half 8 KB | X NT x 128 B]
   float4* red = reinterpret_cast<float4*>(smem + C::S * C::STAGE);
   int4* fin = reinterpret_cast<int4*>(smem + C::S * C::STAGE + C::RED);
   float* sa_s = reinterpret_cast<float*>(smem + C::S * C::STAGE + C::RED + C::FIN);   // [32]
-  float* sw_s = sa_s + 32;                                                                // [2][128]
+  float* sw_s = sa_s + 32;                                                                // [2][64]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::S * C::STAGE + C::RED + C::FIN + C::SCL);
   uint64_t* empty = full + C::S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::S);
@@ -389,7 +406,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
   const int grid = (int)gridDim.x;
   const int KB = p.KB;
-  const Sched sc = schedule_of((int)blockIdx.x, grid, KB, p.mode, p.csize, p.split_tiles, p.total1, p.whole_per);
+  const Sched sc = schedule_of((int)blockIdx.x, grid, p);
 
   if (warp == PRODUCER_WARP) {
     if (lane == 0) {
@@ -401,8 +418,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         Walk w(sc, KB);
         for (; pre < C::S && w.more(); ++pre, w.next(KB)) {
           mbar_arrive_expect_tx(&full[pre], (uint32_t)C::STAGE);
-          bulk_load(stages + pre * C::STAGE, p.wp + ((size_t)w.t * KB + w.kb) * BLOCK_BYTES, BLOCK_BYTES,
-                    &full[pre], pol_w);
+          bulk_load(stages + pre * C::STAGE, unit_block(p, w.u, w.kb), HALF_BYTES, &full[pre], pol_w);
         }
       }
       pdl_wait();  // token codes come from the previous kernel
@@ -414,9 +430,9 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         if (issued >= pre) {
           if (!mbar_wait(&empty[rg.s], rg.ph ^ 1u, abort_flag, p.err, SITE_SKINNY_EMPTY, p.limit_ns)) break;
           mbar_arrive_expect_tx(&full[rg.s], (uint32_t)C::STAGE);
-          bulk_load(st, p.wp + ((size_t)w.t * KB + w.kb) * BLOCK_BYTES, BLOCK_BYTES, &full[rg.s], pol_w);
+          bulk_load(st, unit_block(p, w.u, w.kb), HALF_BYTES, &full[rg.s], pol_w);
         }
-        tma_load_2d(st + BLOCK_BYTES, &tmX, w.kb * BK, 0, &full[rg.s], pol_x);
+        tma_load_2d(st + HALF_BYTES, &tmX, w.kb * BK, 0, &full[rg.s], pol_x);
       }
       // Never leave with copies in flight.
       for (int s = 0; s < C::S && s < issued; ++s) {
@@ -435,56 +451,59 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
   // ------------------------------------------------------------------ consumers
   const int kq = warp & (KQ - 1);   // K bytes [32 kq, 32 kq + 32) of each block
-  const int rg = warp / KQ;         // rows [64 rg, 64 rg + 64): row tiles 4 rg .. 4 rg + 3
+  const int rg = warp / KQ;         // rows [32 rg, 32 rg + 32) of the unit: row tiles 2 rg, 2 rg + 1
   const int g = lane >> 2, c = lane & 3;
-  const int mt_f = warp;            // the row tile this warp finalizes
+  const int mt_f = warp >> 1;       // finalizer share: row tile mt_f, token tiles nh, nh + 2, ...
+  const int nh = warp & 1;
   pdl_wait();                       // scales and workspace belong to the previous kernel until here
-  const int t_first = (sc.s1 > sc.s0) ? sc.s0 / KB : sc.w0;
-  const int t_last = (sc.w1 > sc.w0) ? sc.w1 - 1 : (sc.s1 - 1) / KB;
-  const int t_first1 = sc.s0 / KB;  // first tile of the split range (its slot 0)
+  const int u_first = (sc.s1 > sc.s0) ? sc.s0 / KB : sc.w0;
+  const int u_last = (sc.w1 > sc.w0) ? sc.w1 - 1 : (sc.s1 - 1) / KB;
+  const int u_first1 = sc.s0 / KB;  // first unit of the split range (its slot 0)
   // Stage the dequantization scales the epilogues will need: every token's
-  // sa, and sw of the first and last tile of this CTA (read after the first
+  // sa, and sw of the first and last unit of this CTA (read after the first
   // run-end barrier, which orders these stores).
   if (!p.acc_out) {
-    for (int i = threadIdx.x; i < 32 + 2 * BM; i += CWARPS * 32) {
+    for (int i = threadIdx.x; i < 32 + 2 * UM; i += CWARPS * 32) {
       if (i < 32) {
         sa_s[i] = (i < p.M) ? __ldg(&p.sa[i]) : 0.f;
       } else {
         const int r = i - 32;
-        const int n = (r < BM ? t_first : t_last) * BM + (r & (BM - 1));
+        const int n = (r < UM ? u_first : u_last) * UM + (r & (UM - 1));
         sw_s[r] = (n < p.N) ? __ldg(&p.sw[n]) : 0.f;
       }
     }
   }
 
-  float acc[4][NT8][4];
+  float acc[2][NT8][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 2; ++i)
 #pragma unroll
     for (int n = 0; n < NT8; ++n)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[i][n][j] = 0.f;
-  // Finished integer sums of this warp's row tile, kept in shared memory
-  // (touched once per run).
-  int4* share = fin + mt_f * NT8 * 32 + lane;
+  // Finished integer sums of this warp's finalizer share, kept in shared
+  // memory (touched once per run): token tile nh + 2h at share[2h * 32].
+  int4* share = fin + ((size_t)mt_f * NT8 + nh) * 32 + lane;
 #pragma unroll
-  for (int ni = 0; ni < NT8; ++ni) share[ni * 32] = make_int4(0, 0, 0, 0);
+  for (int h = 0; h < NH; ++h)
+    if (nh + 2 * h < NT8) share[2 * h * 32] = make_int4(0, 0, 0, 0);
 
-  // Per-lane address parts.  ldmatrix over one K step of 32 rows: lanes
-  // 8i..8i+7 give rows 8i..8i+7, i.e. matrix i = (row tile i >> 1, row half
-  // i & 1).  The second K step's chunk differs from the first in bit 0 only,
-  // i.e. its offset is the first one's ^ 16.
-  const uint32_t a_off = (uint32_t)((rg * 64 + lane) * BK + (((2 * kq) ^ (lane & 7)) << 4));
-  const uint32_t b_off = (uint32_t)(BLOCK_BYTES + g * BK + (((2 * kq) ^ g) << 4) + 4 * c);
+  // Per-lane address parts.  ldmatrix over one K step of the warp's 32 rows:
+  // lanes 8i..8i+7 give rows 8i..8i+7, i.e. matrix i = (row tile i >> 1, row
+  // half i & 1); rows keep their swizzle phase because units start at a
+  // multiple of 8 rows.  The second K step's chunk differs from the first in
+  // bit 0 only, i.e. its offset is the first one's ^ 16.
+  const uint32_t a_off = (uint32_t)((rg * 32 + lane) * BK + (((2 * kq) ^ (lane & 7)) << 4));
+  const uint32_t b_off = (uint32_t)(HALF_BYTES + g * BK + (((2 * kq) ^ g) << 4) + 4 * c);
   const uint32_t stages_u32 = smem_u32(stages);
 
   bool bad = false;
   // Partial segments of the split range (at most two: its first and last)
   // are counted together when the range ends, so that one fence covers both.
-  int seg_ta = -1, seg_na = 0, seg_tb = -1, seg_nb = 0;
-  // sw of tile t: staged for the CTA's first and last tile.
-  auto sw_of = [&](int t) -> const float* {
-    return t == t_first ? sw_s : t == t_last ? sw_s + BM : p.sw + (size_t)t * BM;
+  int seg_ua = -1, seg_na = 0, seg_ub = -1, seg_nb = 0;
+  // sw of unit u: staged for the CTA's first and last unit.
+  auto sw_of = [&](int u) -> const float* {
+    return u == u_first ? sw_s : u == u_last ? sw_s + UM : p.sw + (size_t)u * UM;
   };
   Walk w(sc, KB);
   Ring<C::S> r;
@@ -503,19 +522,15 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 #pragma unroll
         for (int ni = 0; ni < NT8; ++ni)
           s8x4_to_f16x4(lds32(st + (b_off ^ (ks << 4)) + (uint32_t)(ni * 8 * BK)), bq[ni][0], bq[ni][1]);
+        uint32_t d[4];
+        ldsm_x4(st + (a_off ^ (ks << 4)), d[0], d[1], d[2], d[3]);
 #pragma unroll
-        for (int i2 = 0; i2 < 2; ++i2) {
-          uint32_t d[4];
-          ldsm_x4(st + (a_off ^ (ks << 4)) + (uint32_t)(i2 * 32 * BK), d[0], d[1], d[2], d[3]);
+        for (int i = 0; i < 2; ++i) {
+          uint32_t a0, a1, a2, a3;
+          u8x4_to_f16x4(d[2 * i], a0, a2);       // rows g: K slots 2c.. (bytes 4c, 4c+1), 2c+8.. (4c+2, 4c+3)
+          u8x4_to_f16x4(d[2 * i + 1], a1, a3);   // rows g + 8
 #pragma unroll
-          for (int ii = 0; ii < 2; ++ii) {
-            uint32_t a0, a1, a2, a3;
-            u8x4_to_f16x4(d[2 * ii], a0, a2);       // rows g: K slots 2c.. (bytes 4c, 4c+1), 2c+8.. (4c+2, 4c+3)
-            u8x4_to_f16x4(d[2 * ii + 1], a1, a3);   // rows g + 8
-#pragma unroll
-            for (int ni = 0; ni < NT8; ++ni)
-              mma_16816(acc[2 * i2 + ii][ni], a0, a1, a2, a3, bq[ni][0], bq[ni][1]);
-          }
+          for (int ni = 0; ni < NT8; ++ni) mma_16816(acc[i][ni], a0, a1, a2, a3, bq[ni][0], bq[ni][1]);
         }
       }
       __syncwarp();
@@ -528,17 +543,19 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     // and carries the abort decision to every consumer warp.
     if (named_barrier_or(RED_BAR, CWARPS * 32, bad ? 1u : 0u)) break;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 2; ++i)
 #pragma unroll
       for (int ni = 0; ni < NT8; ++ni) {
-        red[(((4 * rg + i) * KQ + kq) * NT8 + ni) * 32 + lane] =
+        red[(((2 * rg + i) * KQ + kq) * NT8 + ni) * 32 + lane] =
             make_float4(acc[i][ni][0], acc[i][ni][1], acc[i][ni][2], acc[i][ni][3]);
         acc[i][ni][0] = acc[i][ni][1] = acc[i][ni][2] = acc[i][ni][3] = 0.f;
       }
     named_barrier_or(RED_BAR, CWARPS * 32, 0u);
 #pragma unroll
-    for (int ni = 0; ni < NT8; ++ni) {
-      int4 f = share[ni * 32];
+    for (int h = 0; h < NH; ++h) {
+      const int ni = nh + 2 * h;
+      if (ni >= NT8) break;
+      int4 f = share[2 * h * 32];
 #pragma unroll
       for (int q = 0; q < KQ; ++q) {
         const float4 v = red[((mt_f * KQ + q) * NT8 + ni) * 32 + lane];
@@ -547,71 +564,75 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         f.z += __float2int_rn(v.z);
         f.w += __float2int_rn(v.w);
       }
-      share[ni * 32] = f;
+      share[2 * h * 32] = f;
     }
     if (!w.seg_last(KB)) continue;
 
-    // ---- end of this CTA's segment of tile t.
-    const int t = w.t;
+    // ---- end of this CTA's segment of unit u.
+    const int u = w.u;
     const int nb = w.kb - w.kb_first + 1;
     if (p.mode == 1) break;   // the only segment: summed across the cluster below
     if (nb == KB) {
-      int4 v[NT8];
+      int4 v[NH];
 #pragma unroll
-      for (int ni = 0; ni < NT8; ++ni) v[ni] = share[ni * 32];
-      epilogue<NT8>(p, v, t, mt_f, lane, sa_s, sw_of(t));   // the whole tile
+      for (int h = 0; h < NH; ++h) v[h] = (nh + 2 * h < NT8) ? share[2 * h * 32] : make_int4(0, 0, 0, 0);
+      epilogue<NT8>(p, v, u, mt_f, nh, lane, sa_s, sw_of(u));   // the whole unit
     } else {
       // Partial segment of the split range: store the share into this CTA's
       // slot for it (0 = the range's first segment, 1 = its last).
-      int4* slot = p.slots + ((size_t)blockIdx.x * 2 + (t == t_first1 ? 0 : 1)) * C::SLOT +
-                   (size_t)mt_f * NT8 * 32 + lane;
+      int4* slot = p.slots + ((size_t)blockIdx.x * 2 + (u == u_first1 ? 0 : 1)) * C::SLOT +
+                   ((size_t)mt_f * NT8 + nh) * 32 + lane;
 #pragma unroll
-      for (int ni = 0; ni < NT8; ++ni) slot[ni * 32] = share[ni * 32];
-      if (seg_ta < 0) {
-        seg_ta = t;
+      for (int h = 0; h < NH; ++h)
+        if (nh + 2 * h < NT8) slot[2 * h * 32] = share[2 * h * 32];
+      if (seg_ua < 0) {
+        seg_ua = u;
         seg_na = nb;
       } else {
-        seg_tb = t;
+        seg_ub = u;
         seg_nb = nb;
       }
     }
-    if (w.phase == 1 && w.left == 1 && seg_ta >= 0) {
+    if (w.phase == 1 && w.left == 1 && seg_ua >= 0) {
       // The split range ends here: publish its partial segments now, while
-      // the whole tiles (if any) still stream.
-      count_segments<NT8>(p, seg_ta, seg_na, seg_tb, seg_nb, mt_f, lane, grid, sa_s, sw_of(seg_ta),
-                          seg_tb >= 0 ? sw_of(seg_tb) : sw_s);
-      seg_ta = -1;
+      // the whole units (if any) still stream.
+      count_segments<NT8>(p, seg_ua, seg_na, seg_ub, seg_nb, warp, mt_f, nh, lane, grid, sa_s, sw_of(seg_ua),
+                          seg_ub >= 0 ? sw_of(seg_ub) : sw_s);
+      seg_ua = -1;
     }
 #pragma unroll
-    for (int ni = 0; ni < NT8; ++ni) share[ni * 32] = make_int4(0, 0, 0, 0);
+    for (int h = 0; h < NH; ++h)
+      if (nh + 2 * h < NT8) share[2 * h * 32] = make_int4(0, 0, 0, 0);
   }
 
   if (p.mode == 1) {
     // Cluster split: every CTA of the cluster holds the sums of one K slice of
-    // tile t in `fin`.  After the barrier each row tile is finished by one
-    // CTA (row tile mt in the CTA of rank mt % C), reading the other slices
-    // through distributed shared memory; the second barrier keeps every CTA's
-    // shared memory alive until those reads are done.
+    // unit u in `fin`.  After the barrier each finalizer share (row tile,
+    // token-tile parity) is finished by one CTA (the share of warp w by the
+    // CTA of rank w % C), reading the other slices through distributed shared
+    // memory; the second barrier keeps every CTA's shared memory alive until
+    // those reads are done.
     __syncwarp();
     cluster_sync_all();
     const int csz = p.csize;
     const int rank = (int)blockIdx.x % csz;
-    if (!bad && (mt_f % csz) == rank) {
-      int4 v[NT8];
+    if (!bad && (warp % csz) == rank) {
+      int4 v[NH];
 #pragma unroll
-      for (int ni = 0; ni < NT8; ++ni) v[ni] = share[ni * 32];
+      for (int h = 0; h < NH; ++h) v[h] = (nh + 2 * h < NT8) ? share[2 * h * 32] : make_int4(0, 0, 0, 0);
       for (int q = 0; q < csz; ++q) {
         if (q == rank) continue;
 #pragma unroll
-        for (int ni = 0; ni < NT8; ++ni) {
-          const int4 u = ld_dsmem_int4(share + ni * 32, (uint32_t)q);
-          v[ni].x += u.x;
-          v[ni].y += u.y;
-          v[ni].z += u.z;
-          v[ni].w += u.w;
+        for (int h = 0; h < NH; ++h) {
+          if (nh + 2 * h >= NT8) break;
+          const int4 x = ld_dsmem_int4(share + 2 * h * 32, (uint32_t)q);
+          v[h].x += x.x;
+          v[h].y += x.y;
+          v[h].z += x.z;
+          v[h].w += x.w;
         }
       }
-      epilogue<NT8>(p, v, t_first, mt_f, lane, sa_s, sw_s);
+      epilogue<NT8>(p, v, u_first, mt_f, nh, lane, sa_s, sw_s);
     }
     __syncwarp();
     cluster_sync_all();
@@ -678,25 +699,27 @@ static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t
   cudaGetDevice(&dev);
   cudaError_t e = configure<NT8>(dev);
   if (e != cudaSuccess) return e;
-  const int n_tiles = (p.N + BM - 1) / BM;
-  // Few tiles: one cluster per tile, as many K slices as fit in one wave.
-  int csize = std::min(std::min(8, sms / n_tiles), p.KB);
-  while (csize >= 2 && resident_clusters<NT8>(dev, csize) < n_tiles) --csize;
+  const int n_units = (p.N + UM - 1) / UM;
+  const int slots = std::min(2 * sms, MAX_CTAS);   // two CTAs per SM
+  // Few units: one cluster per unit, with the most K slices that keep every
+  // cluster resident in one wave.
+  int csize = std::min(std::min(8, slots / n_units), p.KB);
+  while (csize >= 2 && resident_clusters<NT8>(dev, csize) < n_units) --csize;
   int grid;
   if (csize >= 2) {
     p.mode = 1;
     p.csize = csize;
-    p.split_tiles = 0;
+    p.split_units = 0;
     p.total1 = 0;
     p.whole_per = 0;
-    grid = n_tiles * csize;
+    grid = n_units * csize;
   } else {
     p.mode = 0;
     p.csize = 1;
-    grid = std::min(sms, MAX_CTAS);
-    p.whole_per = n_tiles / grid;
-    p.split_tiles = n_tiles - p.whole_per * grid;
-    p.total1 = p.split_tiles * p.KB;
+    grid = slots;
+    p.whole_per = n_units / grid;
+    p.split_units = n_units - p.whole_per * grid;
+    p.total1 = p.split_units * p.KB;
     if (p.whole_per == 0) grid = std::min(grid, p.total1);
     if ((unsigned long long)(p.total1 + 1) * (unsigned long long)(grid + 1) >= (1ull << 32))
       return cudaErrorInvalidValue;
@@ -706,20 +729,20 @@ static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t
   return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8>, tx, p);
 }
 
-bool handles(int M) { return M >= 1 && M <= 16; }
+bool handles(int M) { return M >= 1 && M <= 24; }
 
-// Partial-sum slots this kernel may need after the counters: two per CTA.
-// Like the counters they are zero between calls (each is zeroed by its
-// reader).
+// Partial-sum slots this kernel may need after the counters: two per CTA,
+// each 64 rows x NT int32.  Like the counters they are zero between calls
+// (each is zeroed by its reader).
 size_t slots_bytes(int M, int N, int K) {
   if (!handles(M) || N <= 0 || K <= 0) return 0;
-  const long long total = (long long)((N + BM - 1) / BM) * ((K + BK - 1) / BK);
-  const long long ctas = std::min<long long>(total, MAX_CTAS);
-  return (size_t)ctas * 2 * (size_t)BM * 8 * ((M + 7) / 8) * 4;
+  const long long items = (long long)((N + UM - 1) / UM) * ((K + BK - 1) / BK);
+  const long long ctas = std::min<long long>(items, MAX_CTAS);
+  return (size_t)ctas * 2 * (size_t)UM * 8 * ((M + 7) / 8) * 4;
 }
 
-// Arguments were validated by the caller; ws_cnt holds >= n_tiles * 16
-// zeroed counters, `slots` slots_bytes() bytes (no initial value needed).
+// Arguments were validated by the caller; ws_cnt holds >= 8 zeroed counters
+// per 64-row unit, `slots` slots_bytes() bytes (no initial value needed).
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
                     void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream) {
   const int nt8 = (M + 7) / 8;
@@ -746,7 +769,8 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   cudaError_t e;
   switch (nt8) {
     case 1: e = launch<1>(tx, p, sms, stream); break;
-    default: e = launch<2>(tx, p, sms, stream); break;   // handles() keeps M <= 16
+    case 2: e = launch<2>(tx, p, sms, stream); break;
+    default: e = launch<3>(tx, p, sms, stream); break;   // handles() keeps M <= 24
   }
   if (e == cudaErrorInvalidValue) return QUASAR_ERR_UNSUPPORTED;
   return cuda_status(e);
