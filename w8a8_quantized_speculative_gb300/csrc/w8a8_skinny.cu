@@ -72,17 +72,20 @@ constexpr int RED_BAR = 1;        // named barrier of the consumer warps
 constexpr int MAX_CTAS = 320;     // grid cap (two CTAs per SM); sizes the partial-sum slots
 constexpr int CNT_PER_UNIT = 8;   // workspace counters per unit (16 per 128-row tile)
 constexpr int SMEM_CAP = 112 * 1024;
+constexpr int G = 2;              // K blocks per pipeline stage (one handshake per pair)
 // A warp adds 32 products per block into each fp32 accumulator, each product
 // at most 127^2 = 16129 in magnitude: 32 blocks x 32 x 16129 < 2^24, so over
 // a run of <= 32 blocks every partial sum is an exact integer in fp32.
 constexpr int RUN_BLOCKS = 32;
+static_assert(RUN_BLOCKS % 2 == 0, "runs end on a stage boundary");
 
 template <int NT8>
 struct Cfg {
   static constexpr int NT = 8 * NT8;                        // token columns (padded to 8)
   static constexpr int NH = (NT8 + 1) / 2;                  // token tiles of one finalizer share
   static constexpr int XB = NT * BK;                        // INT8 token tile of a block
-  static constexpr int STAGE = HALF_BYTES + XB;             // multiple of 1024 (swizzle atoms)
+  static constexpr int BLK = HALF_BYTES + XB;               // one block: weight half + token tile
+  static constexpr int STAGE = G * BLK;                     // multiple of 1024 (swizzle atoms)
   static constexpr int RED = UT * KQ * NT8 * 32 * 16;       // fp32 partials: [row tile][kq][token tile][lane]
   static constexpr int FIN = UT * NT8 * 32 * 16;            // int32 run sums: [row tile][token tile][lane]
   static constexpr int SLOT = UT * NT8 * 32;                // int4 per partial-sum slot (64 rows x NT)
@@ -91,8 +94,8 @@ struct Cfg {
   static constexpr int S_FIT = (SMEM_CAP - FIXED) / STAGE;
   static constexpr int S = S_FIT < 12 ? S_FIT : 12;         // stages in flight
   static constexpr int SMEM = FIXED + S * STAGE;
-  static_assert(STAGE % 1024 == 0, "stage alignment");
-  static_assert(S >= 4, "pipeline depth");
+  static_assert(BLK % 1024 == 0, "block alignment");
+  static_assert(S >= 3, "pipeline depth");
   static_assert(SMEM <= SMEM_CAP, "two CTAs per SM");
 };
 
@@ -149,11 +152,12 @@ QUASAR_DEVICE_INLINE Sched schedule_of(int c, int grid, const Params& p) {
   return sc;
 }
 
-// Walks a schedule one K block per step.  Segments (the CTA's blocks of one
-// unit within a phase) and accumulation runs (<= RUN_BLOCKS blocks of a
-// segment) are contiguous.
+// Walks a schedule one stage (g <= G consecutive K blocks) per step.
+// Segments (the CTA's blocks of one unit within a phase) and accumulation
+// runs (<= RUN_BLOCKS blocks of a segment, RUN_BLOCKS a multiple of G) are
+// contiguous and always end on a stage boundary.
 struct Walk {
-  int u, kb, kb_first, left, left2, w_next, phase;
+  int u, kb, kb_first, left, left2, w_next, phase, g;
   __device__ Walk(const Sched& sc, int KB) {
     if (sc.s1 > sc.s0) {
       phase = 1;
@@ -169,13 +173,20 @@ struct Walk {
       left2 = 0;
     }
     w_next = sc.w0;
+    size(KB);
+  }
+  __device__ void size(int KB) {
+    g = G;
+    if (g > left) g = left;
+    if (g > KB - kb) g = KB - kb;
   }
   __device__ bool more() const { return left > 0; }
-  __device__ bool seg_last(int KB) const { return left == 1 || kb + 1 == KB; }
-  __device__ bool run_last(int KB) const { return seg_last(KB) || ((kb - kb_first + 1) % RUN_BLOCKS) == 0; }
+  __device__ bool seg_last(int KB) const { return left == g || kb + g == KB; }
+  __device__ bool run_last(int KB) const { return seg_last(KB) || ((kb - kb_first + g) % RUN_BLOCKS) == 0; }
   __device__ void next(int KB) {
-    --left;
-    if (++kb == KB) {
+    left -= g;
+    kb += g;
+    if (kb == KB) {
       kb = 0;
       kb_first = 0;
       ++u;
@@ -187,6 +198,7 @@ struct Walk {
       left = left2;
       left2 = 0;
     }
+    if (left > 0) size(KB);
   }
 };
 
@@ -417,8 +429,10 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       {
         Walk w(sc, KB);
         for (; pre < C::S && w.more(); ++pre, w.next(KB)) {
-          mbar_arrive_expect_tx(&full[pre], (uint32_t)C::STAGE);
-          bulk_load(stages + pre * C::STAGE, unit_block(p, w.u, w.kb), HALF_BYTES, &full[pre], pol_w);
+          mbar_arrive_expect_tx(&full[pre], (uint32_t)(w.g * C::BLK));
+          for (int b = 0; b < w.g; ++b)
+            bulk_load(stages + pre * C::STAGE + b * C::BLK, unit_block(p, w.u, w.kb + b), HALF_BYTES, &full[pre],
+                      pol_w);
         }
       }
       pdl_wait();  // token codes come from the previous kernel
@@ -429,10 +443,12 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         uint8_t* st = stages + rg.s * C::STAGE;
         if (issued >= pre) {
           if (!mbar_wait(&empty[rg.s], rg.ph ^ 1u, abort_flag, p.err, SITE_SKINNY_EMPTY, p.limit_ns)) break;
-          mbar_arrive_expect_tx(&full[rg.s], (uint32_t)C::STAGE);
-          bulk_load(st, unit_block(p, w.u, w.kb), HALF_BYTES, &full[rg.s], pol_w);
+          mbar_arrive_expect_tx(&full[rg.s], (uint32_t)(w.g * C::BLK));
+          for (int b = 0; b < w.g; ++b)
+            bulk_load(st + b * C::BLK, unit_block(p, w.u, w.kb + b), HALF_BYTES, &full[rg.s], pol_w);
         }
-        tma_load_2d(st + HALF_BYTES, &tmX, w.kb * BK, 0, &full[rg.s], pol_x);
+        for (int b = 0; b < w.g; ++b)
+          tma_load_2d(st + b * C::BLK + HALF_BYTES, &tmX, (w.kb + b) * BK, 0, &full[rg.s], pol_x);
       }
       // Never leave with copies in flight.
       for (int s = 0; s < C::S && s < issued; ++s) {
@@ -513,7 +529,10 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       bad = !__all_sync(0xffffffffu, ok);
     }
     if (!bad) {
-      const uint32_t st = stages_u32 + (uint32_t)(r.s * C::STAGE);
+#pragma unroll
+      for (int b = 0; b < G; ++b) {
+      if (b >= w.g) break;
+      const uint32_t st = stages_u32 + (uint32_t)(r.s * C::STAGE + b * C::BLK);
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {
         // Token operands (row n = 8 ni + g of the swizzled tile sits at
@@ -532,6 +551,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 #pragma unroll
           for (int ni = 0; ni < NT8; ++ni) mma_16816(acc[i][ni], a0, a1, a2, a3, bq[ni][0], bq[ni][1]);
         }
+      }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[r.s]);
@@ -570,7 +590,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
     // ---- end of this CTA's segment of unit u.
     const int u = w.u;
-    const int nb = w.kb - w.kb_first + 1;
+    const int nb = w.kb + w.g - w.kb_first;
     if (p.mode == 1) break;   // the only segment: summed across the cluster below
     if (nb == KB) {
       int4 v[NH];
@@ -593,7 +613,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         seg_nb = nb;
       }
     }
-    if (w.phase == 1 && w.left == 1 && seg_ua >= 0) {
+    if (w.phase == 1 && w.left == w.g && seg_ua >= 0) {
       // The split range ends here: publish its partial segments now, while
       // the whole units (if any) still stream.
       count_segments<NT8>(p, seg_ua, seg_na, seg_ub, seg_nb, warp, mt_f, nh, lane, grid, sa_s, sw_of(seg_ua),
