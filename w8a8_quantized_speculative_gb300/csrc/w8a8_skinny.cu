@@ -23,12 +23,11 @@
 //
 // Work units.  A unit is 64 weight rows (half of a packed 128-row tile: its
 // blocks are contiguous 8 KB halves of the 16 KB packed blocks) over all of
-// K.  Two CTAs share each SM (~112 KB of shared memory each), so sixteen
-// consumer warps per SM hide each other's latencies.  Inside a CTA,
-// consumer warp (kq, rg) owns K bytes [32 kq, 32 kq + 32) of rows
-// [32 rg, 32 rg + 32) of the unit: 2 row tiles x 2 K steps x NT/8 token
-// tiles of MMAs per block.  The four K owners of a row tile are summed
-// through shared memory once per accumulation run.
+// K.  Two CTAs share each SM (~113 KB of shared memory each).  Inside a
+// CTA, consumer warp kq owns K bytes [32 kq, 32 kq + 32) of all 64 rows: 4
+// row tiles x 2 K steps x NT/8 token tiles of MMAs per block, so each
+// token operand is widened once per CTA.  The four K owners of a row tile
+// are summed through shared memory once per accumulation run.
 //
 // Schedules.  A split unit's sums must cross CTAs, and doing that at the end
 // of a launch puts a chain of dependent memory round trips after the last
@@ -63,15 +62,14 @@ constexpr int BK = 128;           // K bytes per block
 constexpr int PACKED_BLOCK = TILE_ROWS * BK;   // 16 KB packed block
 constexpr int HALF_BYTES = UM * BK;            // 8 KB: one unit's part of a block
 constexpr int KQ = 4;             // K quarters (32 K = 2 MMA K steps each)
-constexpr int RG = 2;             // row groups (32 rows = 2 row tiles each)
 constexpr int UT = UM / 16;       // row tiles per unit
-constexpr int CWARPS = KQ * RG;   // consumer warps; warp w finalizes (row tile w >> 1, token-tile parity w & 1)
+constexpr int CWARPS = KQ;        // consumer warps: warp w owns K quarter w of all rows, finalizes row tile w
 constexpr int PRODUCER_WARP = CWARPS;
 constexpr int THREADS = 32 * (CWARPS + 1);
 constexpr int RED_BAR = 1;        // named barrier of the consumer warps
 constexpr int MAX_CTAS = 320;     // grid cap (two CTAs per SM); sizes the partial-sum slots
 constexpr int CNT_PER_UNIT = 8;   // workspace counters per unit (16 per 128-row tile)
-constexpr int SMEM_CAP = 112 * 1024;
+constexpr int SMEM_CAP = 113 * 1024;   // two CTAs per SM
 constexpr int G = 2;              // K blocks per pipeline stage (one handshake per pair)
 // A warp adds 32 products per block into each fp32 accumulator, each product
 // at most 127^2 = 16129 in magnitude: 32 blocks x 32 x 16129 < 2^24, so over
@@ -79,10 +77,14 @@ constexpr int G = 2;              // K blocks per pipeline stage (one handshake 
 constexpr int RUN_BLOCKS = 32;
 static_assert(RUN_BLOCKS % 2 == 0, "runs end on a stage boundary");
 
-template <int NT8>
+// RIR: the run-end reduction buffer overlays the stage ring.  Only valid
+// when a CTA's single accumulation run ends after its last block (the ring
+// is then idle): the cluster schedule with K slices of <= RUN_BLOCKS blocks.
+// The space it frees becomes more stages in flight.
+template <int NT8, bool RIR = false>
 struct Cfg {
   static constexpr int NT = 8 * NT8;                        // token columns (padded to 8)
-  static constexpr int NH = (NT8 + 1) / 2;                  // token tiles of one finalizer share
+  static constexpr int NH = NT8;                            // token tiles of one finalizer share
   static constexpr int XB = NT * BK;                        // INT8 token tile of a block
   static constexpr int BLK = HALF_BYTES + XB;               // one block: weight half + token tile
   static constexpr int STAGE = G * BLK;                     // multiple of 1024 (swizzle atoms)
@@ -90,13 +92,14 @@ struct Cfg {
   static constexpr int FIN = UT * NT8 * 32 * 16;            // int32 run sums: [row tile][token tile][lane]
   static constexpr int SLOT = UT * NT8 * 32;                // int4 per partial-sum slot (64 rows x NT)
   static constexpr int SCL = 1024;                          // staged scales: sa[32], sw of 2 units
-  static constexpr int FIXED = 1024 + RED + FIN + SCL + 256;
+  static constexpr int FIXED = 1024 + (RIR ? 0 : RED) + FIN + SCL + 256;
   static constexpr int S_FIT = (SMEM_CAP - FIXED) / STAGE;
   static constexpr int S = S_FIT < 12 ? S_FIT : 12;         // stages in flight
   static constexpr int SMEM = FIXED + S * STAGE;
   static_assert(BLK % 1024 == 0, "block alignment");
   static_assert(S >= 3, "pipeline depth");
   static_assert(SMEM <= SMEM_CAP, "two CTAs per SM");
+  static_assert(!RIR || RED <= S * STAGE, "reduction buffer fits in the ring");
 };
 
 struct Params {
@@ -259,9 +262,9 @@ QUASAR_DEVICE_INLINE void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// A finalizer warp's share of a unit is row tile mt and token tiles nh,
-// nh + 2, ...: lane holds int4 v[h] for token tile ni = nh + 2h, whose
-// element j is row 8 (j >> 1) + g of the row tile, token 8 ni + 2c + (j & 1).
+// A finalizer warp's share of a unit is row tile mt and every token tile:
+// lane holds int4 v[ni] (nh = 0 below), whose element j is row 8 (j >> 1) + g
+// of the row tile, token 8 ni + 2c + (j & 1).
 // `sa_s` holds sa of every token (shared memory), `swu` sw of the unit's 64
 // rows (shared memory for the CTA's first and last unit, else global).
 template <int NT8>
@@ -276,7 +279,7 @@ QUASAR_DEVICE_INLINE void epilogue(const Params& p, const int4 (&v4)[Cfg<NT8>::N
   }
 #pragma unroll
   for (int h = 0; h < Cfg<NT8>::NH; ++h) {
-    const int ni = nh + 2 * h;
+    const int ni = nh + h;
     if (ni >= NT8) break;
     const int32_t v[4] = {v4[h].x, v4[h].y, v4[h].z, v4[h].w};
 #pragma unroll
@@ -319,7 +322,7 @@ QUASAR_DEVICE_INLINE void load_slots(const Params& p, int u, int mt, int nh, int
       const int4* slot = slot_ptr<NT8>(p, c0 + q <= c_hi ? c0 + q : c_hi, u, mt, nh, lane, grid);
 #pragma unroll
       for (int h = 0; h < NH; ++h)
-        v[q][h] = (c0 + q <= c_hi && nh + 2 * h < NT8) ? __ldcg(slot + 2 * h * 32) : make_int4(0, 0, 0, 0);
+        v[q][h] = (c0 + q <= c_hi && nh + h < NT8) ? __ldcg(slot + h * 32) : make_int4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -343,7 +346,7 @@ QUASAR_DEVICE_INLINE void zero_slots(const Params& p, int u, int mt, int nh, int
     int4* slot = slot_ptr<NT8>(p, cc, u, mt, nh, lane, grid);
 #pragma unroll
     for (int h = 0; h < Cfg<NT8>::NH; ++h)
-      if (nh + 2 * h < NT8) __stcg(slot + 2 * h * 32, make_int4(0, 0, 0, 0));
+      if (nh + h < NT8) __stcg(slot + h * 32, make_int4(0, 0, 0, 0));
   }
 }
 
@@ -384,19 +387,48 @@ QUASAR_DEVICE_INLINE void count_segments(const Params& p, int ua, int na, int ub
   }
 }
 
+// One K block of this warp's work: its two K steps of the unit's 64 rows
+// against every token tile.  Token operands: row n = 8 ni + g of the
+// swizzled tile sits at n * 128, chunk ch at (ch ^ (n & 7)) * 16.
 template <int NT8>
+QUASAR_DEVICE_INLINE void consume_block(uint32_t st, uint32_t a_off, uint32_t b_off, float (&acc)[UT][NT8][4]) {
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    uint32_t bq[NT8][2];
+#pragma unroll
+    for (int ni = 0; ni < NT8; ++ni)
+      s8x4_to_f16x4(lds32(st + (b_off ^ (ks << 4)) + (uint32_t)(ni * 8 * BK)), bq[ni][0], bq[ni][1]);
+#pragma unroll
+    for (int i2 = 0; i2 < UT / 2; ++i2) {
+      uint32_t d[4];
+      ldsm_x4(st + (a_off ^ (ks << 4)) + (uint32_t)(i2 * 32 * BK), d[0], d[1], d[2], d[3]);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        uint32_t a0, a1, a2, a3;
+        u8x4_to_f16x4(d[2 * i], a0, a2);       // rows g: K slots 2c.. (bytes 4c, 4c+1), 2c+8.. (4c+2, 4c+3)
+        u8x4_to_f16x4(d[2 * i + 1], a1, a3);   // rows g + 8
+#pragma unroll
+        for (int ni = 0; ni < NT8; ++ni)
+          mma_16816(acc[2 * i2 + i][ni], a0, a1, a2, a3, bq[ni][0], bq[ni][1]);
+      }
+    }
+  }
+}
+
+template <int NT8, bool RIR>
 __global__ void __launch_bounds__(THREADS, 2)
 w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
-  using C = Cfg<NT8>;
+  using C = Cfg<NT8, RIR>;
   constexpr int NH = C::NH;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;                                     // S x [W half 8 KB | X NT x 128 B]
-  float4* red = reinterpret_cast<float4*>(smem + C::S * C::STAGE);
-  int4* fin = reinterpret_cast<int4*>(smem + C::S * C::STAGE + C::RED);
-  float* sa_s = reinterpret_cast<float*>(smem + C::S * C::STAGE + C::RED + C::FIN);   // [32]
+  constexpr int RED_OWN = RIR ? 0 : C::RED;                  // bytes of a separate reduction buffer
+  float4* red = reinterpret_cast<float4*>(RIR ? stages : smem + C::S * C::STAGE);
+  int4* fin = reinterpret_cast<int4*>(smem + C::S * C::STAGE + RED_OWN);
+  float* sa_s = reinterpret_cast<float*>(smem + C::S * C::STAGE + RED_OWN + C::FIN);   // [32]
   float* sw_s = sa_s + 32;                                                                // [2][64]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::S * C::STAGE + C::RED + C::FIN + C::SCL);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::S * C::STAGE + RED_OWN + C::FIN + C::SCL);
   uint64_t* empty = full + C::S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::S);
 
@@ -466,11 +498,10 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   }
 
   // ------------------------------------------------------------------ consumers
-  const int kq = warp & (KQ - 1);   // K bytes [32 kq, 32 kq + 32) of each block
-  const int rg = warp / KQ;         // rows [32 rg, 32 rg + 32) of the unit: row tiles 2 rg, 2 rg + 1
+  const int kq = warp;              // K bytes [32 kq, 32 kq + 32) of each block, all 64 rows
   const int g = lane >> 2, c = lane & 3;
-  const int mt_f = warp >> 1;       // finalizer share: row tile mt_f, token tiles nh, nh + 2, ...
-  const int nh = warp & 1;
+  const int mt_f = warp;            // finalizer share: row tile mt_f, every token tile
+  const int nh = 0;
   pdl_wait();                       // scales and workspace belong to the previous kernel until here
   const int u_first = (sc.s1 > sc.s0) ? sc.s0 / KB : sc.w0;
   const int u_last = (sc.w1 > sc.w0) ? sc.w1 - 1 : (sc.s1 - 1) / KB;
@@ -490,26 +521,27 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     }
   }
 
-  float acc[2][NT8][4];
+  float acc[UT][NT8][4];
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
+  for (int i = 0; i < UT; ++i)
 #pragma unroll
     for (int n = 0; n < NT8; ++n)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[i][n][j] = 0.f;
   // Finished integer sums of this warp's finalizer share, kept in shared
-  // memory (touched once per run): token tile nh + 2h at share[2h * 32].
+  // memory (touched once per run): token tile h at share[h * 32].
   int4* share = fin + ((size_t)mt_f * NT8 + nh) * 32 + lane;
 #pragma unroll
   for (int h = 0; h < NH; ++h)
-    if (nh + 2 * h < NT8) share[2 * h * 32] = make_int4(0, 0, 0, 0);
+    if (nh + h < NT8) share[h * 32] = make_int4(0, 0, 0, 0);
 
-  // Per-lane address parts.  ldmatrix over one K step of the warp's 32 rows:
-  // lanes 8i..8i+7 give rows 8i..8i+7, i.e. matrix i = (row tile i >> 1, row
-  // half i & 1); rows keep their swizzle phase because units start at a
-  // multiple of 8 rows.  The second K step's chunk differs from the first in
-  // bit 0 only, i.e. its offset is the first one's ^ 16.
-  const uint32_t a_off = (uint32_t)((rg * 32 + lane) * BK + (((2 * kq) ^ (lane & 7)) << 4));
+  // Per-lane address parts.  ldmatrix over one K step of 32 rows: lanes
+  // 8i..8i+7 give rows 8i..8i+7, i.e. matrix i = (row tile i >> 1, row half
+  // i & 1); the next 32 rows are 32 * BK further.  Rows keep their swizzle
+  // phase because units start at a multiple of 8 rows.  The second K step's
+  // chunk differs from the first in bit 0 only, i.e. its offset is the first
+  // one's ^ 16.
+  const uint32_t a_off = (uint32_t)(lane * BK + (((2 * kq) ^ (lane & 7)) << 4));
   const uint32_t b_off = (uint32_t)(HALF_BYTES + g * BK + (((2 * kq) ^ g) << 4) + 4 * c);
   const uint32_t stages_u32 = smem_u32(stages);
 
@@ -529,29 +561,14 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       bad = !__all_sync(0xffffffffu, ok);
     }
     if (!bad) {
+      const uint32_t st0 = stages_u32 + (uint32_t)(r.s * C::STAGE);
+      // A full pair takes a straight-line path so that the two blocks'
+      // loads and MMAs can interleave; a segment's odd tail takes one block.
+      if (w.g == G) {
 #pragma unroll
-      for (int b = 0; b < G; ++b) {
-      if (b >= w.g) break;
-      const uint32_t st = stages_u32 + (uint32_t)(r.s * C::STAGE + b * C::BLK);
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        // Token operands (row n = 8 ni + g of the swizzled tile sits at
-        // n * 128, chunk ch at (ch ^ (n & 7)) * 16).
-        uint32_t bq[NT8][2];
-#pragma unroll
-        for (int ni = 0; ni < NT8; ++ni)
-          s8x4_to_f16x4(lds32(st + (b_off ^ (ks << 4)) + (uint32_t)(ni * 8 * BK)), bq[ni][0], bq[ni][1]);
-        uint32_t d[4];
-        ldsm_x4(st + (a_off ^ (ks << 4)), d[0], d[1], d[2], d[3]);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          uint32_t a0, a1, a2, a3;
-          u8x4_to_f16x4(d[2 * i], a0, a2);       // rows g: K slots 2c.. (bytes 4c, 4c+1), 2c+8.. (4c+2, 4c+3)
-          u8x4_to_f16x4(d[2 * i + 1], a1, a3);   // rows g + 8
-#pragma unroll
-          for (int ni = 0; ni < NT8; ++ni) mma_16816(acc[i][ni], a0, a1, a2, a3, bq[ni][0], bq[ni][1]);
-        }
-      }
+        for (int b = 0; b < G; ++b) consume_block<NT8>(st0 + (uint32_t)(b * C::BLK), a_off, b_off, acc);
+      } else {
+        consume_block<NT8>(st0, a_off, b_off, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[r.s]);
@@ -563,19 +580,19 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     // and carries the abort decision to every consumer warp.
     if (named_barrier_or(RED_BAR, CWARPS * 32, bad ? 1u : 0u)) break;
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < UT; ++i)
 #pragma unroll
       for (int ni = 0; ni < NT8; ++ni) {
-        red[(((2 * rg + i) * KQ + kq) * NT8 + ni) * 32 + lane] =
+        red[((i * KQ + kq) * NT8 + ni) * 32 + lane] =
             make_float4(acc[i][ni][0], acc[i][ni][1], acc[i][ni][2], acc[i][ni][3]);
         acc[i][ni][0] = acc[i][ni][1] = acc[i][ni][2] = acc[i][ni][3] = 0.f;
       }
     named_barrier_or(RED_BAR, CWARPS * 32, 0u);
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
-      const int ni = nh + 2 * h;
+      const int ni = nh + h;
       if (ni >= NT8) break;
-      int4 f = share[2 * h * 32];
+      int4 f = share[h * 32];
 #pragma unroll
       for (int q = 0; q < KQ; ++q) {
         const float4 v = red[((mt_f * KQ + q) * NT8 + ni) * 32 + lane];
@@ -584,7 +601,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         f.z += __float2int_rn(v.z);
         f.w += __float2int_rn(v.w);
       }
-      share[2 * h * 32] = f;
+      share[h * 32] = f;
     }
     if (!w.seg_last(KB)) continue;
 
@@ -595,7 +612,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     if (nb == KB) {
       int4 v[NH];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) v[h] = (nh + 2 * h < NT8) ? share[2 * h * 32] : make_int4(0, 0, 0, 0);
+      for (int h = 0; h < NH; ++h) v[h] = (nh + h < NT8) ? share[h * 32] : make_int4(0, 0, 0, 0);
       epilogue<NT8>(p, v, u, mt_f, nh, lane, sa_s, sw_of(u));   // the whole unit
     } else {
       // Partial segment of the split range: store the share into this CTA's
@@ -604,7 +621,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
                    ((size_t)mt_f * NT8 + nh) * 32 + lane;
 #pragma unroll
       for (int h = 0; h < NH; ++h)
-        if (nh + 2 * h < NT8) slot[2 * h * 32] = share[2 * h * 32];
+        if (nh + h < NT8) slot[h * 32] = share[h * 32];
       if (seg_ua < 0) {
         seg_ua = u;
         seg_na = nb;
@@ -622,7 +639,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     }
 #pragma unroll
     for (int h = 0; h < NH; ++h)
-      if (nh + 2 * h < NT8) share[2 * h * 32] = make_int4(0, 0, 0, 0);
+      if (nh + h < NT8) share[h * 32] = make_int4(0, 0, 0, 0);
   }
 
   if (p.mode == 1) {
@@ -639,13 +656,13 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     if (!bad && (warp % csz) == rank) {
       int4 v[NH];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) v[h] = (nh + 2 * h < NT8) ? share[2 * h * 32] : make_int4(0, 0, 0, 0);
+      for (int h = 0; h < NH; ++h) v[h] = (nh + h < NT8) ? share[h * 32] : make_int4(0, 0, 0, 0);
       for (int q = 0; q < csz; ++q) {
         if (q == rank) continue;
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          if (nh + 2 * h >= NT8) break;
-          const int4 x = ld_dsmem_int4(share + 2 * h * 32, (uint32_t)q);
+          if (nh + h >= NT8) break;
+          const int4 x = ld_dsmem_int4(share + h * 32, (uint32_t)q);
           v[h].x += x.x;
           v[h].y += x.y;
           v[h].z += x.z;
@@ -661,25 +678,25 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
 // ------------------------------------------------------------------ host side
 
-template <int NT8>
+template <int NT8, bool RIR>
 static cudaError_t configure(int dev) {
   static int configured[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(w8a8_skinny_kernel<NT8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<NT8>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(w8a8_skinny_kernel<NT8, RIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<NT8, RIR>::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   return cudaSuccess;
 }
 
-template <int NT8>
+template <int NT8, bool RIR>
 static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = Cfg<NT8>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<NT8, RIR>::SMEM;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -692,8 +709,8 @@ static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cu
   return cfg;
 }
 
-// Clusters of `csize` CTAs of this kernel that the device keeps resident at
-// once (0 if unknown); cached per device and cluster size.
+// Clusters of `csize` CTAs of the cluster-schedule kernel that the device
+// keeps resident at once (0 if unknown); cached per device and cluster size.
 template <int NT8>
 static int resident_clusters(int dev, int csize) {
   static int cache[64][9];
@@ -701,9 +718,9 @@ static int resident_clusters(int dev, int csize) {
   if (dev < 0 || dev >= 64 || csize < 2 || csize > 8) return 0;
   if (!init[dev][csize]) {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = config_of<NT8>(csize * 16, csize, nullptr, attr);
+    cudaLaunchConfig_t cfg = config_of<NT8, true>(csize * 16, csize, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, w8a8_skinny_kernel<NT8>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, w8a8_skinny_kernel<NT8, true>, &cfg) != cudaSuccess) {
       n = 0;
       cudaGetLastError();
     }
@@ -717,36 +734,36 @@ template <int NT8>
 static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaError_t e = configure<NT8>(dev);
+  cudaError_t e = configure<NT8, true>(dev);
+  if (e == cudaSuccess) e = configure<NT8, false>(dev);
   if (e != cudaSuccess) return e;
   const int n_units = (p.N + UM - 1) / UM;
   const int slots = std::min(2 * sms, MAX_CTAS);   // two CTAs per SM
   // Few units: one cluster per unit, with the most K slices that keep every
-  // cluster resident in one wave.
+  // cluster resident in one wave; each slice must be one accumulation run.
   int csize = std::min(std::min(8, slots / n_units), p.KB);
   while (csize >= 2 && resident_clusters<NT8>(dev, csize) < n_units) --csize;
-  int grid;
+  if (csize >= 2 && (p.KB + csize - 1) / csize > RUN_BLOCKS) csize = 1;
+  cudaLaunchAttribute attr[2];
   if (csize >= 2) {
     p.mode = 1;
     p.csize = csize;
     p.split_units = 0;
     p.total1 = 0;
     p.whole_per = 0;
-    grid = n_units * csize;
-  } else {
-    p.mode = 0;
-    p.csize = 1;
-    grid = slots;
-    p.whole_per = n_units / grid;
-    p.split_units = n_units - p.whole_per * grid;
-    p.total1 = p.split_units * p.KB;
-    if (p.whole_per == 0) grid = std::min(grid, p.total1);
-    if ((unsigned long long)(p.total1 + 1) * (unsigned long long)(grid + 1) >= (1ull << 32))
-      return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = config_of<NT8, true>(n_units * csize, csize, stream, attr);
+    return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, true>, tx, p);
   }
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = config_of<NT8>(grid, p.csize, stream, attr);
-  return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8>, tx, p);
+  p.mode = 0;
+  p.csize = 1;
+  int grid = slots;
+  p.whole_per = n_units / grid;
+  p.split_units = n_units - p.whole_per * grid;
+  p.total1 = p.split_units * p.KB;
+  if (p.whole_per == 0) grid = std::min(grid, p.total1);
+  if ((unsigned long long)(p.total1 + 1) * (unsigned long long)(grid + 1) >= (1ull << 32)) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = config_of<NT8, false>(grid, 1, stream, attr);
+  return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, false>, tx, p);
 }
 
 bool handles(int M) { return M >= 1 && M <= 24; }
