@@ -140,7 +140,8 @@ def test_int8_gemm_adversarial_extremes(K):
 # Larger M checks the tcgen05 kernel.
 SKINNY_SHAPES = [(1, 8, 16), (2, 1000, 4112), (7, 136, 1040), (9, 512, 256), (16, 4096, 4096),
                  (3, 12288, 256), (5, 19456, 512), (12, 24576, 1024), (20, 6144, 4096),
-                 (23, 264, 2064), (24, 6144, 4096), (31, 8, 12288), (32, 1152, 2048)]
+                 (23, 264, 2064), (24, 6144, 4096), (28, 6144, 4096), (32, 24576, 1024),
+                 (31, 8, 12288), (32, 1152, 2048)]
 
 
 @pytest.mark.parametrize("M,N,K", SKINNY_SHAPES)

@@ -97,7 +97,7 @@ struct Cfg {
   static constexpr int S = S_FIT < 12 ? S_FIT : 12;         // stages in flight
   static constexpr int SMEM = FIXED + S * STAGE;
   static_assert(BLK % 1024 == 0, "block alignment");
-  static_assert(S >= 3, "pipeline depth");
+  static_assert(S >= 2, "pipeline depth");
   static_assert(SMEM <= SMEM_CAP, "two CTAs per SM");
   static_assert(!RIR || RED <= S * STAGE, "reduction buffer fits in the ring");
 };
