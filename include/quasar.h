@@ -179,6 +179,33 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
                                    void* workspace, size_t ws_bytes,
                                    quasar_stream_t stream);
 
+/* A2 + A3 + A4 in one call: smooth + quantize the BF16 activations and run
+ * the W8A8 linear on the codes.
+ *   Y[m][n] is bit-identical to quasar_smooth_quant_act(X, smooth) followed by
+ *   quasar_w8a8_linear on its outputs (same codes, same sa, same epilogue).
+ *   X [M][ldx] BF16 (ldx >= K, ldx % 8 == 0, 16-byte aligned), smooth [K]
+ *   fp32 (16-byte aligned), Wp / sw / Y / sizes as for quasar_w8a8_linear.
+ *   For a few tokens and few weight rows (the register-path kernel's cluster
+ *   schedule with short K slices) this is a single launch: each CTA smooths
+ *   and quantizes its own K slice on chip, the CTAs of a cluster exchange
+ *   per-token partial absmax values through distributed shared memory, and
+ *   the weight stream never waits for the previous kernel.  Other shapes run
+ *   the quantizer into the workspace's scratch tail, then the linear.
+ *   workspace: >= quasar_w8a8_linear_fused_workspace_size(M, N, K) bytes;
+ *   its first quasar_w8a8_linear_workspace_size(M, N, K) bytes follow the
+ *   zero-filled contract of quasar_w8a8_linear, the rest is scratch with no
+ *   required content.  The single-launch shapes do not touch it (it may be
+ *   NULL for them).  (The pages fuse the quantizer into the pipeline only as
+ *   a per-token step before the INT8 matmul; the fusion is this library's.)
+ * ------------------------------------------------------------------------ */
+size_t quasar_w8a8_linear_fused_workspace_size(int M, int N, int K);
+quasar_status_t quasar_w8a8_linear_fused(const void* X_bf16, int ldx, const float* smooth,
+                                         const int8_t* Wp, const float* sw,
+                                         int M, int N, int K,
+                                         void* Y_bf16, int ldy,
+                                         void* workspace, size_t ws_bytes,
+                                         quasar_stream_t stream);
+
 /* A3 alone: the exact int32 accumulator acc[M][N] (row stride N) instead of
  * Y, same kernel and workspace contract.  For checking and for callers
  * with their own epilogue. */

@@ -118,3 +118,31 @@ def test_quant_and_verify_reject_bad_arguments(lib):
     assert v(FAKE, 1001, FAKE, 2, 3, 1000, 0.0, None, FAKE, None, FAKE, 1 << 20, None) == 2   # ldl % 8
     assert v(FAKE, 1000, FAKE, 2, 3, 1000, 0.0, None, FAKE, None, FAKE, 16, None) == 3        # workspace
     assert v(FAKE, 1000, FAKE, 0, 3, 1000, 0.0, None, FAKE, None, FAKE, 0, None) == 0         # B == 0
+
+
+def test_fused_linear_rejects_bad_arguments(lib):
+    f = lib.quasar_w8a8_linear_fused
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p] + \
+        [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    names = ["x", "ldx", "smooth", "wp", "sw", "M", "N", "K", "y", "ldy", "ws", "wsb", "stream"]
+    ok_args = [FAKE, 128, FAKE, FAKE, FAKE, 8, 128, 128, FAKE, 128, FAKE, 1 << 20, None]
+
+    def call(**kw):
+        a = list(ok_args)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+
+    assert call(x=None) == 1
+    assert call(smooth=None) == 1
+    assert call(M=-1) == 1
+    assert call(K=100) == 2          # K % 16
+    assert call(ldx=64) == 2         # ldx < K
+    assert call(ldx=132) == 2        # ldx % 8
+    assert call(x=FAKE_ODD) == 2     # 16-byte alignment
+    assert call(smooth=FAKE_ODD) == 2
+    assert call(M=0) == 0            # empty batch is a no-op
+    lib.quasar_w8a8_linear_fused_workspace_size.restype = ctypes.c_size_t
+    lib.quasar_w8a8_linear_workspace_size.restype = ctypes.c_size_t
+    lin = lib.quasar_w8a8_linear_workspace_size(20, 24576, 4096)
+    assert lib.quasar_w8a8_linear_fused_workspace_size(20, 24576, 4096) == lin + 20 * 4096 + 256

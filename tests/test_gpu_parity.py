@@ -335,3 +335,72 @@ def test_verify_sampled_two_level_closed_form():
         n_acc, _ = q.verify_accept(dev_bf16(lg), dev(np.array([draft], np.int32)), temperature=1.0,
                                    u=dev(np.array([u], np.float32)))
         assert int(n_acc[0]) == want
+
+
+# ---------------------------------------------------------------- A2 fused into A3 + A4
+
+def _fused_vs_two_step(x_bits, w_bits, smooth, ldx_pad=0):
+    """Y of the fused call against smooth_quant_act + w8a8_linear (bit for bit)
+    and against the oracle's identically ordered dequant (1 ulp)."""
+    M, K = x_bits.shape
+    xd = dev_bf16(x_bits)
+    if ldx_pad:
+        big = torch.zeros((M, K + ldx_pad), dtype=torch.bfloat16, device="cuda")
+        big[:, :K] = xd
+        xd = big[:, :K]
+    wq, sw = q.pack_weights(dev_bf16(w_bits), smooth)
+    ws = q.Workspace()
+    y_f = q.w8a8_linear_fused(xd, smooth, wq, sw, workspace=ws)
+    xq, sa = q.smooth_quant_act(xd, smooth)
+    y_2 = q.w8a8_linear(xq, sa, wq, sw)
+    torch.cuda.synchronize()
+    assert torch.equal(y_f.view(torch.int16), y_2.view(torch.int16)), "fused != smooth_quant_act + w8a8_linear"
+    N = sw.numel()
+    lin = int(q.lib.quasar_w8a8_linear_workspace_size(M, N, K))
+    assert int(ws.buf[:lin].count_nonzero()) == 0, "workspace counters / sums not left zero-filled"
+    s_np = smooth.cpu().numpy()
+    xq_r, sa_r = orc.smooth_quant_act(x_bits, s_np)
+    wq_r, sw_r = orc.pack_weights(w_bits, s_np)
+    y_r = orc.w8a8_linear(xq_r, sa_r, wq_r, sw_r)
+    assert bf16_ulp_distance(host_bf16_bits(y_f), y_r).max() <= BF16_ULP_TOL
+
+
+def test_fused_small_case():
+    case = synth.small_case()
+    x, w, xc = case.x(), case.w(), case.x_cal()
+    smooth = q.calibrate_smooth(dev_bf16(xc), dev_bf16(w))
+    _fused_vs_two_step(x, w, smooth)
+
+
+@pytest.mark.parametrize("maker", ["attention", "mlp"])
+def test_fused_qwen3_shapes(maker):
+    """qkv / o_proj at M = 20 take the single-launch path; gate_up (many
+    units) and down (long K slices) at M = 40 fall back to two launches."""
+    cases = synth.attention_cases() if maker == "attention" else synth.mlp_cases(M=20)
+    for case in cases:
+        x, w, xc = case.x(), case.w(), case.x_cal()
+        smooth = q.calibrate_smooth(dev_bf16(xc), dev_bf16(w))
+        _fused_vs_two_step(x, w, smooth)
+
+
+@pytest.mark.parametrize("M,N,K,pad", [(1, 4096, 4096, 0), (24, 6144, 4096, 0), (13, 1024, 1040, 8),
+                                       (5, 136, 272, 0), (9, 2048, 2048, 64)])
+def test_fused_random_shapes(M, N, K, pad):
+    rng = np.random.default_rng(M * 31 + N + K)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((M, K)) * (1 + 20 * (rng.random(K) < 0.01)))
+    w = synth.f32_to_bf16_bits(rng.standard_normal((N, K)) * 0.02)
+    smooth = dev(rng.uniform(0.25, 4.0, K).astype(np.float32))
+    _fused_vs_two_step(x, w, smooth, ldx_pad=pad)
+
+
+def test_fused_zero_token_rows():
+    """A token whose smoothed row is all zero gets absmax 0: scale 0, codes 0, Y row 0."""
+    rng = np.random.default_rng(11)
+    M, N, K = 12, 4096, 4096
+    xf = rng.standard_normal((M, K))
+    xf[3] = 0.0
+    xf[11] = 0.0
+    x = synth.f32_to_bf16_bits(xf)
+    w = synth.f32_to_bf16_bits(rng.standard_normal((N, K)) * 0.02)
+    smooth = dev(rng.uniform(0.5, 2.0, K).astype(np.float32))
+    _fused_vs_two_step(x, w, smooth)

@@ -55,6 +55,8 @@ bool handles(int M);
 size_t slots_bytes(int M, int N, int K);
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
                     void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream);
+quasar_status_t run_fused(const uint16_t* X, int ldx, const float* smooth, const int8_t* Wp, const float* sw, int M,
+                          int N, int K, void* Y, int ldy, cudaStream_t stream, bool* done);
 }  // namespace skinny
 
 namespace gemm {
@@ -646,6 +648,41 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   return cuda_status(e);
 }
 
+// ------------------------------------------------------ fused activation path
+//
+// Smooth + quantize (A2) and the linear (A3 + A4) in one call.  Shapes that
+// take the register-path kernel's cluster schedule with short K slices run
+// as one launch that quantizes the activations on chip; the others run the
+// quantizer into the workspace's scratch tail and then the linear.
+
+size_t fused_workspace_size(int M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return workspace_size(M, N, K) + align256((size_t)M * K) + align256((size_t)M * 4);
+}
+
+quasar_status_t run_fused(const void* X, int ldx, const float* smooth, const int8_t* Wp, const float* sw, int M,
+                          int N, int K, void* Y, int ldy, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (M < 0 || N <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
+  if (K % 16 != 0 || N % 8 != 0 || K > 131072) return QUASAR_ERR_UNSUPPORTED;
+  if (ldy < N || ldy % 8 != 0 || ldx < K || ldx % 8 != 0) return QUASAR_ERR_UNSUPPORTED;
+  if (M == 0) return QUASAR_OK;  // empty batch: nothing is read or written
+  if (!X || !smooth || !Wp || !sw || !Y) return QUASAR_ERR_INVALID_ARG;
+  if (!aligned(X, 16) || !aligned(smooth, 16) || !aligned(Wp, 16) || !aligned(Y, 16) || !aligned(sw, 4))
+    return QUASAR_ERR_UNSUPPORTED;
+  bool done = false;
+  const quasar_status_t st = skinny::run_fused(reinterpret_cast<const uint16_t*>(X), ldx, smooth, Wp, sw, M, N, K, Y,
+                                               ldy, stream, &done);
+  if (st != QUASAR_OK || done) return st;
+  // Two launches: codes and scales into the scratch tail, then the linear.
+  const size_t lin = workspace_size(M, N, K);
+  if (!ws || ws_bytes < fused_workspace_size(M, N, K) || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
+  int8_t* xq = reinterpret_cast<int8_t*>(ws) + lin;
+  float* sa = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + lin + align256((size_t)M * K));
+  const quasar_status_t sq = quasar_smooth_quant_act(X, ldx, smooth, M, K, xq, sa, reinterpret_cast<quasar_stream_t>(stream));
+  if (sq != QUASAR_OK) return sq;
+  return run(xq, sa, Wp, sw, M, N, K, Y, ldy, nullptr, ws, lin, stream);
+}
+
 // ---------------------------------------------------------- no-allocation path
 //
 // For callers that cannot pass a workspace.  The split-K scratch lives in a
@@ -694,6 +731,17 @@ quasar_status_t quasar_w8a8_linear_noalloc(const int8_t* Xq, const float* sa, co
 }
 
 size_t quasar_w8a8_linear_workspace_size(int M, int N, int K) { return quasar::gemm::workspace_size(M, N, K); }
+
+size_t quasar_w8a8_linear_fused_workspace_size(int M, int N, int K) {
+  return quasar::gemm::fused_workspace_size(M, N, K);
+}
+
+quasar_status_t quasar_w8a8_linear_fused(const void* X_bf16, int ldx, const float* smooth, const int8_t* Wp,
+                                         const float* sw, int M, int N, int K, void* Y_bf16, int ldy, void* workspace,
+                                         size_t ws_bytes, quasar_stream_t stream) {
+  return quasar::gemm::run_fused(X_bf16, ldx, smooth, Wp, sw, M, N, K, Y_bf16, ldy, workspace, ws_bytes,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
 
 quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M,
                                    int N, int K, void* Y_bf16, int ldy, void* workspace, size_t ws_bytes,

@@ -77,22 +77,34 @@ constexpr int G = 2;              // K blocks per pipeline stage (one handshake 
 constexpr int RUN_BLOCKS = 32;
 static_assert(RUN_BLOCKS % 2 == 0, "runs end on a stage boundary");
 
-// RIR: the run-end reduction buffer overlays the stage ring.  Only valid
-// when a CTA's single accumulation run ends after its last block (the ring
-// is then idle): the cluster schedule with K slices of <= RUN_BLOCKS blocks.
-// The space it frees becomes more stages in flight.
-template <int NT8, bool RIR = false>
+// Kernel variants (VAR):
+//  0  stream-K schedule.
+//  1  cluster schedule: the run-end reduction buffer overlays the stage
+//     ring, valid because a CTA's single accumulation run ends after its
+//     last block (the ring is then idle; K slices are <= RUN_BLOCKS blocks).
+//     The space it frees becomes more stages in flight.
+//  2  cluster schedule with the activation prologue fused in: the CTA
+//     smooths and quantizes its own K slice of the BF16 activations into a
+//     resident code region (the cluster exchanges per-token partial absmax
+//     values through distributed shared memory), so stages carry weights
+//     only and the weight stream need not wait for the previous kernel.
+constexpr int XR_BLOCKS = 16;     // variant 2: K blocks of resident activation codes per CTA
+
+template <int NT8, int VAR = 0>
 struct Cfg {
+  static constexpr bool RIR = VAR >= 1;
+  static constexpr bool FUSED = VAR == 2;
   static constexpr int NT = 8 * NT8;                        // token columns (padded to 8)
   static constexpr int NH = NT8;                            // token tiles of one finalizer share
   static constexpr int XB = NT * BK;                        // INT8 token tile of a block
-  static constexpr int BLK = HALF_BYTES + XB;               // one block: weight half + token tile
+  static constexpr int BLK = HALF_BYTES + (FUSED ? 0 : XB); // one block: weight half (+ token tile)
   static constexpr int STAGE = G * BLK;                     // multiple of 1024 (swizzle atoms)
   static constexpr int RED = UT * KQ * NT8 * 32 * 16;       // fp32 partials: [row tile][kq][token tile][lane]
   static constexpr int FIN = UT * NT8 * 32 * 16;            // int32 run sums: [row tile][token tile][lane]
   static constexpr int SLOT = UT * NT8 * 32;                // int4 per partial-sum slot (64 rows x NT)
-  static constexpr int SCL = 1024;                          // staged scales: sa[32], sw of 2 units
-  static constexpr int FIXED = 1024 + (RIR ? 0 : RED) + FIN + SCL + 256;
+  static constexpr int SCL = 1024;                          // staged scales: sa[32], sw[2][64], inv[32], amax[32]
+  static constexpr int XR = FUSED ? XR_BLOCKS * XB : 0;     // resident activation codes (variant 2)
+  static constexpr int FIXED = 1024 + (RIR ? 0 : RED) + FIN + SCL + XR + 256;
   static constexpr int S_FIT = (SMEM_CAP - FIXED) / STAGE;
   static constexpr int S = S_FIT < 12 ? S_FIT : 12;         // stages in flight
   static constexpr int SMEM = FIXED + S * STAGE;
@@ -104,6 +116,9 @@ struct Cfg {
 
 struct Params {
   const uint8_t* wp;  // packed weights, [n_tiles][KB][128 rows][128 B]
+  const uint16_t* x;  // variant 2: BF16 activations [M][ldx]
+  int ldx;
+  const float* smooth;  // variant 2: smoothing factors [K]
   const float* sa;
   const float* sw;
   int M, N, K;
@@ -253,6 +268,36 @@ QUASAR_DEVICE_INLINE int4 ld_dsmem_int4(const void* local, uint32_t rank) {
   return v;
 }
 
+// 32-bit word at the same shared-memory offset in cluster CTA `rank`.
+QUASAR_DEVICE_INLINE uint32_t ld_dsmem_u32(const void* local, uint32_t rank) {
+  uint32_t remote, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// Eight BF16 values (one 16-byte load) -> fp32.
+QUASAR_DEVICE_INLINE void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Smoothed activations x' = fp32(x) * smooth (correctly rounded) for the 8
+// consecutive elements k..k+7 of token m.
+QUASAR_DEVICE_INLINE void smoothed8(const Params& p, int m, int k, float (&x)[8]) {
+  const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * p.ldx + k));
+  const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.smooth + k));
+  const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.smooth + k) + 1);
+  bf16x8_to_f32(raw, x);
+  const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], sv[i]);
+}
+
 // D += A (16 x 16, fp16, row) * B (16 x 8, fp16, col), fp32 accumulate.
 QUASAR_DEVICE_INLINE void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                     uint32_t b1) {
@@ -388,20 +433,22 @@ QUASAR_DEVICE_INLINE void count_segments(const Params& p, int ua, int na, int ub
 }
 
 // One K block of this warp's work: its two K steps of the unit's 64 rows
-// against every token tile.  Token operands: row n = 8 ni + g of the
-// swizzled tile sits at n * 128, chunk ch at (ch ^ (n & 7)) * 16.
+// (weight half at wst) against every token tile (token tile at xst).  Token
+// operands: row n = 8 ni + g of the swizzled tile sits at n * 128, chunk ch
+// at (ch ^ (n & 7)) * 16.
 template <int NT8>
-QUASAR_DEVICE_INLINE void consume_block(uint32_t st, uint32_t a_off, uint32_t b_off, float (&acc)[UT][NT8][4]) {
+QUASAR_DEVICE_INLINE void consume_block(uint32_t wst, uint32_t xst, uint32_t a_off, uint32_t b_off,
+                                        float (&acc)[UT][NT8][4]) {
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     uint32_t bq[NT8][2];
 #pragma unroll
     for (int ni = 0; ni < NT8; ++ni)
-      s8x4_to_f16x4(lds32(st + (b_off ^ (ks << 4)) + (uint32_t)(ni * 8 * BK)), bq[ni][0], bq[ni][1]);
+      s8x4_to_f16x4(lds32(xst + (b_off ^ (ks << 4)) + (uint32_t)(ni * 8 * BK)), bq[ni][0], bq[ni][1]);
 #pragma unroll
     for (int i2 = 0; i2 < UT / 2; ++i2) {
       uint32_t d[4];
-      ldsm_x4(st + (a_off ^ (ks << 4)) + (uint32_t)(i2 * 32 * BK), d[0], d[1], d[2], d[3]);
+      ldsm_x4(wst + (a_off ^ (ks << 4)) + (uint32_t)(i2 * 32 * BK), d[0], d[1], d[2], d[3]);
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         uint32_t a0, a1, a2, a3;
@@ -415,10 +462,11 @@ QUASAR_DEVICE_INLINE void consume_block(uint32_t st, uint32_t a_off, uint32_t b_
   }
 }
 
-template <int NT8, bool RIR>
+template <int NT8, int VAR>
 __global__ void __launch_bounds__(THREADS, 2)
 w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
-  using C = Cfg<NT8, RIR>;
+  using C = Cfg<NT8, VAR>;
+  constexpr bool RIR = C::RIR, FUSED = C::FUSED;
   constexpr int NH = C::NH;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -428,7 +476,10 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   int4* fin = reinterpret_cast<int4*>(smem + C::S * C::STAGE + RED_OWN);
   float* sa_s = reinterpret_cast<float*>(smem + C::S * C::STAGE + RED_OWN + C::FIN);   // [32]
   float* sw_s = sa_s + 32;                                                                // [2][64]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::S * C::STAGE + RED_OWN + C::FIN + C::SCL);
+  float* inv_s = sw_s + 2 * UM;                                                           // [32] variant 2
+  unsigned int* amax_s = reinterpret_cast<unsigned int*>(inv_s + 32);                     // [32] variant 2
+  uint8_t* xr = smem + C::S * C::STAGE + RED_OWN + C::FIN + C::SCL;                       // variant 2 codes
+  uint64_t* full = reinterpret_cast<uint64_t*>(xr + C::XR);
   uint64_t* empty = full + C::S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::S);
 
@@ -445,7 +496,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == PRODUCER_WARP && lane == 0) prefetch_tmap(&tmX);
+  if (!FUSED && warp == PRODUCER_WARP && lane == 0) prefetch_tmap(&tmX);
   __syncthreads();
 
   const int grid = (int)gridDim.x;
@@ -453,21 +504,25 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   const Sched sc = schedule_of((int)blockIdx.x, grid, p);
 
   if (warp == PRODUCER_WARP) {
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
+    // Weights do not depend on the previous kernel: fill every stage first.
+    int pre = 0;
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
-      // Weights do not depend on the previous kernel: fill every stage first.
-      int pre = 0;
-      {
-        Walk w(sc, KB);
-        for (; pre < C::S && w.more(); ++pre, w.next(KB)) {
-          mbar_arrive_expect_tx(&full[pre], (uint32_t)(w.g * C::BLK));
-          for (int b = 0; b < w.g; ++b)
-            bulk_load(stages + pre * C::STAGE + b * C::BLK, unit_block(p, w.u, w.kb + b), HALF_BYTES, &full[pre],
-                      pol_w);
-        }
+      Walk w(sc, KB);
+      for (; pre < C::S && w.more(); ++pre, w.next(KB)) {
+        mbar_arrive_expect_tx(&full[pre], (uint32_t)(w.g * C::BLK));
+        for (int b = 0; b < w.g; ++b)
+          bulk_load(stages + pre * C::STAGE + b * C::BLK, unit_block(p, w.u, w.kb + b), HALF_BYTES, &full[pre],
+                    pol_w);
       }
-      pdl_wait();  // token codes come from the previous kernel
+    }
+    __syncwarp();
+    if (FUSED) cluster_sync_all();   // the consumers' prologue barrier (partial absmax exchange)
+    if (lane == 0) {
+      // Token codes come from the previous kernel (variants 0 and 1); the
+      // fused variant streams weights only and never reads its outputs.
+      if (!FUSED) pdl_wait();
       Walk w(sc, KB);
       Ring<C::S> rg;
       int issued = 0;
@@ -479,8 +534,9 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
           for (int b = 0; b < w.g; ++b)
             bulk_load(st + b * C::BLK, unit_block(p, w.u, w.kb + b), HALF_BYTES, &full[rg.s], pol_w);
         }
-        for (int b = 0; b < w.g; ++b)
-          tma_load_2d(st + b * C::BLK + HALF_BYTES, &tmX, (w.kb + b) * BK, 0, &full[rg.s], pol_x);
+        if (!FUSED)
+          for (int b = 0; b < w.g; ++b)
+            tma_load_2d(st + b * C::BLK + HALF_BYTES, &tmX, (w.kb + b) * BK, 0, &full[rg.s], pol_x);
       }
       // Never leave with copies in flight.
       for (int s = 0; s < C::S && s < issued; ++s) {
@@ -490,7 +546,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       }
     }
     __syncwarp();
-    if (p.mode == 1) {   // the consumers' two cluster barriers
+    if (p.mode == 1) {   // the consumers' two cluster barriers at the end
       cluster_sync_all();
       cluster_sync_all();
     }
@@ -512,13 +568,74 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   if (!p.acc_out) {
     for (int i = threadIdx.x; i < 32 + 2 * UM; i += CWARPS * 32) {
       if (i < 32) {
-        sa_s[i] = (i < p.M) ? __ldg(&p.sa[i]) : 0.f;
+        if (!FUSED) sa_s[i] = (i < p.M) ? __ldg(&p.sa[i]) : 0.f;
       } else {
         const int r = i - 32;
         const int n = (r < UM ? u_first : u_last) * UM + (r & (UM - 1));
         sw_s[r] = (n < p.N) ? __ldg(&p.sw[n]) : 0.f;
       }
     }
+  }
+
+  // Variant 2: smooth and quantize this CTA's K slice of the activations
+  // into the resident code region, with the same fp32 steps as the
+  // stand-alone quantizer: x' = x * smooth, a = max |x'| over the whole row,
+  // code = clamp(rne(x' * (127 / a)), -127, 127), sa = a / 127 (0 if a = 0).
+  const int kbs0 = sc.s0 % KB;      // first K block of the slice (cluster schedule: a single unit)
+  const uint32_t xr_u32 = smem_u32(xr);
+  if (FUSED) {
+    const int nblk = sc.s1 - sc.s0;   // <= XR_BLOCKS (host)
+    const int k0 = kbs0 * BK;
+    const int k1 = min(p.K, (kbs0 + nblk) * BK);
+    const int nvec = (k1 - k0) / 8;
+    for (int i = threadIdx.x; i < nblk * C::XB / 16; i += CWARPS * 32)
+      reinterpret_cast<uint4*>(xr)[i] = make_uint4(0u, 0u, 0u, 0u);   // token rows >= M, K beyond the matrix
+    // Pass 1: this slice's absmax of every token (one warp per token).
+    for (int m = warp; m < p.M; m += CWARPS) {
+      float a = 0.f;
+      for (int v = lane; v < nvec; v += 32) {
+        float x[8];
+        smoothed8(p, m, k0 + 8 * v, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      if (lane == 0) amax_s[m] = __float_as_uint(a);
+    }
+    // Exchange the slices' partial absmax values across the cluster (the
+    // producer warp takes part in this barrier too).
+    __syncwarp();
+    cluster_sync_all();
+    if (threadIdx.x < p.M) {
+      float a = 0.f;
+      for (int q = 0; q < p.csize; ++q) a = fmaxf(a, __uint_as_float(ld_dsmem_u32(&amax_s[threadIdx.x], (uint32_t)q)));
+      inv_s[threadIdx.x] = a > 0.f ? __fdiv_rn(127.f, a) : 0.f;
+      sa_s[threadIdx.x] = a > 0.f ? __fdiv_rn(a, 127.f) : 0.f;
+    }
+    named_barrier_or(RED_BAR, CWARPS * 32, 0u);
+    // Pass 2: codes, in the token-tile layout the main loop reads (block j
+    // of the slice at j * XB; row m at m * 128, 16-byte chunk c at
+    // (c ^ (m & 7)) * 16).
+    for (int m = warp; m < p.M; m += CWARPS) {
+      const float inv = inv_s[m];
+      if (inv == 0.f) continue;   // all-zero token: codes stay 0
+      for (int v = lane; v < nvec; v += 32) {
+        float x[8];
+        smoothed8(p, m, k0 + 8 * v, x);
+        uint32_t w2[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          int q = __float2int_rn(__fmul_rn(x[i], inv));
+          q = max(-127, min(127, q));
+          w2[i >> 2] |= (uint32_t)(q & 0xFF) << (8 * (i & 3));
+        }
+        const int kk = 8 * v, ch = (kk & 127) >> 4;
+        *reinterpret_cast<uint2*>(xr + (kk >> 7) * C::XB + m * BK + ((ch ^ (m & 7)) << 4) + (kk & 8)) =
+            make_uint2(w2[0], w2[1]);
+      }
+    }
+    named_barrier_or(RED_BAR, CWARPS * 32, 0u);
   }
 
   float acc[UT][NT8][4];
@@ -542,7 +659,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   // chunk differs from the first in bit 0 only, i.e. its offset is the first
   // one's ^ 16.
   const uint32_t a_off = (uint32_t)(lane * BK + (((2 * kq) ^ (lane & 7)) << 4));
-  const uint32_t b_off = (uint32_t)(HALF_BYTES + g * BK + (((2 * kq) ^ g) << 4) + 4 * c);
+  const uint32_t b_off = (uint32_t)(g * BK + (((2 * kq) ^ g) << 4) + 4 * c);
   const uint32_t stages_u32 = smem_u32(stages);
 
   bool bad = false;
@@ -562,13 +679,18 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     }
     if (!bad) {
       const uint32_t st0 = stages_u32 + (uint32_t)(r.s * C::STAGE);
+      // Token tile of block b of the stage: in the stage after the weight
+      // half, or (variant 2) in the resident code region.
+      auto xst = [&](int b) -> uint32_t {
+        return FUSED ? xr_u32 + (uint32_t)((w.kb + b - kbs0) * C::XB) : st0 + (uint32_t)(b * C::BLK + HALF_BYTES);
+      };
       // A full pair takes a straight-line path so that the two blocks'
       // loads and MMAs can interleave; a segment's odd tail takes one block.
       if (w.g == G) {
 #pragma unroll
-        for (int b = 0; b < G; ++b) consume_block<NT8>(st0 + (uint32_t)(b * C::BLK), a_off, b_off, acc);
+        for (int b = 0; b < G; ++b) consume_block<NT8>(st0 + (uint32_t)(b * C::BLK), xst(b), a_off, b_off, acc);
       } else {
-        consume_block<NT8>(st0, a_off, b_off, acc);
+        consume_block<NT8>(st0, xst(0), a_off, b_off, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[r.s]);
@@ -678,25 +800,25 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
 // ------------------------------------------------------------------ host side
 
-template <int NT8, bool RIR>
+template <int NT8, int VAR>
 static cudaError_t configure(int dev) {
   static int configured[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(w8a8_skinny_kernel<NT8, RIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<NT8, RIR>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(w8a8_skinny_kernel<NT8, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<NT8, VAR>::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   return cudaSuccess;
 }
 
-template <int NT8, bool RIR>
+template <int NT8, int VAR>
 static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = Cfg<NT8, RIR>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<NT8, VAR>::SMEM;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -709,18 +831,18 @@ static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cu
   return cfg;
 }
 
-// Clusters of `csize` CTAs of the cluster-schedule kernel that the device
+// Clusters of `csize` CTAs of a cluster-schedule variant that the device
 // keeps resident at once (0 if unknown); cached per device and cluster size.
-template <int NT8>
+template <int NT8, int VAR>
 static int resident_clusters(int dev, int csize) {
   static int cache[64][9];
   static bool init[64][9] = {};
   if (dev < 0 || dev >= 64 || csize < 2 || csize > 8) return 0;
   if (!init[dev][csize]) {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = config_of<NT8, true>(csize * 16, csize, nullptr, attr);
+    cudaLaunchConfig_t cfg = config_of<NT8, VAR>(csize * 16, csize, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, w8a8_skinny_kernel<NT8, true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, w8a8_skinny_kernel<NT8, VAR>, &cfg) != cudaSuccess) {
       n = 0;
       cudaGetLastError();
     }
@@ -730,40 +852,71 @@ static int resident_clusters(int dev, int csize) {
   return cache[dev][csize];
 }
 
+// Cluster size for the cluster schedule of variant VAR (>= 2), or 0 if the
+// shape does not fit it: every cluster resident in one wave, each K slice a
+// single accumulation run and, for the fused variant, at most XR_BLOCKS
+// blocks.
+template <int NT8, int VAR>
+static int cluster_size_for(int dev, int sms, int N, int KB) {
+  const int n_units = (N + UM - 1) / UM;
+  const int slots = std::min(2 * sms, MAX_CTAS);   // two CTAs per SM
+  const int max_slice = VAR == 2 ? XR_BLOCKS : RUN_BLOCKS;
+  int csize = std::min(std::min(8, slots / n_units), KB);
+  while (csize >= 2 && resident_clusters<NT8, VAR>(dev, csize) < n_units) --csize;
+  if (csize >= 2 && (KB + csize - 1) / csize > max_slice) return 0;
+  return csize >= 2 ? csize : 0;
+}
+
 template <int NT8>
 static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaError_t e = configure<NT8, true>(dev);
-  if (e == cudaSuccess) e = configure<NT8, false>(dev);
+  cudaError_t e = configure<NT8, 1>(dev);
+  if (e == cudaSuccess) e = configure<NT8, 0>(dev);
   if (e != cudaSuccess) return e;
   const int n_units = (p.N + UM - 1) / UM;
-  const int slots = std::min(2 * sms, MAX_CTAS);   // two CTAs per SM
-  // Few units: one cluster per unit, with the most K slices that keep every
-  // cluster resident in one wave; each slice must be one accumulation run.
-  int csize = std::min(std::min(8, slots / n_units), p.KB);
-  while (csize >= 2 && resident_clusters<NT8>(dev, csize) < n_units) --csize;
-  if (csize >= 2 && (p.KB + csize - 1) / csize > RUN_BLOCKS) csize = 1;
+  const int csize = cluster_size_for<NT8, 1>(dev, sms, p.N, p.KB);
   cudaLaunchAttribute attr[2];
   if (csize >= 2) {
+    // Few units: one cluster per unit, each CTA one K slice.
     p.mode = 1;
     p.csize = csize;
     p.split_units = 0;
     p.total1 = 0;
     p.whole_per = 0;
-    cudaLaunchConfig_t cfg = config_of<NT8, true>(n_units * csize, csize, stream, attr);
-    return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, true>, tx, p);
+    cudaLaunchConfig_t cfg = config_of<NT8, 1>(n_units * csize, csize, stream, attr);
+    return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, 1>, tx, p);
   }
   p.mode = 0;
   p.csize = 1;
-  int grid = slots;
+  int grid = std::min(2 * sms, MAX_CTAS);
   p.whole_per = n_units / grid;
   p.split_units = n_units - p.whole_per * grid;
   p.total1 = p.split_units * p.KB;
   if (p.whole_per == 0) grid = std::min(grid, p.total1);
   if ((unsigned long long)(p.total1 + 1) * (unsigned long long)(grid + 1) >= (1ull << 32)) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = config_of<NT8, false>(grid, 1, stream, attr);
-  return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, false>, tx, p);
+  cudaLaunchConfig_t cfg = config_of<NT8, 0>(grid, 1, stream, attr);
+  return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, 0>, tx, p);
+}
+
+template <int NT8>
+static cudaError_t launch_fused(Params p, int sms, cudaStream_t stream, bool* fits) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t e = configure<NT8, 2>(dev);
+  if (e != cudaSuccess) return e;
+  const int csize = cluster_size_for<NT8, 2>(dev, sms, p.N, p.KB);
+  *fits = csize >= 2;
+  if (!*fits) return cudaSuccess;
+  p.mode = 1;
+  p.csize = csize;
+  p.split_units = 0;
+  p.total1 = 0;
+  p.whole_per = 0;
+  CUtensorMap unused = {};   // the fused variant reads the activations directly
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = config_of<NT8, 2>(((p.N + UM - 1) / UM) * csize, csize, stream, attr);
+  return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, 2>, unused, p);
 }
 
 bool handles(int M) { return M >= 1 && M <= 24; }
@@ -810,6 +963,44 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
     default: e = launch<3>(tx, p, sms, stream); break;   // handles() keeps M <= 24
   }
   if (e == cudaErrorInvalidValue) return QUASAR_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
+// Smooth + quantize + linear in one launch (variant 2) when the shape takes
+// the cluster schedule with K slices of <= XR_BLOCKS blocks; *done = false
+// (nothing launched) otherwise.  Arguments were validated by the caller.
+quasar_status_t run_fused(const uint16_t* X, int ldx, const float* smooth, const int8_t* Wp, const float* sw, int M,
+                          int N, int K, void* Y, int ldy, cudaStream_t stream, bool* done) {
+  *done = false;
+  if (!handles(M)) return QUASAR_OK;
+  Params p = {};
+  p.wp = reinterpret_cast<const uint8_t*>(Wp);
+  p.x = X;
+  p.ldx = ldx;
+  p.smooth = smooth;
+  p.sa = nullptr;
+  p.sw = sw;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.KB = (K + BK - 1) / BK;
+  p.Y = reinterpret_cast<__nv_bfloat16*>(Y);
+  p.ldy = ldy;
+  p.acc_out = nullptr;
+  p.slots = nullptr;
+  p.ws_cnt = nullptr;
+  p.err = device_error_word();
+  p.limit_ns = wait_limit_ns();
+  if (!p.err) return QUASAR_ERR_CUDA;
+  const int sms = sm_count();
+  if (sms <= 0) return QUASAR_ERR_CUDA;
+  const int nt8 = (M + 7) / 8;
+  cudaError_t e;
+  switch (nt8) {
+    case 1: e = launch_fused<1>(p, sms, stream, done); break;
+    case 2: e = launch_fused<2>(p, sms, stream, done); break;
+    default: e = launch_fused<3>(p, sms, stream, done); break;   // handles() keeps M <= 24
+  }
   return cuda_status(e);
 }
 

@@ -40,6 +40,8 @@ _SIGS = {
     "quasar_smooth_quant_act": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
     "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
+    "quasar_w8a8_linear_fused_workspace_size": (_sz, [_i, _i, _i]),
+    "quasar_w8a8_linear_fused": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_int8_gemm_s32": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "quasar_w8a8_linear_noalloc": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p]),
     "quasar_verify_accept_workspace_size": (_sz, [_i, _i, _i]),
@@ -201,6 +203,24 @@ def w8a8_linear(xq, sa, wp, sw, y=None, workspace: Workspace | None = None, stre
     buf = ws.get(need)
     _check(lib.quasar_w8a8_linear(_ptr(xq), _ptr(sa), _ptr(wp), _ptr(sw), M, N, K, _ptr(y), ldy, _ptr(buf),
                                   buf.numel(), _stream(stream)), "w8a8_linear")
+    return y
+
+
+def w8a8_linear_fused(x, smooth, wp, sw, y=None, workspace: Workspace | None = None, stream=None):
+    """Y bf16 [M][N] = w8a8_linear(*smooth_quant_act(x, smooth), wp, sw), bit-identical, in one call
+    (one launch for the shapes whose K slices the kernel can quantize on chip)."""
+    _need(x, torch.bfloat16, "x")
+    _need(smooth, torch.float32, "smooth")
+    ldx = _rowmajor(x, "x")
+    M, K = x.shape
+    N = sw.numel()
+    _check_packed(wp, N, K)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if y is None else y
+    ldy = _rowmajor(y, "y")
+    ws = _ws(workspace, x.device)
+    buf = ws.get(int(lib.quasar_w8a8_linear_fused_workspace_size(M, N, K)))
+    _check(lib.quasar_w8a8_linear_fused(_ptr(x), ldx, _ptr(smooth), _ptr(wp), _ptr(sw), M, N, K, _ptr(y), ldy,
+                                        _ptr(buf), buf.numel(), _stream(stream)), "w8a8_linear_fused")
     return y
 
 
