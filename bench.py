@@ -1,14 +1,16 @@
 """Benchmark of the W8A8 verify path on GB300.
 
 Headline workload (one "step"): the Qwen3-8B-shaped attention projections of
-a verification pass, M = 4 sequences x (4 drafts + 1) = 20 tokens:
-    smooth+quantize X -> fused qkv W8A8 linear (4096 -> 6144)
-    smooth+quantize X' -> o_proj W8A8 linear (4096 -> 4096)
+a verification pass, M = 4 sequences x (4 drafts + 1) = 20 tokens, each one
+call of the fused entry (smooth + per-token quantize + W8A8 linear; at this
+M the library runs it as a quantize launch and a linear launch):
+    X  -> qkv W8A8 linear (4096 -> 6144)
+    X' -> o_proj W8A8 linear (4096 -> 4096)
 Metric: TB/s of INT8 weight bytes streamed per second (weights + per-channel
 scales), whole job.  Weights rotate through enough packed copies that the
 working set is several times the 129 MB L2 (cold L2 every step).
 
-Also reported: the roofline object for the dominant kernel (the fused GEMM),
+Also reported: the roofline object for the dominant kernel (the qkv linear),
 an end-to-end number through the public API with host buffers, SM clocks
 sampled during the timed region, the CPU oracle as a baseline, an M sweep
 over the four decoder-layer linears with a BF16 cuBLAS GEMM of the same shape
@@ -67,6 +69,12 @@ def weight_bytes(N: int, K: int) -> int:
 def linear_bytes(M: int, N: int, K: int) -> int:
     """All algorithmic bytes of one fused linear launch: Wq, sw, Xq, sa, Y."""
     return N * K + 4 * N + M * K + 4 * M + 2 * M * N
+
+
+def fused_linear_bytes(M: int, N: int, K: int) -> int:
+    """All algorithmic bytes of one fused smooth+quantize+linear launch:
+    Wq, sw, BF16 X, smooth, Y (the codes never leave the chip)."""
+    return N * K + 4 * N + 2 * M * K + 4 * K + 2 * M * N
 
 
 def copies_for_cold_l2(bytes_per_set: int, factor: int = 4) -> int:
@@ -273,15 +281,14 @@ def main_gpu(args):
         l["wq_copies"] = [l["wq"]] + [l["wq"].clone() for _ in range(ncopy - 1)]
         l["sw_copies"] = [l["sw"]] + [l["sw"].clone() for _ in range(ncopy - 1)]
     ws = q.Workspace(dev)
-    ws.get(max(q.lib.quasar_w8a8_linear_workspace_size(l["case"].M, l["case"].N, l["case"].K) for l in lin))
+    ws.get(max(q.lib.quasar_w8a8_linear_fused_workspace_size(l["case"].M, l["case"].N, l["case"].K) for l in lin))
 
     def step(i):
         for l in lin:
-            q.smooth_quant_act(l["x"], l["smooth"], xq=l["xq"], sa=l["sa"])
-            q.w8a8_linear(l["xq"], l["sa"], l["wq_copies"][i % ncopy], l["sw_copies"][i % ncopy], y=l["y"],
-                          workspace=ws)
+            q.w8a8_linear_fused(l["x"], l["smooth"], l["wq_copies"][i % ncopy], l["sw_copies"][i % ncopy],
+                                y=l["y"], workspace=ws)
 
-    launches_per_step = 2 * len(lin)
+    launches_per_step = sum(q.w8a8_linear_fused_launches(l["case"].M, l["case"].N, l["case"].K) for l in lin)
 
     # ---- warm-up (eager), then capture graphs of the step sequence
     with torch.cuda.stream(stream):
@@ -335,15 +342,20 @@ def main_gpu(args):
         ms_max = ms
     value = wb_step * args.steps * world / (ms_max / 1e3) / 1e12
 
-    # ---- roofline: the dominant kernel (fused qkv GEMM) timed alone, cold L2
+    # ---- roofline: the dominant kernel (the qkv linear) timed alone, cold L2
     qkv = lin[0]
     c = qkv["case"]
+    single = q.w8a8_linear_fused_launches(c.M, c.N, c.K) == 1
     nk = 400
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(nk):
-            q.w8a8_linear(qkv["xq"], qkv["sa"], qkv["wq_copies"][i % ncopy], qkv["sw_copies"][i % ncopy],
-                          y=qkv["y"], workspace=ws)
+            if single:
+                q.w8a8_linear_fused(qkv["x"], qkv["smooth"], qkv["wq_copies"][i % ncopy],
+                                    qkv["sw_copies"][i % ncopy], y=qkv["y"], workspace=ws)
+            else:
+                q.w8a8_linear(qkv["xq"], qkv["sa"], qkv["wq_copies"][i % ncopy], qkv["sw_copies"][i % ncopy],
+                              y=qkv["y"], workspace=ws)
     with torch.cuda.stream(stream):
         g.replay()
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -352,14 +364,15 @@ def main_gpu(args):
         k1.record(stream)
     stream.synchronize()
     gemm_us = k0.elapsed_time(k1) * 1e3 / nk
-    alg = linear_bytes(c.M, c.N, c.K)
+    alg = fused_linear_bytes(c.M, c.N, c.K) if single else linear_bytes(c.M, c.N, c.K)
     hbm, bf16, src = load_peaks()
     achieved = alg / (gemm_us * 1e-6) / 1e9
-    traffic = profiled_traffic()
+    traffic = None if single else profiled_traffic()
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic,
-                "kernel": (f"{'w8a8_skinny_kernel' if c.M <= SKINNY_MAX_M else 'w8a8_linear_kernel'} "
-                           f"qkv M={c.M} N={c.N} K={c.K}"),
+                "kernel": (("w8a8_skinny_kernel (fused smooth+quantize prologue)" if single else
+                            "w8a8_skinny_kernel" if c.M <= SKINNY_MAX_M else "w8a8_linear_kernel")
+                           + f" qkv M={c.M} N={c.N} K={c.K}"),
                 "launch_us": gemm_us, "algorithmic_bytes_per_launch": alg,
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s"}
 
@@ -374,9 +387,8 @@ def main_gpu(args):
     def e2e_step(i):
         for hx, dx, hy, l in zip(host_x, dev_x, host_y, lin):
             dx.copy_(hx, non_blocking=True)
-            q.smooth_quant_act(dx, l["smooth"], xq=l["xq"], sa=l["sa"])
-            q.w8a8_linear(l["xq"], l["sa"], l["wq_copies"][i % ncopy], l["sw_copies"][i % ncopy], y=l["y"],
-                          workspace=ws)
+            q.w8a8_linear_fused(dx, l["smooth"], l["wq_copies"][i % ncopy], l["sw_copies"][i % ncopy], y=l["y"],
+                                workspace=ws)
             hy.copy_(l["y"], non_blocking=True)
 
     with torch.cuda.stream(stream):

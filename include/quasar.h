@@ -191,6 +191,8 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
  *   per-token partial absmax values through distributed shared memory, and
  *   the weight stream never waits for the previous kernel.  Other shapes run
  *   the quantizer into the workspace's scratch tail, then the linear.
+ *   Like Wp in quasar_w8a8_linear, `smooth` may be read before the previous
+ *   kernel on `stream` has finished: it must not be written by that kernel.
  *   workspace: >= quasar_w8a8_linear_fused_workspace_size(M, N, K) bytes;
  *   its first quasar_w8a8_linear_workspace_size(M, N, K) bytes follow the
  *   zero-filled contract of quasar_w8a8_linear, the rest is scratch with no
@@ -199,6 +201,11 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
  *   a per-token step before the INT8 matmul; the fusion is this library's.)
  * ------------------------------------------------------------------------ */
 size_t quasar_w8a8_linear_fused_workspace_size(int M, int N, int K);
+/* Kernel launches quasar_w8a8_linear_fused makes for (M, N, K) on the
+ * calling thread's current device: 0 for M <= 0, 1 for the single-launch
+ * shapes, 2 otherwise; -1 if the CUDA runtime fails to answer.  The answer
+ * depends on the device (cluster residency), not on the pointers. */
+int quasar_w8a8_linear_fused_launches(int M, int N, int K);
 quasar_status_t quasar_w8a8_linear_fused(const void* X_bf16, int ldx, const float* smooth,
                                          const int8_t* Wp, const float* sw,
                                          int M, int N, int K,

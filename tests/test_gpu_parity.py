@@ -372,19 +372,24 @@ def test_fused_small_case():
     _fused_vs_two_step(x, w, smooth)
 
 
-@pytest.mark.parametrize("maker", ["attention", "mlp"])
-def test_fused_qwen3_shapes(maker):
-    """qkv / o_proj at M = 20 take the single-launch path; gate_up (many
-    units) and down (long K slices) at M = 40 fall back to two launches."""
-    cases = synth.attention_cases() if maker == "attention" else synth.mlp_cases(M=20)
+@pytest.mark.parametrize("maker,M,want", [("attention", 2, 1), ("attention", 1, 1), ("attention", 20, 2),
+                                           ("attention", 8, 2), ("mlp", 2, 2), ("mlp", 20, 2)])
+def test_fused_qwen3_shapes(maker, M, want):
+    """qkv / o_proj at M <= 2 take the single launch; larger M and the MLP
+    linears (gate_up: more units than one wave of clusters; down at M = 2:
+    K slices too long) fall back to quantize + linear."""
+    cases = synth.attention_cases(M=M) if maker == "attention" else synth.mlp_cases(M=M)
     for case in cases:
+        assert q.w8a8_linear_fused_launches(case.M, case.N, case.K) == want, case.name
         x, w, xc = case.x(), case.w(), case.x_cal()
         smooth = q.calibrate_smooth(dev_bf16(xc), dev_bf16(w))
         _fused_vs_two_step(x, w, smooth)
 
 
 @pytest.mark.parametrize("M,N,K,pad", [(1, 4096, 4096, 0), (24, 6144, 4096, 0), (13, 1024, 1040, 8),
-                                       (5, 136, 272, 0), (9, 2048, 2048, 64)])
+                                       (5, 136, 272, 0), (9, 2048, 2048, 64), (3, 2048, 2064, 24),
+                                       (8, 6144, 4096, 0), (7, 512, 16, 0), (2, 12288, 4096, 0),
+                                       (2, 1024, 1040, 8), (1, 4096, 12288, 0), (2, 136, 2064, 0)])
 def test_fused_random_shapes(M, N, K, pad):
     rng = np.random.default_rng(M * 31 + N + K)
     x = synth.f32_to_bf16_bits(rng.standard_normal((M, K)) * (1 + 20 * (rng.random(K) < 0.01)))
@@ -393,13 +398,15 @@ def test_fused_random_shapes(M, N, K, pad):
     _fused_vs_two_step(x, w, smooth, ldx_pad=pad)
 
 
-def test_fused_zero_token_rows():
+@pytest.mark.parametrize("M", [2, 12])
+def test_fused_zero_token_rows(M):
     """A token whose smoothed row is all zero gets absmax 0: scale 0, codes 0, Y row 0."""
     rng = np.random.default_rng(11)
-    M, N, K = 12, 4096, 4096
+    N, K = 4096, 4096
     xf = rng.standard_normal((M, K))
-    xf[3] = 0.0
-    xf[11] = 0.0
+    xf[M - 1] = 0.0
+    if M > 4:
+        xf[3] = 0.0
     x = synth.f32_to_bf16_bits(xf)
     w = synth.f32_to_bf16_bits(rng.standard_normal((N, K)) * 0.02)
     smooth = dev(rng.uniform(0.5, 2.0, K).astype(np.float32))

@@ -57,6 +57,7 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
                     void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream);
 quasar_status_t run_fused(const uint16_t* X, int ldx, const float* smooth, const int8_t* Wp, const float* sw, int M,
                           int N, int K, void* Y, int ldy, cudaStream_t stream, bool* done);
+int fused_fits(int M, int N, int K);
 }  // namespace skinny
 
 namespace gemm {
@@ -734,6 +735,12 @@ size_t quasar_w8a8_linear_workspace_size(int M, int N, int K) { return quasar::g
 
 size_t quasar_w8a8_linear_fused_workspace_size(int M, int N, int K) {
   return quasar::gemm::fused_workspace_size(M, N, K);
+}
+
+int quasar_w8a8_linear_fused_launches(int M, int N, int K) {
+  if (M <= 0) return 0;
+  const int f = quasar::skinny::fused_fits(M, N, K);
+  return f < 0 ? -1 : (f ? 1 : 2);
 }
 
 quasar_status_t quasar_w8a8_linear_fused(const void* X_bf16, int ldx, const float* smooth, const int8_t* Wp,

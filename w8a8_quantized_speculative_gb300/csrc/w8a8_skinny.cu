@@ -88,12 +88,19 @@ static_assert(RUN_BLOCKS % 2 == 0, "runs end on a stage boundary");
 //     resident code region (the cluster exchanges per-token partial absmax
 //     values through distributed shared memory), so stages carry weights
 //     only and the weight stream need not wait for the previous kernel.
-constexpr int XR_BLOCKS = 16;     // variant 2: K blocks of resident activation codes per CTA
+// Variant 2 (one token tile, M <= 8) shared-memory region XR, for a K
+// slice of nblk blocks: the INT8 codes in the token-tile layout the main
+// loop reads (block j at j * XB), then the slice's BF16 activations
+// ([block][token][128 values]), then its smoothing factors.
+__host__ __device__ __forceinline__ int fused_slice_bytes(int nblk, int M, int XB) {
+  return nblk * (XB + M * 256 + 128 * 4);
+}
 
 template <int NT8, int VAR = 0>
 struct Cfg {
   static constexpr bool RIR = VAR >= 1;
   static constexpr bool FUSED = VAR == 2;
+  static_assert(!FUSED || NT8 == 1, "the fused variant is built for one token tile");
   static constexpr int NT = 8 * NT8;                        // token columns (padded to 8)
   static constexpr int NH = NT8;                            // token tiles of one finalizer share
   static constexpr int XB = NT * BK;                        // INT8 token tile of a block
@@ -102,11 +109,15 @@ struct Cfg {
   static constexpr int RED = UT * KQ * NT8 * 32 * 16;       // fp32 partials: [row tile][kq][token tile][lane]
   static constexpr int FIN = UT * NT8 * 32 * 16;            // int32 run sums: [row tile][token tile][lane]
   static constexpr int SLOT = UT * NT8 * 32;                // int4 per partial-sum slot (64 rows x NT)
-  static constexpr int SCL = 1024;                          // staged scales: sa[32], sw[2][64], inv[32], amax[32]
-  static constexpr int XR = FUSED ? XR_BLOCKS * XB : 0;     // resident activation codes (variant 2)
-  static constexpr int FIXED = 1024 + (RIR ? 0 : RED) + FIN + SCL + XR + 256;
-  static constexpr int S_FIT = (SMEM_CAP - FIXED) / STAGE;
-  static constexpr int S = S_FIT < 12 ? S_FIT : 12;         // stages in flight
+  // Staged scales: sa[32], sw[2][64], inv[32], and (variant 2) the cluster's
+  // partial absmax values amax[rank][32].
+  static constexpr int SCL = FUSED ? 2048 : 1024;
+  static constexpr int BASE = 1024 + (RIR ? 0 : RED) + FIN + SCL + 256;
+  static constexpr int S_FIT = (SMEM_CAP - BASE) / STAGE;
+  // Variant 2 keeps four stages and gives the rest to the activation region.
+  static constexpr int S = FUSED ? 4 : (S_FIT < 12 ? S_FIT : 12);   // stages in flight
+  static constexpr int XR = FUSED ? ((SMEM_CAP - BASE - S * STAGE) & ~1023) : 0;
+  static constexpr int FIXED = BASE + XR;
   static constexpr int SMEM = FIXED + S * STAGE;
   static_assert(BLK % 1024 == 0, "block alignment");
   static_assert(S >= 2, "pipeline depth");
@@ -276,6 +287,13 @@ QUASAR_DEVICE_INLINE uint32_t ld_dsmem_u32(const void* local, uint32_t rank) {
   return v;
 }
 
+// Store a 32-bit word at the same shared-memory offset in cluster CTA `rank`.
+QUASAR_DEVICE_INLINE void st_dsmem_f32(void* local, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
 // Eight BF16 values (one 16-byte load) -> fp32.
 QUASAR_DEVICE_INLINE void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -286,17 +304,42 @@ QUASAR_DEVICE_INLINE void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
-// Smoothed activations x' = fp32(x) * smooth (correctly rounded) for the 8
-// consecutive elements k..k+7 of token m.
-QUASAR_DEVICE_INLINE void smoothed8(const Params& p, int m, int k, float (&x)[8]) {
-  const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * p.ldx + k));
-  const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.smooth + k));
-  const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.smooth + k) + 1);
+// Smoothed activations x' = fp32(x) * smooth (correctly rounded) of 8
+// consecutive elements, from their raw BF16 bits and smoothing factors.
+QUASAR_DEVICE_INLINE void smooth8(const uint4& raw, const float (&s)[8], float (&x)[8]) {
   bf16x8_to_f32(raw, x);
-  const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], sv[i]);
+  for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], s[i]);
 }
+
+QUASAR_DEVICE_INLINE void lds_smooth8(const float* p, float (&s)[8]) {
+  const float4 s0 = reinterpret_cast<const float4*>(p)[0];
+  const float4 s1 = reinterpret_cast<const float4*>(p)[1];
+  s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
+  s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+}
+
+// Codes of 8 smoothed activations: rne(x' * inv) as int8, packed.  Adding
+// 1.5 * 2^23 to the (separately rounded) product rounds it to the nearest
+// integer, ties to even, and leaves that integer's two's-complement low byte
+// in the low byte of the sum's bits.  No clamp is needed: |x'| <= absmax, so
+// |x' * inv| < 127.5 and the result is within [-127, 127]; a NaN product (an
+// infinite absmax) gives byte 0, as the convert-and-clamp form does.
+QUASAR_DEVICE_INLINE uint2 quant8(const uint4& raw, const float (&s)[8], float inv) {
+  float x[8];
+  smooth8(raw, s, x);
+  uint32_t b[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) b[i] = __float_as_uint(__fadd_rn(__fmul_rn(x[i], inv), 12582912.f));
+  return make_uint2(__byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410),
+                    __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410));
+}
+
+QUASAR_DEVICE_INLINE void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+
+QUASAR_DEVICE_INLINE void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // D += A (16 x 16, fp16, row) * B (16 x 8, fp16, col), fp32 accumulate.
 QUASAR_DEVICE_INLINE void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -477,8 +520,8 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   float* sa_s = reinterpret_cast<float*>(smem + C::S * C::STAGE + RED_OWN + C::FIN);   // [32]
   float* sw_s = sa_s + 32;                                                                // [2][64]
   float* inv_s = sw_s + 2 * UM;                                                           // [32] variant 2
-  unsigned int* amax_s = reinterpret_cast<unsigned int*>(inv_s + 32);                     // [32] variant 2
-  uint8_t* xr = smem + C::S * C::STAGE + RED_OWN + C::FIN + C::SCL;                       // variant 2 codes
+  float* amax_s = inv_s + 32;                                                             // [8][32] variant 2
+  uint8_t* xr = smem + C::S * C::STAGE + RED_OWN + C::FIN + C::SCL;                       // variant 2 region
   uint64_t* full = reinterpret_cast<uint64_t*>(xr + C::XR);
   uint64_t* empty = full + C::S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::S);
@@ -558,6 +601,17 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   const int g = lane >> 2, c = lane & 3;
   const int mt_f = warp;            // finalizer share: row tile mt_f, every token tile
   const int nh = 0;
+  // Variant 2: the CTA's K slice (blocks kbs0 .. kbs0 + nblk - 1 of its unit)
+  // and its parts of XR (the host checks that they fit).
+  const int kbs0 = sc.s0 % KB;      // first K block of the slice (cluster schedule: a single unit)
+  const int nblk = sc.s1 - sc.s0;
+  uint8_t* xs = xr + nblk * C::XB;                                        // activations [j][m][256 B]
+  float* smo = reinterpret_cast<float*>(xs + (FUSED ? nblk * p.M * 256 : 0));   // smoothing factors
+  if (FUSED) {
+    // Model parameters, like the weights: read before the previous kernel ends.
+    const int n16 = (min(p.K, (kbs0 + nblk) * BK) - kbs0 * BK) / 4;
+    for (int i = threadIdx.x; i < n16; i += CWARPS * 32) cp_async16(smo + 4 * i, p.smooth + kbs0 * BK + 4 * i);
+  }
   pdl_wait();                       // scales and workspace belong to the previous kernel until here
   const int u_first = (sc.s1 > sc.s0) ? sc.s0 / KB : sc.w0;
   const int u_last = (sc.w1 > sc.w0) ? sc.w1 - 1 : (sc.s1 - 1) / KB;
@@ -578,64 +632,80 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   }
 
   // Variant 2: smooth and quantize this CTA's K slice of the activations
-  // into the resident code region, with the same fp32 steps as the
-  // stand-alone quantizer: x' = x * smooth, a = max |x'| over the whole row,
-  // code = clamp(rne(x' * (127 / a)), -127, 127), sa = a / 127 (0 if a = 0).
-  const int kbs0 = sc.s0 % KB;      // first K block of the slice (cluster schedule: a single unit)
+  // into the code region, with the same fp32 steps as the stand-alone
+  // quantizer: x' = x * smooth, a = max |x'| over the whole row,
+  // code = rne(x' * (127 / a)) (clamped to [-127, 127]), sa = a / 127 (0 if
+  // a = 0).  Work item it = (j * M + m) * 16 + vv is 16-byte column vv of
+  // token m in block j, so a half warp shares one (j, m).
   const uint32_t xr_u32 = smem_u32(xr);
   if (FUSED) {
-    const int nblk = sc.s1 - sc.s0;   // <= XR_BLOCKS (host)
+    constexpr int PT = CWARPS * 32;   // prologue threads
     const int k0 = kbs0 * BK;
-    const int k1 = min(p.K, (kbs0 + nblk) * BK);
-    const int nvec = (k1 - k0) / 8;
-    for (int i = threadIdx.x; i < nblk * C::XB / 16; i += CWARPS * 32)
-      reinterpret_cast<uint4*>(xr)[i] = make_uint4(0u, 0u, 0u, 0u);   // token rows >= M, K beyond the matrix
-    // Pass 1: this slice's absmax of every token (one warp per token).
-    for (int m = warp; m < p.M; m += CWARPS) {
+    const int nvec = (min(p.K, (kbs0 + nblk) * BK) - k0) / 8;   // 8-element vectors of a token's slice
+    const int tid = threadIdx.x;
+    const int total = nblk * p.M * 16;
+    unsigned int* amax_l = reinterpret_cast<unsigned int*>(inv_s);   // this slice's absmax bits, until pass 2
+    for (int i = tid; i < nblk * C::XB / 16; i += PT)
+      reinterpret_cast<uint4*>(xr)[i] = make_uint4(0u, 0u, 0u, 0u);   // rows >= M, columns beyond the slice
+    if (tid < 32) amax_l[tid] = 0u;
+    // Every activation vector of the slice, in flight at once.
+    for (int m = 0; m < p.M; ++m) {
+      const uint16_t* src = p.x + (size_t)m * p.ldx + k0;
+      for (int v = tid; v < nvec; v += PT) cp_async16(xs + ((v >> 4) * p.M + m) * 256 + (v & 15) * 16, src + 8 * v);
+    }
+    cp_async_wait_all();              // this thread's activations and smoothing factors
+    named_barrier_or(RED_BAR, PT, 0u);
+    // Pass 1: partial absmax of every token over this slice.  The loop is
+    // uniform per warp so that the half-warp reduction has all lanes.  The
+    // maxima are never NaN (fmaxf from 0 drops NaN), so an unsigned max of
+    // the bit patterns is the float max.
+    for (int base = tid & ~31; base < total; base += PT) {
+      const int it = base + lane;
+      const int rest = it >> 4, vv = it & 15;
+      const int j = rest / p.M, m = rest - j * p.M;
+      const int v = 16 * j + vv;
       float a = 0.f;
-      for (int v = lane; v < nvec; v += 32) {
-        float x[8];
-        smoothed8(p, m, k0 + 8 * v, x);
+      if (it < total && v < nvec) {
+        float sv[8], x[8];
+        lds_smooth8(smo + 8 * v, sv);
+        smooth8(*reinterpret_cast<const uint4*>(xs + rest * 256 + vv * 16), sv, x);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
+        for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(x[e]));
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-      if (lane == 0) amax_s[m] = __float_as_uint(a);
+      for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      if (it < total && vv == 0) atomicMax(&amax_l[m], __float_as_uint(a));
     }
-    // Exchange the slices' partial absmax values across the cluster (the
-    // producer warp takes part in this barrier too).
+    named_barrier_or(RED_BAR, PT, 0u);
+    // Push this slice's maxima into every cluster CTA's amax[this rank][m];
+    // the cluster barrier orders those stores before the reads below (the
+    // producer warp takes part in it too).
+    const uint32_t rank = (uint32_t)((int)blockIdx.x % p.csize);
+    if (tid < p.M)
+      for (int q = 0; q < p.csize; ++q) st_dsmem_f32(&amax_s[rank * 32 + tid], (uint32_t)q, __uint_as_float(amax_l[tid]));
     __syncwarp();
     cluster_sync_all();
-    if (threadIdx.x < p.M) {
-      float a = 0.f;
-      for (int q = 0; q < p.csize; ++q) a = fmaxf(a, __uint_as_float(ld_dsmem_u32(&amax_s[threadIdx.x], (uint32_t)q)));
-      inv_s[threadIdx.x] = a > 0.f ? __fdiv_rn(127.f, a) : 0.f;
-      sa_s[threadIdx.x] = a > 0.f ? __fdiv_rn(a, 127.f) : 0.f;
+    if (tid < p.M) {
+      float am = 0.f;
+      for (int q = 0; q < p.csize; ++q) am = fmaxf(am, amax_s[q * 32 + tid]);
+      inv_s[tid] = am > 0.f ? __fdiv_rn(127.f, am) : 0.f;
+      sa_s[tid] = am > 0.f ? __fdiv_rn(am, 127.f) : 0.f;
     }
-    named_barrier_or(RED_BAR, CWARPS * 32, 0u);
-    // Pass 2: codes, in the token-tile layout the main loop reads (block j
-    // of the slice at j * XB; row m at m * 128, 16-byte chunk c at
-    // (c ^ (m & 7)) * 16).
-    for (int m = warp; m < p.M; m += CWARPS) {
-      const float inv = inv_s[m];
-      if (inv == 0.f) continue;   // all-zero token: codes stay 0
-      for (int v = lane; v < nvec; v += 32) {
-        float x[8];
-        smoothed8(p, m, k0 + 8 * v, x);
-        uint32_t w2[2] = {0u, 0u};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          int q = __float2int_rn(__fmul_rn(x[i], inv));
-          q = max(-127, min(127, q));
-          w2[i >> 2] |= (uint32_t)(q & 0xFF) << (8 * (i & 3));
-        }
-        const int kk = 8 * v, ch = (kk & 127) >> 4;
-        *reinterpret_cast<uint2*>(xr + (kk >> 7) * C::XB + m * BK + ((ch ^ (m & 7)) << 4) + (kk & 8)) =
-            make_uint2(w2[0], w2[1]);
+    named_barrier_or(RED_BAR, PT, 0u);
+    // Pass 2: codes (block j at j * XB; token m at m * 128, 16-byte chunk c
+    // at (c ^ (m & 7)) * 16).
+    for (int it = tid; it < total; it += PT) {
+      const int rest = it >> 4, vv = it & 15;
+      const int j = rest / p.M, m = rest - j * p.M;
+      const int v = 16 * j + vv;
+      if (v < nvec) {
+        float sv[8];
+        lds_smooth8(smo + 8 * v, sv);
+        const uint2 code = quant8(*reinterpret_cast<const uint4*>(xs + rest * 256 + vv * 16), sv, inv_s[m]);
+        *reinterpret_cast<uint2*>(xr + j * C::XB + m * BK + (((vv >> 1) ^ (m & 7)) << 4) + 8 * (vv & 1)) = code;
       }
     }
-    named_barrier_or(RED_BAR, CWARPS * 32, 0u);
+    named_barrier_or(RED_BAR, PT, 0u);
   }
 
   float acc[UT][NT8][4];
@@ -853,14 +923,13 @@ static int resident_clusters(int dev, int csize) {
 }
 
 // Cluster size for the cluster schedule of variant VAR (>= 2), or 0 if the
-// shape does not fit it: every cluster resident in one wave, each K slice a
-// single accumulation run and, for the fused variant, at most XR_BLOCKS
-// blocks.
+// shape does not fit it: every cluster resident in one wave and each K slice
+// a single accumulation run of at most `max_slice` blocks.
 template <int NT8, int VAR>
-static int cluster_size_for(int dev, int sms, int N, int KB) {
+static int cluster_size_for(int dev, int sms, int N, int KB, int max_slice = RUN_BLOCKS) {
   const int n_units = (N + UM - 1) / UM;
   const int slots = std::min(2 * sms, MAX_CTAS);   // two CTAs per SM
-  const int max_slice = VAR == 2 ? XR_BLOCKS : RUN_BLOCKS;
+  max_slice = std::min(max_slice, RUN_BLOCKS);
   int csize = std::min(std::min(8, slots / n_units), KB);
   while (csize >= 2 && resident_clusters<NT8, VAR>(dev, csize) < n_units) --csize;
   if (csize >= 2 && (KB + csize - 1) / csize > max_slice) return 0;
@@ -899,13 +968,22 @@ static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t
   return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, 0>, tx, p);
 }
 
+// Longest K slice (blocks) whose BF16 activations fit variant 2's region.
+template <int NT8>
+static int fused_max_slice(int M) {
+  using C = Cfg<NT8, 2>;
+  int n = RUN_BLOCKS;
+  while (n > 0 && fused_slice_bytes(n, M, C::XB) > C::XR) --n;
+  return n;
+}
+
 template <int NT8>
 static cudaError_t launch_fused(Params p, int sms, cudaStream_t stream, bool* fits) {
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t e = configure<NT8, 2>(dev);
   if (e != cudaSuccess) return e;
-  const int csize = cluster_size_for<NT8, 2>(dev, sms, p.N, p.KB);
+  const int csize = cluster_size_for<NT8, 2>(dev, sms, p.N, p.KB, fused_max_slice<NT8>(p.M));
   *fits = csize >= 2;
   if (!*fits) return cudaSuccess;
   p.mode = 1;
@@ -920,6 +998,28 @@ static cudaError_t launch_fused(Params p, int sms, cudaStream_t stream, bool* fi
 }
 
 bool handles(int M) { return M >= 1 && M <= 24; }
+
+template <int NT8>
+static int fused_fits(int M, int N, int K) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || configure<NT8, 2>(dev) != cudaSuccess) return -1;
+  const int sms = sm_count();
+  if (sms <= 0) return -1;
+  return cluster_size_for<NT8, 2>(dev, sms, N, (K + BK - 1) / BK, fused_max_slice<NT8>(M)) >= 2 ? 1 : 0;
+}
+
+// 1 if run_fused covers (M, N, K) with its single launch on the current
+// device, 0 if it leaves the shape to the two-launch path, -1 on a CUDA error.
+// Tokens up to which run_fused takes its single launch.  Every cluster
+// smooths and quantizes all of X for its own unit, so the prologue grows
+// with M; measured on GB300 for the Qwen3-8B linears it beats a quantize
+// launch plus the linear at M = 1 and draws level at M = 2.
+constexpr int FUSED_MAX_M = 2;
+
+int fused_fits(int M, int N, int K) {
+  if (M < 1 || M > FUSED_MAX_M) return 0;
+  return fused_fits<1>(M, N, K);
+}
 
 // Partial-sum slots this kernel may need after the counters: two per CTA,
 // each 64 rows x NT int32.  Like the counters they are zero between calls
@@ -967,12 +1067,12 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
 }
 
 // Smooth + quantize + linear in one launch (variant 2) when the shape takes
-// the cluster schedule with K slices of <= XR_BLOCKS blocks; *done = false
-// (nothing launched) otherwise.  Arguments were validated by the caller.
+// the cluster schedule with K slices whose activations fit the region XR;
+// *done = false (nothing launched) otherwise.  Arguments were validated by the caller.
 quasar_status_t run_fused(const uint16_t* X, int ldx, const float* smooth, const int8_t* Wp, const float* sw, int M,
                           int N, int K, void* Y, int ldy, cudaStream_t stream, bool* done) {
   *done = false;
-  if (!handles(M)) return QUASAR_OK;
+  if (M < 1 || M > FUSED_MAX_M) return QUASAR_OK;
   Params p = {};
   p.wp = reinterpret_cast<const uint8_t*>(Wp);
   p.x = X;
@@ -994,14 +1094,7 @@ quasar_status_t run_fused(const uint16_t* X, int ldx, const float* smooth, const
   if (!p.err) return QUASAR_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return QUASAR_ERR_CUDA;
-  const int nt8 = (M + 7) / 8;
-  cudaError_t e;
-  switch (nt8) {
-    case 1: e = launch_fused<1>(p, sms, stream, done); break;
-    case 2: e = launch_fused<2>(p, sms, stream, done); break;
-    default: e = launch_fused<3>(p, sms, stream, done); break;   // handles() keeps M <= 24
-  }
-  return cuda_status(e);
+  return cuda_status(launch_fused<1>(p, sms, stream, done));
 }
 
 }  // namespace skinny

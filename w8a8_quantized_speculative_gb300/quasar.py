@@ -41,6 +41,7 @@ _SIGS = {
     "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_w8a8_linear_fused_workspace_size": (_sz, [_i, _i, _i]),
+    "quasar_w8a8_linear_fused_launches": (_i, [_i, _i, _i]),
     "quasar_w8a8_linear_fused": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_int8_gemm_s32": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "quasar_w8a8_linear_noalloc": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p]),
@@ -222,6 +223,14 @@ def w8a8_linear_fused(x, smooth, wp, sw, y=None, workspace: Workspace | None = N
     _check(lib.quasar_w8a8_linear_fused(_ptr(x), ldx, _ptr(smooth), _ptr(wp), _ptr(sw), M, N, K, _ptr(y), ldy,
                                         _ptr(buf), buf.numel(), _stream(stream)), "w8a8_linear_fused")
     return y
+
+
+def w8a8_linear_fused_launches(M: int, N: int, K: int) -> int:
+    """Kernel launches w8a8_linear_fused makes for this shape on the current device (1 or 2; 0 if M == 0)."""
+    n = int(lib.quasar_w8a8_linear_fused_launches(M, N, K))
+    if n < 0:
+        raise QuasarError(4, "w8a8_linear_fused_launches")
+    return n
 
 
 def int8_gemm_s32(xq, wp, N: int, acc=None, workspace: Workspace | None = None, stream=None):
