@@ -2,8 +2,7 @@
 
 Headline workload (one "step"): the Qwen3-8B-shaped attention projections of
 a verification pass, M = 4 sequences x (4 drafts + 1) = 20 tokens, each one
-call of the fused entry (smooth + per-token quantize + W8A8 linear; at this
-M the library runs it as a quantize launch and a linear launch):
+call of the fused entry (smooth + per-token quantize, then the W8A8 linear):
     X  -> qkv W8A8 linear (4096 -> 6144)
     X' -> o_proj W8A8 linear (4096 -> 4096)
 Metric: TB/s of INT8 weight bytes streamed per second (weights + per-channel
@@ -69,12 +68,6 @@ def weight_bytes(N: int, K: int) -> int:
 def linear_bytes(M: int, N: int, K: int) -> int:
     """All algorithmic bytes of one fused linear launch: Wq, sw, Xq, sa, Y."""
     return N * K + 4 * N + M * K + 4 * M + 2 * M * N
-
-
-def fused_linear_bytes(M: int, N: int, K: int) -> int:
-    """All algorithmic bytes of one fused smooth+quantize+linear launch:
-    Wq, sw, BF16 X, smooth, Y (the codes never leave the chip)."""
-    return N * K + 4 * N + 2 * M * K + 4 * K + 2 * M * N
 
 
 def copies_for_cold_l2(bytes_per_set: int, factor: int = 4) -> int:
@@ -288,7 +281,7 @@ def main_gpu(args):
             q.w8a8_linear_fused(l["x"], l["smooth"], l["wq_copies"][i % ncopy], l["sw_copies"][i % ncopy],
                                 y=l["y"], workspace=ws)
 
-    launches_per_step = sum(q.w8a8_linear_fused_launches(l["case"].M, l["case"].N, l["case"].K) for l in lin)
+    launches_per_step = 2 * len(lin)   # each fused call: the quantizer, then the linear
 
     # ---- warm-up (eager), then capture graphs of the step sequence
     with torch.cuda.stream(stream):
@@ -345,17 +338,12 @@ def main_gpu(args):
     # ---- roofline: the dominant kernel (the qkv linear) timed alone, cold L2
     qkv = lin[0]
     c = qkv["case"]
-    single = q.w8a8_linear_fused_launches(c.M, c.N, c.K) == 1
     nk = 400
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(nk):
-            if single:
-                q.w8a8_linear_fused(qkv["x"], qkv["smooth"], qkv["wq_copies"][i % ncopy],
-                                    qkv["sw_copies"][i % ncopy], y=qkv["y"], workspace=ws)
-            else:
-                q.w8a8_linear(qkv["xq"], qkv["sa"], qkv["wq_copies"][i % ncopy], qkv["sw_copies"][i % ncopy],
-                              y=qkv["y"], workspace=ws)
+            q.w8a8_linear(qkv["xq"], qkv["sa"], qkv["wq_copies"][i % ncopy], qkv["sw_copies"][i % ncopy],
+                          y=qkv["y"], workspace=ws)
     with torch.cuda.stream(stream):
         g.replay()
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -364,15 +352,14 @@ def main_gpu(args):
         k1.record(stream)
     stream.synchronize()
     gemm_us = k0.elapsed_time(k1) * 1e3 / nk
-    alg = fused_linear_bytes(c.M, c.N, c.K) if single else linear_bytes(c.M, c.N, c.K)
+    alg = linear_bytes(c.M, c.N, c.K)
     hbm, bf16, src = load_peaks()
     achieved = alg / (gemm_us * 1e-6) / 1e9
-    traffic = None if single else profiled_traffic()
+    traffic = profiled_traffic()
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic,
-                "kernel": (("w8a8_skinny_kernel (fused smooth+quantize prologue)" if single else
-                            "w8a8_skinny_kernel" if c.M <= SKINNY_MAX_M else "w8a8_linear_kernel")
-                           + f" qkv M={c.M} N={c.N} K={c.K}"),
+                "kernel": (f"{'w8a8_skinny_kernel' if c.M <= SKINNY_MAX_M else 'w8a8_linear_kernel'} "
+                           f"qkv M={c.M} N={c.N} K={c.K}"),
                 "launch_us": gemm_us, "algorithmic_bytes_per_launch": alg,
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s"}
 

@@ -182,30 +182,17 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
 /* A2 + A3 + A4 in one call: smooth + quantize the BF16 activations and run
  * the W8A8 linear on the codes.
  *   Y[m][n] is bit-identical to quasar_smooth_quant_act(X, smooth) followed by
- *   quasar_w8a8_linear on its outputs (same codes, same sa, same epilogue).
+ *   quasar_w8a8_linear on its outputs (same codes, same sa, same epilogue);
+ *   it is those two launches, with the codes and scales kept in the
+ *   workspace instead of caller buffers.
  *   X [M][ldx] BF16 (ldx >= K, ldx % 8 == 0, 16-byte aligned), smooth [K]
  *   fp32 (16-byte aligned), Wp / sw / Y / sizes as for quasar_w8a8_linear.
- *   For a few tokens and few weight rows (the register-path kernel's cluster
- *   schedule with short K slices) this is a single launch: each CTA smooths
- *   and quantizes its own K slice on chip, the CTAs of a cluster exchange
- *   per-token partial absmax values through distributed shared memory, and
- *   the weight stream never waits for the previous kernel.  Other shapes run
- *   the quantizer into the workspace's scratch tail, then the linear.
- *   Like Wp in quasar_w8a8_linear, `smooth` may be read before the previous
- *   kernel on `stream` has finished: it must not be written by that kernel.
  *   workspace: >= quasar_w8a8_linear_fused_workspace_size(M, N, K) bytes;
  *   its first quasar_w8a8_linear_workspace_size(M, N, K) bytes follow the
  *   zero-filled contract of quasar_w8a8_linear, the rest is scratch with no
- *   required content.  The single-launch shapes do not touch it (it may be
- *   NULL for them).  (The pages fuse the quantizer into the pipeline only as
- *   a per-token step before the INT8 matmul; the fusion is this library's.)
+ *   required content.
  * ------------------------------------------------------------------------ */
 size_t quasar_w8a8_linear_fused_workspace_size(int M, int N, int K);
-/* Kernel launches quasar_w8a8_linear_fused makes for (M, N, K) on the
- * calling thread's current device: 0 for M <= 0, 1 for the single-launch
- * shapes, 2 otherwise; -1 if the CUDA runtime fails to answer.  The answer
- * depends on the device (cluster residency), not on the pointers. */
-int quasar_w8a8_linear_fused_launches(int M, int N, int K);
 quasar_status_t quasar_w8a8_linear_fused(const void* X_bf16, int ldx, const float* smooth,
                                          const int8_t* Wp, const float* sw,
                                          int M, int N, int K,

@@ -51,6 +51,3 @@ def test_aggregate_and_cold_l2_helpers():
     assert t == 4.0 and v == pytest.approx(300.0 / 0.004)
     assert bench.copies_for_cold_l2(42 * 2**20) * 42 * 2**20 >= 4 * bench.L2_BYTES
     assert bench.linear_bytes(20, 6144, 4096) == 6144 * 4096 + 4 * 6144 + 20 * 4096 + 80 + 2 * 20 * 6144
-    # the fused call reads BF16 X and smooth instead of the codes and sa
-    assert bench.fused_linear_bytes(20, 6144, 4096) == 6144 * 4096 + 4 * 6144 + 2 * 20 * 4096 + 4 * 4096 \
-        + 2 * 20 * 6144

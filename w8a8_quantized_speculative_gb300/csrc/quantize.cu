@@ -10,9 +10,10 @@
 //   q[k]  = clamp(rne(v[k] * (127 / a)), -127, 127)
 // in fp32 with IEEE rounding (division and multiply correctly rounded, no
 // contraction).  One CTA per row: 128-bit loads of 8 BF16 values, warp-shuffle
-// absmax, then a second pass that re-derives v (bit-identical) and stores
-// 8 codes per 64-bit store.  Rows are short (<= 24 KB) and the second pass
-// is served from L1/L2.
+// absmax, then a second pass that stores 8 codes per 64-bit store.  Activation
+// rows of up to 12288 values keep the whole row in registers (one memory
+// round trip); longer rows and the weights re-derive v in the second pass
+// (bit-identical), served from L1/L2.
 //
 // Activation codes are written row-major [M][K].  Weight codes are written in
 // the packed layout the W8A8 linear streams: 128 x 128 blocks, tile-major,
@@ -117,6 +118,75 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const uint16_t* __r
   }
 }
 
+// Activation rows of up to THREADS * 8 * VPT values: every load of the row
+// (and of its smoothing factors) is issued before any is used, both passes
+// run from registers, so a row costs one memory round trip.  This matters
+// on the verification path: the quantizer runs while the next linear's
+// weight stream already fills the memory system, and each dependent round
+// trip then waits behind it.  Same arithmetic as quant_rows_kernel<false,
+// false>.
+template <int VPT>
+__global__ void __launch_bounds__(THREADS) quant_act_kernel(const uint16_t* __restrict__ in, int ld,
+                                                            const float* __restrict__ smooth, int K,
+                                                            int8_t* __restrict__ q, float* __restrict__ scale) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int row = blockIdx.x;
+  const uint16_t* src = in + (size_t)row * ld;
+  const int nvec = K / 8;
+  uint4 raw[VPT];
+  float4 sm[2 * VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * THREADS;
+    if (v < nvec) {
+      raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+      sm[2 * i] = __ldg(reinterpret_cast<const float4*>(smooth) + 2 * v);
+      sm[2 * i + 1] = __ldg(reinterpret_cast<const float4*>(smooth) + 2 * v + 1);
+    }
+  }
+  float x[VPT][8];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * THREADS;
+    bf16x8_to_f32(raw[i], x[i]);
+    const float s[8] = {sm[2 * i].x, sm[2 * i].y, sm[2 * i].z, sm[2 * i].w,
+                        sm[2 * i + 1].x, sm[2 * i + 1].y, sm[2 * i + 1].z, sm[2 * i + 1].w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      x[i][e] = __fmul_rn(x[i][e], s[e]);
+      if (v < nvec) amax = fmaxf(amax, fabsf(x[i][e]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[THREADS / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < THREADS / 32; ++w) amax = fmaxf(amax, red[w]);
+  const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
+  if (threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
+  int8_t* dst = q + (size_t)row * K;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * THREADS;
+    if (v >= nvec) continue;
+    uint32_t packed[2] = {0u, 0u};
+    if (amax > 0.f) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        int c = __float2int_rn(__fmul_rn(x[i][e], inv));
+        c = max(-127, min(127, c));
+        packed[e >> 2] |= (uint32_t)(c & 0xFF) << (8 * (e & 3));
+      }
+    }
+    reinterpret_cast<uint2*>(dst)[v] = make_uint2(packed[0], packed[1]);
+  }
+}
+
 // Row-major INT8 codes [N][K] -> packed layout, 16 bytes per thread.
 __global__ void tile_weights_kernel(const int8_t* __restrict__ src, int N, int K, int8_t* __restrict__ dst) {
   const int chunks = K / 16;
@@ -160,8 +230,11 @@ static quasar_status_t run(const void* in, int ld, const float* smooth, int rows
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, quant_rows_kernel<DIVIDE, PACKED>,
-                                        reinterpret_cast<const uint16_t*>(in), ld, smooth, K, q, scale));
+  const uint16_t* x = reinterpret_cast<const uint16_t*>(in);
+  const int vpt = (K / 8 + THREADS - 1) / THREADS;   // 8-value vectors per thread
+  if (!DIVIDE && vpt <= 2) return cuda_status(cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, x, ld, smooth, K, q, scale));
+  if (!DIVIDE && vpt <= 6) return cuda_status(cudaLaunchKernelEx(&cfg, quant_act_kernel<6>, x, ld, smooth, K, q, scale));
+  return cuda_status(cudaLaunchKernelEx(&cfg, quant_rows_kernel<DIVIDE, PACKED>, x, ld, smooth, K, q, scale));
 }
 
 }  // namespace quant

@@ -55,9 +55,6 @@ bool handles(int M);
 size_t slots_bytes(int M, int N, int K);
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
                     void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream);
-quasar_status_t run_fused(const uint16_t* X, int ldx, const float* smooth, const int8_t* Wp, const float* sw, int M,
-                          int N, int K, void* Y, int ldy, cudaStream_t stream, bool* done);
-int fused_fits(int M, int N, int K);
 }  // namespace skinny
 
 namespace gemm {
@@ -651,10 +648,10 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
 
 // ------------------------------------------------------ fused activation path
 //
-// Smooth + quantize (A2) and the linear (A3 + A4) in one call.  Shapes that
-// take the register-path kernel's cluster schedule with short K slices run
-// as one launch that quantizes the activations on chip; the others run the
-// quantizer into the workspace's scratch tail and then the linear.
+// Smooth + quantize (A2) and the linear (A3 + A4) in one call: the quantizer
+// writes codes and scales into the workspace's scratch tail, then the linear
+// reads them (two launches, the second overlapping the first through
+// programmatic dependent launch).
 
 size_t fused_workspace_size(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
@@ -670,11 +667,6 @@ quasar_status_t run_fused(const void* X, int ldx, const float* smooth, const int
   if (!X || !smooth || !Wp || !sw || !Y) return QUASAR_ERR_INVALID_ARG;
   if (!aligned(X, 16) || !aligned(smooth, 16) || !aligned(Wp, 16) || !aligned(Y, 16) || !aligned(sw, 4))
     return QUASAR_ERR_UNSUPPORTED;
-  bool done = false;
-  const quasar_status_t st = skinny::run_fused(reinterpret_cast<const uint16_t*>(X), ldx, smooth, Wp, sw, M, N, K, Y,
-                                               ldy, stream, &done);
-  if (st != QUASAR_OK || done) return st;
-  // Two launches: codes and scales into the scratch tail, then the linear.
   const size_t lin = workspace_size(M, N, K);
   if (!ws || ws_bytes < fused_workspace_size(M, N, K) || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
   int8_t* xq = reinterpret_cast<int8_t*>(ws) + lin;
@@ -735,12 +727,6 @@ size_t quasar_w8a8_linear_workspace_size(int M, int N, int K) { return quasar::g
 
 size_t quasar_w8a8_linear_fused_workspace_size(int M, int N, int K) {
   return quasar::gemm::fused_workspace_size(M, N, K);
-}
-
-int quasar_w8a8_linear_fused_launches(int M, int N, int K) {
-  if (M <= 0) return 0;
-  const int f = quasar::skinny::fused_fits(M, N, K);
-  return f < 0 ? -1 : (f ? 1 : 2);
 }
 
 quasar_status_t quasar_w8a8_linear_fused(const void* X_bf16, int ldx, const float* smooth, const int8_t* Wp,

@@ -77,47 +77,24 @@ constexpr int G = 2;              // K blocks per pipeline stage (one handshake 
 constexpr int RUN_BLOCKS = 32;
 static_assert(RUN_BLOCKS % 2 == 0, "runs end on a stage boundary");
 
-// Kernel variants (VAR):
-//  0  stream-K schedule.
-//  1  cluster schedule: the run-end reduction buffer overlays the stage
-//     ring, valid because a CTA's single accumulation run ends after its
-//     last block (the ring is then idle; K slices are <= RUN_BLOCKS blocks).
-//     The space it frees becomes more stages in flight.
-//  2  cluster schedule with the activation prologue fused in: the CTA
-//     smooths and quantizes its own K slice of the BF16 activations into a
-//     resident code region (the cluster exchanges per-token partial absmax
-//     values through distributed shared memory), so stages carry weights
-//     only and the weight stream need not wait for the previous kernel.
-// Variant 2 (one token tile, M <= 8) shared-memory region XR, for a K
-// slice of nblk blocks: the INT8 codes in the token-tile layout the main
-// loop reads (block j at j * XB), then the slice's BF16 activations
-// ([block][token][128 values]), then its smoothing factors.
-__host__ __device__ __forceinline__ int fused_slice_bytes(int nblk, int M, int XB) {
-  return nblk * (XB + M * 256 + 128 * 4);
-}
-
-template <int NT8, int VAR = 0>
+// RIR: the run-end reduction buffer overlays the stage ring.  Only valid
+// when a CTA's single accumulation run ends after its last block (the ring
+// is then idle): the cluster schedule with K slices of <= RUN_BLOCKS blocks.
+// The space it frees becomes more stages in flight.
+template <int NT8, bool RIR = false>
 struct Cfg {
-  static constexpr bool RIR = VAR >= 1;
-  static constexpr bool FUSED = VAR == 2;
-  static_assert(!FUSED || NT8 == 1, "the fused variant is built for one token tile");
   static constexpr int NT = 8 * NT8;                        // token columns (padded to 8)
   static constexpr int NH = NT8;                            // token tiles of one finalizer share
   static constexpr int XB = NT * BK;                        // INT8 token tile of a block
-  static constexpr int BLK = HALF_BYTES + (FUSED ? 0 : XB); // one block: weight half (+ token tile)
+  static constexpr int BLK = HALF_BYTES + XB;               // one block: weight half + token tile
   static constexpr int STAGE = G * BLK;                     // multiple of 1024 (swizzle atoms)
   static constexpr int RED = UT * KQ * NT8 * 32 * 16;       // fp32 partials: [row tile][kq][token tile][lane]
   static constexpr int FIN = UT * NT8 * 32 * 16;            // int32 run sums: [row tile][token tile][lane]
   static constexpr int SLOT = UT * NT8 * 32;                // int4 per partial-sum slot (64 rows x NT)
-  // Staged scales: sa[32], sw[2][64], inv[32], and (variant 2) the cluster's
-  // partial absmax values amax[rank][32].
-  static constexpr int SCL = FUSED ? 2048 : 1024;
-  static constexpr int BASE = 1024 + (RIR ? 0 : RED) + FIN + SCL + 256;
-  static constexpr int S_FIT = (SMEM_CAP - BASE) / STAGE;
-  // Variant 2 keeps four stages and gives the rest to the activation region.
-  static constexpr int S = FUSED ? 4 : (S_FIT < 12 ? S_FIT : 12);   // stages in flight
-  static constexpr int XR = FUSED ? ((SMEM_CAP - BASE - S * STAGE) & ~1023) : 0;
-  static constexpr int FIXED = BASE + XR;
+  static constexpr int SCL = 1024;                          // staged scales: sa[32], sw of 2 units
+  static constexpr int FIXED = 1024 + (RIR ? 0 : RED) + FIN + SCL + 256;
+  static constexpr int S_FIT = (SMEM_CAP - FIXED) / STAGE;
+  static constexpr int S = S_FIT < 12 ? S_FIT : 12;         // stages in flight
   static constexpr int SMEM = FIXED + S * STAGE;
   static_assert(BLK % 1024 == 0, "block alignment");
   static_assert(S >= 2, "pipeline depth");
@@ -127,9 +104,6 @@ struct Cfg {
 
 struct Params {
   const uint8_t* wp;  // packed weights, [n_tiles][KB][128 rows][128 B]
-  const uint16_t* x;  // variant 2: BF16 activations [M][ldx]
-  int ldx;
-  const float* smooth;  // variant 2: smoothing factors [K]
   const float* sa;
   const float* sw;
   int M, N, K;
@@ -279,68 +253,6 @@ QUASAR_DEVICE_INLINE int4 ld_dsmem_int4(const void* local, uint32_t rank) {
   return v;
 }
 
-// 32-bit word at the same shared-memory offset in cluster CTA `rank`.
-QUASAR_DEVICE_INLINE uint32_t ld_dsmem_u32(const void* local, uint32_t rank) {
-  uint32_t remote, v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-  return v;
-}
-
-// Store a 32-bit word at the same shared-memory offset in cluster CTA `rank`.
-QUASAR_DEVICE_INLINE void st_dsmem_f32(void* local, uint32_t rank, float v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
-
-// Eight BF16 values (one 16-byte load) -> fp32.
-QUASAR_DEVICE_INLINE void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-// Smoothed activations x' = fp32(x) * smooth (correctly rounded) of 8
-// consecutive elements, from their raw BF16 bits and smoothing factors.
-QUASAR_DEVICE_INLINE void smooth8(const uint4& raw, const float (&s)[8], float (&x)[8]) {
-  bf16x8_to_f32(raw, x);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], s[i]);
-}
-
-QUASAR_DEVICE_INLINE void lds_smooth8(const float* p, float (&s)[8]) {
-  const float4 s0 = reinterpret_cast<const float4*>(p)[0];
-  const float4 s1 = reinterpret_cast<const float4*>(p)[1];
-  s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
-  s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
-}
-
-// Codes of 8 smoothed activations: rne(x' * inv) as int8, packed.  Adding
-// 1.5 * 2^23 to the (separately rounded) product rounds it to the nearest
-// integer, ties to even, and leaves that integer's two's-complement low byte
-// in the low byte of the sum's bits.  No clamp is needed: |x'| <= absmax, so
-// |x' * inv| < 127.5 and the result is within [-127, 127]; a NaN product (an
-// infinite absmax) gives byte 0, as the convert-and-clamp form does.
-QUASAR_DEVICE_INLINE uint2 quant8(const uint4& raw, const float (&s)[8], float inv) {
-  float x[8];
-  smooth8(raw, s, x);
-  uint32_t b[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) b[i] = __float_as_uint(__fadd_rn(__fmul_rn(x[i], inv), 12582912.f));
-  return make_uint2(__byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410),
-                    __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410));
-}
-
-QUASAR_DEVICE_INLINE void cp_async16(void* dst_smem, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
-}
-
-QUASAR_DEVICE_INLINE void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // D += A (16 x 16, fp16, row) * B (16 x 8, fp16, col), fp32 accumulate.
 QUASAR_DEVICE_INLINE void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                     uint32_t b1) {
@@ -476,22 +388,20 @@ QUASAR_DEVICE_INLINE void count_segments(const Params& p, int ua, int na, int ub
 }
 
 // One K block of this warp's work: its two K steps of the unit's 64 rows
-// (weight half at wst) against every token tile (token tile at xst).  Token
-// operands: row n = 8 ni + g of the swizzled tile sits at n * 128, chunk ch
-// at (ch ^ (n & 7)) * 16.
+// against every token tile.  Token operands: row n = 8 ni + g of the
+// swizzled tile sits at n * 128, chunk ch at (ch ^ (n & 7)) * 16.
 template <int NT8>
-QUASAR_DEVICE_INLINE void consume_block(uint32_t wst, uint32_t xst, uint32_t a_off, uint32_t b_off,
-                                        float (&acc)[UT][NT8][4]) {
+QUASAR_DEVICE_INLINE void consume_block(uint32_t st, uint32_t a_off, uint32_t b_off, float (&acc)[UT][NT8][4]) {
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     uint32_t bq[NT8][2];
 #pragma unroll
     for (int ni = 0; ni < NT8; ++ni)
-      s8x4_to_f16x4(lds32(xst + (b_off ^ (ks << 4)) + (uint32_t)(ni * 8 * BK)), bq[ni][0], bq[ni][1]);
+      s8x4_to_f16x4(lds32(st + (b_off ^ (ks << 4)) + (uint32_t)(ni * 8 * BK)), bq[ni][0], bq[ni][1]);
 #pragma unroll
     for (int i2 = 0; i2 < UT / 2; ++i2) {
       uint32_t d[4];
-      ldsm_x4(wst + (a_off ^ (ks << 4)) + (uint32_t)(i2 * 32 * BK), d[0], d[1], d[2], d[3]);
+      ldsm_x4(st + (a_off ^ (ks << 4)) + (uint32_t)(i2 * 32 * BK), d[0], d[1], d[2], d[3]);
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         uint32_t a0, a1, a2, a3;
@@ -505,11 +415,10 @@ QUASAR_DEVICE_INLINE void consume_block(uint32_t wst, uint32_t xst, uint32_t a_o
   }
 }
 
-template <int NT8, int VAR>
+template <int NT8, bool RIR>
 __global__ void __launch_bounds__(THREADS, 2)
 w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
-  using C = Cfg<NT8, VAR>;
-  constexpr bool RIR = C::RIR, FUSED = C::FUSED;
+  using C = Cfg<NT8, RIR>;
   constexpr int NH = C::NH;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -519,10 +428,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   int4* fin = reinterpret_cast<int4*>(smem + C::S * C::STAGE + RED_OWN);
   float* sa_s = reinterpret_cast<float*>(smem + C::S * C::STAGE + RED_OWN + C::FIN);   // [32]
   float* sw_s = sa_s + 32;                                                                // [2][64]
-  float* inv_s = sw_s + 2 * UM;                                                           // [32] variant 2
-  float* amax_s = inv_s + 32;                                                             // [8][32] variant 2
-  uint8_t* xr = smem + C::S * C::STAGE + RED_OWN + C::FIN + C::SCL;                       // variant 2 region
-  uint64_t* full = reinterpret_cast<uint64_t*>(xr + C::XR);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::S * C::STAGE + RED_OWN + C::FIN + C::SCL);
   uint64_t* empty = full + C::S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::S);
 
@@ -539,7 +445,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (!FUSED && warp == PRODUCER_WARP && lane == 0) prefetch_tmap(&tmX);
+  if (warp == PRODUCER_WARP && lane == 0) prefetch_tmap(&tmX);
   __syncthreads();
 
   const int grid = (int)gridDim.x;
@@ -547,25 +453,21 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   const Sched sc = schedule_of((int)blockIdx.x, grid, p);
 
   if (warp == PRODUCER_WARP) {
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_x = policy_evict_last();
-    // Weights do not depend on the previous kernel: fill every stage first.
-    int pre = 0;
     if (lane == 0) {
-      Walk w(sc, KB);
-      for (; pre < C::S && w.more(); ++pre, w.next(KB)) {
-        mbar_arrive_expect_tx(&full[pre], (uint32_t)(w.g * C::BLK));
-        for (int b = 0; b < w.g; ++b)
-          bulk_load(stages + pre * C::STAGE + b * C::BLK, unit_block(p, w.u, w.kb + b), HALF_BYTES, &full[pre],
-                    pol_w);
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      // Weights do not depend on the previous kernel: fill every stage first.
+      int pre = 0;
+      {
+        Walk w(sc, KB);
+        for (; pre < C::S && w.more(); ++pre, w.next(KB)) {
+          mbar_arrive_expect_tx(&full[pre], (uint32_t)(w.g * C::BLK));
+          for (int b = 0; b < w.g; ++b)
+            bulk_load(stages + pre * C::STAGE + b * C::BLK, unit_block(p, w.u, w.kb + b), HALF_BYTES, &full[pre],
+                      pol_w);
+        }
       }
-    }
-    __syncwarp();
-    if (FUSED) cluster_sync_all();   // the consumers' prologue barrier (partial absmax exchange)
-    if (lane == 0) {
-      // Token codes come from the previous kernel (variants 0 and 1); the
-      // fused variant streams weights only and never reads its outputs.
-      if (!FUSED) pdl_wait();
+      pdl_wait();  // token codes come from the previous kernel
       Walk w(sc, KB);
       Ring<C::S> rg;
       int issued = 0;
@@ -577,9 +479,8 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
           for (int b = 0; b < w.g; ++b)
             bulk_load(st + b * C::BLK, unit_block(p, w.u, w.kb + b), HALF_BYTES, &full[rg.s], pol_w);
         }
-        if (!FUSED)
-          for (int b = 0; b < w.g; ++b)
-            tma_load_2d(st + b * C::BLK + HALF_BYTES, &tmX, (w.kb + b) * BK, 0, &full[rg.s], pol_x);
+        for (int b = 0; b < w.g; ++b)
+          tma_load_2d(st + b * C::BLK + HALF_BYTES, &tmX, (w.kb + b) * BK, 0, &full[rg.s], pol_x);
       }
       // Never leave with copies in flight.
       for (int s = 0; s < C::S && s < issued; ++s) {
@@ -589,7 +490,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       }
     }
     __syncwarp();
-    if (p.mode == 1) {   // the consumers' two cluster barriers at the end
+    if (p.mode == 1) {   // the consumers' two cluster barriers
       cluster_sync_all();
       cluster_sync_all();
     }
@@ -601,17 +502,6 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   const int g = lane >> 2, c = lane & 3;
   const int mt_f = warp;            // finalizer share: row tile mt_f, every token tile
   const int nh = 0;
-  // Variant 2: the CTA's K slice (blocks kbs0 .. kbs0 + nblk - 1 of its unit)
-  // and its parts of XR (the host checks that they fit).
-  const int kbs0 = sc.s0 % KB;      // first K block of the slice (cluster schedule: a single unit)
-  const int nblk = sc.s1 - sc.s0;
-  uint8_t* xs = xr + nblk * C::XB;                                        // activations [j][m][256 B]
-  float* smo = reinterpret_cast<float*>(xs + (FUSED ? nblk * p.M * 256 : 0));   // smoothing factors
-  if (FUSED) {
-    // Model parameters, like the weights: read before the previous kernel ends.
-    const int n16 = (min(p.K, (kbs0 + nblk) * BK) - kbs0 * BK) / 4;
-    for (int i = threadIdx.x; i < n16; i += CWARPS * 32) cp_async16(smo + 4 * i, p.smooth + kbs0 * BK + 4 * i);
-  }
   pdl_wait();                       // scales and workspace belong to the previous kernel until here
   const int u_first = (sc.s1 > sc.s0) ? sc.s0 / KB : sc.w0;
   const int u_last = (sc.w1 > sc.w0) ? sc.w1 - 1 : (sc.s1 - 1) / KB;
@@ -622,90 +512,13 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   if (!p.acc_out) {
     for (int i = threadIdx.x; i < 32 + 2 * UM; i += CWARPS * 32) {
       if (i < 32) {
-        if (!FUSED) sa_s[i] = (i < p.M) ? __ldg(&p.sa[i]) : 0.f;
+        sa_s[i] = (i < p.M) ? __ldg(&p.sa[i]) : 0.f;
       } else {
         const int r = i - 32;
         const int n = (r < UM ? u_first : u_last) * UM + (r & (UM - 1));
         sw_s[r] = (n < p.N) ? __ldg(&p.sw[n]) : 0.f;
       }
     }
-  }
-
-  // Variant 2: smooth and quantize this CTA's K slice of the activations
-  // into the code region, with the same fp32 steps as the stand-alone
-  // quantizer: x' = x * smooth, a = max |x'| over the whole row,
-  // code = rne(x' * (127 / a)) (clamped to [-127, 127]), sa = a / 127 (0 if
-  // a = 0).  Work item it = (j * M + m) * 16 + vv is 16-byte column vv of
-  // token m in block j, so a half warp shares one (j, m).
-  const uint32_t xr_u32 = smem_u32(xr);
-  if (FUSED) {
-    constexpr int PT = CWARPS * 32;   // prologue threads
-    const int k0 = kbs0 * BK;
-    const int nvec = (min(p.K, (kbs0 + nblk) * BK) - k0) / 8;   // 8-element vectors of a token's slice
-    const int tid = threadIdx.x;
-    const int total = nblk * p.M * 16;
-    unsigned int* amax_l = reinterpret_cast<unsigned int*>(inv_s);   // this slice's absmax bits, until pass 2
-    for (int i = tid; i < nblk * C::XB / 16; i += PT)
-      reinterpret_cast<uint4*>(xr)[i] = make_uint4(0u, 0u, 0u, 0u);   // rows >= M, columns beyond the slice
-    if (tid < 32) amax_l[tid] = 0u;
-    // Every activation vector of the slice, in flight at once.
-    for (int m = 0; m < p.M; ++m) {
-      const uint16_t* src = p.x + (size_t)m * p.ldx + k0;
-      for (int v = tid; v < nvec; v += PT) cp_async16(xs + ((v >> 4) * p.M + m) * 256 + (v & 15) * 16, src + 8 * v);
-    }
-    cp_async_wait_all();              // this thread's activations and smoothing factors
-    named_barrier_or(RED_BAR, PT, 0u);
-    // Pass 1: partial absmax of every token over this slice.  The loop is
-    // uniform per warp so that the half-warp reduction has all lanes.  The
-    // maxima are never NaN (fmaxf from 0 drops NaN), so an unsigned max of
-    // the bit patterns is the float max.
-    for (int base = tid & ~31; base < total; base += PT) {
-      const int it = base + lane;
-      const int rest = it >> 4, vv = it & 15;
-      const int j = rest / p.M, m = rest - j * p.M;
-      const int v = 16 * j + vv;
-      float a = 0.f;
-      if (it < total && v < nvec) {
-        float sv[8], x[8];
-        lds_smooth8(smo + 8 * v, sv);
-        smooth8(*reinterpret_cast<const uint4*>(xs + rest * 256 + vv * 16), sv, x);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(x[e]));
-      }
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-      if (it < total && vv == 0) atomicMax(&amax_l[m], __float_as_uint(a));
-    }
-    named_barrier_or(RED_BAR, PT, 0u);
-    // Push this slice's maxima into every cluster CTA's amax[this rank][m];
-    // the cluster barrier orders those stores before the reads below (the
-    // producer warp takes part in it too).
-    const uint32_t rank = (uint32_t)((int)blockIdx.x % p.csize);
-    if (tid < p.M)
-      for (int q = 0; q < p.csize; ++q) st_dsmem_f32(&amax_s[rank * 32 + tid], (uint32_t)q, __uint_as_float(amax_l[tid]));
-    __syncwarp();
-    cluster_sync_all();
-    if (tid < p.M) {
-      float am = 0.f;
-      for (int q = 0; q < p.csize; ++q) am = fmaxf(am, amax_s[q * 32 + tid]);
-      inv_s[tid] = am > 0.f ? __fdiv_rn(127.f, am) : 0.f;
-      sa_s[tid] = am > 0.f ? __fdiv_rn(am, 127.f) : 0.f;
-    }
-    named_barrier_or(RED_BAR, PT, 0u);
-    // Pass 2: codes (block j at j * XB; token m at m * 128, 16-byte chunk c
-    // at (c ^ (m & 7)) * 16).
-    for (int it = tid; it < total; it += PT) {
-      const int rest = it >> 4, vv = it & 15;
-      const int j = rest / p.M, m = rest - j * p.M;
-      const int v = 16 * j + vv;
-      if (v < nvec) {
-        float sv[8];
-        lds_smooth8(smo + 8 * v, sv);
-        const uint2 code = quant8(*reinterpret_cast<const uint4*>(xs + rest * 256 + vv * 16), sv, inv_s[m]);
-        *reinterpret_cast<uint2*>(xr + j * C::XB + m * BK + (((vv >> 1) ^ (m & 7)) << 4) + 8 * (vv & 1)) = code;
-      }
-    }
-    named_barrier_or(RED_BAR, PT, 0u);
   }
 
   float acc[UT][NT8][4];
@@ -729,7 +542,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   // chunk differs from the first in bit 0 only, i.e. its offset is the first
   // one's ^ 16.
   const uint32_t a_off = (uint32_t)(lane * BK + (((2 * kq) ^ (lane & 7)) << 4));
-  const uint32_t b_off = (uint32_t)(g * BK + (((2 * kq) ^ g) << 4) + 4 * c);
+  const uint32_t b_off = (uint32_t)(HALF_BYTES + g * BK + (((2 * kq) ^ g) << 4) + 4 * c);
   const uint32_t stages_u32 = smem_u32(stages);
 
   bool bad = false;
@@ -749,18 +562,13 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     }
     if (!bad) {
       const uint32_t st0 = stages_u32 + (uint32_t)(r.s * C::STAGE);
-      // Token tile of block b of the stage: in the stage after the weight
-      // half, or (variant 2) in the resident code region.
-      auto xst = [&](int b) -> uint32_t {
-        return FUSED ? xr_u32 + (uint32_t)((w.kb + b - kbs0) * C::XB) : st0 + (uint32_t)(b * C::BLK + HALF_BYTES);
-      };
       // A full pair takes a straight-line path so that the two blocks'
       // loads and MMAs can interleave; a segment's odd tail takes one block.
       if (w.g == G) {
 #pragma unroll
-        for (int b = 0; b < G; ++b) consume_block<NT8>(st0 + (uint32_t)(b * C::BLK), xst(b), a_off, b_off, acc);
+        for (int b = 0; b < G; ++b) consume_block<NT8>(st0 + (uint32_t)(b * C::BLK), a_off, b_off, acc);
       } else {
-        consume_block<NT8>(st0, xst(0), a_off, b_off, acc);
+        consume_block<NT8>(st0, a_off, b_off, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[r.s]);
@@ -870,25 +678,25 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
 // ------------------------------------------------------------------ host side
 
-template <int NT8, int VAR>
+template <int NT8, bool RIR>
 static cudaError_t configure(int dev) {
   static int configured[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(w8a8_skinny_kernel<NT8, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<NT8, VAR>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(w8a8_skinny_kernel<NT8, RIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<NT8, RIR>::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   return cudaSuccess;
 }
 
-template <int NT8, int VAR>
+template <int NT8, bool RIR>
 static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = Cfg<NT8, VAR>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<NT8, RIR>::SMEM;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -901,18 +709,18 @@ static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cu
   return cfg;
 }
 
-// Clusters of `csize` CTAs of a cluster-schedule variant that the device
+// Clusters of `csize` CTAs of the cluster-schedule kernel that the device
 // keeps resident at once (0 if unknown); cached per device and cluster size.
-template <int NT8, int VAR>
+template <int NT8>
 static int resident_clusters(int dev, int csize) {
   static int cache[64][9];
   static bool init[64][9] = {};
   if (dev < 0 || dev >= 64 || csize < 2 || csize > 8) return 0;
   if (!init[dev][csize]) {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = config_of<NT8, VAR>(csize * 16, csize, nullptr, attr);
+    cudaLaunchConfig_t cfg = config_of<NT8, true>(csize * 16, csize, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, w8a8_skinny_kernel<NT8, VAR>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, w8a8_skinny_kernel<NT8, true>, &cfg) != cudaSuccess) {
       n = 0;
       cudaGetLastError();
     }
@@ -922,104 +730,43 @@ static int resident_clusters(int dev, int csize) {
   return cache[dev][csize];
 }
 
-// Cluster size for the cluster schedule of variant VAR (>= 2), or 0 if the
-// shape does not fit it: every cluster resident in one wave and each K slice
-// a single accumulation run of at most `max_slice` blocks.
-template <int NT8, int VAR>
-static int cluster_size_for(int dev, int sms, int N, int KB, int max_slice = RUN_BLOCKS) {
-  const int n_units = (N + UM - 1) / UM;
-  const int slots = std::min(2 * sms, MAX_CTAS);   // two CTAs per SM
-  max_slice = std::min(max_slice, RUN_BLOCKS);
-  int csize = std::min(std::min(8, slots / n_units), KB);
-  while (csize >= 2 && resident_clusters<NT8, VAR>(dev, csize) < n_units) --csize;
-  if (csize >= 2 && (KB + csize - 1) / csize > max_slice) return 0;
-  return csize >= 2 ? csize : 0;
-}
-
 template <int NT8>
 static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaError_t e = configure<NT8, 1>(dev);
-  if (e == cudaSuccess) e = configure<NT8, 0>(dev);
+  cudaError_t e = configure<NT8, true>(dev);
+  if (e == cudaSuccess) e = configure<NT8, false>(dev);
   if (e != cudaSuccess) return e;
   const int n_units = (p.N + UM - 1) / UM;
-  const int csize = cluster_size_for<NT8, 1>(dev, sms, p.N, p.KB);
+  const int slots = std::min(2 * sms, MAX_CTAS);   // two CTAs per SM
+  // Few units: one cluster per unit, with the most K slices that keep every
+  // cluster resident in one wave; each slice must be one accumulation run.
+  int csize = std::min(std::min(8, slots / n_units), p.KB);
+  while (csize >= 2 && resident_clusters<NT8>(dev, csize) < n_units) --csize;
+  if (csize >= 2 && (p.KB + csize - 1) / csize > RUN_BLOCKS) csize = 1;
   cudaLaunchAttribute attr[2];
   if (csize >= 2) {
-    // Few units: one cluster per unit, each CTA one K slice.
     p.mode = 1;
     p.csize = csize;
     p.split_units = 0;
     p.total1 = 0;
     p.whole_per = 0;
-    cudaLaunchConfig_t cfg = config_of<NT8, 1>(n_units * csize, csize, stream, attr);
-    return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, 1>, tx, p);
+    cudaLaunchConfig_t cfg = config_of<NT8, true>(n_units * csize, csize, stream, attr);
+    return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, true>, tx, p);
   }
   p.mode = 0;
   p.csize = 1;
-  int grid = std::min(2 * sms, MAX_CTAS);
+  int grid = slots;
   p.whole_per = n_units / grid;
   p.split_units = n_units - p.whole_per * grid;
   p.total1 = p.split_units * p.KB;
   if (p.whole_per == 0) grid = std::min(grid, p.total1);
   if ((unsigned long long)(p.total1 + 1) * (unsigned long long)(grid + 1) >= (1ull << 32)) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = config_of<NT8, 0>(grid, 1, stream, attr);
-  return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, 0>, tx, p);
-}
-
-// Longest K slice (blocks) whose BF16 activations fit variant 2's region.
-template <int NT8>
-static int fused_max_slice(int M) {
-  using C = Cfg<NT8, 2>;
-  int n = RUN_BLOCKS;
-  while (n > 0 && fused_slice_bytes(n, M, C::XB) > C::XR) --n;
-  return n;
-}
-
-template <int NT8>
-static cudaError_t launch_fused(Params p, int sms, cudaStream_t stream, bool* fits) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  cudaError_t e = configure<NT8, 2>(dev);
-  if (e != cudaSuccess) return e;
-  const int csize = cluster_size_for<NT8, 2>(dev, sms, p.N, p.KB, fused_max_slice<NT8>(p.M));
-  *fits = csize >= 2;
-  if (!*fits) return cudaSuccess;
-  p.mode = 1;
-  p.csize = csize;
-  p.split_units = 0;
-  p.total1 = 0;
-  p.whole_per = 0;
-  CUtensorMap unused = {};   // the fused variant reads the activations directly
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = config_of<NT8, 2>(((p.N + UM - 1) / UM) * csize, csize, stream, attr);
-  return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, 2>, unused, p);
+  cudaLaunchConfig_t cfg = config_of<NT8, false>(grid, 1, stream, attr);
+  return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, false>, tx, p);
 }
 
 bool handles(int M) { return M >= 1 && M <= 24; }
-
-template <int NT8>
-static int fused_fits(int M, int N, int K) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || configure<NT8, 2>(dev) != cudaSuccess) return -1;
-  const int sms = sm_count();
-  if (sms <= 0) return -1;
-  return cluster_size_for<NT8, 2>(dev, sms, N, (K + BK - 1) / BK, fused_max_slice<NT8>(M)) >= 2 ? 1 : 0;
-}
-
-// 1 if run_fused covers (M, N, K) with its single launch on the current
-// device, 0 if it leaves the shape to the two-launch path, -1 on a CUDA error.
-// Tokens up to which run_fused takes its single launch.  Every cluster
-// smooths and quantizes all of X for its own unit, so the prologue grows
-// with M; measured on GB300 for the Qwen3-8B linears it beats a quantize
-// launch plus the linear at M = 1 and draws level at M = 2.
-constexpr int FUSED_MAX_M = 2;
-
-int fused_fits(int M, int N, int K) {
-  if (M < 1 || M > FUSED_MAX_M) return 0;
-  return fused_fits<1>(M, N, K);
-}
 
 // Partial-sum slots this kernel may need after the counters: two per CTA,
 // each 64 rows x NT int32.  Like the counters they are zero between calls
@@ -1064,37 +811,6 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   }
   if (e == cudaErrorInvalidValue) return QUASAR_ERR_UNSUPPORTED;
   return cuda_status(e);
-}
-
-// Smooth + quantize + linear in one launch (variant 2) when the shape takes
-// the cluster schedule with K slices whose activations fit the region XR;
-// *done = false (nothing launched) otherwise.  Arguments were validated by the caller.
-quasar_status_t run_fused(const uint16_t* X, int ldx, const float* smooth, const int8_t* Wp, const float* sw, int M,
-                          int N, int K, void* Y, int ldy, cudaStream_t stream, bool* done) {
-  *done = false;
-  if (M < 1 || M > FUSED_MAX_M) return QUASAR_OK;
-  Params p = {};
-  p.wp = reinterpret_cast<const uint8_t*>(Wp);
-  p.x = X;
-  p.ldx = ldx;
-  p.smooth = smooth;
-  p.sa = nullptr;
-  p.sw = sw;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.KB = (K + BK - 1) / BK;
-  p.Y = reinterpret_cast<__nv_bfloat16*>(Y);
-  p.ldy = ldy;
-  p.acc_out = nullptr;
-  p.slots = nullptr;
-  p.ws_cnt = nullptr;
-  p.err = device_error_word();
-  p.limit_ns = wait_limit_ns();
-  if (!p.err) return QUASAR_ERR_CUDA;
-  const int sms = sm_count();
-  if (sms <= 0) return QUASAR_ERR_CUDA;
-  return cuda_status(launch_fused<1>(p, sms, stream, done));
 }
 
 }  // namespace skinny

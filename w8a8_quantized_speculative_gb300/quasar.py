@@ -41,7 +41,6 @@ _SIGS = {
     "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_w8a8_linear_fused_workspace_size": (_sz, [_i, _i, _i]),
-    "quasar_w8a8_linear_fused_launches": (_i, [_i, _i, _i]),
     "quasar_w8a8_linear_fused": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_int8_gemm_s32": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "quasar_w8a8_linear_noalloc": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p]),
@@ -209,7 +208,7 @@ def w8a8_linear(xq, sa, wp, sw, y=None, workspace: Workspace | None = None, stre
 
 def w8a8_linear_fused(x, smooth, wp, sw, y=None, workspace: Workspace | None = None, stream=None):
     """Y bf16 [M][N] = w8a8_linear(*smooth_quant_act(x, smooth), wp, sw), bit-identical, in one call
-    (one launch for the shapes whose K slices the kernel can quantize on chip)."""
+    (codes and scales live in the workspace)."""
     _need(x, torch.bfloat16, "x")
     _need(smooth, torch.float32, "smooth")
     ldx = _rowmajor(x, "x")
@@ -223,14 +222,6 @@ def w8a8_linear_fused(x, smooth, wp, sw, y=None, workspace: Workspace | None = N
     _check(lib.quasar_w8a8_linear_fused(_ptr(x), ldx, _ptr(smooth), _ptr(wp), _ptr(sw), M, N, K, _ptr(y), ldy,
                                         _ptr(buf), buf.numel(), _stream(stream)), "w8a8_linear_fused")
     return y
-
-
-def w8a8_linear_fused_launches(M: int, N: int, K: int) -> int:
-    """Kernel launches w8a8_linear_fused makes for this shape on the current device (1 or 2; 0 if M == 0)."""
-    n = int(lib.quasar_w8a8_linear_fused_launches(M, N, K))
-    if n < 0:
-        raise QuasarError(4, "w8a8_linear_fused_launches")
-    return n
 
 
 def int8_gemm_s32(xq, wp, N: int, acc=None, workspace: Workspace | None = None, stream=None):
