@@ -36,6 +36,16 @@ The pages leave the numeric details open.  The readings taken here are:
       (or D); the next token is the argmax of row n_acc.
   R6  T > 0: the drafter is deterministic, so draft j is accepted iff
       u[j] < p_j, p_j = softmax(logits_j / T)[draft_j], evaluated in fp64.
+  R7  lossless output token (the pages name the rejection sampling lossless
+      but do not spell out the correction; this is the standard speculative
+      sampling rule with the deterministic drafter of R6, whose
+      distribution is one-hot at the draft): at the first rejection j the
+      next token is drawn from norm(max(0, p_j - onehot(draft_j))), i.e.
+      p_j without the draft token, renormalised; after D acceptances the
+      bonus token is drawn from p_D.  Drawn by inverse CDF with one uniform
+      u_next per sequence: the smallest v whose cumulative weight exceeds
+      u_next times the total; if no weight is left, the lowest index other
+      than the draft.
 
 Every function below is pinned by tests under ``tests/`` against hand-derived
 values, closed forms, invariants or brute force (see each docstring).
@@ -234,4 +244,38 @@ def verify_accept(logits_bits: np.ndarray, draft: np.ndarray, temperature: float
                 break
         if temperature == 0:
             nxt[b] = int(np.argmax(lg[b, n_acc[b]]))
+    return n_acc, nxt
+
+
+def verify_sample(logits_bits: np.ndarray, draft: np.ndarray, temperature: float, u: np.ndarray,
+                  u_next: np.ndarray):
+    """Accepted prefix length and the lossless next token (readings R6, R7).
+
+    zh §2 "无损拒绝采样" (lossless rejection sampling on the high-precision
+    logits).  T > 0.  n_acc as verify_accept; next[b] is drawn from the
+    residual of row n_acc[b] (that row's softmax without the rejected draft
+    token) or, when every draft was accepted, from the bonus row D, by
+    inverse CDF on u_next[b], all in fp64.  Pinned by closed forms (two-level
+    rows, explicit CDFs) and by a chi-square test that the emitted token is
+    distributed as the target softmax whatever the draft (losslessness).
+    """
+    assert temperature > 0
+    lg = bf16_to_f32(logits_bits).astype(F64)
+    B, R, V = lg.shape
+    D = R - 1
+    n_acc, _ = verify_accept(logits_bits, draft, temperature, u)
+    nxt = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        j = int(n_acc[b])
+        z = lg[b, j] / temperature
+        w = np.exp(z - z.max())
+        d = int(draft[b, j]) if j < D else -1
+        if 0 <= d < V:
+            w[d] = 0.0
+        total = w.sum()
+        if total <= 0.0:
+            nxt[b] = 1 if d == 0 else 0
+            continue
+        cdf = np.cumsum(w)
+        nxt[b] = min(int(np.searchsorted(cdf, u_next[b] * total, side="right")), V - 1)
     return n_acc, nxt

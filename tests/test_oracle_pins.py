@@ -351,3 +351,80 @@ def test_verify_forced_mask_invariant():
         want = D if ok.all() else int(np.argmin(ok))
         assert n_acc[b] == want
         assert nxt[b] == am[b, want]
+
+
+# ---------------------------------------------------------------- lossless next token (R7)
+
+@pytest.mark.parametrize("T", [1.0, 0.5])
+def test_sample_residual_two_level_closed_form(T):
+    """Reject the hot draft of a two-level row: the residual is uniform over
+    the V - 1 other tokens, so u_next = (k + 1/2) / (V - 1) must give the
+    k-th token that is not the hot one."""
+    V, L, hot = 64, 3.0, 17
+    row = np.zeros(V, np.float32)
+    row[hot] = L
+    bits = bf16(np.stack([row, row])[None])        # D = 1
+    c = math.exp(L / T)
+    p_hot = c / (c + V - 1)
+    others = [v for v in range(V) if v != hot]
+    for k in (0, 1, 16, 17, 40, V - 2):
+        u = np.array([[(1 + p_hot) / 2]], np.float32)                 # rejects the hot draft
+        n_acc, nxt = orc.verify_sample(bits, np.array([[hot]], np.int32), T, u, np.array([(k + 0.5) / (V - 1)]))
+        assert int(n_acc[0]) == 0 and int(nxt[0]) == others[k]
+
+
+def test_sample_bonus_explicit_cdf():
+    """Every draft accepted: the bonus row is sampled from its full softmax.
+    Row weights 1, 1, 1, 3, 1, ... (logit ln 3 at token 3): the CDF steps are
+    known exactly."""
+    V = 8
+    row = np.zeros(V, np.float32)
+    lg = np.stack([row, row])
+    lg[1, 3] = math.log(3.0)                        # bonus row (rounded to BF16; weights read back)
+    bits = synth.f32_to_bf16_bits(lg[None])
+    w = np.exp(orc.bf16_to_f32(bits)[0, 1].astype(np.float64))
+    cdf = np.cumsum(w) / w.sum()
+    for v in range(V):
+        lo = cdf[v - 1] if v else 0.0
+        u_next = (lo + cdf[v]) / 2
+        n_acc, nxt = orc.verify_sample(bits, np.array([[0]], np.int32), 1.0, np.array([[0.0]], np.float32),
+                                       np.array([u_next]))
+        assert int(n_acc[0]) == 1 and int(nxt[0]) == v
+
+
+def test_sample_rejects_draft_never_resampled():
+    """The rejected draft token has no residual mass: it is never drawn."""
+    V = 16
+    rng = np.random.default_rng(5)
+    bits = synth.f32_to_bf16_bits(rng.standard_normal((1, 2, V)))
+    d = 7
+    for u_next in np.linspace(0, 1, 97, endpoint=False):
+        n_acc, nxt = orc.verify_sample(bits, np.array([[d]], np.int32), 1.0, np.array([[0.999999]], np.float32),
+                                       np.array([u_next]))
+        assert int(n_acc[0]) == 0 and int(nxt[0]) != d
+
+
+@pytest.mark.parametrize("d", [0, 2, 5])
+def test_sample_is_lossless_chi_square(d):
+    """Losslessness: with a fixed draft d, the token emitted at position 0
+    (d if accepted, else the residual draw) is distributed as the target
+    softmax p_0.  20000 seeded draws, chi-square against p_0 at alpha 1e-4."""
+    V, N = 6, 20000
+    rng = np.random.default_rng(100 + d)
+    logits = np.array([[0.3, -0.2, 1.1, 0.0, -1.0, 0.6], [0.0] * V], np.float32)
+    bits = synth.f32_to_bf16_bits(np.repeat(logits[None], N, axis=0))
+    draft = np.full((N, 1), d, np.int32)
+    u = rng.random((N, 1)).astype(np.float32)
+    u_next = rng.random(N)
+    n_acc, nxt = orc.verify_sample(bits, draft, 1.0, u, u_next)
+    emitted = np.where(n_acc == 1, d, nxt)
+    z = orc.bf16_to_f32(bits)[0, 0].astype(np.float64)
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    counts = np.bincount(emitted, minlength=V)
+    chi2 = float(((counts - N * p) ** 2 / (N * p)).sum())
+    assert chi2 < 25.74, (chi2, counts, N * p)      # chi-square(5) upper 1e-4 point
+    # a residual that kept the draft token would fail: check that it is detectable
+    keep = np.where(n_acc == 1, d, np.minimum(np.searchsorted(np.cumsum(p), u_next, side="right"), V - 1))
+    bad = float(((np.bincount(keep, minlength=V) - N * p) ** 2 / (N * p)).sum())
+    assert bad > 100.0
