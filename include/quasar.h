@@ -269,6 +269,31 @@ quasar_status_t quasar_verify_accept(const void* logits_bf16, int ldl,
                                      void* workspace, size_t ws_bytes,
                                      quasar_stream_t stream);
 
+/* A5 with T > 0 and the lossless next token.
+ *
+ * zh §2 (lossless rejection sampling on the high-precision logits).  The
+ * acceptance test is that of quasar_verify_accept for T > 0.  With the
+ * deterministic drafter, the speculative-sampling correction at the first
+ * rejected position j is a draw from norm(max(0, p_j - onehot(draft_j))),
+ * i.e. p_j without the draft token, renormalised; after D acceptances the
+ * bonus token is a draw from p_D.  next_token[b] is that draw by inverse
+ * CDF: the smallest v whose cumulative weight exp(logit/T - max) exceeds
+ * u_next[b] times the row's total (fp32; the draft token carries no
+ * weight); a row with no weight left gives the lowest index other than the
+ * draft.  Emitted tokens are then distributed as the target softmax
+ * whatever the drafts are.
+ *   temperature > 0 (finite); u [B][D] as above (may be NULL iff D == 0);
+ *   u_next [B] fp32 in [0, 1); next_token [B] int32 output (both required);
+ *   other arguments, sizes and the workspace as quasar_verify_accept.
+ * ------------------------------------------------------------------------ */
+quasar_status_t quasar_verify_sample(const void* logits_bf16, int ldl,
+                                     const int32_t* draft, int B, int D, int V,
+                                     float temperature, const float* u,
+                                     const float* u_next,
+                                     int32_t* n_acc, int32_t* next_token,
+                                     void* workspace, size_t ws_bytes,
+                                     quasar_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -146,3 +146,27 @@ def test_fused_linear_rejects_bad_arguments(lib):
     lib.quasar_w8a8_linear_workspace_size.restype = ctypes.c_size_t
     lin = lib.quasar_w8a8_linear_workspace_size(20, 24576, 4096)
     assert lib.quasar_w8a8_linear_fused_workspace_size(20, 24576, 4096) == lin + 20 * 4096 + 256
+
+
+def test_verify_sample_rejects_bad_arguments(lib):
+    f = lib.quasar_verify_sample
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p] + [ctypes.c_int] * 3 + \
+        [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+         ctypes.c_size_t, ctypes.c_void_p]
+    names = ["lg", "ldl", "draft", "B", "D", "V", "T", "u", "un", "n_acc", "nxt", "ws", "wsb", "stream"]
+    ok_args = [FAKE, 128, FAKE, 2, 3, 128, 1.0, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None]
+
+    def call(**kw):
+        a = list(ok_args)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+
+    assert call(T=0.0) == 1             # sampling needs T > 0
+    assert call(T=float("inf")) == 1
+    assert call(un=None) == 1
+    assert call(nxt=None) == 1
+    assert call(u=None) == 1            # D > 0 needs the acceptance uniforms
+    assert call(ldl=100) == 2
+    assert call(B=0) == 0

@@ -4,6 +4,8 @@ lengths) and fp32 scales must match bit for bit; BF16 outputs within 1 BF16
 ulp of the oracle's identically ordered fp32 dequant (the kernels are built
 to match exactly, and the tests report the worst distance).
 """
+import math
+
 import numpy as np
 import pytest
 
@@ -408,3 +410,88 @@ def test_fused_zero_token_rows(M):
     w = synth.f32_to_bf16_bits(rng.standard_normal((N, K)) * 0.02)
     smooth = dev(rng.uniform(0.5, 2.0, K).astype(np.float32))
     _fused_vs_two_step(x, w, smooth)
+
+
+# ---------------------------------------------------------------- A5 lossless next token
+
+def _u_next_midpoints(lg_bits, d, T, n_acc, rng, min_frac=1e-4):
+    """u_next per sequence at the middle of a random token's interval of the
+    row the oracle resamples (so fp32 rounding cannot move the draw)."""
+    lg = orc.bf16_to_f32(lg_bits).astype(np.float64)
+    B, R, V = lg.shape
+    D = R - 1
+    out = np.zeros(B, np.float64)
+    for b in range(B):
+        j = int(n_acc[b])
+        z = lg[b, j] / T
+        w = np.exp(z - z.max())
+        if j < D:
+            w[d[b, j]] = 0.0
+        cdf = np.cumsum(w) / w.sum()
+        frac = np.diff(np.concatenate([[0.0], cdf]))
+        cand = np.flatnonzero(frac >= min_frac)
+        t = int(rng.choice(cand))
+        lo = cdf[t - 1] if t else 0.0
+        out[b] = (lo + cdf[t]) / 2
+    return out.astype(np.float32)
+
+
+def _acc_uniforms(lg, d, T, seed, p_acc=0.7):
+    p = orc.acceptance_probabilities(lg, d, T)
+    acc = np.random.default_rng(seed).random(p.shape) < p_acc
+    return np.where(acc, 0.5 * p, p + 0.5 * (1 - p)).astype(np.float32)
+
+
+@pytest.mark.parametrize("B,D,V,T", [(16, 6, 4096, 1.0), (16, 6, 4096, 0.7), (9, 3, 1000, 2.0), (4, 0, 784, 1.0),
+                                     (32, 8, 151936, 1.0)])
+def test_verify_sample_matches_oracle(B, D, V, T):
+    lg, draft, mask, _ = synth.verify_inputs(B, D, V, 701, 702, 703, 704, std=3.0)
+    am = np.argmax(orc.bf16_to_f32(lg), axis=2)
+    d = np.where(mask, am[:, :D], draft).astype(np.int32)
+    u = _acc_uniforms(lg, d, T, 705) if D else np.zeros((B, 0), np.float32)
+    n_r, _ = orc.verify_accept(lg, d, T, u)
+    u_next = _u_next_midpoints(lg, d, T, n_r, np.random.default_rng(706))
+    n_acc, nxt = q.verify_sample(dev_bf16(lg), dev(d), T, dev(u), dev(u_next))
+    n_o, nxt_o = orc.verify_sample(lg, d, T, u, u_next.astype(np.float64))
+    assert np.array_equal(n_acc.cpu().numpy(), n_o)
+    assert np.array_equal(nxt.cpu().numpy(), nxt_o)
+    if D:
+        rej = n_o < D
+        assert not np.any(nxt_o[rej] == d[rej, n_o[rej]]), "a rejected draft was drawn again"
+
+
+def test_verify_sample_two_level_closed_form():
+    V, L, hot = 1024, 3.0, 17
+    row = np.zeros(V, np.float32)
+    row[hot] = L
+    lg = synth.f32_to_bf16_bits(np.stack([row, row])[None].astype(np.float32))
+    c = math.exp(L)
+    p_hot = c / (c + V - 1)
+    others = [v for v in range(V) if v != hot]
+    for k in (0, 16, 17, 500, V - 2):
+        u = np.array([[(1 + p_hot) / 2]], np.float32)
+        n_acc, nxt = q.verify_sample(dev_bf16(lg), dev(np.array([[hot]], np.int32)), 1.0, dev(u),
+                                     dev(np.array([(k + 0.5) / (V - 1)], np.float32)))
+        assert int(n_acc[0]) == 0 and int(nxt[0]) == others[k]
+
+
+def test_verify_sample_is_lossless_on_gpu():
+    """8192 sequences with the same rows (V = 8), seeded uniforms: the emitted
+    token at position 0 is distributed as the target softmax (chi-square, 1e-4)."""
+    V, N, d = 8, 8192, 2
+    rng = np.random.default_rng(707)
+    logits = np.array([[0.3, -0.2, 1.1, 0.0, -1.0, 0.6, -0.4, 0.2], [0.0] * V], np.float32)
+    lg = synth.f32_to_bf16_bits(np.repeat(logits[None], N, axis=0))
+    draft = np.full((N, 1), d, np.int32)
+    u = rng.random((N, 1)).astype(np.float32)
+    u_next = rng.random(N).astype(np.float32)
+    n_acc, nxt = q.verify_sample(dev_bf16(lg), dev(draft), 1.0, dev(u), dev(u_next))
+    n_acc, nxt = n_acc.cpu().numpy(), nxt.cpu().numpy()
+    emitted = np.where(n_acc == 1, d, nxt)
+    z = orc.bf16_to_f32(lg)[0, 0].astype(np.float64)
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    counts = np.bincount(emitted, minlength=V)
+    chi2 = float(((counts - N * p) ** 2 / (N * p)).sum())
+    assert chi2 < 29.88, (chi2, counts, N * p)      # chi-square(7) upper 1e-4 point
+    assert not np.any(nxt[n_acc == 0] == d)

@@ -10,7 +10,7 @@
 //
 // The step is an HBM scan of B*(D+1)*V BF16 logits.  Each row is cut into S
 // chunks so that about 8 x 152 CTAs stream it with 128-bit non-allocating
-// loads; a CTA reduces its chunk to (max, first argmax, running max, sum of
+// loads, four per thread in flight; a CTA reduces its chunk to (max, first argmax, running max, sum of
 // exp) and stores that record.  The last CTA of a sequence (an atomic count;
 // nobody waits) merges the records of its D+1 rows in chunk order, which
 // makes every result deterministic, then zeroes those records and the counter.
@@ -22,6 +22,7 @@ namespace quasar {
 namespace verify {
 
 constexpr int THREADS = 256;
+constexpr int LOADS = 4;          // 16-byte loads per thread in flight
 constexpr int TARGET_CTAS = 8 * 152;
 constexpr int MIN_CHUNK = 4096;
 
@@ -32,6 +33,7 @@ struct Partial {
   float s;     // sum of exp(logit/T - m) over the chunk (T > 0)
 };
 
+// Chunks per row the workspace provides for (device independent).
 static int chunks_for(long long rows, int V) {
   long long s = (TARGET_CTAS + rows - 1) / rows;
   long long smax = (V + MIN_CHUNK - 1) / MIN_CHUNK;
@@ -39,14 +41,16 @@ static int chunks_for(long long rows, int V) {
   return s < 1 ? 1 : (int)s;
 }
 
-// Chunk length (multiple of 8 elements) and the number of non-empty chunks.
-static void chunk_geometry(long long rows, int V, int* ch, int* S) {
-  const int s0 = chunks_for(rows, V);
+// Chunk length (multiple of 8 elements) and the number of non-empty chunks
+// for s0 requested chunks.
+static void chunk_geometry_s(int V, int s0, int* ch, int* S) {
   int len = (V + s0 - 1) / s0;
   len = (len + 7) & ~7;
   *ch = len;
   *S = (V + len - 1) / len;
 }
+
+static void chunk_geometry(long long rows, int V, int* ch, int* S) { chunk_geometry_s(V, chunks_for(rows, V), ch, S); }
 
 QUASAR_DEVICE_INLINE uint4 ld_stream(const void* p) {
   uint4 v;
@@ -75,11 +79,106 @@ QUASAR_DEVICE_INLINE void lse_merge(float& m, float& s, float m2, float s2) {
   m = M;
 }
 
+// Lossless next token of sequence b (whole CTA): an inverse-CDF draw with
+// uniform un from row j's weights w(v) = exp(logit(v) / T - M), M the row
+// max, without the rejected draft token when j < D.  The chunk holding the
+// target comes from the chunk records (mass s_c * exp(m_c - M)); that chunk
+// is then scanned: every thread sums a contiguous sub-range, a block prefix
+// sum places the sub-ranges, and the last thread whose prefix does not
+// exceed the target walks its sub-range to the first running sum above it
+// (or its last positive weight), so the result always has positive weight.
+// A row with no weight left draws the lowest index other than the draft.
+template <int NTH>
+__device__ void resample(const uint16_t* __restrict__ logits, int ldl, const int32_t* __restrict__ draft, int D,
+                         int V, int CH, int S, float invT, int b, int j, float un, const Partial* __restrict__ part,
+                         int32_t* __restrict__ next_token) {
+  __shared__ float s_M, s_t;
+  __shared__ int s_c, s_pick;
+  __shared__ float s_wsum[NTH / 32];
+  const size_t row = (size_t)b * (D + 1) + j;
+  const Partial* pr = part + row * S;
+  const uint16_t* src = logits + row * ldl;
+  const int dx = j < D ? draft[(size_t)b * D + j] : -1;
+  const bool excl = dx >= 0 && dx < V;
+  const int tid = threadIdx.x;
+  auto mass = [&](int c, float M, float wd) {
+    const float sc = __ldcg(&pr[c].s);
+    float a = sc > 0.f ? sc * expf(__ldcg(&pr[c].m) - M) : 0.f;
+    if (excl && c == dx / CH) a = fmaxf(a - wd, 0.f);
+    return a;
+  };
+  if (tid == 0) {
+    float M = -INFINITY;
+    for (int c = 0; c < S; ++c)
+      if (__ldcg(&pr[c].s) > 0.f) M = fmaxf(M, __ldcg(&pr[c].m));
+    const float wd = excl ? expf(__uint_as_float((uint32_t)src[dx] << 16) * invT - M) : 0.f;
+    float Z = 0.f;
+    for (int c = 0; c < S; ++c) Z += mass(c, M, wd);
+    const float target = un * Z;
+    float A = 0.f;
+    int cs = -1;
+    for (int c = 0; c < S; ++c) {
+      const float a = mass(c, M, wd);
+      if (a > 0.f) cs = c;
+      if (a > 0.f && A + a > target) break;
+      A += a;
+    }
+    s_M = M;
+    s_c = Z > 0.f ? cs : -1;
+    s_t = target - A;
+    s_pick = -1;
+  }
+  __syncthreads();
+  if (s_c < 0) {   // no weight left
+    if (tid == 0) next_token[b] = dx == 0 ? 1 : 0;
+    return;
+  }
+  const float M = s_M, t = s_t;
+  const int c0 = s_c * CH, c1 = min(V, c0 + CH);
+  const int per = (c1 - c0 + NTH - 1) / NTH;
+  const int v0 = min(c1, c0 + tid * per), v1 = min(c1, v0 + per);
+  auto w = [&](int v) { return v == dx ? 0.f : expf(__uint_as_float((uint32_t)src[v] << 16) * invT - M); };
+  float loc = 0.f;
+  for (int v = v0; v < v1; ++v) loc += w(v);
+  // Block exclusive prefix of the sub-range sums (fixed shape: deterministic).
+  const int lane = tid & 31, wp = tid >> 5;
+  float inc = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) s_wsum[wp] = inc;
+  __syncthreads();
+  float pre = inc - loc;
+  for (int q = 0; q < wp; ++q) pre += s_wsum[q];
+  if (loc > 0.f && pre <= t) atomicMax(&s_pick, tid);
+  __syncthreads();
+  // A chunk whose recorded mass was only rounding left over from the
+  // removed draft holds no weight when rescanned: fall back as for an empty row.
+  if (s_pick < 0 && tid == 0) next_token[b] = dx == 0 ? 1 : 0;
+  if (tid == s_pick) {
+    float run = pre;
+    int got = -1, last = -1;
+    for (int v = v0; v < v1; ++v) {
+      const float x = w(v);
+      if (x > 0.f) last = v;
+      run += x;
+      if (x > 0.f && run > t) {
+        got = v;
+        break;
+      }
+    }
+    next_token[b] = got >= 0 ? got : last;
+  }
+}
+
 template <bool SAMPLED>
 __global__ void __launch_bounds__(THREADS)
 verify_kernel(const uint16_t* __restrict__ logits, int ldl, const int32_t* __restrict__ draft, int D, int V,
-              int CH, int S, float invT, const float* __restrict__ u, int32_t* __restrict__ n_acc,
-              int32_t* __restrict__ next_token, Partial* __restrict__ part, unsigned int* __restrict__ cnt) {
+              int CH, int S, float invT, const float* __restrict__ u, const float* __restrict__ u_next,
+              int32_t* __restrict__ n_acc, int32_t* __restrict__ next_token, Partial* __restrict__ part,
+              unsigned int* __restrict__ cnt) {
   const int row = blockIdx.y;
   const int c = blockIdx.x;
   const int b = row / (D + 1);
@@ -106,15 +205,26 @@ verify_kernel(const uint16_t* __restrict__ logits, int ldl, const int32_t* __res
       }
     }
   };
-  for (int v = start + threadIdx.x * 8; v < vend; v += THREADS * 8) {
-    const uint4 raw = ld_stream(src + v);
+  auto take8 = [&](const uint4& raw, int v) {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       take(__uint_as_float(w[i] << 16), v + 2 * i);
       take(__uint_as_float(w[i] & 0xFFFF0000u), v + 2 * i + 1);
     }
+  };
+  // LOADS loads of each thread in flight before any is used (one load per
+  // step left too few bytes in flight per SM to cover HBM latency); each
+  // thread still takes its elements in increasing index order.
+  int v = start + threadIdx.x * 8;
+  for (; v + (LOADS - 1) * THREADS * 8 < vend; v += LOADS * THREADS * 8) {
+    uint4 raw[LOADS];
+#pragma unroll
+    for (int i = 0; i < LOADS; ++i) raw[i] = ld_stream(src + v + i * THREADS * 8);
+#pragma unroll
+    for (int i = 0; i < LOADS; ++i) take8(raw[i], v + i * THREADS * 8);
   }
+  for (; v < vend; v += THREADS * 8) take8(ld_stream(src + v), v);
   for (int v = vend + threadIdx.x; v < end; v += THREADS) take(__uint_as_float((uint32_t)src[v] << 16), v);
 
   // Block reduction (fixed shape, so deterministic).
@@ -147,50 +257,59 @@ verify_kernel(const uint16_t* __restrict__ logits, int ldl, const int32_t* __res
     is_last = (old + 1 == total) ? 1 : 0;
   }
   __syncthreads();
-  if (!is_last || warp != 0) return;
+  if (!is_last) return;
 
   // Last CTA of sequence b: merge each row's chunk records in chunk order.
   __threadfence();
-  int first_fail = D;
-  for (int j = lane; j <= D; j += 32) {
-    const Partial* pr = part + ((size_t)b * (D + 1) + j) * S;
-    float rb = -INFINITY, rm = -INFINITY, rs = 0.f;
-    int ri = INT_MAX;
-    for (int cc = 0; cc < S; ++cc) {
-      const float pb = __ldcg(&pr[cc].best);
-      const int pi = __ldcg(&pr[cc].idx);
-      arg_merge(rb, ri, pb, pi);
-      if (SAMPLED) lse_merge(rm, rs, __ldcg(&pr[cc].m), __ldcg(&pr[cc].s));
-    }
-    if (j < D) {
-      const int d = draft[(size_t)b * D + j];
-      bool ok;
-      if (d < 0 || d >= V) {
-        ok = false;  // out-of-vocabulary draft: rejected, never dereferenced
-      } else if (SAMPLED) {
-        const float ld = __uint_as_float((uint32_t)logits[((size_t)b * (D + 1) + j) * ldl + d] << 16);
-        const float pj = __fdiv_rn(expf(ld * invT - rm), rs);
-        ok = u[(size_t)b * D + j] < pj;
-      } else {
-        ok = (d == ri);
+  __shared__ int s_fail;
+  if (warp == 0) {
+    int first_fail = D;
+    for (int j = lane; j <= D; j += 32) {
+      const Partial* pr = part + ((size_t)b * (D + 1) + j) * S;
+      float rb = -INFINITY, rm = -INFINITY, rs = 0.f;
+      int ri = INT_MAX;
+      for (int cc = 0; cc < S; ++cc) {
+        const float pb = __ldcg(&pr[cc].best);
+        const int pi = __ldcg(&pr[cc].idx);
+        arg_merge(rb, ri, pb, pi);
+        if (SAMPLED) lse_merge(rm, rs, __ldcg(&pr[cc].m), __ldcg(&pr[cc].s));
       }
-      if (!ok) first_fail = min(first_fail, j);
+      if (j < D) {
+        const int d = draft[(size_t)b * D + j];
+        bool ok;
+        if (d < 0 || d >= V) {
+          ok = false;  // out-of-vocabulary draft: rejected, never dereferenced
+        } else if (SAMPLED) {
+          const float ld = __uint_as_float((uint32_t)logits[((size_t)b * (D + 1) + j) * ldl + d] << 16);
+          const float pj = __fdiv_rn(expf(ld * invT - rm), rs);
+          ok = u[(size_t)b * D + j] < pj;
+        } else {
+          ok = (d == ri);
+        }
+        if (!ok) first_fail = min(first_fail, j);
+      }
+    }
+  #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) first_fail = min(first_fail, __shfl_xor_sync(0xffffffffu, first_fail, o));
+    if (lane == 0) {
+      n_acc[b] = first_fail;
+      s_fail = first_fail;
+      if (!SAMPLED && next_token) {
+        const Partial* pr = part + ((size_t)b * (D + 1) + first_fail) * S;
+        float rb = -INFINITY;
+        int ri = INT_MAX;
+        for (int cc = 0; cc < S; ++cc) arg_merge(rb, ri, __ldcg(&pr[cc].best), __ldcg(&pr[cc].idx));
+        next_token[b] = ri;
+      }
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) first_fail = min(first_fail, __shfl_xor_sync(0xffffffffu, first_fail, o));
-  if (lane == 0) {
-    n_acc[b] = first_fail;
-    if (!SAMPLED && next_token) {
-      const Partial* pr = part + ((size_t)b * (D + 1) + first_fail) * S;
-      float rb = -INFINITY;
-      int ri = INT_MAX;
-      for (int cc = 0; cc < S; ++cc) arg_merge(rb, ri, __ldcg(&pr[cc].best), __ldcg(&pr[cc].idx));
-      next_token[b] = ri;
-    }
+  if (SAMPLED && u_next) {
+    __syncthreads();
+    resample<THREADS>(logits, ldl, draft, D, V, CH, S, invT, b, s_fail, u_next[b], part, next_token);
   }
   // Leave the workspace zero-filled for the next call (its records and counter).
-  __syncwarp();
+  __syncthreads();
+  if (warp != 0) return;
   for (int j = lane; j <= D; j += 32) {
     Partial* pr = part + ((size_t)b * (D + 1) + j) * S;
     for (int cc = 0; cc < S; ++cc) __stcg(reinterpret_cast<float4*>(&pr[cc]), make_float4(0.f, 0.f, 0.f, 0.f));
@@ -208,6 +327,50 @@ size_t workspace_size(int B, int D, int V) {
   return align256((size_t)B * 4) + (size_t)rows * S * sizeof(Partial);
 }
 
+static quasar_status_t run(const void* logits_bf16, int ldl, const int32_t* draft, int B, int D, int V,
+                           float temperature, const float* u, const float* u_next, int32_t* n_acc,
+                           int32_t* next_token, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (B < 0 || D < 0 || V <= 0) return QUASAR_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f) || temperature == INFINITY) return QUASAR_ERR_INVALID_ARG;
+  const bool sampled = temperature > 0.f;
+  if (ldl < V || ldl % 8 != 0) return QUASAR_ERR_UNSUPPORTED;
+  if (B == 0) return QUASAR_OK;  // no sequences: nothing is read or written
+  if (!logits_bf16 || !n_acc || (D > 0 && !draft) || (sampled && D > 0 && !u)) return QUASAR_ERR_INVALID_ARG;
+  if (!aligned(logits_bf16, 16)) return QUASAR_ERR_UNSUPPORTED;
+  if ((long long)B * (D + 1) > 65535) return QUASAR_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < workspace_size(B, D, V) || !aligned(workspace, 256)) return QUASAR_ERR_WORKSPACE;
+  const long long rows = (long long)B * (D + 1);
+  // As many chunks per row as fill one wave of resident CTAs (a second,
+  // mostly empty wave would leave HBM idle), within the workspace's records.
+  int ch, S;
+  chunk_geometry(rows, V, &ch, &S);
+  {
+    int per_sm = 0;
+    const cudaError_t e = sampled ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<true>, THREADS, 0)
+                                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<false>, THREADS, 0);
+    const long long resident = (long long)per_sm * sm_count();
+    if (e == cudaSuccess && resident > 0) {
+      const long long want = resident / rows;
+      const int s0 = (int)(want < 1 ? 1 : (want < S ? want : S));
+      chunk_geometry_s(V, s0, &ch, &S);
+    } else {
+      cudaGetLastError();
+    }
+  }
+  unsigned int* cnt = reinterpret_cast<unsigned int*>(workspace);
+  Partial* part = reinterpret_cast<Partial*>(reinterpret_cast<uint8_t*>(workspace) + align256((size_t)B * 4));
+  const dim3 grid(S, (unsigned)rows);
+  const float invT = sampled ? 1.0f / temperature : 0.f;
+  const uint16_t* lg = reinterpret_cast<const uint16_t*>(logits_bf16);
+  if (sampled)
+    verify_kernel<true><<<grid, THREADS, 0, stream>>>(lg, ldl, draft, D, V, ch, S, invT, u, u_next, n_acc,
+                                                      next_token, part, cnt);
+  else
+    verify_kernel<false><<<grid, THREADS, 0, stream>>>(lg, ldl, draft, D, V, ch, S, invT, u, nullptr, n_acc,
+                                                       next_token, part, cnt);
+  return cuda_status(cudaGetLastError());
+}
+
 }  // namespace verify
 }  // namespace quasar
 
@@ -217,35 +380,19 @@ size_t quasar_verify_accept_workspace_size(int B, int D, int V) { return quasar:
 
 quasar_status_t quasar_verify_accept(const void* logits_bf16, int ldl, const int32_t* draft, int B, int D, int V,
                                      float temperature, const float* u, int32_t* n_acc, int32_t* next_token,
-                                     void* workspace, size_t ws_bytes, quasar_stream_t stream_) {
-  using namespace quasar;
-  using namespace quasar::verify;
-  if (B < 0 || D < 0 || V <= 0) return QUASAR_ERR_INVALID_ARG;
-  if (!(temperature >= 0.f) || temperature == INFINITY) return QUASAR_ERR_INVALID_ARG;
-  const bool sampled = temperature > 0.f;
-  if (sampled && next_token) return QUASAR_ERR_INVALID_ARG;
-  if (ldl < V || ldl % 8 != 0) return QUASAR_ERR_UNSUPPORTED;
-  if (B == 0) return QUASAR_OK;  // no sequences: nothing is read or written
-  if (!logits_bf16 || !n_acc || (D > 0 && !draft) || (sampled && D > 0 && !u)) return QUASAR_ERR_INVALID_ARG;
-  if (!aligned(logits_bf16, 16)) return QUASAR_ERR_UNSUPPORTED;
-  if ((long long)B * (D + 1) > 65535) return QUASAR_ERR_UNSUPPORTED;
-  if (!workspace || ws_bytes < workspace_size(B, D, V) || !aligned(workspace, 256)) return QUASAR_ERR_WORKSPACE;
-  const long long rows = (long long)B * (D + 1);
-  int ch, S;
-  chunk_geometry(rows, V, &ch, &S);
-  unsigned int* cnt = reinterpret_cast<unsigned int*>(workspace);
-  Partial* part = reinterpret_cast<Partial*>(reinterpret_cast<uint8_t*>(workspace) + align256((size_t)B * 4));
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  const dim3 grid(S, (unsigned)rows);
-  const float invT = sampled ? 1.0f / temperature : 0.f;
-  const uint16_t* lg = reinterpret_cast<const uint16_t*>(logits_bf16);
-  if (sampled)
-    verify_kernel<true><<<grid, THREADS, 0, stream>>>(lg, ldl, draft, D, V, ch, S, invT, u, n_acc, nullptr, part,
-                                                      cnt);
-  else
-    verify_kernel<false><<<grid, THREADS, 0, stream>>>(lg, ldl, draft, D, V, ch, S, invT, u, n_acc, next_token,
-                                                       part, cnt);
-  return cuda_status(cudaGetLastError());
+                                     void* workspace, size_t ws_bytes, quasar_stream_t stream) {
+  if (temperature > 0.f && next_token) return QUASAR_ERR_INVALID_ARG;
+  return quasar::verify::run(logits_bf16, ldl, draft, B, D, V, temperature, u, nullptr, n_acc, next_token, workspace,
+                             ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+quasar_status_t quasar_verify_sample(const void* logits_bf16, int ldl, const int32_t* draft, int B, int D, int V,
+                                     float temperature, const float* u, const float* u_next, int32_t* n_acc,
+                                     int32_t* next_token, void* workspace, size_t ws_bytes, quasar_stream_t stream) {
+  if (!(temperature > 0.f) || temperature == INFINITY) return QUASAR_ERR_INVALID_ARG;
+  if (B > 0 && (!u_next || !next_token)) return QUASAR_ERR_INVALID_ARG;
+  return quasar::verify::run(logits_bf16, ldl, draft, B, D, V, temperature, u, u_next, n_acc, next_token, workspace,
+                             ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

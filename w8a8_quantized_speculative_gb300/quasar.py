@@ -46,6 +46,7 @@ _SIGS = {
     "quasar_w8a8_linear_noalloc": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p]),
     "quasar_verify_accept_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_verify_accept": (_i, [_p, _i, _p, _i, _i, _i, _f, _p, _p, _p, _p, _sz, _p]),
+    "quasar_verify_sample": (_i, [_p, _i, _p, _i, _i, _i, _f, _p, _p, _p, _p, _p, _sz, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -264,6 +265,31 @@ def verify_accept(logits: torch.Tensor, draft: torch.Tensor, temperature: float 
            "verify_accept")
     return n_acc, next_token
 
+
+
+def verify_sample(logits: torch.Tensor, draft: torch.Tensor, temperature: float, u, u_next, n_acc=None,
+                  next_token=None, workspace: Workspace | None = None, stream=None):
+    """T > 0: accepted prefix length (int32 [B]) and the lossless next token
+    (int32 [B]): a draw from row n_acc's softmax without the rejected draft,
+    or from the bonus row after D acceptances, by inverse CDF on u_next [B]."""
+    _need(logits, torch.bfloat16, "logits")
+    _need(draft, torch.int32, "draft")
+    _need(u_next, torch.float32, "u_next")
+    if logits.dim() != 3 or logits.stride(2) != 1 or (
+            logits.shape[0] > 1 and logits.stride(0) != logits.shape[1] * logits.stride(1)):
+        raise ValueError("logits must be [B][D+1][V] with unit inner stride and evenly spaced rows")
+    B, R, V = logits.shape
+    D = R - 1
+    if D > 0:
+        _need(u, torch.float32, "u")
+    n_acc = torch.empty(B, dtype=torch.int32, device=logits.device) if n_acc is None else n_acc
+    next_token = torch.empty(B, dtype=torch.int32, device=logits.device) if next_token is None else next_token
+    ws = _ws(workspace, logits.device)
+    buf = ws.get(int(lib.quasar_verify_accept_workspace_size(B, D, V)))
+    _check(lib.quasar_verify_sample(_ptr(logits), logits.stride(1), _ptr(draft), B, D, V, float(temperature),
+                                    _ptr(u), _ptr(u_next), _ptr(n_acc), _ptr(next_token), _ptr(buf), buf.numel(),
+                                    _stream(stream)), "verify_sample")
+    return n_acc, next_token
 
 def get_device_error(stream=None):
     """Synchronise and return (status, site) of the library's device error word."""
