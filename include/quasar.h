@@ -61,6 +61,15 @@ int quasar_version(void);
  * After a timeout, any workspace in use must be zero-filled again. */
 quasar_status_t quasar_get_device_error(quasar_stream_t stream, uint32_t* site);
 
+/* Self-test of the bounded waits (this library's failure handling; the pages
+ * have no counterpart): launches one CTA whose thread waits on an mbarrier
+ * that nothing completes.  The wait runs out after `limit_ns` (1 us .. 10 s),
+ * records site code 12 in the device error word and the kernel returns; the
+ * context stays usable and quasar_get_device_error reports
+ * QUASAR_ERR_TIMEOUT.  Returns QUASAR_ERR_INVALID_ARG for a limit out of
+ * range, else the launch status. */
+quasar_status_t quasar_selftest_wait_timeout(uint64_t limit_ns, quasar_stream_t stream);
+
 /* Bound for the device-side waits, in nanoseconds (default 2e9 = 2 s).
  * Host-side setting applied to the next launches; 0 restores the default. */
 quasar_status_t quasar_set_wait_limit_ns(uint64_t ns);

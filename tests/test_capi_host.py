@@ -170,3 +170,12 @@ def test_verify_sample_rejects_bad_arguments(lib):
     assert call(u=None) == 1            # D > 0 needs the acceptance uniforms
     assert call(ldl=100) == 2
     assert call(B=0) == 0
+
+
+def test_selftest_wait_rejects_limits_out_of_range(lib):
+    f = lib.quasar_selftest_wait_timeout
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_uint64, ctypes.c_void_p]
+    assert f(0, None) == 1
+    assert f(999, None) == 1
+    assert f(10_000_000_001, None) == 1

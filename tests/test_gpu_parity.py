@@ -495,3 +495,24 @@ def test_verify_sample_is_lossless_on_gpu():
     chi2 = float(((counts - N * p) ** 2 / (N * p)).sum())
     assert chi2 < 29.88, (chi2, counts, N * p)      # chi-square(7) upper 1e-4 point
     assert not np.any(nxt[n_acc == 0] == d)
+
+
+# ---------------------------------------------------------------- bounded waits
+
+def test_bounded_wait_runs_out_and_context_survives():
+    """A wait on a barrier nothing completes gives up after its limit, the
+    error word reports it (site 12), and the next call runs normally."""
+    st, _ = q.get_device_error()
+    assert st == 0
+    q.selftest_wait_timeout(2_000_000)
+    st, site = q.get_device_error()
+    assert st == 5 and (site & 0xFFFF) == 12
+    st, site = q.get_device_error()
+    assert st == 0 and site == 0                     # read and cleared
+    case = synth.small_case()
+    x, w, s, (xq, sa, wq, sw) = gpu_linear_case(case)
+    y = q.w8a8_linear(xq, sa, wq, sw)
+    xq_r, sa_r = orc.smooth_quant_act(x, s)
+    wq_r, sw_r = orc.pack_weights(w, s)
+    assert np.array_equal(host_bf16_bits(y), orc.w8a8_linear(xq_r, sa_r, wq_r, sw_r))
+    assert q.get_device_error()[0] == 0

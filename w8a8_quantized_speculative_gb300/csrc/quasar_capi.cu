@@ -37,6 +37,21 @@ unsigned int* device_error_word() {
 
 unsigned long long wait_limit_ns() { return g_wait_ns.load(); }
 
+// Self-test of the bounded waits: one thread waits on an mbarrier that
+// nothing ever completes, runs out after limit_ns, records SITE_SELFTEST and
+// returns.
+__global__ void wait_selftest_kernel(unsigned int* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0u, &abort_flag, err, SITE_SELFTEST, limit_ns);
+}
+
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
@@ -101,6 +116,14 @@ int quasar_version(void) { return (1 << 16) | 0; }
 quasar_status_t quasar_set_wait_limit_ns(uint64_t ns) {
   quasar::g_wait_ns.store(ns ? ns : quasar::kDefaultWaitNs);
   return QUASAR_OK;
+}
+
+quasar_status_t quasar_selftest_wait_timeout(uint64_t limit_ns, quasar_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 10000000000ull) return QUASAR_ERR_INVALID_ARG;
+  unsigned int* err = quasar::device_error_word();
+  if (!err) return QUASAR_ERR_CUDA;
+  quasar::wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err, limit_ns);
+  return quasar::cuda_status(cudaGetLastError());
 }
 
 quasar_status_t quasar_get_device_error(quasar_stream_t stream, uint32_t* site) {

@@ -47,6 +47,7 @@ enum : unsigned int {
   SITE_SKINNY_FULL = 8,
   SITE_SKINNY_EMPTY = 9,
   SITE_SKINNY_DRAIN = 10,
+  SITE_SELFTEST = 12,
 };
 
 // ---------------------------------------------------------------- device side

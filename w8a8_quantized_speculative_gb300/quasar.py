@@ -32,6 +32,7 @@ _SIGS = {
     "quasar_version": (_i, []),
     "quasar_get_device_error": (_i, [_p, ctypes.POINTER(ctypes.c_uint32)]),
     "quasar_set_wait_limit_ns": (_i, [ctypes.c_uint64]),
+    "quasar_selftest_wait_timeout": (_i, [ctypes.c_uint64, _p]),
     "quasar_calibrate_workspace_size": (_sz, [_i]),
     "quasar_calibrate_smooth": (_i, [_p, _i, _i, _p, _i, _i, _i, _f, _p, _p, _sz, _p]),
     "quasar_packed_weight_bytes": (_sz, [_i, _i]),
@@ -296,6 +297,12 @@ def get_device_error(stream=None):
     site = ctypes.c_uint32(0)
     st = lib.quasar_get_device_error(_stream(stream), ctypes.byref(site))
     return st, site.value
+
+
+def selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None):
+    """Launch a kernel whose bounded wait must run out after limit_ns (the
+    error word then reports QUASAR_ERR_TIMEOUT with site 12)."""
+    _check(lib.quasar_selftest_wait_timeout(int(limit_ns), _stream(stream)), "selftest_wait_timeout")
 
 
 def set_wait_limit_ns(ns: int):
