@@ -241,6 +241,14 @@ QUASAR_DEVICE_INLINE void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Cluster barrier that orders execution only: no CTA leaves before every
+// thread of the cluster has arrived (the remote shared-memory loads it waits
+// for have returned their values by then), without waiting for this
+// thread's global stores to become visible.
+QUASAR_DEVICE_INLINE void cluster_sync_exec() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // int4 at the same shared-memory offset in cluster CTA `rank`.
 QUASAR_DEVICE_INLINE int4 ld_dsmem_int4(const void* local, uint32_t rank) {
   uint32_t remote;
@@ -492,7 +500,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     __syncwarp();
     if (p.mode == 1) {   // the consumers' two cluster barriers
       cluster_sync_all();
-      cluster_sync_all();
+      cluster_sync_exec();
     }
     return;
   }
@@ -672,7 +680,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       epilogue<NT8>(p, v, u_first, mt_f, nh, lane, sa_s, sw_s);
     }
     __syncwarp();
-    cluster_sync_all();
+    cluster_sync_exec();
   }
 }
 
