@@ -46,6 +46,10 @@ The pages leave the numeric details open.  The readings taken here are:
       u_next per sequence: the smallest v whose cumulative weight exceeds
       u_next times the total; if no weight is left, the lowest index other
       than the draft.
+  R8  4-bit weights (the pages' future ultra-low-bit verifier, a kernel
+      variant only): per output channel, scale = absmax/7, code =
+      clamp(rne(w' * (7/absmax)), -7, 7), in fp32 as R2; activations as R2;
+      the same exact integer GEMM and dequantization (R3, R4).
 
 Every function below is pinned by tests under ``tests/`` against hand-derived
 values, closed forms, invariants or brute force (see each docstring).
@@ -105,14 +109,16 @@ def calibrate_smooth(x_cal_bits: np.ndarray, w_bits: np.ndarray, alpha: float = 
 # ---------------------------------------------------------------------------
 # Symmetric per-row quantizer (reading R2).
 
-def quantize_rows(v: np.ndarray):
-    """Quantize each row of an fp32 matrix to INT8 codes with one fp32 scale.
+def quantize_rows(v: np.ndarray, qmax: int = QMAX):
+    """Quantize each row of an fp32 matrix to integer codes with one fp32 scale.
 
-    pt §2: symmetric uniform quantization to 8 bits.  For a row with
-    absmax a > 0: scale = a/127, code = clamp(rne(v * (127/a)), -127, 127).
-    Pinned: tie-rounding fixture, |code*scale - v| <= scale/2 bound, a code
-    of magnitude 127 in every nonzero row, zero rows.
+    pt §2: symmetric uniform quantization to 8 bits (qmax = 127; qmax = 7
+    for the 4-bit weights of reading R8).  For a row with absmax a > 0:
+    scale = a/qmax, code = clamp(rne(v * (qmax/a)), -qmax, qmax).
+    Pinned: tie-rounding fixtures, |code*scale - v| <= scale/2 bound, a code
+    of magnitude qmax in every nonzero row, zero rows.
     """
+    QMAX = qmax
     v = np.asarray(v, dtype=F32)
     amax = np.abs(v).max(axis=1) if v.shape[1] else np.zeros(v.shape[0], F32)
     scale = np.zeros(v.shape[0], dtype=F32)
@@ -137,6 +143,14 @@ def pack_weights(w_bits: np.ndarray, smooth: np.ndarray):
     w = bf16_to_f32(w_bits)
     wp = w / np.asarray(smooth, dtype=F32)[None, :]     # correctly rounded fp32 division
     return quantize_rows(wp)
+
+
+def pack_weights_w4(w_bits: np.ndarray, smooth: np.ndarray):
+    """4-bit weights (reading R8): as pack_weights with codes in [-7, 7],
+    sw = absmax / 7.  Returns (Wq int8 [N][K] holding the 4-bit codes, sw)."""
+    w = bf16_to_f32(w_bits)
+    wp = w / np.asarray(smooth, dtype=F32)[None, :]
+    return quantize_rows(wp, qmax=7)
 
 
 def smooth_quant_act(x_bits: np.ndarray, smooth: np.ndarray):

@@ -428,3 +428,36 @@ def test_sample_is_lossless_chi_square(d):
     keep = np.where(n_acc == 1, d, np.minimum(np.searchsorted(np.cumsum(p), u_next, side="right"), V - 1))
     bad = float(((np.bincount(keep, minlength=V) - N * p) ** 2 / (N * p)).sum())
     assert bad > 100.0
+
+
+# ---------------------------------------------------------------- 4-bit weights (R8)
+
+def test_quantizer_w4_fixture():
+    """Hand-derived: absmax 3.5 -> inv = 7/3.5 = 2, scale = 0.5; codes
+    rne(1) = 1, rne(-3.5) = -4 (tie to even), rne(7) = 7, rne(2.5) = 2."""
+    v = np.array([[0.5, -1.75, 3.5, 1.25], [0.0, 0.0, 0.0, 0.0]], np.float32)
+    codes, scale = orc.quantize_rows(v, qmax=7)
+    assert codes.tolist() == [[1, -4, 7, 2], [0, 0, 0, 0]]
+    assert scale.tolist() == [0.5, 0.0]
+
+
+def test_quantizer_w4_invariants():
+    rng = np.random.default_rng(44)
+    v = (rng.standard_normal((64, 300)) * rng.uniform(0.01, 10, (64, 1))).astype(np.float32)
+    codes, scale = orc.quantize_rows(v, qmax=7)
+    assert codes.min() >= -7 and codes.max() <= 7
+    assert np.all(np.abs(codes).max(axis=1) == 7)
+    err = np.abs(codes.astype(np.float64) * scale[:, None] - v)
+    assert np.all(err <= scale[:, None] * (0.5 + 1e-5))
+
+
+def test_pack_weights_w4_is_smoothed_quantizer():
+    """Folding the smoothing factor first, then the 4-bit per-channel
+    quantizer; a code of magnitude 7 in every row."""
+    rng = np.random.default_rng(45)
+    w = synth.f32_to_bf16_bits(rng.standard_normal((16, 64)) * 0.02)
+    s = rng.uniform(0.5, 2.0, 64).astype(np.float32)
+    wq, sw = orc.pack_weights_w4(w, s)
+    wq_ref, sw_ref = orc.quantize_rows(orc.bf16_to_f32(w) / s[None, :], qmax=7)
+    assert np.array_equal(wq, wq_ref) and np.array_equal(sw, sw_ref)
+    assert np.all(np.abs(wq).max(axis=1) == 7)
