@@ -397,6 +397,7 @@ def main_gpu(args):
     extra = {}
     if rank == 0 and world == 1 and not args.no_extras:
         extra["sweep"] = run_sweep(q, dev, stream, ws, hbm)
+        extra["sweep_w4a8"] = run_sweep_w4(q, dev, stream, ws, hbm)
         extra["verify"] = run_verify(q, dev, stream, ws, hbm)
 
     cpu = None
@@ -479,6 +480,34 @@ def run_sweep(q, dev, stream, ws, hbm):
                         "cublas_bf16_us": round(cub, 3),
                         "speedup_vs_bf16": round(cub / us, 3)})
         del wqs, sws, wbf
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_sweep_w4(q, dev, stream, ws, hbm):
+    """The W4A8 variant (4-bit weight blocks, register-path kernel, M <= 24)
+    on the same linears, cold L2; bytes per weight halve."""
+    import torch
+    out = []
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    for name in ("qkv", "o", "gate_up", "down"):
+        K, N = synth.LINEARS[name]
+        ncopy = copies_for_cold_l2(N * K // 2)
+        w4 = torch.randint(-7, 8, (N, K), dtype=torch.int8, device=dev, generator=gen)
+        wps = [q.tile_weights_w4(w4) for _ in range(ncopy)]
+        del w4
+        sw = torch.rand(N, device=dev, generator=gen) * 1e-3
+        for M in (1, 8, 20):
+            xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
+            sa = torch.rand(M, device=dev, generator=gen)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws.get(q.lib.quasar_w8a8_linear_workspace_size(M, N, K))
+            us = _time_graph(torch, stream, lambda i: q.w4a8_linear(xq, sa, wps[i % ncopy], sw, y=y, workspace=ws), 60)
+            tb = (N * K // 2 + 4 * N) / (us * 1e-6) / 1e12
+            out.append({"linear": name, "M": M, "us": round(us, 3), "weight_TBps": round(tb, 3),
+                        "hbm_frac": round(tb * 1e3 / hbm, 3)})
+        del wps
         torch.cuda.empty_cache()
     return out
 

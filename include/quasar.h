@@ -188,6 +188,45 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
                                    void* workspace, size_t ws_bytes,
                                    quasar_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * W4A8 variant (NEXT-4; the pages' future ultra-low-bit verifier, as a
+ * kernel variant only -- no accuracy claim).
+ *
+ * pt §2 step 1 with 4-bit codes: per output channel n, in fp32 as A1,
+ *   w' = float(W[n][k]) / smooth[k],  a = max_k |w'|,  sw[n] = a / 7,
+ *   Wq4[n][k] = clamp(rne(w' * (7 / a)), -7, 7)        (0 if a == 0)
+ * and then the A3 + A4 linear with the same exact integer sums and the same
+ * epilogue: Y = bf16_rne((float(acc) * sa[m]) * sw[n]).
+ *
+ * Packed 4-bit layout: blocks of 128 rows x 128 K, block (tn, kb) at byte
+ * offset (tn * KB + kb) * 8192; row r (n = 128 tn + r) takes bytes
+ * [64 r, 64 r + 64); its 16-byte chunk c (k = 128 kb + 32 c .. +31) sits
+ * at chunk position c ^ ((r >> 1) & 3).  Byte j = 4 w + b of a chunk holds
+ * code(k0 + 4 w + b) + 8 in its low nibble and code(k0 + 16 + 4 w + b) + 8
+ * in its high nibble (k0 = 128 kb + 32 c).  Rows n >= N and columns k >= K
+ * hold code 0 (nibble 8).  Size: quasar_packed_weight_bytes_w4(N, K).
+ *
+ *   quasar_pack_weights_w4: W [N][ldw] BF16 (ldw >= K, ldw % 8 == 0),
+ *     smooth [K] fp32 -> Wp4 (K % 16 == 0), sw [N] fp32.
+ *   quasar_tile_weights_w4: row-major codes [N][K] in [-8, 7] -> Wp4.
+ *   quasar_w4a8_linear: as quasar_w8a8_linear with Wp4 for Wp, for
+ *     1 <= M <= 24 (the register-path kernel; QUASAR_ERR_UNSUPPORTED
+ *     above); workspace: quasar_w8a8_linear_workspace_size(M, N, K) bytes
+ *     under the same zero-filled contract.
+ * ------------------------------------------------------------------------ */
+size_t quasar_packed_weight_bytes_w4(int N, int K);
+quasar_status_t quasar_pack_weights_w4(const void* W_bf16, int ldw, const float* smooth,
+                                       int N, int K, int8_t* Wp4, float* sw,
+                                       quasar_stream_t stream);
+quasar_status_t quasar_tile_weights_w4(const int8_t* Wq4, int N, int K, int8_t* Wp4,
+                                       quasar_stream_t stream);
+quasar_status_t quasar_w4a8_linear(const int8_t* Xq, const float* sa,
+                                   const int8_t* Wp4, const float* sw,
+                                   int M, int N, int K,
+                                   void* Y_bf16, int ldy,
+                                   void* workspace, size_t ws_bytes,
+                                   quasar_stream_t stream);
+
 /* A2 + A3 + A4 in one call: smooth + quantize the BF16 activations and run
  * the W8A8 linear on the codes.
  *   Y[m][n] is bit-identical to quasar_smooth_quant_act(X, smooth) followed by

@@ -516,3 +516,73 @@ def test_bounded_wait_runs_out_and_context_survives():
     wq_r, sw_r = orc.pack_weights(w, s)
     assert np.array_equal(host_bf16_bits(y), orc.w8a8_linear(xq_r, sa_r, wq_r, sw_r))
     assert q.get_device_error()[0] == 0
+
+
+# ---------------------------------------------------------------- W4A8 variant
+
+from tests.gpu_util import unpack_weights_w4  # noqa: E402
+
+
+@pytest.mark.parametrize("N,K", [(136, 144), (512, 4096), (264, 1040)])
+def test_tile_weights_w4_layout(N, K):
+    rng = np.random.default_rng(N + K)
+    wq = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    wp = q.tile_weights_w4(dev(wq)).cpu().numpy()
+    assert wp.size == q.packed_weight_bytes_w4(N, K)
+    assert np.array_equal(unpack_weights_w4(wp, N, K), wq)
+    full = unpack_weights_w4(wp, ((N + 127) // 128) * 128, ((K + 127) // 128) * 128)
+    assert not full[N:].any() and not full[:, K:].any()
+
+
+@pytest.mark.parametrize("name", ["qkv", "down"])
+def test_pack_weights_w4_bit_exact(name):
+    K, N = synth.LINEARS[name]
+    case = synth.sweep_case(name, 16)
+    w = case.w()
+    s = orc.calibrate_smooth(case.x_cal(), w)
+    wp, sw = q.pack_weights_w4(dev_bf16(w), dev(s))
+    wq_r, sw_r = orc.pack_weights_w4(w, s)
+    assert np.array_equal(unpack_weights_w4(wp.cpu().numpy(), N, K), wq_r)
+    assert np.array_equal(sw.cpu().numpy().view(np.uint32), sw_r.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 16), (3, 136, 144), (8, 512, 256), (16, 4096, 4096), (20, 6144, 4096),
+                                   (24, 264, 2064), (12, 24576, 1024), (5, 19456, 512), (20, 4096, 12288)])
+def test_w4a8_linear_matches_oracle(M, N, K):
+    rng = np.random.default_rng(M * 31 + N + K)
+    xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    wq = rng.integers(-7, 8, size=(N, K)).astype(np.int8)
+    sa = rng.uniform(0.01, 0.1, M).astype(np.float32)
+    sw = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    ws = q.Workspace()
+    y = q.w4a8_linear(dev(xq), dev(sa), q.tile_weights_w4(dev(wq)), dev(sw), workspace=ws)
+    y_r = orc.w8a8_linear(xq, sa, wq, sw)
+    assert np.array_equal(host_bf16_bits(y), y_r)
+    check_ws_zero(ws)
+
+
+def test_w4a8_qwen3_attention_end_to_end():
+    """Calibrate, pack to 4 bits, quantize the activations, run the W4A8
+    linear: identical to the oracle's W4A8 result, and near the unquantized
+    product."""
+    for case in synth.attention_cases():
+        x, w, xc = case.x(), case.w(), case.x_cal()
+        smooth = q.calibrate_smooth(dev_bf16(xc), dev_bf16(w))
+        s = smooth.cpu().numpy()
+        wp, sw = q.pack_weights_w4(dev_bf16(w), smooth)
+        xq, sa = q.smooth_quant_act(dev_bf16(x), smooth)
+        y = q.w4a8_linear(xq, sa, wp, sw)
+        xq_r, sa_r = orc.smooth_quant_act(x, s)
+        wq_r, sw_r = orc.pack_weights_w4(w, s)
+        assert np.array_equal(host_bf16_bits(y), orc.w8a8_linear(xq_r, sa_r, wq_r, sw_r))
+        yv = synth.bf16_bits_to_f32(host_bf16_bits(y)).astype(np.float64)
+        ref = orc.reference_linear_f64(x, w)
+        # a sanity bound only (per-channel 4-bit codes, no accuracy claim): ~0.2 here
+        assert np.linalg.norm(yv - ref) / np.linalg.norm(ref) <= 0.3, case.name
+
+
+def test_w4a8_rejects_large_m():
+    xq = torch.zeros((32, 256), dtype=torch.int8, device="cuda")
+    wp = q.tile_weights_w4(torch.zeros((128, 256), dtype=torch.int8, device="cuda"))
+    with pytest.raises(q.QuasarError):
+        q.w4a8_linear(xq, torch.ones(32, device="cuda"), wp, torch.ones(128, device="cuda"))

@@ -198,6 +198,82 @@ __global__ void tile_weights_kernel(const int8_t* __restrict__ src, int N, int K
   *reinterpret_cast<uint4*>(dst + packed_offset(n, k, (K + 127) >> 7)) = make_uint4(v.x ^ b, v.y ^ b, v.z ^ b, v.w ^ b);
 }
 
+// ---- 4-bit weights.  Byte offset of 16-byte chunk c (K values 32c .. 32c+31
+// of a block) of packed row n: blocks of 128 rows x 128 K are 8 KB, row r
+// at 64 r, chunk c at (c ^ ((r >> 1) & 3)) * 16.  Byte j = 4 w + b of a
+// chunk holds code(32c + 4w + b) + 8 in its low nibble and
+// code(32c + 16 + 4w + b) + 8 in its high nibble.
+QUASAR_DEVICE_INLINE size_t packed4_offset(int n, int k32, int KB) {
+  const int r = n & 127, c = (k32 & 127) >> 5;
+  return (((size_t)(n >> 7) * KB + (k32 >> 7)) * 128 + r) * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+}
+
+// Sixteen packed bytes from the 32 codes of one chunk (missing K: code 0).
+QUASAR_DEVICE_INLINE uint4 pack4_chunk(const int (&code)[32]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t lo = (uint32_t)(code[4 * q + b] + 8) & 0xF, hi = (uint32_t)(code[16 + 4 * q + b] + 8) & 0xF;
+      v |= (lo | (hi << 4)) << (8 * b);
+    }
+    w[q] = v;
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One CTA per weight row: w' = W / smooth, a = max |w'|, sw = a / 7,
+// code = clamp(rne(w' * (7 / a)), -7, 7); the second pass packs 32 codes
+// per thread step.
+__global__ void __launch_bounds__(THREADS) quant_rows_w4_kernel(const uint16_t* __restrict__ in, int ld,
+                                                                const float* __restrict__ smooth, int K,
+                                                                int8_t* __restrict__ q, float* __restrict__ scale) {
+  const int row = blockIdx.x;
+  const uint16_t* src = in + (size_t)row * ld;
+  float amax = 0.f;
+  for (int k = threadIdx.x; k < K; k += THREADS)
+    amax = fmaxf(amax, fabsf(__fdiv_rn(__uint_as_float((uint32_t)src[k] << 16), smooth[k])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[THREADS / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < THREADS / 32; ++w) amax = fmaxf(amax, red[w]);
+  const float inv = amax > 0.f ? __fdiv_rn(7.f, amax) : 0.f;
+  if (threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 7.f) : 0.f;
+  const int KB = (K + 127) >> 7;
+  for (int k32 = 32 * threadIdx.x; k32 < K; k32 += 32 * THREADS) {
+    int code[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int k = k32 + i;
+      int c = 0;
+      if (k < K && amax > 0.f) {
+        c = __float2int_rn(__fmul_rn(__fdiv_rn(__uint_as_float((uint32_t)src[k] << 16), smooth[k]), inv));
+        c = max(-7, min(7, c));
+      }
+      code[i] = c;
+    }
+    *reinterpret_cast<uint4*>(q + packed4_offset(row, k32, KB)) = pack4_chunk(code);
+  }
+}
+
+// Row-major codes [N][K] in [-8, 7] -> 4-bit packed layout, one chunk per thread.
+__global__ void tile_weights_w4_kernel(const int8_t* __restrict__ src, int N, int K, int8_t* __restrict__ dst) {
+  const int chunks = (K + 31) / 32;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)N * chunks) return;
+  const int n = (int)(i / chunks), k32 = (int)(i % chunks) * 32;
+  int code[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) code[j] = k32 + j < K ? (int)src[(size_t)n * K + k32 + j] : 0;
+  *reinterpret_cast<uint4*>(dst + packed4_offset(n, k32, (K + 127) >> 7)) = pack4_chunk(code);
+}
+
 size_t packed_bytes(int N, int K) {
   if (N <= 0 || K <= 0) return 0;
   return (size_t)((N + 127) / 128) * ((K + 127) / 128) * 128 * 128;
@@ -260,6 +336,37 @@ quasar_status_t quasar_tile_weights(const int8_t* Wq, int N, int K, int8_t* Wp, 
   if (e != cudaSuccess) return cuda_status(e);
   const long long items = (long long)N * (K / 16);
   quant::tile_weights_kernel<<<(unsigned)((items + 255) / 256), 256, 0, stream>>>(Wq, N, K, Wp);
+  return cuda_status(cudaGetLastError());
+}
+
+size_t quasar_packed_weight_bytes_w4(int N, int K) { return quasar::quant::packed_bytes(N, K) / 2; }
+
+quasar_status_t quasar_pack_weights_w4(const void* W_bf16, int ldw, const float* smooth, int N, int K, int8_t* Wp4,
+                                       float* sw, quasar_stream_t stream_) {
+  using namespace quasar;
+  if (N < 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
+  if (K % 16 != 0 || ldw < K || ldw % 8 != 0) return QUASAR_ERR_UNSUPPORTED;
+  if (N == 0) return QUASAR_OK;
+  if (!W_bf16 || !smooth || !Wp4 || !sw) return QUASAR_ERR_INVALID_ARG;
+  if (!aligned(W_bf16, 16) || !aligned(smooth, 4) || !aligned(Wp4, 16) || !aligned(sw, 4)) return QUASAR_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  cudaError_t e = cudaMemsetAsync(Wp4, 0x88, quant::packed_bytes(N, K) / 2, stream);   // padding: code 0
+  if (e != cudaSuccess) return cuda_status(e);
+  quant::quant_rows_w4_kernel<<<N, quant::THREADS, 0, stream>>>(reinterpret_cast<const uint16_t*>(W_bf16), ldw, smooth,
+                                                                 K, Wp4, sw);
+  return cuda_status(cudaGetLastError());
+}
+
+quasar_status_t quasar_tile_weights_w4(const int8_t* Wq4, int N, int K, int8_t* Wp4, quasar_stream_t stream_) {
+  using namespace quasar;
+  if (N <= 0 || K <= 0 || !Wq4 || !Wp4) return QUASAR_ERR_INVALID_ARG;
+  if (K % 16 != 0) return QUASAR_ERR_UNSUPPORTED;
+  if (!aligned(Wp4, 16)) return QUASAR_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  cudaError_t e = cudaMemsetAsync(Wp4, 0x88, quant::packed_bytes(N, K) / 2, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  const long long items = (long long)N * ((K + 31) / 32);
+  quant::tile_weights_w4_kernel<<<(unsigned)((items + 255) / 256), 256, 0, stream>>>(Wq4, N, K, Wp4);
   return cuda_status(cudaGetLastError());
 }
 

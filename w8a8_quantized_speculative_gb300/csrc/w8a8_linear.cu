@@ -54,7 +54,8 @@ namespace skinny {  // w8a8_skinny.cu: the register-path kernel for M <= 32
 bool handles(int M);
 size_t slots_bytes(int M, int N, int K);
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
-                    void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream);
+                    void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream,
+                    bool w4);
 }  // namespace skinny
 
 namespace gemm {
@@ -607,7 +608,8 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   int32_t* ws_acc = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + align256((size_t)s.tiles * CONV_WARPS * 4));
   // A few tokens: the register-path kernel (same packed weights, same
   // workspace layout, fewer counters per tile).
-  if (skinny::handles(M)) return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream);
+  if (skinny::handles(M))
+    return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream, false);
 
 
   CUtensorMap tx;
@@ -644,6 +646,29 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
     default: e = launch_nt<128>(tx, p, grid, stream); break;
   }
   return cuda_status(e);
+}
+
+// ------------------------------------------------------------ 4-bit weights
+//
+// W4A8: the register-path kernel with 4-bit weight blocks (same schedules,
+// same workspace); the token counts it serves (M <= 24) are where the weight
+// stream sets the time.
+quasar_status_t run_w4(const int8_t* Xq, const float* sa, const int8_t* Wp4, const float* sw, int M, int N, int K,
+                       void* Y, int ldy, int32_t* acc_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (M < 0 || N <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
+  if (K % 16 != 0 || N % 8 != 0 || K > 131072) return QUASAR_ERR_UNSUPPORTED;
+  if (!acc_out && (ldy < N || ldy % 8 != 0)) return QUASAR_ERR_UNSUPPORTED;
+  if (M == 0) return QUASAR_OK;
+  if (!skinny::handles(M)) return QUASAR_ERR_UNSUPPORTED;
+  if (!Xq || !Wp4 || (!acc_out && (!Y || !sa || !sw))) return QUASAR_ERR_INVALID_ARG;
+  if (!aligned(Xq, 16) || !aligned(Wp4, 16) || (Y && !aligned(Y, 16)) || (acc_out && !aligned(acc_out, 16)) ||
+      (sa && !aligned(sa, 4)) || (sw && !aligned(sw, 4)))
+    return QUASAR_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < workspace_size(M, N, K) || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
+  const Shape s = shape_of(M, N, K);
+  uint32_t* ws_cnt = reinterpret_cast<uint32_t*>(ws);
+  void* slots = reinterpret_cast<uint8_t*>(ws) + align256((size_t)s.tiles * CONV_WARPS * 4);
+  return skinny::run(Xq, sa, Wp4, sw, M, N, K, Y, ldy, acc_out, ws_cnt, slots, stream, true);
 }
 
 // ------------------------------------------------------ fused activation path
@@ -741,6 +766,13 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa, const int8
                                    quasar_stream_t stream) {
   return quasar::gemm::run(Xq, sa, Wp, sw, M, N, K, Y_bf16, ldy, nullptr, workspace, ws_bytes,
                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+quasar_status_t quasar_w4a8_linear(const int8_t* Xq, const float* sa, const int8_t* Wp4, const float* sw, int M,
+                                   int N, int K, void* Y_bf16, int ldy, void* workspace, size_t ws_bytes,
+                                   quasar_stream_t stream) {
+  return quasar::gemm::run_w4(Xq, sa, Wp4, sw, M, N, K, Y_bf16, ldy, nullptr, workspace, ws_bytes,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 quasar_status_t quasar_int8_gemm_s32(const int8_t* Xq, const int8_t* Wp, int M, int N, int K, int32_t* acc,

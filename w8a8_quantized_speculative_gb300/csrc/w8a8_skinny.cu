@@ -61,6 +61,12 @@ constexpr int UM = 64;            // rows of a work unit (half a tile)
 constexpr int BK = 128;           // K bytes per block
 constexpr int PACKED_BLOCK = TILE_ROWS * BK;   // 16 KB packed block
 constexpr int HALF_BYTES = UM * BK;            // 8 KB: one unit's part of a block
+// 4-bit weights (W4): 64 bytes per row, the same 128 x 128 blocks at half
+// the size (8 KB, a unit's half 4 KB).
+template <bool W4>
+__host__ __device__ constexpr int packed_block() { return W4 ? PACKED_BLOCK / 2 : PACKED_BLOCK; }
+template <bool W4>
+__host__ __device__ constexpr int half_bytes() { return W4 ? HALF_BYTES / 2 : HALF_BYTES; }
 constexpr int KQ = 4;             // K quarters (32 K = 2 MMA K steps each)
 constexpr int UT = UM / 16;       // row tiles per unit
 constexpr int CWARPS = KQ;        // consumer warps: warp w owns K quarter w of all rows, finalizes row tile w
@@ -81,12 +87,13 @@ static_assert(RUN_BLOCKS % 2 == 0, "runs end on a stage boundary");
 // when a CTA's single accumulation run ends after its last block (the ring
 // is then idle): the cluster schedule with K slices of <= RUN_BLOCKS blocks.
 // The space it frees becomes more stages in flight.
-template <int NT8, bool RIR = false>
+template <int NT8, bool RIR = false, bool W4 = false>
 struct Cfg {
   static constexpr int NT = 8 * NT8;                        // token columns (padded to 8)
   static constexpr int NH = NT8;                            // token tiles of one finalizer share
   static constexpr int XB = NT * BK;                        // INT8 token tile of a block
-  static constexpr int BLK = HALF_BYTES + XB;               // one block: weight half + token tile
+  static constexpr int HB = half_bytes<W4>();               // a unit's weight bytes of a block
+  static constexpr int BLK = HB + XB;                       // one block: weight half + token tile
   static constexpr int STAGE = G * BLK;                     // multiple of 1024 (swizzle atoms)
   static constexpr int RED = UT * KQ * NT8 * 32 * 16;       // fp32 partials: [row tile][kq][token tile][lane]
   static constexpr int FIN = UT * NT8 * 32 * 16;            // int32 run sums: [row tile][token tile][lane]
@@ -218,8 +225,9 @@ struct Ring {
 };
 
 // Global address of unit u's half of packed block (tile u / 2, K block kb).
+template <bool W4>
 QUASAR_DEVICE_INLINE const uint8_t* unit_block(const Params& p, int u, int kb) {
-  return p.wp + ((size_t)(u >> 1) * p.KB + kb) * PACKED_BLOCK + (size_t)(u & 1) * HALF_BYTES;
+  return p.wp + ((size_t)(u >> 1) * p.KB + kb) * packed_block<W4>() + (size_t)(u & 1) * half_bytes<W4>();
 }
 
 QUASAR_DEVICE_INLINE void ldsm_x4(uint32_t addr, uint32_t& d0, uint32_t& d1, uint32_t& d2, uint32_t& d3) {
@@ -398,8 +406,49 @@ QUASAR_DEVICE_INLINE void count_segments(const Params& p, int ua, int na, int ub
 // One K block of this warp's work: its two K steps of the unit's 64 rows
 // against every token tile.  Token operands: row n = 8 ni + g of the
 // swizzled tile sits at n * 128, chunk ch at (ch ^ (n & 7)) * 16.
-template <int NT8>
+// Four bytes, each holding a 4-bit code + 8 (code in [-8, 7]) -> two fp16x2
+// words holding the codes exactly: the byte goes into the low mantissa of
+// 1024 (0x6400) and 1032 = 1024 + 8 is subtracted.
+QUASAR_DEVICE_INLINE void n4x4_to_f16x4(uint32_t u, uint32_t& lo, uint32_t& hi) {
+  uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+  uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+template <int NT8, bool W4>
 QUASAR_DEVICE_INLINE void consume_block(uint32_t st, uint32_t a_off, uint32_t b_off, float (&acc)[UT][NT8][4]) {
+  if constexpr (W4) {
+    // 4-bit weights: one ldmatrix word holds a row's 4 K values of both
+    // 16-K steps (low nibbles: the first, high nibbles: the second), each
+    // stored as code + 8.
+    uint32_t bq[2][NT8][2];
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+      for (int ni = 0; ni < NT8; ++ni)
+        s8x4_to_f16x4(lds32(st + (b_off ^ (ks << 4)) + (uint32_t)(ni * 8 * BK)), bq[ks][ni][0], bq[ks][ni][1]);
+#pragma unroll
+    for (int i2 = 0; i2 < UT / 2; ++i2) {
+      uint32_t d[4];
+      ldsm_x4(st + a_off + (uint32_t)(i2 * 32 * 64), d[0], d[1], d[2], d[3]);
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          uint32_t a0, a1, a2, a3;
+          n4x4_to_f16x4(ks ? (d[2 * i] >> 4) & 0x0F0F0F0Fu : d[2 * i] & 0x0F0F0F0Fu, a0, a2);
+          n4x4_to_f16x4(ks ? (d[2 * i + 1] >> 4) & 0x0F0F0F0Fu : d[2 * i + 1] & 0x0F0F0F0Fu, a1, a3);
+#pragma unroll
+          for (int ni = 0; ni < NT8; ++ni)
+            mma_16816(acc[2 * i2 + i][ni], a0, a1, a2, a3, bq[ks][ni][0], bq[ks][ni][1]);
+        }
+    }
+    return;
+  }
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     uint32_t bq[NT8][2];
@@ -423,10 +472,10 @@ QUASAR_DEVICE_INLINE void consume_block(uint32_t st, uint32_t a_off, uint32_t b_
   }
 }
 
-template <int NT8, bool RIR>
+template <int NT8, bool RIR, bool W4>
 __global__ void __launch_bounds__(THREADS, 2)
 w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
-  using C = Cfg<NT8, RIR>;
+  using C = Cfg<NT8, RIR, W4>;
   constexpr int NH = C::NH;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -471,7 +520,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         for (; pre < C::S && w.more(); ++pre, w.next(KB)) {
           mbar_arrive_expect_tx(&full[pre], (uint32_t)(w.g * C::BLK));
           for (int b = 0; b < w.g; ++b)
-            bulk_load(stages + pre * C::STAGE + b * C::BLK, unit_block(p, w.u, w.kb + b), HALF_BYTES, &full[pre],
+            bulk_load(stages + pre * C::STAGE + b * C::BLK, unit_block<W4>(p, w.u, w.kb + b), C::HB, &full[pre],
                       pol_w);
         }
       }
@@ -485,10 +534,10 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
           if (!mbar_wait(&empty[rg.s], rg.ph ^ 1u, abort_flag, p.err, SITE_SKINNY_EMPTY, p.limit_ns)) break;
           mbar_arrive_expect_tx(&full[rg.s], (uint32_t)(w.g * C::BLK));
           for (int b = 0; b < w.g; ++b)
-            bulk_load(st + b * C::BLK, unit_block(p, w.u, w.kb + b), HALF_BYTES, &full[rg.s], pol_w);
+            bulk_load(st + b * C::BLK, unit_block<W4>(p, w.u, w.kb + b), C::HB, &full[rg.s], pol_w);
         }
         for (int b = 0; b < w.g; ++b)
-          tma_load_2d(st + b * C::BLK + HALF_BYTES, &tmX, (w.kb + b) * BK, 0, &full[rg.s], pol_x);
+          tma_load_2d(st + b * C::BLK + C::HB, &tmX, (w.kb + b) * BK, 0, &full[rg.s], pol_x);
       }
       // Never leave with copies in flight.
       for (int s = 0; s < C::S && s < issued; ++s) {
@@ -549,8 +598,11 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   // phase because units start at a multiple of 8 rows.  The second K step's
   // chunk differs from the first in bit 0 only, i.e. its offset is the first
   // one's ^ 16.
-  const uint32_t a_off = (uint32_t)(lane * BK + (((2 * kq) ^ (lane & 7)) << 4));
-  const uint32_t b_off = (uint32_t)(HALF_BYTES + g * BK + (((2 * kq) ^ g) << 4) + 4 * c);
+  // W4: row r of a block is 64 bytes, 16-byte chunk kq (this warp's K
+  // quarter) at (kq ^ ((r >> 1) & 3)) * 16.
+  const uint32_t a_off = W4 ? (uint32_t)(lane * 64 + ((kq ^ ((lane >> 1) & 3)) << 4))
+                            : (uint32_t)(lane * BK + (((2 * kq) ^ (lane & 7)) << 4));
+  const uint32_t b_off = (uint32_t)(C::HB + g * BK + (((2 * kq) ^ g) << 4) + 4 * c);
   const uint32_t stages_u32 = smem_u32(stages);
 
   bool bad = false;
@@ -574,9 +626,9 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       // loads and MMAs can interleave; a segment's odd tail takes one block.
       if (w.g == G) {
 #pragma unroll
-        for (int b = 0; b < G; ++b) consume_block<NT8>(st0 + (uint32_t)(b * C::BLK), a_off, b_off, acc);
+        for (int b = 0; b < G; ++b) consume_block<NT8, W4>(st0 + (uint32_t)(b * C::BLK), a_off, b_off, acc);
       } else {
-        consume_block<NT8>(st0, a_off, b_off, acc);
+        consume_block<NT8, W4>(st0, a_off, b_off, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[r.s]);
@@ -686,25 +738,25 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
 // ------------------------------------------------------------------ host side
 
-template <int NT8, bool RIR>
+template <int NT8, bool RIR, bool W4>
 static cudaError_t configure(int dev) {
   static int configured[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(w8a8_skinny_kernel<NT8, RIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<NT8, RIR>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(w8a8_skinny_kernel<NT8, RIR, W4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NT8, RIR, W4>::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   return cudaSuccess;
 }
 
-template <int NT8, bool RIR>
+template <int NT8, bool RIR, bool W4>
 static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = Cfg<NT8, RIR>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<NT8, RIR, W4>::SMEM;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -719,16 +771,16 @@ static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cu
 
 // Clusters of `csize` CTAs of the cluster-schedule kernel that the device
 // keeps resident at once (0 if unknown); cached per device and cluster size.
-template <int NT8>
+template <int NT8, bool W4>
 static int resident_clusters(int dev, int csize) {
   static int cache[64][9];
   static bool init[64][9] = {};
   if (dev < 0 || dev >= 64 || csize < 2 || csize > 8) return 0;
   if (!init[dev][csize]) {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = config_of<NT8, true>(csize * 16, csize, nullptr, attr);
+    cudaLaunchConfig_t cfg = config_of<NT8, true, W4>(csize * 16, csize, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, w8a8_skinny_kernel<NT8, true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, w8a8_skinny_kernel<NT8, true, W4>, &cfg) != cudaSuccess) {
       n = 0;
       cudaGetLastError();
     }
@@ -738,19 +790,19 @@ static int resident_clusters(int dev, int csize) {
   return cache[dev][csize];
 }
 
-template <int NT8>
+template <int NT8, bool W4>
 static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaError_t e = configure<NT8, true>(dev);
-  if (e == cudaSuccess) e = configure<NT8, false>(dev);
+  cudaError_t e = configure<NT8, true, W4>(dev);
+  if (e == cudaSuccess) e = configure<NT8, false, W4>(dev);
   if (e != cudaSuccess) return e;
   const int n_units = (p.N + UM - 1) / UM;
   const int slots = std::min(2 * sms, MAX_CTAS);   // two CTAs per SM
   // Few units: one cluster per unit, with the most K slices that keep every
   // cluster resident in one wave; each slice must be one accumulation run.
   int csize = std::min(std::min(8, slots / n_units), p.KB);
-  while (csize >= 2 && resident_clusters<NT8>(dev, csize) < n_units) --csize;
+  while (csize >= 2 && resident_clusters<NT8, W4>(dev, csize) < n_units) --csize;
   if (csize >= 2 && (p.KB + csize - 1) / csize > RUN_BLOCKS) csize = 1;
   cudaLaunchAttribute attr[2];
   if (csize >= 2) {
@@ -759,8 +811,8 @@ static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t
     p.split_units = 0;
     p.total1 = 0;
     p.whole_per = 0;
-    cudaLaunchConfig_t cfg = config_of<NT8, true>(n_units * csize, csize, stream, attr);
-    return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, true>, tx, p);
+    cudaLaunchConfig_t cfg = config_of<NT8, true, W4>(n_units * csize, csize, stream, attr);
+    return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, true, W4>, tx, p);
   }
   p.mode = 0;
   p.csize = 1;
@@ -770,8 +822,8 @@ static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t
   p.total1 = p.split_units * p.KB;
   if (p.whole_per == 0) grid = std::min(grid, p.total1);
   if ((unsigned long long)(p.total1 + 1) * (unsigned long long)(grid + 1) >= (1ull << 32)) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = config_of<NT8, false>(grid, 1, stream, attr);
-  return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, false>, tx, p);
+  cudaLaunchConfig_t cfg = config_of<NT8, false, W4>(grid, 1, stream, attr);
+  return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, false, W4>, tx, p);
 }
 
 bool handles(int M) { return M >= 1 && M <= 24; }
@@ -789,7 +841,8 @@ size_t slots_bytes(int M, int N, int K) {
 // Arguments were validated by the caller; ws_cnt holds >= 8 zeroed counters
 // per 64-row unit, `slots` slots_bytes() bytes (no initial value needed).
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
-                    void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream) {
+                    void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream,
+                    bool w4) {
   const int nt8 = (M + 7) / 8;
   CUtensorMap tx;
   if (!encode_2d_u8(&tx, Xq, K, M, BK, 8 * nt8)) return QUASAR_ERR_CUDA;
@@ -812,10 +865,13 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   const int sms = sm_count();
   if (sms <= 0) return QUASAR_ERR_CUDA;
   cudaError_t e;
-  switch (nt8) {
-    case 1: e = launch<1>(tx, p, sms, stream); break;
-    case 2: e = launch<2>(tx, p, sms, stream); break;
-    default: e = launch<3>(tx, p, sms, stream); break;   // handles() keeps M <= 24
+  switch (nt8 + (w4 ? 3 : 0)) {
+    case 1: e = launch<1, false>(tx, p, sms, stream); break;
+    case 2: e = launch<2, false>(tx, p, sms, stream); break;
+    case 3: e = launch<3, false>(tx, p, sms, stream); break;   // handles() keeps M <= 24
+    case 4: e = launch<1, true>(tx, p, sms, stream); break;
+    case 5: e = launch<2, true>(tx, p, sms, stream); break;
+    default: e = launch<3, true>(tx, p, sms, stream); break;
   }
   if (e == cudaErrorInvalidValue) return QUASAR_ERR_UNSUPPORTED;
   return cuda_status(e);

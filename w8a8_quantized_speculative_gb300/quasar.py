@@ -38,6 +38,10 @@ _SIGS = {
     "quasar_packed_weight_bytes": (_sz, [_i, _i]),
     "quasar_pack_weights": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
     "quasar_tile_weights": (_i, [_p, _i, _i, _p, _p]),
+    "quasar_packed_weight_bytes_w4": (_sz, [_i, _i]),
+    "quasar_pack_weights_w4": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
+    "quasar_tile_weights_w4": (_i, [_p, _i, _i, _p, _p]),
+    "quasar_w4a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_smooth_quant_act": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
     "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
@@ -170,6 +174,51 @@ def tile_weights(wq: torch.Tensor, wp=None, stream=None):
     wp = torch.empty(packed_weight_bytes(N, K), dtype=torch.int8, device=wq.device) if wp is None else wp
     _check(lib.quasar_tile_weights(_ptr(wq), N, K, _ptr(wp), _stream(stream)), "tile_weights")
     return wp
+
+
+def packed_weight_bytes_w4(N: int, K: int) -> int:
+    return int(lib.quasar_packed_weight_bytes_w4(N, K))
+
+
+def pack_weights_w4(w: torch.Tensor, smooth: torch.Tensor, wp=None, sw=None, stream=None):
+    """(Wp4 packed 4-bit [packed_weight_bytes_w4], sw fp32 [N]) from BF16 W [N][K]."""
+    _need(w, torch.bfloat16, "w")
+    _need(smooth, torch.float32, "smooth")
+    ldw = _rowmajor(w, "w")
+    N, K = w.shape
+    wp = torch.empty(packed_weight_bytes_w4(N, K), dtype=torch.int8, device=w.device) if wp is None else wp
+    sw = torch.empty(N, dtype=torch.float32, device=w.device) if sw is None else sw
+    _check(lib.quasar_pack_weights_w4(_ptr(w), ldw, _ptr(smooth), N, K, _ptr(wp), _ptr(sw), _stream(stream)),
+           "pack_weights_w4")
+    return wp, sw
+
+
+def tile_weights_w4(wq: torch.Tensor, wp=None, stream=None):
+    """Packed 4-bit weights from row-major codes [N][K] in [-8, 7] (int8)."""
+    _need(wq, torch.int8, "wq")
+    if not wq.is_contiguous():
+        raise ValueError("wq must be contiguous")
+    N, K = wq.shape
+    wp = torch.empty(packed_weight_bytes_w4(N, K), dtype=torch.int8, device=wq.device) if wp is None else wp
+    _check(lib.quasar_tile_weights_w4(_ptr(wq), N, K, _ptr(wp), _stream(stream)), "tile_weights_w4")
+    return wp
+
+
+def w4a8_linear(xq, sa, wp4, sw, y=None, workspace: Workspace | None = None, stream=None):
+    """Y bf16 [M][N] from INT8 codes and 4-bit packed weights (M <= 24)."""
+    _need(xq, torch.int8, "xq")
+    _need(wp4, torch.int8, "wp4")
+    M, K = xq.shape
+    N = sw.numel()
+    if wp4.numel() < packed_weight_bytes_w4(N, K) or not wp4.is_contiguous():
+        raise ValueError("wp4 must be a contiguous packed 4-bit weight buffer of packed_weight_bytes_w4(N, K)")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if y is None else y
+    ldy = _rowmajor(y, "y")
+    ws = _ws(workspace, xq.device)
+    buf = ws.get(int(lib.quasar_w8a8_linear_workspace_size(M, N, K)))
+    _check(lib.quasar_w4a8_linear(_ptr(xq), _ptr(sa), _ptr(wp4), _ptr(sw), M, N, K, _ptr(y), ldy, _ptr(buf),
+                                  buf.numel(), _stream(stream)), "w4a8_linear")
+    return y
 
 
 def smooth_quant_act(x: torch.Tensor, smooth: torch.Tensor, xq=None, sa=None, stream=None):
