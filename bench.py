@@ -13,7 +13,8 @@ Also reported: the roofline object for the dominant kernel (the qkv linear),
 an end-to-end number through the public API with host buffers, SM clocks
 sampled during the timed region, the CPU oracle as a baseline, an M sweep
 over the four decoder-layer linears with a BF16 cuBLAS GEMM of the same shape
-as a bandwidth reference, and the verification kernel at B=32, D=8,
+as a bandwidth reference, the same linears with 4-bit weights (W4A8) at
+M = 1, 8, 20, and the verification kernel at B=32, D=8,
 V=151936.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
