@@ -586,3 +586,34 @@ def test_w4a8_rejects_large_m():
     wp = q.tile_weights_w4(torch.zeros((128, 256), dtype=torch.int8, device="cuda"))
     with pytest.raises(q.QuasarError):
         q.w4a8_linear(xq, torch.ones(32, device="cuda"), wp, torch.ones(128, device="cuda"))
+
+
+# ---------------------------------------------------------------- documented limits
+
+@pytest.mark.parametrize("M", [1, 40])
+def test_int8_gemm_at_max_k(M):
+    """K = 131072, the documented limit: all-extreme operands put |acc| at
+    127 * 127 * 131072 = 2.11e9 < 2^31 (exact int32), through both kernels."""
+    N, K = 16, 131072
+    xq = np.full((M, K), 127, np.int8)
+    xq[:, 1::3] = -127
+    wq = np.full((N, K), 127, np.int8)
+    wq[1::2, ::5] = -127
+    ws = q.Workspace()
+    acc = q.int8_gemm_s32(dev(xq), q.tile_weights(dev(wq)), N, workspace=ws).cpu().numpy()
+    assert np.array_equal(acc.astype(np.int64), orc.int_gemm(xq, wq))
+    check_ws_zero(ws)
+
+
+def test_verify_at_max_rows():
+    """B * (D + 1) = 65535 logits rows, the documented limit, small V."""
+    D, V = 4, 64
+    B = 65535 // (D + 1)
+    lg, draft, mask, _ = synth.verify_inputs(B, D, V, 801, 802, 803, 804)
+    am = np.argmax(orc.bf16_to_f32(lg), axis=2)
+    d = np.where(mask, am[:, :D], draft).astype(np.int32)
+    n_acc, nxt = q.verify_accept(dev_bf16(lg), dev(d))
+    ok = d == am[:, :D]
+    want = np.where(ok.all(axis=1), D, np.argmin(ok, axis=1))
+    assert np.array_equal(n_acc.cpu().numpy(), want)
+    assert np.array_equal(nxt.cpu().numpy(), am[np.arange(B), want])
