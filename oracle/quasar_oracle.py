@@ -50,6 +50,10 @@ The pages leave the numeric details open.  The readings taken here are:
       variant only): per output channel, scale = absmax/7, code =
       clamp(rne(w' * (7/absmax)), -7, 7), in fp32 as R2; activations as R2;
       the same exact integer GEMM and dequantization (R3, R4).
+  R9  BF16 lm_head (the verifier's last matmul, which the pages keep in BF16
+      ahead of the high-precision acceptance test): logits = the exact
+      product H·W^T of the BF16 inputs, rounded once to BF16 (nearest, ties
+      to even); acceptance as R5/R6 on those logits.
 
 Every function below is pinned by tests under ``tests/`` against hand-derived
 values, closed forms, invariants or brute force (see each docstring).
@@ -80,6 +84,33 @@ def f32_to_bf16(x: np.ndarray) -> np.ndarray:
     rem = u & 0xFFFF
     up = (rem > 0x8000) | ((rem == 0x8000) & ((keep & 1) == 1))
     return (keep + up.astype(np.uint64)).astype(np.uint16)
+
+
+def f64_to_bf16(x: np.ndarray) -> np.ndarray:
+    """fp64 -> BF16 bits, rounded once (nearest, ties to even; finite inputs
+    in the normal range).  Going through fp32 first would round twice.
+
+    Pinned by exact midpoints, a value just above a midpoint that fp32 would
+    collapse onto it, and agreement with f32_to_bf16 on fp32 inputs."""
+    x = np.asarray(x, dtype=F64)
+    m, e = np.frexp(x)                       # x = m * 2^e, 0.5 <= |m| < 1
+    r = np.rint(np.ldexp(m, 8))              # 8 significant bits, half to even
+    y = np.ldexp(r, e - 8).astype(F32)       # exact: 8 bits fit in fp32
+    return (y.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def bf16_midpoint_distance(x: np.ndarray) -> np.ndarray:
+    """|x - nearest rounding midpoint| for BF16 rounding of fp64 x: how far x
+    may move before its BF16 value can change.  0 at a midpoint; half the
+    spacing at a BF16 number inside a binade; at a power of two 2^p the
+    nearest midpoint is the one below, 2^p - 2^(p-9).  Pinned by those cases."""
+    x = np.abs(np.asarray(x, dtype=F64))
+    _, e = np.frexp(x)                       # x in [2^(e-1), 2^e)
+    ulp = np.ldexp(1.0, e - 8)               # BF16 spacing on that binade
+    frac = x / ulp - np.floor(x / ulp)
+    inside = np.abs(frac - 0.5) * ulp
+    below = x - np.ldexp(1.0, e - 1) * (1.0 - 2.0 ** -9)   # midpoint under the binade's first number
+    return np.minimum(inside, below)
 
 
 # ---------------------------------------------------------------------------
@@ -259,6 +290,33 @@ def verify_accept(logits_bits: np.ndarray, draft: np.ndarray, temperature: float
         if temperature == 0:
             nxt[b] = int(np.argmax(lg[b, n_acc[b]]))
     return n_acc, nxt
+
+
+def lm_head_logits(h_bits: np.ndarray, w_bits: np.ndarray, chunk: int = 8192) -> np.ndarray:
+    """logits[r][v] = bf16_rne(sum_k H[r][k] * W[v][k]) (reading R9) -> BF16 bits.
+
+    The products of BF16 numbers are exact in fp64 and the fp64 sum of K of
+    them is the exact sum up to fp64 rounding, far below a BF16 spacing; the
+    vocabulary is processed in slices of `chunk` rows only to bound memory.
+    Pinned by exact rational brute force on tiny inputs and by a closed form
+    (weights that select and scale one hidden entry per vocabulary row)."""
+    h = bf16_to_f32(h_bits).astype(F64)
+    V = w_bits.shape[0]
+    out = np.empty((h.shape[0], V), dtype=np.uint16)
+    for v0 in range(0, V, chunk):
+        w = bf16_to_f32(w_bits[v0:v0 + chunk]).astype(F64)
+        out[:, v0:v0 + chunk] = f64_to_bf16(h @ w.T)
+    return out
+
+
+def lm_head_verify(h_bits: np.ndarray, w_bits: np.ndarray, draft: np.ndarray, temperature: float = 0.0,
+                   u: np.ndarray | None = None):
+    """The lm_head followed by verification: verify_accept on lm_head_logits
+    (R9, then R5/R6).  h [B*(D+1)][K] holds row b*(D+1)+j for draft j of
+    sequence b (j = D: the bonus position)."""
+    B, D = draft.shape
+    lg = lm_head_logits(h_bits, w_bits).reshape(B, D + 1, w_bits.shape[0])
+    return verify_accept(lg, draft, temperature, u)
 
 
 def verify_sample(logits_bits: np.ndarray, draft: np.ndarray, temperature: float, u: np.ndarray,

@@ -35,3 +35,17 @@ def round_to_f32(q: Fraction) -> Fraction:
     if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
         fl += 1
     return fl * u
+
+
+def round_to_bf16(q: Fraction) -> Fraction:
+    """Nearest BF16 value to the rational q, ties to even (normal range):
+    8 significant bits, spacing 2^(e-7) on [2^e, 2^(e+1))."""
+    if q == 0:
+        return Fraction(0)
+    u = ulp_f32(q) * 2 ** 16
+    n = q / u
+    fl = math.floor(n)
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return fl * u

@@ -461,3 +461,78 @@ def test_pack_weights_w4_is_smoothed_quantizer():
     wq_ref, sw_ref = orc.quantize_rows(orc.bf16_to_f32(w) / s[None, :], qmax=7)
     assert np.array_equal(wq, wq_ref) and np.array_equal(sw, sw_ref)
     assert np.all(np.abs(wq).max(axis=1) == 7)
+
+
+# ------------------------------------------------ BF16 lm_head (reading R9)
+
+def _bf16_value(bits):
+    return Fraction(float(np.array([int(bits) << 16], np.uint32).view(np.float32)[0]))
+
+
+def test_f64_to_bf16_midpoints_and_double_rounding():
+    from tests.exact import round_to_bf16
+    cases = [1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -8 + 2 ** -30, -(1 + 2 ** -8 + 2 ** -30), 3.0, 1e-3,
+             -7.123456789, 2.0 ** -100, 65504.25]
+    got = orc.f64_to_bf16(np.array(cases))
+    for x, g in zip(cases, got):
+        assert _bf16_value(g) == round_to_bf16(Fraction(x)), x
+    # exact midpoints go to the even neighbour; just above the first one rounds up, which a
+    # detour through fp32 (1 + 2^-8 + 2^-30 -> 1 + 2^-8 -> 1.0) would lose
+    assert [int(v) for v in got[:3]] == [0x3F80, 0x3F82, 0x3F81]
+
+
+def test_f64_to_bf16_agrees_with_f32_path_on_f32_inputs():
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    assert np.array_equal(orc.f64_to_bf16(x.astype(np.float64)), orc.f32_to_bf16(x))
+
+
+def test_bf16_midpoint_distance_cases():
+    u9 = 2.0 ** -9
+    x = np.array([1 + 2 ** -8, 1.0, 2.0, 1 + 2 ** -7, 1.5, 1 - 2 ** -9, 1 + 2 ** -9, -(1 + 2 ** -7)])
+    want = np.array([0, 1, 2, 2, 2, 0, 1, 2]) * u9
+    assert np.array_equal(orc.bf16_midpoint_distance(x), want)
+
+
+def test_lm_head_logits_exact_brute_force():
+    from tests.exact import round_to_bf16
+    rng = np.random.default_rng(11)
+    R, K, V = 3, 16, 7
+    h = orc.f32_to_bf16(rng.standard_normal((R, K)).astype(np.float32))
+    w = orc.f32_to_bf16((rng.standard_normal((V, K)) * 0.05).astype(np.float32))
+    got = orc.lm_head_logits(h, w, chunk=3)   # several vocabulary slices and a ragged last one
+    for r in range(R):
+        for v in range(V):
+            exact = sum(_bf16_value(h[r, k]) * _bf16_value(w[v, k]) for k in range(K))
+            assert _bf16_value(got[r, v]) == round_to_bf16(exact), (r, v)
+
+
+def test_lm_head_logits_selector_closed_form():
+    # W[v] = 2^s_v * e_{k_v}: logits[r][v] = 2^s_v * H[r][k_v] exactly
+    rng = np.random.default_rng(12)
+    R, K, V = 5, 32, 40
+    h = orc.f32_to_bf16(rng.standard_normal((R, K)).astype(np.float32))
+    kv = rng.integers(0, K, V)
+    sv = rng.integers(-3, 4, V)
+    w = np.zeros((V, K), np.float32)
+    w[np.arange(V), kv] = 2.0 ** sv
+    got = orc.bf16_to_f32(orc.lm_head_logits(h, orc.f32_to_bf16(w)))
+    want = orc.bf16_to_f32(h)[:, kv] * (2.0 ** sv)[None, :]
+    assert np.array_equal(got, want.astype(np.float32))
+
+
+def test_lm_head_verify_hand_built():
+    # Hidden rows pick the vocabulary row holding their maximum; W = identity
+    # on the first V coordinates, so each row's argmax is where its maximum sits.
+    B, D, V, K = 2, 3, 8, 8
+    top = np.array([[5, 1, 6, 2], [0, 3, 3, 7]])      # argmax of rows j = 0..3 of each sequence
+    h = np.zeros((B * (D + 1), K), np.float32)
+    for b in range(B):
+        for j in range(D + 1):
+            h[b * (D + 1) + j] = -1.0
+            h[b * (D + 1) + j, top[b, j]] = 2.0
+    w = np.eye(V, K, dtype=np.float32)
+    draft = np.array([[5, 1, 4], [0, 3, 3]], np.int32)  # seq 0 fails at j = 2; seq 1 accepts all
+    n_acc, nxt = orc.lm_head_verify(orc.f32_to_bf16(h), orc.f32_to_bf16(w), draft)
+    assert n_acc.tolist() == [2, 3]
+    assert nxt.tolist() == [6, 7]
