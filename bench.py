@@ -460,6 +460,7 @@ def main_gpu(args):
         extra["sweep"] = run_sweep(q, dev, stream, ws, hbm)
         extra["sweep_w4a8"] = run_sweep_w4(q, dev, stream, ws, hbm)
         extra["verify"] = run_verify(q, dev, stream, ws, hbm)
+        extra["lm_head"] = run_lm_head(q, dev, stream, bf16)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -598,6 +599,55 @@ def run_verify(q, dev, stream, ws, hbm):
                 (nxt.long() == ref[torch.arange(B, device=dev), n_acc.long()]).all().item())}
 
 
+def run_lm_head(q, dev, stream, bf16_peak):
+    """The verification step's BF16 lm_head (Qwen3-8B, 4096 -> 151936) at
+    B = 32 sequences x (8 drafts + 1): the fused lm_head + verification
+    (greedy and T = 1; no logits written), the same tcgen05 kernel writing
+    its logits, and the unfused pair cuBLAS logits + the verification
+    kernel.  The 1.24 GB weight is ten times the L2, so every launch streams
+    it from HBM."""
+    import torch
+    B, D, V, K = 32, 8, synth.VOCAB, synth.HIDDEN
+    rows = B * (D + 1)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2)
+    h = torch.randn((rows, K), device=dev, generator=gen).to(torch.bfloat16)
+    w = (torch.randn((V, K), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+    draft = torch.randint(0, V, (B, D), dtype=torch.int32, device=dev, generator=gen)
+    u = torch.rand((B, D), device=dev, generator=gen)
+    lg = torch.empty((rows, V), dtype=torch.bfloat16, device=dev)
+    n_acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    ws_f, ws_v = q.Workspace(dev), q.Workspace(dev)
+    ws_f.get(q.lib.quasar_lm_head_verify_workspace_size(B, D, V))
+    ws_v.get(q.lib.quasar_verify_accept_workspace_size(B, D, V))
+    n = 10
+    t = {
+        "fused_greedy_us": _time_graph(torch, stream, lambda i: q.lm_head_verify(
+            h, w, draft, 0.0, n_acc=n_acc, next_token=nxt, workspace=ws_f), n),
+        "fused_T1_us": _time_graph(torch, stream, lambda i: q.lm_head_verify(
+            h, w, draft, 1.0, u, n_acc=n_acc, workspace=ws_f), n),
+        "logits_tcgen05_us": _time_graph(torch, stream, lambda i: q.lm_head_logits(h, w, logits=lg), n),
+        "logits_cublas_us": _time_graph(torch, stream, lambda i: torch.matmul(h, w.t(), out=lg), n),
+    }
+    t["cublas_plus_verify_us"] = _time_graph(torch, stream, lambda i: (
+        torch.matmul(h, w.t(), out=lg),
+        q.verify_accept(lg.view(B, D + 1, V), draft, n_acc=n_acc, next_token=nxt, workspace=ws_v)), n)
+    flops = 2.0 * rows * K * V
+    wbytes = V * K * 2
+    peak = bf16_peak
+    out = {"B": B, "D": D, "V": V, "K": K, "rows": rows, "flop_per_launch": flops, "weight_bytes": wbytes}
+    for k, us in t.items():
+        out[k] = round(us, 2)
+    fg = t["fused_greedy_us"]
+    out["fused_greedy_TFLOPs"] = round(flops / (fg * 1e-6) / 1e12, 1)
+    out["fused_greedy_tensor_frac"] = round(flops / (fg * 1e-6) / 1e12 / peak, 3) if peak else None
+    out["fused_greedy_weight_TBps"] = round(wbytes / (fg * 1e-6) / 1e12, 3)
+    out["speedup_vs_cublas_plus_verify"] = round(t["cublas_plus_verify_us"] / fg, 3)
+    out["peak_source"] = "bf16 burst of MEASURED_PEAKS.json (fallback 1.9 PFLOP/s if absent)"
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -606,11 +656,19 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the M sweep and verify sub-benchmarks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lm-head-only", action="store_true",
+                    help="run only the fused lm_head + verification sub-benchmark (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.lm_head_only:
+        import torch
+        from w8a8_quantized_speculative_gb300 import quasar as q
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"lm_head": run_lm_head(q, dev, torch.cuda.Stream(dev), load_peaks()[1])}), flush=True)
     else:
         main_gpu(args)
 

@@ -342,6 +342,54 @@ quasar_status_t quasar_verify_sample(const void* logits_bf16, int ldl,
                                      void* workspace, size_t ws_bytes,
                                      quasar_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Fused BF16 lm_head + verification (the logits are never written).
+ *
+ * nl §2 / ko §2: the verifier's last matmul stays in BF16 and the drafts are
+ * checked on its high-precision logits; zh §2: greedy or rejection
+ * acceptance.  For token row c = b*(D+1) + j (j = D: the bonus position):
+ *   l[c][v] = bf16_rne(fp32 sum_k H[c][k] * W[v][k])   (tensor cores, fp32
+ *             accumulation in an unspecified order)
+ * and then exactly the acceptance rule of quasar_verify_accept on l, with
+ * the row reductions (max, lowest-index argmax, sum of exp((l - max)/T),
+ * the draft's logit) taken inside the matmul's epilogue.
+ *   H      [B*(D+1)][ldh] BF16 hidden states (final-norm output), row c as
+ *          above; ldh >= K, ldh % 8 == 0; 16-byte aligned
+ *   W      [V][ldw] BF16 lm_head weight (row v = vocabulary entry v);
+ *          ldw >= K, ldw % 8 == 0; 16-byte aligned
+ *   K      hidden size, K % 8 == 0
+ *   draft  [B][D] int32 in [0, V); u [B][D] fp32 in [0,1), required iff
+ *          T > 0 and D > 0; n_acc [B] int32 output; next_token [B] int32
+ *          (argmax of row n_acc) or NULL, and NULL when T > 0
+ *   Sizes: B >= 0 (0 = no-op), D >= 0, V >= 1, B*(D+1) <= 512
+ *          (QUASAR_ERR_UNSUPPORTED above).
+ *   workspace: >= quasar_lm_head_verify_workspace_size(B, D, V) bytes,
+ *   256-byte aligned, ZERO-FILLED before first use and left zero-filled by
+ *   the call (same contract as quasar_w8a8_linear).
+ * Two launches (the matmul with its epilogue, then one CTA per row merging
+ * the per-tile records); asynchronous on `stream`.
+ * ------------------------------------------------------------------------ */
+size_t quasar_lm_head_verify_workspace_size(int B, int D, int V);
+quasar_status_t quasar_lm_head_verify(const void* H_bf16, int ldh,
+                                      const void* W_bf16, int ldw, int K,
+                                      const int32_t* draft, int B, int D, int V,
+                                      float temperature, const float* u,
+                                      int32_t* n_acc, int32_t* next_token,
+                                      void* workspace, size_t ws_bytes,
+                                      quasar_stream_t stream);
+
+/* The same BF16 lm_head kernel writing its logits instead:
+ *   logits[m][v] = bf16_rne(fp32 sum_k H[m][k] * W[v][k]),
+ *   logits [M][ldl] BF16 (ldl >= V), 2-byte aligned; 0 <= M <= 512;
+ *   H, W, K as above.  No workspace.  For checking the matmul on its own and
+ *   for callers that need the logits tensor.
+ * ------------------------------------------------------------------------ */
+quasar_status_t quasar_lm_head_logits(const void* H_bf16, int ldh,
+                                      const void* W_bf16, int ldw,
+                                      int M, int V, int K,
+                                      void* logits_bf16, long long ldl,
+                                      quasar_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -179,3 +179,45 @@ def test_selftest_wait_rejects_limits_out_of_range(lib):
     assert f(0, None) == 1
     assert f(999, None) == 1
     assert f(10_000_000_001, None) == 1
+
+
+def test_lm_head_rejects_bad_arguments(lib):
+    lib.quasar_lm_head_verify_workspace_size.restype = ctypes.c_size_t
+    # counters [B], row results [B*(D+1)] x 16 B, draft logits [B*(D+1)], records [B*(D+1)][ceil(V/128)] x 8 B
+    assert lib.quasar_lm_head_verify_workspace_size(32, 8, 151936) == 256 + 4608 + 1280 + 288 * 1187 * 8
+    f = lib.quasar_lm_head_verify
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    names = ["h", "ldh", "w", "ldw", "K", "draft", "B", "D", "V", "T", "u", "n_acc", "nxt", "ws", "wsb", "stream"]
+    ok_args = [FAKE, 64, FAKE, 64, 64, FAKE, 2, 3, 1000, 0.0, None, FAKE, FAKE, FAKE, 1 << 20, None]
+
+    def call(**kw):
+        a = list(ok_args)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+
+    assert call(B=-1) == 1
+    assert call(T=-1.0) == 1
+    assert call(T=float("inf")) == 1
+    assert call(T=1.0) == 1                  # T > 0 needs u and no next token
+    assert call(T=1.0, u=FAKE) == 1
+    assert call(n_acc=None) == 1
+    assert call(draft=None) == 1
+    assert call(B=52, D=9) == 2              # 520 token rows > 512
+    assert call(ws=None) == 3
+    assert call(wsb=100) == 3
+    assert call(K=60, ldh=64, ldw=64) == 2   # K % 8
+    assert call(ldh=32) == 2                 # ldh < K
+    assert call(h=None) == 1
+    assert call(B=0) == 0
+    g = lib.quasar_lm_head_logits
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p]
+    assert g(FAKE, 64, FAKE, 64, 2, 1000, 64, FAKE, 999, None) == 2     # ldl < V
+    assert g(FAKE, 64, FAKE, 64, 513, 1000, 64, FAKE, 1000, None) == 2  # M > 512
+    assert g(FAKE, 64, FAKE, 64, 2, 1000, 64, None, 1000, None) == 1
+    assert g(FAKE, 64, FAKE, 64, 0, 1000, 64, None, 1000, None) == 0

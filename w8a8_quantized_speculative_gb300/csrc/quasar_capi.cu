@@ -93,6 +93,20 @@ bool encode_2d_u8(CUtensorMap* map, const void* base, int inner, int outer, int 
   return r == CUDA_SUCCESS;
 }
 
+bool encode_2d_bf16(CUtensorMap* map, const void* base, int inner, int outer, long long ld, int box_inner,
+                    int box_outer) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 quasar_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? QUASAR_OK : QUASAR_ERR_CUDA; }
 
 }  // namespace quasar

@@ -32,6 +32,13 @@ quasar_status_t cuda_status(cudaError_t e); // maps a CUDA error to a status
 // box_inner bytes; out-of-range elements read as zero.
 bool encode_2d_u8(CUtensorMap* map, const void* base, int inner, int outer, int box_inner, int box_outer);
 
+// 2-D tensor map over a row-major BF16 matrix [outer][inner] whose rows are
+// `ld` elements apart (ld * 2 a multiple of 16 bytes), 128B-swizzled boxes of
+// box_outer rows x box_inner elements (box_inner * 2 <= 128); out-of-range
+// elements read as zero.
+bool encode_2d_bf16(CUtensorMap* map, const void* base, int inner, int outer, long long ld, int box_inner,
+                    int box_outer);
+
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Error site codes recorded in the device error word (low 16 bits = site,
@@ -48,6 +55,11 @@ enum : unsigned int {
   SITE_SKINNY_EMPTY = 9,
   SITE_SKINNY_DRAIN = 10,
   SITE_SELFTEST = 12,
+  SITE_LMH_FULL = 13,
+  SITE_LMH_EMPTY = 14,
+  SITE_LMH_ACCFULL = 15,
+  SITE_LMH_ACCFREE = 16,
+  SITE_LMH_DRAIN = 17,
 };
 
 // ---------------------------------------------------------------- device side
@@ -251,6 +263,19 @@ QUASAR_DEVICE_INLINE void tmem_ld8(uint32_t taddr, uint32_t* r) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                : "r"(taddr)
                : "memory");
+}
+
+// Load 32 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+QUASAR_DEVICE_INLINE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
 }
 
 // ---- bit helpers ---------------------------------------------------------------

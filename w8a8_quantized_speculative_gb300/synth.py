@@ -168,3 +168,68 @@ def verify_inputs(B: int, D: int, V: int, seed_logits: int = 501, seed_draft: in
     lg = logits(seed_logits, B * (D + 1), V, std).reshape(B, D + 1, V)
     return (lg, draft_tokens(seed_draft, B, D, V), bernoulli_mask(seed_mask, (B, D)),
             uniforms(seed_u, (B, D)))
+
+
+# ---------------------------------------------------------------------------
+# The verifier's BF16 lm_head (hidden states -> logits over the vocabulary).
+
+def hidden_states(seed: int, rows: int, K: int) -> np.ndarray:
+    """BF16 final hidden states H[rows][K] ~ N(0,1) (an RMS-normalised
+    activation with unit gain)."""
+    return f32_to_bf16_bits(_rng(seed).standard_normal((rows, K)).astype(np.float32))
+
+
+def _bf16_inplace(a: np.ndarray) -> np.ndarray:
+    """fp32 -> BF16 bits (nearest, ties to even) for finite values, in 32-bit
+    arithmetic on the array's own storage (large weight slices)."""
+    b = a.view(np.uint32)
+    b += np.uint32(0x7FFF) + ((b >> 16) & np.uint32(1))
+    return (b >> 16).astype(np.uint16)
+
+
+def _sliced(seed: int, V: int, K: int, chunk: int, draw) -> np.ndarray:
+    """A [V][K] BF16 matrix drawn slice by slice of ``chunk`` rows, slice i
+    from its own generator PCG64(SeedSequence(seed).spawn(n)[i]); slices are
+    drawn on a thread pool (the bytes do not depend on the thread count)."""
+    from concurrent.futures import ThreadPoolExecutor
+    n_sl = (V + chunk - 1) // chunk
+    seqs = np.random.SeedSequence(seed).spawn(n_sl)
+    out = np.empty((V, K), dtype=np.uint16)
+
+    def job(i):
+        v0 = i * chunk
+        n = min(chunk, V - v0)
+        out[v0:v0 + n] = _bf16_inplace(draw(np.random.Generator(np.random.PCG64(seqs[i])), n))
+
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        list(ex.map(job, range(n_sl)))
+    return out
+
+
+def lm_head_weight(seed: int, V: int, K: int, std: float = 0.02, chunk: int = 8192) -> np.ndarray:
+    """BF16 lm_head weight W[V][K] ~ N(0, std^2), drawn directly in fp32
+    (``standard_normal(dtype=float32)``) slice by slice: the Qwen3-8B
+    vocabulary makes it 622 M values."""
+    def draw(g, n):
+        x = g.standard_normal((n, K), dtype=np.float32)
+        x *= np.float32(std)
+        return x
+    return _sliced(seed, V, K, chunk, draw)
+
+
+def grid_hidden_states(seed: int, rows: int, K: int, amp: int = 4) -> np.ndarray:
+    """BF16 hidden states on an integer grid: uniform integers in [-amp, amp]."""
+    return f32_to_bf16_bits(_rng(seed).integers(-amp, amp + 1, size=(rows, K)).astype(np.float32))
+
+
+def grid_lm_head_weight(seed: int, V: int, K: int, amp: int = 32, shift: int = 6,
+                        chunk: int = 8192) -> np.ndarray:
+    """BF16 lm_head weight on a dyadic grid: uniform integers in [-amp, amp]
+    times 2^-shift.  With grid_hidden_states every product is a multiple of
+    2^-shift and, for K up to 4096, every partial sum of a row stays below
+    2^19 of those units, so any fp32 summation order gives the exact sum."""
+    def draw(g, n):
+        x = g.integers(-amp, amp + 1, size=(n, K), dtype=np.int16).astype(np.float32)
+        x *= np.float32(2.0 ** -shift)
+        return x
+    return _sliced(seed, V, K, chunk, draw)
