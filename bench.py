@@ -613,6 +613,7 @@ def run_lm_head(q, dev, stream, bf16_peak):
     gen.manual_seed(2)
     h = torch.randn((rows, K), device=dev, generator=gen).to(torch.bfloat16)
     w = (torch.randn((V, K), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+    wp = q.pack_lm_head(w)
     draft = torch.randint(0, V, (B, D), dtype=torch.int32, device=dev, generator=gen)
     u = torch.rand((B, D), device=dev, generator=gen)
     lg = torch.empty((rows, V), dtype=torch.bfloat16, device=dev)
@@ -624,10 +625,10 @@ def run_lm_head(q, dev, stream, bf16_peak):
     n = 10
     t = {
         "fused_greedy_us": _time_graph(torch, stream, lambda i: q.lm_head_verify(
-            h, w, draft, 0.0, n_acc=n_acc, next_token=nxt, workspace=ws_f), n),
+            h, wp, draft, 0.0, n_acc=n_acc, next_token=nxt, workspace=ws_f), n),
         "fused_T1_us": _time_graph(torch, stream, lambda i: q.lm_head_verify(
-            h, w, draft, 1.0, u, n_acc=n_acc, workspace=ws_f), n),
-        "logits_tcgen05_us": _time_graph(torch, stream, lambda i: q.lm_head_logits(h, w, logits=lg), n),
+            h, wp, draft, 1.0, u, n_acc=n_acc, workspace=ws_f), n),
+        "logits_tcgen05_us": _time_graph(torch, stream, lambda i: q.lm_head_logits(h, wp, logits=lg), n),
         "logits_cublas_us": _time_graph(torch, stream, lambda i: torch.matmul(h, w.t(), out=lg), n),
     }
     t["cublas_plus_verify_us"] = _time_graph(torch, stream, lambda i: (

@@ -343,6 +343,23 @@ quasar_status_t quasar_verify_sample(const void* logits_bf16, int ldl,
                                      quasar_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * BF16 lm_head weight packing (offline).
+ *
+ * The lm_head kernels stream the weight as contiguous 16 KB blocks, each
+ * already in the layout the tensor cores read: 128 vocabulary rows x 64 K
+ * values of BF16.  Block (t, kb) (t = vocabulary tile, kb = K block; KB =
+ * ceil(K/64)) starts at byte (t*KB + kb) * 16384; inside it, row r (entry
+ * v = 128t + r) occupies bytes r*128 .. r*128+127, and its 16-byte chunk c
+ * (K values 64kb + 8c .. +7) sits at chunk position c ^ (r % 8).  Rows past
+ * V and K values past K are zero.
+ *   W   [V][ldw] BF16 row-major, ldw >= K, ldw % 8 == 0, 16-byte aligned
+ *   K % 8 == 0; Wp: quasar_lm_head_packed_bytes(V, K) bytes, 16-byte aligned
+ * ------------------------------------------------------------------------ */
+size_t quasar_lm_head_packed_bytes(int V, int K);
+quasar_status_t quasar_pack_lm_head(const void* W_bf16, int ldw, int V, int K,
+                                    void* Wp, quasar_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Fused BF16 lm_head + verification (the logits are never written).
  *
  * nl §2 / ko §2: the verifier's last matmul stays in BF16 and the drafts are
@@ -355,8 +372,7 @@ quasar_status_t quasar_verify_sample(const void* logits_bf16, int ldl,
  * the draft's logit) taken inside the matmul's epilogue.
  *   H      [B*(D+1)][ldh] BF16 hidden states (final-norm output), row c as
  *          above; ldh >= K, ldh % 8 == 0; 16-byte aligned
- *   W      [V][ldw] BF16 lm_head weight (row v = vocabulary entry v);
- *          ldw >= K, ldw % 8 == 0; 16-byte aligned
+ *   Wp     the lm_head weight W [V][K] packed by quasar_pack_lm_head
  *   K      hidden size, K % 8 == 0
  *   draft  [B][D] int32 in [0, V); u [B][D] fp32 in [0,1), required iff
  *          T > 0 and D > 0; n_acc [B] int32 output; next_token [B] int32
@@ -371,7 +387,7 @@ quasar_status_t quasar_verify_sample(const void* logits_bf16, int ldl,
  * ------------------------------------------------------------------------ */
 size_t quasar_lm_head_verify_workspace_size(int B, int D, int V);
 quasar_status_t quasar_lm_head_verify(const void* H_bf16, int ldh,
-                                      const void* W_bf16, int ldw, int K,
+                                      const void* Wp, int K,
                                       const int32_t* draft, int B, int D, int V,
                                       float temperature, const float* u,
                                       int32_t* n_acc, int32_t* next_token,
@@ -381,12 +397,11 @@ quasar_status_t quasar_lm_head_verify(const void* H_bf16, int ldh,
 /* The same BF16 lm_head kernel writing its logits instead:
  *   logits[m][v] = bf16_rne(fp32 sum_k H[m][k] * W[v][k]),
  *   logits [M][ldl] BF16 (ldl >= V), 2-byte aligned; 0 <= M <= 512;
- *   H, W, K as above.  No workspace.  For checking the matmul on its own and
- *   for callers that need the logits tensor.
+ *   H, Wp, K as above.  No workspace.  For checking the matmul on its own
+ *   and for callers that need the logits tensor.
  * ------------------------------------------------------------------------ */
 quasar_status_t quasar_lm_head_logits(const void* H_bf16, int ldh,
-                                      const void* W_bf16, int ldw,
-                                      int M, int V, int K,
+                                      const void* Wp, int M, int V, int K,
                                       void* logits_bf16, long long ldl,
                                       quasar_stream_t stream);
 

@@ -187,11 +187,11 @@ def test_lm_head_rejects_bad_arguments(lib):
     assert lib.quasar_lm_head_verify_workspace_size(32, 8, 151936) == 256 + 4608 + 1280 + 288 * 1187 * 8
     f = lib.quasar_lm_head_verify
     f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
-    names = ["h", "ldh", "w", "ldw", "K", "draft", "B", "D", "V", "T", "u", "n_acc", "nxt", "ws", "wsb", "stream"]
-    ok_args = [FAKE, 64, FAKE, 64, 64, FAKE, 2, 3, 1000, 0.0, None, FAKE, FAKE, FAKE, 1 << 20, None]
+    names = ["h", "ldh", "wp", "K", "draft", "B", "D", "V", "T", "u", "n_acc", "nxt", "ws", "wsb", "stream"]
+    ok_args = [FAKE, 64, FAKE, 64, FAKE, 2, 3, 1000, 0.0, None, FAKE, FAKE, FAKE, 1 << 20, None]
 
     def call(**kw):
         a = list(ok_args)
@@ -209,15 +209,28 @@ def test_lm_head_rejects_bad_arguments(lib):
     assert call(B=52, D=9) == 2              # 520 token rows > 512
     assert call(ws=None) == 3
     assert call(wsb=100) == 3
-    assert call(K=60, ldh=64, ldw=64) == 2   # K % 8
+    assert call(K=60, ldh=64) == 2           # K % 8
     assert call(ldh=32) == 2                 # ldh < K
     assert call(h=None) == 1
+    assert call(wp=None) == 1
+    assert call(wp=FAKE_ODD) == 2            # 16-byte alignment
     assert call(B=0) == 0
     g = lib.quasar_lm_head_logits
     g.restype = ctypes.c_int
-    g.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+    g.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                   ctypes.c_int, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p]
-    assert g(FAKE, 64, FAKE, 64, 2, 1000, 64, FAKE, 999, None) == 2     # ldl < V
-    assert g(FAKE, 64, FAKE, 64, 513, 1000, 64, FAKE, 1000, None) == 2  # M > 512
-    assert g(FAKE, 64, FAKE, 64, 2, 1000, 64, None, 1000, None) == 1
-    assert g(FAKE, 64, FAKE, 64, 0, 1000, 64, None, 1000, None) == 0
+    assert g(FAKE, 64, FAKE, 2, 1000, 64, FAKE, 999, None) == 2     # ldl < V
+    assert g(FAKE, 64, FAKE, 513, 1000, 64, FAKE, 1000, None) == 2  # M > 512
+    assert g(FAKE, 64, FAKE, 2, 1000, 64, None, 1000, None) == 1
+    assert g(FAKE, 64, FAKE, 0, 1000, 64, None, 1000, None) == 0
+    lib.quasar_lm_head_packed_bytes.restype = ctypes.c_size_t
+    assert lib.quasar_lm_head_packed_bytes(151936, 4096) == 1187 * 64 * 16384
+    assert lib.quasar_lm_head_packed_bytes(1000, 200) == 8 * 4 * 16384
+    pk = lib.quasar_pack_lm_head
+    pk.restype = ctypes.c_int
+    pk.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    assert pk(FAKE, 64, 0, 64, FAKE, None) == 1
+    assert pk(FAKE, 64, 100, 60, FAKE, None) == 2       # K % 8
+    assert pk(FAKE, 32, 100, 64, FAKE, None) == 2       # ldw < K
+    assert pk(FAKE_ODD, 64, 100, 64, FAKE, None) == 2
+    assert pk(None, 64, 100, 64, FAKE, None) == 1

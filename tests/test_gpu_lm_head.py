@@ -94,11 +94,39 @@ def run_verify(h, w, draft, T=0.0, u=None, ldh=None):
         wide[:, :h.shape[1]] = h_d
         h_d = wide[:, :h.shape[1]]
     ws = q.Workspace()
-    n_acc, nxt = q.lm_head_verify(h_d, dev_bf16(w), dev(draft), T, None if u is None else dev(u), workspace=ws)
+    n_acc, nxt = q.lm_head_verify(h_d, q.pack_lm_head(dev_bf16(w)), dev(draft), T, None if u is None else dev(u),
+                                  workspace=ws)
     torch.cuda.synchronize()
     assert q.get_device_error()[0] == q.OK
     assert not ws.buf.any().item(), "the workspace must be left zero-filled"
     return n_acc.cpu().numpy(), (None if nxt is None else nxt.cpu().numpy())
+
+
+# ------------------------------------------------------------- packing
+
+def unpack_lm_head(buf: np.ndarray, V: int, K: int) -> np.ndarray:
+    """[V][K] BF16 bits from the packed layout documented in include/quasar.h:
+    16 KB blocks (tile t, K block kb) at (t*KB + kb) * 16384, row r at r*128,
+    its 16-byte chunk c at chunk position c ^ (r % 8)."""
+    KB, T = -(-K // 64), -(-V // 128)
+    blk = buf.view(np.uint16).reshape(T, KB, 128, 8, 8)        # [t][kb][row][pos][8 values]
+    r = np.arange(128)[:, None]
+    c = np.arange(8)[None, :]
+    rows = blk[:, :, r, c ^ (r & 7), :]                         # chunk c of row r
+    full = rows.transpose(0, 2, 1, 3, 4).reshape(T * 128, KB * 64)
+    return full[:V, :K], full
+
+
+@pytest.mark.parametrize("V,K", [(1000, 200), (128, 64), (300, 72), (VOCAB, HID)])
+def test_pack_layout(V, K):
+    w = synth.grid_lm_head_weight(661, V, K) if V < VOCAB else synth.lm_head_weight(505, V, K)
+    wp = q.pack_lm_head(dev_bf16(w))
+    assert wp.buf.numel() == -(-V // 128) * -(-K // 64) * 16384
+    got, full = unpack_lm_head(wp.buf.cpu().numpy(), V, K)
+    assert np.array_equal(got, w)
+    pad = full.copy()
+    pad[:V, :K] = 0
+    assert not pad.any(), "rows past V and K values past K must be zero"
 
 
 # ------------------------------------------------------------- logits
@@ -108,7 +136,7 @@ def run_verify(h, w, draft, T=0.0, u=None, ldh=None):
 def test_logits_grid_bit_exact(M, V, K):
     h = synth.grid_hidden_states(601 + M, M, K)
     w = synth.grid_lm_head_weight(602 + V, V, K)
-    got = host_bf16_bits(q.lm_head_logits(dev_bf16(h), dev_bf16(w)))
+    got = host_bf16_bits(q.lm_head_logits(dev_bf16(h), q.pack_lm_head(dev_bf16(w))))
     want = orc.lm_head_logits(h, w)
     bad = np.argwhere(got != want)
     assert bad.size == 0, f"{len(bad)} logits differ, first at {bad[:3].tolist()}"
@@ -118,7 +146,7 @@ def test_logits_grid_bit_exact(M, V, K):
 def test_logits_recipe_within_one_ulp(M, V, K):
     h = synth.hidden_states(611, M, K)
     w = synth.lm_head_weight(612, V, K)
-    _check_recipe_logits(h, w, host_bf16_bits(q.lm_head_logits(dev_bf16(h), dev_bf16(w))))
+    _check_recipe_logits(h, w, host_bf16_bits(q.lm_head_logits(dev_bf16(h), q.pack_lm_head(dev_bf16(w)))))
 
 
 def _check_recipe_logits(h, w, got, pre=None):
@@ -141,12 +169,13 @@ def test_logits_strided_rows_and_empty():
     wide = torch.zeros(M, K + 72, dtype=torch.bfloat16, device="cuda")
     wide[:, :K] = dev_bf16(h)
     out = torch.full((M, V + 40), 7.0, dtype=torch.bfloat16, device="cuda")
-    q.lm_head_logits(wide[:, :K], dev_bf16(w), logits=out[:, :V])
+    q.lm_head_logits(wide[:, :K], q.pack_lm_head(dev_bf16(w)), logits=out[:, :V])
     got = host_bf16_bits(out)
     assert np.array_equal(got[:, :V], orc.lm_head_logits(h, w))
     assert np.all(orc.bf16_to_f32(got[:, V:]) == 7.0), "columns past V must not be written"
     empty = torch.empty(0, V, dtype=torch.bfloat16, device="cuda")
-    q.lm_head_logits(torch.empty(0, K, dtype=torch.bfloat16, device="cuda"), dev_bf16(w), logits=empty)
+    q.lm_head_logits(torch.empty(0, K, dtype=torch.bfloat16, device="cuda"), q.pack_lm_head(dev_bf16(w)),
+                     logits=empty)
     torch.cuda.synchronize()
 
 
@@ -184,7 +213,7 @@ def test_fused_sampled_grid_matches_oracle(B, D, V, K, T):
 
 
 def test_fused_empty_batch():
-    w = dev_bf16(synth.grid_lm_head_weight(651, 1000, 64))
+    w = q.pack_lm_head(dev_bf16(synth.grid_lm_head_weight(651, 1000, 64)))
     h = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
     n_acc, nxt = q.lm_head_verify(h, w, torch.empty(0, 3, dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
@@ -207,7 +236,7 @@ def recipe_c5():
 
 def test_recipe_logits_full_vocab(recipe_c5):
     B, D, h, w, lg, lo, hi, draft = recipe_c5
-    got = host_bf16_bits(q.lm_head_logits(dev_bf16(h), dev_bf16(w)))
+    got = host_bf16_bits(q.lm_head_logits(dev_bf16(h), q.pack_lm_head(dev_bf16(w))))
     _check_recipe_logits(h, w, got, (lg, lo, hi))
 
 
@@ -216,7 +245,7 @@ def test_recipe_fused_greedy(recipe_c5):
     V = w.shape[0]
     n_acc, nxt = run_verify(h, w, draft)
     # bit for bit against the unfused GPU path on this kernel's own logits
-    lg_gpu = q.lm_head_logits(dev_bf16(h), dev_bf16(w)).view(B, D + 1, V)
+    lg_gpu = q.lm_head_logits(dev_bf16(h), q.pack_lm_head(dev_bf16(w))).view(B, D + 1, V)
     n2, x2 = q.verify_accept(lg_gpu, dev(draft))
     assert np.array_equal(n_acc, n2.cpu().numpy()) and np.array_equal(nxt, x2.cpu().numpy())
     # against the oracle wherever no logit inside its interval can change a decision

@@ -13,12 +13,17 @@
 // lm_head_kernel: persistent, one CTA per SM, vocabulary tiles dealt round
 // robin.  Swap-AB: 128 vocabulary rows are the MMA's M (the A operand, from
 // the weight stream), the token rows its N (B, at most 256 per MMA, two MMAs
-// for more).  Both operands arrive by TMA in 128B-swizzled K-major tiles of
-// 64 K values; tcgen05.mma kind::f16 with BF16 inputs accumulates in fp32 in
-// TMEM.  Roles: warps 0-3 drain the accumulator (TMEM lane quarter = warp),
-// warp 4 issues the copies, warp 5 the MMAs, warp 6 does every mbarrier wait
-// for warp 5 (an MMA-issuing thread that touches memory waits for its queued
-// MMAs to be accepted, which would drain the tensor pipe at every stage).
+// for more).  The weight is packed offline into contiguous 16 KB blocks of
+// 128 rows x 64 K values, each already in the 128B-swizzled K-major layout
+// the MMA reads, and streams in with 1-D bulk copies: whole blocks keep the
+// HBM accesses long and sequential, where a 2-D tile of a row-major [V][K]
+// weight would read 128 bytes from each of 128 rows 8 KB apart.  The token
+// rows come by TMA (they are small and stay in L2).  tcgen05.mma kind::f16
+// with BF16 inputs accumulates in fp32 in TMEM.  Roles: warps 0-3 drain the
+// accumulator (TMEM lane quarter = warp), warp 4 issues the copies, warp 5
+// the MMAs, warp 6 does every mbarrier wait for warp 5 (an MMA-issuing
+// thread that touches memory waits for its queued MMAs to be accepted, which
+// would drain the tensor pipe at every stage).
 //
 // The accumulator of local tile i sits at TMEM column 0 (i even) or
 // 512 - Tp (i odd).  For Tp <= 256 the two regions are disjoint, so the
@@ -46,8 +51,8 @@ namespace lmhead {
 
 constexpr int BMV = 128;            // vocabulary rows per tile (MMA M)
 constexpr int BKE = 64;             // K elements per stage (one 128-byte swizzle row)
-constexpr int A_BYTES = BMV * 128;  // 16 KB of weights per stage
-constexpr int EPI_WARPS = 4;
+constexpr int A_BYTES = BMV * 128;  // 16 KB of weights per stage (one packed block)
+constexpr int EPI_WARPS = 4;       // warps 0-3: accumulator drain (TMEM lane quarter = warp)
 constexpr int PRODUCER_WARP = 4;
 constexpr int MMA_WARP = 5;
 constexpr int WAITER_WARP = 6;
@@ -71,6 +76,7 @@ struct Params {
   int KB;          // K steps of 64
   int stages;
   uint32_t idesc;
+  const uint8_t* wp;      // packed weight blocks [n_vt][KB][16 KB]
   __nv_bfloat16* logits;  // MODE_LOGITS: [Mt][ldl]
   long long ldl;
   uint2* rec;      // [Mt][n_vt] {key, fp32 bits of the tile's exp-sum}
@@ -99,9 +105,10 @@ QUASAR_DEVICE_INLINE uint64_t sw128_desc(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// The four K=16 MMAs of one 64-K stage for one token block, issued from one
-// asm statement so that nothing is scheduled between them.  Descriptor
-// starts advance 32 bytes (2 units of 16) per K step inside the swizzle row.
+// The four K=16 MMAs of one 64-K stage for one token block, both operands
+// from shared memory, issued from one asm statement so that nothing is
+// scheduled between them.  Descriptor starts advance 32 bytes (2 units of
+// 16) per K step inside the 128-byte swizzle row.
 QUASAR_DEVICE_INLINE void mma_stage(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
   asm volatile(
       "{\n\t.reg .pred p, t;\n\t"
@@ -118,13 +125,6 @@ QUASAR_DEVICE_INLINE void mma_stage(uint32_t d, uint64_t a, uint64_t b, uint32_t
 
 QUASAR_DEVICE_INLINE void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-QUASAR_DEVICE_INLINE void l2_prefetch_2d(const void* tmap, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(tmap)),
-               "r"(x), "r"(y)
-               : "memory");
 }
 
 // BF16 bits <-> a 16-bit key whose unsigned order is the numeric order.
@@ -164,8 +164,7 @@ QUASAR_DEVICE_INLINE T transpose_reduce32(T (&v)[32], int lane, Op op) {
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    lm_head_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
-                   const Params p) {
+    lm_head_kernel(const __grid_constant__ CUtensorMap tmH, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
@@ -204,7 +203,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
   }
   if (warp == PRODUCER_WARP && lane == 0) {
-    prefetch_tmap(&tmW);
     prefetch_tmap(&tmH);
   }
   tc_fence_before();
@@ -226,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = 0; i < pre; ++i) {
         const int t = (int)blockIdx.x + (i / KB) * (int)gridDim.x;
         mbar_arrive_expect_tx(&full[i], STAGE);
-        tma_load_2d(ring + (size_t)i * STAGE, &tmW, (i % KB) * BKE, t * BMV, &full[i], pol_w);
+        bulk_load(ring + (size_t)i * STAGE, p.wp + ((size_t)t * KB + i % KB) * A_BYTES, A_BYTES, &full[i], pol_w);
       }
       pdl_wait();  // H is written by the previous kernel
       int issued = 0;
@@ -239,12 +237,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (i >= pre) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err, SITE_LMH_EMPTY, p.limit_ns)) break;
           mbar_arrive_expect_tx(&full[s], STAGE);
-          tma_load_2d(st, &tmW, kb * BKE, t * BMV, &full[s], pol_w);
+          bulk_load(st, p.wp + ((size_t)t * KB + kb) * A_BYTES, A_BYTES, &full[s], pol_w);
         }
-        // Warm L2 with the weights S stages ahead, so that the copy issued
-        // when that stage frees finds them there.
-        const int ia = i + S;
-        if (ia < items) l2_prefetch_2d(&tmW, (ia % KB) * BKE, ((int)blockIdx.x + (ia / KB) * (int)gridDim.x) * BMV);
         for (int h = 0; h < p.nmma; ++h)
           tma_load_2d(st + A_BYTES + (size_t)h * p.Nh * 128, &tmH, kb * BKE, h * p.Nh, &full[s], pol_h);
       }
@@ -301,7 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int tid = threadIdx.x;  // 0..127
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const int G = Tp / 32;
-    const int n_ovl = Tp > 256 ? (2 * Tp - TMEM_COLS) / 32 : 0;
+    const int n_ovl = 2 * Tp > TMEM_COLS ? (2 * Tp - TMEM_COLS) / 32 : 0;
     pdl_wait();  // drafts come from, and the outputs are read by, neighbouring kernels
     if (MODE == MODE_SAMPLED) {
       for (int c = tid; c < Tp; c += 128) {
@@ -554,8 +548,7 @@ size_t verify_workspace_size(int B, int D, int V) {
 }
 
 template <int MODE>
-static cudaError_t launch_main(const CUtensorMap& tw, const CUtensorMap& th, const Params& p, int grid,
-                               cudaStream_t stream) {
+static cudaError_t launch_main(const CUtensorMap& th, const Params& p, int grid, cudaStream_t stream) {
   const uint32_t smem = smem_bytes(p.Tp, p.stages);
   cudaError_t e = cudaFuncSetAttribute(lm_head_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_LIMIT);
@@ -570,7 +563,7 @@ static cudaError_t launch_main(const CUtensorMap& tw, const CUtensorMap& th, con
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lm_head_kernel<MODE>, tw, th, p);
+  return cudaLaunchKernelEx(&cfg, lm_head_kernel<MODE>, th, p);
 }
 
 template <int MODE>
@@ -589,13 +582,12 @@ static cudaError_t launch_fin(const FinParams& f, int rows, cudaStream_t stream)
 }
 
 // Shared argument checks and the main kernel's parameters.
-static quasar_status_t setup(const void* H, long long ldh, const void* W, long long ldw, int Mt, int V, int K,
-                             CUtensorMap* tw, CUtensorMap* th, Params* p, int* grid) {
+static quasar_status_t setup(const void* H, long long ldh, const void* Wp, int Mt, int V, int K, CUtensorMap* th,
+                             Params* p, int* grid) {
   if (Mt < 0 || V <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
-  if (Mt > MAX_ROWS || K % 8 != 0 || ldh < K || ldw < K || ldh % 8 != 0 || ldw % 8 != 0)
-    return QUASAR_ERR_UNSUPPORTED;
-  if (!H || !W) return QUASAR_ERR_INVALID_ARG;
-  if (!aligned(H, 16) || !aligned(W, 16)) return QUASAR_ERR_UNSUPPORTED;
+  if (Mt > MAX_ROWS || K % 8 != 0 || ldh < K || ldh % 8 != 0) return QUASAR_ERR_UNSUPPORTED;
+  if (!H || !Wp) return QUASAR_ERR_INVALID_ARG;
+  if (!aligned(H, 16) || !aligned(Wp, 16)) return QUASAR_ERR_UNSUPPORTED;
   Params& q = *p;
   q = Params{};
   q.Mt = Mt;
@@ -608,13 +600,13 @@ static quasar_status_t setup(const void* H, long long ldh, const void* W, long l
   q.KB = (K + BKE - 1) / BKE;
   q.stages = stages_for(q.Tp);
   if (q.stages < 2) return QUASAR_ERR_UNSUPPORTED;
+  q.wp = reinterpret_cast<const uint8_t*>(Wp);
   // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B BF16
   // (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at 24.
   q.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(q.Nh >> 3) << 17) | ((uint32_t)(BMV >> 4) << 24);
   q.err = device_error_word();
   q.limit_ns = wait_limit_ns();
   if (!q.err) return QUASAR_ERR_CUDA;
-  if (!encode_2d_bf16(tw, W, K, V, ldw, BKE, BMV)) return QUASAR_ERR_CUDA;
   if (!encode_2d_bf16(th, H, K, Mt, ldh, BKE, q.Nh)) return QUASAR_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return QUASAR_ERR_CUDA;
@@ -622,25 +614,25 @@ static quasar_status_t setup(const void* H, long long ldh, const void* W, long l
   return QUASAR_OK;
 }
 
-quasar_status_t run_logits(const void* H, int ldh, const void* W, int ldw, int M, int V, int K, void* logits,
+quasar_status_t run_logits(const void* H, int ldh, const void* Wp, int M, int V, int K, void* logits,
                            long long ldl, cudaStream_t stream) {
   if (M < 0 || V <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
   if (ldl < V) return QUASAR_ERR_UNSUPPORTED;
   if (M == 0) return QUASAR_OK;
   if (!logits) return QUASAR_ERR_INVALID_ARG;
   if (!aligned(logits, 2)) return QUASAR_ERR_UNSUPPORTED;
-  CUtensorMap tw, th;
+  CUtensorMap th;
   Params p;
   int grid = 0;
-  quasar_status_t st = setup(H, ldh, W, ldw, M, V, K, &tw, &th, &p, &grid);
+  quasar_status_t st = setup(H, ldh, Wp, M, V, K, &th, &p, &grid);
   if (st != QUASAR_OK) return st;
   p.logits = reinterpret_cast<__nv_bfloat16*>(logits);
   p.ldl = ldl;
-  return cuda_status(launch_main<MODE_LOGITS>(tw, th, p, grid, stream));
+  return cuda_status(launch_main<MODE_LOGITS>(th, p, grid, stream));
 }
 
-quasar_status_t run_verify(const void* H, int ldh, const void* W, int ldw, int K, const int32_t* draft, int B, int D,
-                           int V, float temperature, const float* u, int32_t* n_acc, int32_t* next, void* ws,
+quasar_status_t run_verify(const void* H, int ldh, const void* Wp, int K, const int32_t* draft, int B, int D, int V,
+                           float temperature, const float* u, int32_t* n_acc, int32_t* next, void* ws,
                            size_t ws_bytes, cudaStream_t stream) {
   if (B < 0 || D < 0 || V <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
   if (!(temperature >= 0.f) || !(temperature < INFINITY)) return QUASAR_ERR_INVALID_ARG;
@@ -650,10 +642,10 @@ quasar_status_t run_verify(const void* H, int ldh, const void* W, int ldw, int K
   if (!n_acc || (D > 0 && !draft) || (sampled && D > 0 && !u) || (sampled && next)) return QUASAR_ERR_INVALID_ARG;
   if (!ws || ws_bytes < verify_workspace_size(B, D, V) || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
   const int Mt = B * (D + 1);
-  CUtensorMap tw, th;
+  CUtensorMap th;
   Params p;
   int grid = 0;
-  quasar_status_t st = setup(H, ldh, W, ldw, Mt, V, K, &tw, &th, &p, &grid);
+  quasar_status_t st = setup(H, ldh, Wp, Mt, V, K, &th, &p, &grid);
   if (st != QUASAR_OK) return st;
 
   uint8_t* w8 = reinterpret_cast<uint8_t*>(ws);
@@ -687,13 +679,53 @@ quasar_status_t run_verify(const void* H, int ldh, const void* W, int ldw, int K
 
   cudaError_t e;
   if (sampled) {
-    e = launch_main<MODE_SAMPLED>(tw, th, p, grid, stream);
+    e = launch_main<MODE_SAMPLED>(th, p, grid, stream);
     if (e == cudaSuccess) e = launch_fin<MODE_SAMPLED>(f, Mt, stream);
   } else {
-    e = launch_main<MODE_GREEDY>(tw, th, p, grid, stream);
+    e = launch_main<MODE_GREEDY>(th, p, grid, stream);
     if (e == cudaSuccess) e = launch_fin<MODE_GREEDY>(f, Mt, stream);
   }
   return cuda_status(e);
+}
+
+// ------------------------------------------------------------ offline packing
+
+size_t packed_bytes(int V, int K) {
+  if (V <= 0 || K <= 0) return 0;
+  return (size_t)((V + BMV - 1) / BMV) * (size_t)((K + BKE - 1) / BKE) * A_BYTES;
+}
+
+// One thread per 16-byte chunk of the packed weight: block (t, kb), row r,
+// position pos holds the K values kb*64 + 8c .. +8 of vocabulary row
+// t*128 + r with c = pos ^ (r % 8); chunks past V or K are zero.
+__global__ void pack_kernel(const uint4* __restrict__ W, long long ldw16, int V, int K8, int KB, long long chunks,
+                            uint4* __restrict__ out) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int pos = (int)(i & 7);
+    const int r = (int)((i >> 3) & (BMV - 1));
+    const long long blk = i >> 10;  // 128 rows x 8 chunks per block
+    const int kb = (int)(blk % KB);
+    const long long t = blk / KB;
+    const long long v = t * BMV + r;
+    const int c8 = kb * 8 + (pos ^ (r & 7));  // 16-byte chunk index along K
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (v < V && c8 < K8) val = W[v * ldw16 + c8];
+    out[i] = val;
+  }
+}
+
+quasar_status_t run_pack(const void* W, int ldw, int V, int K, void* Wp, cudaStream_t stream) {
+  if (V <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
+  if (K % 8 != 0 || ldw < K || ldw % 8 != 0) return QUASAR_ERR_UNSUPPORTED;
+  if (!W || !Wp) return QUASAR_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(Wp, 16)) return QUASAR_ERR_UNSUPPORTED;
+  const long long chunks = (long long)(packed_bytes(V, K) / 16);
+  const int sms = sm_count();
+  if (sms <= 0) return QUASAR_ERR_CUDA;
+  pack_kernel<<<sms * 8, 256, 0, stream>>>(reinterpret_cast<const uint4*>(W), ldw / 8, V, K / 8,
+                                          (K + BKE - 1) / BKE, chunks, reinterpret_cast<uint4*>(Wp));
+  return cuda_status(cudaGetLastError());
 }
 
 }  // namespace lmhead
@@ -701,21 +733,27 @@ quasar_status_t run_verify(const void* H, int ldh, const void* W, int ldw, int K
 
 extern "C" {
 
+size_t quasar_lm_head_packed_bytes(int V, int K) { return quasar::lmhead::packed_bytes(V, K); }
+
+quasar_status_t quasar_pack_lm_head(const void* W_bf16, int ldw, int V, int K, void* Wp, quasar_stream_t stream) {
+  return quasar::lmhead::run_pack(W_bf16, ldw, V, K, Wp, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t quasar_lm_head_verify_workspace_size(int B, int D, int V) {
   return quasar::lmhead::verify_workspace_size(B, D, V);
 }
 
-quasar_status_t quasar_lm_head_logits(const void* H_bf16, int ldh, const void* W_bf16, int ldw, int M, int V, int K,
+quasar_status_t quasar_lm_head_logits(const void* H_bf16, int ldh, const void* Wp, int M, int V, int K,
                                       void* logits_bf16, long long ldl, quasar_stream_t stream) {
-  return quasar::lmhead::run_logits(H_bf16, ldh, W_bf16, ldw, M, V, K, logits_bf16, ldl,
+  return quasar::lmhead::run_logits(H_bf16, ldh, Wp, M, V, K, logits_bf16, ldl,
                                     reinterpret_cast<cudaStream_t>(stream));
 }
 
-quasar_status_t quasar_lm_head_verify(const void* H_bf16, int ldh, const void* W_bf16, int ldw, int K,
-                                      const int32_t* draft, int B, int D, int V, float temperature, const float* u,
-                                      int32_t* n_acc, int32_t* next_token, void* workspace, size_t ws_bytes,
+quasar_status_t quasar_lm_head_verify(const void* H_bf16, int ldh, const void* Wp, int K, const int32_t* draft,
+                                      int B, int D, int V, float temperature, const float* u, int32_t* n_acc,
+                                      int32_t* next_token, void* workspace, size_t ws_bytes,
                                       quasar_stream_t stream) {
-  return quasar::lmhead::run_verify(H_bf16, ldh, W_bf16, ldw, K, draft, B, D, V, temperature, u, n_acc, next_token,
+  return quasar::lmhead::run_verify(H_bf16, ldh, Wp, K, draft, B, D, V, temperature, u, n_acc, next_token,
                                     workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 

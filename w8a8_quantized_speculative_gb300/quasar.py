@@ -53,8 +53,10 @@ _SIGS = {
     "quasar_verify_accept": (_i, [_p, _i, _p, _i, _i, _i, _f, _p, _p, _p, _p, _sz, _p]),
     "quasar_verify_sample": (_i, [_p, _i, _p, _i, _i, _i, _f, _p, _p, _p, _p, _p, _sz, _p]),
     "quasar_lm_head_verify_workspace_size": (_sz, [_i, _i, _i]),
-    "quasar_lm_head_verify": (_i, [_p, _i, _p, _i, _i, _p, _i, _i, _i, _f, _p, _p, _p, _p, _sz, _p]),
-    "quasar_lm_head_logits": (_i, [_p, _i, _p, _i, _i, _i, _i, _p, ctypes.c_longlong, _p]),
+    "quasar_lm_head_packed_bytes": (_sz, [_i, _i]),
+    "quasar_pack_lm_head": (_i, [_p, _i, _i, _i, _p, _p]),
+    "quasar_lm_head_verify": (_i, [_p, _i, _p, _i, _p, _i, _i, _i, _f, _p, _p, _p, _p, _sz, _p]),
+    "quasar_lm_head_logits": (_i, [_p, _i, _p, _i, _i, _i, _p, ctypes.c_longlong, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -344,43 +346,59 @@ def verify_sample(logits: torch.Tensor, draft: torch.Tensor, temperature: float,
                                     _stream(stream)), "verify_sample")
     return n_acc, next_token
 
-def lm_head_logits(h: torch.Tensor, w: torch.Tensor, logits=None, stream=None):
-    """logits[m][v] = bf16(fp32 sum_k h[m][k] * w[v][k]) (bf16 [M][V]) from
-    the tcgen05 lm_head kernel.  h: bf16 [M][K], w: bf16 [V][K]."""
-    _need(h, torch.bfloat16, "h")
+class PackedLmHead:
+    """An lm_head weight W [V][K] (BF16) packed by quasar_pack_lm_head into
+    the kernels' 16 KB block layout (see include/quasar.h)."""
+
+    def __init__(self, buf: torch.Tensor, V: int, K: int):
+        self.buf, self.V, self.K = buf, V, K
+
+
+def pack_lm_head(w: torch.Tensor, stream=None) -> PackedLmHead:
+    """Pack a BF16 lm_head weight [V][K] (offline, once)."""
     _need(w, torch.bfloat16, "w")
-    ldh, ldw = _rowmajor(h, "h"), _rowmajor(w, "w")
+    ldw = _rowmajor(w, "w")
+    V, K = w.shape
+    buf = torch.empty(int(lib.quasar_lm_head_packed_bytes(V, K)), dtype=torch.uint8, device=w.device)
+    _check(lib.quasar_pack_lm_head(_ptr(w), ldw, V, K, _ptr(buf), _stream(stream)), "pack_lm_head")
+    return PackedLmHead(buf, V, K)
+
+
+def lm_head_logits(h: torch.Tensor, wp: PackedLmHead, logits=None, stream=None):
+    """logits[m][v] = bf16(fp32 sum_k h[m][k] * W[v][k]) (bf16 [M][V]) from
+    the tcgen05 lm_head kernel.  h: bf16 [M][K]; wp: pack_lm_head(W)."""
+    _need(h, torch.bfloat16, "h")
+    ldh = _rowmajor(h, "h")
     M, K = h.shape
-    V = w.shape[0]
-    if w.shape[1] != K:
-        raise ValueError("h and w must share K")
+    V = wp.V
+    if wp.K != K:
+        raise ValueError("h and the packed weight must share K")
     if logits is None:
         logits = torch.empty(M, V, dtype=torch.bfloat16, device=h.device)
     _need(logits, torch.bfloat16, "logits")
     ldl = _rowmajor(logits, "logits")
-    _check(lib.quasar_lm_head_logits(_ptr(h), ldh, _ptr(w), ldw, M, V, K, _ptr(logits), ldl, _stream(stream)),
+    _check(lib.quasar_lm_head_logits(_ptr(h), ldh, _ptr(wp.buf), M, V, K, _ptr(logits), ldl, _stream(stream)),
            "lm_head_logits")
     return logits
 
 
-def lm_head_verify(h: torch.Tensor, w: torch.Tensor, draft: torch.Tensor, temperature: float = 0.0, u=None,
+def lm_head_verify(h: torch.Tensor, wp: PackedLmHead, draft: torch.Tensor, temperature: float = 0.0, u=None,
                    want_next: bool = True, n_acc=None, next_token=None, workspace: Workspace | None = None,
                    stream=None):
     """The BF16 lm_head and verification in one call, without writing the
     logits: accepted prefix length (int32 [B]) and, for T == 0, the next
     token.  h: bf16 [B*(D+1)][K] (row b*(D+1)+j scores draft j of sequence
-    b), w: bf16 [V][K], draft: int32 [B][D], u: fp32 [B][D] for T > 0."""
+    b), wp: pack_lm_head(W), draft: int32 [B][D], u: fp32 [B][D] for T > 0."""
     _need(h, torch.bfloat16, "h")
-    _need(w, torch.bfloat16, "w")
     _need(draft, torch.int32, "draft")
-    ldh, ldw = _rowmajor(h, "h"), _rowmajor(w, "w")
+    ldh = _rowmajor(h, "h")
     if draft.dim() != 2 or not draft.is_contiguous():
         raise ValueError("draft must be a contiguous [B][D] tensor")
     B, D = draft.shape
     K = h.shape[1]
-    V = w.shape[0]
-    if h.shape[0] != B * (D + 1) or w.shape[1] != K:
-        raise ValueError("h must be [B*(D+1)][K] and w [V][K]")
+    V = wp.V
+    if h.shape[0] != B * (D + 1) or wp.K != K:
+        raise ValueError("h must be [B*(D+1)][K] with the packed weight's K")
     n_acc = torch.empty(B, dtype=torch.int32, device=h.device) if n_acc is None else n_acc
     sampled = temperature > 0
     if sampled:
@@ -391,7 +409,7 @@ def lm_head_verify(h: torch.Tensor, w: torch.Tensor, draft: torch.Tensor, temper
         next_token = torch.empty(B, dtype=torch.int32, device=h.device)
     ws = _ws(workspace, h.device)
     buf = ws.get(int(lib.quasar_lm_head_verify_workspace_size(B, D, V)))
-    _check(lib.quasar_lm_head_verify(_ptr(h), ldh, _ptr(w), ldw, K, _ptr(draft), B, D, V, float(temperature),
+    _check(lib.quasar_lm_head_verify(_ptr(h), ldh, _ptr(wp.buf), K, _ptr(draft), B, D, V, float(temperature),
                                      _ptr(u), _ptr(n_acc), _ptr(next_token), _ptr(buf), buf.numel(),
                                      _stream(stream)), "lm_head_verify")
     return n_acc, next_token
