@@ -394,6 +394,25 @@ quasar_status_t quasar_lm_head_verify(const void* H_bf16, int ldh,
                                       void* workspace, size_t ws_bytes,
                                       quasar_stream_t stream);
 
+/* The fused lm_head + verification for T > 0 with the lossless next token:
+ * the acceptance test of quasar_lm_head_verify at T > 0, then next_token[b]
+ * drawn exactly as quasar_verify_sample draws it (inverse CDF on u_next[b]
+ * over row n_acc's softmax without the rejected draft, or over the bonus
+ * row after D acceptances).  The vocabulary tile holding the draw is found
+ * from the per-tile records; its 128 logits are recomputed from Wp and H
+ * (fp32 sums, one rounding to BF16) for the walk inside it.
+ *   temperature > 0; u as above; u_next [B] fp32 in [0, 1); next_token [B]
+ *   int32 output (both required); everything else as quasar_lm_head_verify.
+ * ------------------------------------------------------------------------ */
+quasar_status_t quasar_lm_head_verify_sample(const void* H_bf16, int ldh,
+                                             const void* Wp, int K,
+                                             const int32_t* draft, int B, int D, int V,
+                                             float temperature, const float* u,
+                                             const float* u_next,
+                                             int32_t* n_acc, int32_t* next_token,
+                                             void* workspace, size_t ws_bytes,
+                                             quasar_stream_t stream);
+
 /* The same BF16 lm_head kernel writing its logits instead:
  *   logits[m][v] = bf16_rne(fp32 sum_k H[m][k] * W[v][k]),
  *   logits [M][ldl] BF16 (ldl >= V), 2-byte aligned; 0 <= M <= 512;

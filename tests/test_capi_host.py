@@ -223,6 +223,16 @@ def test_lm_head_rejects_bad_arguments(lib):
     assert g(FAKE, 64, FAKE, 513, 1000, 64, FAKE, 1000, None) == 2  # M > 512
     assert g(FAKE, 64, FAKE, 2, 1000, 64, None, 1000, None) == 1
     assert g(FAKE, 64, FAKE, 0, 1000, 64, None, 1000, None) == 0
+    fs = lib.quasar_lm_head_verify_sample
+    fs.restype = ctypes.c_int
+    fs.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                   ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    assert fs(FAKE, 64, FAKE, 64, FAKE, 2, 3, 1000, 0.0, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == 1  # T > 0
+    assert fs(FAKE, 64, FAKE, 64, FAKE, 2, 3, 1000, 1.0, FAKE, None, FAKE, FAKE, FAKE, 1 << 20, None) == 1  # u_next
+    assert fs(FAKE, 64, FAKE, 64, FAKE, 2, 3, 1000, 1.0, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, None) == 1  # next
+    assert fs(FAKE, 64, FAKE, 64, FAKE, 2, 3, 1000, 1.0, None, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == 1  # u
+    assert fs(FAKE, 64, FAKE, 64, FAKE, 0, 3, 1000, 1.0, None, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == 0  # B = 0
     lib.quasar_lm_head_packed_bytes.restype = ctypes.c_size_t
     assert lib.quasar_lm_head_packed_bytes(151936, 4096) == 1187 * 64 * 16384
     assert lib.quasar_lm_head_packed_bytes(1000, 200) == 8 * 4 * 16384

@@ -30,6 +30,7 @@ if not torch.cuda.is_available():
 
 import oracle as orc  # noqa: E402
 from tests.gpu_util import dev, dev_bf16, host_bf16_bits  # noqa: E402
+from tests.test_gpu_parity import _acc_uniforms, _u_next_midpoints  # noqa: E402
 from w8a8_quantized_speculative_gb300 import quasar as q  # noqa: E402
 from w8a8_quantized_speculative_gb300 import synth  # noqa: E402
 
@@ -210,6 +211,50 @@ def test_fused_sampled_grid_matches_oracle(B, D, V, K, T):
     want_n, _ = orc.verify_accept(lg.reshape(B, D + 1, V), draft, T, u)
     assert np.array_equal(n_acc, want_n)
     assert 0 < want_n.mean() < D, "the case should accept some drafts and reject others"
+
+
+@pytest.mark.parametrize("B,D,V,K,T", [(3, 5, 40000, 512, 40.0), (4, 0, 5000, 128, 20.0), (6, 2, 1000, 200, 8.0),
+                                       (32, 8, VOCAB, HID, 60.0)])
+def test_fused_sample_next_grid_matches_oracle(B, D, V, K, T):
+    """The lossless next token of the fused path against the oracle's
+    verify_sample on the same (exact) logits, u_next at the middle of a
+    token's interval."""
+    h = synth.grid_hidden_states(671 + B, B * (D + 1), K)
+    w = synth.grid_lm_head_weight(672 + V, V, K)
+    lg = orc.lm_head_logits(h, w).reshape(B, D + 1, V)
+    draft = forced_drafts(lg, B, D, 673, 674)
+    u = _acc_uniforms(lg, draft, T, 675) if D else np.zeros((B, 0), np.float32)
+    n_r, _ = orc.verify_accept(lg, draft, T, u)
+    u_next = _u_next_midpoints(lg, draft, T, n_r, np.random.default_rng(676))
+    ws = q.Workspace()
+    n_acc, nxt = q.lm_head_verify_sample(dev_bf16(h), q.pack_lm_head(dev_bf16(w)), dev(draft), T,
+                                         dev(u) if D else None, dev(u_next), workspace=ws)
+    torch.cuda.synchronize()
+    assert q.get_device_error()[0] == q.OK
+    assert not ws.buf.any().item(), "the workspace must be left zero-filled"
+    n_o, nxt_o = orc.verify_sample(lg, draft, T, u, u_next.astype(np.float64))
+    assert np.array_equal(n_acc.cpu().numpy(), n_o)
+    assert np.array_equal(nxt.cpu().numpy(), nxt_o)
+    if D:
+        assert 0 < n_o.mean() < D or B < 4
+
+
+def test_fused_sample_next_recipe_matches_unfused(recipe_c5):
+    """On the workload recipe the fused draw equals verify_sample run on the
+    same kernel's logits (u_next at interval midpoints of those logits)."""
+    B, D, h, w, lg, lo, hi, draft = recipe_c5
+    V = w.shape[0]
+    T = 1.0
+    wp = q.pack_lm_head(dev_bf16(w))
+    lg_gpu = q.lm_head_logits(dev_bf16(h), wp)
+    lg_bits = host_bf16_bits(lg_gpu).reshape(B, D + 1, V)
+    u = _acc_uniforms(lg_bits, draft, T, 677)
+    n_g, _ = orc.verify_accept(lg_bits, draft, T, u)
+    u_next = _u_next_midpoints(lg_bits, draft, T, n_g, np.random.default_rng(678))
+    n1, x1 = q.lm_head_verify_sample(dev_bf16(h), wp, dev(draft), T, dev(u), dev(u_next))
+    n2, x2 = q.verify_sample(lg_gpu.view(B, D + 1, V), dev(draft), T, dev(u), dev(u_next))
+    assert np.array_equal(n1.cpu().numpy(), n2.cpu().numpy())
+    assert np.array_equal(x1.cpu().numpy(), x2.cpu().numpy())
 
 
 def test_fused_empty_batch():

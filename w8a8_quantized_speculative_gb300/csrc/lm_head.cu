@@ -64,7 +64,8 @@ constexpr int MAX_ROWS = 512;       // token rows per call (TMEM columns)
 constexpr int MAX_STAGES = 8;
 constexpr int SMEM_LIMIT = 232448;
 
-enum Mode : int { MODE_LOGITS = 0, MODE_GREEDY = 1, MODE_SAMPLED = 2 };
+// MODE_SAMPLE_NEXT is a finishing mode only: the matmul runs as MODE_SAMPLED.
+enum Mode : int { MODE_LOGITS = 0, MODE_GREEDY = 1, MODE_SAMPLED = 2, MODE_SAMPLE_NEXT = 3 };
 
 struct Params {
   int Mt;          // token rows (B * (D + 1) for verification)
@@ -404,7 +405,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 struct RowResult {
   int argmax;
   float p;      // softmax probability of the draft (T > 0)
-  int pad0, pad1;
+  float m;      // the row's largest logit (T > 0)
+  float s;      // the row's sum of exp((l - m) / T) (T > 0)
 };
 
 struct FinParams {
@@ -419,16 +421,166 @@ struct FinParams {
   int32_t* next;
   RowResult* rows;   // [B*(D+1)]
   unsigned int* cnt; // [B], zero between calls
+  // MODE_SAMPLE_NEXT: the lossless next token
+  const float* u_next;
+  const __nv_bfloat16* H;
+  long long ldh;
+  const uint8_t* wp;
+  int K, KB, V;
 };
 
 constexpr int FIN_THREADS = 256;
 
+// Exclusive prefix sum of one float per thread over the block, in thread
+// order (a fixed order: the result is deterministic); returns the total.
+QUASAR_DEVICE_INLINE float block_exclusive_scan(float x, float* s_warp, float& excl) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float incl = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) s_warp[w] = incl;
+  __syncthreads();
+  float before = 0.f, total = 0.f;
+  for (int k = 0; k < FIN_THREADS / 32; ++k) {
+    if (k < w) before += s_warp[k];
+    total += s_warp[k];
+  }
+  __syncthreads();
+  excl = before + incl - x;
+  return total;
+}
+
+// The lossless next token for T > 0 (the rule of quasar_verify_sample): a
+// draw by inverse CDF on u_next from row n's softmax without the rejected
+// draft (n < D) or from the bonus row (n = D).  The tile records give each
+// vocabulary tile's weight; the tile holding u_next x total is found by a
+// prefix sum in tile order, and its 128 logits are recomputed from the
+// packed weight (fp32 sums, one rounding to BF16) for the walk inside it.
+QUASAR_DEVICE_INLINE void draw_next(const FinParams& f, int b, int n, float* s_warp, float* s_f, int* s_i) {
+  const int tid = threadIdx.x;
+  const int R = f.D + 1;
+  const int cr = b * R + n;
+  const float m = __ldcg(&f.rows[cr].m);
+  const int dr = n < f.D ? __ldcg(&f.draft[(size_t)b * f.D + n]) : -1;
+  const float wd = dr >= 0 ? exp2f((__ldcg(&f.dl[cr]) - m) * f.k2) : 0.f;
+  const uint2* rec = f.rec + (size_t)cr * f.n_vt;
+  // Tile weights: thread tid owns the contiguous tiles [t0, t1).
+  const int per = (f.n_vt + FIN_THREADS - 1) / FIN_THREADS;
+  const int t0 = min(tid * per, f.n_vt), t1 = min(t0 + per, f.n_vt);
+  float mine = 0.f;
+  for (int t = t0; t < t1; ++t) {
+    const uint2 r = __ldcg(&rec[t]);
+    float wt = __uint_as_float(r.y) * exp2f((key_value(r.x) - m) * f.k2);
+    if (dr >= 0 && t == dr / BMV) wt = fmaxf(wt - wd, 0.f);
+    mine += wt;
+  }
+  float excl;
+  const float total = block_exclusive_scan(mine, s_warp, excl);
+  if (tid == 0) {
+    s_i[0] = -1;
+    s_i[1] = -1;
+  }
+  __syncthreads();
+  if (!(total > 0.f)) {  // no weight left: the lowest index other than the draft
+    if (tid == 0) f.next[b] = dr == 0 ? 1 : 0;
+    return;
+  }
+  const float target = __ldcg(&f.u_next[b]) * total;
+  {
+    float run = excl;
+    for (int t = t0; t < t1; ++t) {
+      const uint2 r = __ldcg(&rec[t]);
+      float wt = __uint_as_float(r.y) * exp2f((key_value(r.x) - m) * f.k2);
+      if (dr >= 0 && t == dr / BMV) wt = fmaxf(wt - wd, 0.f);
+      if (wt > 0.f) {
+        if (run + wt > target) {
+          atomicMin(reinterpret_cast<unsigned int*>(&s_i[0]), (unsigned int)t);  // -1 is the largest
+          break;
+        }
+        atomicMax(&s_i[1], t);  // last tile with weight (rounding fallback)
+      }
+      run += wt;
+    }
+  }
+  __syncthreads();
+  const int ts = s_i[0] >= 0 ? s_i[0] : s_i[1];
+  // cumulative weight before tile ts, recomputed in the same order by its owner
+  if (tid == 0) s_f[0] = 0.f;
+  __syncthreads();
+  if (ts >= t0 && ts < t1) {
+    float run = excl;
+    for (int t = t0; t < ts; ++t) {
+      const uint2 r = __ldcg(&rec[t]);
+      float wt = __uint_as_float(r.y) * exp2f((key_value(r.x) - m) * f.k2);
+      if (dr >= 0 && t == dr / BMV) wt = fmaxf(wt - wd, 0.f);
+      run += wt;
+    }
+    s_f[0] = run;
+  }
+  // Recompute the tile's logits for token row cr: two threads per row, each
+  // half of the K blocks of the packed weight.
+  const int r = tid & (BMV - 1), kh = tid >> 7;
+  const int kb0 = kh * ((f.KB + 1) / 2), kb1 = min(f.KB, kb0 + (f.KB + 1) / 2);
+  const __nv_bfloat16* hrow = f.H + (size_t)cr * f.ldh;
+  float acc = 0.f;
+  for (int kb = kb0; kb < kb1; ++kb) {
+    const uint8_t* wrow = f.wp + ((size_t)ts * f.KB + kb) * A_BYTES + r * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int k0 = kb * BKE + 8 * c;
+      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wrow + ((c ^ (r & 7)) << 4)));
+      const __nv_bfloat16* wb = reinterpret_cast<const __nv_bfloat16*>(&wv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (k0 + e < f.K) acc += __bfloat162float(wb[e]) * __bfloat162float(hrow[k0 + e]);
+    }
+  }
+  s_f[8 + tid] = acc;
+  __syncthreads();
+  float e = 0.f;
+  if (tid < BMV) {
+    const int v = ts * BMV + tid;
+    const float x = __bfloat162float(__float2bfloat16_rn(s_f[8 + tid] + s_f[8 + BMV + tid]));
+    e = (v < f.V && v != dr) ? exp2f((x - m) * f.k2) : 0.f;
+  }
+  float ex;
+  block_exclusive_scan(tid < BMV ? e : 0.f, s_warp, ex);
+  const float tgt = target - s_f[0];
+  if (tid == 0) {
+    s_i[2] = -1;
+    s_i[3] = -1;
+  }
+  __syncthreads();
+  if (tid < BMV && e > 0.f) {
+    if (ex + e > tgt) atomicMin(reinterpret_cast<unsigned int*>(&s_i[2]), (unsigned int)tid);
+    atomicMax(&s_i[3], tid);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int v = s_i[2] >= 0 ? s_i[2] : s_i[3];
+    if (v >= 0) {
+      v += ts * BMV;
+    } else {  // the recomputed tile has no weight left (rounding): the row's argmax, else the lowest non-draft index
+      v = __ldcg(&f.rows[cr].argmax);
+      if (v == dr) v = dr == 0 ? 1 : 0;
+    }
+    f.next[b] = v;
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(FIN_THREADS) lm_head_finalize_kernel(const FinParams f) {
+  constexpr bool SAMPLED = MODE == MODE_SAMPLED || MODE == MODE_SAMPLE_NEXT;
+  constexpr bool KEEP = MODE == MODE_SAMPLE_NEXT;  // records stay until the draw
   __shared__ uint32_t s_ord[FIN_THREADS / 32];
   __shared__ int s_idx[FIN_THREADS / 32];
   __shared__ float s_sum[FIN_THREADS / 32];
-  __shared__ int s_last;
+  __shared__ float s_f[8 + FIN_THREADS];
+  __shared__ int s_i[4];
+  __shared__ int s_last, s_n;
   pdl_wait();
   const int c = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -439,7 +591,7 @@ __global__ void __launch_bounds__(FIN_THREADS) lm_head_finalize_kernel(const Fin
   int bi = INT_MAX;
   for (int t = tid; t < f.n_vt; t += FIN_THREADS) {
     const uint32_t k = __ldcg(&rec[t].x);
-    if (MODE != MODE_SAMPLED) rec[t] = make_uint2(0u, 0u);  // leave the workspace zero-filled
+    if (!SAMPLED) rec[t] = make_uint2(0u, 0u);  // leave the workspace zero-filled
     const uint32_t o = k >> 16;
     const int idx = t * BMV + (int)(0xFFFFu - (k & 0xFFFFu));
     if (o > bo || (o == bo && idx < bi)) {
@@ -471,15 +623,15 @@ __global__ void __launch_bounds__(FIN_THREADS) lm_head_finalize_kernel(const Fin
 
   const int R = f.D + 1;
   const int b = c / R, j = c - b * R;
-  float pj = 0.f;
-  if (MODE == MODE_SAMPLED) {
+  float pj = 0.f, m = 0.f, tot = 0.f;
+  if (SAMPLED) {
     // Pass 2: the row's sum of exp((l - max) / T), tile sums rescaled to the
     // row maximum, in a fixed order.
-    const float m = key_value(bo << 16);
+    m = key_value(bo << 16);
     float s = 0.f;
     for (int t = tid; t < f.n_vt; t += FIN_THREADS) {
       const uint2 r = __ldcg(&rec[t]);
-      rec[t] = make_uint2(0u, 0u);
+      if (!KEEP) rec[t] = make_uint2(0u, 0u);
       s += __uint_as_float(r.y) * exp2f((key_value(r.x) - m) * f.k2);
     }
 #pragma unroll
@@ -487,45 +639,54 @@ __global__ void __launch_bounds__(FIN_THREADS) lm_head_finalize_kernel(const Fin
     __syncthreads();  // s_ord / s_idx reads above are done before s_sum is written
     if (lane == 0) s_sum[w] = s;
     __syncthreads();
-    float tot = 0.f;
     for (int k = 0; k < FIN_THREADS / 32; ++k) tot += s_sum[k];
-    if (j < f.D) {
-      if (tid == 0) pj = exp2f((__ldcg(&f.dl[c]) - m) * f.k2) / tot;
-      if (tid == 0) f.dl[c] = 0.f;
+    if (j < f.D && tid == 0) {
+      pj = exp2f((__ldcg(&f.dl[c]) - m) * f.k2) / tot;
+      if (!KEEP) f.dl[c] = 0.f;
     }
   }
 
   if (tid == 0) {
-    RowResult rr;
-    rr.argmax = bi;
-    rr.p = pj;
-    rr.pad0 = rr.pad1 = 0;
-    f.rows[c] = rr;
+    f.rows[c] = RowResult{bi, pj, m, tot};
     __threadfence();
     const unsigned int prev = atomicAdd(&f.cnt[b], 1u);
     s_last = (prev == (unsigned int)(R - 1)) ? 1 : 0;
   }
   __syncthreads();
-  if (!s_last || tid != 0) return;
+  if (!s_last) return;
   __threadfence();
-  int n = f.D;
-  for (int jj = 0; jj < f.D; ++jj) {
-    const int am = __ldcg(&f.rows[b * R + jj].argmax);
-    const float pr = __ldcg(&f.rows[b * R + jj].p);
-    bool okj;
-    if (MODE == MODE_SAMPLED)
-      okj = __ldcg(&f.u[(size_t)b * f.D + jj]) < pr;
-    else
-      okj = __ldcg(&f.draft[(size_t)b * f.D + jj]) == am;
-    if (!okj) {
-      n = jj;
-      break;
+  if (tid == 0) {
+    int n = f.D;
+    for (int jj = 0; jj < f.D; ++jj) {
+      const int am = __ldcg(&f.rows[b * R + jj].argmax);
+      const float pr = __ldcg(&f.rows[b * R + jj].p);
+      bool okj;
+      if (SAMPLED)
+        okj = __ldcg(&f.u[(size_t)b * f.D + jj]) < pr;
+      else
+        okj = __ldcg(&f.draft[(size_t)b * f.D + jj]) == am;
+      if (!okj) {
+        n = jj;
+        break;
+      }
     }
+    f.n_acc[b] = n;
+    if (!SAMPLED && f.next) f.next[b] = __ldcg(&f.rows[b * R + n].argmax);
+    s_n = n;
   }
-  f.n_acc[b] = n;
-  if (f.next) f.next[b] = __ldcg(&f.rows[b * R + n].argmax);
-  for (int jj = 0; jj < R; ++jj) f.rows[b * R + jj] = RowResult{0, 0.f, 0, 0};
-  f.cnt[b] = 0;
+  __syncthreads();
+  if (MODE == MODE_SAMPLE_NEXT) {
+    draw_next(f, b, s_n, s_sum, s_f, s_i);
+    __syncthreads();
+    // the records and draft logits of this sequence's rows were kept for
+    // the draw: zero them now
+    for (size_t i = tid; i < (size_t)R * f.n_vt; i += FIN_THREADS) f.rec[(size_t)b * R * f.n_vt + i] = make_uint2(0u, 0u);
+    for (int jj = tid; jj < R; jj += FIN_THREADS) f.dl[b * R + jj] = 0.f;
+  }
+  if (tid == 0) {
+    for (int jj = 0; jj < R; ++jj) f.rows[b * R + jj] = RowResult{0, 0.f, 0.f, 0.f};
+    f.cnt[b] = 0;
+  }
 }
 
 // ------------------------------------------------------------ host side
@@ -632,14 +793,17 @@ quasar_status_t run_logits(const void* H, int ldh, const void* Wp, int M, int V,
 }
 
 quasar_status_t run_verify(const void* H, int ldh, const void* Wp, int K, const int32_t* draft, int B, int D, int V,
-                           float temperature, const float* u, int32_t* n_acc, int32_t* next, void* ws,
-                           size_t ws_bytes, cudaStream_t stream) {
+                           float temperature, const float* u, const float* u_next, int32_t* n_acc, int32_t* next,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (B < 0 || D < 0 || V <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
   if (!(temperature >= 0.f) || !(temperature < INFINITY)) return QUASAR_ERR_INVALID_ARG;
   const bool sampled = temperature > 0.f;
+  const bool draw = u_next != nullptr;  // T > 0 with the lossless next token
+  if (draw && (!sampled || !next)) return QUASAR_ERR_INVALID_ARG;
   if (B == 0) return QUASAR_OK;
   if ((long long)B * (D + 1) > MAX_ROWS) return QUASAR_ERR_UNSUPPORTED;
-  if (!n_acc || (D > 0 && !draft) || (sampled && D > 0 && !u) || (sampled && next)) return QUASAR_ERR_INVALID_ARG;
+  if (!n_acc || (D > 0 && !draft) || (sampled && D > 0 && !u) || (sampled && !draw && next))
+    return QUASAR_ERR_INVALID_ARG;
   if (!ws || ws_bytes < verify_workspace_size(B, D, V) || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
   const int Mt = B * (D + 1);
   CUtensorMap th;
@@ -676,11 +840,19 @@ quasar_status_t run_verify(const void* H, int ldh, const void* Wp, int K, const 
   f.next = next;
   f.rows = rows;
   f.cnt = cnt;
+  f.u_next = u_next;
+  f.H = reinterpret_cast<const __nv_bfloat16*>(H);
+  f.ldh = ldh;
+  f.wp = p.wp;
+  f.K = K;
+  f.KB = p.KB;
+  f.V = V;
 
   cudaError_t e;
   if (sampled) {
     e = launch_main<MODE_SAMPLED>(th, p, grid, stream);
-    if (e == cudaSuccess) e = launch_fin<MODE_SAMPLED>(f, Mt, stream);
+    if (e == cudaSuccess)
+      e = draw ? launch_fin<MODE_SAMPLE_NEXT>(f, Mt, stream) : launch_fin<MODE_SAMPLED>(f, Mt, stream);
   } else {
     e = launch_main<MODE_GREEDY>(th, p, grid, stream);
     if (e == cudaSuccess) e = launch_fin<MODE_GREEDY>(f, Mt, stream);
@@ -753,7 +925,17 @@ quasar_status_t quasar_lm_head_verify(const void* H_bf16, int ldh, const void* W
                                       int B, int D, int V, float temperature, const float* u, int32_t* n_acc,
                                       int32_t* next_token, void* workspace, size_t ws_bytes,
                                       quasar_stream_t stream) {
-  return quasar::lmhead::run_verify(H_bf16, ldh, Wp, K, draft, B, D, V, temperature, u, n_acc, next_token,
+  return quasar::lmhead::run_verify(H_bf16, ldh, Wp, K, draft, B, D, V, temperature, u, nullptr, n_acc, next_token,
+                                    workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+quasar_status_t quasar_lm_head_verify_sample(const void* H_bf16, int ldh, const void* Wp, int K,
+                                             const int32_t* draft, int B, int D, int V, float temperature,
+                                             const float* u, const float* u_next, int32_t* n_acc,
+                                             int32_t* next_token, void* workspace, size_t ws_bytes,
+                                             quasar_stream_t stream) {
+  if (!u_next || !next_token || !(temperature > 0.f)) return QUASAR_ERR_INVALID_ARG;
+  return quasar::lmhead::run_verify(H_bf16, ldh, Wp, K, draft, B, D, V, temperature, u, u_next, n_acc, next_token,
                                     workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 

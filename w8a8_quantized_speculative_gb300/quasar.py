@@ -57,6 +57,7 @@ _SIGS = {
     "quasar_pack_lm_head": (_i, [_p, _i, _i, _i, _p, _p]),
     "quasar_lm_head_verify": (_i, [_p, _i, _p, _i, _p, _i, _i, _i, _f, _p, _p, _p, _p, _sz, _p]),
     "quasar_lm_head_logits": (_i, [_p, _i, _p, _i, _i, _i, _p, ctypes.c_longlong, _p]),
+    "quasar_lm_head_verify_sample": (_i, [_p, _i, _p, _i, _p, _i, _i, _i, _f, _p, _p, _p, _p, _p, _sz, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -412,6 +413,34 @@ def lm_head_verify(h: torch.Tensor, wp: PackedLmHead, draft: torch.Tensor, tempe
     _check(lib.quasar_lm_head_verify(_ptr(h), ldh, _ptr(wp.buf), K, _ptr(draft), B, D, V, float(temperature),
                                      _ptr(u), _ptr(n_acc), _ptr(next_token), _ptr(buf), buf.numel(),
                                      _stream(stream)), "lm_head_verify")
+    return n_acc, next_token
+
+
+def lm_head_verify_sample(h: torch.Tensor, wp: PackedLmHead, draft: torch.Tensor, temperature: float, u, u_next,
+                          n_acc=None, next_token=None, workspace: Workspace | None = None, stream=None):
+    """T > 0: the BF16 lm_head and the acceptance test in one call, plus the
+    lossless next token (int32 [B]) drawn by inverse CDF on u_next [B], as
+    verify_sample draws it; the logits are never written."""
+    _need(h, torch.bfloat16, "h")
+    _need(draft, torch.int32, "draft")
+    _need(u_next, torch.float32, "u_next")
+    ldh = _rowmajor(h, "h")
+    if draft.dim() != 2 or not draft.is_contiguous():
+        raise ValueError("draft must be a contiguous [B][D] tensor")
+    B, D = draft.shape
+    K = h.shape[1]
+    if h.shape[0] != B * (D + 1) or wp.K != K:
+        raise ValueError("h must be [B*(D+1)][K] with the packed weight's K")
+    if D > 0:
+        _need(u, torch.float32, "u")
+    n_acc = torch.empty(B, dtype=torch.int32, device=h.device) if n_acc is None else n_acc
+    next_token = torch.empty(B, dtype=torch.int32, device=h.device) if next_token is None else next_token
+    ws = _ws(workspace, h.device)
+    buf = ws.get(int(lib.quasar_lm_head_verify_workspace_size(B, D, wp.V)))
+    _check(lib.quasar_lm_head_verify_sample(_ptr(h), ldh, _ptr(wp.buf), K, _ptr(draft), B, D, wp.V,
+                                            float(temperature), _ptr(u), _ptr(u_next), _ptr(n_acc),
+                                            _ptr(next_token), _ptr(buf), buf.numel(), _stream(stream)),
+           "lm_head_verify_sample")
     return n_acc, next_token
 
 
