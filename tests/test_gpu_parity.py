@@ -120,10 +120,10 @@ def test_int8_gemm_bit_exact(M, N, K):
     check_ws_zero(ws)
 
 
-@pytest.mark.parametrize("K", [1024, 4096, 12288])
-def test_int8_gemm_adversarial_extremes(K):
+@pytest.mark.parametrize("M,K", [(24, 1024), (24, 4096), (24, 12288), (64, 4096), (40, 12288), (256, 4096)])
+def test_int8_gemm_adversarial_extremes(M, K):
     """All products at +-127^2: every fp32 accumulation run sits at its exactness limit."""
-    M, N = 24, 256
+    N = 256
     xq = np.full((M, K), 127, np.int8)
     xq[1::2] = -127
     xq[2, ::2] = -127
@@ -139,11 +139,12 @@ def test_int8_gemm_adversarial_extremes(K):
 # every token-tile width, ragged M / N / K and each schedule: one cluster per
 # unit (few units, cluster sizes 2-8), split units stream-K only (<= 303
 # units), whole units only (304 units), and split-then-whole (384 units).
-# Larger M checks the tcgen05 kernel.
+# Larger M (25 .. 64 here) checks the tcgen05 kernel at the same shapes.
 SKINNY_SHAPES = [(1, 8, 16), (2, 1000, 4112), (7, 136, 1040), (9, 512, 256), (16, 4096, 4096),
                  (3, 12288, 256), (5, 19456, 512), (12, 24576, 1024), (20, 6144, 4096),
                  (23, 264, 2064), (24, 6144, 4096), (28, 6144, 4096), (32, 24576, 1024),
-                 (31, 8, 12288), (32, 1152, 2048)]
+                 (31, 8, 12288), (32, 1152, 2048), (33, 136, 1040), (40, 6144, 4096), (48, 9728, 1024),
+                 (56, 12288, 2048), (57, 264, 2064), (64, 1000, 4112), (64, 4096, 12288), (64, 8, 16)]
 
 
 @pytest.mark.parametrize("M,N,K", SKINNY_SHAPES)
