@@ -132,7 +132,8 @@ def test_pack_layout(V, K):
 
 # ------------------------------------------------------------- logits
 
-@pytest.mark.parametrize("M,V,K", [(1, 1000, 200), (20, 1000, 200), (32, 2048, 64), (256, 20000, 128),
+@pytest.mark.parametrize("M,V,K", [(1, 1, 8), (3, 5, 8), (17, 130, 16), (1, 1000, 200), (20, 1000, 200),
+                                   (32, 2048, 64), (256, 20000, 128),
                                    (257, 40000, 256), (300, 40000, 512), (512, 40000, 256)])
 def test_logits_grid_bit_exact(M, V, K):
     h = synth.grid_hidden_states(601 + M, M, K)
@@ -182,7 +183,8 @@ def test_logits_strided_rows_and_empty():
 
 # ------------------------------------------------------------- fused verification, exact grid
 
-@pytest.mark.parametrize("B,D,V,K", [(3, 5, 40000, 512), (4, 0, 5000, 128), (1, 7, 1000, 200),
+@pytest.mark.parametrize("B,D,V,K", [(3, 5, 40000, 512), (4, 0, 5000, 128), (1, 7, 1000, 200), (2, 2, 5, 8),
+                                     (1, 0, 1, 8),
                                      (51, 9, 40000, 256), (32, 8, VOCAB, HID)])
 def test_fused_greedy_grid_matches_oracle(B, D, V, K):
     h = synth.grid_hidden_states(631 + B, B * (D + 1), K)
