@@ -14,8 +14,10 @@ an end-to-end number through the public API with host buffers, SM clocks
 sampled during the timed region, the CPU oracle as a baseline, an M sweep
 over the four decoder-layer linears with a BF16 cuBLAS GEMM of the same shape
 as a bandwidth reference, the same linears with 4-bit weights (W4A8) at
-M = 1, 8, 20, and the verification kernel at B=32, D=8,
-V=151936.
+M = 1, 8, 20, the verification kernel at B=32, D=8,
+V=151936, the fused BF16 lm_head + verification at the same B, D, V, and the
+whole verification step of four decoder layers' W8A8 linears plus the lm_head
+at 288 token rows against the same chain on BF16 cuBLAS.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch with torch.distributed.run; each rank runs an independent
@@ -461,6 +463,7 @@ def main_gpu(args):
         extra["sweep_w4a8"] = run_sweep_w4(q, dev, stream, ws, hbm)
         extra["verify"] = run_verify(q, dev, stream, ws, hbm)
         extra["lm_head"] = run_lm_head(q, dev, stream, bf16)
+        extra["verification_step"] = run_verification_step(q, dev, stream, bf16)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -649,6 +652,70 @@ def run_lm_head(q, dev, stream, bf16_peak):
     return out
 
 
+def run_verification_step(q, dev, stream, bf16_peak):
+    """Verification step of 32 sequences x (8 drafts + 1) = 288 token rows:
+    four Qwen3-8B decoder layers' W8A8 linears (qkv, o, gate_up, down; each
+    one call of the fused smooth + quantize + linear entry) and the BF16
+    lm_head with fused greedy verification, against the same chain on BF16
+    cuBLAS (torch.matmul for every linear and the lm_head) followed by the
+    verification kernel.  The glue between the linears (RMSNorm, attention,
+    SiLU * up) is not on this path and is left out of both sides: every
+    linear reads its own synthetic activations.  Cold L2 by construction
+    (0.77 GB of INT8 and 1.54 GB of BF16 layer weights, 1.24 GB of lm_head)."""
+    import torch
+    B, D, V, H = 32, 8, synth.VOCAB, synth.HIDDEN
+    M = B * (D + 1)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    layers = []
+    for _ in range(4):
+        lay = []
+        for name in ("qkv", "o", "gate_up", "down"):
+            K, N = synth.LINEARS[name]
+            wq = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev, generator=gen)
+            lay.append({"K": K, "N": N, "wp": q.tile_weights(wq), "sw": torch.rand(N, device=dev, generator=gen) * 1e-3,
+                        "smooth": torch.rand(K, device=dev, generator=gen) + 0.5,
+                        "x": torch.randn((M, K), device=dev, generator=gen).to(torch.bfloat16),
+                        "y": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                        "wb": (torch.randn((N, K), device=dev, generator=gen) * 0.02).to(torch.bfloat16)})
+            del wq
+        layers.append(lay)
+    h = torch.randn((M, H), device=dev, generator=gen).to(torch.bfloat16)
+    w = (torch.randn((V, H), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+    wp = q.pack_lm_head(w)
+    draft = torch.randint(0, V, (B, D), dtype=torch.int32, device=dev, generator=gen)
+    lg = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
+    n_acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    ws_l, ws_h, ws_v = q.Workspace(dev), q.Workspace(dev), q.Workspace(dev)
+    ws_l.get(max(q.lib.quasar_w8a8_linear_fused_workspace_size(M, l["N"], l["K"]) for l in layers[0]))
+    ws_h.get(q.lib.quasar_lm_head_verify_workspace_size(B, D, V))
+    ws_v.get(q.lib.quasar_verify_accept_workspace_size(B, D, V))
+
+    def ours(i):
+        for lay in layers:
+            for l in lay:
+                q.w8a8_linear_fused(l["x"], l["smooth"], l["wp"], l["sw"], y=l["y"], workspace=ws_l)
+        q.lm_head_verify(h, wp, draft, 0.0, n_acc=n_acc, next_token=nxt, workspace=ws_h)
+
+    def bf16(i):
+        for lay in layers:
+            for l in lay:
+                torch.matmul(l["x"], l["wb"].t(), out=l["y"])
+        torch.matmul(h, w.t(), out=lg)
+        q.verify_accept(lg.view(B, D + 1, V), draft, n_acc=n_acc, next_token=nxt, workspace=ws_v)
+
+    us = _time_graph(torch, stream, ours, 3)
+    us_bf = _time_graph(torch, stream, bf16, 3)
+    lin_bytes = sum(l["N"] * l["K"] + 4 * l["N"] for lay in layers for l in lay)
+    out = {"B": B, "D": D, "token_rows": M, "layers": 4, "us": round(us, 1), "bf16_cublas_us": round(us_bf, 1),
+           "speedup_vs_bf16": round(us_bf / us, 3), "int8_weight_bytes": lin_bytes, "lm_head_bf16_bytes": V * H * 2,
+           "note": "glue (RMSNorm, attention, SiLU*up) left out of both sides"}
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -659,11 +726,20 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lm-head-only", action="store_true",
                     help="run only the fused lm_head + verification sub-benchmark (profiling)")
+    ap.add_argument("--verification-step-only", action="store_true",
+                    help="run only the 4-layer verification-step sub-benchmark")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.verification_step_only:
+        import torch
+        from w8a8_quantized_speculative_gb300 import quasar as q
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"verification_step": run_verification_step(q, dev, torch.cuda.Stream(dev),
+                                                                     load_peaks()[1])}), flush=True)
     elif args.lm_head_only:
         import torch
         from w8a8_quantized_speculative_gb300 import quasar as q
