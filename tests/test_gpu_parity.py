@@ -106,6 +106,7 @@ def test_pack_and_tile_ragged(N, K):
 SHAPES = [
     (1, 8, 16), (5, 136, 144), (8, 512, 256), (16, 128, 1024), (17, 264, 1040), (20, 384, 4096),
     (33, 256, 2048), (64, 640, 1152), (65, 128, 384), (128, 256, 512), (130, 136, 272), (256, 512, 1024),
+    (192, 1000, 2064), (288, 640, 4096), (200, 136, 272),   # 96-token tiles
 ]
 
 
@@ -120,7 +121,8 @@ def test_int8_gemm_bit_exact(M, N, K):
     check_ws_zero(ws)
 
 
-@pytest.mark.parametrize("M,K", [(24, 1024), (24, 4096), (24, 12288), (64, 4096), (40, 12288), (256, 4096)])
+@pytest.mark.parametrize("M,K", [(24, 1024), (24, 4096), (24, 12288), (64, 4096), (40, 12288), (256, 4096),
+                                 (288, 12288)])
 def test_int8_gemm_adversarial_extremes(M, K):
     """All products at +-127^2: every fp32 accumulation run sits at its exactness limit."""
     N = 256
@@ -235,7 +237,7 @@ def test_qwen3_shaped_linears(maker):
     check_ws_zero(ws)
 
 
-@pytest.mark.parametrize("M", [1, 64, 256])
+@pytest.mark.parametrize("M", [1, 64, 256, 288])
 def test_sweep_linear_sampled(M):
     """Full-size qkv / gate_up at sweep sizes, the launch configuration the
     benchmark times; every output compared (the oracle is a BLAS matmul)."""

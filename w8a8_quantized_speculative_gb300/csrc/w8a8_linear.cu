@@ -75,9 +75,9 @@ constexpr int BLOCK_BYTES = BM * BK;   // one packed weight block
 template <int NT>
 struct Cfg {
   // Blocks per pipeline stage: two 128-K blocks per handshake halve the
-  // per-byte cost of the barrier round trips; NT = 128 keeps one (TMEM).
-  static constexpr int G = (NT == 128) ? 1 : 2;
-  static constexpr int S2 = (NT == 128) ? 3 : (NT == 64) ? 2 : 3;   // converted stages (TMEM A + smem B)
+  // per-byte cost of the barrier round trips; NT >= 96 keeps one (TMEM).
+  static constexpr int G = (NT >= 96) ? 1 : 2;
+  static constexpr int S2 = (NT >= 96) ? 3 : (NT == 64) ? 2 : 3;    // converted stages (TMEM A + smem B)
   static constexpr int W_BYTES = G * BLOCK_BYTES;            // INT8 weight blocks of a stage
   static constexpr int XB_BYTES = NT * BK;                   // INT8 token tile of one block
   static constexpr int STAGE1 = W_BYTES + G * XB_BYTES;      // multiple of 1024
@@ -539,7 +539,16 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
 // ------------------------------------------------------------------ host side
 
-static int pick_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+// Token tile: the smallest of 16 / 32 / 64 that holds M, else 128 -- or 96
+// above 128 tokens when three-quarter tiles pad less (288 = 3 x 96 instead of
+// 2 x 128 + a quarter-full third tile).
+static int pick_nt(int M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M > 128 && 96 * ((M + 95) / 96) < 128 * ((M + 127) / 128)) return 96;
+  return 128;
+}
 
 struct Shape {
   int NT, m_tiles, n_tiles, tiles, KB;
@@ -643,6 +652,7 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
     case 16: e = launch_nt<16>(tx, p, grid, stream); break;
     case 32: e = launch_nt<32>(tx, p, grid, stream); break;
     case 64: e = launch_nt<64>(tx, p, grid, stream); break;
+    case 96: e = launch_nt<96>(tx, p, grid, stream); break;
     default: e = launch_nt<128>(tx, p, grid, stream); break;
   }
   return cuda_status(e);
