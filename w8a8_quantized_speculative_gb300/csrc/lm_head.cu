@@ -711,9 +711,16 @@ size_t verify_workspace_size(int B, int D, int V) {
 template <int MODE>
 static cudaError_t launch_main(const CUtensorMap& th, const Params& p, int grid, cudaStream_t stream) {
   const uint32_t smem = smem_bytes(p.Tp, p.stages);
-  cudaError_t e = cudaFuncSetAttribute(lm_head_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_LIMIT);
+  static int configured[64] = {0};  // per device: the opt-in shared-memory size is set once
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(lm_head_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
