@@ -83,7 +83,10 @@ struct Cfg {
   static constexpr int STAGE1 = W_BYTES + G * XB_BYTES;      // multiple of 1024
   static constexpr int B16_BLOCK = NT * BK * 2;              // fp16 token tile of one block (2 atoms)
   static constexpr int B16_BYTES = G * B16_BLOCK;
-  static constexpr int S1 = (NT == 16) ? 5 : (NT == 32) ? 4 : 3;  // INT8 stages
+  // INT8 stages: as many as the shared memory holds next to the converted
+  // stages (the pipeline is bound by copies in flight), at most 5.
+  static constexpr int S1_FIT = (232448 - 1024 - 256 - S2 * G * NT * BK * 2) / (G * (BM * BK + NT * BK));
+  static constexpr int S1 = (NT == 16) ? 5 : (NT == 32) ? 4 : (NT == 64) ? 3 : (S1_FIT < 5 ? S1_FIT : 5);
   static constexpr int A_COLS = G * BK / 2;                  // TMEM columns per A stage (fp16 pairs)
   static constexpr int TMEM_A0 = 2 * NT;                     // A stages follow two accumulators
   static constexpr int TOK = NT / 4;                         // accumulator columns per converter thread
