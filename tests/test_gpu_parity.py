@@ -107,6 +107,7 @@ SHAPES = [
     (1, 8, 16), (5, 136, 144), (8, 512, 256), (16, 128, 1024), (17, 264, 1040), (20, 384, 4096),
     (33, 256, 2048), (64, 640, 1152), (65, 128, 384), (128, 256, 512), (130, 136, 272), (256, 512, 1024),
     (192, 1000, 2064), (288, 640, 4096), (200, 136, 272),   # 96-token tiles
+    (130, 16384, 1040), (256, 16392, 256),                  # tokens pre-widened to fp16 (>= 128 weight tiles)
 ]
 
 
@@ -121,11 +122,11 @@ def test_int8_gemm_bit_exact(M, N, K):
     check_ws_zero(ws)
 
 
-@pytest.mark.parametrize("M,K", [(24, 1024), (24, 4096), (24, 12288), (64, 4096), (40, 12288), (256, 4096),
-                                 (288, 12288)])
-def test_int8_gemm_adversarial_extremes(M, K):
-    """All products at +-127^2: every fp32 accumulation run sits at its exactness limit."""
-    N = 256
+@pytest.mark.parametrize("M,K,N", [(24, 1024, 256), (24, 4096, 256), (24, 12288, 256), (64, 4096, 256),
+                                   (40, 12288, 256), (256, 4096, 256), (288, 12288, 256), (288, 4096, 16384)])
+def test_int8_gemm_adversarial_extremes(M, K, N):
+    """All products at +-127^2: every fp32 accumulation run sits at its exactness limit
+    (N = 16384: the path that takes the tokens pre-widened to fp16)."""
     xq = np.full((M, K), 127, np.int8)
     xq[1::2] = -127
     xq[2, ::2] = -127

@@ -72,21 +72,26 @@ constexpr int MMA_BAR_ID = 1;   // named barrier pairing the MMA and waiter warp
 constexpr int TMEM_COLS = 512;
 constexpr int BLOCK_BYTES = BM * BK;   // one packed weight block
 
-template <int NT>
+// XH: the token codes arrive already widened to fp16 (one copy per call in
+// the workspace) and are copied by TMA straight into the MMA's B layout;
+// the converters then widen only the weights, and the INT8 ring carries
+// weight blocks alone.
+template <int NT, bool XH = false>
 struct Cfg {
   // Blocks per pipeline stage: two 128-K blocks per handshake halve the
   // per-byte cost of the barrier round trips; NT >= 96 keeps one (TMEM).
   static constexpr int G = (NT >= 96) ? 1 : 2;
   static constexpr int S2 = (NT >= 96) ? 3 : (NT == 64) ? 2 : 3;    // converted stages (TMEM A + smem B)
   static constexpr int W_BYTES = G * BLOCK_BYTES;            // INT8 weight blocks of a stage
-  static constexpr int XB_BYTES = NT * BK;                   // INT8 token tile of one block
+  static constexpr int XB_BYTES = XH ? 0 : NT * BK;          // INT8 token tile of one block
   static constexpr int STAGE1 = W_BYTES + G * XB_BYTES;      // multiple of 1024
   static constexpr int B16_BLOCK = NT * BK * 2;              // fp16 token tile of one block (2 atoms)
   static constexpr int B16_BYTES = G * B16_BLOCK;
   // INT8 stages: as many as the shared memory holds next to the converted
   // stages (the pipeline is bound by copies in flight), at most 5.
-  static constexpr int S1_FIT = (232448 - 1024 - 256 - S2 * G * NT * BK * 2) / (G * (BM * BK + NT * BK));
-  static constexpr int S1 = (NT == 16) ? 5 : (NT == 32) ? 4 : (NT == 64) ? 3 : (S1_FIT < 5 ? S1_FIT : 5);
+  static constexpr int S1_FIT = (232448 - 1024 - 256 - S2 * G * NT * BK * 2) / (G * (BM * BK + XB_BYTES));
+  static constexpr int S1 = XH ? (S1_FIT < 8 ? S1_FIT : 8)
+                               : (NT == 16) ? 5 : (NT == 32) ? 4 : (NT == 64) ? 3 : (S1_FIT < 5 ? S1_FIT : 5);
   static constexpr int A_COLS = G * BK / 2;                  // TMEM columns per A stage (fp16 pairs)
   static constexpr int TMEM_A0 = 2 * NT;                     // A stages follow two accumulators
   static constexpr int TOK = NT / 4;                         // accumulator columns per converter thread
@@ -297,10 +302,10 @@ QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4
   return true;
 }
 
-template <int NT>
+template <int NT, bool XH = false>
 __global__ void __launch_bounds__(THREADS, 1)
 w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
-  using C = Cfg<NT>;
+  using C = Cfg<NT, XH>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage1 = smem;                                  // S1 x [W 16KB | X NT*128]
@@ -323,7 +328,8 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::S1; ++s) { mbar_init(&full1[s], 1); mbar_init(&empty1[s], CONV_WARPS); }
-    for (int s = 0; s < C::S2; ++s) { mbar_init(&full2[s], CONV_WARPS); mbar_init(&empty2[s], 1); }
+    // XH: the producer's fp16 token copy is one more arrival (with its bytes)
+    for (int s = 0; s < C::S2; ++s) { mbar_init(&full2[s], CONV_WARPS + (XH ? 1 : 0)); mbar_init(&empty2[s], 1); }
     for (int a = 0; a < 2; ++a) mbar_init(&accempty[a], CONV_WARPS);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -334,6 +340,7 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     tmem_relinquish();
   }
   if (warp == PRODUCER_WARP && lane == 0) prefetch_tmap(&tmX);
+  const uint32_t xtx = XH ? (uint32_t)C::B16_BLOCK : 0u;  // bytes of one block's fp16 token tile
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -373,9 +380,10 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
           bulk_load(st, p.wp + ((size_t)(w.t / m_tiles) * KB + w.kb) * BLOCK_BYTES, (uint32_t)(w.g * BLOCK_BYTES),
                     &full1[rg.s], pol_w);
         }
-        for (int b = 0; b < w.g; ++b)
-          tma_load_2d(st + C::W_BYTES + b * C::XB_BYTES, &tmX, (w.kb + b) * BK, (w.t % m_tiles) * NT, &full1[rg.s],
-                      pol_x);
+        if (!XH)
+          for (int b = 0; b < w.g; ++b)
+            tma_load_2d(st + C::W_BYTES + b * C::XB_BYTES, &tmX, (w.kb + b) * BK, (w.t % m_tiles) * NT, &full1[rg.s],
+                        pol_x);
       }
       // Never leave with copies in flight: wait for the last phase issued on
       // every stage (already complete in a normal run).
@@ -383,6 +391,31 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         const int last = s + ((issued - 1 - s) / C::S1) * C::S1;
         volatile int dummy = 0;
         mbar_wait(&full1[s], (uint32_t)(last / C::S1) & 1u, &dummy, p.err, SITE_GEMM_DRAIN, p.limit_ns);
+      }
+    } else if (XH && lane == 1) {
+      // fp16 token tiles, straight into the converted ring's B slots (two
+      // 64-column swizzle atoms per block), once the MMAs have released them.
+      const uint64_t pol_x = policy_evict_last();
+      pdl_wait();  // the widened tokens are written by the previous kernel
+      Walk<C::G> w(b0, b1, KB);
+      Ring<C::S2> r2;
+      int issued = 0;
+      for (int j = 0; w.more(); ++j, w.next(KB), r2.next(), ++issued) {
+        if (j >= C::S2 && !mbar_wait(&empty2[r2.s], r2.ph ^ 1u, abort_flag, p.err, SITE_GEMM_EMPTY2, p.limit_ns))
+          break;
+        mbar_arrive_expect_tx(&full2[r2.s], (uint32_t)w.g * xtx);
+        uint8_t* bd = b16 + r2.s * C::B16_BYTES;
+        for (int b = 0; b < w.g; ++b)
+          for (int a = 0; a < 2; ++a)
+            tma_load_2d(bd + b * C::B16_BLOCK + a * (NT * 128), &tmX, (w.kb + b) * BK + a * 64, (w.t % m_tiles) * NT,
+                        &full2[r2.s], pol_x);
+      }
+      // The MMA warp consumes every phase issued here in a normal run; after
+      // an abort, wait (bounded) for the copies of the last phases to land.
+      for (int s = 0; s < C::S2 && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / C::S2) * C::S2;
+        volatile int dummy = 0;
+        mbar_wait(&full2[s], (uint32_t)(last / C::S2) & 1u, &dummy, p.err, SITE_GEMM_DRAIN, p.limit_ns);
       }
     }
   } else if (warp == MMA_WARP || warp == WAITER_WARP) {
@@ -482,8 +515,8 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         tmem_st16(tmem + lane_off + (uint32_t)(C::TMEM_A0 + r2.s * C::A_COLS + b * (BK / 2) + 16 * h), a);
       }
       // B: the token tiles, NT rows x 8 chunks per block, widened into the
-      // swizzled fp16 tiles.
-      {
+      // swizzled fp16 tiles (XH: the producer copies them in already widened).
+      if (!XH) {
         uint8_t* bd = b16 + r2.s * C::B16_BYTES;
         for (int idx = ct; idx < w.g * NT * 8; idx += CONV_WARPS * 32) {
           const int b = idx / (NT * 8), rem = idx - b * (NT * 8);
@@ -569,37 +602,65 @@ static Shape shape_of(int M, int N, int K) {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Token tiles of 96 or 128 on layers of at least 128 weight tiles (N >= 16384):
+// the tokens are widened to fp16 once per call (an M x K copy in the
+// workspace, one extra launch and a clearing memset) instead of once per
+// weight tile inside the kernel.  Measured: gate_up 24576 x 4096 at M = 256
+// 95.5 -> 85.3 us; the widening launch costs more than it saves on layers of
+// 32-48 tiles (qkv, o_proj, down lose 0.5-2.5 us), so those keep the in-kernel path.
+static bool use_xh(int M, const Shape& s) { return !skinny::handles(M) && s.NT >= 96 && s.n_tiles >= 128; }
+
 size_t workspace_size(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   Shape s = shape_of(M, N, K);
   // counters, then the int32 split-K sums of this kernel or the partial-sum
-  // slots of the register-path kernel
+  // slots of the register-path kernel, then (96/128-token tiles) the fp16
+  // token copy
   return align256((size_t)s.tiles * CONV_WARPS * 4) +
-         align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K)));
+         align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K))) +
+         (use_xh(M, s) ? align256((size_t)M * K * 2) : 0);
 }
 
-template <int NT>
+// INT8 token codes -> the same values in fp16 (exact), 16 codes per thread.
+__global__ void __launch_bounds__(256) widen_tokens_kernel(const int8_t* __restrict__ xq, long long n16,
+                                                           uint4* __restrict__ xh) {
+  pdl_launch_dependents();
+  pdl_wait();  // the codes are written by the previous kernel
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(xq)[i];
+    uint4 o0, o1;
+    s8x4_to_f16x4(v.x, o0.x, o0.y);
+    s8x4_to_f16x4(v.y, o0.z, o0.w);
+    s8x4_to_f16x4(v.z, o1.x, o1.y);
+    s8x4_to_f16x4(v.w, o1.z, o1.w);
+    xh[2 * i] = o0;
+    xh[2 * i + 1] = o1;
+  }
+}
+
+template <int NT, bool XH = false>
 static cudaError_t launch_nt(const CUtensorMap& tx, const Params& p, int grid, cudaStream_t stream) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(w8a8_linear_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<NT>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(w8a8_linear_kernel<NT, XH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<NT, XH>::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = Cfg<NT>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<NT, XH>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_linear_kernel<NT>, tx, p);
+  return cudaLaunchKernelEx(&cfg, w8a8_linear_kernel<NT, XH>, tx, p);
 }
 
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
@@ -624,8 +685,18 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
     return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream, false);
 
 
+  const bool xh_path = use_xh(M, s);
+  uint4* xh = xh_path ? reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws) +
+                                                 align256((size_t)s.tiles * CONV_WARPS * 4) +
+                                                 align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K))))
+                      : nullptr;
   CUtensorMap tx;
-  if (!encode_2d_u8(&tx, Xq, K, M, BK, s.NT)) return QUASAR_ERR_CUDA;
+  if (xh_path) {
+    // fp16 copy [M][K]: boxes of 64 values (one 128-byte swizzle row) x NT rows
+    if (!encode_2d_bf16(&tx, xh, K, M, K, 64, s.NT)) return QUASAR_ERR_CUDA;
+  } else if (!encode_2d_u8(&tx, Xq, K, M, BK, s.NT)) {
+    return QUASAR_ERR_CUDA;
+  }
 
   Params p;
   p.wp = reinterpret_cast<const uint8_t*>(Wp);
@@ -651,6 +722,24 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   if (sms <= 0) return QUASAR_ERR_CUDA;
   const int grid = std::min(p.total, sms);
   cudaError_t e;
+  if (xh_path) {
+    const long long n16 = (long long)M * K / 16;
+    cudaLaunchConfig_t wc = {};
+    wc.gridDim = dim3((unsigned)std::min<long long>((n16 + 255) / 256, (long long)sms * 4));
+    wc.blockDim = dim3(256);
+    wc.stream = stream;
+    cudaLaunchAttribute wa[1];
+    wa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    wa[0].val.programmaticStreamSerializationAllowed = 1;
+    wc.attrs = wa;
+    wc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&wc, widen_tokens_kernel, Xq, n16, xh);
+    if (e == cudaSuccess)
+      e = (s.NT == 96) ? launch_nt<96, true>(tx, p, grid, stream) : launch_nt<128, true>(tx, p, grid, stream);
+    // leave the workspace zero-filled (the fp16 copy is scratch of this call)
+    if (e == cudaSuccess) e = cudaMemsetAsync(xh, 0, (size_t)M * K * 2, stream);
+    return cuda_status(e);
+  }
   switch (s.NT) {
     case 16: e = launch_nt<16>(tx, p, grid, stream); break;
     case 32: e = launch_nt<32>(tx, p, grid, stream); break;
