@@ -392,7 +392,10 @@ def test_fused_qwen3_shapes(maker, M):
 @pytest.mark.parametrize("M,N,K,pad", [(1, 4096, 4096, 0), (24, 6144, 4096, 0), (13, 1024, 1040, 8),
                                        (5, 136, 272, 0), (9, 2048, 2048, 64), (3, 2048, 2064, 24),
                                        (8, 6144, 4096, 0), (7, 512, 16, 0), (2, 12288, 4096, 0),
-                                       (2, 1024, 1040, 8), (1, 4096, 12288, 0), (2, 136, 2064, 0)])
+                                       (2, 1024, 1040, 8), (1, 4096, 12288, 0), (2, 136, 2064, 0),
+                                       # 96/128-token tiles: the quantizer's fp16 codes feed the linear
+                                       (130, 1024, 1040, 8), (288, 6144, 4096, 0), (256, 4096, 12288, 16),
+                                       (97, 136, 16, 0), (288, 1000, 16384, 0)])
 def test_fused_random_shapes(M, N, K, pad):
     rng = np.random.default_rng(M * 31 + N + K)
     x = synth.f32_to_bf16_bits(rng.standard_normal((M, K)) * (1 + 20 * (rng.random(K) < 0.01)))
@@ -401,7 +404,7 @@ def test_fused_random_shapes(M, N, K, pad):
     _fused_vs_two_step(x, w, smooth, ldx_pad=pad)
 
 
-@pytest.mark.parametrize("M", [2, 12])
+@pytest.mark.parametrize("M", [2, 12, 200])
 def test_fused_zero_token_rows(M):
     """A token whose smoothed row is all zero gets absmax 0: scale 0, codes 0, Y row 0."""
     rng = np.random.default_rng(11)

@@ -125,10 +125,14 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const uint16_t* __r
 // weight stream already fills the memory system, and each dependent round
 // trip then waits behind it.  Same arithmetic as quant_rows_kernel<false,
 // false>.
+//
+// `xh` (optional): the same codes as fp16 [rows][K] (exact), for a linear that
+// takes its token operand already widened.
 template <int VPT>
 __global__ void __launch_bounds__(THREADS) quant_act_kernel(const uint16_t* __restrict__ in, int ld,
                                                             const float* __restrict__ smooth, int K,
-                                                            int8_t* __restrict__ q, float* __restrict__ scale) {
+                                                            int8_t* __restrict__ q, float* __restrict__ scale,
+                                                            uint4* __restrict__ xh) {
   pdl_launch_dependents();
   pdl_wait();
   const int row = blockIdx.x;
@@ -184,6 +188,12 @@ __global__ void __launch_bounds__(THREADS) quant_act_kernel(const uint16_t* __re
       }
     }
     reinterpret_cast<uint2*>(dst)[v] = make_uint2(packed[0], packed[1]);
+    if (xh) {
+      uint4 h;
+      s8x4_to_f16x4(packed[0], h.x, h.y);
+      s8x4_to_f16x4(packed[1], h.z, h.w);
+      xh[(size_t)row * nvec + v] = h;
+    }
   }
 }
 
@@ -281,7 +291,7 @@ size_t packed_bytes(int N, int K) {
 
 template <bool DIVIDE, bool PACKED>
 static quasar_status_t run(const void* in, int ld, const float* smooth, int rows, int K, int8_t* q, float* scale,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, void* xh = nullptr) {
   if (rows < 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
   if (K % 16 != 0 || ld < K || ld % 8 != 0) return QUASAR_ERR_UNSUPPORTED;
   if (rows == 0) return QUASAR_OK;  // empty batch: nothing is read or written
@@ -308,9 +318,23 @@ static quasar_status_t run(const void* in, int ld, const float* smooth, int rows
   cfg.numAttrs = 1;
   const uint16_t* x = reinterpret_cast<const uint16_t*>(in);
   const int vpt = (K / 8 + THREADS - 1) / THREADS;   // 8-value vectors per thread
-  if (!DIVIDE && vpt <= 2) return cuda_status(cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, x, ld, smooth, K, q, scale));
-  if (!DIVIDE && vpt <= 6) return cuda_status(cudaLaunchKernelEx(&cfg, quant_act_kernel<6>, x, ld, smooth, K, q, scale));
+  uint4* xh4 = reinterpret_cast<uint4*>(xh);
+  if (!DIVIDE && vpt <= 2)
+    return cuda_status(cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, x, ld, smooth, K, q, scale, xh4));
+  if (!DIVIDE && vpt <= 6)
+    return cuda_status(cudaLaunchKernelEx(&cfg, quant_act_kernel<6>, x, ld, smooth, K, q, scale, xh4));
+  if (xh) return QUASAR_ERR_UNSUPPORTED;  // rows too long for the one-pass kernel: no fp16 copy
   return cuda_status(cudaLaunchKernelEx(&cfg, quant_rows_kernel<DIVIDE, PACKED>, x, ld, smooth, K, q, scale));
+}
+
+// Smooth + quantize (quasar_smooth_quant_act) and also write the codes as
+// fp16 into `xh` [M][K]; QUASAR_ERR_UNSUPPORTED (nothing launched) when K is
+// beyond the one-pass kernel's rows.
+quasar_status_t smooth_quant_act_f16(const void* X_bf16, int ldx, const float* smooth, int M, int K, int8_t* Xq,
+                                     float* sa, void* xh, cudaStream_t stream) {
+  if (!xh || !aligned(xh, 16)) return QUASAR_ERR_INVALID_ARG;
+  if ((K / 8 + THREADS - 1) / THREADS > 6) return QUASAR_ERR_UNSUPPORTED;
+  return run<false, false>(X_bf16, ldx, smooth, M, K, Xq, sa, stream, xh);
 }
 
 }  // namespace quant

@@ -58,6 +58,11 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
                     bool w4);
 }  // namespace skinny
 
+namespace quant {
+quasar_status_t smooth_quant_act_f16(const void* X_bf16, int ldx, const float* smooth, int M, int K, int8_t* Xq,
+                                     float* sa, void* xh, cudaStream_t stream);
+}  // namespace quant
+
 namespace gemm {
 
 constexpr int BM = 128;        // weight rows per tile (MMA M)
@@ -663,8 +668,11 @@ static cudaError_t launch_nt(const CUtensorMap& tx, const Params& p, int grid, c
   return cudaLaunchKernelEx(&cfg, w8a8_linear_kernel<NT, XH>, tx, p);
 }
 
+// `xh_ext` (optional, the one-call entry): the token codes already widened to
+// fp16 [M][K] by the quantizer; 96/128-token tiles then take them from there.
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
-                    void* Y, int ldy, int32_t* acc_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                    void* Y, int ldy, int32_t* acc_out, void* ws, size_t ws_bytes, cudaStream_t stream,
+                    const void* xh_ext = nullptr) {
   if (M < 0 || N <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
   if (K % 16 != 0 || N % 8 != 0 || K > 131072) return QUASAR_ERR_UNSUPPORTED;
   if (!acc_out && (ldy < N || ldy % 8 != 0)) return QUASAR_ERR_UNSUPPORTED;
@@ -685,11 +693,13 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
     return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream, false);
 
 
-  const bool xh_path = use_xh(M, s);
-  uint4* xh = xh_path ? reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws) +
-                                                 align256((size_t)s.tiles * CONV_WARPS * 4) +
-                                                 align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K))))
-                      : nullptr;
+  const bool ext = xh_ext != nullptr && s.NT >= 96;
+  const bool xh_path = ext || use_xh(M, s);
+  uint4* xh = ext ? reinterpret_cast<uint4*>(const_cast<void*>(xh_ext))
+              : xh_path ? reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws) +
+                                                   align256((size_t)s.tiles * CONV_WARPS * 4) +
+                                                   align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K))))
+                        : nullptr;
   CUtensorMap tx;
   if (xh_path) {
     // fp16 copy [M][K]: boxes of 64 values (one 128-byte swizzle row) x NT rows
@@ -733,11 +743,11 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
     wa[0].val.programmaticStreamSerializationAllowed = 1;
     wc.attrs = wa;
     wc.numAttrs = 1;
-    e = cudaLaunchKernelEx(&wc, widen_tokens_kernel, Xq, n16, xh);
+    e = ext ? cudaSuccess : cudaLaunchKernelEx(&wc, widen_tokens_kernel, Xq, n16, xh);
     if (e == cudaSuccess)
       e = (s.NT == 96) ? launch_nt<96, true>(tx, p, grid, stream) : launch_nt<128, true>(tx, p, grid, stream);
-    // leave the workspace zero-filled (the fp16 copy is scratch of this call)
-    if (e == cudaSuccess) e = cudaMemsetAsync(xh, 0, (size_t)M * K * 2, stream);
+    // leave the workspace zero-filled (the internal fp16 copy is scratch of this call)
+    if (e == cudaSuccess && !ext) e = cudaMemsetAsync(xh, 0, (size_t)M * K * 2, stream);
     return cuda_status(e);
   }
   switch (s.NT) {
@@ -780,9 +790,14 @@ quasar_status_t run_w4(const int8_t* Xq, const float* sa, const int8_t* Wp4, con
 // reads them (two launches, the second overlapping the first through
 // programmatic dependent launch).
 
+// The linear's workspace, then the quantizer's codes and scales, then (96/128-
+// token tiles) the codes again as fp16 for the linear's token operand.
+static bool fused_xh(int M, int N, int K) { return !skinny::handles(M) && shape_of(M, N, K).NT >= 96; }
+
 size_t fused_workspace_size(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  return workspace_size(M, N, K) + align256((size_t)M * K) + align256((size_t)M * 4);
+  return workspace_size(M, N, K) + align256((size_t)M * K) + align256((size_t)M * 4) +
+         (fused_xh(M, N, K) ? align256((size_t)M * K * 2) : 0);
 }
 
 quasar_status_t run_fused(const void* X, int ldx, const float* smooth, const int8_t* Wp, const float* sw, int M,
@@ -798,6 +813,14 @@ quasar_status_t run_fused(const void* X, int ldx, const float* smooth, const int
   if (!ws || ws_bytes < fused_workspace_size(M, N, K) || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
   int8_t* xq = reinterpret_cast<int8_t*>(ws) + lin;
   float* sa = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + lin + align256((size_t)M * K));
+  if (fused_xh(M, N, K)) {
+    // The quantizer also writes the codes as fp16: the linear's token
+    // operand without a widening launch (rows up to the one-pass kernel's).
+    void* xh = reinterpret_cast<uint8_t*>(ws) + lin + align256((size_t)M * K) + align256((size_t)M * 4);
+    const quasar_status_t sq = quant::smooth_quant_act_f16(X, ldx, smooth, M, K, xq, sa, xh, stream);
+    if (sq == QUASAR_OK) return run(xq, sa, Wp, sw, M, N, K, Y, ldy, nullptr, ws, lin, stream, xh);
+    if (sq != QUASAR_ERR_UNSUPPORTED) return sq;
+  }
   const quasar_status_t sq = quasar_smooth_quant_act(X, ldx, smooth, M, K, xq, sa, reinterpret_cast<quasar_stream_t>(stream));
   if (sq != QUASAR_OK) return sq;
   return run(xq, sa, Wp, sw, M, N, K, Y, ldy, nullptr, ws, lin, stream);
