@@ -232,7 +232,7 @@ quasar_status_t quasar_w4a8_linear(const int8_t* Xq, const float* sa,
  *   Y[m][n] is bit-identical to quasar_smooth_quant_act(X, smooth) followed by
  *   quasar_w8a8_linear on its outputs (same codes, same sa, same epilogue);
  *   it is those two launches, with the codes and scales kept in the
- *   workspace instead of caller buffers (above 64 tokens the quantizer also
+ *   workspace instead of caller buffers (above 32 tokens the quantizer also
  *   writes the codes as fp16 there, the linear's token operand).
  *   X [M][ldx] BF16 (ldx >= K, ldx % 8 == 0, 16-byte aligned), smooth [K]
  *   fp32 (16-byte aligned), Wp / sw / Y / sizes as for quasar_w8a8_linear.

@@ -393,8 +393,9 @@ def test_fused_qwen3_shapes(maker, M):
                                        (5, 136, 272, 0), (9, 2048, 2048, 64), (3, 2048, 2064, 24),
                                        (8, 6144, 4096, 0), (7, 512, 16, 0), (2, 12288, 4096, 0),
                                        (2, 1024, 1040, 8), (1, 4096, 12288, 0), (2, 136, 2064, 0),
-                                       # 96/128-token tiles: the quantizer's fp16 codes feed the linear
+                                       # 64- to 128-token tiles: the quantizer's fp16 codes feed the linear
                                        (130, 1024, 1040, 8), (288, 6144, 4096, 0), (256, 4096, 12288, 16),
+                                       (40, 24576, 4096, 0), (33, 136, 1040, 8), (64, 4096, 12288, 0),
                                        (97, 136, 16, 0), (288, 1000, 16384, 0)])
 def test_fused_random_shapes(M, N, K, pad):
     rng = np.random.default_rng(M * 31 + N + K)

@@ -669,7 +669,7 @@ static cudaError_t launch_nt(const CUtensorMap& tx, const Params& p, int grid, c
 }
 
 // `xh_ext` (optional, the one-call entry): the token codes already widened to
-// fp16 [M][K] by the quantizer; 96/128-token tiles then take them from there.
+// fp16 [M][K] by the quantizer; 64- to 128-token tiles then take them from there.
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
                     void* Y, int ldy, int32_t* acc_out, void* ws, size_t ws_bytes, cudaStream_t stream,
                     const void* xh_ext = nullptr) {
@@ -693,7 +693,7 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
     return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream, false);
 
 
-  const bool ext = xh_ext != nullptr && s.NT >= 96;
+  const bool ext = xh_ext != nullptr && s.NT >= 64;
   const bool xh_path = ext || use_xh(M, s);
   uint4* xh = ext ? reinterpret_cast<uint4*>(const_cast<void*>(xh_ext))
               : xh_path ? reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws) +
@@ -745,7 +745,9 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
     wc.numAttrs = 1;
     e = ext ? cudaSuccess : cudaLaunchKernelEx(&wc, widen_tokens_kernel, Xq, n16, xh);
     if (e == cudaSuccess)
-      e = (s.NT == 96) ? launch_nt<96, true>(tx, p, grid, stream) : launch_nt<128, true>(tx, p, grid, stream);
+      e = (s.NT == 64)   ? launch_nt<64, true>(tx, p, grid, stream)
+          : (s.NT == 96) ? launch_nt<96, true>(tx, p, grid, stream)
+                         : launch_nt<128, true>(tx, p, grid, stream);
     // leave the workspace zero-filled (the internal fp16 copy is scratch of this call)
     if (e == cudaSuccess && !ext) e = cudaMemsetAsync(xh, 0, (size_t)M * K * 2, stream);
     return cuda_status(e);
@@ -790,9 +792,9 @@ quasar_status_t run_w4(const int8_t* Xq, const float* sa, const int8_t* Wp4, con
 // reads them (two launches, the second overlapping the first through
 // programmatic dependent launch).
 
-// The linear's workspace, then the quantizer's codes and scales, then (96/128-
-// token tiles) the codes again as fp16 for the linear's token operand.
-static bool fused_xh(int M, int N, int K) { return !skinny::handles(M) && shape_of(M, N, K).NT >= 96; }
+// The linear's workspace, then the quantizer's codes and scales, then (64- to
+// 128-token tiles) the codes again as fp16 for the linear's token operand.
+static bool fused_xh(int M, int N, int K) { return !skinny::handles(M) && shape_of(M, N, K).NT >= 64; }
 
 size_t fused_workspace_size(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
