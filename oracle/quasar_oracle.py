@@ -54,6 +54,17 @@ The pages leave the numeric details open.  The readings taken here are:
       ahead of the high-precision acceptance test): logits = the exact
       product H·W^T of the BF16 inputs, rounded once to BF16 (nearest, ties
       to even); acceptance as R5/R6 on those logits.
+  R10 the MLP glue between gate_up and down (the pages dequantize to BF16
+      before the nonlinear layers; the block then re-smooths and
+      re-quantizes for down): h = bf16_rne(silu(g) * u) with g, u the BF16
+      gate and up halves of the gate_up output, silu(g) = g / (1 + exp(-g))
+      in fp32, one rounding to BF16 at the end.  So that the quantized codes
+      of h are a fixed function of the inputs, exp is a stated fp32
+      algorithm (Cody and Waite's reduction t = n*ln2 + r with ln2 split in
+      a 15-bit head and a tail, then the degree-7 Taylor polynomial of e^r
+      by Horner, times 2^n; each step one correctly rounded fp32 operation;
+      the argument clamped to [-87, 88]), within 2 fp32 ulp of the true
+      exponential.  Then h is smoothed and quantized as R2.
 
 Every function below is pinned by tests under ``tests/`` against hand-derived
 values, closed forms, invariants or brute force (see each docstring).
@@ -191,6 +202,71 @@ def smooth_quant_act(x_bits: np.ndarray, smooth: np.ndarray):
     x = bf16_to_f32(x_bits)
     xp = x * np.asarray(smooth, dtype=F32)[None, :]
     return quantize_rows(xp)
+
+
+# ---------------------------------------------------------------------------
+# The MLP glue before down: SiLU(gate) * up, then smooth + quantize (R10).
+
+def _f32_bits(b: int) -> np.float32:
+    return np.array([b], dtype=np.uint32).view(F32)[0]
+
+
+EXP_LOG2E = _f32_bits(0x3FB8AA3B)     # 1/ln2 rounded to fp32
+EXP_LN2_HI = _f32_bits(0x3F317200)    # ln2 to 15 significant bits: n * head is exact for |n| < 2^9
+EXP_LN2_LO = _f32_bits(0x35BFBE8E)    # ln2 - head, rounded to fp32
+# 1/k! rounded to fp32, k = 7 down to 2 (Taylor coefficients of e^r).
+EXP_TAYLOR = tuple(_f32_bits(b) for b in (0x39500D01, 0x3AB60B61, 0x3C088889, 0x3D2AAAAB, 0x3E2AAAAB, 0x3F000000))
+
+
+def exp_f32(t: np.ndarray) -> np.ndarray:
+    """The fp32 exponential of reading R10, for t in [-87, 88].
+
+    Cody and Waite, "Software Manual for the Elementary Functions" (1980):
+    n = rint(t / ln2), r = (t - n*ln2_head) - n*ln2_tail, then
+    e^r = 1 + r(1 + r(1/2! + ... + r/7!)) by Horner and the result p * 2^n,
+    every operation rounded to fp32 separately (numpy float32 arithmetic).
+    Pinned: within 2 fp32 ulp of the fp64 exponential on a dense grid of the
+    range, exactly 1 at 0, and the head/tail split and coefficients checked
+    against ln2 and 1/k!."""
+    t = np.asarray(t, dtype=F32)
+    n = np.rint(t * EXP_LOG2E).astype(F32)
+    r = (t - n * EXP_LN2_HI) - n * EXP_LN2_LO
+    p = np.full(t.shape, EXP_TAYLOR[0], dtype=F32)
+    for c in EXP_TAYLOR[1:] + (F32(1.0), F32(1.0)):
+        p = p * r + c
+    two_n = ((n.astype(np.int32) + 127).astype(np.uint32) << 23).view(F32)
+    return (p * two_n).astype(F32)
+
+
+def silu_f32(g: np.ndarray) -> np.ndarray:
+    """silu(g) = g / (1 + exp(-g)) in fp32 with exp_f32 (argument clamped to
+    [-87, 88]; beyond 87 the exponential is below 2^-125 and 1 + e = 1)."""
+    g = np.asarray(g, dtype=F32)
+    t = np.minimum(np.maximum(-g, F32(-87.0)), F32(88.0))
+    return g / (F32(1.0) + exp_f32(t))
+
+
+def silu_mul(gu_bits: np.ndarray, inter: int) -> np.ndarray:
+    """h = bf16_rne(silu(g) * u) (reading R10) for gate_up rows laid out as
+    [gate (inter values) | up (inter values)].  Returns BF16 bits [M][inter].
+    Pinned: gate/up asymmetry by hand, silu(0) = 0, silu(g) = g for large g,
+    and agreement with the fp64 SiLU rounded once wherever the fp64 value is
+    not within rounding noise of a BF16 midpoint."""
+    gu = np.asarray(gu_bits, dtype=np.uint16)
+    g = bf16_to_f32(gu[:, :inter])
+    u = bf16_to_f32(gu[:, inter:2 * inter])
+    return f32_to_bf16(silu_f32(g) * u)
+
+
+def silu_mul_f64(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """silu(g) * u in fp64 (the accuracy yardstick and the calibration glue)."""
+    g = np.asarray(g, dtype=F64)
+    return g / (1.0 + np.exp(-g)) * np.asarray(u, dtype=F64)
+
+
+def silu_mul_smooth_quant(gu_bits: np.ndarray, inter: int, smooth: np.ndarray):
+    """The MLP glue as one step: h = silu_mul(...), then smooth_quant_act(h)."""
+    return smooth_quant_act(silu_mul(gu_bits, inter), smooth)
 
 
 # ---------------------------------------------------------------------------

@@ -536,3 +536,99 @@ def test_lm_head_verify_hand_built():
     n_acc, nxt = orc.lm_head_verify(orc.f32_to_bf16(h), orc.f32_to_bf16(w), draft)
     assert n_acc.tolist() == [2, 3]
     assert nxt.tolist() == [6, 7]
+
+
+# ------------------------------------- MLP glue: SiLU(gate) * up (reading R10)
+
+def test_exp_f32_constants():
+    """The reduction constants and coefficients are what the algorithm says:
+    log2(e), ln2 split in a head whose products with every n of the range
+    are exact and a tail, and 1/k! -- each the fp32 rounding of the exact
+    value (rational arithmetic)."""
+    ln2 = Fraction(math.log(2))          # fp64 ln2: 2^-53 relative, far below what is checked
+    hi, lo = Fraction(float(orc.EXP_LN2_HI)), Fraction(float(orc.EXP_LN2_LO))
+    assert abs(hi + lo - ln2) <= ulp_f32(lo)
+    assert round_to_f32(ln2 - hi) == lo
+    for n in range(-126, 128):           # n * head is exact in fp32
+        assert round_to_f32(n * hi) == n * hi if n else True
+    assert Fraction(float(orc.EXP_LOG2E)) == round_to_f32(1 / ln2)
+    for k, c in zip(range(7, 1, -1), orc.EXP_TAYLOR):
+        assert Fraction(float(c)) == round_to_f32(Fraction(1, math.factorial(k)))
+
+
+def test_exp_f32_within_two_ulp():
+    """Against the fp64 exponential on a dense grid of the clamped range (a
+    dropped Taylor term already gives ~3 ulp, a dropped ln2 tail thousands)."""
+    t = np.linspace(-87.0, 88.0, 2_000_001).astype(np.float32)
+    t = np.concatenate([t, np.float32(2.0) ** -np.arange(1, 40, dtype=np.float32),
+                        -np.float32(2.0) ** -np.arange(1, 40, dtype=np.float32)])
+    ref = np.exp(t.astype(np.float64))
+    err = np.abs(orc.exp_f32(t).astype(np.float64) - ref) / np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert err.max() <= 2.0
+    assert orc.exp_f32(np.float32(0.0)) == np.float32(1.0)
+
+
+def test_silu_f32_closed_forms_and_accuracy():
+    """silu(0) = 0; for g >= 18, e^-g < 2^-25 so 1 + e rounds to 1 and silu(g)
+    is g exactly; elsewhere within 3 ulp of g / (1 + e^-g) in fp64 (exp's 2 ulp
+    plus two roundings)."""
+    big = np.array([18.0, 20.0, 87.5, 1000.0, 3.0e38], np.float32)
+    assert np.array_equal(orc.silu_f32(big), big)
+    assert orc.silu_f32(np.zeros(3, np.float32)).tolist() == [0.0, 0.0, 0.0]
+    g = np.linspace(-87.0, 80.0, 1_000_001).astype(np.float32)
+    g = g[g != 0]
+    ref = g.astype(np.float64) / (1.0 + np.exp(-g.astype(np.float64)))
+    err = np.abs(orc.silu_f32(g).astype(np.float64) - ref) / np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    assert err.max() <= 3.0
+    # below the clamp the result stays a tiny negative number of the right sign
+    tail = orc.silu_f32(np.array([-90.0, -1000.0], np.float32))
+    assert np.all(tail < 0) and np.all(tail > -1e-30)
+
+
+def test_silu_mul_gate_up_order_by_hand():
+    """Row layout [gate | up]: silu(20) * 0.5 = 10 exactly; silu(0) * 7 = 0;
+    silu(2) * -1 = -2 / (1 + e^-2) = -1.761594... -> BF16 -1.7578125 (spacing
+    2^-7 on [1, 2): it lies 0.00378 from -1.7578125 and 0.00403 from
+    -1.765625).  Swapping gate and up changes every nonzero entry."""
+    g = [20.0, 0.0, 2.0]
+    u = [0.5, 7.0, -1.0]
+    h = orc.silu_mul(bf16([g + u]), 3)
+    assert orc.bf16_to_f32(h).tolist() == [[10.0, 0.0, -1.7578125]]
+    swapped = orc.silu_mul(bf16([u + g]), 3)
+    assert not np.array_equal(orc.bf16_to_f32(swapped)[0, [0, 2]], orc.bf16_to_f32(h)[0, [0, 2]])
+
+
+def test_silu_mul_is_the_fp64_value_rounded_once():
+    """On data shaped like a gate_up output, h equals the fp64 silu(g) * u
+    rounded once to BF16 wherever that value is not within fp32 noise of a
+    BF16 rounding midpoint, and is never more than one BF16 step away."""
+    rng = np.random.default_rng(61)
+    M, inter = 16, 4096
+    gu = synth.f32_to_bf16_bits(rng.standard_normal((M, 2 * inter)) * rng.uniform(0.5, 8.0, (M, 1)))
+    h = orc.silu_mul(gu, inter)
+    g = orc.bf16_to_f32(gu[:, :inter]).astype(np.float64)
+    u = orc.bf16_to_f32(gu[:, inter:]).astype(np.float64)
+    ref = orc.silu_mul_f64(g, u)
+    ref_bits = orc.f64_to_bf16(ref)
+    clear = orc.bf16_midpoint_distance(ref) > 1e-6 * np.abs(ref)
+    assert clear.mean() > 0.99
+    assert np.array_equal(h[clear], ref_bits[clear])
+    step = np.abs(orc.bf16_to_f32(h).astype(np.float64) - orc.bf16_to_f32(ref_bits))
+    assert np.all(step <= np.spacing(np.abs(orc.bf16_to_f32(ref_bits))) * 65536 + 1e-38)
+
+
+def test_silu_mul_smooth_quant_is_the_composition():
+    """The glue step quantizes h exactly as the activation quantizer does: a
+    code of magnitude 127 in every nonzero row, codes * sa within sa/2 of
+    fp32(h) * smooth, and a zero gate row gives a zero row."""
+    rng = np.random.default_rng(62)
+    M, inter = 6, 256
+    gu = synth.f32_to_bf16_bits(rng.standard_normal((M, 2 * inter)) * 3.0)
+    gu[3, :inter] = 0                     # silu(0) = 0: the whole row of h is 0
+    s = rng.uniform(0.25, 4.0, inter).astype(np.float32)
+    xq, sa = orc.silu_mul_smooth_quant(gu, inter, s)
+    hv = orc.bf16_to_f32(orc.silu_mul(gu, inter)).astype(np.float64) * s[None, :]
+    assert sa[3] == 0 and not xq[3].any()
+    nz = sa > 0
+    assert np.all(np.abs(xq[nz]).max(axis=1) == 127)
+    assert np.all(np.abs(xq.astype(np.float64) * sa[:, None] - hv) <= sa[:, None] * (0.5 + 1e-5))
