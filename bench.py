@@ -17,7 +17,8 @@ as a bandwidth reference, the same linears with 4-bit weights (W4A8) at
 M = 1, 8, 20, the verification kernel at B=32, D=8,
 V=151936, the fused BF16 lm_head + verification at the same B, D, V, and the
 whole verification step of four decoder layers' W8A8 linears plus the lm_head
-at 288 token rows against the same chain on BF16 cuBLAS.
+at 288 token rows against the same chain on BF16 cuBLAS, and the MLP block at
+M = 40 (gate_up, SiLU * up with down's quantizer, down) against BF16 cuBLAS.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch with torch.distributed.run; each rank runs an independent
@@ -464,6 +465,7 @@ def main_gpu(args):
         extra["verify"] = run_verify(q, dev, stream, ws, hbm)
         extra["lm_head"] = run_lm_head(q, dev, stream, bf16)
         extra["verification_step"] = run_verification_step(q, dev, stream, bf16)
+        extra["mlp_block"] = run_mlp_block(q, dev, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -652,6 +654,64 @@ def run_lm_head(q, dev, stream, bf16_peak):
     return out
 
 
+def run_mlp_block(q, dev, stream):
+    """The Qwen3-8B MLP block at M = 40 (8 sequences x (4 drafts + 1)):
+    gate_up as one call of the fused smooth + quantize + W8A8 linear, then
+    SiLU(gate) * up with down's smooth + quantize in one launch, then the down
+    W8A8 linear; against BF16 cuBLAS gate_up, torch SiLU * up and BF16 cuBLAS
+    down.  Weight sets rotate so that L2 is cold."""
+    import torch
+    import torch.nn.functional as F
+    M = 40
+    K, N_gu = synth.LINEARS["gate_up"]
+    inter, N_dn = synth.LINEARS["down"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    ncopy = copies_for_cold_l2(N_gu * K + N_dn * inter)
+    sets = []
+    for _ in range(ncopy):
+        st = {}
+        for tag, (N, Kl) in (("gu", (N_gu, K)), ("dn", (N_dn, inter))):
+            st["wp_" + tag] = q.tile_weights(torch.randint(-127, 128, (N, Kl), dtype=torch.int8, device=dev,
+                                                           generator=gen))
+            st["sw_" + tag] = torch.rand(N, device=dev, generator=gen) * 1e-3
+            st["wb_" + tag] = (torch.randn((N, Kl), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+        sets.append(st)
+    x = torch.randn((M, K), device=dev, generator=gen).to(torch.bfloat16)
+    s_gu = torch.rand(K, device=dev, generator=gen) + 0.5
+    s_dn = torch.rand(inter, device=dev, generator=gen) + 0.5
+    gu = torch.empty((M, N_gu), dtype=torch.bfloat16, device=dev)
+    xq = torch.empty((M, inter), dtype=torch.int8, device=dev)
+    sa = torch.empty(M, dtype=torch.float32, device=dev)
+    y = torch.empty((M, N_dn), dtype=torch.bfloat16, device=dev)
+    h_b = torch.empty((M, inter), dtype=torch.bfloat16, device=dev)
+    ws = q.Workspace(dev)
+    ws.get(max(q.lib.quasar_w8a8_linear_fused_workspace_size(M, N_gu, K),
+               q.lib.quasar_w8a8_linear_workspace_size(M, N_dn, inter)))
+
+    def ours(i):
+        st = sets[i % ncopy]
+        q.w8a8_linear_fused(x, s_gu, st["wp_gu"], st["sw_gu"], y=gu, workspace=ws)
+        q.silu_mul_smooth_quant(gu, s_dn, xq=xq, sa=sa)
+        q.w8a8_linear(xq, sa, st["wp_dn"], st["sw_dn"], y=y, workspace=ws)
+
+    def bf16(i):
+        st = sets[i % ncopy]
+        torch.matmul(x, st["wb_gu"].t(), out=gu)
+        torch.mul(F.silu(gu[:, :inter]), gu[:, inter:], out=h_b)
+        torch.matmul(h_b, st["wb_dn"].t(), out=y)
+
+    us = _time_graph(torch, stream, ours, 2 * ncopy)
+    us_bf = _time_graph(torch, stream, bf16, 2 * ncopy)
+    wbytes = N_gu * K + 4 * N_gu + N_dn * inter + 4 * N_dn
+    out = {"M": M, "us": round(us, 1), "bf16_cublas_us": round(us_bf, 1), "speedup_vs_bf16": round(us_bf / us, 3),
+           "int8_weight_bytes": wbytes, "weight_TBps": round(wbytes / (us * 1e-6) / 1e12, 3),
+           "launches": 4, "weight_sets": ncopy}
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_verification_step(q, dev, stream, bf16_peak):
     """Verification step of 32 sequences x (8 drafts + 1) = 288 token rows:
     four Qwen3-8B decoder layers' W8A8 linears (qkv, o, gate_up, down; each
@@ -728,6 +788,8 @@ def main():
                     help="run only the fused lm_head + verification sub-benchmark (profiling)")
     ap.add_argument("--verification-step-only", action="store_true",
                     help="run only the 4-layer verification-step sub-benchmark")
+    ap.add_argument("--mlp-block-only", action="store_true",
+                    help="run only the M = 40 MLP-block sub-benchmark")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -740,6 +802,12 @@ def main():
         torch.cuda.set_device(dev)
         print(json.dumps({"verification_step": run_verification_step(q, dev, torch.cuda.Stream(dev),
                                                                      load_peaks()[1])}), flush=True)
+    elif args.mlp_block_only:
+        import torch
+        from w8a8_quantized_speculative_gb300 import quasar as q
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"mlp_block": run_mlp_block(q, dev, torch.cuda.Stream(dev))}), flush=True)
     elif args.lm_head_only:
         import torch
         from w8a8_quantized_speculative_gb300 import quasar as q

@@ -155,6 +155,36 @@ quasar_status_t quasar_smooth_quant_act(const void* X_bf16, int ldx, const float
                                         quasar_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * A2 for the MLP block's down projection: SiLU(gate) * up, then smooth +
+ * quantize, in one launch.
+ *
+ * zh §2 / pt §2: the verifier dequantizes to BF16 ahead of the nonlinear
+ * layers; the MLP's down linear then smooths and quantizes its input like any
+ * other.  Per token m and k < I, in fp32:
+ *   g = float(GU[m][k]), u = float(GU[m][I + k])   (gate half, then up half)
+ *   h[k]  = bf16_rne( (g / (1 + exp(-g))) * u )     (one rounding to BF16)
+ *   then exactly quasar_smooth_quant_act on the row h (x' = float(h) * smooth).
+ * exp is a fixed fp32 algorithm so that the codes are a fixed function of the
+ * inputs: Cody and Waite's reduction t = n ln2 + r (ln2 as a 15-bit head
+ * 0x3F317200 plus a tail 0x35BFBE8E, n = rint(t * 0x3FB8AA3B)), the degree-7
+ * Taylor polynomial of e^r by Horner with fp32 coefficients 1/k!, times 2^n,
+ * every step one correctly rounded fp32 operation, the argument -g clamped
+ * to [-87, 88]; it is within 2 ulp of e^t.
+ *
+ *   GU     [M][ldgu] BF16 (the gate_up linear's output: gate in columns
+ *          0..I-1, up in I..2I-1), ldgu >= 2 I, ldgu % 8 == 0, 16-byte
+ *          aligned; M >= 0 (M == 0: no-op)
+ *   smooth [I] fp32 (down's smoothing vector), 16-byte aligned
+ *   Xq     [M][I] INT8 output (I % 16 == 0), sa [M] fp32 output
+ *   Returns QUASAR_ERR_UNSUPPORTED for I % 16 != 0, ldgu < 2 I or
+ *   ldgu % 8 != 0, QUASAR_ERR_INVALID_ARG for I <= 0, I > 2^29 or a null
+ *   pointer.  Feed Xq, sa to quasar_w8a8_linear with down's packed weights.
+ * ------------------------------------------------------------------------ */
+quasar_status_t quasar_silu_mul_smooth_quant(const void* GU_bf16, int ldgu, const float* smooth,
+                                             int M, int I, int8_t* Xq, float* sa,
+                                             quasar_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * A3 + A4  W8A8 linear: exact INT8 GEMM with fused BF16 dequant epilogue.
  *
  * pt §2 steps 3-4 / ko §2: the matmul runs on INT8 operands and the result

@@ -122,6 +122,22 @@ def test_quant_and_verify_reject_bad_arguments(lib):
     assert v(FAKE, 1000, FAKE, 0, 3, 1000, 0.0, None, FAKE, None, FAKE, 0, None) == 0         # B == 0
 
 
+def test_silu_mul_quant_rejects_bad_arguments(lib):
+    """The MLP glue entry: rows of [gate | up] need ldgu >= 2 I."""
+    g = lib.quasar_silu_mul_smooth_quant
+    g.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    assert g(FAKE, 256, FAKE, 4, 120, FAKE, FAKE, None) == 2     # I % 16
+    assert g(FAKE, 255, FAKE, 4, 128, FAKE, FAKE, None) == 2     # ldgu < 2 I
+    assert g(FAKE, 260, FAKE, 4, 128, FAKE, FAKE, None) == 2     # ldgu % 8
+    assert g(FAKE, 256, FAKE, 4, 0, FAKE, FAKE, None) == 1       # I <= 0
+    assert g(FAKE, 1 << 30, FAKE, 4, (1 << 29) + 16, FAKE, FAKE, None) == 1   # 2 I overflows
+    assert g(None, 256, FAKE, 4, 128, FAKE, FAKE, None) == 1
+    assert g(FAKE, 256, FAKE, 4, 128, FAKE, None, None) == 1
+    assert g(FAKE_ODD, 256, FAKE, 4, 128, FAKE, FAKE, None) == 2  # 16-byte alignment
+    assert g(FAKE, 256, FAKE, 0, 128, FAKE, FAKE, None) == 0     # M == 0: nothing launched
+
+
 def test_fused_linear_rejects_bad_arguments(lib):
     f = lib.quasar_w8a8_linear_fused
     f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p] + \

@@ -15,6 +15,11 @@
 // round trip); longer rows and the weights re-derive v in the second pass
 // (bit-identical), served from L1/L2.
 //
+// The MLP block's glue before down takes the same activation path on
+// h = bf16_rne(silu(gate) * up) computed from the gate_up output row as it is
+// loaded (quasar_silu_mul_smooth_quant): the pages dequantize to BF16 ahead of
+// the nonlinear layers, and down then re-smooths and re-quantizes.
+//
 // Activation codes are written row-major [M][K].  Weight codes are written in
 // the packed layout the W8A8 linear streams: 128 x 128 blocks, tile-major,
 // each block 16 KB contiguous with the 16-byte chunks of row r stored in
@@ -43,13 +48,52 @@ QUASAR_DEVICE_INLINE void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
+// The MLP glue before down (SiLU(gate) * up, rounded once to BF16) needs an
+// exponential whose every bit is fixed, because the rounded h decides the
+// codes.  exp_cw: Cody and Waite's argument reduction t = n ln2 + r, with
+// ln2 split in a 15-bit head (n * head is exact for |n| < 2^9) and a tail,
+// then the degree-7 Taylor polynomial of e^r by Horner, times 2^n.  Each step
+// is one correctly rounded fp32 operation (no contraction); within 2 ulp of
+// e^t on [-87, 88], the range callers clamp to (2^n stays a normal number).
+QUASAR_DEVICE_INLINE float exp_cw(float t) {
+  const float n = rintf(__fmul_rn(t, __uint_as_float(0x3FB8AA3Bu)));                   // t / ln2
+  const float r = __fsub_rn(__fsub_rn(t, __fmul_rn(n, __uint_as_float(0x3F317200u))),  // ln2 head
+                            __fmul_rn(n, __uint_as_float(0x35BFBE8Eu)));                // ln2 tail
+  float p = __uint_as_float(0x39500D01u);                                                // 1/7!
+  p = __fadd_rn(__fmul_rn(p, r), __uint_as_float(0x3AB60B61u));                         // 1/6!
+  p = __fadd_rn(__fmul_rn(p, r), __uint_as_float(0x3C088889u));                         // 1/5!
+  p = __fadd_rn(__fmul_rn(p, r), __uint_as_float(0x3D2AAAABu));                         // 1/4!
+  p = __fadd_rn(__fmul_rn(p, r), __uint_as_float(0x3E2AAAABu));                         // 1/3!
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  return __fmul_rn(p, __uint_as_float((uint32_t)((int)n + 127) << 23));
+}
+
+// h = bf16_rne(silu(g) * u) as fp32, silu(g) = g / (1 + exp(-g)) with the
+// exponential's argument clamped to [-87, 88].
+QUASAR_DEVICE_INLINE float silu_mul_bf16(float g, float u) {
+  const float t = fminf(fmaxf(-g, -87.f), 88.f);
+  const float s = __fdiv_rn(g, __fadd_rn(1.f, exp_cw(t)));
+  return __bfloat162float(__float2bfloat16_rn(__fmul_rn(s, u)));
+}
+
+// GLU rows hold [gate (K values) | up (K values)]: replace the 8 gate values
+// in f by h = silu(gate) * up.
+QUASAR_DEVICE_INLINE void glu8(float (&f)[8], const uint4& up) {
+  float u[8];
+  bf16x8_to_f32(up, u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) f[i] = silu_mul_bf16(f[i], u[i]);
+}
+
 // Byte offset of code (n, k) in the packed weight layout (k a multiple of 8).
 QUASAR_DEVICE_INLINE size_t packed_offset(int n, int k, int KB) {
   const int r = n & 127, kk = k & 127, c = kk >> 4;
   return (((size_t)(n >> 7) * KB + (k >> 7)) * 128 + r) * 128 + ((c ^ (r & 7)) << 4) + (kk & 15);
 }
 
-template <bool DIVIDE, bool PACKED>
+template <bool DIVIDE, bool PACKED, bool GLU = false>
 __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const uint16_t* __restrict__ in, int ld,
                                                              const float* __restrict__ smooth, int K,
                                                              int8_t* __restrict__ q, float* __restrict__ scale) {
@@ -70,6 +114,7 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const uint16_t* __r
     const float4 s1 = __ldg(reinterpret_cast<const float4*>(smooth) + 2 * v + 1);
     float f[8];
     bf16x8_to_f32(raw, f);
+    if constexpr (GLU) glu8(f, __ldg(reinterpret_cast<const uint4*>(src + K) + v));
     const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(smooth_op<DIVIDE>(f[i], s[i])));
@@ -102,6 +147,7 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const uint16_t* __r
       const float4 s1 = __ldg(reinterpret_cast<const float4*>(smooth) + 2 * v + 1);
       float f[8];
       bf16x8_to_f32(raw, f);
+      if constexpr (GLU) glu8(f, __ldg(reinterpret_cast<const uint4*>(src + K) + v));
       const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -127,8 +173,9 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const uint16_t* __r
 // false>.
 //
 // `xh` (optional): the same codes as fp16 [rows][K] (exact), for a linear that
-// takes its token operand already widened.
-template <int VPT>
+// takes its token operand already widened.  GLU: the row is [gate | up] and
+// the values quantized are h = bf16_rne(silu(gate) * up).
+template <int VPT, bool GLU = false>
 __global__ void __launch_bounds__(THREADS) quant_act_kernel(const uint16_t* __restrict__ in, int ld,
                                                             const float* __restrict__ smooth, int K,
                                                             int8_t* __restrict__ q, float* __restrict__ scale,
@@ -139,12 +186,14 @@ __global__ void __launch_bounds__(THREADS) quant_act_kernel(const uint16_t* __re
   const uint16_t* src = in + (size_t)row * ld;
   const int nvec = K / 8;
   uint4 raw[VPT];
+  uint4 rawu[GLU ? VPT : 1];
   float4 sm[2 * VPT];
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int v = threadIdx.x + i * THREADS;
     if (v < nvec) {
       raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+      if constexpr (GLU) rawu[i] = __ldg(reinterpret_cast<const uint4*>(src + K) + v);
       sm[2 * i] = __ldg(reinterpret_cast<const float4*>(smooth) + 2 * v);
       sm[2 * i + 1] = __ldg(reinterpret_cast<const float4*>(smooth) + 2 * v + 1);
     }
@@ -155,6 +204,9 @@ __global__ void __launch_bounds__(THREADS) quant_act_kernel(const uint16_t* __re
   for (int i = 0; i < VPT; ++i) {
     const int v = threadIdx.x + i * THREADS;
     bf16x8_to_f32(raw[i], x[i]);
+    if constexpr (GLU) {
+      if (v < nvec) glu8(x[i], rawu[i]);
+    }
     const float s[8] = {sm[2 * i].x, sm[2 * i].y, sm[2 * i].z, sm[2 * i].w,
                         sm[2 * i + 1].x, sm[2 * i + 1].y, sm[2 * i + 1].z, sm[2 * i + 1].w};
 #pragma unroll
@@ -289,11 +341,14 @@ size_t packed_bytes(int N, int K) {
   return (size_t)((N + 127) / 128) * ((K + 127) / 128) * 128 * 128;
 }
 
-template <bool DIVIDE, bool PACKED>
+// GLU: rows of [gate (K values) | up (K values)], quantizing silu(gate) * up
+// (activations only: not with DIVIDE or PACKED).
+template <bool DIVIDE, bool PACKED, bool GLU = false>
 static quasar_status_t run(const void* in, int ld, const float* smooth, int rows, int K, int8_t* q, float* scale,
                            cudaStream_t stream, void* xh = nullptr) {
-  if (rows < 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
-  if (K % 16 != 0 || ld < K || ld % 8 != 0) return QUASAR_ERR_UNSUPPORTED;
+  static_assert(!(GLU && (DIVIDE || PACKED)), "the GLU glue is an activation step");
+  if (rows < 0 || K <= 0 || (GLU && K > (1 << 29))) return QUASAR_ERR_INVALID_ARG;
+  if (K % 16 != 0 || ld < (GLU ? 2 * K : K) || ld % 8 != 0) return QUASAR_ERR_UNSUPPORTED;
   if (rows == 0) return QUASAR_OK;  // empty batch: nothing is read or written
   if (!in || !smooth || !q || !scale) return QUASAR_ERR_INVALID_ARG;
   if (!aligned(in, 16) || !aligned(smooth, 16) || !aligned(q, 16) || !aligned(scale, 4))
@@ -320,11 +375,11 @@ static quasar_status_t run(const void* in, int ld, const float* smooth, int rows
   const int vpt = (K / 8 + THREADS - 1) / THREADS;   // 8-value vectors per thread
   uint4* xh4 = reinterpret_cast<uint4*>(xh);
   if (!DIVIDE && vpt <= 2)
-    return cuda_status(cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, x, ld, smooth, K, q, scale, xh4));
+    return cuda_status(cudaLaunchKernelEx(&cfg, quant_act_kernel<2, GLU>, x, ld, smooth, K, q, scale, xh4));
   if (!DIVIDE && vpt <= 6)
-    return cuda_status(cudaLaunchKernelEx(&cfg, quant_act_kernel<6>, x, ld, smooth, K, q, scale, xh4));
+    return cuda_status(cudaLaunchKernelEx(&cfg, quant_act_kernel<6, GLU>, x, ld, smooth, K, q, scale, xh4));
   if (xh) return QUASAR_ERR_UNSUPPORTED;  // rows too long for the one-pass kernel: no fp16 copy
-  return cuda_status(cudaLaunchKernelEx(&cfg, quant_rows_kernel<DIVIDE, PACKED>, x, ld, smooth, K, q, scale));
+  return cuda_status(cudaLaunchKernelEx(&cfg, quant_rows_kernel<DIVIDE, PACKED, GLU>, x, ld, smooth, K, q, scale));
 }
 
 // Smooth + quantize (quasar_smooth_quant_act) and also write the codes as
@@ -398,6 +453,12 @@ quasar_status_t quasar_smooth_quant_act(const void* X_bf16, int ldx, const float
                                         int8_t* Xq, float* sa, quasar_stream_t stream) {
   return quasar::quant::run<false, false>(X_bf16, ldx, smooth, M, K, Xq, sa,
                                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+quasar_status_t quasar_silu_mul_smooth_quant(const void* GU_bf16, int ldgu, const float* smooth, int M, int I,
+                                             int8_t* Xq, float* sa, quasar_stream_t stream) {
+  return quasar::quant::run<false, false, true>(GU_bf16, ldgu, smooth, M, I, Xq, sa,
+                                                reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

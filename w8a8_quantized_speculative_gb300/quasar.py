@@ -43,6 +43,7 @@ _SIGS = {
     "quasar_tile_weights_w4": (_i, [_p, _i, _i, _p, _p]),
     "quasar_w4a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_smooth_quant_act": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
+    "quasar_silu_mul_smooth_quant": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
     "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_w8a8_linear_fused_workspace_size": (_sz, [_i, _i, _i]),
@@ -237,6 +238,24 @@ def smooth_quant_act(x: torch.Tensor, smooth: torch.Tensor, xq=None, sa=None, st
     sa = torch.empty(M, dtype=torch.float32, device=x.device) if sa is None else sa
     _check(lib.quasar_smooth_quant_act(_ptr(x), ldx, _ptr(smooth), M, K, _ptr(xq), _ptr(sa), _stream(stream)),
            "smooth_quant_act")
+    return xq, sa
+
+
+def silu_mul_smooth_quant(gu: torch.Tensor, smooth: torch.Tensor, xq=None, sa=None, stream=None):
+    """(Xq int8 [M][I], sa fp32 [M]) of h = bf16(silu(gate) * up), from the
+    gate_up output gu [M][2I] (gate in columns 0..I-1, up in I..2I-1) and
+    down's smooth [I]: the MLP glue before down, one launch."""
+    _need(gu, torch.bfloat16, "gu")
+    _need(smooth, torch.float32, "smooth")
+    ldgu = _rowmajor(gu, "gu")
+    M, two_i = gu.shape
+    if two_i % 2:
+        raise ValueError("gu must hold [gate | up] halves of equal width")
+    inter = two_i // 2
+    xq = torch.empty((M, inter), dtype=torch.int8, device=gu.device) if xq is None else xq
+    sa = torch.empty(M, dtype=torch.float32, device=gu.device) if sa is None else sa
+    _check(lib.quasar_silu_mul_smooth_quant(_ptr(gu), ldgu, _ptr(smooth), M, inter, _ptr(xq), _ptr(sa),
+                                            _stream(stream)), "silu_mul_smooth_quant")
     return xq, sa
 
 
