@@ -87,9 +87,13 @@ def _gate_up_like(seed, M, inter, width=None):
     return synth.f32_to_bf16_bits(a)
 
 
-@pytest.mark.parametrize("M,inter", [(1, 16), (3, 48), (20, 4096), (40, 12288), (256, 12288), (7, 16384)])
+@pytest.mark.parametrize("M,inter", [(1, 16), (3, 48), (20, 4096), (40, 12288), (256, 12288), (7, 16384),
+                                     (5, 4112), (2, 8208), (3, 40960)])
 def test_silu_mul_smooth_quant_bit_exact(M, inter):
-    """Codes and scales bit for bit; 16384-wide rows take the two-pass kernel."""
+    """Codes and scales bit for bit on every launch shape: one CTA per row
+    (16, 48; 8208, which no cluster divides), clusters of 2 CTAs (4096; 4112
+    with two vectors per thread) and of 8 (12288, 16384), and the two-pass
+    kernel (40960)."""
     gu = _gate_up_like(2000 + M, M, inter)
     s = np.exp(np.random.default_rng(inter).uniform(-2, 2, inter)).astype(np.float32)
     xq, sa = q.silu_mul_smooth_quant(dev_bf16(gu), dev(s))
@@ -101,7 +105,7 @@ def test_silu_mul_smooth_quant_bit_exact(M, inter):
 
 
 def test_silu_mul_smooth_quant_strided_and_empty():
-    M, inter, width = 5, 256, 2 * 256 + 64
+    M, inter, width = 5, 4096, 2 * 4096 + 64
     full = _gate_up_like(2077, M, inter, width)
     s = np.linspace(0.5, 2.0, inter).astype(np.float32)
     xq, sa = q.silu_mul_smooth_quant(dev_bf16(full)[:, :2 * inter], dev(s))

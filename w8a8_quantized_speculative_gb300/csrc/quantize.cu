@@ -249,6 +249,128 @@ __global__ void __launch_bounds__(THREADS) quant_act_kernel(const uint16_t* __re
   }
 }
 
+// The GLU glue of long rows, one row per thread-block cluster of C CTAs: CTA
+// r of the cluster takes values [r K/C, (r+1) K/C) of the row (at most
+// 2048 VPT of them, VPT 8-value vectors per thread), so a few rows still fill
+// the GPU.  The row's absmax is the largest of the C CTAs' partial maxima,
+// read from each CTA's shared memory across the cluster; a max is exact in
+// any order, so codes and scale are those of quant_act_kernel<*, true>.
+QUASAR_DEVICE_INLINE uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+QUASAR_DEVICE_INLINE uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+QUASAR_DEVICE_INLINE float ld_cluster_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(THREADS) glu_quant_cluster_kernel(const uint16_t* __restrict__ in, int ld,
+                                                                    const float* __restrict__ smooth, int K, int C,
+                                                                    int8_t* __restrict__ q,
+                                                                    float* __restrict__ scale) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int rank = (int)cluster_ctarank();
+  const int row = (int)cluster_id_x();
+  const int slice = K / C;                                   // a multiple of 8
+  const int nvec = slice / 8;
+  const uint16_t* src = in + (size_t)row * ld + (size_t)rank * slice;
+  const float* sms = smooth + (size_t)rank * slice;
+  uint4 raw[VPT], rawu[VPT];
+  float4 sm[2 * VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * THREADS;
+    if (v < nvec) {
+      raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+      rawu[i] = __ldg(reinterpret_cast<const uint4*>(src + K) + v);
+      sm[2 * i] = __ldg(reinterpret_cast<const float4*>(sms) + 2 * v);
+      sm[2 * i + 1] = __ldg(reinterpret_cast<const float4*>(sms) + 2 * v + 1);
+    }
+  }
+  float x[VPT][8];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * THREADS;
+    if (v >= nvec) continue;
+    bf16x8_to_f32(raw[i], x[i]);
+    glu8(x[i], rawu[i]);
+    const float s[8] = {sm[2 * i].x, sm[2 * i].y, sm[2 * i].z, sm[2 * i].w,
+                        sm[2 * i + 1].x, sm[2 * i + 1].y, sm[2 * i + 1].z, sm[2 * i + 1].w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      x[i][e] = __fmul_rn(x[i][e], s[e]);
+      amax = fmaxf(amax, fabsf(x[i][e]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[THREADS / 32];
+  __shared__ float cta_amax;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = red[0];
+#pragma unroll
+    for (int w = 1; w < THREADS / 32; ++w) a = fmaxf(a, red[w]);
+    cta_amax = a;
+  }
+  // Every CTA's partial maximum is in its shared memory before any is read.
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  amax = 0.f;
+  for (int r = 0; r < C; ++r) amax = fmaxf(amax, ld_cluster_f32(&cta_amax, (uint32_t)r));
+  // Reads done: arrive now, wait before exiting so that no CTA's shared
+  // memory goes away while another CTA of the cluster may still read it.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
+  if (rank == 0 && threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
+  int8_t* dst = q + (size_t)row * K + (size_t)rank * slice;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * THREADS;
+    if (v >= nvec) continue;
+    uint32_t packed[2] = {0u, 0u};
+    if (amax > 0.f) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        int c = __float2int_rn(__fmul_rn(x[i][e], inv));
+        c = max(-127, min(127, c));
+        packed[e >> 2] |= (uint32_t)(c & 0xFF) << (8 * (e & 3));
+      }
+    }
+    reinterpret_cast<uint2*>(dst)[v] = make_uint2(packed[0], packed[1]);
+  }
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Cluster shape for a GLU row of K values: the smallest C in {2, 4, 8} that
+// divides the row into 8-value vectors with at most 2048 * vpt values per
+// CTA, trying vpt = 1 first; {0, 0} when rows of K <= 2048 fit one CTA's
+// single vector per thread, or no shape fits.
+struct GluCluster {
+  int C, vpt;
+};
+static GluCluster glu_cluster(int K) {
+  if (K <= 2048) return {0, 0};
+  for (int vpt = 1; vpt <= 2; ++vpt)
+    for (int C = 2; C <= 8; C *= 2)
+      if (K % (8 * C) == 0 && K / C <= 2048 * vpt) return {C, vpt};
+  return {0, 0};
+}
+
 // Row-major INT8 codes [N][K] -> packed layout, 16 bytes per thread.
 __global__ void tile_weights_kernel(const int8_t* __restrict__ src, int N, int K, int8_t* __restrict__ dst) {
   const int chunks = K / 16;
@@ -372,6 +494,24 @@ static quasar_status_t run(const void* in, int ld, const float* smooth, int rows
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const uint16_t* x = reinterpret_cast<const uint16_t*>(in);
+  if constexpr (GLU) {
+    const GluCluster gc = glu_cluster(K);
+    if (gc.C > 1) {
+      cudaLaunchAttribute cattr[2];
+      cattr[0] = attr[0];
+      cattr[1].id = cudaLaunchAttributeClusterDimension;
+      cattr[1].val.clusterDim.x = (unsigned)gc.C;
+      cattr[1].val.clusterDim.y = 1;
+      cattr[1].val.clusterDim.z = 1;
+      cudaLaunchConfig_t ccfg = cfg;
+      ccfg.gridDim = dim3((unsigned)rows * (unsigned)gc.C);
+      ccfg.attrs = cattr;
+      ccfg.numAttrs = 2;
+      if (gc.vpt == 1)
+        return cuda_status(cudaLaunchKernelEx(&ccfg, glu_quant_cluster_kernel<1>, x, ld, smooth, K, gc.C, q, scale));
+      return cuda_status(cudaLaunchKernelEx(&ccfg, glu_quant_cluster_kernel<2>, x, ld, smooth, K, gc.C, q, scale));
+    }
+  }
   const int vpt = (K / 8 + THREADS - 1) / THREADS;   // 8-value vectors per thread
   uint4* xh4 = reinterpret_cast<uint4*>(xh);
   if (!DIVIDE && vpt <= 2)
