@@ -65,6 +65,17 @@ The pages leave the numeric details open.  The readings taken here are:
       by Horner, times 2^n; each step one correctly rounded fp32 operation;
       the argument clamped to [-87, 88]), within 2 fp32 ulp of the true
       exponential.  Then h is smoothed and quantized as R2.
+  R11 the RMSNorm ahead of qkv and gate_up, fused with their smooth +
+      quantize (the producer of those linears' BF16 input): per token,
+      ss = sum_k x_k^2 (each square exact in fp64; the sum correctly
+      rounded), r = fp32_rn(1 / sqrt(ss / K + eps)) in fp64 (division,
+      square root and division correctly rounded, one rounding to fp32),
+      t_k = bf16_rne(x_k * r), h_k = bf16_rne(t_k * gamma_k) in fp32 (the
+      usual BF16 RMSNorm: normalise, round to the activation type, apply the
+      BF16 weight), then h smoothed and quantized as R2.  A device sums the
+      squares in its own order, which can move ss by a few fp64 ulps, so a
+      row whose fp64 inverse RMS lies within 2^-38 (relative) of an fp32
+      rounding midpoint is ambiguous: compared by count, not bit for bit.
 
 Every function below is pinned by tests under ``tests/`` against hand-derived
 values, closed forms, invariants or brute force (see each docstring).
@@ -267,6 +278,49 @@ def silu_mul_f64(g: np.ndarray, u: np.ndarray) -> np.ndarray:
 def silu_mul_smooth_quant(gu_bits: np.ndarray, inter: int, smooth: np.ndarray):
     """The MLP glue as one step: h = silu_mul(...), then smooth_quant_act(h)."""
     return smooth_quant_act(silu_mul(gu_bits, inter), smooth)
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm ahead of qkv / gate_up, then smooth + quantize (R11).
+
+def rms_inverse(x_bits: np.ndarray, eps: float):
+    """Per row: (r fp32, r64 fp64) with r64 = 1 / sqrt(ss / K + eps) in fp64,
+    ss the correctly rounded sum of the exact fp64 squares (math.fsum), and
+    r = r64 rounded once to fp32.  Pinned by an exact rational sum and by
+    the scale invariance of r under powers of two (eps = 0)."""
+    import math
+    x = bf16_to_f32(x_bits).astype(F64)
+    K = x.shape[1]
+    ss = np.array([math.fsum(row) for row in x * x], dtype=F64)
+    r64 = 1.0 / np.sqrt(ss / F64(K) + F64(F32(eps)))
+    return r64.astype(F32), r64
+
+
+def rms_ambiguous(r64: np.ndarray, band: float = 2.0 ** -38) -> np.ndarray:
+    """Rows whose fp64 inverse RMS lies within `band` (relative) of an fp32
+    rounding midpoint, where a few fp64 ulps of summation order could flip
+    its fp32 value.  Pinned on a constructed midpoint and a value far from
+    one."""
+    r64 = np.asarray(r64, dtype=F64)
+    m, e = np.frexp(r64)                      # r64 = m * 2^e, 0.5 <= m < 1
+    scaled = np.ldexp(m, 24)                  # 24 significant bits: fp32 spacing is 1 here
+    dist = np.abs(scaled - np.floor(scaled) - 0.5)
+    return dist <= band * scaled
+
+
+def rms_norm(x_bits: np.ndarray, gamma_bits: np.ndarray, eps: float) -> np.ndarray:
+    """h = bf16(bf16(x * r) * gamma) per token (reading R11); BF16 bits.
+    Pinned: a hand case where the intermediate rounding decides a tie,
+    scale invariance (eps = 0), a zero row, gamma = 2^j scaling exactly, and
+    agreement with the fp64 normalisation within two BF16 roundings."""
+    r, _ = rms_inverse(x_bits, eps)
+    t = f32_to_bf16(bf16_to_f32(x_bits) * r[:, None])
+    return f32_to_bf16(bf16_to_f32(t) * bf16_to_f32(gamma_bits)[None, :])
+
+
+def rms_norm_smooth_quant(x_bits: np.ndarray, gamma_bits: np.ndarray, eps: float, smooth: np.ndarray):
+    """RMSNorm (R11), then smooth_quant_act.  Returns (Xq, sa)."""
+    return smooth_quant_act(rms_norm(x_bits, gamma_bits, eps), smooth)
 
 
 # ---------------------------------------------------------------------------

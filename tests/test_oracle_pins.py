@@ -632,3 +632,90 @@ def test_silu_mul_smooth_quant_is_the_composition():
     nz = sa > 0
     assert np.all(np.abs(xq[nz]).max(axis=1) == 127)
     assert np.all(np.abs(xq.astype(np.float64) * sa[:, None] - hv) <= sa[:, None] * (0.5 + 1e-5))
+
+
+# ------------------------------------------- RMSNorm ahead of qkv (reading R11)
+
+def test_rms_norm_hand_case_intermediate_rounding():
+    """x = [3, 4], eps = 0: ss = 25, ms = 12.5, r = fp32(1/sqrt(12.5)).
+    t = bf16(3r) = 0.84765625 (3r = 0.848528, spacing 2^-8 on [0.5, 1)),
+    bf16(4r) = 1.1328125 (4r = 1.131371, spacing 2^-7).  With gamma = 1.5:
+    0.84765625 * 1.5 = 1.271484 -> 1.2734375; 1.1328125 * 1.5 = 1.69921875
+    is a tie between 1.6953125 and 1.703125 -> the even 1.703125.  Rounding
+    once instead (4r * 1.5 = 1.697056) would give 1.6953125."""
+    x = bf16([[3.0, 4.0]])
+    assert orc.bf16_to_f32(orc.rms_norm(x, bf16([1.0, 1.0]), 0.0)).tolist() == [[0.84765625, 1.1328125]]
+    assert orc.bf16_to_f32(orc.rms_norm(x, bf16([1.5, 1.5]), 0.0)).tolist() == [[1.2734375, 1.703125]]
+    r, r64 = orc.rms_inverse(x, 0.0)
+    assert Fraction(float(r[0])) == round_to_f32(Fraction(float(r64[0])))
+    assert abs(r64[0] - 1.0 / math.sqrt(12.5)) <= 1e-16
+
+
+def test_rms_inverse_sum_is_correctly_rounded():
+    """ss is the exact sum of the squares rounded once: checked with rational
+    arithmetic on rows mixing magnitudes 2^-20 .. 2^12 (where a plain fp64
+    running sum rounds)."""
+    rng = np.random.default_rng(71)
+    v = rng.standard_normal((4, 300)) * np.exp2(rng.integers(-20, 12, (4, 300)))
+    x = synth.f32_to_bf16_bits(v)
+    _, r64 = orc.rms_inverse(x, 0.0)
+    for i in range(4):
+        exact = sum(Fraction(float(a)) ** 2 for a in orc.bf16_to_f32(x[i]))
+        ss = float(exact)                          # Fraction -> float rounds correctly
+        assert r64[i] == 1.0 / math.sqrt(ss / 300.0)
+
+
+def test_rms_norm_scale_invariance_zero_row_and_gamma():
+    """With eps = 0 the normalisation ignores the row's scale exactly for
+    powers of two; a zero row gives zeros (r = 1/sqrt(eps)); gamma = 2^j
+    scales t exactly."""
+    rng = np.random.default_rng(72)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((5, 64)))
+    g = synth.f32_to_bf16_bits(1.0 + 0.1 * rng.standard_normal(64))
+    h = orc.rms_norm(x, g, 0.0)
+    for j in (-3, 5):
+        xs = synth.f32_to_bf16_bits(orc.bf16_to_f32(x).astype(np.float64) * 2.0 ** j)
+        assert np.array_equal(orc.rms_norm(xs, g, 0.0), h)
+    z = np.zeros((1, 64), np.uint16)
+    assert not orc.bf16_to_f32(orc.rms_norm(z, g, 1e-6)).any()
+    ones = bf16(np.ones(64))
+    t = orc.rms_norm(x, ones, 0.0)
+    assert np.array_equal(orc.bf16_to_f32(orc.rms_norm(x, bf16(np.full(64, 4.0)), 0.0)),
+                          orc.bf16_to_f32(t) * 4.0)
+
+
+def test_rms_norm_close_to_fp64_normalisation():
+    """Within two BF16 roundings of x / sqrt(mean(x^2) + eps) * gamma in
+    fp64: |h - t*gamma| <= ulp(h)/2 and |gamma| * |t - x*r| <= |gamma| *
+    ulp(t)/2 <= ulp(h) (h ~ t*gamma, so ulp(t)*|gamma| <= 2 ulp(h)), 1.5 BF16
+    steps in all; equal to it rounded once for most entries."""
+    rng = np.random.default_rng(73)
+    K = 4096
+    x = synth.activations(74, 16, K, synth.outlier_channels(75, K, 41), 30.0)
+    g = synth.f32_to_bf16_bits(1.0 + 0.1 * rng.standard_normal(K))
+    h = orc.bf16_to_f32(orc.rms_norm(x, g, 1e-6)).astype(np.float64)
+    xv = orc.bf16_to_f32(x).astype(np.float64)
+    ref = xv / np.sqrt((xv * xv).mean(axis=1, keepdims=True) + 1e-6) * orc.bf16_to_f32(g).astype(np.float64)[None, :]
+    step = np.spacing(np.maximum(np.abs(ref), np.abs(h)).astype(np.float32)).astype(np.float64) * 65536
+    assert np.all(np.abs(h - ref) <= 1.51 * step)
+    assert np.mean(orc.f64_to_bf16(ref) == orc.f32_to_bf16(h.astype(np.float32))) > 0.7
+
+
+def test_rms_ambiguous_band():
+    """A value on an fp32 rounding midpoint is flagged, one a quarter of the
+    spacing away is not, nor is an exact fp32 value."""
+    one = 1.0
+    mid = one + 2.0 ** -24                      # halfway between 1 and 1 + 2^-23
+    flags = orc.rms_ambiguous(np.array([mid, mid * (1 + 2.0 ** -45), one + 2.0 ** -25, 0.75]))
+    assert flags.tolist() == [True, True, False, False]
+
+
+def test_rms_norm_smooth_quant_is_the_composition():
+    rng = np.random.default_rng(76)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((6, 128)) * 3.0)
+    x[2] = 0
+    g = synth.f32_to_bf16_bits(1.0 + 0.1 * rng.standard_normal(128))
+    s = rng.uniform(0.25, 4.0, 128).astype(np.float32)
+    xq, sa = orc.rms_norm_smooth_quant(x, g, 1e-6, s)
+    assert sa[2] == 0 and not xq[2].any()
+    assert np.all(np.abs(xq[sa > 0]).max(axis=1) == 127)
