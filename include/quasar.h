@@ -155,6 +155,34 @@ quasar_status_t quasar_smooth_quant_act(const void* X_bf16, int ldx, const float
                                         quasar_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * A2 for qkv and gate_up: RMSNorm, then smooth + quantize, in one launch.
+ *
+ * pt §2 step 2 / zh §2: the BF16 input of a verify linear is smoothed and
+ * quantized on the fly; here that input is the RMSNorm of the residual
+ * stream and is formed on the way in.  Per token m, with K values:
+ *   ss = sum_k float(X[m][k])^2         (each square exact in fp64; fp64 sum)
+ *   r  = fp32_rn( 1 / sqrt(ss / K + eps) )   (fp64, IEEE division and sqrt)
+ *   t[k] = bf16_rne(float(X[m][k]) * r),  h[k] = bf16_rne(float(t[k]) * gamma[k])
+ *   then exactly quasar_smooth_quant_act on the row h.
+ * The sum is taken in the kernel's own order, which can move ss by a few
+ * fp64 ulps from the correctly rounded sum; r (and so the row's codes) can
+ * differ from a correctly rounded evaluation only when 1 / sqrt(ss/K + eps)
+ * lies within 2^-38 (relative) of an fp32 rounding midpoint.
+ *
+ *   X      [M][ldx] BF16, ldx >= K, ldx % 8 == 0, 16-byte aligned; M >= 0
+ *   gamma  [K] BF16 (the norm's weight), 16-byte aligned
+ *   eps    > 0 and finite (1e-6 for Qwen3)
+ *   smooth [K] fp32 (the linear's smoothing vector), 16-byte aligned
+ *   Xq     [M][K] INT8 output (K % 16 == 0, K <= 12288), sa [M] fp32 output
+ *   Returns QUASAR_ERR_UNSUPPORTED for K % 16 != 0, K > 12288, ldx < K,
+ *   ldx % 8 != 0 or a misaligned pointer; QUASAR_ERR_INVALID_ARG for K <= 0,
+ *   eps <= 0 or not finite, or a null pointer.
+ * ------------------------------------------------------------------------ */
+quasar_status_t quasar_rmsnorm_smooth_quant(const void* X_bf16, int ldx, const void* gamma_bf16,
+                                            float eps, const float* smooth, int M, int K,
+                                            int8_t* Xq, float* sa, quasar_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * A2 for the MLP block's down projection: SiLU(gate) * up, then smooth +
  * quantize, in one launch.
  *

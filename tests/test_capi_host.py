@@ -138,6 +138,20 @@ def test_silu_mul_quant_rejects_bad_arguments(lib):
     assert g(FAKE, 256, FAKE, 0, 128, FAKE, FAKE, None) == 0     # M == 0: nothing launched
 
 
+def test_rmsnorm_quant_rejects_bad_arguments(lib):
+    r = lib.quasar_rmsnorm_smooth_quant
+    r.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert r(FAKE, 128, FAKE, 1e-6, FAKE, 4, 120, FAKE, FAKE, None) == 2      # K % 16
+    assert r(FAKE, 64, FAKE, 1e-6, FAKE, 4, 128, FAKE, FAKE, None) == 2       # ldx < K
+    assert r(FAKE, 12304, FAKE, 1e-6, FAKE, 4, 12304, FAKE, FAKE, None) == 2  # rows beyond 12288 values
+    assert r(FAKE, 128, FAKE, 0.0, FAKE, 4, 128, FAKE, FAKE, None) == 1       # eps must be > 0
+    assert r(FAKE, 128, FAKE, float("inf"), FAKE, 4, 128, FAKE, FAKE, None) == 1
+    assert r(FAKE, 128, None, 1e-6, FAKE, 4, 128, FAKE, FAKE, None) == 1      # gamma
+    assert r(FAKE, 128, FAKE_ODD, 1e-6, FAKE, 4, 128, FAKE, FAKE, None) == 2  # gamma alignment
+    assert r(FAKE, 128, FAKE, 1e-6, FAKE, 0, 128, FAKE, FAKE, None) == 0      # M == 0
+
+
 def test_fused_linear_rejects_bad_arguments(lib):
     f = lib.quasar_w8a8_linear_fused
     f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p] + \

@@ -71,6 +71,75 @@ def test_smooth_quant_act_strided_rows():
     assert np.array_equal(xq.cpu().numpy(), xq_r) and np.array_equal(sa.cpu().numpy(), sa_r)
 
 
+# ---------------------------------------- RMSNorm ahead of qkv / gate_up
+
+def _norm_weight(seed, K):
+    return synth.f32_to_bf16_bits(1.0 + 0.1 * np.random.default_rng(seed).standard_normal(K))
+
+
+def _rms_compare(x, g, s, xq, sa):
+    """Codes and scales bit for bit on every row whose inverse RMS is not in
+    the fp64-order band (reading R11); returns the number of banded rows."""
+    xq_r, sa_r = orc.rms_norm_smooth_quant(x, g, 1e-6, s)
+    _, r64 = orc.rms_inverse(x, 1e-6)
+    ok = ~orc.rms_ambiguous(r64)
+    assert np.array_equal(sa.cpu().numpy()[ok].view(np.uint32), sa_r[ok].view(np.uint32))
+    assert np.array_equal(xq.cpu().numpy()[ok], xq_r[ok])
+    return int((~ok).sum())
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (3, 48), (20, 4096), (40, 4096), (288, 4096), (7, 5120), (3, 12288)])
+def test_rmsnorm_smooth_quant_bit_exact(M, K):
+    """Both launch shapes (up to 4096 and up to 12288 values per row), an
+    all-zero row (r = 1/sqrt(eps), h = 0) and outlier channels."""
+    x = synth.activations(3000 + M, M, K, synth.outlier_channels(8, K, max(1, K // 100)), 30.0)
+    if M > 2:
+        x[2] = 0
+    g = _norm_weight(K + M, K)
+    s = np.exp(np.random.default_rng(K).uniform(-2, 2, K)).astype(np.float32)
+    xq, sa = q.rmsnorm_smooth_quant(dev_bf16(x), dev_bf16(g), dev(s), eps=1e-6)
+    assert _rms_compare(x, g, s, xq, sa) <= 1
+    if M > 2:
+        assert sa.cpu().numpy()[2] == 0 and not xq.cpu().numpy()[2].any()
+
+
+def test_rmsnorm_smooth_quant_strided_and_empty():
+    M, K, ld = 5, 4096, 4096 + 64
+    full = synth.activations(3077, M, ld)
+    g = _norm_weight(3078, K)
+    s = np.linspace(0.5, 2.0, K).astype(np.float32)
+    xq, sa = q.rmsnorm_smooth_quant(dev_bf16(full)[:, :K], dev_bf16(g), dev(s))
+    assert _rms_compare(np.ascontiguousarray(full[:, :K]), g, s, xq, sa) <= 1
+    xq0, sa0 = q.rmsnorm_smooth_quant(torch.zeros((0, K), dtype=torch.bfloat16, device="cuda"), dev_bf16(g), dev(s))
+    assert xq0.shape == (0, K) and sa0.shape == (0,)
+
+
+def test_rmsnorm_then_qkv_chain():
+    """The attention block's input path at M = 20: RMSNorm + smooth + quantize
+    in one launch, then the qkv W8A8 linear, against the oracle's chain; the
+    smooth is calibrated on the normalised calibration batch."""
+    case = synth.attention_cases()[0]
+    x, w, xc = case.x(), case.w(), case.x_cal()
+    g = _norm_weight(3079, case.K)
+    h_cal = orc.rms_norm(xc, g, 1e-6)
+    s = q.calibrate_smooth(dev_bf16(h_cal), dev_bf16(w))
+    s_r = orc.calibrate_smooth(h_cal, w)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_r.view(np.uint32))
+    wq, sw = q.pack_weights(dev_bf16(w), s)
+    ws = q.Workspace()
+    xq, sa = q.rmsnorm_smooth_quant(dev_bf16(x), dev_bf16(g), s)
+    y = q.w8a8_linear(xq, sa, wq, sw, workspace=ws)
+    assert _rms_compare(x, g, s_r, xq, sa) == 0
+    xq_r, sa_r = orc.rms_norm_smooth_quant(x, g, 1e-6, s_r)
+    y_r = orc.w8a8_linear(xq_r, sa_r, *orc.pack_weights(w, s_r))
+    assert bf16_ulp_distance(host_bf16_bits(y), y_r).max() <= BF16_ULP_TOL
+    hv = orc.bf16_to_f32(orc.rms_norm(x, g, 1e-6)).astype(np.float64)
+    ref = hv @ orc.bf16_to_f32(w).astype(np.float64).T
+    yv = synth.bf16_bits_to_f32(host_bf16_bits(y)).astype(np.float64)
+    assert np.linalg.norm(yv - ref) / np.linalg.norm(ref) <= 2e-2
+    check_ws_zero(ws)
+
+
 # ------------------------------------------- MLP glue before down (SiLU * up)
 
 def _gate_up_like(seed, M, inter, width=None):

@@ -249,6 +249,112 @@ __global__ void __launch_bounds__(THREADS) quant_act_kernel(const uint16_t* __re
   }
 }
 
+QUASAR_DEVICE_INLINE float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// RMSNorm ahead of a linear (qkv, gate_up) fused with its smooth + quantize,
+// one CTA per row of up to 2048 VPT values, every load issued up front as in
+// quant_act_kernel.  Per row: ss = sum of the squares of the BF16 inputs, each
+// square exact in fp64, summed in fp64 in this kernel's order (per thread,
+// a butterfly across the warp, the warps in order); r = fp32_rn(1 /
+// sqrt(ss / K + eps)) with IEEE fp64 division and square root; t = bf16(x *
+// r), h = bf16(t * gamma); then the A2 quantizer on fp32(h) * smooth.  The
+// order of the sum can move ss by a few fp64 ulps from the correctly rounded
+// sum, which changes r only when 1 / sqrt(...) lies within a hair (2^-38
+// relative) of an fp32 rounding midpoint.
+template <int VPT>
+__global__ void __launch_bounds__(THREADS) rms_quant_kernel(const uint16_t* __restrict__ in, int ld,
+                                                            const uint16_t* __restrict__ gamma, float eps,
+                                                            const float* __restrict__ smooth, int K,
+                                                            int8_t* __restrict__ q, float* __restrict__ scale) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int row = blockIdx.x;
+  const uint16_t* src = in + (size_t)row * ld;
+  const int nvec = K / 8;
+  uint4 raw[VPT], gw[VPT];
+  float4 sm[2 * VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * THREADS;
+    if (v < nvec) {
+      raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+      gw[i] = __ldg(reinterpret_cast<const uint4*>(gamma) + v);
+      sm[2 * i] = __ldg(reinterpret_cast<const float4*>(smooth) + 2 * v);
+      sm[2 * i + 1] = __ldg(reinterpret_cast<const float4*>(smooth) + 2 * v + 1);
+    }
+  }
+  float x[VPT][8];
+  double ss = 0.0;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * THREADS;
+    if (v >= nvec) continue;
+    bf16x8_to_f32(raw[i], x[i]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const double d = (double)x[i][e];
+      ss = __dadd_rn(ss, __dmul_rn(d, d));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+  __shared__ double red64[THREADS / 32];
+  __shared__ float r_s;
+  if ((threadIdx.x & 31) == 0) red64[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = red64[0];
+#pragma unroll
+    for (int w = 1; w < THREADS / 32; ++w) t = __dadd_rn(t, red64[w]);
+    const double ms = __ddiv_rn(t, (double)K);
+    r_s = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(ms, (double)eps))));
+  }
+  __syncthreads();
+  const float r = r_s;
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * THREADS;
+    if (v >= nvec) continue;
+    float g[8];
+    bf16x8_to_f32(gw[i], g);
+    const float s[8] = {sm[2 * i].x, sm[2 * i].y, sm[2 * i].z, sm[2 * i].w,
+                        sm[2 * i + 1].x, sm[2 * i + 1].y, sm[2 * i + 1].z, sm[2 * i + 1].w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float h = bf16_round(__fmul_rn(bf16_round(__fmul_rn(x[i][e], r)), g[e]));
+      x[i][e] = __fmul_rn(h, s[e]);
+      amax = fmaxf(amax, fabsf(x[i][e]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[THREADS / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < THREADS / 32; ++w) amax = fmaxf(amax, red[w]);
+  const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
+  if (threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
+  int8_t* dst = q + (size_t)row * K;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * THREADS;
+    if (v >= nvec) continue;
+    uint32_t packed[2] = {0u, 0u};
+    if (amax > 0.f) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        int c = __float2int_rn(__fmul_rn(x[i][e], inv));
+        c = max(-127, min(127, c));
+        packed[e >> 2] |= (uint32_t)(c & 0xFF) << (8 * (e & 3));
+      }
+    }
+    reinterpret_cast<uint2*>(dst)[v] = make_uint2(packed[0], packed[1]);
+  }
+}
+
 // The GLU glue of long rows, one row per thread-block cluster of C CTAs: CTA
 // r of the cluster takes values [r K/C, (r+1) K/C) of the row (at most
 // 2048 VPT of them, VPT 8-value vectors per thread), so a few rows still fill
@@ -593,6 +699,33 @@ quasar_status_t quasar_smooth_quant_act(const void* X_bf16, int ldx, const float
                                         int8_t* Xq, float* sa, quasar_stream_t stream) {
   return quasar::quant::run<false, false>(X_bf16, ldx, smooth, M, K, Xq, sa,
                                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+quasar_status_t quasar_rmsnorm_smooth_quant(const void* X_bf16, int ldx, const void* gamma_bf16, float eps,
+                                            const float* smooth, int M, int K, int8_t* Xq, float* sa,
+                                            quasar_stream_t stream_) {
+  using namespace quasar;
+  if (M < 0 || K <= 0 || !(eps > 0.f) || !(eps < 3.0e38f)) return QUASAR_ERR_INVALID_ARG;
+  if (K % 16 != 0 || ldx < K || ldx % 8 != 0 || K > 2048 * 6) return QUASAR_ERR_UNSUPPORTED;
+  if (M == 0) return QUASAR_OK;
+  if (!X_bf16 || !gamma_bf16 || !smooth || !Xq || !sa) return QUASAR_ERR_INVALID_ARG;
+  if (!aligned(X_bf16, 16) || !aligned(gamma_bf16, 16) || !aligned(smooth, 16) || !aligned(Xq, 16) ||
+      !aligned(sa, 4))
+    return QUASAR_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(M);
+  cfg.blockDim = dim3(quant::THREADS);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream_);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const uint16_t* x = reinterpret_cast<const uint16_t*>(X_bf16);
+  const uint16_t* g = reinterpret_cast<const uint16_t*>(gamma_bf16);
+  if (K / 8 <= 2 * quant::THREADS)
+    return cuda_status(cudaLaunchKernelEx(&cfg, quant::rms_quant_kernel<2>, x, ldx, g, eps, smooth, K, Xq, sa));
+  return cuda_status(cudaLaunchKernelEx(&cfg, quant::rms_quant_kernel<6>, x, ldx, g, eps, smooth, K, Xq, sa));
 }
 
 quasar_status_t quasar_silu_mul_smooth_quant(const void* GU_bf16, int ldgu, const float* smooth, int M, int I,

@@ -44,6 +44,7 @@ _SIGS = {
     "quasar_w4a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_smooth_quant_act": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
     "quasar_silu_mul_smooth_quant": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
+    "quasar_rmsnorm_smooth_quant": (_i, [_p, _i, _p, _f, _p, _i, _i, _p, _p, _p]),
     "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_w8a8_linear_fused_workspace_size": (_sz, [_i, _i, _i]),
@@ -238,6 +239,23 @@ def smooth_quant_act(x: torch.Tensor, smooth: torch.Tensor, xq=None, sa=None, st
     sa = torch.empty(M, dtype=torch.float32, device=x.device) if sa is None else sa
     _check(lib.quasar_smooth_quant_act(_ptr(x), ldx, _ptr(smooth), M, K, _ptr(xq), _ptr(sa), _stream(stream)),
            "smooth_quant_act")
+    return xq, sa
+
+
+def rmsnorm_smooth_quant(x: torch.Tensor, gamma: torch.Tensor, smooth: torch.Tensor, eps: float = 1e-6, xq=None,
+                         sa=None, stream=None):
+    """(Xq int8 [M][K], sa fp32 [M]) of h = bf16(bf16(x * r) * gamma), r the
+    row's inverse RMS, from BF16 x [M][K], the norm's BF16 weight gamma [K]
+    and the linear's smooth [K]: RMSNorm ahead of qkv / gate_up, one launch."""
+    _need(x, torch.bfloat16, "x")
+    _need(gamma, torch.bfloat16, "gamma")
+    _need(smooth, torch.float32, "smooth")
+    ldx = _rowmajor(x, "x")
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.int8, device=x.device) if xq is None else xq
+    sa = torch.empty(M, dtype=torch.float32, device=x.device) if sa is None else sa
+    _check(lib.quasar_rmsnorm_smooth_quant(_ptr(x), ldx, _ptr(gamma), float(eps), _ptr(smooth), M, K, _ptr(xq),
+                                           _ptr(sa), _stream(stream)), "rmsnorm_smooth_quant")
     return xq, sa
 
 
