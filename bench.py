@@ -18,7 +18,9 @@ M = 1, 8, 20, the verification kernel at B=32, D=8,
 V=151936, the fused BF16 lm_head + verification at the same B, D, V, and the
 whole verification step of four decoder layers' W8A8 linears plus the lm_head
 at 288 token rows against the same chain on BF16 cuBLAS, and the MLP block at
-M = 40 (gate_up, SiLU * up with down's quantizer, down) against BF16 cuBLAS.
+M = 40 (gate_up, SiLU * up with down's quantizer, down) against BF16 cuBLAS,
+and RMSNorm + smooth + quantize in one launch against torch's RMSNorm followed
+by the quantizer.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch with torch.distributed.run; each rank runs an independent
@@ -466,6 +468,10 @@ def main_gpu(args):
         extra["lm_head"] = run_lm_head(q, dev, stream, bf16)
         extra["verification_step"] = run_verification_step(q, dev, stream, bf16)
         extra["mlp_block"] = run_mlp_block(q, dev, stream)
+        try:
+            extra["rmsnorm_quant"] = run_rmsnorm_quant(q, dev, stream)
+        except Exception as exc:                       # keep the main line if this extra fails
+            extra["rmsnorm_quant"] = {"error": f"{type(exc).__name__}: {exc}"[:200]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -709,6 +715,37 @@ def run_mlp_block(q, dev, stream):
            "launches": 4, "weight_sets": ncopy}
     del sets
     torch.cuda.empty_cache()
+    return out
+
+
+def run_rmsnorm_quant(q, dev, stream):
+    """RMSNorm + smooth + quantize ahead of qkv (Qwen3-8B hidden 4096, eps
+    1e-6) in one launch, at M = 20 and 288, against torch's BF16 RMSNorm
+    (fp32 statistics, as the usual module computes them) followed by
+    quasar_smooth_quant_act.  Inputs are L2-resident, as when the previous
+    kernel has just written them."""
+    import torch
+    K = synth.HIDDEN
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    g = (1.0 + 0.1 * torch.randn(K, device=dev, generator=gen)).to(torch.bfloat16)
+    s = torch.rand(K, device=dev, generator=gen) + 0.5
+    out = {"K": K}
+    for M in (20, 288):
+        x = torch.randn((M, K), device=dev, generator=gen).to(torch.bfloat16)
+        xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+        sa = torch.empty(M, dtype=torch.float32, device=dev)
+
+        def ours(i):
+            q.rmsnorm_smooth_quant(x, g, s, eps=1e-6, xq=xq, sa=sa)
+
+        def torch_then_quant(i):
+            xf = x.float()
+            h = (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + 1e-6)).to(torch.bfloat16) * g
+            q.smooth_quant_act(h, s, xq=xq, sa=sa)
+
+        out[f"M{M}_us"] = round(_time_graph(torch, stream, ours, 50), 2)
+        out[f"M{M}_torch_norm_plus_quant_us"] = round(_time_graph(torch, stream, torch_then_quant, 50), 2)
     return out
 
 
