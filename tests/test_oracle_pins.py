@@ -585,6 +585,19 @@ def test_silu_f32_closed_forms_and_accuracy():
     assert np.all(tail < 0) and np.all(tail > -1e-30)
 
 
+def test_silu_f32_rounding_sequence():
+    """silu(g) = g / d with d = fp32(1 + e) and ONE correctly rounded
+    division, checked in rational arithmetic on 400 BF16 gate values (a
+    reciprocal-then-multiply form rounds twice and differs on some)."""
+    g = orc.bf16_to_f32(synth.f32_to_bf16_bits(np.linspace(-20.0, 20.0, 400)))
+    g = g[g != 0]
+    e = orc.exp_f32(np.minimum(np.maximum(-g, np.float32(-87.0)), np.float32(88.0)))
+    got = orc.silu_f32(g)
+    for gi, ei, si in zip(g, e, got):
+        d = round_to_f32(1 + Fraction(float(ei)))
+        assert Fraction(float(si)) == round_to_f32(Fraction(float(gi)) / d)
+
+
 def test_silu_mul_gate_up_order_by_hand():
     """Row layout [gate | up]: silu(20) * 0.5 = 10 exactly; silu(0) * 7 = 0;
     silu(2) * -1 = -2 / (1 + e^-2) = -1.761594... -> BF16 -1.7578125 (spacing
