@@ -9,9 +9,11 @@
  *
  * Common conventions
  *  - Every pointer argument is DEVICE memory owned by the caller unless the
- *    comment says otherwise.  The library never allocates device memory and
- *    keeps no per-call state; the only library-owned device object is a
- *    32-bit error word read by quasar_get_device_error().
+ *    comment says otherwise.  No call allocates device memory and none keeps
+ *    per-call state.  The library image owns two fixed device objects, held
+ *    by every GPU that loads it until the process exits: a 32-bit error word
+ *    read by quasar_get_device_error(), and the QUASAR_NOALLOC_SCRATCH_BYTES
+ *    array used only by quasar_w8a8_linear_noalloc().
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream).  Host-side argument checks happen first; a call that
  *    fails them returns an error code and launches nothing.

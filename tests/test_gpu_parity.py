@@ -184,6 +184,41 @@ def test_silu_mul_smooth_quant_strided_and_empty():
     assert xq0.shape == (0, inter) and sa0.shape == (0,)
 
 
+def test_silu_mul_smooth_quant_against_fp64_band():
+    """The glue checked without relying on the stated fp32 exponential: on
+    gate_up-like rows at M = 40, I = 12288, h is compared (through the codes
+    and scales the kernel emits) with the fp64 silu(g) * u rounded once to
+    BF16.  An entry counts as clear when that fp64 value lies more than 1e-6
+    (relative) from a BF16 rounding midpoint, far beyond the few fp32 ulps by
+    which any faithful fp32 evaluation of silu(g) * u can differ from it.  In
+    every row whose absmax cannot move (each unclear entry of |h * smooth|
+    below 0.99 of the row maximum) the scale must equal the one computed from
+    the fp64 reference, the codes at clear entries must be equal, and at
+    unclear entries they may differ by one."""
+    M, inter = 40, 12288
+    rng = np.random.default_rng(4112)
+    a = rng.standard_normal((M, 2 * inter)) * rng.uniform(0.5, 8.0, (M, 1))
+    a[rng.integers(0, M, 64), rng.integers(0, inter, 64)] = 1000.0     # silu(g) = g
+    gu = synth.f32_to_bf16_bits(a)
+    s = np.exp(np.random.default_rng(inter).uniform(-2, 2, inter)).astype(np.float32)
+    xq, sa = q.silu_mul_smooth_quant(dev_bf16(gu), dev(s))
+    xq, sa = xq.cpu().numpy(), sa.cpu().numpy()
+
+    g = orc.bf16_to_f32(gu[:, :inter]).astype(np.float64)
+    u = orc.bf16_to_f32(gu[:, inter:]).astype(np.float64)
+    ref = orc.silu_mul_f64(g, u)
+    ref_bits = orc.f64_to_bf16(ref)
+    clear = orc.bf16_midpoint_distance(ref) > 1e-6 * np.abs(ref)
+    xq_r, sa_r = orc.smooth_quant_act(ref_bits, s)
+    v = np.abs(orc.bf16_to_f32(ref_bits).astype(np.float64) * s[None, :])
+    decidable = np.array([np.all(v[m, ~clear[m]] < 0.99 * v[m].max()) for m in range(M)])
+    assert decidable.mean() >= 0.9, decidable.mean()
+    for m in np.flatnonzero(decidable):
+        assert sa[m].view(np.uint32) == sa_r[m].view(np.uint32), m
+        assert np.array_equal(xq[m, clear[m]], xq_r[m, clear[m]]), m
+        assert np.abs(xq[m].astype(np.int32) - xq_r[m].astype(np.int32)).max() <= 1, m
+
+
 def test_mlp_block_chain():
     """The Qwen3-8B MLP block at M = 40 (8 sequences x (4 drafts + 1)), all on
     the GPU: gate_up W8A8 linear -> SiLU(gate) * up + smooth + quantize -> down
@@ -447,13 +482,26 @@ def test_verify_greedy_random(B, D, V):
     lg, draft, mask, _ = synth.verify_inputs(B, D, V, 501, 502, 503, 504)
     am = np.argmax(orc.bf16_to_f32(lg), axis=2)
     d = np.where(mask, am[:, :D], draft).astype(np.int32)
-    # plant ties: copy the max to a later and to an earlier index in some rows
-    for b in range(0, B, 3):
-        j = 0
-        k = int(am[b, j])
-        lg[b, j, (k + 7) % V] = lg[b, j, k]
+    # plant ties on row 0: copy the max to a later index (rows b = 0 mod 3:
+    # the argmax stays put) or to an earlier one (rows b = 1 mod 3: the
+    # earlier copy becomes the first-index argmax, and the draft is left on
+    # the old maximum, which the lowest-index rule must now reject)
+    late = list(range(0, B, 3))
+    early = [b for b in range(1, B, 3) if int(am[b, 0]) >= 7]
+    for b in late:
+        k = int(am[b, 0])
+        lg[b, 0, (k + 7) % V] = lg[b, 0, k]
+    for b in early:
+        k = int(am[b, 0])
+        lg[b, 0, k - 7] = lg[b, 0, k]
+    old_am = am
     am = np.argmax(orc.bf16_to_f32(lg), axis=2)
+    for b in early:
+        assert am[b, 0] == old_am[b, 0] - 7
     d = np.where(mask, am[:, :D], d).astype(np.int32)
+    if D > 0:
+        for b in early:
+            d[b, 0] = old_am[b, 0]          # a tied maximum, not the first one
     ws = q.Workspace()
     Vp = (V + 7) // 8 * 8            # row stride must be a multiple of 8 elements
     padded = np.zeros((B, D + 1, Vp), np.uint16)

@@ -50,7 +50,7 @@
 #include "quasar_common.cuh"
 
 namespace quasar {
-namespace skinny {  // w8a8_skinny.cu: the register-path kernel for M <= 32
+namespace skinny {  // w8a8_skinny.cu: the register-path kernel, M <= 24 (skinny::handles)
 bool handles(int M);
 size_t slots_bytes(int M, int N, int K);
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,

@@ -16,10 +16,12 @@
 // runs at ~2048 flop/clk/SM on sm_103a and takes its weight operand straight
 // from registers: at M <= 8 it covers 128 weight bytes per cycle, at M = 32
 // still 32, against the ~22 bytes per cycle an SM must stream for HBM-rate.
-// So for M <= 32 the weights go HBM -> shared memory (1-D bulk copies of the
-// same packed blocks the tcgen05 kernel reads) -> registers (ldmatrix) ->
+// So for a few tokens the weights go HBM -> shared memory (1-D bulk copies of
+// the same packed blocks the tcgen05 kernel reads) -> registers (ldmatrix) ->
 // fp16 (exact) -> mma.sync, with fp32 accumulators that stay exact integers
-// (see RUN_BLOCKS), and the tcgen05 kernel keeps the larger M.
+// (see RUN_BLOCKS).  Measured, this path is the faster one up to 24 tokens
+// (handles() below is the one place that sets the split); the tcgen05 kernel
+// takes larger M.
 //
 // Work units.  A unit is 64 weight rows (half of a packed 128-row tile: its
 // blocks are contiguous 8 KB halves of the 16 KB packed blocks) over all of
