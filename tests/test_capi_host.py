@@ -65,8 +65,10 @@ def test_workspace_sizes(lib):
     assert lib.quasar_packed_weight_bytes(136, 144) == 2 * 2 * 16384
     assert ws(0, 6144, 4096) == 0
     assert ws(256, 4096, 4096) >= 256 * 4096 * 4
-    # >= 128 weight tiles at 96/128-token tiles: + the fp16 token copy M x K x 2
-    assert ws(256, 24576, 4096) == 192 * 2 * 16 * 4 + 256 * 24576 * 4 + 256 * 4096 * 2
+    # token tiles of >= 128 rows: + the fp16 token copy M x K x 2, and the
+    # counters sized for the 64-row fallback tiles (4 x 192 tiles x 16 warps)
+    assert ws(256, 24576, 4096) == 4 * 192 * 16 * 4 + 256 * 24576 * 4 + 256 * 4096 * 2
+    assert ws(128, 6144, 4096) == 2 * 48 * 16 * 4 + 128 * 6144 * 4 + 128 * 4096 * 2
     assert lib.quasar_calibrate_workspace_size(4096) == 8 * 4096
     assert lib.quasar_verify_accept_workspace_size(32, 8, 151936) > 0
     assert lib.quasar_verify_accept_workspace_size(0, 8, 151936) == 0

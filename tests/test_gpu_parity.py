@@ -295,11 +295,17 @@ def test_pack_and_tile_ragged(N, K):
 
 # ---------------------------------------------------------------- A3 exact integer GEMM
 
+# Token tiles of 16 / 32 / 64 rows (tokens widened inside the kernel), 128 /
+# 144 rows (the fp16 token copy by TMA and the converters' register split),
+# two 144-row tiles at 257-288 tokens and 128-row tiles otherwise above 144;
+# the work split (K parts per tile, whole tiles, or stream-K ranges) follows
+# the tile count, so these shapes take each of them.
 SHAPES = [
     (1, 8, 16), (5, 136, 144), (8, 512, 256), (16, 128, 1024), (17, 264, 1040), (20, 384, 4096),
     (33, 256, 2048), (64, 640, 1152), (65, 128, 384), (128, 256, 512), (130, 136, 272), (256, 512, 1024),
-    (192, 1000, 2064), (288, 640, 4096), (200, 136, 272),   # 96-token tiles
-    (130, 16384, 1040), (256, 16392, 256),                  # tokens pre-widened to fp16 (>= 128 weight tiles)
+    (192, 1000, 2064), (288, 640, 4096), (200, 136, 272), (145, 520, 1040), (300, 272, 2064),
+    (512, 264, 1024), (129, 6144, 4096), (256, 4096, 12288),
+    (130, 16384, 1040), (256, 16392, 256),
 ]
 
 
@@ -315,7 +321,8 @@ def test_int8_gemm_bit_exact(M, N, K):
 
 
 @pytest.mark.parametrize("M,K,N", [(24, 1024, 256), (24, 4096, 256), (24, 12288, 256), (64, 4096, 256),
-                                   (40, 12288, 256), (256, 4096, 256), (288, 12288, 256), (288, 4096, 16384)])
+                                   (40, 12288, 256), (256, 4096, 256), (256, 12288, 256), (144, 4096, 256),
+                                   (288, 12288, 256), (288, 4096, 16384)])
 def test_int8_gemm_adversarial_extremes(M, K, N):
     """All products at +-127^2: every fp32 accumulation run sits at its exactness limit
     (N = 16384: the path that takes the tokens pre-widened to fp16)."""

@@ -265,6 +265,17 @@ QUASAR_DEVICE_INLINE void tmem_ld8(uint32_t taddr, uint32_t* r) {
                : "memory");
 }
 
+// Load 16 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+QUASAR_DEVICE_INLINE void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // Load 32 consecutive 32-bit columns of this warp's 32 TMEM lanes.
 QUASAR_DEVICE_INLINE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -277,6 +288,15 @@ QUASAR_DEVICE_INLINE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
+
+// Per-warpgroup register budget (every warp of a warpgroup executes these
+// together).  `dec` returns registers to the CTA's pool, `inc` waits until the
+// pool can grant the increase: a split must never ask for more than the
+// warpgroups give back, or the increase waits forever.
+template <int N>
+QUASAR_DEVICE_INLINE void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+QUASAR_DEVICE_INLINE void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
 // ---- bit helpers ---------------------------------------------------------------
 

@@ -72,43 +72,69 @@ constexpr int CONV_WARPS = 16;
 constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
 constexpr int WAITER_WARP = 18;
-constexpr int THREADS = 32 * (CONV_WARPS + 3);
 constexpr int MMA_BAR_ID = 1;   // named barrier pairing the MMA and waiter warps
+constexpr int CONV_BAR_ID = 2;  // named barrier of the converter warps
 constexpr int TMEM_COLS = 512;
 constexpr int BLOCK_BYTES = BM * BK;   // one packed weight block
+constexpr int SMEM_OPTIN = 232448;     // shared memory a block may opt into
 
-// XH: the token codes arrive already widened to fp16 (one copy per call in
-// the workspace) and are copied by TMA straight into the MMA's B layout;
-// the converters then widen only the weights, and the INT8 ring carries
-// weight blocks alone.
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A/B fp16
+// (format 0), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+template <int NT>
+__host__ __device__ constexpr uint32_t idesc() {
+  return (1u << 4) | (uint32_t(NT >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+}
+
+// NT: token rows of one tile (the MMA's N).  XH: the token codes arrive
+// already widened to fp16 (one copy per call in the workspace, or written by
+// the quantizer of the one-call entry) and are copied by TMA straight into
+// the MMA's B layout; the converters then widen only the weights, and the
+// INT8 ring carries weight blocks alone.
 template <int NT, bool XH = false>
 struct Cfg {
+  // Wide tiles (NT >= 128) keep NT/4 int32 run sums per converter thread.
+  // A fifth warpgroup (copy, MMA, waiter and one spare warp) lets the block
+  // move registers from those warps to the converters (setmaxnreg): launched
+  // at REGS_LAUNCH per thread, the converters rise to REGS_CONV and the
+  // fifth warpgroup drops to REGS_AUX, which gives back exactly what the
+  // converters take.  The host checks the launch count before using it.
+  static constexpr bool WIDE = NT >= 128;
+  static constexpr int WARPS = CONV_WARPS + (WIDE ? 4 : 3);
+  static constexpr int THREADS = 32 * WARPS;
+  static constexpr int REGS_LAUNCH = 96;
+  static constexpr int REGS_CONV = 104;
+  static constexpr int REGS_AUX = 64;
   // Blocks per pipeline stage: two 128-K blocks per handshake halve the
   // per-byte cost of the barrier round trips; NT >= 96 keeps one (TMEM).
   static constexpr int G = (NT >= 96) ? 1 : 2;
-  static constexpr int S2 = (NT >= 96) ? 3 : (NT == 64) ? 2 : 3;    // converted stages (TMEM A + smem B)
+  static constexpr int A_COLS = G * BK / 2;                  // TMEM columns per A stage (fp16 pairs)
+  // Accumulators in TMEM: two (a run drains while the next accumulates)
+  // unless the tile is too wide to leave room for the A stages.
+  static constexpr int NACC = (2 * NT + 2 * A_COLS <= TMEM_COLS) ? 2 : 1;
+  static constexpr int TMEM_A0 = NACC * NT;                  // A stages follow the accumulators
+  // Converted stages (TMEM A + shared-memory B) and INT8 stages, sized so
+  // that the operand bytes in flight cover the copy latency at each width.
+  static constexpr int S2 = XH ? (NT == 144 ? 3 : NT == 128 ? 4 : 2) : (NT == 64 ? 2 : 3);
   static constexpr int W_BYTES = G * BLOCK_BYTES;            // INT8 weight blocks of a stage
   static constexpr int XB_BYTES = XH ? 0 : NT * BK;          // INT8 token tile of one block
   static constexpr int STAGE1 = W_BYTES + G * XB_BYTES;      // multiple of 1024
   static constexpr int B16_BLOCK = NT * BK * 2;              // fp16 token tile of one block (2 atoms)
   static constexpr int B16_BYTES = G * B16_BLOCK;
-  // INT8 stages: as many as the shared memory holds next to the converted
-  // stages (the pipeline is bound by copies in flight), at most 5.
-  static constexpr int S1_FIT = (232448 - 1024 - 256 - S2 * G * NT * BK * 2) / (G * (BM * BK + XB_BYTES));
-  static constexpr int S1 = XH ? (S1_FIT < 8 ? S1_FIT : 8)
-                               : (NT == 16) ? 5 : (NT == 32) ? 4 : (NT == 64) ? 3 : (S1_FIT < 5 ? S1_FIT : 5);
-  static constexpr int A_COLS = G * BK / 2;                  // TMEM columns per A stage (fp16 pairs)
-  static constexpr int TMEM_A0 = 2 * NT;                     // A stages follow two accumulators
+  static constexpr int S1_FIT = (SMEM_OPTIN - 1024 - 256 - S2 * B16_BYTES) / STAGE1;
+  static constexpr int S1 = XH ? (S1_FIT < 8 ? S1_FIT : 8) : (NT == 16) ? 5 : (NT == 32) ? 4 : 3;
   static constexpr int TOK = NT / 4;                         // accumulator columns per converter thread
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = 1024 + S1 * STAGE1 + S2 * B16_BYTES + BAR_BYTES;
   static_assert(RUN_MAX % G == 0, "stages never straddle an accumulation run");
   static_assert(TMEM_A0 + S2 * A_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(STAGE1 % 1024 == 0 && B16_BLOCK % 1024 == 0, "1024B alignment of swizzled tiles");
-  static_assert(SMEM <= 232448, "shared memory budget");
-  // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A/B fp16
-  // (format 0), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-  static constexpr uint32_t IDESC = (1u << 4) | (uint32_t(NT >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+  static_assert(S1 >= 2 && S2 >= 2, "pipeline depth");
+  static_assert(BM * NT * 4 <= S1 * STAGE1, "a cluster's partial sums fit over the INT8 ring");
+  static_assert(SMEM <= SMEM_OPTIN, "shared memory budget");
+  static_assert(NT % 16 == 0 && NT <= 144 && TOK % 4 == 0, "MMA N");
+  static_assert(!WIDE || XH, "wide tiles take the fp16 token copy");
+  static_assert(!WIDE || (CONV_WARPS * 32 * (REGS_CONV - REGS_LAUNCH) <= 4 * 32 * (REGS_LAUNCH - REGS_AUX)),
+                "register split: the converters never take more than the fifth warpgroup returns");
 };
 
 struct Params {
@@ -120,6 +146,9 @@ struct Params {
   int m_tiles;     // token tiles of NT
   int tiles;       // n_tiles * m_tiles
   int total;       // tiles * KB
+  int tile_ranges; // 1: each CTA takes whole tiles (a contiguous run of them), never part of one
+  int csize;       // > 1: thread-block clusters of csize CTAs, one per tile, each CTA a K part;
+                   // the parts are summed through distributed shared memory
   __nv_bfloat16* Y;
   int ldy;
   int32_t* acc_out;   // int32 mode when non-null
@@ -202,25 +231,42 @@ QUASAR_DEVICE_INLINE void mma_burst4(uint32_t d_tmem, uint32_t a_tmem, uint64_t 
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %4, t;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %4, t;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %4, t;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem + (K0 + 0) * 8), "l"(bdesc + o0), "r"(acc0), "r"(Cfg<NT>::IDESC),
+      ::"r"(d_tmem), "r"(a_tmem + (K0 + 0) * 8), "l"(bdesc + o0), "r"(acc0), "r"(idesc<NT>()),
       "r"(a_tmem + (K0 + 1) * 8), "l"(bdesc + o1), "r"(a_tmem + (K0 + 2) * 8), "l"(bdesc + o2),
       "r"(a_tmem + (K0 + 3) * 8), "l"(bdesc + o3)
       : "memory");
 }
 
-template <int NT>
-QUASAR_DEVICE_INLINE void drain_acc(uint32_t taddr, int32_t (&acc)[NT / 4]) {
-  // NT/4 fp32 accumulator columns, each an exact integer: convert and add.
-  uint32_t v[NT / 4];
-  if constexpr (NT / 4 == 4) {
-    tmem_ld4(taddr, v);
-  } else {
+// TOK fp32 accumulator columns of this thread's TMEM lane, each an exact
+// integer: convert and add to the int32 run sums, 16 columns per load (then
+// 8 and 4 for the tail) so that the temporaries stay small next to the sums
+// (measured: two loads per wait spilled at wide tiles and ran slower).
+template <int TOK>
+QUASAR_DEVICE_INLINE void drain_acc(uint32_t taddr, int32_t (&acc)[TOK]) {
 #pragma unroll
-    for (int g = 0; g < NT / 32; ++g) tmem_ld8(taddr + g * 8, v + g * 8);
+  for (int c = 0; c + 16 <= TOK; c += 16) {
+    uint32_t v[16];
+    tmem_ld16(taddr + c, v);
+    tc_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[c + j] += __float2int_rn(__uint_as_float(v[j]));
   }
-  tc_wait_ld();
+  constexpr int T1 = TOK & ~15;
+  if constexpr ((TOK & 8) != 0) {
+    uint32_t v[8];
+    tmem_ld8(taddr + T1, v);
+    tc_wait_ld();
 #pragma unroll
-  for (int j = 0; j < NT / 4; ++j) acc[j] += __float2int_rn(__uint_as_float(v[j]));
+    for (int j = 0; j < 8; ++j) acc[T1 + j] += __float2int_rn(__uint_as_float(v[j]));
+  }
+  constexpr int T2 = TOK & ~7;
+  if constexpr ((TOK & 4) != 0) {
+    uint32_t v[4];
+    tmem_ld4(taddr + T2, v);
+    tc_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[T2 + j] += __float2int_rn(__uint_as_float(v[j]));
+  }
 }
 
 // A finished accumulation run whose TMEM sums still have to be drained, and
@@ -236,22 +282,23 @@ struct PendingRun {
 // Drain run `pr.R` from TMEM into the int32 registers; if it closes a
 // segment, publish / finish the segment (see the file comment) and clear the
 // registers.  Returns false if a bounded wait ran out.
-template <int NT>
+template <int NT, int NACC>
 QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4], uint64_t* empty2,
                                      uint64_t* accempty, uint32_t tmem_lane, int h, volatile int* abort_flag,
                                      const Params& p, int warp, int lane, int row, int KB, int m_tiles) {
   constexpr int TOK = NT / 4;
-  const int a = pr.R & 1;
+  const int a = pr.R % NACC;
   // The commit that frees the run's last stage tracks every MMA issued
   // before it, i.e. the whole run: its completion means the sums are final.
   const bool okf = mbar_wait(&empty2[pr.s2], pr.ph2, abort_flag, p.err, SITE_GEMM_ACCFULL, p.limit_ns);
   if (!__all_sync(0xffffffffu, okf)) return false;
   tc_fence_after();
-  drain_acc<NT>(tmem_lane + (uint32_t)(a * NT + h * TOK), acc);
+  drain_acc<TOK>(tmem_lane + (uint32_t)(a * NT + h * TOK), acc);
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(&accempty[a]);
   if (!pr.flush) return true;
+  if (p.csize > 1) return true;   // summed across the cluster after the loop
 
   const int t = pr.t;
   const int n = (t / m_tiles) * BM + row;
@@ -277,6 +324,9 @@ QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4
     }
     emit = __shfl_sync(0xffffffffu, last, 0) != 0;
     if (emit) {
+      // Every contribution is in L2 now: take the sums and leave zeros for
+      // the next call in one atomic exchange each (measured faster than plain
+      // loads followed by plain stores).
       __threadfence();
       if (n < p.N) {
 #pragma unroll
@@ -307,10 +357,83 @@ QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4
   return true;
 }
 
-template <int NT, bool XH = false>
-__global__ void __launch_bounds__(THREADS, 1)
-w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
+// Cluster-wide barrier of every thread of the cluster: with release /
+// acquire ordering of shared-memory writes (full), or ordering execution
+// only (exec: the remote loads it follows have returned their values).
+QUASAR_DEVICE_INLINE void cluster_barrier_full() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+QUASAR_DEVICE_INLINE void cluster_barrier_exec() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// int4 at the same shared-memory offset in cluster CTA `rank`.
+QUASAR_DEVICE_INLINE int4 ld_cluster_int4(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  int4 v;
+  asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
+// Cluster phase of a split tile (csize CTAs, one K part each): every CTA has
+// left its int32 sums in `part` ([NT token columns][128 weight rows]); CTA
+// `rank` finishes rows [4 u0, 4 u1) of the tile, reading the other parts
+// through distributed shared memory, and writes them (dequantized, or the
+// int32 sums).  Four consecutive rows per item: one 16-byte load per part and
+// consecutive threads on consecutive rows of Y.
+template <int NT>
+QUASAR_DEVICE_INLINE void cluster_finalize(const Params& p, const int32_t* part, int t, int rank, int ct) {
+  const int csize = p.csize;
+  const int u0 = rank * (BM / 4) / csize, u1 = (rank + 1) * (BM / 4) / csize;
+  const int nu = u1 - u0;
+  const int n_base = (t / p.m_tiles) * BM;
+  const int m_base = (t % p.m_tiles) * NT;
+  for (int i = ct; i < nu * NT; i += CONV_WARPS * 32) {
+    const int col = i / nu;
+    const int u = u0 + (i - col * nu);
+    const int m = m_base + col;
+    const int n = n_base + 4 * u;
+    if (m >= p.M || n >= p.N) continue;
+    int4 v = make_int4(0, 0, 0, 0);
+    for (int q = 0; q < csize; ++q) {
+      const int4 x = ld_cluster_int4(part + col * BM + 4 * u, (uint32_t)q);
+      v.x += x.x;
+      v.y += x.y;
+      v.z += x.z;
+      v.w += x.w;
+    }
+    if (p.acc_out) {
+      *reinterpret_cast<int4*>(p.acc_out + (size_t)m * p.N + n) = v;
+    } else {
+      const float sam = p.sa[m];
+      const float y0 = __fmul_rn(__fmul_rn(__int2float_rn(v.x), sam), p.sw[n]);
+      const float y1 = __fmul_rn(__fmul_rn(__int2float_rn(v.y), sam), p.sw[n + 1]);
+      const float y2 = __fmul_rn(__fmul_rn(__int2float_rn(v.z), sam), p.sw[n + 2]);
+      const float y3 = __fmul_rn(__fmul_rn(__int2float_rn(v.w), sam), p.sw[n + 3]);
+      const __nv_bfloat162 lo = __halves2bfloat162(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+      const __nv_bfloat162 hi = __halves2bfloat162(__float2bfloat16_rn(y2), __float2bfloat16_rn(y3));
+      uint2 out;
+      out.x = *reinterpret_cast<const uint32_t*>(&lo);
+      out.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(p.Y + (size_t)m * p.ldy + n) = out;
+    }
+  }
+}
+
+// Which warp roles one copy of the kernel body contains: all of them, or
+// (wide tiles, after the register split) the converters or the other warps
+// alone, so that each copy is compiled under its own register limit.
+enum Roles { ROLES_ALL = 0, ROLES_CONV = 1, ROLES_AUX = 2 };
+
+template <int NT, bool XH, int ROLES>
+QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
   using C = Cfg<NT, XH>;
+  constexpr bool CONV = ROLES != ROLES_AUX;   // this copy runs the converter warps
+  constexpr bool AUX = ROLES != ROLES_CONV;   // this copy runs the copy / MMA / waiter warps
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage1 = smem;                                  // S1 x [W 16KB | X NT*128]
@@ -320,7 +443,7 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   uint64_t* empty1 = full1 + C::S1;           // [S1] converters -> producer
   uint64_t* full2 = empty1 + C::S1;           // [S2] converters -> MMA
   uint64_t* empty2 = full2 + C::S2;           // [S2] MMA -> converters
-  uint64_t* accempty = empty2 + C::S2;        // [2]  drain -> MMA
+  uint64_t* accempty = empty2 + C::S2;        // [NACC] drain -> MMA
   uint64_t* mma_done = accempty + 2;          // [1]  final MMA drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -331,20 +454,20 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   // Let the next kernel in the stream be scheduled onto SMs as they free up.
   pdl_launch_dependents();
 
-  if (threadIdx.x == 0) {
+  if (CONV && threadIdx.x == 0) {
     for (int s = 0; s < C::S1; ++s) { mbar_init(&full1[s], 1); mbar_init(&empty1[s], CONV_WARPS); }
     // XH: the producer's fp16 token copy is one more arrival (with its bytes)
     for (int s = 0; s < C::S2; ++s) { mbar_init(&full2[s], CONV_WARPS + (XH ? 1 : 0)); mbar_init(&empty2[s], 1); }
-    for (int a = 0; a < 2; ++a) mbar_init(&accempty[a], CONV_WARPS);
+    for (int a = 0; a < C::NACC; ++a) mbar_init(&accempty[a], CONV_WARPS);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == MMA_WARP) {
+  if (AUX && warp == MMA_WARP) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == PRODUCER_WARP && lane == 0) prefetch_tmap(&tmX);
+  if (AUX && warp == PRODUCER_WARP && lane == 0) prefetch_tmap(&tmX);
   const uint32_t xtx = XH ? (uint32_t)C::B16_BLOCK : 0u;  // bytes of one block's fp16 token tile
   tc_fence_before();
   __syncthreads();
@@ -352,12 +475,14 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   const uint32_t tmem = *tmem_slot;
 
   // This CTA's contiguous range of (tile, K block) work items.
-  const int b0 = (int)((long long)blockIdx.x * p.total / gridDim.x);
-  const int b1 = (int)((long long)(blockIdx.x + 1) * p.total / gridDim.x);
+  const int b0 = p.tile_ranges ? (int)((long long)blockIdx.x * p.tiles / gridDim.x) * p.KB
+                               : (int)((long long)blockIdx.x * p.total / gridDim.x);
+  const int b1 = p.tile_ranges ? (int)((long long)(blockIdx.x + 1) * p.tiles / gridDim.x) * p.KB
+                               : (int)((long long)(blockIdx.x + 1) * p.total / gridDim.x);
   const int KB = p.KB;
   const int m_tiles = p.m_tiles;
 
-  if (warp == PRODUCER_WARP) {
+  if (AUX && warp == PRODUCER_WARP) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
@@ -423,7 +548,12 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         mbar_wait(&full2[s], (uint32_t)(last / C::S2) & 1u, &dummy, p.err, SITE_GEMM_DRAIN, p.limit_ns);
       }
     }
-  } else if (warp == MMA_WARP || warp == WAITER_WARP) {
+    __syncwarp();
+    if (p.csize > 1) {
+      cluster_barrier_full();
+      cluster_barrier_exec();
+    }
+  } else if (AUX && (warp == MMA_WARP || warp == WAITER_WARP)) {
     // Any memory access by the thread that issues tcgen05.mma waits until
     // its queued MMAs have been accepted by the tensor pipe, so a barrier
     // wait between stages would drain the pipe.  The waiter warp therefore
@@ -441,8 +571,9 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       uint32_t abort_in = 0;
       if (warp == WAITER_WARP) {
         bool ok = true;
-        if (run_first && R >= 2)
-          ok = mbar_wait(&accempty[R & 1], ((R >> 1) - 1) & 1, abort_flag, p.err, SITE_GEMM_ACCEMPTY, p.limit_ns);
+        if (run_first && R >= C::NACC)
+          ok = mbar_wait(&accempty[R % C::NACC], (uint32_t)((R / C::NACC) - 1) & 1u, abort_flag, p.err,
+                         SITE_GEMM_ACCEMPTY, p.limit_ns);
         ok = ok && mbar_wait(&full2[rg.s], rg.ph, abort_flag, p.err, SITE_GEMM_FULL2, p.limit_ns);
         abort_in = __all_sync(0xffffffffu, ok) ? 0u : 1u;
       }
@@ -450,7 +581,7 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       if (warp == MMA_WARP) {
         if (lane == 0) {
           tc_fence_after();
-          const uint32_t d_tmem = tmem + (uint32_t)((R & 1) * NT);
+          const uint32_t d_tmem = tmem + (uint32_t)((R % C::NACC) * NT);
           const uint32_t a_tmem = tmem + (uint32_t)(C::TMEM_A0 + rg.s * C::A_COLS);
           const uint64_t bdesc = bdesc0 + (uint64_t)((rg.s * C::B16_BYTES) >> 4);
           const uint32_t acc0 = run_first ? 0u : 1u;
@@ -474,7 +605,12 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       volatile int dummy = 0;
       mbar_wait(mma_done, 0, &dummy, p.err, SITE_GEMM_DRAIN, p.limit_ns);
     }
-  } else {
+    __syncwarp();
+    if (p.csize > 1) {
+      cluster_barrier_full();
+      cluster_barrier_exec();
+    }
+  } else if (CONV && warp < CONV_WARPS) {
     // ---------------------------------------------------------------- converters
     const int q = warp & 3;       // TMEM lane quadrant = weight rows 32q..32q+31
     const int h = warp >> 2;      // K quarter of each A block; token quarter of the accumulator
@@ -551,8 +687,8 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       // Drain the run finished one stage ago (its MMAs have had a whole
       // stage to complete), then remember this stage's run if it ends here.
       if (pend.R >= 0) {
-        if (!finish_run<NT>(pend, acc, empty2, accempty, tmem + lane_off, h, abort_flag, p, warp, lane, row, KB,
-                            m_tiles))
+        if (!finish_run<NT, C::NACC>(pend, acc, empty2, accempty, tmem + lane_off, h, abort_flag, p, warp, lane,
+                                     row, KB, m_tiles))
           break;
         pend.R = -1;
       }
@@ -567,27 +703,70 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       }
     }
     if (pend.R >= 0)
-      finish_run<NT>(pend, acc, empty2, accempty, tmem + lane_off, h, abort_flag, p, warp, lane, row, KB, m_tiles);
+      finish_run<NT, C::NACC>(pend, acc, empty2, accempty, tmem + lane_off, h, abort_flag, p, warp, lane, row, KB,
+                              m_tiles);
+    __syncwarp();
+    if (p.csize > 1) {
+      // Split tile of a cluster: this CTA's part of the sums goes to shared
+      // memory (over the INT8 ring, idle once every converter warp is past
+      // its last block), then the cluster adds the parts.
+      int32_t* part = reinterpret_cast<int32_t*>(stage1);
+      named_barrier_or(CONV_BAR_ID, CONV_WARPS * 32, 0u);
+#pragma unroll
+      for (int jj = 0; jj < C::TOK; ++jj) part[(h * C::TOK + jj) * BM + row] = acc[jj];
+      cluster_barrier_full();
+      cluster_finalize<NT>(p, part, b0 / KB, (int)(blockIdx.x % (unsigned)p.csize), ct);
+      cluster_barrier_exec();
+    }
+  } else if (p.csize > 1) {
+    // the spare warp of the fifth warpgroup
+    cluster_barrier_full();
+    cluster_barrier_exec();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == MMA_WARP) {
+  if (AUX && warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
+template <int NT, bool XH = false>
+__global__ void __launch_bounds__(Cfg<NT, XH>::THREADS, 1)
+w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
+  using C = Cfg<NT, XH>;
+  if constexpr (C::WIDE) {
+    // Move registers from the fifth warpgroup to the converters before
+    // anything else runs (warpgroup-uniform: warps 0-15 and 16-19); each
+    // side then runs its own copy of the body under its own limit.
+    if ((threadIdx.x >> 5) < CONV_WARPS) {
+      regs_inc<C::REGS_CONV>();
+      linear_body<NT, XH, ROLES_CONV>(tmX, p);
+    } else {
+      regs_dec<C::REGS_AUX>();
+      linear_body<NT, XH, ROLES_AUX>(tmX, p);
+    }
+  } else {
+    linear_body<NT, XH, ROLES_ALL>(tmX, p);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 
-// Token tile: the smallest of 16 / 32 / 64 that holds M, else 128 -- or 96
-// above 128 tokens when three-quarter tiles pad less (288 = 3 x 96 instead of
-// 2 x 128 + a quarter-full third tile).
+// Token tile: the smallest of 16 / 32 / 64 / 128 / 144 rows that holds M,
+// so that up to 144 tokens every weight block is widened once per launch and
+// meets all tokens in one accumulator; above, tiles of 128 rows, or 144 for
+// 257-288 tokens (32 sequences x 9 positions: two tiles, not three).  A
+// single 256-row tile was built and measured: its 64 run sums per converter
+// thread spill, and it ran no faster than two 128-row tiles.
 static int pick_nt(int M) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
-  if (M > 128 && 96 * ((M + 95) / 96) < 128 * ((M + 127) / 128)) return 96;
+  if (M <= 128) return 128;
+  if (M <= 144) return 144;
+  if (M > 256 && M <= 288) return 144;
   return 128;
 }
 
@@ -595,9 +774,9 @@ struct Shape {
   int NT, m_tiles, n_tiles, tiles, KB;
 };
 
-static Shape shape_of(int M, int N, int K) {
+static Shape shape_with(int M, int N, int K, int nt) {
   Shape s;
-  s.NT = pick_nt(M);
+  s.NT = nt;
   s.m_tiles = (M + s.NT - 1) / s.NT;
   s.n_tiles = (N + BM - 1) / BM;
   s.tiles = s.n_tiles * s.m_tiles;
@@ -605,24 +784,32 @@ static Shape shape_of(int M, int N, int K) {
   return s;
 }
 
+static Shape shape_of(int M, int N, int K) { return shape_with(M, N, K, pick_nt(M)); }
+
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Token tiles of 96 or 128 on layers of at least 128 weight tiles (N >= 16384):
-// the tokens are widened to fp16 once per call (an M x K copy in the
-// workspace, one extra launch and a clearing memset) instead of once per
-// weight tile inside the kernel.  Measured: gate_up 24576 x 4096 at M = 256
-// 95.5 -> 85.3 us; the widening launch costs more than it saves on layers of
-// 32-48 tiles (qkv, o_proj, down lose 0.5-2.5 us), so those keep the in-kernel path.
-static bool use_xh(int M, const Shape& s) { return !skinny::handles(M) && s.NT >= 96 && s.n_tiles >= 128; }
+// Tiles of 128 rows and more always take the fp16 token copy: widening the
+// tokens inside the kernel would cost the converters more than the weights
+// per block.  Through quasar_w8a8_linear the copy is made by one small
+// launch into the workspace (and cleared afterwards); the one-call entry's
+// quantizer writes it directly.
+static bool use_xh(int M, const Shape& s) { return !skinny::handles(M) && s.NT >= 128; }
+
+// Counter region: one counter per (tile, converter warp), sized for the
+// 64-row fallback of wide tiles too so that both use the same layout.
+static size_t cnt_bytes(int M, int N, int K) {
+  const Shape s = shape_of(M, N, K);
+  const int tiles = std::max(s.tiles, shape_with(M, N, K, std::min(s.NT, 64)).tiles);
+  return align256((size_t)tiles * CONV_WARPS * 4);
+}
 
 size_t workspace_size(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   Shape s = shape_of(M, N, K);
   // counters, then the int32 split-K sums of this kernel or the partial-sum
-  // slots of the register-path kernel, then (96/128-token tiles) the fp16
+  // slots of the register-path kernel, then (tiles of >= 128 rows) the fp16
   // token copy
-  return align256((size_t)s.tiles * CONV_WARPS * 4) +
-         align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K))) +
+  return cnt_bytes(M, N, K) + align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K))) +
          (use_xh(M, s) ? align256((size_t)M * K * 2) : 0);
 }
 
@@ -644,28 +831,171 @@ __global__ void __launch_bounds__(256) widen_tokens_kernel(const int8_t* __restr
   }
 }
 
-template <int NT, bool XH = false>
-static cudaError_t launch_nt(const CUtensorMap& tx, const Params& p, int grid, cudaStream_t stream) {
+// Wide variants rely on the block's register split: the launch count must
+// leave the converters' increase covered by what the fifth warpgroup gives
+// back.  Checked once per device against the compiled kernel; 0 = usable.
+template <int NT, bool XH>
+static cudaError_t check_split(int dev) {
+  using C = Cfg<NT, XH>;
+  if constexpr (!C::WIDE) {
+    return cudaSuccess;
+  } else {
+    static int state[64] = {0};   // 0 unknown, 1 usable, 2 not usable
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!state[dev]) {
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_linear_kernel<NT, XH>);
+      if (e != cudaSuccess) return e;
+      const int r = fa.numRegs;
+      const bool ok = r >= C::REGS_AUX && r <= C::REGS_CONV &&
+                      (long long)CONV_WARPS * 32 * (C::REGS_CONV - r) <= (long long)4 * 32 * (r - C::REGS_AUX);
+      state[dev] = ok ? 1 : 2;
+    }
+    return state[dev] == 1 ? cudaSuccess : cudaErrorNotSupported;
+  }
+}
+
+template <int NT, bool XH>
+static cudaError_t configure(int dev) {
   static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(w8a8_linear_kernel<NT, XH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<NT, XH>::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
+  return check_split<NT, XH>(dev);
+}
+
+template <int NT, bool XH>
+static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(Cfg<NT, XH>::THREADS);
   cfg.dynamicSmemBytes = Cfg<NT, XH>::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)csize;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = csize > 1 ? 2 : 1;
+  return cfg;
+}
+
+// Clusters of `csize` CTAs of this variant the device keeps resident at once
+// (0 if unknown); cached per device and size.
+template <int NT, bool XH>
+static int resident_clusters(int dev, int csize) {
+  static int cache[64][5];
+  static bool init[64][5] = {};
+  if (dev < 0 || dev >= 64 || csize < 2 || csize > 4) return 0;
+  if (!init[dev][csize]) {
+    int n = 0;
+    if (configure<NT, XH>(dev) == cudaSuccess) {
+      cudaLaunchAttribute attr[2];
+      cudaLaunchConfig_t cfg = config_of<NT, XH>(csize * 8, csize, nullptr, attr);
+      if (cudaOccupancyMaxActiveClusters(&n, w8a8_linear_kernel<NT, XH>, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cache[dev][csize] = n;
+    init[dev][csize] = true;
+  }
+  return cache[dev][csize];
+}
+
+template <int NT, bool XH = false>
+static cudaError_t launch_nt(const CUtensorMap& tx, const Params& p, int grid, cudaStream_t stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t e = configure<NT, XH>(dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = config_of<NT, XH>(grid, p.csize, stream, attr);
   return cudaLaunchKernelEx(&cfg, w8a8_linear_kernel<NT, XH>, tx, p);
+}
+
+// Resident clusters of `csize` CTAs for the variant a shape launches.
+static int resident_for(const Shape& s, bool xh, int csize) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (xh) {
+    switch (s.NT) {
+      case 64: return resident_clusters<64, true>(dev, csize);
+      case 128: return resident_clusters<128, true>(dev, csize);
+      default: return resident_clusters<144, true>(dev, csize);
+    }
+  }
+  switch (s.NT) {
+    case 16: return resident_clusters<16, false>(dev, csize);
+    case 32: return resident_clusters<32, false>(dev, csize);
+    default: return resident_clusters<64, false>(dev, csize);
+  }
+}
+
+// Whether the wide variant for this tile width can run on the current device.
+static bool wide_usable(int nt) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaError_t e = nt == 128 ? check_split<128, true>(dev) : check_split<144, true>(dev);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e == cudaSuccess;
+}
+
+// Work split.  Four ways to deal the (tile, K block) items over one CTA per
+// SM, chosen by a cost in K blocks: the most blocks any CTA streams plus a
+// penalty for each cross-CTA reduction a CTA takes part in.  Measured (a
+// globaltimer trace per phase): a block takes ~0.4 us at tiles of <= 64
+// tokens and ~0.8 us at 128 or more (the MMA rate), the integer atomics,
+// fence, counter and read-back that end a split tile 2-6 us, i.e. ~5 blocks'
+// time, and a cluster's exchange through distributed shared memory well
+// under a microsecond.
+//  * a cluster of C CTAs per tile (grid = tiles x C, all clusters resident at
+//    once), each CTA one K part, the parts summed in shared memory;
+//  * P parts per tile (grid = tiles x P, tiles <= SMs): every CTA owns one
+//    segment of one tile (P = 1: whole tiles, no reduction at all);
+//  * whole tiles in contiguous runs (tiles > SMs: each CTA takes
+//    ceil(tiles / SMs) or one fewer, no reduction);
+//  * equal contiguous ranges of items (stream-K): balanced, but most CTAs
+//    publish a partial tile twice, once in the middle of their range.
+struct Split {
+  int grid;
+  int tile_ranges;
+  int csize;
+};
+
+static Split split_of(const Shape& s, bool xh, int sms) {
+  const long long rho = 5, rho_cluster = 1;
+  const long long total = (long long)s.tiles * s.KB;
+  Split best{(int)std::min<long long>(total, sms), 0, 1};
+  long long best_cost = (total + sms - 1) / sms + (s.tiles < total ? 2 * rho : 0);
+  if (s.tiles <= sms) {
+    const int pmax = std::min(sms / s.tiles, s.KB);
+    for (int P = 1; P <= pmax; ++P) {
+      const long long cost = (s.KB + P - 1) / P + (P > 1 ? rho : 0);
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = Split{s.tiles * P, 0, 1};
+      }
+    }
+    for (int C = 2; C <= std::min(pmax, 4); ++C) {
+      const long long cost = (s.KB + C - 1) / C + rho_cluster;
+      if (cost < best_cost && resident_for(s, xh, C) >= s.tiles) {
+        best_cost = cost;
+        best = Split{s.tiles * C, 0, C};
+      }
+    }
+  } else {
+    const long long cost = (long long)((s.tiles + sms - 1) / sms) * s.KB;
+    if (cost <= best_cost) best = Split{sms, 1, 1};
+  }
+  return best;
 }
 
 // `xh_ext` (optional, the one-call entry): the token codes already widened to
@@ -686,19 +1016,20 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
 
   Shape s = shape_of(M, N, K);
   uint32_t* ws_cnt = reinterpret_cast<uint32_t*>(ws);
-  int32_t* ws_acc = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + align256((size_t)s.tiles * CONV_WARPS * 4));
+  int32_t* ws_acc = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + cnt_bytes(M, N, K));
+  const size_t xh_off = cnt_bytes(M, N, K) + align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K)));
   // A few tokens: the register-path kernel (same packed weights, same
   // workspace layout, fewer counters per tile).
   if (skinny::handles(M))
     return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream, false);
-
+  // Wide tiles whose register split the device cannot honour fall back to
+  // 64-row tiles (fewer counters and no fp16 copy: the workspace suffices).
+  if (s.NT >= 128 && !wide_usable(s.NT)) s = shape_with(M, N, K, 64);
 
   const bool ext = xh_ext != nullptr && s.NT >= 64;
   const bool xh_path = ext || use_xh(M, s);
   uint4* xh = ext ? reinterpret_cast<uint4*>(const_cast<void*>(xh_ext))
-              : xh_path ? reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws) +
-                                                   align256((size_t)s.tiles * CONV_WARPS * 4) +
-                                                   align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K))))
+              : xh_path ? reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws) + xh_off)
                         : nullptr;
   CUtensorMap tx;
   if (xh_path) {
@@ -730,7 +1061,10 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
 
   const int sms = sm_count();
   if (sms <= 0) return QUASAR_ERR_CUDA;
-  const int grid = std::min(p.total, sms);
+  const Split sp = split_of(s, xh_path, sms);
+  const int grid = sp.grid;
+  p.tile_ranges = sp.tile_ranges;
+  p.csize = sp.csize;
   cudaError_t e;
   if (xh_path) {
     const long long n16 = (long long)M * K / 16;
@@ -744,20 +1078,21 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
     wc.attrs = wa;
     wc.numAttrs = 1;
     e = ext ? cudaSuccess : cudaLaunchKernelEx(&wc, widen_tokens_kernel, Xq, n16, xh);
-    if (e == cudaSuccess)
-      e = (s.NT == 64)   ? launch_nt<64, true>(tx, p, grid, stream)
-          : (s.NT == 96) ? launch_nt<96, true>(tx, p, grid, stream)
-                         : launch_nt<128, true>(tx, p, grid, stream);
+    if (e == cudaSuccess) {
+      switch (s.NT) {
+        case 64: e = launch_nt<64, true>(tx, p, grid, stream); break;
+        case 128: e = launch_nt<128, true>(tx, p, grid, stream); break;
+        default: e = launch_nt<144, true>(tx, p, grid, stream); break;
+      }
+    }
     // leave the workspace zero-filled (the internal fp16 copy is scratch of this call)
     if (e == cudaSuccess && !ext) e = cudaMemsetAsync(xh, 0, (size_t)M * K * 2, stream);
     return cuda_status(e);
   }
-  switch (s.NT) {
+  switch (s.NT) {   // tiles of >= 128 rows always take the fp16 copy above
     case 16: e = launch_nt<16>(tx, p, grid, stream); break;
     case 32: e = launch_nt<32>(tx, p, grid, stream); break;
-    case 64: e = launch_nt<64>(tx, p, grid, stream); break;
-    case 96: e = launch_nt<96>(tx, p, grid, stream); break;
-    default: e = launch_nt<128>(tx, p, grid, stream); break;
+    default: e = launch_nt<64>(tx, p, grid, stream); break;
   }
   return cuda_status(e);
 }
@@ -781,7 +1116,7 @@ quasar_status_t run_w4(const int8_t* Xq, const float* sa, const int8_t* Wp4, con
   if (!ws || ws_bytes < workspace_size(M, N, K) || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
   const Shape s = shape_of(M, N, K);
   uint32_t* ws_cnt = reinterpret_cast<uint32_t*>(ws);
-  void* slots = reinterpret_cast<uint8_t*>(ws) + align256((size_t)s.tiles * CONV_WARPS * 4);
+  void* slots = reinterpret_cast<uint8_t*>(ws) + cnt_bytes(M, N, K);
   return skinny::run(Xq, sa, Wp4, sw, M, N, K, Y, ldy, acc_out, ws_cnt, slots, stream, true);
 }
 
