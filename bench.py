@@ -749,66 +749,195 @@ def run_rmsnorm_quant(q, dev, stream):
     return out
 
 
+class VerificationStep:
+    """The workload's verification step: 32 sequences x (8 drafts + 1) = 288
+    token rows through four Qwen3-8B-shaped decoder layers and the BF16
+    lm_head, then the acceptance test of the drafts.  Random-init synthetic
+    weights (BF16 W ~ N(0, 0.02); INT8 packed from them with a smooth vector
+    calibrated on 64 seeded N(0, 1) tokens; RMSNorm weights 1 + 0.1 N(0, 1)),
+    hidden states N(0, 1).
+
+    Per layer on this library's path:
+        RMSNorm + smooth + quantize (one launch) -> qkv W8A8 linear
+        -> attention (torch SDPA in BF16: causal within each sequence's 9
+           positions, 32 query / 8 KV heads of 128; no RoPE or q/k norm)
+        -> o_proj (smooth + quantize + W8A8 linear, one call) -> residual add
+        -> RMSNorm + smooth + quantize -> gate_up W8A8 linear
+        -> SiLU(gate) * up + smooth + quantize (one launch) -> down W8A8 linear
+        -> residual add
+    then the final RMSNorm (torch) and the fused BF16 lm_head + acceptance
+    (greedy, or rejection sampling at T = 1 with seeded uniforms).  The BF16
+    chain runs the same glue with torch RMSNorm, BF16 cuBLAS (torch.matmul)
+    for every linear and the lm_head, torch SiLU * up, then the verification
+    kernel on the logits.  The attention, residual adds and final norm are
+    torch on both sides."""
+
+    B, D, LAYERS, HEADS, KV_HEADS, HEAD_DIM = 32, 8, 4, 32, 8, 128
+
+    def __init__(self, q, dev, layers: int = LAYERS, seed: int = 501):
+        import torch
+        self.q, self.dev = q, dev
+        self.layers_n = layers
+        B, D, H, V = self.B, self.D, synth.HIDDEN, synth.VOCAB
+        self.M = B * (D + 1)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+        self.layers = []
+        for _ in range(layers):
+            lay = {}
+            for name in ("qkv", "o", "gate_up", "down"):
+                K, N = synth.LINEARS[name]
+                wb = (torch.randn((N, K), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+                xc = torch.randn((64, K), device=dev, generator=gen).to(torch.bfloat16)
+                smooth = q.calibrate_smooth(xc, wb)
+                wp, sw = q.pack_weights(wb, smooth)
+                lay[name] = {"K": K, "N": N, "wb": wb, "wp": wp, "sw": sw, "smooth": smooth}
+            for g in ("g_attn", "g_mlp"):
+                lay[g] = (1.0 + 0.1 * torch.randn(H, device=dev, generator=gen)).to(torch.bfloat16)
+            self.layers.append(lay)
+        self.g_final = (1.0 + 0.1 * torch.randn(H, device=dev, generator=gen)).to(torch.bfloat16)
+        self.h0 = torch.randn((self.M, H), device=dev, generator=gen).to(torch.bfloat16)
+        w = (torch.randn((V, H), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+        self.w_head = w
+        self.wp_head = q.pack_lm_head(w)
+        self.u = torch.rand((B, D), device=dev, generator=gen).clamp_(max=1.0 - 2.0 ** -24)
+        self.draft = torch.zeros((B, D), dtype=torch.int32, device=dev)
+        self.ws = q.Workspace(dev)
+        self.ws_f = q.Workspace(dev)   # the one-call linear leaves scratch in its workspace
+        self.ws_v = q.Workspace(dev)
+        self.n_acc = torch.empty(B, dtype=torch.int32, device=dev)
+        self.nxt = torch.empty(B, dtype=torch.int32, device=dev)
+        self.n_acc_bf = torch.empty(B, dtype=torch.int32, device=dev)
+        self.nxt_bf = torch.empty(B, dtype=torch.int32, device=dev)
+        self.logits = torch.empty((self.M, V), dtype=torch.bfloat16, device=dev)
+        self.gen = gen
+
+    # -- glue shared by both chains (torch, BF16)
+    def attention(self, qkv):
+        import torch
+        B, S, Hq, Hk, Dh = self.B, self.D + 1, self.HEADS, self.KV_HEADS, self.HEAD_DIM
+        qh = qkv[:, :Hq * Dh].view(B, S, Hq, Dh).transpose(1, 2)
+        kh = qkv[:, Hq * Dh:(Hq + Hk) * Dh].view(B, S, Hk, Dh).transpose(1, 2)
+        vh = qkv[:, (Hq + Hk) * Dh:].view(B, S, Hk, Dh).transpose(1, 2)
+        kh = kh.repeat_interleave(Hq // Hk, dim=1)
+        vh = vh.repeat_interleave(Hq // Hk, dim=1)
+        o = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, is_causal=True)
+        return o.transpose(1, 2).reshape(self.M, Hq * Dh).contiguous()
+
+    def final_norm(self, h):
+        import torch
+        return torch.nn.functional.rms_norm(h, (h.shape[1],), weight=self.g_final, eps=1e-6)
+
+    # -- this library's path
+    def hidden_ours(self):
+        q, ws = self.q, self.ws
+        h = self.h0
+        for lay in self.layers:
+            a = lay["qkv"]
+            xq, sa = q.rmsnorm_smooth_quant(h, lay["g_attn"], a["smooth"])
+            qkv = q.w8a8_linear(xq, sa, a["wp"], a["sw"], workspace=ws)
+            o = lay["o"]
+            h = h + q.w8a8_linear_fused(self.attention(qkv), o["smooth"], o["wp"], o["sw"], workspace=self.ws_f)
+            g = lay["gate_up"]
+            xq, sa = q.rmsnorm_smooth_quant(h, lay["g_mlp"], g["smooth"])
+            gu = q.w8a8_linear(xq, sa, g["wp"], g["sw"], workspace=ws)
+            d = lay["down"]
+            xq, sa = q.silu_mul_smooth_quant(gu, d["smooth"])
+            h = h + q.w8a8_linear(xq, sa, d["wp"], d["sw"], workspace=ws)
+        return self.final_norm(h)
+
+    def step_ours(self, temperature: float = 0.0):
+        hf = self.hidden_ours()
+        return self.q.lm_head_verify(hf, self.wp_head, self.draft, temperature, u=self.u if temperature > 0 else None,
+                                     n_acc=self.n_acc, next_token=self.nxt, workspace=self.ws)
+
+    # -- the BF16 chain
+    def hidden_bf16(self):
+        import torch
+        h = self.h0
+        K = h.shape[1]
+        for lay in self.layers:
+            x = torch.nn.functional.rms_norm(h, (K,), weight=lay["g_attn"], eps=1e-6)
+            qkv = torch.matmul(x, lay["qkv"]["wb"].t())
+            h = h + torch.matmul(self.attention(qkv), lay["o"]["wb"].t())
+            x = torch.nn.functional.rms_norm(h, (K,), weight=lay["g_mlp"], eps=1e-6)
+            gu = torch.matmul(x, lay["gate_up"]["wb"].t())
+            inter = gu.shape[1] // 2
+            hm = torch.nn.functional.silu(gu[:, :inter]) * gu[:, inter:]
+            h = h + torch.matmul(hm, lay["down"]["wb"].t())
+        return self.final_norm(h)
+
+    def step_bf16(self, temperature: float = 0.0):
+        import torch
+        hf = self.hidden_bf16()
+        torch.matmul(hf, self.w_head.t(), out=self.logits)
+        return self.q.verify_accept(self.logits.view(self.B, self.D + 1, -1), self.draft, temperature,
+                                    u=self.u if temperature > 0 else None, n_acc=self.n_acc_bf,
+                                    next_token=self.nxt_bf, workspace=self.ws_v)
+
+    def logits_ours(self):
+        """This path's logits (the lm_head kernel's logits mode on the same
+        hidden states), [B][D+1][V]."""
+        return self.q.lm_head_logits(self.hidden_ours(), self.wp_head).view(self.B, self.D + 1, -1)
+
+    def set_drafts(self, logits, seed: int = 502):
+        """Drafts uniform over the vocabulary, half the positions (a seeded
+        Bernoulli(0.5) mask) forced to the target's choice on `logits`
+        (first-index argmax of row j for draft j)."""
+        import torch
+        B, D = self.B, self.D
+        g = torch.Generator(device=self.dev)
+        g.manual_seed(seed)
+        rnd = torch.randint(0, logits.shape[-1], (B, D), dtype=torch.int32, device=self.dev, generator=g)
+        mask = torch.rand((B, D), device=self.dev, generator=g) < 0.5
+        am = torch.argmax(logits[:, :D, :].float(), dim=2).to(torch.int32)
+        self.draft.copy_(torch.where(mask, am, rnd))
+        return mask
+
+
 def run_verification_step(q, dev, stream, bf16_peak):
-    """Verification step of 32 sequences x (8 drafts + 1) = 288 token rows:
-    four Qwen3-8B decoder layers' W8A8 linears (qkv, o, gate_up, down; each
-    one call of the fused smooth + quantize + linear entry) and the BF16
-    lm_head with fused greedy verification, against the same chain on BF16
-    cuBLAS (torch.matmul for every linear and the lm_head) followed by the
-    verification kernel.  The glue between the linears (RMSNorm, attention,
-    SiLU * up) is not on this path and is left out of both sides: every
-    linear reads its own synthetic activations.  Cold L2 by construction
-    (0.77 GB of INT8 and 1.54 GB of BF16 layer weights, 1.24 GB of lm_head)."""
+    """The verification step (VerificationStep) timed on this path and on
+    the BF16 chain, greedy and T = 1, with the accepted prefix length of
+    every sequence.  The drafts are set once from this path's logits.  The
+    fused lm_head's decisions are checked here against the verification
+    kernel run on the same kernel's logits (logits mode); the oracle check
+    of those decisions is a GPU test."""
     import torch
-    B, D, V, H = 32, 8, synth.VOCAB, synth.HIDDEN
-    M = B * (D + 1)
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(3)
-    layers = []
-    for _ in range(4):
-        lay = []
-        for name in ("qkv", "o", "gate_up", "down"):
-            K, N = synth.LINEARS[name]
-            wq = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev, generator=gen)
-            lay.append({"K": K, "N": N, "wp": q.tile_weights(wq), "sw": torch.rand(N, device=dev, generator=gen) * 1e-3,
-                        "smooth": torch.rand(K, device=dev, generator=gen) + 0.5,
-                        "x": torch.randn((M, K), device=dev, generator=gen).to(torch.bfloat16),
-                        "y": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
-                        "wb": (torch.randn((N, K), device=dev, generator=gen) * 0.02).to(torch.bfloat16)})
-            del wq
-        layers.append(lay)
-    h = torch.randn((M, H), device=dev, generator=gen).to(torch.bfloat16)
-    w = (torch.randn((V, H), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
-    wp = q.pack_lm_head(w)
-    draft = torch.randint(0, V, (B, D), dtype=torch.int32, device=dev, generator=gen)
-    lg = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
-    n_acc = torch.empty(B, dtype=torch.int32, device=dev)
-    nxt = torch.empty(B, dtype=torch.int32, device=dev)
-    ws_l, ws_h, ws_v = q.Workspace(dev), q.Workspace(dev), q.Workspace(dev)
-    ws_l.get(max(q.lib.quasar_w8a8_linear_fused_workspace_size(M, l["N"], l["K"]) for l in layers[0]))
-    ws_h.get(q.lib.quasar_lm_head_verify_workspace_size(B, D, V))
-    ws_v.get(q.lib.quasar_verify_accept_workspace_size(B, D, V))
-
-    def ours(i):
-        for lay in layers:
-            for l in lay:
-                q.w8a8_linear_fused(l["x"], l["smooth"], l["wp"], l["sw"], y=l["y"], workspace=ws_l)
-        q.lm_head_verify(h, wp, draft, 0.0, n_acc=n_acc, next_token=nxt, workspace=ws_h)
-
-    def bf16(i):
-        for lay in layers:
-            for l in lay:
-                torch.matmul(l["x"], l["wb"].t(), out=l["y"])
-        torch.matmul(h, w.t(), out=lg)
-        q.verify_accept(lg.view(B, D + 1, V), draft, n_acc=n_acc, next_token=nxt, workspace=ws_v)
-
-    us = _time_graph(torch, stream, ours, 3)
-    us_bf = _time_graph(torch, stream, bf16, 3)
-    lin_bytes = sum(l["N"] * l["K"] + 4 * l["N"] for lay in layers for l in lay)
-    out = {"B": B, "D": D, "token_rows": M, "layers": 4, "us": round(us, 1), "bf16_cublas_us": round(us_bf, 1),
-           "speedup_vs_bf16": round(us_bf / us, 3), "int8_weight_bytes": lin_bytes, "lm_head_bf16_bytes": V * H * 2,
-           "note": "glue (RMSNorm, attention, SiLU*up) left out of both sides"}
-    del layers
+    vs = VerificationStep(q, dev)
+    with torch.cuda.stream(stream):
+        lg = vs.logits_ours()
+        vs.set_drafts(lg)
+        ref_g, _ = q.verify_accept(lg, vs.draft, workspace=vs.ws_v)
+        ref_s, _ = q.verify_accept(lg, vs.draft, 1.0, u=vs.u, workspace=vs.ws_v)
+        ours_g = vs.step_ours(0.0)[0].clone()
+        ours_s = vs.step_ours(1.0)[0].clone()
+        bf_g = vs.step_bf16(0.0)[0].clone()
+        bf_s = vs.step_bf16(1.0)[0].clone()
+    stream.synchronize()
+    us = {}
+    for name, fn in (("ours_greedy", lambda i: vs.step_ours(0.0)), ("ours_t1", lambda i: vs.step_ours(1.0)),
+                     ("bf16_greedy", lambda i: vs.step_bf16(0.0)), ("bf16_t1", lambda i: vs.step_bf16(1.0))):
+        us[name] = _time_graph(torch, stream, fn, 3)
+    st, site = q.get_device_error(stream)
+    lin_bytes = sum(l[n]["N"] * l[n]["K"] + 4 * l[n]["N"] for l in vs.layers for n in ("qkv", "o", "gate_up", "down"))
+    n_acc = lambda t: [int(v) for v in t.cpu().tolist()]
+    out = {"B": vs.B, "D": vs.D, "token_rows": vs.M, "layers": vs.layers_n,
+           "us": round(us["ours_greedy"], 1), "bf16_cublas_us": round(us["bf16_greedy"], 1),
+           "speedup_vs_bf16": round(us["bf16_greedy"] / us["ours_greedy"], 3),
+           "t1_us": round(us["ours_t1"], 1), "bf16_cublas_t1_us": round(us["bf16_t1"], 1),
+           "t1_speedup_vs_bf16": round(us["bf16_t1"] / us["ours_t1"], 3),
+           "n_acc_greedy": n_acc(ours_g), "n_acc_t1": n_acc(ours_s),
+           "mean_acceptance_len_greedy": round(float(ours_g.float().mean()) + 1, 3),
+           "mean_acceptance_len_t1": round(float(ours_s.float().mean()) + 1, 3),
+           "fused_equals_unfused_on_same_logits": bool(torch.equal(ours_g, ref_g) and torch.equal(ours_s, ref_s)),
+           "bf16_chain_n_acc_greedy": n_acc(bf_g), "bf16_chain_n_acc_t1": n_acc(bf_s),
+           "int8_weight_bytes": lin_bytes, "lm_head_bf16_bytes": synth.VOCAB * synth.HIDDEN * 2,
+           "device_error": st,
+           "glue": "RMSNorm ahead of qkv / gate_up and SiLU*up ahead of down fused into this library's "
+                   "quantizers; attention (SDPA, BF16), residual adds and the final RMSNorm in torch on "
+                   "both sides",
+           "drafts": "uniform over the vocabulary, half forced to this path's greedy choice"}
+    del vs
     torch.cuda.empty_cache()
     return out
 

@@ -234,13 +234,18 @@ quasar_status_t quasar_silu_mul_smooth_quant(const void* GU_bf16, int ldgu, cons
  *   reads Xq / sa and writes Y and the workspace only after that kernel's
  *   writes are visible.
  *   workspace: >= quasar_w8a8_linear_workspace_size(M, N, K) bytes of device
- *   memory that is ZERO-FILLED before its first use.  The call leaves it
- *   zero-filled again when it completes without a device error, so one
- *   workspace can serve every linear on a stream.  Calls that share a
- *   workspace must not run concurrently.  After QUASAR_ERR_TIMEOUT from
- *   quasar_get_device_error the workspace must be zero-filled again.
+ *   memory whose first quasar_w8a8_linear_workspace_zeroed_bytes(M, N, K)
+ *   bytes (split-K counters and, above 24 tokens, int32 partial sums) are
+ *   ZERO when the call starts; the rest may hold anything.  The call leaves
+ *   all quasar_w8a8_linear_workspace_size(M, N, K) bytes zero-filled again
+ *   when it completes without a device error, so one zero-filled workspace
+ *   can serve every linear on a stream (but see the one-call entry below,
+ *   which leaves scratch behind).  Calls that share a workspace must not run
+ *   concurrently.  After QUASAR_ERR_TIMEOUT from quasar_get_device_error the
+ *   workspace must be zero-filled again.
  * ------------------------------------------------------------------------ */
 size_t quasar_w8a8_linear_workspace_size(int M, int N, int K);
+size_t quasar_w8a8_linear_workspace_zeroed_bytes(int M, int N, int K);
 quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
                                    const int8_t* Wp, const float* sw,
                                    int M, int N, int K,
@@ -297,9 +302,12 @@ quasar_status_t quasar_w4a8_linear(const int8_t* Xq, const float* sa,
  *   X [M][ldx] BF16 (ldx >= K, ldx % 8 == 0, 16-byte aligned), smooth [K]
  *   fp32 (16-byte aligned), Wp / sw / Y / sizes as for quasar_w8a8_linear.
  *   workspace: >= quasar_w8a8_linear_fused_workspace_size(M, N, K) bytes;
- *   its first quasar_w8a8_linear_workspace_size(M, N, K) bytes follow the
- *   zero-filled contract of quasar_w8a8_linear, the rest is scratch with no
- *   required content.
+ *   its first quasar_w8a8_linear_workspace_zeroed_bytes(M, N, K) bytes
+ *   must be zero on entry as for quasar_w8a8_linear, and its first
+ *   quasar_w8a8_linear_workspace_size(M, N, K) bytes are zero again on
+ *   return; the bytes after those hold the codes and scales afterwards
+ *   (scratch).  A later call on the same buffer whose zero prefix reaches
+ *   into that scratch needs it cleared first (or a buffer of its own).
  * ------------------------------------------------------------------------ */
 size_t quasar_w8a8_linear_fused_workspace_size(int M, int N, int K);
 quasar_status_t quasar_w8a8_linear_fused(const void* X_bf16, int ldx, const float* smooth,

@@ -69,6 +69,17 @@ def test_workspace_sizes(lib):
     # counters sized for the 64-row fallback tiles (4 x 192 tiles x 16 warps)
     assert ws(256, 24576, 4096) == 4 * 192 * 16 * 4 + 256 * 24576 * 4 + 256 * 4096 * 2
     assert ws(128, 6144, 4096) == 2 * 48 * 16 * 4 + 128 * 6144 * 4 + 128 * 4096 * 2
+    # the prefix that must be zero on entry: counters, plus the int32 sums
+    # above 24 tokens (the register path's slots and the fp16 token copy
+    # need no initial content)
+    zb = lib.quasar_w8a8_linear_workspace_zeroed_bytes
+    zb.restype = ctypes.c_size_t
+    assert zb(20, 6144, 4096) == 3072
+    assert zb(64, 4096, 4096) == 2048 + 64 * 4096 * 4
+    assert zb(256, 24576, 4096) == 4 * 192 * 16 * 4 + 256 * 24576 * 4
+    assert zb(0, 6144, 4096) == 0
+    for M, N, K in [(1, 8, 16), (24, 24576, 12288), (40, 4096, 12288), (288, 6144, 4096)]:
+        assert zb(M, N, K) <= ws(M, N, K)
     assert lib.quasar_calibrate_workspace_size(4096) == 8 * 4096
     assert lib.quasar_verify_accept_workspace_size(32, 8, 151936) > 0
     assert lib.quasar_verify_accept_workspace_size(0, 8, 151936) == 0

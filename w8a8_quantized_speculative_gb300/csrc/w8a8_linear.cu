@@ -803,6 +803,14 @@ static size_t cnt_bytes(int M, int N, int K) {
   return align256((size_t)tiles * CONV_WARPS * 4);
 }
 
+// The prefix that must be zero when a call starts: the counters and, on the
+// tcgen05 path, the int32 sums of split tiles.  The register-path kernel's
+// partial-sum slots and the fp16 token copy need no initial content.
+size_t zeroed_bytes(int M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return cnt_bytes(M, N, K) + (skinny::handles(M) ? 0 : align256((size_t)M * N * 4));
+}
+
 size_t workspace_size(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   Shape s = shape_of(M, N, K);
@@ -1211,6 +1219,10 @@ quasar_status_t quasar_w8a8_linear_noalloc(const int8_t* Xq, const float* sa, co
 }
 
 size_t quasar_w8a8_linear_workspace_size(int M, int N, int K) { return quasar::gemm::workspace_size(M, N, K); }
+
+size_t quasar_w8a8_linear_workspace_zeroed_bytes(int M, int N, int K) {
+  return quasar::gemm::zeroed_bytes(M, N, K);
+}
 
 size_t quasar_w8a8_linear_fused_workspace_size(int M, int N, int K) {
   return quasar::gemm::fused_workspace_size(M, N, K);

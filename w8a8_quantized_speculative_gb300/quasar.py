@@ -46,6 +46,7 @@ _SIGS = {
     "quasar_silu_mul_smooth_quant": (_i, [_p, _i, _p, _i, _i, _p, _p, _p]),
     "quasar_rmsnorm_smooth_quant": (_i, [_p, _i, _p, _f, _p, _i, _i, _p, _p, _p]),
     "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
+    "quasar_w8a8_linear_workspace_zeroed_bytes": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_w8a8_linear_fused_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear_fused": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
@@ -106,23 +107,45 @@ def _rowmajor(t: torch.Tensor, name: str):
 
 
 class Workspace:
-    """Zero-filled device scratch that grows on demand.  The library leaves a
-    workspace zero-filled after each successful call, so one instance can be
-    shared by consecutive calls on the same stream."""
+    """Zero-filled device scratch that grows on demand.  Every call leaves
+    the part of the workspace it needs zero-filled, except the one-call
+    linear (w8a8_linear_fused), which leaves its codes and scales after that
+    part; this object remembers that range and clears the overlap before a
+    later call that needs those bytes zero, so one instance can be shared by
+    consecutive calls on the same stream."""
 
     def __init__(self, device=None):
         self.device = torch.device(device) if device is not None else torch.device("cuda")
         self.buf = None
+        self.dirty = None          # (lo, hi): bytes a call may have left nonzero
 
-    def get(self, nbytes: int) -> torch.Tensor:
+    def get(self, nbytes: int, zero_prefix: int | None = None, stream=None) -> torch.Tensor:
+        """The buffer, at least `nbytes` long, with its first `zero_prefix`
+        bytes (default: all `nbytes`) zero when the next call on `stream` starts."""
         nbytes = max(int(nbytes), 256)
         if self.buf is None or self.buf.numel() < nbytes:
             self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+            self.dirty = None
+        z = nbytes if zero_prefix is None else int(zero_prefix)
+        if self.dirty is not None and self.dirty[0] < z:
+            lo, hi = self.dirty[0], min(self.dirty[1], z)
+            if stream is None:
+                self.buf[lo:hi].zero_()
+            else:
+                with torch.cuda.stream(stream):
+                    self.buf[lo:hi].zero_()
+            self.dirty = (z, self.dirty[1]) if self.dirty[1] > z else None
         return self.buf
+
+    def mark_dirty(self, lo: int, hi: int):
+        if hi <= lo:
+            return
+        self.dirty = (lo, hi) if self.dirty is None else (min(lo, self.dirty[0]), max(hi, self.dirty[1]))
 
     def reset(self):
         if self.buf is not None:
             self.buf.zero_()
+        self.dirty = None
 
 
 _default_ws = {}
@@ -223,7 +246,8 @@ def w4a8_linear(xq, sa, wp4, sw, y=None, workspace: Workspace | None = None, str
     y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if y is None else y
     ldy = _rowmajor(y, "y")
     ws = _ws(workspace, xq.device)
-    buf = ws.get(int(lib.quasar_w8a8_linear_workspace_size(M, N, K)))
+    buf = ws.get(int(lib.quasar_w8a8_linear_workspace_size(M, N, K)),
+                 zero_prefix=int(lib.quasar_w8a8_linear_workspace_zeroed_bytes(M, N, K)), stream=stream)
     _check(lib.quasar_w4a8_linear(_ptr(xq), _ptr(sa), _ptr(wp4), _ptr(sw), M, N, K, _ptr(y), ldy, _ptr(buf),
                                   buf.numel(), _stream(stream)), "w4a8_linear")
     return y
@@ -294,7 +318,7 @@ def w8a8_linear(xq, sa, wp, sw, y=None, workspace: Workspace | None = None, stre
     ldy = _rowmajor(y, "y")
     ws = _ws(workspace, xq.device)
     need = int(lib.quasar_w8a8_linear_workspace_size(M, N, K))
-    buf = ws.get(need)
+    buf = ws.get(need, zero_prefix=int(lib.quasar_w8a8_linear_workspace_zeroed_bytes(M, N, K)), stream=stream)
     _check(lib.quasar_w8a8_linear(_ptr(xq), _ptr(sa), _ptr(wp), _ptr(sw), M, N, K, _ptr(y), ldy, _ptr(buf),
                                   buf.numel(), _stream(stream)), "w8a8_linear")
     return y
@@ -312,9 +336,12 @@ def w8a8_linear_fused(x, smooth, wp, sw, y=None, workspace: Workspace | None = N
     y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if y is None else y
     ldy = _rowmajor(y, "y")
     ws = _ws(workspace, x.device)
-    buf = ws.get(int(lib.quasar_w8a8_linear_fused_workspace_size(M, N, K)))
+    need = int(lib.quasar_w8a8_linear_fused_workspace_size(M, N, K))
+    buf = ws.get(need, zero_prefix=int(lib.quasar_w8a8_linear_workspace_zeroed_bytes(M, N, K)), stream=stream)
     _check(lib.quasar_w8a8_linear_fused(_ptr(x), ldx, _ptr(smooth), _ptr(wp), _ptr(sw), M, N, K, _ptr(y), ldy,
                                         _ptr(buf), buf.numel(), _stream(stream)), "w8a8_linear_fused")
+    if M > 0:
+        ws.mark_dirty(int(lib.quasar_w8a8_linear_workspace_size(M, N, K)), need)
     return y
 
 
@@ -325,7 +352,8 @@ def int8_gemm_s32(xq, wp, N: int, acc=None, workspace: Workspace | None = None, 
     _check_packed(wp, N, K)
     acc = torch.empty((M, N), dtype=torch.int32, device=xq.device) if acc is None else acc
     ws = _ws(workspace, xq.device)
-    buf = ws.get(int(lib.quasar_w8a8_linear_workspace_size(M, N, K)))
+    buf = ws.get(int(lib.quasar_w8a8_linear_workspace_size(M, N, K)),
+                 zero_prefix=int(lib.quasar_w8a8_linear_workspace_zeroed_bytes(M, N, K)), stream=stream)
     _check(lib.quasar_int8_gemm_s32(_ptr(xq), _ptr(wp), M, N, K, _ptr(acc), _ptr(buf), buf.numel(),
                                     _stream(stream)), "int8_gemm_s32")
     return acc
