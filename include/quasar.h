@@ -72,6 +72,24 @@ quasar_status_t quasar_get_device_error(quasar_stream_t stream, uint32_t* site);
  * range, else the launch status. */
 quasar_status_t quasar_selftest_wait_timeout(uint64_t limit_ns, quasar_stream_t stream);
 
+/* Tensor-pipe rate probe (a measurement utility; the pages have no
+ * counterpart).  Runs one CTA per SM that issues `iters` groups of four MMAs
+ * of one form and records, in `out` (DEVICE, >= 4 * SM-count 64-bit slots,
+ * caller-owned, overwritten), per CTA b: out[4b] = clock64 cycles of the MMA
+ * loop (0 if its bounded wait ran out), out[4b+1] = MMAs issued, out[4b+2] =
+ * tcgen05.st instructions of the store traffic (form 2), out[4b+3] = cycles
+ * that traffic ran.  Forms: 0 = tcgen05.mma kind::f16 M = 128, N = n, K = 16,
+ * A in TMEM and B in shared memory; 1 = the same with A in shared memory;
+ * 2 = form 0 while 16 warps store into another TMEM region (the W8A8 tcgen05
+ * kernel's converter traffic); 3 = mma.sync m16n8k16 fp16 -> fp32 from
+ * registers, 16 warps (n ignored); 4 / 5 = form 0 with each group's K steps
+ * spread over 2 / 4 independent accumulators (n <= 128 / 64); 6 = form 1
+ * with M = 64.  n: 16 .. 256, a multiple of 16 (forms other than 3);
+ * 1 <= iters <= 2^20.  Asynchronous on `stream`; returns
+ * QUASAR_ERR_INVALID_ARG / QUASAR_ERR_UNSUPPORTED for bad arguments. */
+quasar_status_t quasar_probe_tensor_rate(int form, int n, int iters, unsigned long long* out,
+                                         int out_slots, quasar_stream_t stream);
+
 /* Bound for the device-side waits, in nanoseconds (default 2e9 = 2 s).
  * Host-side setting applied to the next launches; 0 restores the default. */
 quasar_status_t quasar_set_wait_limit_ns(uint64_t ns);

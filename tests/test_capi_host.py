@@ -289,3 +289,14 @@ def test_lm_head_rejects_bad_arguments(lib):
     assert pk(FAKE, 32, 100, 64, FAKE, None) == 2       # ldw < K
     assert pk(FAKE_ODD, 64, 100, 64, FAKE, None) == 2
     assert pk(None, 64, 100, 64, FAKE, None) == 1
+
+
+def test_tensor_probe_rejects_bad_arguments(lib):
+    f = lib.quasar_probe_tensor_rate
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    assert f(0, 128, 16, None, 1024, None) == 1           # no output buffer
+    assert f(7, 128, 16, FAKE, 1024, None) == 1           # unknown form
+    assert f(0, 128, 0, FAKE, 1024, None) == 1            # no iterations
+    assert f(0, 24, 16, FAKE, 1024, None) == 2            # N not a multiple of 16
+    assert f(0, 272, 16, FAKE, 1024, None) == 2           # N above 256
+    assert f(5, 128, 16, FAKE, 1024, None) == 2           # four accumulators of 128 columns do not fit

@@ -837,3 +837,19 @@ def test_verify_at_max_rows():
     want = np.where(ok.all(axis=1), D, np.argmin(ok, axis=1))
     assert np.array_equal(n_acc.cpu().numpy(), want)
     assert np.array_equal(nxt.cpu().numpy(), am[np.arange(B), want])
+
+
+# ---------------------------------------------------------------- tensor-pipe probe
+
+def test_tensor_probe_rates_are_plausible():
+    """The probe issues real MMAs: the tcgen05 rate at N = 256 lies within
+    the nominal 4096 MAC per SM clock, falls with N (fixed issue cost per
+    instruction), and mma.sync stays under its 2048 flop per SM clock."""
+    wide = q.probe_tensor_rate("tcgen05_ts", 256, 1024)
+    narrow = q.probe_tensor_rate("tcgen05_ts", 64, 1024)
+    assert 1000 < wide["mac_per_clk_per_sm"] <= 4096 * 1.02
+    assert narrow["mac_per_clk_per_sm"] < wide["mac_per_clk_per_sm"]
+    hm = q.probe_tensor_rate("mma_sync", iters=1024)
+    assert 100 < hm["mac_per_clk_per_sm"] <= 1024 * 1.02
+    st, site = q.get_device_error()
+    assert st == 0, site

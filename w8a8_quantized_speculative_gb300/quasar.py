@@ -47,6 +47,7 @@ _SIGS = {
     "quasar_rmsnorm_smooth_quant": (_i, [_p, _i, _p, _f, _p, _i, _i, _p, _p, _p]),
     "quasar_w8a8_linear_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear_workspace_zeroed_bytes": (_sz, [_i, _i, _i]),
+    "quasar_probe_tensor_rate": (_i, [_i, _i, _i, _p, _i, _p]),
     "quasar_w8a8_linear": (_i, [_p, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
     "quasar_w8a8_linear_fused_workspace_size": (_sz, [_i, _i, _i]),
     "quasar_w8a8_linear_fused": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _p, _i, _p, _sz, _p]),
@@ -507,6 +508,37 @@ def lm_head_verify_sample(h: torch.Tensor, wp: PackedLmHead, draft: torch.Tensor
                                             _ptr(next_token), _ptr(buf), buf.numel(), _stream(stream)),
            "lm_head_verify_sample")
     return n_acc, next_token
+
+
+PROBE_FORMS = {"tcgen05_ts": 0, "tcgen05_ss": 1, "tcgen05_ts_with_tmem_stores": 2, "mma_sync": 3,
+               "tcgen05_ts_2chains": 4, "tcgen05_ts_4chains": 5, "tcgen05_ss_m64": 6}
+
+
+def probe_tensor_rate(form: str, n: int = 128, iters: int = 4096, stream=None):
+    """Measured rate of one MMA form on every SM (see quasar_probe_tensor_rate):
+    returns dict(mac_per_clk_per_sm, cycles_per_mma, tmem_st_per_clk_per_sm)
+    averaged over the SMs."""
+    f = PROBE_FORMS[form]
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    out = torch.zeros(4 * sms, dtype=torch.int64, device="cuda")
+    _check(lib.quasar_probe_tensor_rate(f, int(n), int(iters), _ptr(out), out.numel(), _stream(stream)),
+           "probe_tensor_rate")
+    torch.cuda.synchronize()
+    o = out.view(sms, 4).cpu().numpy().astype("float64")
+    ok = o[:, 0] > 0
+    if not ok.any():
+        raise QuasarError("probe_tensor_rate: every bounded wait ran out")
+    cyc, mmas = o[ok, 0], o[ok, 1]
+    if f == 3:
+        macs = mmas * 16 * 8 * 16               # mmas counts every warp's mma.sync (16 x 8 x 16 each)
+        per_issuer = mmas / 16                  # one issuing warp's share
+    else:
+        macs = mmas * (64 if f == 6 else 128) * n * 16
+        per_issuer = mmas
+    res = {"mac_per_clk_per_sm": float((macs / cyc).mean()), "cycles_per_mma": float((cyc / per_issuer).mean())}
+    if f == 2:
+        res["tmem_st_per_clk_per_sm"] = float((o[ok, 2] / o[ok, 3].clip(min=1)).mean())
+    return res
 
 
 def get_device_error(stream=None):
