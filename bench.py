@@ -753,6 +753,54 @@ def run_rmsnorm_quant(q, dev, stream):
     return out
 
 
+def profile_kernels(q, which: str, launches: int = 4):
+    """Launch one kernel of the path a few times at its workload shape, for an
+    ncu capture (no timing): `verify` (greedy, B = 32, D = 8, V = 151936),
+    `glue` (SiLU * up + smooth + quantize, M = 40, I = 12288), `rmsnorm`
+    (RMSNorm + smooth + quantize, M = 288, K = 4096), `qkv64` / `qkv256`
+    (the W8A8 linear, qkv 4096 -> 6144 at M = 64 / 256; weights rotate over
+    six copies, 151 MB > L2)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    if which == "verify":
+        B, D, V = 32, 8, synth.VOCAB
+        lgs = [torch.randn((B, D + 1, V), device=dev, generator=gen).to(torch.bfloat16) for _ in range(3)]
+        draft = lgs[0].float().argmax(dim=2).to(torch.int32)[:, :D].contiguous()
+        for i in range(launches):
+            q.verify_accept(lgs[i % 3], draft)
+    elif which == "glue":
+        M, I = 40, synth.INTERMEDIATE
+        gu = (torch.randn((M, 2 * I), device=dev, generator=gen) * 4).to(torch.bfloat16)
+        smooth = torch.rand(I, device=dev, generator=gen) + 0.5
+        for _ in range(launches):
+            q.silu_mul_smooth_quant(gu, smooth)
+    elif which == "rmsnorm":
+        M, K = 288, synth.HIDDEN
+        x = torch.randn((M, K), device=dev, generator=gen).to(torch.bfloat16)
+        g = (1 + 0.1 * torch.randn(K, device=dev, generator=gen)).to(torch.bfloat16)
+        smooth = torch.rand(K, device=dev, generator=gen) + 0.5
+        for _ in range(launches):
+            q.rmsnorm_smooth_quant(x, g, smooth)
+    elif which in ("qkv64", "qkv256"):
+        M = 64 if which == "qkv64" else 256
+        K, N = synth.LINEARS["qkv"]
+        wqs = [torch.randint(-127, 128, (N * K,), dtype=torch.int8, device=dev, generator=gen) for _ in range(6)]
+        sw = torch.rand(N, device=dev, generator=gen) * 1e-3
+        xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
+        sa = torch.rand(M, device=dev, generator=gen)
+        ws = q.Workspace(dev)
+        for i in range(launches):
+            q.w8a8_linear(xq, sa, wqs[i % 6], sw, workspace=ws)
+    else:
+        raise ValueError(which)
+    torch.cuda.synchronize()
+    st, site = q.get_device_error()
+    print(json.dumps({"profiled": which, "launches": launches, "device_error": st}), flush=True)
+
+
 def run_tensor_probe(q):
     """Measured issue rate of the MMA forms the kernels use (one CTA per SM,
     clock64 cycles): tcgen05.mma kind::f16 M = 128 with A in TMEM at the
@@ -980,11 +1028,16 @@ def main():
                     help="run only the 4-layer verification-step sub-benchmark")
     ap.add_argument("--mlp-block-only", action="store_true",
                     help="run only the M = 40 MLP-block sub-benchmark")
+    ap.add_argument("--profile-kernels", choices=["verify", "glue", "rmsnorm", "qkv64", "qkv256"],
+                    help="launch one kernel a few times at its workload shape (for ncu), no timing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.profile_kernels:
+        from w8a8_quantized_speculative_gb300 import quasar as q
+        profile_kernels(q, args.profile_kernels)
     elif args.verification_step_only:
         import torch
         from w8a8_quantized_speculative_gb300 import quasar as q

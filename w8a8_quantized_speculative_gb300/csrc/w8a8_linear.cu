@@ -102,8 +102,8 @@ struct Cfg {
   static constexpr int WARPS = CONV_WARPS + (WIDE ? 4 : 3);
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int REGS_LAUNCH = 96;
-  static constexpr int REGS_CONV = 104;
-  static constexpr int REGS_AUX = 64;
+  static constexpr int REGS_CONV = NT >= 192 ? 112 : 104;
+  static constexpr int REGS_AUX = NT >= 192 ? 32 : 64;
   // Blocks per pipeline stage: two 128-K blocks per handshake halve the
   // per-byte cost of the barrier round trips; NT >= 96 keeps one (TMEM).
   static constexpr int G = (NT >= 96) ? 1 : 2;
@@ -114,7 +114,8 @@ struct Cfg {
   static constexpr int TMEM_A0 = NACC * NT;                  // A stages follow the accumulators
   // Converted stages (TMEM A + shared-memory B) and INT8 stages, sized so
   // that the operand bytes in flight cover the copy latency at each width.
-  static constexpr int S2 = XH ? (NT == 144 ? 3 : NT == 128 ? 4 : 2) : (NT == 64 ? 2 : 3);
+  static constexpr int S2 = XH ? (NT == 256 ? 3 : NT == 192 ? 2 : NT == 144 ? 3 : NT == 128 ? 4 : 2)
+                               : (NT == 64 ? 2 : 3);
   static constexpr int W_BYTES = G * BLOCK_BYTES;            // INT8 weight blocks of a stage
   static constexpr int XB_BYTES = XH ? 0 : NT * BK;          // INT8 token tile of one block
   static constexpr int STAGE1 = W_BYTES + G * XB_BYTES;      // multiple of 1024
@@ -129,9 +130,12 @@ struct Cfg {
   static_assert(TMEM_A0 + S2 * A_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(STAGE1 % 1024 == 0 && B16_BLOCK % 1024 == 0, "1024B alignment of swizzled tiles");
   static_assert(S1 >= 2 && S2 >= 2, "pipeline depth");
-  static_assert(BM * NT * 4 <= S1 * STAGE1, "a cluster's partial sums fit over the INT8 ring");
+  // A cluster's partial sums (BM x NT int32) go over the INT8 ring, or over
+  // the converted ring when that is the larger one (both idle by then).
+  static constexpr bool PART_IN_B16 = BM * NT * 4 > S1 * STAGE1;
+  static_assert(BM * NT * 4 <= (PART_IN_B16 ? S2 * B16_BYTES : S1 * STAGE1), "cluster partial sums fit");
   static_assert(SMEM <= SMEM_OPTIN, "shared memory budget");
-  static_assert(NT % 16 == 0 && NT <= 144 && TOK % 4 == 0, "MMA N");
+  static_assert(NT % 16 == 0 && NT <= 256 && TOK % 4 == 0, "MMA N");
   static_assert(!WIDE || XH, "wide tiles take the fp16 token copy");
   static_assert(!WIDE || (CONV_WARPS * 32 * (REGS_CONV - REGS_LAUNCH) <= 4 * 32 * (REGS_LAUNCH - REGS_AUX)),
                 "register split: the converters never take more than the fifth warpgroup returns");
@@ -710,7 +714,7 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
       // Split tile of a cluster: this CTA's part of the sums goes to shared
       // memory (over the INT8 ring, idle once every converter warp is past
       // its last block), then the cluster adds the parts.
-      int32_t* part = reinterpret_cast<int32_t*>(stage1);
+      int32_t* part = reinterpret_cast<int32_t*>(C::PART_IN_B16 ? b16 : stage1);
       named_barrier_or(CONV_BAR_ID, CONV_WARPS * 32, 0u);
 #pragma unroll
       for (int jj = 0; jj < C::TOK; ++jj) part[(h * C::TOK + jj) * BM + row] = acc[jj];
@@ -754,20 +758,24 @@ w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
 
 // ------------------------------------------------------------------ host side
 
-// Token tile: the smallest of 16 / 32 / 64 / 128 / 144 rows that holds M,
-// so that up to 144 tokens every weight block is widened once per launch and
-// meets all tokens in one accumulator; above, tiles of 128 rows, or 144 for
-// 257-288 tokens (32 sequences x 9 positions: two tiles, not three).  A
-// single 256-row tile was built and measured: its 64 run sums per converter
-// thread spill, and it ran no faster than two 128-row tiles.
+// Token tile: the smallest of 16 / 32 / 64 / 128 / 144 / 192 / 256 rows that
+// holds M, so that every weight block is widened once per launch and meets
+// all tokens in one accumulator.  Measured (quasar_probe_tensor_rate): a
+// kind::f16 MMA of M = 128, K = 16 costs ~114 cycles for every N <= 192 and
+// ~138 at N = 256, so one wide tile beats two narrow passes (256 tokens:
+// 8 x 138 cycles per weight block instead of 16 x 114).  257-288 tokens (32
+// sequences x 9 positions) need two instructions per K step whatever the
+// split: two 144-row tiles; more tokens, 256-row tiles.
 static int pick_nt(int M) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
   if (M <= 128) return 128;
   if (M <= 144) return 144;
-  if (M > 256 && M <= 288) return 144;
-  return 128;
+  if (M <= 192) return 192;
+  if (M <= 256) return 256;
+  if (M <= 288) return 144;
+  return 256;
 }
 
 struct Shape {
@@ -937,7 +945,9 @@ static int resident_for(const Shape& s, bool xh, int csize) {
     switch (s.NT) {
       case 64: return resident_clusters<64, true>(dev, csize);
       case 128: return resident_clusters<128, true>(dev, csize);
-      default: return resident_clusters<144, true>(dev, csize);
+      case 144: return resident_clusters<144, true>(dev, csize);
+      case 192: return resident_clusters<192, true>(dev, csize);
+      default: return resident_clusters<256, true>(dev, csize);
     }
   }
   switch (s.NT) {
@@ -951,7 +961,10 @@ static int resident_for(const Shape& s, bool xh, int csize) {
 static bool wide_usable(int nt) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  cudaError_t e = nt == 128 ? check_split<128, true>(dev) : check_split<144, true>(dev);
+  cudaError_t e = nt == 128   ? check_split<128, true>(dev)
+                  : nt == 144 ? check_split<144, true>(dev)
+                  : nt == 192 ? check_split<192, true>(dev)
+                              : check_split<256, true>(dev);
   if (e != cudaSuccess) cudaGetLastError();
   return e == cudaSuccess;
 }
@@ -979,7 +992,9 @@ struct Split {
 };
 
 static Split split_of(const Shape& s, bool xh, int sms) {
-  const long long rho = 5, rho_cluster = 1;
+  // a split tile's atomics and read-back cost ~5 blocks' time at narrow
+  // tiles, ~10 at tiles of 192 or more tokens (measured 5-12 us at 256)
+  const long long rho = s.NT >= 192 ? 10 : 5, rho_cluster = 1;
   const long long total = (long long)s.tiles * s.KB;
   Split best{(int)std::min<long long>(total, sms), 0, 1};
   long long best_cost = (total + sms - 1) / sms + (s.tiles < total ? 2 * rho : 0);
@@ -1090,7 +1105,9 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
       switch (s.NT) {
         case 64: e = launch_nt<64, true>(tx, p, grid, stream); break;
         case 128: e = launch_nt<128, true>(tx, p, grid, stream); break;
-        default: e = launch_nt<144, true>(tx, p, grid, stream); break;
+        case 144: e = launch_nt<144, true>(tx, p, grid, stream); break;
+        case 192: e = launch_nt<192, true>(tx, p, grid, stream); break;
+        default: e = launch_nt<256, true>(tx, p, grid, stream); break;
       }
     }
     // leave the workspace zero-filled (the internal fp16 copy is scratch of this call)
