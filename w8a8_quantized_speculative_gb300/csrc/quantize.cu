@@ -253,14 +253,22 @@ QUASAR_DEVICE_INLINE float bf16_round(float v) { return __bfloat162float(__float
 
 // RMSNorm ahead of a linear (qkv, gate_up) fused with its smooth + quantize,
 // one CTA per row of up to 2048 VPT values, every load issued up front as in
-// quant_act_kernel.  Per row: ss = sum of the squares of the BF16 inputs, each
-// square exact in fp64, summed in fp64 in this kernel's order (per thread,
-// a butterfly across the warp, the warps in order); r = fp32_rn(1 /
-// sqrt(ss / K + eps)) with IEEE fp64 division and square root; t = bf16(x *
-// r), h = bf16(t * gamma); then the A2 quantizer on fp32(h) * smooth.  The
-// order of the sum can move ss by a few fp64 ulps from the correctly rounded
-// sum, which changes r only when 1 / sqrt(...) lies within a hair (2^-38
-// relative) of an fp32 rounding midpoint.
+// quant_act_kernel.  Per row: ss = sum of the squares of the BF16 inputs.  A
+// BF16 value has 8 significant bits, so its square is exact in fp32 (inside
+// [2^-120, 2^120]); each thread sums each group of eight squares in fp32 with
+// Neumaier's compensation (every rounding error of the running sum is
+// recovered exactly and kept in a second term) and adds the two terms of
+// each group to an fp64 total; a thread holding a value outside [2^-60,
+// 2^60] (where a square could leave fp32's normal range) sums its squares in
+// fp64 instead.  The thread totals are added in fp64 (a butterfly across the
+// warp, the warps in order); r = fp32_rn(1 / sqrt(ss / K + eps)) with IEEE
+// fp64 division and square root; t = bf16(x * r), h = bf16(t * gamma); then
+// the A2 quantizer on fp32(h) * smooth.  The per-group compensation errors
+// (below 64 x 2^-48 of the group's sum) and the order of the fp64 additions
+// move ss by well under 2^-39 relative from the correctly rounded sum, which
+// changes r only when 1 / sqrt(...) lies within a hair (2^-38 relative) of an
+// fp32 rounding midpoint.  (GB300 issues fp64 at a small fraction of the fp32
+// rate: an all-fp64 sum took ~15 us for 288 rows of 4096.)
 template <int VPT>
 __global__ void __launch_bounds__(THREADS) rms_quant_kernel(const uint16_t* __restrict__ in, int ld,
                                                             const uint16_t* __restrict__ gamma, float eps,
@@ -285,15 +293,35 @@ __global__ void __launch_bounds__(THREADS) rms_quant_kernel(const uint16_t* __re
   }
   float x[VPT][8];
   double ss = 0.0;
+  bool wide = false;   // a value outside [2^-60, 2^60] (not zero): square this thread's values in fp64
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int v = threadIdx.x + i * THREADS;
     if (v >= nvec) continue;
     bf16x8_to_f32(raw[i], x[i]);
+    float sg = 0.f, cg = 0.f;   // the group's running sum and the exact sum of its rounding errors
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const double d = (double)x[i][e];
-      ss = __dadd_rn(ss, __dmul_rn(d, d));
+      const uint32_t ex = (__float_as_uint(x[i][e]) >> 23) & 0xFFu;
+      wide |= x[i][e] != 0.f && (ex < 127u - 60u || ex > 127u + 60u);
+      const float y = __fmul_rn(x[i][e], x[i][e]);
+      const float t = __fadd_rn(sg, y);
+      cg = __fadd_rn(cg, __fadd_rn(__fsub_rn(fmaxf(sg, y), t), fminf(sg, y)));
+      sg = t;
+    }
+    ss = __dadd_rn(ss, __dadd_rn((double)sg, (double)cg));
+  }
+  if (wide) {
+    ss = 0.0;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = threadIdx.x + i * THREADS;
+      if (v >= nvec) continue;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const double d = (double)x[i][e];
+        ss = __dadd_rn(ss, __dmul_rn(d, d));
+      }
     }
   }
 #pragma unroll
