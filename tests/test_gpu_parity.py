@@ -103,6 +103,27 @@ def test_rmsnorm_smooth_quant_bit_exact(M, K):
         assert sa.cpu().numpy()[2] == 0 and not xq.cpu().numpy()[2].any()
 
 
+def test_rmsnorm_smooth_quant_extreme_magnitudes():
+    """Rows whose values leave [2^-60, 2^60], where the kernel squares in
+    fp64 instead of its compensated fp32 sums (a square could leave fp32's
+    normal range): N(0, 1) scaled by 2^70, 2^-70 and 2^100, a row mixing
+    2^65 and 2^-65, BF16 subnormals, and one ordinary row."""
+    M, K = 6, 4096
+    rng = np.random.default_rng(3100)
+    a = rng.standard_normal((M, K))
+    a[0] *= 2.0 ** 70
+    a[1] *= 2.0 ** -70
+    a[2, : K // 2] *= 2.0 ** 65
+    a[2, K // 2:] *= 2.0 ** -65
+    a[3] *= 2.0 ** 100
+    a[4] *= 2.0 ** -130
+    x = synth.f32_to_bf16_bits(a.astype(np.float32))
+    g = _norm_weight(3101, K)
+    s = np.exp(rng.uniform(-1, 1, K)).astype(np.float32)
+    xq, sa = q.rmsnorm_smooth_quant(dev_bf16(x), dev_bf16(g), dev(s), eps=1e-6)
+    assert _rms_compare(x, g, s, xq, sa) == 0
+
+
 def test_rmsnorm_smooth_quant_strided_and_empty():
     M, K, ld = 5, 4096, 4096 + 64
     full = synth.activations(3077, M, ld)

@@ -130,10 +130,14 @@ struct Cfg {
   static_assert(TMEM_A0 + S2 * A_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(STAGE1 % 1024 == 0 && B16_BLOCK % 1024 == 0, "1024B alignment of swizzled tiles");
   static_assert(S1 >= 2 && S2 >= 2, "pipeline depth");
-  // A cluster's partial sums (BM x NT int32) go over the INT8 ring, or over
-  // the converted ring when that is the larger one (both idle by then).
-  static constexpr bool PART_IN_B16 = BM * NT * 4 > S1 * STAGE1;
-  static_assert(BM * NT * 4 <= (PART_IN_B16 ? S2 * B16_BYTES : S1 * STAGE1), "cluster partial sums fit");
+  // The partial sums a CTA of a cluster receives (csize senders x NT columns
+  // x its share of the rows: at most 132 rows' worth, 3 x 44) go over the
+  // INT8 ring, or over the converted ring when that is the larger one (both
+  // idle by then).
+  static constexpr int PART_BYTES = 132 * NT * 4;
+  static constexpr bool PART_IN_B16 = PART_BYTES > S1 * STAGE1;
+  static_assert(PART_BYTES <= (PART_IN_B16 ? S2 * B16_BYTES : S1 * STAGE1), "cluster partial sums fit");
+  static_assert((BM + NT) * 4 <= (PART_IN_B16 ? S1 * STAGE1 : S2 * B16_BYTES), "epilogue scales fit");
   static_assert(SMEM <= SMEM_OPTIN, "shared memory budget");
   static_assert(NT % 16 == 0 && NT <= 256 && TOK % 4 == 0, "MMA N");
   static_assert(!WIDE || XH, "wide tiles take the fp16 token copy");
@@ -371,40 +375,84 @@ QUASAR_DEVICE_INLINE void cluster_barrier_exec() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
-// int4 at the same shared-memory offset in cluster CTA `rank`.
-QUASAR_DEVICE_INLINE int4 ld_cluster_int4(const void* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  int4 v;
-  asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(remote)
-               : "memory");
-  return v;
+
+// Cluster phase of a split tile (csize CTAs, one K part each).  CTA `rank`
+// finishes the rows [4 u0, 4 u1) of the tile (units of four rows split evenly
+// over the cluster).  Every CTA first pushes its int32 sums for those rows
+// into that CTA's shared memory (remote stores, which the sender does not
+// wait for; measured, pulling them with remote loads ran at ~30 GB/s per
+// SM), laid out [sender rank][token column][row - 4 u0] with a row stride of
+// RPR; after a release / acquire cluster barrier each CTA adds the csize
+// parts from its own shared memory and writes its rows (dequantized, or the
+// int32 sums).  Four consecutive rows per item: consecutive threads on
+// consecutive rows of Y.
+constexpr int RPR_MAX = 64;   // rows per rank of a cluster of 2 (the largest share)
+
+QUASAR_DEVICE_INLINE int rows_per_rank(int csize) { return (((BM / 4) + csize - 1) / csize) * 4; }
+QUASAR_DEVICE_INLINE int rank_first_unit(int r, int csize) { return r * (BM / 4) / csize; }
+
+QUASAR_DEVICE_INLINE void st_cluster_u32(uint32_t remote_addr, int32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote_addr), "r"(v) : "memory");
 }
 
-// Cluster phase of a split tile (csize CTAs, one K part each): every CTA has
-// left its int32 sums in `part` ([NT token columns][128 weight rows]); CTA
-// `rank` finishes rows [4 u0, 4 u1) of the tile, reading the other parts
-// through distributed shared memory, and writes them (dequantized, or the
-// int32 sums).  Four consecutive rows per item: one 16-byte load per part and
-// consecutive threads on consecutive rows of Y.
+QUASAR_DEVICE_INLINE uint32_t map_to_rank(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  return remote;
+}
+
+// This thread's TOK sums (weight row `row`, token columns h*TOK ..) pushed
+// to the CTA that finishes the row.
 template <int NT>
-QUASAR_DEVICE_INLINE void cluster_finalize(const Params& p, const int32_t* part, int t, int rank, int ct) {
+QUASAR_DEVICE_INLINE void cluster_push(const Params& p, int32_t* part, const int32_t (&acc)[NT / 4], int row, int h,
+                                       int my_rank) {
+  constexpr int TOK = NT / 4;
   const int csize = p.csize;
-  const int u0 = rank * (BM / 4) / csize, u1 = (rank + 1) * (BM / 4) / csize;
+  const int rpr = rows_per_rank(csize);
+  int owner = 0;
+  while (owner + 1 < csize && rank_first_unit(owner + 1, csize) * 4 <= row) ++owner;
+  const int lr = row - rank_first_unit(owner, csize) * 4;
+  const uint32_t base = map_to_rank(part, (uint32_t)owner);
+  const uint32_t at = base + (uint32_t)(((my_rank * NT + h * TOK) * rpr + lr) * 4);
+#pragma unroll
+  for (int jj = 0; jj < TOK; ++jj) st_cluster_u32(at + (uint32_t)(jj * rpr * 4), acc[jj]);
+}
+
+// The epilogue scales of tile t in shared memory (sw of its 128 weight rows,
+// then sa of its NT token rows), loaded ahead so that the finalize reads
+// no global memory.
+template <int NT>
+QUASAR_DEVICE_INLINE void stage_scales(const Params& p, float* sc, int t, int ct) {
+  const int n_base = (t / p.m_tiles) * BM;
+  const int m_base = (t % p.m_tiles) * NT;
+  if (p.acc_out) return;
+  for (int i = ct; i < BM + NT; i += CONV_WARPS * 32) {
+    if (i < BM) {
+      sc[i] = n_base + i < p.N ? __ldg(p.sw + n_base + i) : 0.f;
+    } else {
+      const int m = m_base + (i - BM);
+      sc[i] = m < p.M ? __ldg(p.sa + m) : 0.f;
+    }
+  }
+}
+
+template <int NT>
+QUASAR_DEVICE_INLINE void cluster_finalize(const Params& p, const int32_t* part, const float* sc, int t, int rank,
+                                           int ct) {
+  const int csize = p.csize;   // 2 .. 4
+  const int rpr = rows_per_rank(csize);
+  const int u0 = rank_first_unit(rank, csize), u1 = rank_first_unit(rank + 1, csize);
   const int nu = u1 - u0;
   const int n_base = (t / p.m_tiles) * BM;
   const int m_base = (t % p.m_tiles) * NT;
   for (int i = ct; i < nu * NT; i += CONV_WARPS * 32) {
-    const int col = i / nu;
-    const int u = u0 + (i - col * nu);
+    const int col = i / nu, lu = i - col * nu;
     const int m = m_base + col;
-    const int n = n_base + 4 * u;
+    const int n = n_base + 4 * (u0 + lu);
     if (m >= p.M || n >= p.N) continue;
     int4 v = make_int4(0, 0, 0, 0);
     for (int q = 0; q < csize; ++q) {
-      const int4 x = ld_cluster_int4(part + col * BM + 4 * u, (uint32_t)q);
+      const int4 x = *reinterpret_cast<const int4*>(part + (q * NT + col) * rpr + 4 * lu);
       v.x += x.x;
       v.y += x.y;
       v.z += x.z;
@@ -413,11 +461,12 @@ QUASAR_DEVICE_INLINE void cluster_finalize(const Params& p, const int32_t* part,
     if (p.acc_out) {
       *reinterpret_cast<int4*>(p.acc_out + (size_t)m * p.N + n) = v;
     } else {
-      const float sam = p.sa[m];
-      const float y0 = __fmul_rn(__fmul_rn(__int2float_rn(v.x), sam), p.sw[n]);
-      const float y1 = __fmul_rn(__fmul_rn(__int2float_rn(v.y), sam), p.sw[n + 1]);
-      const float y2 = __fmul_rn(__fmul_rn(__int2float_rn(v.z), sam), p.sw[n + 2]);
-      const float y3 = __fmul_rn(__fmul_rn(__int2float_rn(v.w), sam), p.sw[n + 3]);
+      const float sam = sc[BM + col];
+      const float4 swv = *reinterpret_cast<const float4*>(sc + n - n_base);
+      const float y0 = __fmul_rn(__fmul_rn(__int2float_rn(v.x), sam), swv.x);
+      const float y1 = __fmul_rn(__fmul_rn(__int2float_rn(v.y), sam), swv.y);
+      const float y2 = __fmul_rn(__fmul_rn(__int2float_rn(v.z), sam), swv.z);
+      const float y3 = __fmul_rn(__fmul_rn(__int2float_rn(v.w), sam), swv.w);
       const __nv_bfloat162 lo = __halves2bfloat162(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
       const __nv_bfloat162 hi = __halves2bfloat162(__float2bfloat16_rn(y2), __float2bfloat16_rn(y3));
       uint2 out;
@@ -553,8 +602,8 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
       }
     }
     __syncwarp();
-    if (p.csize > 1) {
-      cluster_barrier_full();
+    if (p.csize > 1) {   // the converters' two cluster barriers (no data of this warp crosses them)
+      cluster_barrier_exec();
       cluster_barrier_exec();
     }
   } else if (AUX && (warp == MMA_WARP || warp == WAITER_WARP)) {
@@ -610,8 +659,8 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
       mbar_wait(mma_done, 0, &dummy, p.err, SITE_GEMM_DRAIN, p.limit_ns);
     }
     __syncwarp();
-    if (p.csize > 1) {
-      cluster_barrier_full();
+    if (p.csize > 1) {   // the converters' two cluster barriers (no data of this warp crosses them)
+      cluster_barrier_exec();
       cluster_barrier_exec();
     }
   } else if (CONV && warp < CONV_WARPS) {
@@ -711,20 +760,22 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
                               m_tiles);
     __syncwarp();
     if (p.csize > 1) {
-      // Split tile of a cluster: this CTA's part of the sums goes to shared
-      // memory (over the INT8 ring, idle once every converter warp is past
-      // its last block), then the cluster adds the parts.
+      // Split tile of a cluster: the sums go to the CTA that finishes their
+      // rows, into its INT8 or converted ring, which the first barrier shows
+      // idle in every CTA (all blocks converted, every MMA complete).
       int32_t* part = reinterpret_cast<int32_t*>(C::PART_IN_B16 ? b16 : stage1);
-      named_barrier_or(CONV_BAR_ID, CONV_WARPS * 32, 0u);
-#pragma unroll
-      for (int jj = 0; jj < C::TOK; ++jj) part[(h * C::TOK + jj) * BM + row] = acc[jj];
-      cluster_barrier_full();
-      cluster_finalize<NT>(p, part, b0 / KB, (int)(blockIdx.x % (unsigned)p.csize), ct);
+      float* sc = reinterpret_cast<float*>(C::PART_IN_B16 ? stage1 : b16);   // the other ring: scales
+      const int my_rank = (int)(blockIdx.x % (unsigned)p.csize);
+      named_barrier_or(CONV_BAR_ID, CONV_WARPS * 32, 0u);   // every converter is past the rings
+      stage_scales<NT>(p, sc, b0 / KB, ct);
       cluster_barrier_exec();
+      cluster_push<NT>(p, part, acc, row, h, my_rank);
+      cluster_barrier_full();
+      cluster_finalize<NT>(p, part, sc, b0 / KB, my_rank, ct);
     }
   } else if (p.csize > 1) {
     // the spare warp of the fifth warpgroup
-    cluster_barrier_full();
+    cluster_barrier_exec();
     cluster_barrier_exec();
   }
 
