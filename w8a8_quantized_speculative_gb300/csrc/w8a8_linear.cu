@@ -17,33 +17,38 @@
 //    integer below 16129*1024 < 2^24 and fp32 holds it exactly.  Each run is
 //    drained to int32 registers (cvt.rni), so the result is the exact
 //    integer sum for any K.
-//  * Swap-AB: weight rows fill the MMA's M = 128 side, tokens the N side
-//    (NT = 16..128).  The weight tile is the A operand and lives in TMEM:
-//    converter warps read the INT8 tile from shared memory, widen it in
-//    registers and tcgen05.st it into TMEM.  Shared memory then carries ~2
-//    bytes per weight (one bulk-copy write + one read) instead of the ~6 a
-//    widened shared-memory A operand would cost.  The small token tile is
-//    widened into a 128B-swizzled K-major shared-memory B operand.
+//  * Swap-AB: weight rows fill the MMA's M = 128 side, tokens the N side:
+//    one token tile of up to 256 rows (two of 144 at 257-288 tokens), so each
+//    weight block is widened once per launch and meets every token in one
+//    instruction per K step.  A kind::f16 MMA of M = 128, K = 16 costs ~114
+//    cycles for any N <= 192 and ~138 at N = 256 (measured with
+//    quasar_probe_tensor_rate), so at a few tokens this kernel is bound by 8
+//    such instructions per 16 KB weight block, not by its operands.
+//  * The weight tile is the A operand and lives in TMEM: converter warps read
+//    the INT8 tile from shared memory, widen it in registers and tcgen05.st
+//    it into TMEM.  The token tile is the B operand in a 128B-swizzled
+//    K-major shared-memory layout, widened in the kernel for tiles of up to
+//    64 rows, or copied in already widened (an fp16 copy made once per call)
+//    by TMA for wider tiles.
 //  * Weights arrive pre-packed (quasar_pack_weights) as contiguous 16 KB
 //    blocks of 128 rows x 128 K, rows already in the 128B-swizzled order and
 //    each code stored biased by +128, so one 1-D bulk copy per block streams
-//    them from HBM and widening a byte takes no sign fix-up.  Tokens come
-//    through a 2-D TMA tensor map.
-//  * Persistent grid of one CTA per SM.  The (weight tile, K block) work list
-//    is split into equal contiguous ranges, one per CTA (stream-K style), so
-//    every SM streams the same number of weight bytes.  A CTA whose range
-//    covers a whole tile writes Y directly; partial tiles are summed with
-//    integer atomics (order-independent, so still exact and deterministic)
-//    into a zero-filled workspace.  Each converter warp owns the same
-//    32-row x NT/4-token sub-tile in every CTA, so completion is counted per
-//    (tile, warp): the warp whose K-block count completes the sub-tile (no
-//    warp ever waits on another CTA) applies the epilogue and re-zeroes the
-//    workspace slice and counter it used.
+//    them from HBM and widening a byte takes no sign fix-up.
+//  * Work split, chosen per shape by a cost in blocks (split_of): a cluster
+//    of 2-4 CTAs per weight tile, each a K part, the parts pushed into the
+//    CTA that finishes each row slice through distributed shared memory; K
+//    parts per tile summed with integer atomics into a zero-filled workspace
+//    (completion counted per (tile, converter warp): the warp that completes
+//    a sub-tile applies the epilogue and re-zeroes what it used; no CTA ever
+//    waits on another); whole tiles; or equal contiguous ranges of the
+//    (tile, K block) list over one CTA per SM (stream-K).
 //  * Programmatic dependent launch: the weight stream of the first stages
 //    starts before the previous kernel in the stream has finished; token
 //    loads and every global write wait for it (griddepcontrol.wait).
 //  * Warp roles: warps 0-15 convert (and drain / run the epilogue), warp 16
-//    issues the copies, warp 17 allocates TMEM and issues MMAs.
+//    issues the copies, warp 17 issues MMAs, warp 18 does every mbarrier
+//    wait for the MMA warp; tiles of >= 128 rows add a spare warp so that the
+//    fifth warpgroup can hand registers to the converters (setmaxnreg).
 #include <algorithm>
 #include <mutex>
 
