@@ -466,7 +466,7 @@ def main_gpu(args):
     extra = {}
     if rank == 0 and world == 1 and not args.no_extras:
         extra["sweep"] = run_sweep(q, dev, stream, ws, hbm)
-        extra["sweep_w4a8"] = run_sweep_w4(q, dev, stream, ws, hbm)
+        extra["sweep_w4a8"] = run_sweep_w4(q, dev, stream, ws, hbm, extra["sweep"])
         extra["verify"] = run_verify(q, dev, stream, ws, hbm)
         try:
             extra["tensor_probe"] = run_tensor_probe(q)
@@ -564,9 +564,11 @@ def run_sweep(q, dev, stream, ws, hbm):
     return out
 
 
-def run_sweep_w4(q, dev, stream, ws, hbm):
-    """The W4A8 variant (4-bit weight blocks, register-path kernel, M <= 24)
-    on the same linears, cold L2; bytes per weight halve."""
+def run_sweep_w4(q, dev, stream, ws, hbm, w8_rows=()):
+    """The W4A8 variant (4-bit weight blocks: the register-path kernel up to
+    24 tokens, the tcgen05 kernel above) on the same linears, cold L2; bytes
+    per weight halve.  `vs_w8a8`: the W8A8 sweep's time at the same shape
+    over this one (> 1: the 4-bit blocks are faster)."""
     import torch
     out = []
     gen = torch.Generator(device=dev)
@@ -578,15 +580,19 @@ def run_sweep_w4(q, dev, stream, ws, hbm):
         wps = [q.tile_weights_w4(w4) for _ in range(ncopy)]
         del w4
         sw = torch.rand(N, device=dev, generator=gen) * 1e-3
-        for M in (1, 8, 20):
+        for M in (1, 8, 16, 32, 64, 128, 256):
             xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
             sa = torch.rand(M, device=dev, generator=gen)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws.get(q.lib.quasar_w8a8_linear_workspace_size(M, N, K))
             us = _time_graph(torch, stream, lambda i: q.w4a8_linear(xq, sa, wps[i % ncopy], sw, y=y, workspace=ws), 60)
             tb = (N * K // 2 + 4 * N) / (us * 1e-6) / 1e12
-            out.append({"linear": name, "M": M, "us": round(us, 3), "weight_TBps": round(tb, 3),
-                        "hbm_frac": round(tb * 1e3 / hbm, 3)})
+            row = {"linear": name, "M": M, "us": round(us, 3), "weight_TBps": round(tb, 3),
+                   "hbm_frac": round(tb * 1e3 / hbm, 3)}
+            w8 = [r["us"] for r in w8_rows if r["linear"] == name and r["M"] == M]
+            if w8:
+                row["vs_w8a8"] = round(w8[0] / us, 3)
+            out.append(row)
         del wps
         torch.cuda.empty_cache()
     return out

@@ -292,10 +292,13 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
  *   quasar_pack_weights_w4: W [N][ldw] BF16 (ldw >= K, ldw % 8 == 0),
  *     smooth [K] fp32 -> Wp4 (K % 16 == 0), sw [N] fp32.
  *   quasar_tile_weights_w4: row-major codes [N][K] in [-8, 7] -> Wp4.
- *   quasar_w4a8_linear: as quasar_w8a8_linear with Wp4 for Wp, for
- *     1 <= M <= 24 (the register-path kernel; QUASAR_ERR_UNSUPPORTED
- *     above); workspace: quasar_w8a8_linear_workspace_size(M, N, K) bytes
- *     under the same zero-filled contract.
+ *   quasar_w4a8_linear: as quasar_w8a8_linear with Wp4 for Wp, same
+ *     argument rules, limits and error codes, any M >= 0 (the register-path
+ *     kernel up to 24 tokens, the tcgen05 kernel above, both reading the
+ *     4-bit blocks directly); workspace: quasar_w8a8_linear_workspace_size
+ *     (M, N, K) bytes under the same contract (the first
+ *     quasar_w8a8_linear_workspace_zeroed_bytes(M, N, K) zero on entry and
+ *     left zero).
  * ------------------------------------------------------------------------ */
 size_t quasar_packed_weight_bytes_w4(int N, int K);
 quasar_status_t quasar_pack_weights_w4(const void* W_bf16, int ldw, const float* smooth,

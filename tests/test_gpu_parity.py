@@ -788,7 +788,13 @@ def test_pack_weights_w4_bit_exact(name):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 16), (3, 136, 144), (8, 512, 256), (16, 4096, 4096), (20, 6144, 4096),
-                                   (24, 264, 2064), (12, 24576, 1024), (5, 19456, 512), (20, 4096, 12288)])
+                                   (24, 264, 2064), (12, 24576, 1024), (5, 19456, 512), (20, 4096, 12288),
+                                   # tcgen05 kernel: every token-tile width, ragged rows / K tails,
+                                   # cluster, K-part, whole-tile and stream-K splits
+                                   (25, 6144, 4096), (32, 4096, 4096), (40, 24576, 4096), (64, 6144, 4096),
+                                   (65, 520, 1040), (100, 264, 2064), (128, 4096, 12288), (145, 4096, 4096),
+                                   (192, 6144, 4096), (200, 136, 144), (256, 4096, 12288), (288, 6144, 4096),
+                                   (300, 512, 512), (33, 19456, 512)])
 def test_w4a8_linear_matches_oracle(M, N, K):
     rng = np.random.default_rng(M * 31 + N + K)
     xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
@@ -822,11 +828,26 @@ def test_w4a8_qwen3_attention_end_to_end():
         assert np.linalg.norm(yv - ref) / np.linalg.norm(ref) <= 0.3, case.name
 
 
-def test_w4a8_rejects_large_m():
-    xq = torch.zeros((32, 256), dtype=torch.int8, device="cuda")
-    wp = q.tile_weights_w4(torch.zeros((128, 256), dtype=torch.int8, device="cuda"))
-    with pytest.raises(q.QuasarError):
-        q.w4a8_linear(xq, torch.ones(32, device="cuda"), wp, torch.ones(128, device="cuda"))
+@pytest.mark.parametrize("name", ["qkv", "o", "gate_up", "down"])
+@pytest.mark.parametrize("M", [25, 40, 64, 96, 160, 224, 288])
+def test_w4a8_equals_w8a8_on_4bit_codes(name, M):
+    """Codes in [-8, 7] packed both ways: the 4-bit and the 8-bit kernels sum
+    the same integers, so the outputs are bit-identical whatever work split
+    each picks at the Qwen3-8B layer shapes (the two variants' shared-memory
+    budgets differ, so their cluster residency and split choices can)."""
+    K, N = synth.LINEARS[name]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(M * 7 + N)
+    wq = torch.randint(-8, 8, (N, K), dtype=torch.int8, device="cuda", generator=gen)
+    xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device="cuda", generator=gen)
+    sa = torch.rand(M, device="cuda", generator=gen) * 0.1
+    sw = torch.rand(N, device="cuda", generator=gen) * 1e-2
+    ws = q.Workspace()
+    y4 = q.w4a8_linear(xq, sa, q.tile_weights_w4(wq), sw, workspace=ws)
+    check_ws_zero(ws)
+    y8 = q.w8a8_linear(xq, sa, q.tile_weights(wq), sw, workspace=ws)
+    assert torch.equal(y4.view(torch.int16), y8.view(torch.int16))
+    assert q.get_device_error()[0] == 0
 
 
 # ---------------------------------------------------------------- documented limits

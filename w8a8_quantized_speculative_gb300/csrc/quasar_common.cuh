@@ -323,4 +323,17 @@ QUASAR_DEVICE_INLINE void u8x4_to_f16x4(uint32_t u, uint32_t& lo, uint32_t& hi) 
   hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
+// Four bytes, each holding a 4-bit code + 8 (code in [-8, 7]) -> two fp16x2
+// words holding the codes exactly: the byte goes into the low mantissa of
+// 1024 (0x6400) and 1032 = 1024 + 8 is subtracted.
+QUASAR_DEVICE_INLINE void n4x4_to_f16x4(uint32_t u, uint32_t& lo, uint32_t& hi) {
+  uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+  uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
 }  // namespace quasar

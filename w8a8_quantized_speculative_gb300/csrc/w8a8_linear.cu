@@ -33,7 +33,9 @@
 //  * Weights arrive pre-packed (quasar_pack_weights) as contiguous 16 KB
 //    blocks of 128 rows x 128 K, rows already in the 128B-swizzled order and
 //    each code stored biased by +128, so one 1-D bulk copy per block streams
-//    them from HBM and widening a byte takes no sign fix-up.
+//    them from HBM and widening a byte takes no sign fix-up.  The W4A8
+//    variant streams 8 KB blocks of 4-bit codes (quasar_pack_weights_w4) and
+//    widens nibbles instead; the rest of the kernel is the same.
 //  * Work split, chosen per shape by a cost in blocks (split_of): a cluster
 //    of 2-4 CTAs per weight tile, each a K part, the parts pushed into the
 //    CTA that finishes each row slice through distributed shared memory; K
@@ -94,8 +96,10 @@ __host__ __device__ constexpr uint32_t idesc() {
 // already widened to fp16 (one copy per call in the workspace, or written by
 // the quantizer of the one-call entry) and are copied by TMA straight into
 // the MMA's B layout; the converters then widen only the weights, and the
-// INT8 ring carries weight blocks alone.
-template <int NT, bool XH = false>
+// INT8 ring carries weight blocks alone.  W4: the weights arrive as 4-bit
+// blocks (quasar_pack_weights_w4: 8 KB per 128 x 128 block) and are widened
+// from nibbles; everything after the widening is the INT8 kernel's.
+template <int NT, bool XH = false, bool W4 = false>
 struct Cfg {
   // Wide tiles (NT >= 128) keep NT/4 int32 run sums per converter thread.
   // A fifth warpgroup (copy, MMA, waiter and one spare warp) lets the block
@@ -121,13 +125,15 @@ struct Cfg {
   // that the operand bytes in flight cover the copy latency at each width.
   static constexpr int S2 = XH ? (NT == 256 ? 3 : NT == 192 ? 2 : NT == 144 ? 3 : NT == 128 ? 4 : 2)
                                : (NT == 64 ? 2 : 3);
-  static constexpr int W_BYTES = G * BLOCK_BYTES;            // INT8 weight blocks of a stage
+  static constexpr int WBLK = W4 ? BLOCK_BYTES / 2 : BLOCK_BYTES;   // bytes of one packed weight block
+  static constexpr int W_BYTES = G * WBLK;                   // weight blocks of a stage
   static constexpr int XB_BYTES = XH ? 0 : NT * BK;          // INT8 token tile of one block
   static constexpr int STAGE1 = W_BYTES + G * XB_BYTES;      // multiple of 1024
   static constexpr int B16_BLOCK = NT * BK * 2;              // fp16 token tile of one block (2 atoms)
   static constexpr int B16_BYTES = G * B16_BLOCK;
   static constexpr int S1_FIT = (SMEM_OPTIN - 1024 - 256 - S2 * B16_BYTES) / STAGE1;
-  static constexpr int S1 = XH ? (S1_FIT < 8 ? S1_FIT : 8) : (NT == 16) ? 5 : (NT == 32) ? 4 : 3;
+  // (4-bit blocks: as many stages as fit, up to 8, for the same bytes in flight)
+  static constexpr int S1 = (XH || W4) ? (S1_FIT < 8 ? S1_FIT : 8) : (NT == 16) ? 5 : (NT == 32) ? 4 : 3;
   static constexpr int TOK = NT / 4;                         // accumulator columns per converter thread
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = 1024 + S1 * STAGE1 + S2 * B16_BYTES + BAR_BYTES;
@@ -137,12 +143,21 @@ struct Cfg {
   static_assert(S1 >= 2 && S2 >= 2, "pipeline depth");
   // The partial sums a CTA of a cluster receives (csize senders x NT columns
   // x its share of the rows: at most 132 rows' worth, 3 x 44) go over the
-  // INT8 ring, or over the converted ring when that is the larger one (both
-  // idle by then).
+  // INT8 ring and the epilogue scales over the converted ring (both idle by
+  // then), or the other way round when the converted ring is the one that
+  // holds the sums; where neither does (4-bit blocks at 192-row tiles) the
+  // sums span both rings, which are contiguous, and the scales take the
+  // converted ring's last KB.  Offsets from the start of the INT8 ring.
   static constexpr int PART_BYTES = 132 * NT * 4;
-  static constexpr bool PART_IN_B16 = PART_BYTES > S1 * STAGE1;
-  static_assert(PART_BYTES <= (PART_IN_B16 ? S2 * B16_BYTES : S1 * STAGE1), "cluster partial sums fit");
-  static_assert((BM + NT) * 4 <= (PART_IN_B16 ? S1 * STAGE1 : S2 * B16_BYTES), "epilogue scales fit");
+  static constexpr int SC_BYTES = (BM + NT) * 4;
+  static constexpr int PART_MODE = PART_BYTES <= S1 * STAGE1 ? 0 : PART_BYTES <= S2 * B16_BYTES ? 1 : 2;
+  static constexpr int PART_OFF = PART_MODE == 1 ? S1 * STAGE1 : 0;
+  static constexpr int SC_OFF = PART_MODE == 0 ? S1 * STAGE1
+                                : PART_MODE == 1 ? 0
+                                                 : S1 * STAGE1 + S2 * B16_BYTES - ((SC_BYTES + 1023) & ~1023);
+  static_assert(PART_MODE != 2 || PART_BYTES <= SC_OFF, "cluster partial sums fit");
+  static_assert(SC_BYTES <= (PART_MODE == 0 ? S2 * B16_BYTES : PART_MODE == 1 ? S1 * STAGE1 : SC_BYTES),
+                "epilogue scales fit");
   static_assert(SMEM <= SMEM_OPTIN, "shared memory budget");
   static_assert(NT % 16 == 0 && NT <= 256 && TOK % 4 == 0, "MMA N");
   static_assert(!WIDE || XH, "wide tiles take the fp16 token copy");
@@ -487,14 +502,14 @@ QUASAR_DEVICE_INLINE void cluster_finalize(const Params& p, const int32_t* part,
 // alone, so that each copy is compiled under its own register limit.
 enum Roles { ROLES_ALL = 0, ROLES_CONV = 1, ROLES_AUX = 2 };
 
-template <int NT, bool XH, int ROLES>
+template <int NT, bool XH, bool W4, int ROLES>
 QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
-  using C = Cfg<NT, XH>;
+  using C = Cfg<NT, XH, W4>;
   constexpr bool CONV = ROLES != ROLES_AUX;   // this copy runs the converter warps
   constexpr bool AUX = ROLES != ROLES_CONV;   // this copy runs the copy / MMA / waiter warps
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stage1 = smem;                                  // S1 x [W 16KB | X NT*128]
+  uint8_t* stage1 = smem;                                  // S1 x [W G x WBLK | X G x NT*128]
   uint8_t* b16 = smem + C::S1 * C::STAGE1;                 // S2 x [2 atoms][NT][128B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(b16 + C::S2 * C::B16_BYTES);
   uint64_t* full1 = bars;                     // [S1] copies -> converters
@@ -551,9 +566,9 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
       {
         Walk<C::G> w(b0, b1, KB);
         for (; pre < C::S1 && w.more(); ++pre, w.next(KB)) {
-          mbar_arrive_expect_tx(&full1[pre], (uint32_t)(w.g * (BLOCK_BYTES + C::XB_BYTES)));
-          bulk_load(stage1 + pre * C::STAGE1, p.wp + ((size_t)(w.t / m_tiles) * KB + w.kb) * BLOCK_BYTES,
-                    (uint32_t)(w.g * BLOCK_BYTES), &full1[pre], pol_w);
+          mbar_arrive_expect_tx(&full1[pre], (uint32_t)(w.g * (C::WBLK + C::XB_BYTES)));
+          bulk_load(stage1 + pre * C::STAGE1, p.wp + ((size_t)(w.t / m_tiles) * KB + w.kb) * C::WBLK,
+                    (uint32_t)(w.g * C::WBLK), &full1[pre], pol_w);
         }
       }
       pdl_wait();  // tokens are written by the previous kernel
@@ -564,8 +579,8 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
         uint8_t* st = stage1 + rg.s * C::STAGE1;
         if (issued >= pre) {
           if (!mbar_wait(&empty1[rg.s], rg.ph ^ 1u, abort_flag, p.err, SITE_GEMM_EMPTY1, p.limit_ns)) break;
-          mbar_arrive_expect_tx(&full1[rg.s], (uint32_t)(w.g * (BLOCK_BYTES + C::XB_BYTES)));
-          bulk_load(st, p.wp + ((size_t)(w.t / m_tiles) * KB + w.kb) * BLOCK_BYTES, (uint32_t)(w.g * BLOCK_BYTES),
+          mbar_arrive_expect_tx(&full1[rg.s], (uint32_t)(w.g * (C::WBLK + C::XB_BYTES)));
+          bulk_load(st, p.wp + ((size_t)(w.t / m_tiles) * KB + w.kb) * C::WBLK, (uint32_t)(w.g * C::WBLK),
                     &full1[rg.s], pol_w);
         }
         if (!XH)
@@ -698,18 +713,30 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
 
       const uint8_t* st = stage1 + r1.s * C::STAGE1;
       // A: this thread's weight row, K quarter h of each block (2 swizzled
-      // 16-byte chunks per block).
+      // 16-byte chunks per block; 4-bit blocks: one chunk, 64-byte rows).
       for (int b = 0; b < w.g; ++b) {
         uint32_t a[16];
-        const uint8_t* wrow = st + b * BLOCK_BYTES + row * 128;
+        if constexpr (W4) {
+          // Byte 4 i + j holds code(32 h + 4 i + j) + 8 in its low nibble and
+          // code(32 h + 16 + 4 i + j) + 8 in its high nibble.
+          const uint4 v = *reinterpret_cast<const uint4*>(st + b * C::WBLK + row * 64 + ((h ^ ((row >> 1) & 3)) << 4));
+          const uint32_t d[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int c = 2 * h + i;
-          const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((c ^ (row & 7)) << 4));
-          u8x4_to_f16x4(v.x, a[8 * i + 0], a[8 * i + 1]);   // packed bytes are code + 128
-          u8x4_to_f16x4(v.y, a[8 * i + 2], a[8 * i + 3]);
-          u8x4_to_f16x4(v.z, a[8 * i + 4], a[8 * i + 5]);
-          u8x4_to_f16x4(v.w, a[8 * i + 6], a[8 * i + 7]);
+          for (int i = 0; i < 4; ++i) {
+            n4x4_to_f16x4(d[i] & 0x0F0F0F0Fu, a[2 * i], a[2 * i + 1]);
+            n4x4_to_f16x4((d[i] >> 4) & 0x0F0F0F0Fu, a[8 + 2 * i], a[9 + 2 * i]);
+          }
+        } else {
+          const uint8_t* wrow = st + b * BLOCK_BYTES + row * 128;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = 2 * h + i;
+            const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((c ^ (row & 7)) << 4));
+            u8x4_to_f16x4(v.x, a[8 * i + 0], a[8 * i + 1]);   // packed bytes are code + 128
+            u8x4_to_f16x4(v.y, a[8 * i + 2], a[8 * i + 3]);
+            u8x4_to_f16x4(v.z, a[8 * i + 4], a[8 * i + 5]);
+            u8x4_to_f16x4(v.w, a[8 * i + 6], a[8 * i + 7]);
+          }
         }
         tmem_st16(tmem + lane_off + (uint32_t)(C::TMEM_A0 + r2.s * C::A_COLS + b * (BK / 2) + 16 * h), a);
       }
@@ -766,10 +793,10 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
     __syncwarp();
     if (p.csize > 1) {
       // Split tile of a cluster: the sums go to the CTA that finishes their
-      // rows, into its INT8 or converted ring, which the first barrier shows
-      // idle in every CTA (all blocks converted, every MMA complete).
-      int32_t* part = reinterpret_cast<int32_t*>(C::PART_IN_B16 ? b16 : stage1);
-      float* sc = reinterpret_cast<float*>(C::PART_IN_B16 ? stage1 : b16);   // the other ring: scales
+      // rows, into its rings, which the first barrier shows idle in every
+      // CTA (all blocks converted, every MMA complete).
+      int32_t* part = reinterpret_cast<int32_t*>(stage1 + C::PART_OFF);
+      float* sc = reinterpret_cast<float*>(stage1 + C::SC_OFF);
       const int my_rank = (int)(blockIdx.x % (unsigned)p.csize);
       named_barrier_or(CONV_BAR_ID, CONV_WARPS * 32, 0u);   // every converter is past the rings
       stage_scales<NT>(p, sc, b0 / KB, ct);
@@ -792,23 +819,23 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
   }
 }
 
-template <int NT, bool XH = false>
-__global__ void __launch_bounds__(Cfg<NT, XH>::THREADS, 1)
+template <int NT, bool XH = false, bool W4 = false>
+__global__ void __launch_bounds__(Cfg<NT, XH, W4>::THREADS, 1)
 w8a8_linear_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
-  using C = Cfg<NT, XH>;
+  using C = Cfg<NT, XH, W4>;
   if constexpr (C::WIDE) {
     // Move registers from the fifth warpgroup to the converters before
     // anything else runs (warpgroup-uniform: warps 0-15 and 16-19); each
     // side then runs its own copy of the body under its own limit.
     if ((threadIdx.x >> 5) < CONV_WARPS) {
       regs_inc<C::REGS_CONV>();
-      linear_body<NT, XH, ROLES_CONV>(tmX, p);
+      linear_body<NT, XH, W4, ROLES_CONV>(tmX, p);
     } else {
       regs_dec<C::REGS_AUX>();
-      linear_body<NT, XH, ROLES_AUX>(tmX, p);
+      linear_body<NT, XH, W4, ROLES_AUX>(tmX, p);
     }
   } else {
-    linear_body<NT, XH, ROLES_ALL>(tmX, p);
+    linear_body<NT, XH, W4, ROLES_ALL>(tmX, p);
   }
 }
 
@@ -906,9 +933,9 @@ __global__ void __launch_bounds__(256) widen_tokens_kernel(const int8_t* __restr
 // Wide variants rely on the block's register split: the launch count must
 // leave the converters' increase covered by what the fifth warpgroup gives
 // back.  Checked once per device against the compiled kernel; 0 = usable.
-template <int NT, bool XH>
+template <int NT, bool XH, bool W4>
 static cudaError_t check_split(int dev) {
-  using C = Cfg<NT, XH>;
+  using C = Cfg<NT, XH, W4>;
   if constexpr (!C::WIDE) {
     return cudaSuccess;
   } else {
@@ -916,7 +943,7 @@ static cudaError_t check_split(int dev) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!state[dev]) {
       cudaFuncAttributes fa;
-      cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_linear_kernel<NT, XH>);
+      cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_linear_kernel<NT, XH, W4>);
       if (e != cudaSuccess) return e;
       const int r = fa.numRegs;
       const bool ok = r >= C::REGS_AUX && r <= C::REGS_CONV &&
@@ -927,25 +954,25 @@ static cudaError_t check_split(int dev) {
   }
 }
 
-template <int NT, bool XH>
+template <int NT, bool XH, bool W4>
 static cudaError_t configure(int dev) {
   static int configured[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(w8a8_linear_kernel<NT, XH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<NT, XH>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(w8a8_linear_kernel<NT, XH, W4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NT, XH, W4>::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  return check_split<NT, XH>(dev);
+  return check_split<NT, XH, W4>(dev);
 }
 
-template <int NT, bool XH>
+template <int NT, bool XH, bool W4>
 static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(Cfg<NT, XH>::THREADS);
-  cfg.dynamicSmemBytes = Cfg<NT, XH>::SMEM;
+  cfg.blockDim = dim3(Cfg<NT, XH, W4>::THREADS);
+  cfg.dynamicSmemBytes = Cfg<NT, XH, W4>::SMEM;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -960,17 +987,17 @@ static cudaLaunchConfig_t config_of(int grid, int csize, cudaStream_t stream, cu
 
 // Clusters of `csize` CTAs of this variant the device keeps resident at once
 // (0 if unknown); cached per device and size.
-template <int NT, bool XH>
+template <int NT, bool XH, bool W4>
 static int resident_clusters(int dev, int csize) {
   static int cache[64][5];
   static bool init[64][5] = {};
   if (dev < 0 || dev >= 64 || csize < 2 || csize > 4) return 0;
   if (!init[dev][csize]) {
     int n = 0;
-    if (configure<NT, XH>(dev) == cudaSuccess) {
+    if (configure<NT, XH, W4>(dev) == cudaSuccess) {
       cudaLaunchAttribute attr[2];
-      cudaLaunchConfig_t cfg = config_of<NT, XH>(csize * 8, csize, nullptr, attr);
-      if (cudaOccupancyMaxActiveClusters(&n, w8a8_linear_kernel<NT, XH>, &cfg) != cudaSuccess) n = 0;
+      cudaLaunchConfig_t cfg = config_of<NT, XH, W4>(csize * 8, csize, nullptr, attr);
+      if (cudaOccupancyMaxActiveClusters(&n, w8a8_linear_kernel<NT, XH, W4>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     cache[dev][csize] = n;
@@ -979,18 +1006,38 @@ static int resident_clusters(int dev, int csize) {
   return cache[dev][csize];
 }
 
-template <int NT, bool XH = false>
+template <int NT, bool XH, bool W4>
 static cudaError_t launch_nt(const CUtensorMap& tx, const Params& p, int grid, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaError_t e = configure<NT, XH>(dev);
+  cudaError_t e = configure<NT, XH, W4>(dev);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = config_of<NT, XH>(grid, p.csize, stream, attr);
-  return cudaLaunchKernelEx(&cfg, w8a8_linear_kernel<NT, XH>, tx, p);
+  cudaLaunchConfig_t cfg = config_of<NT, XH, W4>(grid, p.csize, stream, attr);
+  return cudaLaunchKernelEx(&cfg, w8a8_linear_kernel<NT, XH, W4>, tx, p);
+}
+
+// The variant for a tile width: fp16 token copy (xh) or in-kernel widening.
+template <bool W4>
+static cudaError_t launch_tc(int nt, bool xh, const CUtensorMap& tx, const Params& p, int grid, cudaStream_t stream) {
+  if (xh) {
+    switch (nt) {
+      case 64: return launch_nt<64, true, W4>(tx, p, grid, stream);
+      case 128: return launch_nt<128, true, W4>(tx, p, grid, stream);
+      case 144: return launch_nt<144, true, W4>(tx, p, grid, stream);
+      case 192: return launch_nt<192, true, W4>(tx, p, grid, stream);
+      default: return launch_nt<256, true, W4>(tx, p, grid, stream);
+    }
+  }
+  switch (nt) {   // tiles of >= 128 rows always take the fp16 copy
+    case 16: return launch_nt<16, false, W4>(tx, p, grid, stream);
+    case 32: return launch_nt<32, false, W4>(tx, p, grid, stream);
+    default: return launch_nt<64, false, W4>(tx, p, grid, stream);
+  }
 }
 
 // Resident clusters of `csize` CTAs for the variant a shape launches.
+template <bool W4>
 static int resident_for(const Shape& s, bool xh, int csize) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -999,28 +1046,29 @@ static int resident_for(const Shape& s, bool xh, int csize) {
   }
   if (xh) {
     switch (s.NT) {
-      case 64: return resident_clusters<64, true>(dev, csize);
-      case 128: return resident_clusters<128, true>(dev, csize);
-      case 144: return resident_clusters<144, true>(dev, csize);
-      case 192: return resident_clusters<192, true>(dev, csize);
-      default: return resident_clusters<256, true>(dev, csize);
+      case 64: return resident_clusters<64, true, W4>(dev, csize);
+      case 128: return resident_clusters<128, true, W4>(dev, csize);
+      case 144: return resident_clusters<144, true, W4>(dev, csize);
+      case 192: return resident_clusters<192, true, W4>(dev, csize);
+      default: return resident_clusters<256, true, W4>(dev, csize);
     }
   }
   switch (s.NT) {
-    case 16: return resident_clusters<16, false>(dev, csize);
-    case 32: return resident_clusters<32, false>(dev, csize);
-    default: return resident_clusters<64, false>(dev, csize);
+    case 16: return resident_clusters<16, false, W4>(dev, csize);
+    case 32: return resident_clusters<32, false, W4>(dev, csize);
+    default: return resident_clusters<64, false, W4>(dev, csize);
   }
 }
 
 // Whether the wide variant for this tile width can run on the current device.
+template <bool W4>
 static bool wide_usable(int nt) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  cudaError_t e = nt == 128   ? check_split<128, true>(dev)
-                  : nt == 144 ? check_split<144, true>(dev)
-                  : nt == 192 ? check_split<192, true>(dev)
-                              : check_split<256, true>(dev);
+  cudaError_t e = nt == 128   ? check_split<128, true, W4>(dev)
+                  : nt == 144 ? check_split<144, true, W4>(dev)
+                  : nt == 192 ? check_split<192, true, W4>(dev)
+                              : check_split<256, true, W4>(dev);
   if (e != cudaSuccess) cudaGetLastError();
   return e == cudaSuccess;
 }
@@ -1047,6 +1095,7 @@ struct Split {
   int csize;
 };
 
+template <bool W4>
 static Split split_of(const Shape& s, bool xh, int sms) {
   // a split tile's atomics and read-back cost ~5 blocks' time at narrow
   // tiles, ~10 at tiles of 192 or more tokens (measured 5-12 us at 256)
@@ -1065,7 +1114,7 @@ static Split split_of(const Shape& s, bool xh, int sms) {
     }
     for (int C = 2; C <= std::min(pmax, 4); ++C) {
       const long long cost = (s.KB + C - 1) / C + rho_cluster;
-      if (cost < best_cost && resident_for(s, xh, C) >= s.tiles) {
+      if (cost < best_cost && resident_for<W4>(s, xh, C) >= s.tiles) {
         best_cost = cost;
         best = Split{s.tiles * C, 0, C};
       }
@@ -1079,9 +1128,10 @@ static Split split_of(const Shape& s, bool xh, int sms) {
 
 // `xh_ext` (optional, the one-call entry): the token codes already widened to
 // fp16 [M][K] by the quantizer; 64- to 128-token tiles then take them from there.
+// `w4`: Wp holds 4-bit packed weights (quasar_pack_weights_w4).
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
                     void* Y, int ldy, int32_t* acc_out, void* ws, size_t ws_bytes, cudaStream_t stream,
-                    const void* xh_ext = nullptr) {
+                    const void* xh_ext = nullptr, bool w4 = false) {
   if (M < 0 || N <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
   if (K % 16 != 0 || N % 8 != 0 || K > 131072) return QUASAR_ERR_UNSUPPORTED;
   if (!acc_out && (ldy < N || ldy % 8 != 0)) return QUASAR_ERR_UNSUPPORTED;
@@ -1100,10 +1150,10 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   // A few tokens: the register-path kernel (same packed weights, same
   // workspace layout, fewer counters per tile).
   if (skinny::handles(M))
-    return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream, false);
+    return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream, w4);
   // Wide tiles whose register split the device cannot honour fall back to
   // 64-row tiles (fewer counters and no fp16 copy: the workspace suffices).
-  if (s.NT >= 128 && !wide_usable(s.NT)) s = shape_with(M, N, K, 64);
+  if (s.NT >= 128 && !(w4 ? wide_usable<true>(s.NT) : wide_usable<false>(s.NT))) s = shape_with(M, N, K, 64);
 
   const bool ext = xh_ext != nullptr && s.NT >= 64;
   const bool xh_path = ext || use_xh(M, s);
@@ -1140,7 +1190,7 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
 
   const int sms = sm_count();
   if (sms <= 0) return QUASAR_ERR_CUDA;
-  const Split sp = split_of(s, xh_path, sms);
+  const Split sp = w4 ? split_of<true>(s, xh_path, sms) : split_of<false>(s, xh_path, sms);
   const int grid = sp.grid;
   p.tile_ranges = sp.tile_ranges;
   p.csize = sp.csize;
@@ -1157,48 +1207,14 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
     wc.attrs = wa;
     wc.numAttrs = 1;
     e = ext ? cudaSuccess : cudaLaunchKernelEx(&wc, widen_tokens_kernel, Xq, n16, xh);
-    if (e == cudaSuccess) {
-      switch (s.NT) {
-        case 64: e = launch_nt<64, true>(tx, p, grid, stream); break;
-        case 128: e = launch_nt<128, true>(tx, p, grid, stream); break;
-        case 144: e = launch_nt<144, true>(tx, p, grid, stream); break;
-        case 192: e = launch_nt<192, true>(tx, p, grid, stream); break;
-        default: e = launch_nt<256, true>(tx, p, grid, stream); break;
-      }
-    }
+    if (e == cudaSuccess)
+      e = w4 ? launch_tc<true>(s.NT, true, tx, p, grid, stream) : launch_tc<false>(s.NT, true, tx, p, grid, stream);
     // leave the workspace zero-filled (the internal fp16 copy is scratch of this call)
     if (e == cudaSuccess && !ext) e = cudaMemsetAsync(xh, 0, (size_t)M * K * 2, stream);
     return cuda_status(e);
   }
-  switch (s.NT) {   // tiles of >= 128 rows always take the fp16 copy above
-    case 16: e = launch_nt<16>(tx, p, grid, stream); break;
-    case 32: e = launch_nt<32>(tx, p, grid, stream); break;
-    default: e = launch_nt<64>(tx, p, grid, stream); break;
-  }
+  e = w4 ? launch_tc<true>(s.NT, false, tx, p, grid, stream) : launch_tc<false>(s.NT, false, tx, p, grid, stream);
   return cuda_status(e);
-}
-
-// ------------------------------------------------------------ 4-bit weights
-//
-// W4A8: the register-path kernel with 4-bit weight blocks (same schedules,
-// same workspace); the token counts it serves (M <= 24) are where the weight
-// stream sets the time.
-quasar_status_t run_w4(const int8_t* Xq, const float* sa, const int8_t* Wp4, const float* sw, int M, int N, int K,
-                       void* Y, int ldy, int32_t* acc_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  if (M < 0 || N <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
-  if (K % 16 != 0 || N % 8 != 0 || K > 131072) return QUASAR_ERR_UNSUPPORTED;
-  if (!acc_out && (ldy < N || ldy % 8 != 0)) return QUASAR_ERR_UNSUPPORTED;
-  if (M == 0) return QUASAR_OK;
-  if (!skinny::handles(M)) return QUASAR_ERR_UNSUPPORTED;
-  if (!Xq || !Wp4 || (!acc_out && (!Y || !sa || !sw))) return QUASAR_ERR_INVALID_ARG;
-  if (!aligned(Xq, 16) || !aligned(Wp4, 16) || (Y && !aligned(Y, 16)) || (acc_out && !aligned(acc_out, 16)) ||
-      (sa && !aligned(sa, 4)) || (sw && !aligned(sw, 4)))
-    return QUASAR_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < workspace_size(M, N, K) || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
-  const Shape s = shape_of(M, N, K);
-  uint32_t* ws_cnt = reinterpret_cast<uint32_t*>(ws);
-  void* slots = reinterpret_cast<uint8_t*>(ws) + cnt_bytes(M, N, K);
-  return skinny::run(Xq, sa, Wp4, sw, M, N, K, Y, ldy, acc_out, ws_cnt, slots, stream, true);
 }
 
 // ------------------------------------------------------ fused activation path
@@ -1318,8 +1334,10 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa, const int8
 quasar_status_t quasar_w4a8_linear(const int8_t* Xq, const float* sa, const int8_t* Wp4, const float* sw, int M,
                                    int N, int K, void* Y_bf16, int ldy, void* workspace, size_t ws_bytes,
                                    quasar_stream_t stream) {
-  return quasar::gemm::run_w4(Xq, sa, Wp4, sw, M, N, K, Y_bf16, ldy, nullptr, workspace, ws_bytes,
-                              reinterpret_cast<cudaStream_t>(stream));
+  // 4-bit weight blocks on both kernels: the register path up to 24 tokens,
+  // the tcgen05 kernel (nibbles widened by the converters) above.
+  return quasar::gemm::run(Xq, sa, Wp4, sw, M, N, K, Y_bf16, ldy, nullptr, workspace, ws_bytes,
+                           reinterpret_cast<cudaStream_t>(stream), nullptr, true);
 }
 
 quasar_status_t quasar_int8_gemm_s32(const int8_t* Xq, const int8_t* Wp, int M, int N, int K, int32_t* acc,

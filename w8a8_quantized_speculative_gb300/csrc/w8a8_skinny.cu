@@ -408,18 +408,6 @@ QUASAR_DEVICE_INLINE void count_segments(const Params& p, int ua, int na, int ub
 // One K block of this warp's work: its two K steps of the unit's 64 rows
 // against every token tile.  Token operands: row n = 8 ni + g of the
 // swizzled tile sits at n * 128, chunk ch at (ch ^ (n & 7)) * 16.
-// Four bytes, each holding a 4-bit code + 8 (code in [-8, 7]) -> two fp16x2
-// words holding the codes exactly: the byte goes into the low mantissa of
-// 1024 (0x6400) and 1032 = 1024 + 8 is subtracted.
-QUASAR_DEVICE_INLINE void n4x4_to_f16x4(uint32_t u, uint32_t& lo, uint32_t& hi) {
-  uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
-  uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
-  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
-  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
-  lo = *reinterpret_cast<uint32_t*>(&ha);
-  hi = *reinterpret_cast<uint32_t*>(&hb);
-}
 
 template <int NT8, bool W4>
 QUASAR_DEVICE_INLINE void consume_block(uint32_t st, uint32_t a_off, uint32_t b_off, float (&acc)[UT][NT8][4]) {

@@ -237,7 +237,7 @@ def tile_weights_w4(wq: torch.Tensor, wp=None, stream=None):
 
 
 def w4a8_linear(xq, sa, wp4, sw, y=None, workspace: Workspace | None = None, stream=None):
-    """Y bf16 [M][N] from INT8 codes and 4-bit packed weights (M <= 24)."""
+    """Y bf16 [M][N] from INT8 codes and 4-bit packed weights (any M)."""
     _need(xq, torch.int8, "xq")
     _need(wp4, torch.int8, "wp4")
     M, K = xq.shape
