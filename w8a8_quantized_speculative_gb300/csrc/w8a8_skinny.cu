@@ -76,6 +76,7 @@ constexpr int PRODUCER_WARP = CWARPS;
 constexpr int THREADS = 32 * (CWARPS + 1);
 constexpr int RED_BAR = 1;        // named barrier of the consumer warps
 constexpr int MAX_CTAS = 320;     // grid cap (two CTAs per SM); sizes the partial-sum slots
+constexpr int MAX_CSIZE = 8;      // CTAs per cluster (K slices of one unit), portable cluster limit
 constexpr int CNT_PER_UNIT = 8;   // workspace counters per unit (16 per 128-row tile)
 constexpr int SMEM_CAP = 113 * 1024;   // two CTAs per SM
 constexpr int G = 2;              // K blocks per pipeline stage (one handshake per pair)
@@ -122,6 +123,7 @@ struct Params {
   int split_units;  // mode 0: units [0, split_units) are split stream-K ...
   int total1;       //   ... over their split_units * KB blocks
   int whole_per;    // mode 0: whole units per CTA, after the split units
+  int pre;          // weight stages issued before waiting for the previous kernel
   __nv_bfloat16* Y;
   int ldy;
   int32_t* acc_out;   // int32 mode when non-null
@@ -437,26 +439,26 @@ QUASAR_DEVICE_INLINE void consume_block(uint32_t st, uint32_t a_off, uint32_t b_
             mma_16816(acc[2 * i2 + i][ni], a0, a1, a2, a3, bq[ks][ni][0], bq[ks][ni][1]);
         }
     }
-    return;
-  }
+  } else {
 #pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
-    uint32_t bq[NT8][2];
+    for (int ks = 0; ks < 2; ++ks) {
+      uint32_t bq[NT8][2];
 #pragma unroll
-    for (int ni = 0; ni < NT8; ++ni)
-      s8x4_to_f16x4(lds32(st + (b_off ^ (ks << 4)) + (uint32_t)(ni * 8 * BK)), bq[ni][0], bq[ni][1]);
+      for (int ni = 0; ni < NT8; ++ni)
+        s8x4_to_f16x4(lds32(st + (b_off ^ (ks << 4)) + (uint32_t)(ni * 8 * BK)), bq[ni][0], bq[ni][1]);
 #pragma unroll
-    for (int i2 = 0; i2 < UT / 2; ++i2) {
-      uint32_t d[4];
-      ldsm_x4(st + (a_off ^ (ks << 4)) + (uint32_t)(i2 * 32 * BK), d[0], d[1], d[2], d[3]);
+      for (int i2 = 0; i2 < UT / 2; ++i2) {
+        uint32_t d[4];
+        ldsm_x4(st + (a_off ^ (ks << 4)) + (uint32_t)(i2 * 32 * BK), d[0], d[1], d[2], d[3]);
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        uint32_t a0, a1, a2, a3;
-        u8x4_to_f16x4(d[2 * i], a0, a2);       // rows g: K slots 2c.. (bytes 4c, 4c+1), 2c+8.. (4c+2, 4c+3)
-        u8x4_to_f16x4(d[2 * i + 1], a1, a3);   // rows g + 8
+        for (int i = 0; i < 2; ++i) {
+          uint32_t a0, a1, a2, a3;
+          u8x4_to_f16x4(d[2 * i], a0, a2);       // rows g: K slots 2c.. (bytes 4c, 4c+1), 2c+8.. (4c+2, 4c+3)
+          u8x4_to_f16x4(d[2 * i + 1], a1, a3);   // rows g + 8
 #pragma unroll
-        for (int ni = 0; ni < NT8; ++ni)
-          mma_16816(acc[2 * i2 + i][ni], a0, a1, a2, a3, bq[ni][0], bq[ni][1]);
+          for (int ni = 0; ni < NT8; ++ni)
+            mma_16816(acc[2 * i2 + i][ni], a0, a1, a2, a3, bq[ni][0], bq[ni][1]);
+        }
       }
     }
   }
@@ -503,11 +505,12 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      // Weights do not depend on the previous kernel: fill every stage first.
+      // Weights do not depend on the previous kernel: issue the first p.pre
+      // stages before waiting for it (the host picks the depth).
       int pre = 0;
       {
         Walk w(sc, KB);
-        for (; pre < C::S && w.more(); ++pre, w.next(KB)) {
+        for (; pre < C::S && pre < p.pre && w.more(); ++pre, w.next(KB)) {
           mbar_arrive_expect_tx(&full[pre], (uint32_t)(w.g * C::BLK));
           for (int b = 0; b < w.g; ++b)
             bulk_load(stages + pre * C::STAGE + b * C::BLK, unit_block<W4>(p, w.u, w.kb + b), C::HB, &full[pre],
@@ -707,16 +710,27 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
       int4 v[NH];
 #pragma unroll
       for (int h = 0; h < NH; ++h) v[h] = (nh + h < NT8) ? share[h * 32] : make_int4(0, 0, 0, 0);
-      for (int q = 0; q < csz; ++q) {
-        if (q == rank) continue;
+      // Every remote load is issued before any of them is used: one
+      // distributed-shared-memory round trip instead of one per load.
+      int4 x[MAX_CSIZE - 1][NH];
+#pragma unroll
+      for (int j = 0; j < MAX_CSIZE - 1; ++j) {
+        if (j >= csz - 1) break;
+        const int q = rank + 1 + j < csz ? rank + 1 + j : rank + 1 + j - csz;
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          if (nh + h < NT8) x[j][h] = ld_dsmem_int4(share + h * 32, (uint32_t)q);
+      }
+#pragma unroll
+      for (int j = 0; j < MAX_CSIZE - 1; ++j) {
+        if (j >= csz - 1) break;
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           if (nh + h >= NT8) break;
-          const int4 x = ld_dsmem_int4(share + h * 32, (uint32_t)q);
-          v[h].x += x.x;
-          v[h].y += x.y;
-          v[h].z += x.z;
-          v[h].w += x.w;
+          v[h].x += x[j][h].x;
+          v[h].y += x[j][h].y;
+          v[h].z += x[j][h].z;
+          v[h].w += x[j][h].w;
         }
       }
       epilogue<NT8>(p, v, u_first, mt_f, nh, lane, sa_s, sw_s);
@@ -791,16 +805,26 @@ static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t
   const int slots = std::min(2 * sms, MAX_CTAS);   // two CTAs per SM
   // Few units: one cluster per unit, with the most K slices that keep every
   // cluster resident in one wave; each slice must be one accumulation run.
-  int csize = std::min(std::min(8, slots / n_units), p.KB);
+  int csize = std::min(std::min(MAX_CSIZE, slots / n_units), p.KB);
   while (csize >= 2 && resident_clusters<NT8, W4>(dev, csize) < n_units) --csize;
   if (csize >= 2 && (p.KB + csize - 1) / csize > RUN_BLOCKS) csize = 1;
   cudaLaunchAttribute attr[2];
+  // Weight stages a CTA issues before its dependency wait.  Measured (graph
+  // replays, cold L2, Qwen3-8B shapes): a full ring floods the memory system
+  // just when the previous kernel's last stores and this kernel's first
+  // token loads must get through, which costs CTAs with a short K range
+  // (qkv, o_proj: 8-11 blocks) 6-11% at 8-24 tokens; CTAs with a long
+  // range at a few tokens (down_proj, gate_up: 24-40 blocks, M <= 8) stream
+  // 2% faster with the full ring.  So: one stage unless a CTA's range is
+  // long and its consumers are fast.
+  auto pre_for = [&](int blocks_per_cta) { return (blocks_per_cta <= 16 || p.M > 8) ? 1 : 1 << 30; };
   if (csize >= 2) {
     p.mode = 1;
     p.csize = csize;
     p.split_units = 0;
     p.total1 = 0;
     p.whole_per = 0;
+    p.pre = pre_for((p.KB + csize - 1) / csize);
     cudaLaunchConfig_t cfg = config_of<NT8, true, W4>(n_units * csize, csize, stream, attr);
     return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, true, W4>, tx, p);
   }
@@ -811,6 +835,7 @@ static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t
   p.split_units = n_units - p.whole_per * grid;
   p.total1 = p.split_units * p.KB;
   if (p.whole_per == 0) grid = std::min(grid, p.total1);
+  p.pre = pre_for((p.total1 + grid - 1) / std::max(grid, 1) + p.whole_per * p.KB);
   if ((unsigned long long)(p.total1 + 1) * (unsigned long long)(grid + 1) >= (1ull << 32)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = config_of<NT8, false, W4>(grid, 1, stream, attr);
   return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, false, W4>, tx, p);
