@@ -10,12 +10,13 @@
 // Why a second kernel: with a handful of tokens every weight byte meets at
 // most 32 token columns, so the tensor work per byte is tiny and what counts
 // is how fast the SM can turn staged INT8 weights into MMA operands.  A
-// tcgen05.mma of M = 128, K = 16 takes ~50 cycles whatever N <= 64 is (it is
-// bound by its own operand traffic), i.e. ~41 weight bytes per cycle before
-// the weights are even widened into TMEM.  The warp-level m16n8k16 fp16 MMA
-// runs at ~2048 flop/clk/SM on sm_103a and takes its weight operand straight
-// from registers: at M <= 8 it covers 128 weight bytes per cycle, at M = 32
-// still 32, against the ~22 bytes per cycle an SM must stream for HBM-rate.
+// tcgen05.mma of M = 128, K = 16 costs ~114 cycles for any N <= 192
+// (measured with quasar_probe_tensor_rate), i.e. ~18 weight bytes per cycle
+// before the weights are even widened into TMEM.  The warp-level m16n8k16
+// fp16 MMA covers ~1014 MAC/clk/SM on sm_103a (same probe) and takes its
+// weight operand straight from registers: at M <= 8 that is ~127 weight
+// bytes per cycle, at M = 32 still ~32, against the ~22 bytes per cycle an
+// SM must stream for HBM rate.
 // So for a few tokens the weights go HBM -> shared memory (1-D bulk copies of
 // the same packed blocks the tcgen05 kernel reads) -> registers (ldmatrix) ->
 // fp16 (exact) -> mma.sync, with fp32 accumulators that stay exact integers
