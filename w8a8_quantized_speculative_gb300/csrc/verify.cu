@@ -60,6 +60,15 @@ QUASAR_DEVICE_INLINE uint4 ld_stream(const void* p) {
   return v;
 }
 
+// Count one finished chunk: release (this thread's record is visible before
+// the count) and acquire (the CTA that takes the last count sees every
+// record), one operation instead of a full fence and a relaxed atomic.
+QUASAR_DEVICE_INLINE unsigned int count_acq_rel(unsigned int* p) {
+  unsigned int old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
+}
+
 QUASAR_DEVICE_INLINE void arg_merge(float& b, int& i, float b2, int i2) {
   if (b2 > b || (b2 == b && i2 < i)) {
     b = b2;
@@ -179,6 +188,10 @@ verify_kernel(const uint16_t* __restrict__ logits, int ldl, const int32_t* __res
               int CH, int S, float invT, const float* __restrict__ u, const float* __restrict__ u_next,
               int32_t* __restrict__ n_acc, int32_t* __restrict__ next_token, Partial* __restrict__ part,
               unsigned int* __restrict__ cnt) {
+  // Launched with programmatic dependent launch: the CTAs start while the
+  // previous kernel drains and wait here for its writes (the logits).
+  pdl_launch_dependents();
+  pdl_wait();
   const int row = blockIdx.y;
   const int c = blockIdx.x;
   const int b = row / (D + 1);
@@ -251,9 +264,8 @@ verify_kernel(const uint16_t* __restrict__ logits, int ldl, const int32_t* __res
       if (SAMPLED) lse_merge(r.m, r.s, red[w].m, red[w].s);
     }
     part[(size_t)row * S + c] = r;
-    __threadfence();
     const unsigned int total = (unsigned int)(D + 1) * (unsigned int)S;
-    const unsigned int old = atomicAdd(&cnt[b], 1u);
+    const unsigned int old = count_acq_rel(&cnt[b]);
     is_last = (old + 1 == total) ? 1 : 0;
   }
   __syncthreads();
@@ -264,6 +276,7 @@ verify_kernel(const uint16_t* __restrict__ logits, int ldl, const int32_t* __res
   __shared__ int s_fail;
   if (warp == 0) {
     int first_fail = D;
+    int ri_row = INT_MAX;   // argmax of row `lane` (D < 32: one row per lane)
     for (int j = lane; j <= D; j += 32) {
       const Partial* pr = part + ((size_t)b * (D + 1) + j) * S;
       float rb = -INFINITY, rm = -INFINITY, rs = 0.f;
@@ -274,6 +287,7 @@ verify_kernel(const uint16_t* __restrict__ logits, int ldl, const int32_t* __res
         arg_merge(rb, ri, pb, pi);
         if (SAMPLED) lse_merge(rm, rs, __ldcg(&pr[cc].m), __ldcg(&pr[cc].s));
       }
+      ri_row = ri;
       if (j < D) {
         const int d = draft[(size_t)b * D + j];
         bool ok;
@@ -291,10 +305,13 @@ verify_kernel(const uint16_t* __restrict__ logits, int ldl, const int32_t* __res
     }
   #pragma unroll
     for (int o = 16; o > 0; o >>= 1) first_fail = min(first_fail, __shfl_xor_sync(0xffffffffu, first_fail, o));
+    const int ri_fail = __shfl_sync(0xffffffffu, ri_row, first_fail & 31);
     if (lane == 0) {
       n_acc[b] = first_fail;
       s_fail = first_fail;
-      if (!SAMPLED && next_token) {
+      if (!SAMPLED && next_token && D < 32) {
+        next_token[b] = ri_fail;   // lane first_fail merged that row above
+      } else if (!SAMPLED && next_token) {
         const Partial* pr = part + ((size_t)b * (D + 1) + first_fail) * S;
         float rb = -INFINITY;
         int ri = INT_MAX;
@@ -362,13 +379,21 @@ static quasar_status_t run(const void* logits_bf16, int ldl, const int32_t* draf
   const dim3 grid(S, (unsigned)rows);
   const float invT = sampled ? 1.0f / temperature : 0.f;
   const uint16_t* lg = reinterpret_cast<const uint16_t*>(logits_bf16);
-  if (sampled)
-    verify_kernel<true><<<grid, THREADS, 0, stream>>>(lg, ldl, draft, D, V, ch, S, invT, u, u_next, n_acc,
-                                                      next_token, part, cnt);
-  else
-    verify_kernel<false><<<grid, THREADS, 0, stream>>>(lg, ldl, draft, D, V, ch, S, invT, u, nullptr, n_acc,
-                                                       next_token, part, cnt);
-  return cuda_status(cudaGetLastError());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(THREADS);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      sampled ? cudaLaunchKernelEx(&cfg, verify_kernel<true>, lg, ldl, draft, D, V, ch, S, invT, u, u_next, n_acc,
+                                   next_token, part, cnt)
+              : cudaLaunchKernelEx(&cfg, verify_kernel<false>, lg, ldl, draft, D, V, ch, S, invT, u,
+                                   static_cast<const float*>(nullptr), n_acc, next_token, part, cnt);
+  return cuda_status(e);
 }
 
 }  // namespace verify
