@@ -814,10 +814,12 @@ def run_tensor_probe(q):
     """Measured issue rate of the MMA forms the kernels use (one CTA per SM,
     clock64 cycles): tcgen05.mma kind::f16 M = 128 with A in TMEM at the
     token-tile widths the tcgen05 W8A8 kernel runs, A in shared memory at
-    N = 256, and mma.sync m16n8k16 (the register path).  MAC per SM clock;
-    x 2 x SMs x clock gives the FLOP rate."""
+    N = 256, the two-CTA (cta_group::2, M = 256 over two SMs) form at the
+    lm_head's and the wide tiles' N, and mma.sync m16n8k16 (the register
+    path).  MAC per SM clock; x 2 x SMs x clock gives the FLOP rate."""
     out = {}
-    for form, ns in (("tcgen05_ts", (32, 64, 128, 144, 192, 256)), ("tcgen05_ss", (256,))):
+    for form, ns in (("tcgen05_ts", (32, 64, 128, 144, 192, 256)), ("tcgen05_ss", (256,)),
+                     ("tcgen05_ts_pair", (64, 144, 192))):
         for n in ns:
             r = q.probe_tensor_rate(form, n, 4096)
             out[f"{form}_n{n}"] = {"mac_per_clk_per_sm": round(r["mac_per_clk_per_sm"], 1),
@@ -826,7 +828,9 @@ def run_tensor_probe(q):
     out["mma_sync_m16n8k16"] = {"mac_per_clk_per_sm": round(r["mac_per_clk_per_sm"], 1),
                                 "cycles_per_mma_per_warp": round(r["cycles_per_mma"], 1)}
     out["note"] = ("a tcgen05 kind::f16 M = 128, K = 16 MMA costs the same ~114 cycles for every N <= 192: "
-                   "at few tokens the W8A8 tcgen05 kernel is bound by 8 instructions per 16 KB weight block")
+                   "at few tokens the W8A8 tcgen05 kernel is bound by 8 instructions per 16 KB weight block; "
+                   "the two-CTA form (M = 256 over two SMs) costs the same per instruction, so the per-SM rate "
+                   "is unchanged")
     return out
 
 

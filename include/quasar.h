@@ -84,8 +84,12 @@ quasar_status_t quasar_selftest_wait_timeout(uint64_t limit_ns, quasar_stream_t 
  * kernel's converter traffic); 3 = mma.sync m16n8k16 fp16 -> fp32 from
  * registers, 16 warps (n ignored); 4 / 5 = form 0 with each group's K steps
  * spread over 2 / 4 independent accumulators (n <= 128 / 64); 6 = form 1
- * with M = 64.  n: 16 .. 256, a multiple of 16 (forms other than 3);
- * 1 <= iters <= 2^20.  Asynchronous on `stream`; returns
+ * with M = 64; 7 = tcgen05.mma.cta_group::2 kind::f16 over a cluster of two
+ * CTAs on two SMs, M = 256 (128 A rows in each CTA's TMEM), N = n (n / 2 B
+ * rows in each CTA's shared memory), issued by the even CTA, which records
+ * the counts (n <= 224); 8 = form 7 with A in shared memory.  n: 16 .. 256,
+ * a multiple of 16 (forms other than 3); 1 <= iters <= 2^20.  Asynchronous
+ * on `stream`; returns
  * QUASAR_ERR_INVALID_ARG / QUASAR_ERR_UNSUPPORTED for bad arguments. */
 quasar_status_t quasar_probe_tensor_rate(int form, int n, int iters, unsigned long long* out,
                                          int out_slots, quasar_stream_t stream);

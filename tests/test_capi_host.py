@@ -295,7 +295,8 @@ def test_tensor_probe_rejects_bad_arguments(lib):
     f = lib.quasar_probe_tensor_rate
     f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
     assert f(0, 128, 16, None, 1024, None) == 1           # no output buffer
-    assert f(7, 128, 16, FAKE, 1024, None) == 1           # unknown form
+    assert f(9, 128, 16, FAKE, 1024, None) == 1           # unknown form
+    assert f(7, 256, 16, FAKE, 1024, None) == 2           # pair form: accumulator would reach the A operand
     assert f(0, 128, 0, FAKE, 1024, None) == 1            # no iterations
     assert f(0, 24, 16, FAKE, 1024, None) == 2            # N not a multiple of 16
     assert f(0, 272, 16, FAKE, 1024, None) == 2           # N above 256

@@ -19,7 +19,13 @@
 //      independent accumulators (N <= 128): whether separate accumulation
 //      chains overlap in the tensor pipe
 //   6  form 1 with M = 64 (64 A rows in shared memory)
-// Each CTA records its cycle count (clock64) and the work it issued.
+//   7  tcgen05.mma.cta_group::2 kind::f16, M = 256 over a cluster of two
+//      CTAs on two SMs (128 A rows in each CTA's TMEM), N = n (n / 2 B rows
+//      in each CTA's shared memory), K = 16, issued by the even CTA
+//   8  form 7 with A in shared memory
+// Each CTA records its cycle count (clock64) and the work it issued (in the
+// pair forms the issuing CTA records for both SMs: each does 128 x n x 16
+// MACs per instruction).
 #include "quasar_common.cuh"
 
 namespace quasar {
@@ -147,6 +153,127 @@ tc_probe_kernel(int form, int n, int iters, unsigned long long* out, unsigned in
   }
 }
 
+// ---- two-CTA (cta_group::2) forms
+QUASAR_DEVICE_INLINE uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+QUASAR_DEVICE_INLINE void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Allocation and release are collective over the pair: one warp of each CTA.
+QUASAR_DEVICE_INLINE void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+QUASAR_DEVICE_INLINE void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+QUASAR_DEVICE_INLINE void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Completion of the pair's MMAs arrives on the barrier at the same offset in
+// both CTAs.
+QUASAR_DEVICE_INLINE void tc_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+// The pair kernel takes 256 TMEM columns per CTA: accumulators [0, n), the
+// TMEM A operand (form 7) at PAIR_A_COL; two allocations of that size fit in
+// an SM's 512 columns whichever CTA's request covers which SM.
+constexpr int PAIR_COLS = 256;
+constexpr int PAIR_A_COL = 224;
+
+__global__ void __launch_bounds__(32 * WARPS, 1)
+tc_pair_probe_kernel(int form, int n, int iters, unsigned long long* out, unsigned int* err,
+                     unsigned long long limit_ns) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + SMEM_A;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sb + SMEM_B);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+
+  for (int i = threadIdx.x; i < (SMEM_A + SMEM_B) / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  if (warp == 0) tmem_alloc_pair(tmem_slot, PAIR_COLS);
+  tc_fence_before();
+  cluster_sync_all();   // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after();
+  if (warp == 0) tmem_relinquish_pair();
+  const uint32_t tmem = *tmem_slot;
+  if (form == 7 && warp >= 1 && warp <= 4) {
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0;
+    tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + PAIR_A_COL, z);
+    tc_wait_st();
+  }
+  tc_fence_before();
+  cluster_sync_all();   // both CTAs' operands in place
+  tc_fence_after();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      if (rank == 0) {
+        const uint32_t idesc = (1u << 4) | (uint32_t(n >> 3) << 17) | ((256u >> 4) << 24);
+        const uint64_t bdesc = desc_sw128(smem_u32(sb));
+        const uint64_t adesc = desc_sw128(smem_u32(sa));
+        const unsigned long long t0 = clock64();
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t acc = (it | k) ? 1u : 0u;
+            if (form == 8)
+              asm volatile(
+                  "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                  "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + D_COL),
+                  "l"(adesc + (uint64_t)(2 * k)), "l"(bdesc + (uint64_t)(2 * k)), "r"(idesc), "r"(acc)
+                  : "memory");
+            else
+              asm volatile(
+                  "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                  "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + D_COL),
+                  "r"(tmem + PAIR_A_COL + 8 * k), "l"(bdesc + (uint64_t)(2 * k)), "r"(idesc), "r"(acc)
+                  : "memory");
+          }
+        }
+        tc_commit_pair(bar);
+        const bool ok = mbar_wait(bar, 0, abort_flag, err, SITE_SELFTEST, limit_ns);
+        const unsigned long long t1 = clock64();
+        out[blockIdx.x * 4 + 0] = ok ? t1 - t0 : 0ull;
+        out[blockIdx.x * 4 + 1] = (unsigned long long)iters * 4;
+      } else {
+        // the even CTA's commit arrives here as well; its MMAs write this
+        // CTA's TMEM, so wait for them before releasing it
+        mbar_wait(bar, 0, abort_flag, err, SITE_SELFTEST, limit_ns);
+      }
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, PAIR_COLS);
+  }
+}
+
 // D += A * B, m16n8k16 fp16 -> fp32 from registers.
 QUASAR_DEVICE_INLINE void hmma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                uint32_t b1) {
@@ -185,9 +312,10 @@ extern "C" quasar_status_t quasar_probe_tensor_rate(int form, int n, int iters, 
   using namespace quasar;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (!out || iters <= 0 || iters > (1 << 20)) return QUASAR_ERR_INVALID_ARG;
-  if (form < 0 || form > 6) return QUASAR_ERR_INVALID_ARG;
+  if (form < 0 || form > 8) return QUASAR_ERR_INVALID_ARG;
   if (form != 3 && (n < 16 || n > 256 || n % 16 != 0)) return QUASAR_ERR_UNSUPPORTED;
   if ((form == 4 && n > 128) || (form == 5 && n > 64)) return QUASAR_ERR_UNSUPPORTED;   // accumulators below A_COL
+  if (form == 7 && n > probe::PAIR_A_COL) return QUASAR_ERR_UNSUPPORTED;                // accumulator below the A operand
   const int sms = sm_count();
   if (sms <= 0) return QUASAR_ERR_CUDA;
   if (out_slots < 4 * sms) return QUASAR_ERR_INVALID_ARG;
@@ -215,6 +343,29 @@ extern "C" quasar_status_t quasar_probe_tensor_rate(int form, int n, int iters, 
     e = cudaFuncSetAttribute(probe::tc_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, probe::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_status(e);
     configured[dev] = 1;
+  }
+  if (form == 7 || form == 8) {
+    static int pconf[64] = {0};
+    if (dev >= 0 && dev < 64 && !pconf[dev]) {
+      e = cudaFuncSetAttribute(probe::tc_pair_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               probe::SMEM_BYTES);
+      if (e != cudaSuccess) return cuda_status(e);
+      pconf[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sms / 2 * 2));
+    cfg.blockDim = dim3(32 * probe::WARPS);
+    cfg.dynamicSmemBytes = probe::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, probe::tc_pair_probe_kernel, form, n, iters, out, err,
+                                          wait_limit_ns()));
   }
   probe::tc_probe_kernel<<<sms, 32 * probe::WARPS, probe::SMEM_BYTES, stream>>>(form, n, iters, out, err,
                                                                                  wait_limit_ns());

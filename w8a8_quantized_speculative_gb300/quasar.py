@@ -511,7 +511,8 @@ def lm_head_verify_sample(h: torch.Tensor, wp: PackedLmHead, draft: torch.Tensor
 
 
 PROBE_FORMS = {"tcgen05_ts": 0, "tcgen05_ss": 1, "tcgen05_ts_with_tmem_stores": 2, "mma_sync": 3,
-               "tcgen05_ts_2chains": 4, "tcgen05_ts_4chains": 5, "tcgen05_ss_m64": 6}
+               "tcgen05_ts_2chains": 4, "tcgen05_ts_4chains": 5, "tcgen05_ss_m64": 6,
+               "tcgen05_ts_pair": 7, "tcgen05_ss_pair": 8}
 
 
 def probe_tensor_rate(form: str, n: int = 128, iters: int = 4096, stream=None):
