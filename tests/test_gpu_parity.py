@@ -893,5 +893,9 @@ def test_tensor_probe_rates_are_plausible():
     assert narrow["mac_per_clk_per_sm"] < wide["mac_per_clk_per_sm"]
     hm = q.probe_tensor_rate("mma_sync", iters=1024)
     assert 100 < hm["mac_per_clk_per_sm"] <= 1024 * 1.02
+    # two-CTA form (M = 256 over a pair of SMs): each SM computes its 128 rows
+    # against all N columns per instruction, within the nominal per-SM rate
+    pair = q.probe_tensor_rate("tcgen05_ts_pair", 128, 1024)
+    assert 500 < pair["mac_per_clk_per_sm"] <= 4096 * 1.02
     st, site = q.get_device_error()
     assert st == 0, site
