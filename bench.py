@@ -376,16 +376,31 @@ def main_gpu(args):
     # buffered, as a serving loop runs it: a copy stream brings step i+1's
     # activations in and takes step i's outputs out while the compute stream
     # runs step i; every step's copies are inside the timed region.
+    # Each step's activations (and outputs) share one pinned host buffer and
+    # one device buffer, viewed per linear: one copy in and one copy out per
+    # step instead of one per tensor.
     nb = 2
-    host_x = [[torch.empty((l["case"].M, l["case"].K), dtype=torch.bfloat16).pin_memory() for l in lin]
-              for _ in range(nb)]
+    x_sizes = [l["case"].M * l["case"].K for l in lin]
+    y_sizes = [l["case"].M * l["case"].N for l in lin]
+
+    def views(flat, sizes, shapes):
+        out, off = [], 0
+        for n, shp in zip(sizes, shapes):
+            out.append(flat[off:off + n].view(shp))
+            off += n
+        return out
+
+    x_shapes = [(l["case"].M, l["case"].K) for l in lin]
+    y_shapes = [(l["case"].M, l["case"].N) for l in lin]
+    host_xf = [torch.empty(sum(x_sizes), dtype=torch.bfloat16).pin_memory() for _ in range(nb)]
+    host_yf = [torch.empty(sum(y_sizes), dtype=torch.bfloat16).pin_memory() for _ in range(nb)]
+    dev_xf = [torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=dev) for _ in range(nb)]
+    dev_yf = [torch.empty(sum(y_sizes), dtype=torch.bfloat16, device=dev) for _ in range(nb)]
     for b in range(nb):
-        for hx, l in zip(host_x[b], lin):
+        for hx, l in zip(views(host_xf[b], x_sizes, x_shapes), lin):
             hx.copy_(l["x"].cpu())
-    host_y = [[torch.empty((l["case"].M, l["case"].N), dtype=torch.bfloat16).pin_memory() for l in lin]
-              for _ in range(nb)]
-    dev_x = [[torch.empty_like(l["x"]) for l in lin] for _ in range(nb)]
-    dev_y = [[torch.empty_like(l["y"]) for l in lin] for _ in range(nb)]
+    dev_x = [views(dev_xf[b], x_sizes, x_shapes) for b in range(nb)]
+    dev_y = [views(dev_yf[b], y_sizes, y_shapes) for b in range(nb)]
     copy_stream = torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(nb)]
     ev_done = [torch.cuda.Event() for _ in range(nb)]
@@ -397,8 +412,7 @@ def main_gpu(args):
         if i >= nb:
             copy_stream.wait_event(ev_done[b])       # step i - nb has read dev_x[b]
         with torch.cuda.stream(copy_stream):
-            for hx, dx in zip(host_x[b], dev_x[b]):
-                dx.copy_(hx, non_blocking=True)
+            dev_xf[b].copy_(host_xf[b], non_blocking=True)
         ev_in[b].record(copy_stream)
 
     def compute(i):
@@ -416,8 +430,7 @@ def main_gpu(args):
         b = i % nb
         copy_stream.wait_event(ev_done[b])
         with torch.cuda.stream(copy_stream):
-            for hy, dy in zip(host_y[b], dev_y[b]):
-                hy.copy_(dy, non_blocking=True)
+            host_yf[b].copy_(dev_yf[b], non_blocking=True)
         ev_out[b].record(copy_stream)
 
     fork = torch.cuda.Event()

@@ -154,14 +154,6 @@ tc_probe_kernel(int form, int n, int iters, unsigned long long* out, unsigned in
 }
 
 // ---- two-CTA (cta_group::2) forms
-QUASAR_DEVICE_INLINE uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-QUASAR_DEVICE_INLINE void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // Allocation and release are collective over the pair: one warp of each CTA.
 QUASAR_DEVICE_INLINE void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
@@ -201,7 +193,7 @@ tc_pair_probe_kernel(int form, int n, int iters, unsigned long long* out, unsign
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();
+  const uint32_t rank = cluster_ctarank();
 
   for (int i = threadIdx.x; i < (SMEM_A + SMEM_B) / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
@@ -213,7 +205,7 @@ tc_pair_probe_kernel(int form, int n, int iters, unsigned long long* out, unsign
   fence_proxy_async_smem();
   if (warp == 0) tmem_alloc_pair(tmem_slot, PAIR_COLS);
   tc_fence_before();
-  cluster_sync_all();   // barriers initialised and TMEM allocated in both CTAs
+  cluster_sync_full();   // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   if (warp == 0) tmem_relinquish_pair();
   const uint32_t tmem = *tmem_slot;
@@ -225,7 +217,7 @@ tc_pair_probe_kernel(int form, int n, int iters, unsigned long long* out, unsign
     tc_wait_st();
   }
   tc_fence_before();
-  cluster_sync_all();   // both CTAs' operands in place
+  cluster_sync_full();   // both CTAs' operands in place
   tc_fence_after();
 
   if (warp == 0) {
@@ -267,7 +259,7 @@ tc_pair_probe_kernel(int form, int n, int iters, unsigned long long* out, unsign
     __syncwarp();
   }
   tc_fence_before();
-  cluster_sync_all();
+  cluster_sync_full();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, PAIR_COLS);

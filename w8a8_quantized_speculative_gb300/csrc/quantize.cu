@@ -389,21 +389,8 @@ __global__ void __launch_bounds__(THREADS) rms_quant_kernel(const uint16_t* __re
 // the GPU.  The row's absmax is the largest of the C CTAs' partial maxima,
 // read from each CTA's shared memory across the cluster; a max is exact in
 // any order, so codes and scale are those of quant_act_kernel<*, true>.
-QUASAR_DEVICE_INLINE uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-QUASAR_DEVICE_INLINE uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-
 QUASAR_DEVICE_INLINE float ld_cluster_f32(const float* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  const uint32_t remote = map_to_rank(local, rank);
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
   return v;
@@ -463,12 +450,12 @@ __global__ void __launch_bounds__(THREADS) glu_quant_cluster_kernel(const uint16
     cta_amax = a;
   }
   // Every CTA's partial maximum is in its shared memory before any is read.
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  cluster_sync_full();
   amax = 0.f;
   for (int r = 0; r < C; ++r) amax = fmaxf(amax, ld_cluster_f32(&cta_amax, (uint32_t)r));
   // Reads done: arrive now, wait before exiting so that no CTA's shared
   // memory goes away while another CTA of the cluster may still read it.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  cluster_arrive_relaxed();
   const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
   if (rank == 0 && threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
   int8_t* dst = q + (size_t)row * K + (size_t)rank * slice;
@@ -487,7 +474,7 @@ __global__ void __launch_bounds__(THREADS) glu_quant_cluster_kernel(const uint16
     }
     reinterpret_cast<uint2*>(dst)[v] = make_uint2(packed[0], packed[1]);
   }
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  cluster_wait();
 }
 
 // Cluster shape for a GLU row of K values: the smallest C in {2, 4, 8} that

@@ -298,6 +298,48 @@ QUASAR_DEVICE_INLINE void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned
 template <int N>
 QUASAR_DEVICE_INLINE void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
+// ---- thread-block clusters ------------------------------------------------------
+
+QUASAR_DEVICE_INLINE uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+QUASAR_DEVICE_INLINE uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Cluster-wide barrier of every thread of every CTA in the cluster
+// (warp-converged callers only): release on arrive, acquire on wait, so the
+// shared-memory writes before it are visible to every CTA after it.
+QUASAR_DEVICE_INLINE void cluster_sync_full() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The same barrier ordering execution only: no CTA passes before every
+// thread of the cluster has arrived (remote loads issued before it have
+// returned their values by then), without waiting for this thread's global
+// stores to become visible.
+QUASAR_DEVICE_INLINE void cluster_sync_exec() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Split form of cluster_sync_exec: arrive now, wait later.
+QUASAR_DEVICE_INLINE void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+QUASAR_DEVICE_INLINE void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// Address of the same shared-memory offset in cluster CTA `rank`.
+QUASAR_DEVICE_INLINE uint32_t map_to_rank(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  return remote;
+}
+
 // ---- bit helpers ---------------------------------------------------------------
 
 // Four signed bytes -> two fp16x2 words, exactly.  Each byte b is re-biased

@@ -386,15 +386,6 @@ QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4
   return true;
 }
 
-// Cluster-wide barrier of every thread of the cluster: with release /
-// acquire ordering of shared-memory writes (full), or ordering execution
-// only (exec: the remote loads it follows have returned their values).
-QUASAR_DEVICE_INLINE void cluster_barrier_full() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-QUASAR_DEVICE_INLINE void cluster_barrier_exec() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
-}
 
 
 // Cluster phase of a split tile (csize CTAs, one K part each).  CTA `rank`
@@ -416,11 +407,6 @@ QUASAR_DEVICE_INLINE void st_cluster_u32(uint32_t remote_addr, int32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote_addr), "r"(v) : "memory");
 }
 
-QUASAR_DEVICE_INLINE uint32_t map_to_rank(const void* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  return remote;
-}
 
 // This thread's TOK sums (weight row `row`, token columns h*TOK ..) pushed
 // to the CTA that finishes the row.
@@ -625,8 +611,8 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
     }
     __syncwarp();
     if (p.csize > 1) {   // the converters' two cluster barriers (no data of this warp crosses them)
-      cluster_barrier_exec();
-      cluster_barrier_exec();
+      cluster_sync_exec();
+      cluster_sync_exec();
     }
   } else if (AUX && (warp == MMA_WARP || warp == WAITER_WARP)) {
     // Any memory access by the thread that issues tcgen05.mma waits until
@@ -682,8 +668,8 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
     }
     __syncwarp();
     if (p.csize > 1) {   // the converters' two cluster barriers (no data of this warp crosses them)
-      cluster_barrier_exec();
-      cluster_barrier_exec();
+      cluster_sync_exec();
+      cluster_sync_exec();
     }
   } else if (CONV && warp < CONV_WARPS) {
     // ---------------------------------------------------------------- converters
@@ -802,15 +788,15 @@ QUASAR_DEVICE_INLINE void linear_body(const CUtensorMap& tmX, const Params& p) {
       const int my_rank = (int)(blockIdx.x % (unsigned)p.csize);
       named_barrier_or(CONV_BAR_ID, CONV_WARPS * 32, 0u);   // every converter is past the rings
       stage_scales<NT>(p, sc, b0 / KB, ct);
-      cluster_barrier_exec();
+      cluster_sync_exec();
       cluster_push<NT>(p, part, acc, row, h, my_rank);
-      cluster_barrier_full();
+      cluster_sync_full();
       cluster_finalize<NT>(p, part, sc, b0 / KB, my_rank, ct);
     }
   } else if (p.csize > 1) {
     // the spare warp of the fifth warpgroup
-    cluster_barrier_exec();
-    cluster_barrier_exec();
+    cluster_sync_exec();
+    cluster_sync_exec();
   }
 
   tc_fence_before();

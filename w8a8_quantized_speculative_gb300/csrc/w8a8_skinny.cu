@@ -248,24 +248,9 @@ QUASAR_DEVICE_INLINE uint32_t lds32(uint32_t addr) {
   return v;
 }
 
-// Cluster-wide barrier of every thread of every CTA in the cluster (release
-// on arrive, acquire on wait); warp-converged callers only.
-QUASAR_DEVICE_INLINE void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Cluster barrier that orders execution only: no CTA leaves before every
-// thread of the cluster has arrived (the remote shared-memory loads it waits
-// for have returned their values by then), without waiting for this
-// thread's global stores to become visible.
-QUASAR_DEVICE_INLINE void cluster_sync_exec() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
-}
-
 // int4 at the same shared-memory offset in cluster CTA `rank`.
 QUASAR_DEVICE_INLINE int4 ld_dsmem_int4(const void* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  const uint32_t remote = map_to_rank(local, rank);
   int4 v;
   asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -542,7 +527,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     }
     __syncwarp();
     if (p.mode == 1) {   // the consumers' two cluster barriers
-      cluster_sync_all();
+      cluster_sync_full();
       cluster_sync_exec();
     }
     return;
@@ -704,7 +689,7 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
     // memory; the second barrier keeps every CTA's shared memory alive until
     // those reads are done.
     __syncwarp();
-    cluster_sync_all();
+    cluster_sync_full();
     const int csz = p.csize;
     const int rank = (int)blockIdx.x % csz;
     if (!bad && (warp % csz) == rank) {
