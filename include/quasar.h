@@ -87,7 +87,8 @@ quasar_status_t quasar_selftest_wait_timeout(uint64_t limit_ns, quasar_stream_t 
  * with M = 64; 7 = tcgen05.mma.cta_group::2 kind::f16 over a cluster of two
  * CTAs on two SMs, M = 256 (128 A rows in each CTA's TMEM), N = n (n / 2 B
  * rows in each CTA's shared memory), issued by the even CTA, which records
- * the counts (n <= 224); 8 = form 7 with A in shared memory.  n: 16 .. 256,
+ * the counts (n <= 224; out[4b+2] = the TMEM address CTA b's paired
+ * allocation returned); 8 = form 7 with A in shared memory.  n: 16 .. 256,
  * a multiple of 16 (forms other than 3); 1 <= iters <= 2^20.  Asynchronous
  * on `stream`; returns
  * QUASAR_ERR_INVALID_ARG / QUASAR_ERR_UNSUPPORTED for bad arguments. */

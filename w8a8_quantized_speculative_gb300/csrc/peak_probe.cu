@@ -154,7 +154,8 @@ tc_probe_kernel(int form, int n, int iters, unsigned long long* out, unsigned in
 }
 
 // ---- two-CTA (cta_group::2) forms
-// Allocation and release are collective over the pair: one warp of each CTA.
+// TMEM allocation and release are collective over the pair (one warp of
+// each CTA; both get the same address).
 QUASAR_DEVICE_INLINE void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
                "r"(ncols)
@@ -166,13 +167,13 @@ QUASAR_DEVICE_INLINE void tmem_relinquish_pair() {
 QUASAR_DEVICE_INLINE void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-// Completion of the pair's MMAs arrives on the barrier at the same offset in
-// both CTAs.
-QUASAR_DEVICE_INLINE void tc_commit_pair(uint64_t* bar) {
+// Completion of the pair MMAs this thread issued arrives on the barrier at
+// the same offset in each CTA of `mask` (bit r: cluster rank r).
+QUASAR_DEVICE_INLINE void tc_commit_pair(uint64_t* bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_u32(bar)),
-      "h"((uint16_t)3)
+      "h"(mask)
       : "memory");
 }
 
@@ -209,6 +210,7 @@ tc_pair_probe_kernel(int form, int n, int iters, unsigned long long* out, unsign
   tc_fence_after();
   if (warp == 0) tmem_relinquish_pair();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) out[blockIdx.x * 4 + 2] = tmem;   // the TMEM address this CTA's request returned
   if (form == 7 && warp >= 1 && warp <= 4) {
     uint32_t z[32];
 #pragma unroll
@@ -245,7 +247,7 @@ tc_pair_probe_kernel(int form, int n, int iters, unsigned long long* out, unsign
                   : "memory");
           }
         }
-        tc_commit_pair(bar);
+        tc_commit_pair(bar, 3);
         const bool ok = mbar_wait(bar, 0, abort_flag, err, SITE_SELFTEST, limit_ns);
         const unsigned long long t1 = clock64();
         out[blockIdx.x * 4 + 0] = ok ? t1 - t0 : 0ull;
