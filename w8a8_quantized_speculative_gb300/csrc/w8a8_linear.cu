@@ -394,11 +394,10 @@ QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4
 // into that CTA's shared memory (remote stores, which the sender does not
 // wait for; measured, pulling them with remote loads ran at ~30 GB/s per
 // SM), laid out [sender rank][token column][row - 4 u0] with a row stride of
-// RPR; after a release / acquire cluster barrier each CTA adds the csize
-// parts from its own shared memory and writes its rows (dequantized, or the
-// int32 sums).  Four consecutive rows per item: consecutive threads on
-// consecutive rows of Y.
-constexpr int RPR_MAX = 64;   // rows per rank of a cluster of 2 (the largest share)
+// rows_per_rank(csize) (at most 64, for a cluster of 2); after a release /
+// acquire cluster barrier each CTA adds the csize parts from its own shared
+// memory and writes its rows (dequantized, or the int32 sums).  Four
+// consecutive rows per item: consecutive threads on consecutive rows of Y.
 
 QUASAR_DEVICE_INLINE int rows_per_rank(int csize) { return (((BM / 4) + csize - 1) / csize) * 4; }
 QUASAR_DEVICE_INLINE int rank_first_unit(int r, int csize) { return r * (BM / 4) / csize; }
