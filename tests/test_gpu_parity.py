@@ -867,6 +867,25 @@ def test_int8_gemm_at_max_k(M):
     check_ws_zero(ws)
 
 
+@pytest.mark.parametrize("M", [1, 40, 150])
+def test_w4a8_linear_at_max_k(M):
+    """K = 131072 with 4-bit weights through both kernels (M = 150: the fp16
+    token copy): codes at the 4-bit extremes (-8, 7) against +-127 tokens, the
+    dequantized output bit for bit against the oracle."""
+    N, K = 16, 131072
+    xq = np.full((M, K), 127, np.int8)
+    xq[:, 1::3] = -127
+    wq = np.full((N, K), -8, np.int8)
+    wq[1::2, ::5] = 7
+    rng = np.random.default_rng(M)
+    sa = rng.uniform(1e-4, 1e-3, M).astype(np.float32)
+    sw = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
+    ws = q.Workspace()
+    y = q.w4a8_linear(dev(xq), dev(sa), q.tile_weights_w4(dev(wq)), dev(sw), workspace=ws)
+    assert np.array_equal(host_bf16_bits(y), orc.w8a8_linear(xq, sa, wq, sw))
+    check_ws_zero(ws)
+
+
 def test_verify_at_max_rows():
     """B * (D + 1) = 65535 logits rows, the documented limit, small V."""
     D, V = 4, 64
