@@ -627,18 +627,39 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
         acc[i][ni][0] = acc[i][ni][1] = acc[i][ni][2] = acc[i][ni][3] = 0.f;
       }
     named_barrier_or(RED_BAR, CWARPS * 32, 0u);
+    // The four K owners' partials are exact integers of magnitude at most
+    // blocks x 32 x 127^2; when a group of them sums below 2^24 it is added
+    // in fp32 (exact) before the one conversion to int32: the conversion
+    // unit (16 per SM clock) is the slow part of this step.  Groups of four
+    // for runs of <= 8 blocks (4 x 8 x 32 x 16129 < 2^24), pairs for <= 16.
+    const int run_len = (w.kb + w.g - w.kb_first - 1) % RUN_BLOCKS + 1;
+    const int grp = run_len <= 8 ? 4 : run_len <= 16 ? 2 : 1;
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       const int ni = nh + h;
       if (ni >= NT8) break;
       int4 f = share[h * 32];
+      float4 v[KQ];
 #pragma unroll
-      for (int q = 0; q < KQ; ++q) {
-        const float4 v = red[((mt_f * KQ + q) * NT8 + ni) * 32 + lane];
-        f.x += __float2int_rn(v.x);
-        f.y += __float2int_rn(v.y);
-        f.z += __float2int_rn(v.z);
-        f.w += __float2int_rn(v.w);
+      for (int q = 0; q < KQ; ++q) v[q] = red[((mt_f * KQ + q) * NT8 + ni) * 32 + lane];
+      if (grp == 4) {
+        f.x += __float2int_rn(((v[0].x + v[1].x) + v[2].x) + v[3].x);
+        f.y += __float2int_rn(((v[0].y + v[1].y) + v[2].y) + v[3].y);
+        f.z += __float2int_rn(((v[0].z + v[1].z) + v[2].z) + v[3].z);
+        f.w += __float2int_rn(((v[0].w + v[1].w) + v[2].w) + v[3].w);
+      } else if (grp == 2) {
+        f.x += __float2int_rn(v[0].x + v[1].x) + __float2int_rn(v[2].x + v[3].x);
+        f.y += __float2int_rn(v[0].y + v[1].y) + __float2int_rn(v[2].y + v[3].y);
+        f.z += __float2int_rn(v[0].z + v[1].z) + __float2int_rn(v[2].z + v[3].z);
+        f.w += __float2int_rn(v[0].w + v[1].w) + __float2int_rn(v[2].w + v[3].w);
+      } else {
+#pragma unroll
+        for (int q = 0; q < KQ; ++q) {
+          f.x += __float2int_rn(v[q].x);
+          f.y += __float2int_rn(v[q].y);
+          f.z += __float2int_rn(v[q].z);
+          f.w += __float2int_rn(v[q].w);
+        }
       }
       share[h * 32] = f;
     }
