@@ -290,7 +290,9 @@ def main_gpu(args):
             q.w8a8_linear_fused(l["x"], l["smooth"], l["wq_copies"][i % ncopy], l["sw_copies"][i % ncopy],
                                 y=l["y"], workspace=ws)
 
-    launches_per_step = 2 * len(lin)   # each fused call: the quantizer, then the linear
+    # each fused call: one launch up to 24 tokens (the linear quantizes its own
+    # rows), else the quantizer and then the linear
+    launches_per_step = sum(1 if l["case"].M <= 24 else 2 for l in lin)
 
     # ---- warm-up (eager), then capture graphs of the step sequence
     with torch.cuda.stream(stream):
@@ -781,9 +783,11 @@ def profile_kernels(q, which: str, launches: int = 4):
     """Launch one kernel of the path a few times at its workload shape, for an
     ncu capture (no timing): `verify` (greedy, B = 32, D = 8, V = 151936),
     `glue` (SiLU * up + smooth + quantize, M = 40, I = 12288), `rmsnorm`
-    (RMSNorm + smooth + quantize, M = 288, K = 4096), `qkv64` / `qkv256`
-    (the W8A8 linear, qkv 4096 -> 6144 at M = 64 / 256; weights rotate over
-    six copies, 151 MB > L2)."""
+    (RMSNorm + smooth + quantize, M = 288, K = 4096), `qkv20` / `qkv64` /
+    `qkv256` (the W8A8 linear on codes, qkv 4096 -> 6144 at M = 20 / 64 / 256),
+    `qkv20fused` (the one-call linear on BF16 activations at M = 20: one
+    launch that also quantizes the rows); the weights rotate over six copies,
+    151 MB > L2."""
     import torch
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -808,16 +812,21 @@ def profile_kernels(q, which: str, launches: int = 4):
         smooth = torch.rand(K, device=dev, generator=gen) + 0.5
         for _ in range(launches):
             q.rmsnorm_smooth_quant(x, g, smooth)
-    elif which in ("qkv64", "qkv256"):
-        M = 64 if which == "qkv64" else 256
+    elif which in ("qkv20", "qkv20fused", "qkv64", "qkv256"):
+        M = {"qkv20": 20, "qkv20fused": 20, "qkv64": 64, "qkv256": 256}[which]
         K, N = synth.LINEARS["qkv"]
         wqs = [torch.randint(-127, 128, (N * K,), dtype=torch.int8, device=dev, generator=gen) for _ in range(6)]
         sw = torch.rand(N, device=dev, generator=gen) * 1e-3
         xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
         sa = torch.rand(M, device=dev, generator=gen)
+        x = torch.randn((M, K), device=dev, generator=gen).to(torch.bfloat16)
+        smooth = torch.rand(K, device=dev, generator=gen) + 0.5
         ws = q.Workspace(dev)
         for i in range(launches):
-            q.w8a8_linear(xq, sa, wqs[i % 6], sw, workspace=ws)
+            if which == "qkv20fused":
+                q.w8a8_linear_fused(x, smooth, wqs[i % 6], sw, workspace=ws)
+            else:
+                q.w8a8_linear(xq, sa, wqs[i % 6], sw, workspace=ws)
     else:
         raise ValueError(which)
     torch.cuda.synchronize()
@@ -1056,7 +1065,8 @@ def main():
                     help="run only the 4-layer verification-step sub-benchmark")
     ap.add_argument("--mlp-block-only", action="store_true",
                     help="run only the M = 40 MLP-block sub-benchmark")
-    ap.add_argument("--profile-kernels", choices=["verify", "glue", "rmsnorm", "qkv64", "qkv256"],
+    ap.add_argument("--profile-kernels", choices=["verify", "glue", "rmsnorm", "qkv20", "qkv20fused", "qkv64",
+                                                  "qkv256"],
                     help="launch one kernel a few times at its workload shape (for ncu), no timing")
     args = ap.parse_args()
     if args.warmup < 3:

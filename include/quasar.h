@@ -321,10 +321,18 @@ quasar_status_t quasar_w4a8_linear(const int8_t* Xq, const float* sa,
 /* A2 + A3 + A4 in one call: smooth + quantize the BF16 activations and run
  * the W8A8 linear on the codes.
  *   Y[m][n] is bit-identical to quasar_smooth_quant_act(X, smooth) followed by
- *   quasar_w8a8_linear on its outputs (same codes, same sa, same epilogue);
- *   it is those two launches, with the codes and scales kept in the
- *   workspace instead of caller buffers (above 32 tokens the quantizer also
- *   writes the codes as fp16 there, the linear's token operand).
+ *   quasar_w8a8_linear on its outputs (same codes, same sa, same epilogue),
+ *   with the codes and scales kept in the workspace instead of caller
+ *   buffers.  Up to 24 tokens it is one launch: the linear's CTAs quantize
+ *   the token rows themselves (row r by CTA r mod grid, with the quantizer's
+ *   arithmetic) and publish them to the others through a counter in the
+ *   workspace's zeroed prefix before any CTA reads a code; this needs every
+ *   CTA of the launch resident at once, which the library's grid sizing
+ *   gives on an otherwise idle device (where it cannot, the quantizer runs
+ *   as a launch of its own first).  A wait for the rows that runs out is
+ *   reported like any other bounded wait (site 11).  Above 24 tokens it is
+ *   the two launches (and the quantizer also writes the codes as fp16 in
+ *   the workspace for tiles of >= 64 tokens: the linear's token operand).
  *   X [M][ldx] BF16 (ldx >= K, ldx % 8 == 0, 16-byte aligned), smooth [K]
  *   fp32 (16-byte aligned), Wp / sw / Y / sizes as for quasar_w8a8_linear.
  *   workspace: >= quasar_w8a8_linear_fused_workspace_size(M, N, K) bytes;

@@ -597,6 +597,13 @@ def _fused_vs_two_step(x_bits, w_bits, smooth, ldx_pad=0):
     N = sw.numel()
     lin = int(q.lib.quasar_w8a8_linear_workspace_size(M, N, K))
     assert int(ws.buf[:lin].count_nonzero()) == 0, "workspace counters / sums not left zero-filled"
+    # the codes and scales the call left in its scratch (written inside the
+    # linear's launch up to 24 tokens, by the quantizer above)
+    codes = ws.buf[lin:lin + M * K].view(torch.int8).view(M, K)
+    off = lin + (M * K + 255) // 256 * 256
+    scales = ws.buf[off:off + 4 * M].view(torch.float32)
+    assert torch.equal(codes, xq), "scratch codes != smooth_quant_act"
+    assert torch.equal(scales.view(torch.int32), sa.view(torch.int32)), "scratch scales != smooth_quant_act"
     s_np = smooth.cpu().numpy()
     xq_r, sa_r = orc.smooth_quant_act(x_bits, s_np)
     wq_r, sw_r = orc.pack_weights(w_bits, s_np)
@@ -629,13 +636,48 @@ def test_fused_qwen3_shapes(maker, M):
                                        # 64- to 128-token tiles: the quantizer's fp16 codes feed the linear
                                        (130, 1024, 1040, 8), (288, 6144, 4096, 0), (256, 4096, 12288, 16),
                                        (40, 24576, 4096, 0), (33, 136, 1040, 8), (64, 4096, 12288, 0),
-                                       (97, 136, 16, 0), (288, 1000, 16384, 0)])
+                                       (97, 136, 16, 0), (288, 1000, 16384, 0),
+                                       # fewer CTAs than token rows: CTAs quantize several rows each
+                                       (24, 8, 16, 0), (20, 64, 4096, 8), (17, 8, 2048, 0), (23, 192, 272, 0)])
 def test_fused_random_shapes(M, N, K, pad):
     rng = np.random.default_rng(M * 31 + N + K)
     x = synth.f32_to_bf16_bits(rng.standard_normal((M, K)) * (1 + 20 * (rng.random(K) < 0.01)))
     w = synth.f32_to_bf16_bits(rng.standard_normal((N, K)) * 0.02)
     smooth = dev(rng.uniform(0.25, 4.0, K).astype(np.float32))
     _fused_vs_two_step(x, w, smooth, ldx_pad=pad)
+
+
+def test_fused_back_to_back_one_workspace():
+    """Consecutive one-call linears on one workspace and one stream, with no
+    host synchronisation between them (the row counters of the in-launch
+    quantizer must be back at zero for each next call), against the
+    two-step path."""
+    rng = np.random.default_rng(5)
+    K = 4096
+    shapes = [(20, 6144), (20, 4096), (8, 6144), (24, 4096), (1, 6144), (20, 6144)]
+    packed = {}
+    for N in (6144, 4096):
+        w = synth.f32_to_bf16_bits(rng.standard_normal((N, K)) * 0.02)
+        smooth = dev(rng.uniform(0.25, 4.0, K).astype(np.float32))
+        packed[N] = (smooth,) + tuple(q.pack_weights(dev_bf16(w), smooth))
+    xs = [dev_bf16(synth.f32_to_bf16_bits(rng.standard_normal((M, K)) * (1 + 20 * (rng.random(K) < 0.01))))
+          for M, _ in shapes]
+    ws = q.Workspace()
+    ys = []
+    for _ in range(3):
+        for (M, N), x in zip(shapes, xs):
+            smooth, wq, sw = packed[N]
+            ys.append(q.w8a8_linear_fused(x, smooth, wq, sw, workspace=ws))
+    torch.cuda.synchronize()
+    want = []
+    for (M, N), x in zip(shapes, xs):
+        smooth, wq, sw = packed[N]
+        xq, sa = q.smooth_quant_act(x, smooth)
+        want.append(q.w8a8_linear(xq, sa, wq, sw))
+    torch.cuda.synchronize()
+    for i, y in enumerate(ys):
+        assert torch.equal(y.view(torch.int16), want[i % len(shapes)].view(torch.int16)), f"call {i}"
+    assert q.get_device_error()[0] == q.OK
 
 
 @pytest.mark.parametrize("M", [2, 12, 200])

@@ -54,6 +54,7 @@ enum : unsigned int {
   SITE_SKINNY_FULL = 8,
   SITE_SKINNY_EMPTY = 9,
   SITE_SKINNY_DRAIN = 10,
+  SITE_SKINNY_ROWS = 11,
   SITE_SELFTEST = 12,
   SITE_LMH_FULL = 13,
   SITE_LMH_EMPTY = 14,

@@ -58,11 +58,16 @@
 
 namespace quasar {
 namespace skinny {  // w8a8_skinny.cu: the register-path kernel, M <= 24 (skinny::handles)
+struct FusedIn {
+  const void* X;
+  int ldx;
+  const float* smooth;
+};
 bool handles(int M);
 size_t slots_bytes(int M, int N, int K);
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
                     void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream,
-                    bool w4);
+                    bool w4, const FusedIn* fin);
 }  // namespace skinny
 
 namespace quant {
@@ -1118,7 +1123,7 @@ static Split split_of(const Shape& s, bool xh, int sms) {
 // `w4`: Wp holds 4-bit packed weights (quasar_pack_weights_w4).
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
                     void* Y, int ldy, int32_t* acc_out, void* ws, size_t ws_bytes, cudaStream_t stream,
-                    const void* xh_ext = nullptr, bool w4 = false) {
+                    const void* xh_ext = nullptr, bool w4 = false, const skinny::FusedIn* fin = nullptr) {
   if (M < 0 || N <= 0 || K <= 0) return QUASAR_ERR_INVALID_ARG;
   if (K % 16 != 0 || N % 8 != 0 || K > 131072) return QUASAR_ERR_UNSUPPORTED;
   if (!acc_out && (ldy < N || ldy % 8 != 0)) return QUASAR_ERR_UNSUPPORTED;
@@ -1137,7 +1142,7 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   // A few tokens: the register-path kernel (same packed weights, same
   // workspace layout, fewer counters per tile).
   if (skinny::handles(M))
-    return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream, w4);
+    return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream, w4, fin);
   // Wide tiles whose register split the device cannot honour fall back to
   // 64-row tiles (fewer counters and no fp16 copy: the workspace suffices).
   if (s.NT >= 128 && !(w4 ? wide_usable<true>(s.NT) : wide_usable<false>(s.NT))) s = shape_with(M, N, K, 64);
@@ -1211,10 +1216,11 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
 
 // ------------------------------------------------------ fused activation path
 //
-// Smooth + quantize (A2) and the linear (A3 + A4) in one call: the quantizer
-// writes codes and scales into the workspace's scratch tail, then the linear
-// reads them (two launches, the second overlapping the first through
-// programmatic dependent launch).
+// Smooth + quantize (A2) and the linear (A3 + A4) in one call, the codes and
+// scales kept in the workspace's scratch tail.  Up to 24 tokens the
+// register-path launch quantizes the rows itself (one launch); above, the
+// quantizer writes them and the linear reads them (two launches, the second
+// overlapping the first through programmatic dependent launch).
 
 // The linear's workspace, then the quantizer's codes and scales, then (64- to
 // 128-token tiles) the codes again as fp16 for the linear's token operand.
@@ -1239,6 +1245,10 @@ quasar_status_t run_fused(const void* X, int ldx, const float* smooth, const int
   if (!ws || ws_bytes < fused_workspace_size(M, N, K) || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
   int8_t* xq = reinterpret_cast<int8_t*>(ws) + lin;
   float* sa = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + lin + align256((size_t)M * K));
+  if (skinny::handles(M)) {
+    const skinny::FusedIn fin{X, ldx, smooth};
+    return run(xq, sa, Wp, sw, M, N, K, Y, ldy, nullptr, ws, lin, stream, nullptr, false, &fin);
+  }
   if (fused_xh(M, N, K)) {
     // The quantizer also writes the codes as fp16: the linear's token
     // operand without a widening launch (rows up to the one-pass kernel's).

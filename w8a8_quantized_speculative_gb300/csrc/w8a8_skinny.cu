@@ -113,6 +113,13 @@ struct Cfg {
   static_assert(!RIR || RED <= S * STAGE, "reduction buffer fits in the ring");
 };
 
+// The one-call entry's activations: X [M][ldx] BF16 and the smoothing vector.
+struct FusedIn {
+  const void* X;
+  int ldx;
+  const float* smooth;
+};
+
 struct Params {
   const uint8_t* wp;  // packed weights, [n_tiles][KB][128 rows][128 B]
   const float* sa;
@@ -132,6 +139,16 @@ struct Params {
   uint32_t* ws_cnt;   // [units][8] K-block counters per finalizer warp, zero between calls
   unsigned int* err;
   unsigned long long limit_ns;
+  // One-call entry (X non-null): the launch smooths and quantizes the token
+  // rows itself (row r by CTA r, r + grid, ...) into xq / sa (the buffers the
+  // tensor map and `sa` point at), publishes them on a workspace counter and
+  // loads no token tile before all M rows are published.
+  const uint16_t* X;  // BF16 activations [M][ldx]
+  const float* smooth;
+  int ldx;
+  int8_t* xq;         // codes out, [M][K]
+  float* sa_out;      // scales out (== sa)
+  uint32_t* qflag;    // [0] rows published, [1] waiters past the wait; zero between calls
 };
 
 // First block of CTA c, and the CTA whose range holds block b, for the even
@@ -266,6 +283,156 @@ QUASAR_DEVICE_INLINE void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uin
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------ A2 inside the launch
+//
+// Smooth + quantize of token row r by the 128 consumer threads, with the
+// stand-alone quantizer's arithmetic step for step (so the codes and the
+// scale are bit-identical to it): xs = fp32(x) * smooth[k] rounded once,
+// amax = max |xs| over the row, inv = 127 / amax, code = clamp(rne(xs * inv),
+// -127, 127), sa = amax / 127 (codes and scale 0 for an all-zero row).
+// pt §2 step 2 (per-token symmetric INT8 of the smoothed activations).
+QUASAR_DEVICE_INLINE void bf16x8_f32(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+QUASAR_DEVICE_INLINE void quantize_row(const Params& p, int r, float* red4) {
+  constexpr int T = CWARPS * 32;
+  constexpr int U = 4;   // 8-value vectors per thread and round (a row of <= 4096 values is one round)
+  const int t = threadIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(p.X + (size_t)r * p.ldx);
+  const float4* sm = reinterpret_cast<const float4*>(p.smooth);
+  const int nvec = p.K / 8;
+  const bool one_round = nvec <= U * T;   // then the smoothed values stay in registers for the codes
+  float x[U][8];
+  float amax = 0.f;
+  auto load_round = [&](int v0) {
+    uint4 raw[U];
+    float4 s[2 * U];
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int v = v0 + i * T + t;
+      if (v < nvec) {
+        raw[i] = __ldg(src + v);
+        s[2 * i] = __ldg(sm + 2 * v);
+        s[2 * i + 1] = __ldg(sm + 2 * v + 1);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      if (v0 + i * T + t >= nvec) continue;
+      float xv[8];
+      bf16x8_f32(raw[i], xv);
+      const float sv[8] = {s[2 * i].x, s[2 * i].y, s[2 * i].z, s[2 * i].w,
+                           s[2 * i + 1].x, s[2 * i + 1].y, s[2 * i + 1].z, s[2 * i + 1].w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[i][e] = __fmul_rn(xv[e], sv[e]);
+    }
+  };
+  for (int v0 = 0; v0 < nvec; v0 += U * T) {
+    load_round(v0);
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      if (v0 + i * T + t >= nvec) continue;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[i][e]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((t & 31) == 0) red4[t >> 5] = amax;
+  named_barrier_or(RED_BAR, T, 0u);
+  amax = red4[0];
+#pragma unroll
+  for (int w = 1; w < CWARPS; ++w) amax = fmaxf(amax, red4[w]);
+  const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
+  if (t == 0) p.sa_out[r] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
+  uint2* dst = reinterpret_cast<uint2*>(p.xq + (size_t)r * p.K);
+  for (int v0 = 0; v0 < nvec; v0 += U * T) {
+    if (!one_round) load_round(v0);   // longer rows: the round again (L1 / L2)
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int v = v0 + i * T + t;
+      if (v >= nvec) continue;
+      uint32_t packed[2] = {0u, 0u};
+      if (amax > 0.f) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          int c = __float2int_rn(__fmul_rn(x[i][e], inv));
+          c = max(-127, min(127, c));
+          packed[e >> 2] |= (uint32_t)(c & 0xFF) << (8 * (e & 3));
+        }
+      }
+      dst[v] = make_uint2(packed[0], packed[1]);
+    }
+  }
+  named_barrier_or(RED_BAR, T, 0u);   // red4 is free again; every store of the row is issued
+}
+
+QUASAR_DEVICE_INLINE uint32_t ld_relaxed_u32(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+QUASAR_DEVICE_INLINE void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+
+QUASAR_DEVICE_INLINE float ld_relaxed_f32(const float* ptr) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+QUASAR_DEVICE_INLINE void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Bounded wait (one thread) until every token row is published: relaxed
+// polls of the count, then one acquire fence.  Every CTA of the launch is
+// resident at once (the host sizes the grid to one wave), so the rows'
+// writers always run.  Gives up like mbar_wait.  A thread that saw the count
+// then counts itself past the wait; the last of the 2 x grid waiters (the
+// copy thread and the first consumer thread of each CTA) zeroes both
+// counters for the next call.
+QUASAR_DEVICE_INLINE bool wait_rows(const Params& p, volatile int* abort_flag) {
+  bool ok = true;
+  if (ld_relaxed_u32(p.qflag) < (uint32_t)p.M) {
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (ld_relaxed_u32(p.qflag) >= (uint32_t)p.M) break;
+      if ((it & 15u) == 0) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        if (globaltimer_ns() - t0 > p.limit_ns) {
+          *abort_flag = 1;
+          if (p.err) atomicCAS(p.err, 0u, SITE_SKINNY_ROWS | ((blockIdx.x & 0xFFFFu) << 16));
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  fence_acq_rel_gpu();
+  if (ok && atomicAdd(p.qflag + 1, 1u) == 2u * gridDim.x - 1u) {
+    p.qflag[0] = 0u;
+    p.qflag[1] = 0u;
+  }
+  return ok;
+}
+
+// Publishes this CTA's `rows` finished token rows (one thread, after a
+// barrier with the threads that stored them): a release add, cumulative over
+// those stores.
+QUASAR_DEVICE_INLINE void publish_rows(const Params& p, uint32_t rows) {
+  fence_proxy_async_global();   // the tensor copies of other CTAs read the rows
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p.qflag), "r"(rows) : "memory");
 }
 
 // A finalizer warp's share of a unit is row tile mt and every token tile:
@@ -503,11 +670,23 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
                       pol_w);
         }
       }
-      pdl_wait();  // token codes come from the previous kernel
+      pdl_wait();  // token codes (or X) come from the previous kernel
+      bool rows_ok = true;
+      if (p.X) {
+        // This launch quantizes the tokens: no token tile before every row is
+        // published.  (Filling the rest of the weight ring here instead was
+        // slower: the weight requests delay the rows' own loads.)
+        rows_ok = wait_rows(p, abort_flag);
+        fence_proxy_async_global();   // the rows were written by generic stores; the tensor copies read them
+      }
       Walk w(sc, KB);
       Ring<C::S> rg;
       int issued = 0;
       for (; w.more(); w.next(KB), rg.next(), ++issued) {
+        // After a failed wait only the stages already in flight are
+        // completed (their token tiles read whatever is there), so that
+        // nothing is left in flight.
+        if (!rows_ok && issued >= pre) break;
         uint8_t* st = stages + rg.s * C::STAGE;
         if (issued >= pre) {
           if (!mbar_wait(&empty[rg.s], rg.ph ^ 1u, abort_flag, p.err, SITE_SKINNY_EMPTY, p.limit_ns)) break;
@@ -539,6 +718,19 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   const int mt_f = warp;            // finalizer share: row tile mt_f, every token tile
   const int nh = 0;
   pdl_wait();                       // scales and workspace belong to the previous kernel until here
+  bool bad = false;
+  if (p.X) {
+    // A2 for this CTA's token rows, published with one count per CTA; then
+    // wait for everyone's rows (the scales are read below).
+    float* red4 = reinterpret_cast<float*>(fin);
+    int rows = 0;
+    for (int r = (int)blockIdx.x; r < p.M; r += grid, ++rows) quantize_row(p, r, red4);
+    if (threadIdx.x == 0) {
+      if (rows > 0) publish_rows(p, (uint32_t)rows);
+      bad = !wait_rows(p, abort_flag);
+    }
+    bad = named_barrier_or(RED_BAR, CWARPS * 32, bad ? 1u : 0u);
+  }
   const int u_first = (sc.s1 > sc.s0) ? sc.s0 / KB : sc.w0;
   const int u_last = (sc.w1 > sc.w0) ? sc.w1 - 1 : (sc.s1 - 1) / KB;
   const int u_first1 = sc.s0 / KB;  // first unit of the split range (its slot 0)
@@ -548,7 +740,8 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   if (!p.acc_out) {
     for (int i = threadIdx.x; i < 32 + 2 * UM; i += CWARPS * 32) {
       if (i < 32) {
-        sa_s[i] = (i < p.M) ? __ldg(&p.sa[i]) : 0.f;
+        // written in this launch when p.X: a coherent load after the wait
+        sa_s[i] = (i < p.M) ? (p.X ? ld_relaxed_f32(&p.sa[i]) : __ldg(&p.sa[i])) : 0.f;
       } else {
         const int r = i - 32;
         const int n = (r < UM ? u_first : u_last) * UM + (r & (UM - 1));
@@ -584,7 +777,6 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   const uint32_t b_off = (uint32_t)(C::HB + g * BK + (((2 * kq) ^ g) << 4) + 4 * c);
   const uint32_t stages_u32 = smem_u32(stages);
 
-  bool bad = false;
   // Partial segments of the split range (at most two: its first and last)
   // are counted together when the range ends, so that one fence covers both.
   int seg_ua = -1, seg_na = 0, seg_ub = -1, seg_nb = 0;
@@ -801,6 +993,28 @@ static int resident_clusters(int dev, int csize) {
   return cache[dev][csize];
 }
 
+// CTAs of the stream-K kernel resident per SM (0 if unknown); cached per device.
+template <int NT8, bool W4>
+static int resident_per_sm(int dev) {
+  static int cache[64];
+  static bool init[64] = {};
+  if (dev < 0 || dev >= 64) return 0;
+  if (!init[dev]) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, w8a8_skinny_kernel<NT8, false, W4>, THREADS,
+                                                      Cfg<NT8, false, W4>::SMEM) != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();
+    }
+    cache[dev] = n;
+    init[dev] = true;
+  }
+  return cache[dev];
+}
+
+// Launches the kernel; with p.X set (the launch quantizes its own tokens,
+// which needs every CTA resident at once) returns cudaErrorNotSupported
+// without launching when the grid would not fit in one wave.
 template <int NT8, bool W4>
 static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t stream) {
   int dev = 0;
@@ -826,6 +1040,7 @@ static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t
   // long and its consumers are fast.
   auto pre_for = [&](int blocks_per_cta) { return (blocks_per_cta <= 16 || p.M > 8) ? 1 : 1 << 30; };
   if (csize >= 2) {
+    // (every cluster resident at once: the choice of csize above)
     p.mode = 1;
     p.csize = csize;
     p.split_units = 0;
@@ -844,6 +1059,7 @@ static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t
   if (p.whole_per == 0) grid = std::min(grid, p.total1);
   p.pre = pre_for((p.total1 + grid - 1) / std::max(grid, 1) + p.whole_per * p.KB);
   if ((unsigned long long)(p.total1 + 1) * (unsigned long long)(grid + 1) >= (1ull << 32)) return cudaErrorInvalidValue;
+  if (p.X && grid > resident_per_sm<NT8, W4>(dev) * sms) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = config_of<NT8, false, W4>(grid, 1, stream, attr);
   return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, false, W4>, tx, p);
 }
@@ -862,9 +1078,14 @@ size_t slots_bytes(int M, int N, int K) {
 
 // Arguments were validated by the caller; ws_cnt holds >= 8 zeroed counters
 // per 64-row unit, `slots` slots_bytes() bytes (no initial value needed).
+// With `fin` (the one-call entry) the launch first smooths and quantizes
+// fin->X into Xq / sa itself; its two row counters are ws_cnt[4] and
+// ws_cnt[5], which the stream-K schedule never uses (its counters are
+// [unit][finalizer warp < 4]).  If the grid cannot be resident in one wave
+// it runs the stand-alone quantizer first instead.
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
                     void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream,
-                    bool w4) {
+                    bool w4, const FusedIn* fin) {
   const int nt8 = (M + 7) / 8;
   CUtensorMap tx;
   if (!encode_2d_u8(&tx, Xq, K, M, BK, 8 * nt8)) return QUASAR_ERR_CUDA;
@@ -883,17 +1104,33 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   p.ws_cnt = ws_cnt;
   p.err = device_error_word();
   p.limit_ns = wait_limit_ns();
+  p.X = fin ? reinterpret_cast<const uint16_t*>(fin->X) : nullptr;
+  p.smooth = fin ? fin->smooth : nullptr;
+  p.ldx = fin ? fin->ldx : 0;
+  p.xq = const_cast<int8_t*>(Xq);
+  p.sa_out = const_cast<float*>(sa);
+  p.qflag = ws_cnt + 4;
   if (!p.err) return QUASAR_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return QUASAR_ERR_CUDA;
-  cudaError_t e;
-  switch (nt8 + (w4 ? 3 : 0)) {
-    case 1: e = launch<1, false>(tx, p, sms, stream); break;
-    case 2: e = launch<2, false>(tx, p, sms, stream); break;
-    case 3: e = launch<3, false>(tx, p, sms, stream); break;   // handles() keeps M <= 24
-    case 4: e = launch<1, true>(tx, p, sms, stream); break;
-    case 5: e = launch<2, true>(tx, p, sms, stream); break;
-    default: e = launch<3, true>(tx, p, sms, stream); break;
+  auto go = [&]() -> cudaError_t {
+    switch (nt8 + (w4 ? 3 : 0)) {
+      case 1: return launch<1, false>(tx, p, sms, stream);
+      case 2: return launch<2, false>(tx, p, sms, stream);
+      case 3: return launch<3, false>(tx, p, sms, stream);   // handles() keeps M <= 24
+      case 4: return launch<1, true>(tx, p, sms, stream);
+      case 5: return launch<2, true>(tx, p, sms, stream);
+      default: return launch<3, true>(tx, p, sms, stream);
+    }
+  };
+  cudaError_t e = go();
+  if (e == cudaErrorNotSupported && p.X) {
+    const quasar_status_t sq = quasar_smooth_quant_act(fin->X, fin->ldx, fin->smooth, M, K, const_cast<int8_t*>(Xq),
+                                                       const_cast<float*>(sa),
+                                                       reinterpret_cast<quasar_stream_t>(stream));
+    if (sq != QUASAR_OK) return sq;
+    p.X = nullptr;
+    e = go();
   }
   if (e == cudaErrorInvalidValue) return QUASAR_ERR_UNSUPPORTED;
   return cuda_status(e);
