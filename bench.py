@@ -48,9 +48,10 @@ from w8a8_quantized_speculative_gb300 import synth  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-# The library runs M <= 24 on the register-path kernel, whose device code and
-# launch choices (grid, clusters, schedule) come from w8a8_skinny.cu and the
-# shared device helpers; larger M runs on the tcgen05 kernel (w8a8_linear.cu).
+# The library runs a few tokens (M <= 24; M <= 32 when N <= 8192) on the
+# register-path kernel, whose device code and launch choices (grid, clusters,
+# schedule) come from w8a8_skinny.cu and the shared device helpers; larger M
+# runs on the tcgen05 kernel (w8a8_linear.cu).
 # The headline's dominant kernel is the register-path one: its DRAM traffic
 # counters are valid while these sources are unchanged.
 GEMM_SRCS = [os.path.join(ROOT, "w8a8_quantized_speculative_gb300", "csrc", f)
@@ -290,9 +291,10 @@ def main_gpu(args):
             q.w8a8_linear_fused(l["x"], l["smooth"], l["wq_copies"][i % ncopy], l["sw_copies"][i % ncopy],
                                 y=l["y"], workspace=ws)
 
-    # each fused call: one launch up to 24 tokens (the linear quantizes its own
-    # rows), else the quantizer and then the linear
-    launches_per_step = sum(1 if l["case"].M <= 24 else 2 for l in lin)
+    # each fused call: one launch on the register-path kernel (the linear
+    # quantizes its own rows), else the quantizer and then the linear
+    launches_per_step = sum(1 if (l["case"].M <= 24 or (l["case"].M <= 32 and l["case"].N <= 8192)) else 2
+                            for l in lin)
 
     # ---- warm-up (eager), then capture graphs of the step sequence
     with torch.cuda.stream(stream):
@@ -582,8 +584,8 @@ def run_sweep(q, dev, stream, ws, hbm):
 
 
 def run_sweep_w4(q, dev, stream, ws, hbm, w8_rows=()):
-    """The W4A8 variant (4-bit weight blocks: the register-path kernel up to
-    24 tokens, the tcgen05 kernel above) on the same linears, cold L2; bytes
+    """The W4A8 variant (4-bit weight blocks: the register-path kernel for a
+    few tokens, the tcgen05 kernel above) on the same linears, cold L2; bytes
     per weight halve.  `vs_w8a8`: the W8A8 sweep's time at the same shape
     over this one (> 1: the 4-bit blocks are faster)."""
     import torch

@@ -252,14 +252,16 @@ quasar_status_t quasar_silu_mul_smooth_quant(const void* GU_bf16, int ldgu, cons
  *   Sizes: M >= 0 (0 = no-op), 16 <= K <= 131072 with K % 16 == 0 (the int32
  *   accumulator cannot overflow: 127*127*131072 < 2^31), N >= 8 with
  *   N % 8 == 0.  Tuned for M <= 256 (verification passes); larger M works.
+ *   Two kernels serve it: the register-path kernel for M <= 24, and for
+ *   M <= 32 when N <= 8192; the tcgen05 kernel otherwise.
  *   The kernel is launched with programmatic dependent launch: it may start
  *   streaming Wp before the previous kernel on `stream` has finished, and it
  *   reads Xq / sa and writes Y and the workspace only after that kernel's
  *   writes are visible.
  *   workspace: >= quasar_w8a8_linear_workspace_size(M, N, K) bytes of device
  *   memory whose first quasar_w8a8_linear_workspace_zeroed_bytes(M, N, K)
- *   bytes (split-K counters and, above 24 tokens, int32 partial sums) are
- *   ZERO when the call starts; the rest may hold anything.  The call leaves
+ *   bytes (split-K counters and, on the tcgen05 kernel, int32 partial
+ *   sums) are ZERO when the call starts; the rest may hold anything.  The call leaves
  *   all quasar_w8a8_linear_workspace_size(M, N, K) bytes zero-filled again
  *   when it completes without a device error, so one zero-filled workspace
  *   can serve every linear on a stream (but see the one-call entry below,
@@ -299,7 +301,7 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa,
  *   quasar_tile_weights_w4: row-major codes [N][K] in [-8, 7] -> Wp4.
  *   quasar_w4a8_linear: as quasar_w8a8_linear with Wp4 for Wp, same
  *     argument rules, limits and error codes, any M >= 0 (the register-path
- *     kernel up to 24 tokens, the tcgen05 kernel above, both reading the
+ *     kernel for a few tokens, the tcgen05 kernel above, both reading the
  *     4-bit blocks directly); workspace: quasar_w8a8_linear_workspace_size
  *     (M, N, K) bytes under the same contract (the first
  *     quasar_w8a8_linear_workspace_zeroed_bytes(M, N, K) zero on entry and
@@ -323,16 +325,16 @@ quasar_status_t quasar_w4a8_linear(const int8_t* Xq, const float* sa,
  *   Y[m][n] is bit-identical to quasar_smooth_quant_act(X, smooth) followed by
  *   quasar_w8a8_linear on its outputs (same codes, same sa, same epilogue),
  *   with the codes and scales kept in the workspace instead of caller
- *   buffers.  Up to 24 tokens it is one launch: the linear's CTAs quantize
+ *   buffers.  On the register-path kernel it is one launch: its CTAs quantize
  *   the token rows themselves (row r by CTA r mod grid, with the quantizer's
  *   arithmetic) and publish them to the others through a counter in the
  *   workspace's zeroed prefix before any CTA reads a code; this needs every
  *   CTA of the launch resident at once, which the library's grid sizing
  *   gives on an otherwise idle device (where it cannot, the quantizer runs
  *   as a launch of its own first).  A wait for the rows that runs out is
- *   reported like any other bounded wait (site 11).  Above 24 tokens it is
- *   the two launches (and the quantizer also writes the codes as fp16 in
- *   the workspace for tiles of >= 64 tokens: the linear's token operand).
+ *   reported like any other bounded wait (site 11).  On the tcgen05 kernel
+ *   it is the two launches (and the quantizer also writes the codes as fp16
+ *   in the workspace for tiles of >= 64 tokens: the linear's token operand).
  *   X [M][ldx] BF16 (ldx >= K, ldx % 8 == 0, 16-byte aligned), smooth [K]
  *   fp32 (16-byte aligned), Wp / sw / Y / sizes as for quasar_w8a8_linear.
  *   workspace: >= quasar_w8a8_linear_fused_workspace_size(M, N, K) bytes;

@@ -341,7 +341,8 @@ def test_int8_gemm_bit_exact(M, N, K):
     check_ws_zero(ws)
 
 
-@pytest.mark.parametrize("M,K,N", [(24, 1024, 256), (24, 4096, 256), (24, 12288, 256), (64, 4096, 256),
+@pytest.mark.parametrize("M,K,N", [(24, 1024, 256), (24, 4096, 256), (24, 12288, 256), (32, 4096, 256),
+                                   (32, 12288, 256), (64, 4096, 256),
                                    (40, 12288, 256), (256, 4096, 256), (256, 12288, 256), (144, 4096, 256),
                                    (288, 12288, 256), (288, 4096, 16384)])
 def test_int8_gemm_adversarial_extremes(M, K, N):
@@ -358,12 +359,15 @@ def test_int8_gemm_adversarial_extremes(M, K, N):
     assert acc[0, 0] == 127 * 127 * K
 
 
-# M <= 24 runs on the register-path kernel (64-row units, two CTAs per SM):
+# M <= 24 (M <= 32 for N <= 8192) runs on the register-path kernel (64-row
+# units, two CTAs per SM):
 # every token-tile width, ragged M / N / K and each schedule: one cluster per
 # unit (few units, cluster sizes 2-8), split units stream-K only (<= 303
 # units), whole units only (304 units), and split-then-whole (384 units).
-# Larger M (25 .. 64 here) checks the tcgen05 kernel at the same shapes.
+# Larger M (25 .. 64 here) checks the tcgen05 kernel at the same shapes, and
+# at 25 .. 32 tokens on N <= 8192 the register path's four-token-tile form.
 SKINNY_SHAPES = [(1, 8, 16), (2, 1000, 4112), (7, 136, 1040), (9, 512, 256), (16, 4096, 4096),
+                 (29, 136, 1040), (32, 8192, 1024), (25, 4096, 4096),
                  (3, 12288, 256), (5, 19456, 512), (12, 24576, 1024), (20, 6144, 4096),
                  (23, 264, 2064), (24, 6144, 4096), (28, 6144, 4096), (32, 24576, 1024),
                  (31, 8, 12288), (32, 1152, 2048), (33, 136, 1040), (40, 6144, 4096), (48, 9728, 1024),
@@ -598,7 +602,7 @@ def _fused_vs_two_step(x_bits, w_bits, smooth, ldx_pad=0):
     lin = int(q.lib.quasar_w8a8_linear_workspace_size(M, N, K))
     assert int(ws.buf[:lin].count_nonzero()) == 0, "workspace counters / sums not left zero-filled"
     # the codes and scales the call left in its scratch (written inside the
-    # linear's launch up to 24 tokens, by the quantizer above)
+    # linear's launch on the register path, by the quantizer on the tcgen05 path)
     codes = ws.buf[lin:lin + M * K].view(torch.int8).view(M, K)
     off = lin + (M * K + 255) // 256 * 256
     scales = ws.buf[off:off + 4 * M].view(torch.float32)

@@ -57,13 +57,13 @@
 #include "quasar_common.cuh"
 
 namespace quasar {
-namespace skinny {  // w8a8_skinny.cu: the register-path kernel, M <= 24 (skinny::handles)
+namespace skinny {  // w8a8_skinny.cu: the register-path kernel, a few tokens (skinny::handles)
 struct FusedIn {
   const void* X;
   int ldx;
   const float* smooth;
 };
-bool handles(int M);
+bool handles(int M, int N);
 size_t slots_bytes(int M, int N, int K);
 quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const float* sw, int M, int N, int K,
                     void* Y, int ldy, int32_t* acc_out, uint32_t* ws_cnt, void* slots, cudaStream_t stream,
@@ -876,7 +876,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // per block.  Through quasar_w8a8_linear the copy is made by one small
 // launch into the workspace (and cleared afterwards); the one-call entry's
 // quantizer writes it directly.
-static bool use_xh(int M, const Shape& s) { return !skinny::handles(M) && s.NT >= 128; }
+static bool use_xh(int M, int N, const Shape& s) { return !skinny::handles(M, N) && s.NT >= 128; }
 
 // Counter region: one counter per (tile, converter warp), sized for the
 // 64-row fallback of wide tiles too so that both use the same layout.
@@ -891,7 +891,7 @@ static size_t cnt_bytes(int M, int N, int K) {
 // partial-sum slots and the fp16 token copy need no initial content.
 size_t zeroed_bytes(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  return cnt_bytes(M, N, K) + (skinny::handles(M) ? 0 : align256((size_t)M * N * 4));
+  return cnt_bytes(M, N, K) + (skinny::handles(M, N) ? 0 : align256((size_t)M * N * 4));
 }
 
 size_t workspace_size(int M, int N, int K) {
@@ -901,7 +901,7 @@ size_t workspace_size(int M, int N, int K) {
   // slots of the register-path kernel, then (tiles of >= 128 rows) the fp16
   // token copy
   return cnt_bytes(M, N, K) + align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K))) +
-         (use_xh(M, s) ? align256((size_t)M * K * 2) : 0);
+         (use_xh(M, N, s) ? align256((size_t)M * K * 2) : 0);
 }
 
 // INT8 token codes -> the same values in fp16 (exact), 16 codes per thread.
@@ -1141,14 +1141,14 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   const size_t xh_off = cnt_bytes(M, N, K) + align256(std::max((size_t)M * N * 4, skinny::slots_bytes(M, N, K)));
   // A few tokens: the register-path kernel (same packed weights, same
   // workspace layout, fewer counters per tile).
-  if (skinny::handles(M))
+  if (skinny::handles(M, N))
     return skinny::run(Xq, sa, Wp, sw, M, N, K, Y, ldy, acc_out, ws_cnt, ws_acc, stream, w4, fin);
   // Wide tiles whose register split the device cannot honour fall back to
   // 64-row tiles (fewer counters and no fp16 copy: the workspace suffices).
   if (s.NT >= 128 && !(w4 ? wide_usable<true>(s.NT) : wide_usable<false>(s.NT))) s = shape_with(M, N, K, 64);
 
   const bool ext = xh_ext != nullptr && s.NT >= 64;
-  const bool xh_path = ext || use_xh(M, s);
+  const bool xh_path = ext || use_xh(M, N, s);
   uint4* xh = ext ? reinterpret_cast<uint4*>(const_cast<void*>(xh_ext))
               : xh_path ? reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws) + xh_off)
                         : nullptr;
@@ -1217,14 +1217,15 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
 // ------------------------------------------------------ fused activation path
 //
 // Smooth + quantize (A2) and the linear (A3 + A4) in one call, the codes and
-// scales kept in the workspace's scratch tail.  Up to 24 tokens the
-// register-path launch quantizes the rows itself (one launch); above, the
-// quantizer writes them and the linear reads them (two launches, the second
-// overlapping the first through programmatic dependent launch).
+// scales kept in the workspace's scratch tail.  On the register path (up to
+// 24 tokens, 32 on layers of <= 8192 rows: skinny::handles) the launch
+// quantizes the rows itself (one launch); otherwise the quantizer writes them
+// and the linear reads them (two launches, the second overlapping the first
+// through programmatic dependent launch).
 
 // The linear's workspace, then the quantizer's codes and scales, then (64- to
 // 128-token tiles) the codes again as fp16 for the linear's token operand.
-static bool fused_xh(int M, int N, int K) { return !skinny::handles(M) && shape_of(M, N, K).NT >= 64; }
+static bool fused_xh(int M, int N, int K) { return !skinny::handles(M, N) && shape_of(M, N, K).NT >= 64; }
 
 size_t fused_workspace_size(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
@@ -1245,7 +1246,7 @@ quasar_status_t run_fused(const void* X, int ldx, const float* smooth, const int
   if (!ws || ws_bytes < fused_workspace_size(M, N, K) || !aligned(ws, 256)) return QUASAR_ERR_WORKSPACE;
   int8_t* xq = reinterpret_cast<int8_t*>(ws) + lin;
   float* sa = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + lin + align256((size_t)M * K));
-  if (skinny::handles(M)) {
+  if (skinny::handles(M, N)) {
     const skinny::FusedIn fin{X, ldx, smooth};
     return run(xq, sa, Wp, sw, M, N, K, Y, ldy, nullptr, ws, lin, stream, nullptr, false, &fin);
   }
@@ -1336,8 +1337,9 @@ quasar_status_t quasar_w8a8_linear(const int8_t* Xq, const float* sa, const int8
 quasar_status_t quasar_w4a8_linear(const int8_t* Xq, const float* sa, const int8_t* Wp4, const float* sw, int M,
                                    int N, int K, void* Y_bf16, int ldy, void* workspace, size_t ws_bytes,
                                    quasar_stream_t stream) {
-  // 4-bit weight blocks on both kernels: the register path up to 24 tokens,
-  // the tcgen05 kernel (nibbles widened by the converters) above.
+  // 4-bit weight blocks on both kernels: the register path for a few tokens
+  // (skinny::handles), the tcgen05 kernel (nibbles widened by the converters)
+  // above.
   return quasar::gemm::run(Xq, sa, Wp4, sw, M, N, K, Y_bf16, ldy, nullptr, workspace, ws_bytes,
                            reinterpret_cast<cudaStream_t>(stream), nullptr, true);
 }

@@ -1,5 +1,5 @@
-// A3 + A4 for a few tokens (M <= 24): the W8A8 verify linear on the
-// register tensor path.
+// A3 + A4 for a few tokens (M <= 32, see handles()): the W8A8 verify linear
+// on the register tensor path.
 //
 //   acc[m][n] = sum_k Xq[m][k] * Wq[n][k]        exact integer
 //   Y[m][n]   = bf16_rne((float(acc) * sa[m]) * sw[n])
@@ -20,9 +20,9 @@
 // So for a few tokens the weights go HBM -> shared memory (1-D bulk copies of
 // the same packed blocks the tcgen05 kernel reads) -> registers (ldmatrix) ->
 // fp16 (exact) -> mma.sync, with fp32 accumulators that stay exact integers
-// (see RUN_BLOCKS).  Measured, this path is the faster one up to 24 tokens
-// (handles() below is the one place that sets the split); the tcgen05 kernel
-// takes larger M.
+// (see RUN_BLOCKS).  Measured, this path is the faster one up to 24 tokens,
+// and up to 32 on layers of <= 8192 rows (handles() below is the one place
+// that sets the split); the tcgen05 kernel takes larger M.
 //
 // Work units.  A unit is 64 weight rows (half of a packed 128-row tile: its
 // blocks are contiguous 8 KB halves of the 16 KB packed blocks) over all of
@@ -1064,13 +1064,19 @@ static cudaError_t launch(const CUtensorMap& tx, Params p, int sms, cudaStream_t
   return cudaLaunchKernelEx(&cfg, w8a8_skinny_kernel<NT8, false, W4>, tx, p);
 }
 
-bool handles(int M) { return M >= 1 && M <= 24; }
+// Measured (graph replays, cold L2, Qwen3-8B shapes): this path is faster
+// than the tcgen05 kernel up to 24 tokens on every layer, and at 25-32
+// tokens on layers of up to 8192 rows (qkv 10.4-10.8 against 12.0-12.3 us,
+// o_proj 8.3 against 9.7, down_proj 16.8 against 18.3), where one cluster
+// per unit applies; wider layers (gate_up, 384 units) stream-K at four token
+// tiles slower (34.5 against 30.6 us).
+bool handles(int M, int N) { return M >= 1 && (M <= 24 || (M <= 32 && N <= 8192)); }
 
 // Partial-sum slots this kernel may need after the counters: two per CTA,
 // each 64 rows x NT int32.  Like the counters they are zero between calls
 // (each is zeroed by its reader).
 size_t slots_bytes(int M, int N, int K) {
-  if (!handles(M) || N <= 0 || K <= 0) return 0;
+  if (!handles(M, N) || N <= 0 || K <= 0) return 0;
   const long long items = (long long)((N + UM - 1) / UM) * ((K + BK - 1) / BK);
   const long long ctas = std::min<long long>(items, MAX_CTAS);
   return (size_t)ctas * 2 * (size_t)UM * 8 * ((M + 7) / 8) * 4;
@@ -1114,13 +1120,19 @@ quasar_status_t run(const int8_t* Xq, const float* sa, const int8_t* Wp, const f
   const int sms = sm_count();
   if (sms <= 0) return QUASAR_ERR_CUDA;
   auto go = [&]() -> cudaError_t {
-    switch (nt8 + (w4 ? 3 : 0)) {
+    if (w4) {
+      switch (nt8) {
+        case 1: return launch<1, true>(tx, p, sms, stream);
+        case 2: return launch<2, true>(tx, p, sms, stream);
+        case 3: return launch<3, true>(tx, p, sms, stream);
+        default: return launch<4, true>(tx, p, sms, stream);   // handles() keeps M <= 32
+      }
+    }
+    switch (nt8) {
       case 1: return launch<1, false>(tx, p, sms, stream);
       case 2: return launch<2, false>(tx, p, sms, stream);
-      case 3: return launch<3, false>(tx, p, sms, stream);   // handles() keeps M <= 24
-      case 4: return launch<1, true>(tx, p, sms, stream);
-      case 5: return launch<2, true>(tx, p, sms, stream);
-      default: return launch<3, true>(tx, p, sms, stream);
+      case 3: return launch<3, false>(tx, p, sms, stream);
+      default: return launch<4, false>(tx, p, sms, stream);
     }
   };
   cudaError_t e = go();
