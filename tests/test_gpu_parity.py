@@ -642,7 +642,9 @@ def test_fused_qwen3_shapes(maker, M):
                                        (40, 24576, 4096, 0), (33, 136, 1040, 8), (64, 4096, 12288, 0),
                                        (97, 136, 16, 0), (288, 1000, 16384, 0),
                                        # fewer CTAs than token rows: CTAs quantize several rows each
-                                       (24, 8, 16, 0), (20, 64, 4096, 8), (17, 8, 2048, 0), (23, 192, 272, 0)])
+                                       (24, 8, 16, 0), (20, 64, 4096, 8), (17, 8, 2048, 0), (23, 192, 272, 0),
+                                       # 25-32 tokens on N <= 8192: the register path's four token tiles, one launch
+                                       (28, 4096, 4096, 8), (32, 1024, 1040, 0), (25, 8, 48, 0)])
 def test_fused_random_shapes(M, N, K, pad):
     rng = np.random.default_rng(M * 31 + N + K)
     x = synth.f32_to_bf16_bits(rng.standard_normal((M, K)) * (1 + 20 * (rng.random(K) < 0.01)))
