@@ -70,8 +70,8 @@ def test_workspace_sizes(lib):
     assert ws(256, 24576, 4096) == 4 * 192 * 16 * 4 + 256 * 24576 * 4 + 256 * 4096 * 2
     assert ws(128, 6144, 4096) == 2 * 48 * 16 * 4 + 128 * 6144 * 4 + 128 * 4096 * 2
     # the prefix that must be zero on entry: counters, plus the int32 sums
-    # above 24 tokens (the register path's slots and the fp16 token copy
-    # need no initial content)
+    # of the tcgen05 kernel (the register path's slots and the fp16 token
+    # copy need no initial content)
     zb = lib.quasar_w8a8_linear_workspace_zeroed_bytes
     zb.restype = ctypes.c_size_t
     assert zb(20, 6144, 4096) == 3072
