@@ -9,12 +9,13 @@ Metric: TB/s of INT8 weight bytes streamed per second (weights + per-channel
 scales), whole job.  Weights rotate through enough packed copies that the
 working set is several times the 129 MB L2 (cold L2 every step).
 
-Also reported: the roofline object for the dominant kernel (the qkv linear),
-an end-to-end number through the public API with host buffers, SM clocks
+Also reported: the roofline object for the dominant kernel (the qkv linear on
+ready codes, and as the step runs it: one launch that also quantizes the
+rows), an end-to-end number through the public API with host buffers, SM clocks
 sampled during the timed region, the CPU oracle as a baseline, an M sweep
 over the four decoder-layer linears with a BF16 cuBLAS GEMM of the same shape
 as a bandwidth reference, the same linears with 4-bit weights (W4A8) at
-M = 1, 8, 20, the verification kernel at B=32, D=8,
+the same M, the verification kernel at B=32, D=8,
 V=151936, the fused BF16 lm_head + verification at the same B, D, V, and the
 whole verification step of four decoder layers' W8A8 linears plus the lm_head
 at 288 token rows against the same chain on BF16 cuBLAS, and the MLP block at
@@ -56,7 +57,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # counters are valid while these sources are unchanged.
 GEMM_SRCS = [os.path.join(ROOT, "w8a8_quantized_speculative_gb300", "csrc", f)
              for f in ("w8a8_skinny.cu", "quasar_common.cuh")]
-SKINNY_MAX_M = 24
+def on_register_path(M, N):
+    """The library's split between its two linear kernels (skinny::handles)."""
+    return 1 <= M <= 24 or (M <= 32 and N <= 8192)
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "w8a8_skinny_qkv_m20.json")
 WORKLOAD = ("Qwen3-8B attention projections, W8A8: fused qkv 4096->6144 and o_proj 4096->4096, "
             "M=20 tokens (4 sequences x (4 drafts + 1)), each linear preceded by smooth+quantize")
@@ -293,8 +296,7 @@ def main_gpu(args):
 
     # each fused call: one launch on the register-path kernel (the linear
     # quantizes its own rows), else the quantizer and then the linear
-    launches_per_step = sum(1 if (l["case"].M <= 24 or (l["case"].M <= 32 and l["case"].N <= 8192)) else 2
-                            for l in lin)
+    launches_per_step = sum(1 if on_register_path(l["case"].M, l["case"].N) else 2 for l in lin)
 
     # ---- warm-up (eager), then capture graphs of the step sequence
     with torch.cuda.stream(stream):
@@ -371,10 +373,30 @@ def main_gpu(args):
     traffic = profiled_traffic()
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic,
-                "kernel": (f"{'w8a8_skinny_kernel' if c.M <= SKINNY_MAX_M else 'w8a8_linear_kernel'} "
+                "kernel": (f"{'w8a8_skinny_kernel' if on_register_path(c.M, c.N) else 'w8a8_linear_kernel'} "
                            f"qkv M={c.M} N={c.N} K={c.K}"),
                 "launch_us": gemm_us, "algorithmic_bytes_per_launch": alg,
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s"}
+    # The same kernel as the step runs it: the one-call launch on the BF16
+    # activations (it also smooths and quantizes the token rows), back to
+    # back; its bytes add the activations and the smoothing vector.
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=stream):
+        for i in range(nk):
+            q.w8a8_linear_fused(qkv["x"], qkv["smooth"], qkv["wq_copies"][i % ncopy], qkv["sw_copies"][i % ncopy],
+                                y=qkv["y"], workspace=ws)
+    with torch.cuda.stream(stream):
+        g1.replay()
+        k0.record(stream)
+        g1.replay()
+        k1.record(stream)
+    stream.synchronize()
+    fused_us = k0.elapsed_time(k1) * 1e3 / nk
+    alg1 = c.N * c.K + 4 * c.N + 2 * c.M * c.K + 4 * c.K + 2 * c.M * c.N
+    roofline["one_call_launch"] = {"launch_us": fused_us, "algorithmic_bytes_per_launch": alg1,
+                                   "achieved": alg1 / (fused_us * 1e-6) / 1e9,
+                                   "frac": alg1 / (fused_us * 1e-6) / 1e9 / hbm,
+                                   "note": "the qkv launch as the step runs it (A2 inside the launch)"}
 
     # ---- end to end through the public API with host buffers.  Double
     # buffered, as a serving loop runs it: a copy stream brings step i+1's

@@ -25,8 +25,9 @@ constexpr int THREADS = 256;
 constexpr int LOADS = 4;          // 16-byte loads per thread in flight
 constexpr int TARGET_CTAS = 8 * 152;
 constexpr int MIN_CHUNK = 4096;
+constexpr int MERGE_BATCH = 4;    // chunk records of a row loaded at once by the merging lane
 
-struct Partial {
+struct __align__(16) Partial {   // read back as one float4
   float best;  // max logit in the chunk
   int idx;     // lowest index holding it
   float m;     // running max of logit / T (T > 0)
@@ -272,24 +273,33 @@ verify_kernel(const uint16_t* __restrict__ logits, int ldl, const int32_t* __res
   if (!is_last) return;
 
   // Last CTA of sequence b: merge each row's chunk records in chunk order.
-  __threadfence();
+  // Thread 0's acquire-release count made every record of the sequence
+  // visible to it, and the barrier above orders the loads below after it.
+  // Each lane loads its row's draft token and every record of the row
+  // before using any (one round trip, not one per record).
   __shared__ int s_fail;
   if (warp == 0) {
     int first_fail = D;
     int ri_row = INT_MAX;   // argmax of row `lane` (D < 32: one row per lane)
     for (int j = lane; j <= D; j += 32) {
       const Partial* pr = part + ((size_t)b * (D + 1) + j) * S;
+      const int d = j < D ? draft[(size_t)b * D + j] : -1;
       float rb = -INFINITY, rm = -INFINITY, rs = 0.f;
       int ri = INT_MAX;
-      for (int cc = 0; cc < S; ++cc) {
-        const float pb = __ldcg(&pr[cc].best);
-        const int pi = __ldcg(&pr[cc].idx);
-        arg_merge(rb, ri, pb, pi);
-        if (SAMPLED) lse_merge(rm, rs, __ldcg(&pr[cc].m), __ldcg(&pr[cc].s));
+      for (int c0 = 0; c0 < S; c0 += MERGE_BATCH) {
+        float4 rec[MERGE_BATCH];
+#pragma unroll
+        for (int k = 0; k < MERGE_BATCH; ++k)
+          if (c0 + k < S) rec[k] = __ldcg(reinterpret_cast<const float4*>(pr + c0 + k));
+#pragma unroll
+        for (int k = 0; k < MERGE_BATCH; ++k) {
+          if (c0 + k >= S) break;
+          arg_merge(rb, ri, rec[k].x, __float_as_int(rec[k].y));
+          if (SAMPLED) lse_merge(rm, rs, rec[k].z, rec[k].w);
+        }
       }
       ri_row = ri;
       if (j < D) {
-        const int d = draft[(size_t)b * D + j];
         bool ok;
         if (d < 0 || d >= V) {
           ok = false;  // out-of-vocabulary draft: rejected, never dereferenced
