@@ -339,6 +339,9 @@ QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4
   const int m0 = (t % m_tiles) * NT + h * TOK;
   const bool whole = (pr.kb_first == 0) && (pr.kb_last == KB - 1);
   bool emit = whole;
+  // The row's channel scale, loaded now so that its latency overlaps the
+  // publication below instead of following it.
+  const float swn = (!p.acc_out && n < p.N) ? __ldg(p.sw + n) : 0.f;
   if (!whole) {
     // Split tile: publish this warp's 32 x NT/4 sub-tile with integer
     // atomics, then count the K blocks it covered.  The warp that brings the
@@ -352,16 +355,23 @@ QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4
     __syncwarp();
     uint32_t last = 0;
     if (lane == 0) {
+      // acquire-release: the warp that completes the count sees every other
+      // contributor's sums (each fenced before its count)
       const uint32_t nb = (uint32_t)(pr.kb_last - pr.kb_first + 1);
-      const uint32_t old = atomicAdd(&p.ws_cnt[(size_t)t * CONV_WARPS + warp], nb);
+      uint32_t old;
+      asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;"
+                   : "=r"(old)
+                   : "l"(&p.ws_cnt[(size_t)t * CONV_WARPS + warp]), "r"(nb)
+                   : "memory");
       last = (old + nb == (uint32_t)KB) ? 1u : 0u;
     }
     emit = __shfl_sync(0xffffffffu, last, 0) != 0;
     if (emit) {
-      // Every contribution is in L2 now: take the sums and leave zeros for
-      // the next call in one atomic exchange each (measured faster than plain
-      // loads followed by plain stores).
-      __threadfence();
+      // Every contribution is in L2 now (lane 0's acquire, shared with the
+      // warp by the barrier): take the sums and leave zeros for the next
+      // call in one atomic exchange each (measured faster than plain loads
+      // followed by plain stores).
+      __syncwarp();
       if (n < p.N) {
 #pragma unroll
         for (int jj = 0; jj < TOK; ++jj)
@@ -376,11 +386,10 @@ QUASAR_DEVICE_INLINE bool finish_run(const PendingRun& pr, int32_t (&acc)[NT / 4
       for (int jj = 0; jj < TOK; ++jj)
         if (m0 + jj < p.M) p.acc_out[(size_t)(m0 + jj) * p.N + n] = acc[jj];
     } else {
-      const float swn = p.sw[n];
 #pragma unroll
       for (int jj = 0; jj < TOK; ++jj) {
         if (m0 + jj < p.M) {
-          const float y = __fmul_rn(__fmul_rn(__int2float_rn(acc[jj]), p.sa[m0 + jj]), swn);
+          const float y = __fmul_rn(__fmul_rn(__int2float_rn(acc[jj]), __ldg(p.sa + m0 + jj)), swn);
           p.Y[(size_t)(m0 + jj) * p.ldy + n] = __float2bfloat16_rn(y);
         }
       }
