@@ -287,12 +287,7 @@ QUASAR_DEVICE_INLINE void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uin
 
 // ------------------------------------------------ A2 inside the launch
 //
-// Smooth + quantize of token row r by the 128 consumer threads, with the
-// stand-alone quantizer's arithmetic step for step (so the codes and the
-// scale are bit-identical to it): xs = fp32(x) * smooth[k] rounded once,
-// amax = max |xs| over the row, inv = 127 / amax, code = clamp(rne(xs * inv),
-// -127, 127), sa = amax / 127 (codes and scale 0 for an all-zero row).
-// pt §2 step 2 (per-token symmetric INT8 of the smoothed activations).
+// Eight BF16 values (one 16-byte load) -> fp32, exactly.
 QUASAR_DEVICE_INLINE void bf16x8_f32(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -302,6 +297,12 @@ QUASAR_DEVICE_INLINE void bf16x8_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
+// Smooth + quantize of token row r by the 128 consumer threads, with the
+// stand-alone quantizer's arithmetic step for step (so the codes and the
+// scale are bit-identical to it): xs = fp32(x) * smooth[k] rounded once,
+// amax = max |xs| over the row, inv = 127 / amax, code = clamp(rne(xs * inv),
+// -127, 127), sa = amax / 127 (codes and scale 0 for an all-zero row).
+// pt §2 step 2 (per-token symmetric INT8 of the smoothed activations).
 QUASAR_DEVICE_INLINE void quantize_row(const Params& p, int r, float* red4) {
   constexpr int T = CWARPS * 32;
   constexpr int U = 4;   // 8-value vectors per thread and round (a row of <= 4096 values is one round)
@@ -382,7 +383,6 @@ QUASAR_DEVICE_INLINE uint32_t ld_relaxed_u32(const uint32_t* ptr) {
 }
 
 QUASAR_DEVICE_INLINE void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-
 
 QUASAR_DEVICE_INLINE float ld_relaxed_f32(const float* ptr) {
   float v;
