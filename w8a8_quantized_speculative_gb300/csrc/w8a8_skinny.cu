@@ -392,13 +392,15 @@ QUASAR_DEVICE_INLINE float ld_relaxed_f32(const float* ptr) {
 
 QUASAR_DEVICE_INLINE void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
-// Bounded wait (one thread) until every token row is published: relaxed
-// polls of the count, then one acquire fence.  Every CTA of the launch is
-// resident at once (the host sizes the grid to one wave), so the rows'
-// writers always run.  Gives up like mbar_wait.  A thread that saw the count
-// then counts itself past the wait; the last of the 2 x grid waiters (the
-// copy thread and the first consumer thread of each CTA) zeroes both
-// counters for the next call.
+// Bounded wait (the copy thread of each CTA) until every token row is
+// published: relaxed polls of the count, then one acquire fence.  Every CTA
+// of the launch is resident at once (the host sizes the grid to one wave),
+// so the rows' writers always run.  Gives up like mbar_wait.  A thread that
+// saw the count then counts itself past the wait; the last of the grid's
+// waiters zeroes both counters for the next call.  (One waiter per CTA: the
+// consumers learn of the rows through the first stage's barrier, which the
+// copy thread fills only after its wait; with a second poller per CTA the
+// attention step ran 0.9 us slower.)
 QUASAR_DEVICE_INLINE bool wait_rows(const Params& p, volatile int* abort_flag) {
   bool ok = true;
   if (ld_relaxed_u32(p.qflag) < (uint32_t)p.M) {
@@ -420,7 +422,7 @@ QUASAR_DEVICE_INLINE bool wait_rows(const Params& p, volatile int* abort_flag) {
     }
   }
   fence_acq_rel_gpu();
-  if (ok && atomicAdd(p.qflag + 1, 1u) == 2u * gridDim.x - 1u) {
+  if (ok && atomicAdd(p.qflag + 1, 1u) == gridDim.x - 1u) {
     p.qflag[0] = 0u;
     p.qflag[1] = 0u;
   }
@@ -720,28 +722,28 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   pdl_wait();                       // scales and workspace belong to the previous kernel until here
   bool bad = false;
   if (p.X) {
-    // A2 for this CTA's token rows, published with one count per CTA; then
-    // wait for everyone's rows (the scales are read below).
+    // A2 for this CTA's token rows, published with one count per CTA.  The
+    // consumers then need nothing until their first full stage, which the
+    // copy thread fills only after every row is published.
     float* red4 = reinterpret_cast<float*>(fin);
     int rows = 0;
     for (int r = (int)blockIdx.x; r < p.M; r += grid, ++rows) quantize_row(p, r, red4);
     if (threadIdx.x == 0) {
       if (rows > 0) publish_rows(p, (uint32_t)rows);
-      bad = !wait_rows(p, abort_flag);
     }
-    bad = named_barrier_or(RED_BAR, CWARPS * 32, bad ? 1u : 0u);
+    named_barrier_or(RED_BAR, CWARPS * 32, 0u);
   }
   const int u_first = (sc.s1 > sc.s0) ? sc.s0 / KB : sc.w0;
   const int u_last = (sc.w1 > sc.w0) ? sc.w1 - 1 : (sc.s1 - 1) / KB;
   const int u_first1 = sc.s0 / KB;  // first unit of the split range (its slot 0)
   // Stage the dequantization scales the epilogues will need: every token's
-  // sa, and sw of the first and last unit of this CTA (read after the first
-  // run-end barrier, which orders these stores).
+  // sa (in the one-call launch after the first full stage, below), and sw of
+  // the first and last unit of this CTA (read after the first run-end
+  // barrier, which orders these stores).
   if (!p.acc_out) {
     for (int i = threadIdx.x; i < 32 + 2 * UM; i += CWARPS * 32) {
       if (i < 32) {
-        // written in this launch when p.X: a coherent load after the wait
-        sa_s[i] = (i < p.M) ? (p.X ? ld_relaxed_f32(&p.sa[i]) : __ldg(&p.sa[i])) : 0.f;
+        if (!p.X) sa_s[i] = (i < p.M) ? __ldg(&p.sa[i]) : 0.f;
       } else {
         const int r = i - 32;
         const int n = (r < UM ? u_first : u_last) * UM + (r & (UM - 1));
@@ -786,10 +788,17 @@ w8a8_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const Params p) {
   };
   Walk w(sc, KB);
   Ring<C::S> r;
+  bool sa_late = p.X != nullptr && !p.acc_out;
   for (; w.more(); w.next(KB), r.next()) {
     if (!bad) {
       const bool ok = mbar_wait(&full[r.s], r.ph, abort_flag, p.err, SITE_SKINNY_FULL, p.limit_ns);
       bad = !__all_sync(0xffffffffu, ok);
+      if (sa_late && !bad) {
+        // The copy thread saw every row published (acquire) before it armed
+        // this stage: the token scales written in this launch are visible.
+        for (int i = threadIdx.x; i < 32; i += CWARPS * 32) sa_s[i] = (i < p.M) ? ld_relaxed_f32(&p.sa[i]) : 0.f;
+      }
+      sa_late = false;
     }
     if (!bad) {
       const uint32_t st0 = stages_u32 + (uint32_t)(r.s * C::STAGE);
