@@ -371,8 +371,9 @@ quasar_status_t quasar_int8_gemm_s32(const int8_t* Xq, const int8_t* Wp,
  * until the process exits.
  *   - Arguments, outputs and results are those of quasar_w8a8_linear.
  *   - Returns QUASAR_ERR_WORKSPACE when quasar_w8a8_linear_workspace_size(M,
- *     N, K) exceeds QUASAR_NOALLOC_SCRATCH_BYTES (4 MiB: e.g. M x N up to
- *     about one million output elements).
+ *     N, K) exceeds QUASAR_NOALLOC_SCRATCH_BYTES (8 MiB: e.g. M x N up to
+ *     about two million output elements on the tcgen05 kernel, and every
+ *     register-path shape, whose partial sums need at most 5.3 MB).
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
  *   - Each call clears the part of the array it uses on `stream` before the
@@ -380,7 +381,7 @@ quasar_status_t quasar_int8_gemm_s32(const int8_t* Xq, const int8_t* Wp,
  *   - All calls in the process share the one array: calls that may overlap
  *     on the GPU (different streams, or different host threads) race and
  *     must be serialized by the caller. */
-#define QUASAR_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define QUASAR_NOALLOC_SCRATCH_BYTES (8u << 20)
 quasar_status_t quasar_w8a8_linear_noalloc(const int8_t* Xq, const float* sa,
                                            const int8_t* Wp, const float* sw,
                                            int M, int N, int K,

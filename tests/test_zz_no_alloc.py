@@ -27,6 +27,7 @@ from w8a8_quantized_speculative_gb300 import synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 QUASAR_ERR_WORKSPACE = 3
+SCRATCH = 8 << 20   # QUASAR_NOALLOC_SCRATCH_BYTES
 
 
 def _p(t):
@@ -73,7 +74,16 @@ def test_noalloc_tcgen05_branch(M):
     # qkv (N = 6144, K = 4096) above 32 tokens: the tcgen05 kernel's split-K
     # counters and int32 sums live in the fixed array (about 1.6 MB at M = 64)
     case = synth.sweep_case("qkv", M)
-    assert q.lib.quasar_w8a8_linear_workspace_size(M, case.N, case.K) <= (4 << 20)
+    assert q.lib.quasar_w8a8_linear_workspace_size(M, case.N, case.K) <= SCRATCH
+    _check_twice(case)
+
+
+@pytest.mark.parametrize("name", ["qkv", "o"])
+def test_noalloc_register_path_four_token_tiles(name):
+    # M = 32 on a layer of <= 8192 rows: the register-path kernel with four
+    # token tiles, whose partial-sum slots (5.2 MB) need the larger array
+    case = synth.sweep_case(name, 32)
+    assert q.lib.quasar_w8a8_linear_workspace_size(32, case.N, case.K) <= SCRATCH
     _check_twice(case)
 
 
@@ -83,7 +93,7 @@ def test_noalloc_repeated_call_same_layer():
 
 def test_noalloc_rejects_sizes_beyond_the_fixed_scratch():
     M, N, K = 256, 24576, 4096          # needs ~25 MB of split-K scratch
-    assert q.lib.quasar_w8a8_linear_workspace_size(M, N, K) > (4 << 20)
+    assert q.lib.quasar_w8a8_linear_workspace_size(M, N, K) > SCRATCH
     xq = torch.zeros((M, K), dtype=torch.int8, device="cuda")
     sa = torch.zeros(M, device="cuda")
     wp = torch.zeros(16, dtype=torch.int8, device="cuda")   # never read: the call is refused first
