@@ -78,6 +78,15 @@ def test_workspace_sizes(lib):
     assert zb(64, 4096, 4096) == 2048 + 64 * 4096 * 4
     assert zb(256, 24576, 4096) == 4 * 192 * 16 * 4 + 256 * 24576 * 4
     assert zb(0, 6144, 4096) == 0
+    # 25-32 tokens: the register path (counters only) on layers of <= 8192
+    # rows, the tcgen05 kernel (plus its int32 sums) on wider ones
+    assert zb(32, 4096, 4096) == 32 * 16 * 4
+    assert zb(25, 8192, 4096) == 64 * 16 * 4
+    assert zb(32, 8200, 4096) == 4352 + 32 * 8200 * 4          # 65 tiles x 16 counters, 256-byte aligned
+    assert zb(32, 24576, 4096) == 192 * 16 * 4 + 32 * 24576 * 4
+    assert zb(33, 6144, 4096) == 48 * 16 * 4 + 33 * 6144 * 4
+    # the register path's partial-sum slots at four token tiles: 2 per CTA, 64 rows x 32 int32, 320 CTAs
+    assert ws(32, 4096, 4096) == 32 * 16 * 4 + 2 * 320 * 64 * 32 * 4
     for M, N, K in [(1, 8, 16), (24, 24576, 12288), (40, 4096, 12288), (288, 6144, 4096)]:
         assert zb(M, N, K) <= ws(M, N, K)
     assert lib.quasar_calibrate_workspace_size(4096) == 8 * 4096
